@@ -1,0 +1,217 @@
+/*
+ * libssd — layer-skipping self-speculative decoding on one GB300 (sm_103a).
+ *
+ * The calls follow the problem statement of the pages this library is
+ * built from:
+ *   - LayerSkip blog (marsggbo.github.io, "ACL'24 | LayerSkip ..."),
+ *     §3.1 draft_phase, §3.2 verify_phase, §3.3 layerskip_ssd;
+ *   - SWIFT: On-the-Fly Self-Speculative Decoding (paperlayer.ai digest),
+ *     §4.1/§4.1.2 matchness scoring of candidate layer sets, §4.2
+ *     confidence-aware drafting.
+ *
+ * Model: a Llama-style decoder (RMSNorm, rotate-half RoPE, MHA/GQA
+ * attention, SwiGLU MLP, untied LM head).  Weights are bf16, the residual
+ * stream fp32; every GEMM input (normed hidden state, attention output,
+ * SwiGLU product) and every stored K/V value is rounded to bf16; logits are
+ * fp32.
+ *
+ * Decoding state.  t[0..n-1] are the committed tokens.  The last one,
+ * x = t[n-1], is "pending": it has not yet been run through the full model,
+ * and K/V at positions < n-1 hold full-model values in every layer.
+ *
+ * Threading and streams.  A context is used from one host thread at a time.
+ * Every call enqueues its work on the context's stream; a call that returns
+ * host data (any *_out pointer documented as "host") waits for its stream
+ * with a bounded wait (SSD_ERR_TIMEOUT after the context's timeout).
+ *
+ * Ownership.  The caller owns the weights (device memory) and must keep
+ * them alive and unchanged for the context's lifetime.  The context owns its
+ * KV cache, workspaces and CUDA graphs.  Host buffers are caller-owned and
+ * sized by the documented maxima.
+ *
+ * Errors.  Every call returns an ssd_status; none aborts the process.
+ * ssd_last_error() describes the most recent failure of a context.
+ */
+#ifndef SSD_H_
+#define SSD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SSD_OK = 0,
+  SSD_ERR_INVALID_ARG = 1, /* bad pointer, size, shape or policy            */
+  SSD_ERR_STATE = 2,       /* call made in the wrong order (verify w/o draft)*/
+  SSD_ERR_CAPACITY = 3,    /* max_seq, max_draft or scoring capacity exceeded */
+  SSD_ERR_OOM = 4,         /* device allocation failed                       */
+  SSD_ERR_CUDA = 5,        /* a CUDA runtime call failed                     */
+  SSD_ERR_TIMEOUT = 6      /* a bounded host wait on the stream ran out      */
+} ssd_status;
+
+typedef struct ssd_ctx ssd_ctx;
+
+/* Model shape and context capacities. */
+typedef struct {
+  int32_t n_layers;    /* L                                              */
+  int32_t d_model;     /* D, multiple of 64                              */
+  int32_t n_heads;     /* H                                              */
+  int32_t n_kv_heads;  /* Hkv, divides H                                 */
+  int32_t head_dim;    /* dh: 64 or 128                                  */
+  int32_t ffn_dim;     /* F, multiple of 32                              */
+  int32_t vocab;       /* V, multiple of 16                              */
+  float rope_theta;    /* RoPE base, e.g. 1e4                            */
+  float norm_eps;      /* RMSNorm epsilon, e.g. 1e-5                     */
+  int32_t max_seq;     /* KV capacity in positions (multiple of 64)      */
+  int32_t max_draft;   /* largest d_max any policy may use, 1..15        */
+  int32_t max_score_rows; /* K*N capacity of ssd_score_masks (0: none)   */
+} ssd_config;
+
+/* Device pointers of one decoder layer (borrowed, row-major). */
+typedef struct {
+  const void* attn_norm; /* [D] fp32 RMSNorm gain                          */
+  const void* wqkv;      /* [(H + 2 Hkv) dh, D] bf16: q rows, k rows, v rows */
+  const void* wo;        /* [D, H dh] bf16                                 */
+  const void* mlp_norm;  /* [D] fp32                                       */
+  const void* w_gate;    /* [F, D] bf16                                    */
+  const void* w_up;      /* [F, D] bf16                                    */
+  const void* w_down;    /* [D, F] bf16                                    */
+} ssd_layer_weights;
+
+typedef struct {
+  const void* tok_embed;  /* [V, D] bf16                                    */
+  const void* final_norm; /* [D] fp32                                       */
+  const void* lm_head;    /* [V, D] bf16 (shared by draft and verify)       */
+  const ssd_layer_weights* layers; /* host array of n_layers entries; the
+                                      table is copied by ssd_create       */
+} ssd_weights;
+
+enum { SSD_MODE_SKIP = 0, SSD_MODE_EXIT = 1 };
+
+/* Draft policy (SWIFT §4.2 / LayerSkip §3.1). */
+typedef struct {
+  int32_t mode;          /* SSD_MODE_SKIP: draft runs every layer whose bit
+                            in skip_mask is clear.  SSD_MODE_EXIT: draft runs
+                            layers 0..exit_layer, then the shared final norm
+                            and LM head                                      */
+  uint64_t skip_mask[4]; /* bit l (word l/64) set: layer l skipped (L<=256) */
+  int32_t exit_layer;    /* exit mode: E, 0 <= E < L                         */
+  int32_t d_max;         /* draft at most d_max tokens per round (<= max_draft)*/
+  float tau;             /* stop drafting when top-1 probability < tau;
+                            tau <= 0 never stops                            */
+  float temperature;     /* 0: greedy draft and acceptance; > 0: sampled
+                            draft from softmax(z/T), min(1,p/q) acceptance  */
+  uint64_t seed;         /* Philox4x32-10 key                                */
+} ssd_policy;
+
+typedef struct {
+  int64_t rounds;          /* verify passes                                 */
+  int64_t drafted;         /* draft tokens proposed (sum of d)              */
+  int64_t accepted;        /* draft tokens accepted                         */
+  int64_t emitted;         /* tokens emitted (before truncation to n_tokens)*/
+  int64_t draft_steps;     /* draft forward passes run                      */
+  int64_t kernel_launches; /* library kernels launched (graph nodes counted) */
+  double bytes_streamed;   /* algorithmic HBM bytes: weights + KV read/written */
+} ssd_stats;
+
+/* Creates a context for one model on one device (the current device).
+ * stream: a cudaStream_t (NULL: the legacy default stream).  Validates the
+ * shape (see ssd_config), allocates the KV cache [L][Hkv][max_seq][dh] bf16
+ * (K and V) and the workspaces.  Errors: INVALID_ARG, OOM, CUDA. */
+ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* weights, void* stream,
+                      ssd_ctx** out);
+
+/* Frees everything the context owns.  Waits for its stream.  NULL is OK. */
+ssd_status ssd_destroy(ssd_ctx* ctx);
+
+/* Sets the draft policy; (re)builds the CUDA graphs of the draft step, the
+ * verify pass and the autoregressive step.  Errors: INVALID_ARG, CAPACITY
+ * (d_max > max_draft), CUDA. */
+ssd_status ssd_set_policy(ssd_ctx* ctx, const ssd_policy* policy);
+
+/* Runs tokens[0..n-1] (host) through the full model at positions 0..n-1,
+ * replacing any previous state, and commits the first new token (argmax, or
+ * a sample at T > 0), which it also returns in *first_token_out (host).
+ * After the call n_committed = n + 1.  Errors: INVALID_ARG, CAPACITY
+ * (n + 1 > max_seq), CUDA, TIMEOUT. */
+ssd_status ssd_prefill(ssd_ctx* ctx, const int32_t* tokens, int32_t n, int32_t* first_token_out);
+
+/* LayerSkip §3.1 draft_phase / SWIFT §4.2: drafts up to d_max tokens with
+ * the policy's layer subset, feeding x and then each draft token, stopping
+ * when top-1 confidence < tau.  draft_out (host, >= d_max) receives
+ * y_0..y_{d-1}; conf_out (host, >= d_max + 1, nullable) the confidence of
+ * every draft step run (the stopping step included); *d_out = d.
+ * Errors: STATE (a draft already pending), CAPACITY (positions would pass
+ * max_seq), CUDA, TIMEOUT. */
+ssd_status ssd_draft(ssd_ctx* ctx, int32_t* draft_out, float* conf_out, int32_t* d_out);
+
+/* LayerSkip §3.2 verify_phase: the full model over positions n-1..n-1+d,
+ * reusing the draft's K/V of layers below s0 (s0 = first skipped layer, or
+ * E + 1).  logits_out (host, nullable, [d+1][V] fp32) receives the verify
+ * logits.  Errors: STATE (no draft pending), CUDA, TIMEOUT. */
+ssd_status ssd_verify(ssd_ctx* ctx, float* logits_out);
+
+/* LayerSkip §3.3: greedy prefix acceptance (T = 0) or min(1, p/q)
+ * acceptance with residual / bonus sampling (T > 0); commits the emitted
+ * tokens and rolls the KV length back to the accepted prefix.
+ * emitted_out (host, >= d_max + 1) and *n_emitted_out (1..d+1).
+ * Errors: STATE (no verify pending), CUDA, TIMEOUT. */
+ssd_status ssd_accept(ssd_ctx* ctx, int32_t* emitted_out, int32_t* n_emitted_out);
+
+/* One full round (draft, verify, accept) per iteration until n_tokens tokens
+ * are emitted; extra tokens of the last round are dropped (the committed
+ * length ends exactly n_tokens further).  out (host, nullable, >= n_tokens)
+ * receives the tokens; stats (host, nullable) is filled.
+ * Errors: CAPACITY, STATE (no prefill), CUDA, TIMEOUT. */
+ssd_status ssd_generate(ssd_ctx* ctx, int32_t n_tokens, int32_t* out, ssd_stats* stats);
+
+/* Plain autoregressive decoding with the full model (the baseline the
+ * speedup is measured against), same kernels.  out (host, nullable). */
+ssd_status ssd_decode_ar(ssd_ctx* ctx, int32_t n_tokens, int32_t* out, ssd_stats* stats);
+
+/* SWIFT §4.1.2: scores K candidate skip sets by matchness.  Candidate k
+ * (masks[4k..4k+3], host, bit l = layer l skipped) runs the window inputs
+ * t[n-N-1..n-2] causally through its kept layers, attending to the
+ * full-model K/V of positions < n-N-1 and to its own K/V for the window,
+ * and predicts t[n-N..n-1] by top-1; matchness_out[k] (host) = matches / N,
+ * *best_out = argmax (lowest k on ties).  The shared cache is not modified.
+ * Errors: INVALID_ARG, CAPACITY (K*N > max_score_rows, or N + 1 > n - 1),
+ * CUDA, TIMEOUT. */
+ssd_status ssd_score_masks(ssd_ctx* ctx, const uint64_t* masks, int32_t K, int32_t N,
+                           float* matchness_out, int32_t* best_out);
+
+/* Rolls the committed length back to n (2 <= n <= current n).  The token
+ * t[n-1] becomes pending again. */
+ssd_status ssd_rewind(ssd_ctx* ctx, int32_t n);
+
+/* Copies the committed tokens to out (host, cap entries); *n_out = n. */
+ssd_status ssd_get_tokens(ssd_ctx* ctx, int32_t* out, int32_t cap, int32_t* n_out);
+
+/* Per-kernel-class timing of the decode path, measured with CUDA events on
+ * the context's stream around every launch of n_steps eager autoregressive
+ * steps (the same kernels and launch shapes the captured graphs replay).
+ * Class order: 0 qkv, 1 attention, 2 o_proj, 3 gate_up, 4 down, 5 lm_head,
+ * 6 control (embedding, acceptance and bookkeeping kernels).  The committed
+ * state is restored afterwards.  Errors: STATE (no prefill), CAPACITY, CUDA. */
+typedef struct {
+  double ms[8];       /* average device time per launch                    */
+  double bytes[8];    /* algorithmic HBM bytes per launch (weights + KV)    */
+  int64_t launches[8];
+} ssd_kernel_times;
+ssd_status ssd_profile_decode(ssd_ctx* ctx, int32_t n_steps, ssd_kernel_times* out);
+
+/* Host wait limit in milliseconds for calls that return host data
+ * (default 120000). */
+ssd_status ssd_set_timeout_ms(ssd_ctx* ctx, int32_t ms);
+
+/* Human-readable description of the context's most recent error ("" if
+ * none; a static string for a NULL context). */
+const char* ssd_last_error(const ssd_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SSD_H_ */

@@ -1,0 +1,276 @@
+"""Layer-skipping self-speculative decoding on one GB300 (sm_103a).
+
+Python binding of the libssd C-ABI.  PyTorch only provides device memory and
+streams; every step of the path (embedding, the fused RMSNorm + projections,
+attention with KV append, the LM head with its row summary, drafting,
+verification, acceptance and rollback) runs in the library's CUDA kernels.
+The functions here marshal arguments and raise on error; there is no CPU or
+PyTorch fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+from typing import Dict, List, Optional, Sequence, Tuple
+
+import numpy as np
+import torch
+
+from . import _abi
+from ._abi import (SSDError, SsdConfig, SsdLayerWeights, SsdPolicy, SsdRowStats, SsdStats,
+                   SsdWeights, SSD_MODE_EXIT, SSD_MODE_SKIP)
+
+__all__ = ["SSDContext", "SSDError", "ops", "policy_struct", "stream_handle"]
+
+
+def _lib():
+    return _abi.lib()
+
+
+def stream_handle(stream: Optional[torch.cuda.Stream] = None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def policy_struct(policy) -> SsdPolicy:
+    """Marshals a policy (attributes mode, skip, exit_layer, d_max, tau,
+    temperature, seed — e.g. ``synthetic.Policy``) into ``ssd_policy``."""
+    p = SsdPolicy()
+    p.mode = SSD_MODE_SKIP if policy.mode == "skip" else SSD_MODE_EXIT
+    for l in getattr(policy, "skip", ()):
+        p.skip_mask[l // 64] |= 1 << (l % 64)
+    p.exit_layer = int(getattr(policy, "exit_layer", -1))
+    p.d_max = int(policy.d_max)
+    tau = getattr(policy, "tau", None)
+    p.tau = -1.0 if tau is None else float(tau)
+    p.temperature = float(getattr(policy, "temperature", 0.0))
+    p.seed = int(getattr(policy, "seed", 0)) & ((1 << 64) - 1)
+    return p
+
+
+class SSDContext:
+    """One model on one GPU: owns the library context (KV cache, workspaces,
+    graphs); borrows the weight tensors, which must outlive it."""
+
+    def __init__(self, shape, weights: Dict, max_seq: int, max_draft: int = 15,
+                 max_score_rows: int = 0, stream: Optional[torch.cuda.Stream] = None):
+        self.shape = shape
+        self._weights = weights  # keep the tensors alive
+        cfg = SsdConfig(shape.n_layers, shape.d_model, shape.n_heads, shape.n_kv_heads,
+                        shape.head_dim, shape.ffn_dim, shape.vocab, shape.rope_theta,
+                        shape.norm_eps, max_seq, max_draft, max_score_rows)
+        self._layers = (SsdLayerWeights * shape.n_layers)()
+        for i, lw in enumerate(weights["layers"]):
+            for k in ("wqkv", "wo", "w_gate", "w_up", "w_down"):
+                if lw[k].dtype != torch.bfloat16:
+                    raise ValueError(f"layer {i} {k}: the library computes with bf16 weights")
+            self._layers[i] = SsdLayerWeights(_ptr(lw["attn_norm"]), _ptr(lw["wqkv"]),
+                                              _ptr(lw["wo"]), _ptr(lw["mlp_norm"]),
+                                              _ptr(lw["w_gate"]), _ptr(lw["w_up"]),
+                                              _ptr(lw["w_down"]))
+        w = SsdWeights(_ptr(weights["tok_embed"]), _ptr(weights["final_norm"]),
+                       _ptr(weights["lm_head"]), self._layers)
+        self.stream = stream if stream is not None else torch.cuda.current_stream()
+        h = C.c_void_p()
+        st = _lib().ssd_create(C.byref(cfg), C.byref(w), stream_handle(self.stream), C.byref(h))
+        if st != _abi.SSD_OK:
+            raise SSDError(st, "ssd_create failed")
+        self._h = h
+        self.max_seq = max_seq
+        self.d_max = 0
+        self.vocab = shape.vocab
+
+    # ------------------------------------------------------------------
+    def _check(self, st: int):
+        if st != _abi.SSD_OK:
+            raise SSDError(st, _lib().ssd_last_error(self._h).decode())
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            _lib().ssd_destroy(self._h)
+            self._h = C.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ------------------------------------------------------------------
+    def set_policy(self, policy):
+        self._check(_lib().ssd_set_policy(self._h, C.byref(policy_struct(policy))))
+        self.d_max = int(policy.d_max)
+
+    def prefill(self, tokens: Sequence[int]) -> int:
+        arr = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        first = C.c_int32()
+        self._check(_lib().ssd_prefill(self._h, arr.ctypes.data_as(C.POINTER(C.c_int32)),
+                                       len(arr), C.byref(first)))
+        return int(first.value)
+
+    def draft(self) -> Tuple[List[int], List[float]]:
+        out = (C.c_int32 * max(self.d_max, 1))()
+        conf = (C.c_float * (self.d_max + 1))()
+        d = C.c_int32()
+        self._check(_lib().ssd_draft(self._h, out, conf, C.byref(d)))
+        n_steps = min(d.value + 1, self.d_max) if self.d_max else 0
+        return [out[i] for i in range(d.value)], [conf[i] for i in range(n_steps)]
+
+    def verify(self, want_logits: bool = True, d: Optional[int] = None) -> Optional[np.ndarray]:
+        if not want_logits:
+            self._check(_lib().ssd_verify(self._h, None))
+            return None
+        buf = np.zeros(((self.d_max + 1), self.vocab), dtype=np.float32)
+        self._check(_lib().ssd_verify(self._h, buf.ctypes.data_as(C.POINTER(C.c_float))))
+        return buf if d is None else buf[: d + 1]
+
+    def accept(self) -> List[int]:
+        out = (C.c_int32 * (self.d_max + 1))()
+        n = C.c_int32()
+        self._check(_lib().ssd_accept(self._h, out, C.byref(n)))
+        return [out[i] for i in range(n.value)]
+
+    def generate(self, n_tokens: int, want_tokens: bool = True):
+        out = np.zeros(max(n_tokens, 1), dtype=np.int32)
+        stats = SsdStats()
+        ptr = out.ctypes.data_as(C.POINTER(C.c_int32)) if want_tokens else None
+        self._check(_lib().ssd_generate(self._h, n_tokens, ptr, C.byref(stats)))
+        return (out[:n_tokens].tolist() if want_tokens else None), stats.as_dict()
+
+    def decode_ar(self, n_tokens: int, want_tokens: bool = True):
+        out = np.zeros(max(n_tokens, 1), dtype=np.int32)
+        stats = SsdStats()
+        ptr = out.ctypes.data_as(C.POINTER(C.c_int32)) if want_tokens else None
+        self._check(_lib().ssd_decode_ar(self._h, n_tokens, ptr, C.byref(stats)))
+        return (out[:n_tokens].tolist() if want_tokens else None), stats.as_dict()
+
+    def score_masks(self, masks: Sequence[Sequence[int]], N: int):
+        K = len(masks)
+        words = np.zeros((K, 4), dtype=np.uint64)
+        for k, m in enumerate(masks):
+            for l in m:
+                words[k, l // 64] |= np.uint64(1 << (l % 64))
+        scores = np.zeros(K, dtype=np.float32)
+        best = C.c_int32()
+        self._check(_lib().ssd_score_masks(self._h, words.ctypes.data_as(C.POINTER(C.c_uint64)),
+                                           K, N, scores.ctypes.data_as(C.POINTER(C.c_float)),
+                                           C.byref(best)))
+        return scores, int(best.value)
+
+    def rewind(self, n: int):
+        self._check(_lib().ssd_rewind(self._h, n))
+
+    def tokens(self) -> List[int]:
+        n = C.c_int32()
+        self._check(_lib().ssd_get_tokens(self._h, None, 0, C.byref(n)))
+        buf = (C.c_int32 * max(n.value, 1))()
+        self._check(_lib().ssd_get_tokens(self._h, buf, n.value, C.byref(n)))
+        return [buf[i] for i in range(n.value)]
+
+    def profile_decode(self, n_steps: int) -> dict:
+        """Per-kernel-class device time (CUDA events on the context stream)."""
+        out = _abi.SsdKernelTimes()
+        self._check(_lib().ssd_profile_decode(self._h, n_steps, C.byref(out)))
+        return out.as_dict()
+
+    def set_timeout_ms(self, ms: int):
+        self._check(_lib().ssd_set_timeout_ms(self._h, ms))
+
+
+class _Ops:
+    """Kernel-level entry points on torch CUDA tensors (ssd_ops.h)."""
+
+    @staticmethod
+    def _check(st: int):
+        if st != _abi.SSD_OK:
+            raise SSDError(st, _lib().ssd_ops_last_error().decode())
+
+    def linear(self, W: torch.Tensor, act: torch.Tensor) -> torch.Tensor:
+        R, K = W.shape
+        M = act.shape[0]
+        y = torch.empty(M, R, dtype=torch.float32, device=W.device)
+        self._check(_lib().ssd_op_linear(_ptr(W), R, K, _ptr(act), M, _ptr(y), stream_handle()))
+        return y
+
+    def rmsnorm_linear(self, W, x, gain, eps) -> torch.Tensor:
+        R, K = W.shape
+        M = x.shape[0]
+        y = torch.empty(M, R, dtype=torch.float32, device=W.device)
+        self._check(_lib().ssd_op_rmsnorm_linear(_ptr(W), R, K, _ptr(x), _ptr(gain), eps, M,
+                                                 _ptr(y), stream_handle()))
+        return y
+
+    def residual_linear(self, W, act, x) -> torch.Tensor:
+        R, K = W.shape
+        M = act.shape[0]
+        self._check(_lib().ssd_op_residual_linear(_ptr(W), R, K, _ptr(act), M, _ptr(x),
+                                                  stream_handle()))
+        return x
+
+    def swiglu(self, Wg, Wu, x, gain, eps) -> torch.Tensor:
+        F, K = Wg.shape
+        M = x.shape[0]
+        u = torch.empty(M, F, dtype=torch.bfloat16, device=Wg.device)
+        self._check(_lib().ssd_op_swiglu(_ptr(Wg), _ptr(Wu), F, K, _ptr(x), _ptr(gain), eps, M,
+                                         _ptr(u), stream_handle()))
+        return u
+
+    def attention(self, qkv, pos0, k_cache, v_cache, H, Hkv, dh, theta) -> torch.Tensor:
+        M = qkv.shape[0]
+        max_seq = k_cache.shape[1]
+        out = torch.empty(M, H * dh, dtype=torch.bfloat16, device=qkv.device)
+        self._check(_lib().ssd_op_attention(_ptr(qkv), M, pos0, _ptr(k_cache), _ptr(v_cache),
+                                            max_seq, H, Hkv, dh, theta, _ptr(out),
+                                            stream_handle()))
+        return out
+
+    def lm_head(self, W, x, gain, eps, temperature=0.0, seed=0, round=0, stream_id=0, pos0=0,
+                want_logits=True):
+        V, D = W.shape
+        M = x.shape[0]
+        logits = torch.empty(M, V, dtype=torch.float32, device=W.device) if want_logits else None
+        stats = torch.zeros(M, 12, dtype=torch.int32, device=W.device)
+        self._check(_lib().ssd_op_lm_head(_ptr(W), V, D, _ptr(x), _ptr(gain), eps, M,
+                                          temperature, seed, round, stream_id, pos0,
+                                          _ptr(logits), _ptr(stats), stream_handle()))
+        return logits, stats
+
+    def accept_stochastic(self, P, Q, drafts, T, seed, round, n):
+        d = drafts.shape[0]
+        V = P.shape[1]
+        emitted = torch.zeros(d + 1, dtype=torch.int32, device=P.device)
+        n_em = torch.zeros(1, dtype=torch.int32, device=P.device)
+        self._check(_lib().ssd_op_accept_stochastic(_ptr(P), _ptr(Q) if d else None,
+                                                    _ptr(drafts) if d else None, d, V, T, seed,
+                                                    round, n, _ptr(emitted), _ptr(n_em),
+                                                    stream_handle()))
+        return emitted, n_em
+
+    def philox(self, ctr: torch.Tensor, key: int) -> torch.Tensor:
+        out = torch.empty_like(ctr)
+        self._check(_lib().ssd_op_philox(_ptr(ctr), ctr.shape[0], key, _ptr(out),
+                                         stream_handle()))
+        return out
+
+
+ops = _Ops()
+
+
+def row_stats(stats: torch.Tensor) -> List[dict]:
+    """Decodes an [M, 12] int32 tensor of ssd_row_stats records."""
+    s = stats.cpu()
+    ints = s[:, :4].numpy()
+    flts = s.view(torch.float32)[:, 4:9].numpy()
+    return [{"top1": int(i[0]), "top2": int(i[1]), "sample": int(i[2]), "z1": float(f[0]),
+             "z2": float(f[1]), "lse": float(f[2]), "conf": float(f[3]), "lse_t": float(f[4])}
+            for i, f in zip(ints, flts)]

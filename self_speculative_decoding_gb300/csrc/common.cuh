@@ -1,0 +1,127 @@
+// Device helpers shared by the libssd kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define SSD_DI __device__ __forceinline__
+
+namespace ssd {
+
+typedef __nv_bfloat16 bf16;
+
+// Largest number of rows (token positions) one pass processes together.
+constexpr int kMaxRows = 16;
+// Attention key chunk: keys are split into fixed absolute chunks of this many
+// positions; partial softmax statistics are combined in chunk order.  The
+// chunking depends only on absolute positions, never on how many query rows
+// a pass carries.
+constexpr int kAttnChunk = 64;
+// Columns of the residual stream covered by one sum-of-squares partial (one
+// 16-row group of the producing projection).
+constexpr int kSsGroup = 16;
+
+// Per-row logits summary (same layout as ssd_row_stats in ssd_ops.h).
+struct RowStats {
+  int32_t top1, top2, sample, pad;
+  float z1, z2, lse, conf, lse_t, pad2[3];
+};
+static_assert(sizeof(RowStats) == 48, "RowStats layout");
+
+// Decoding state kept in device memory so that captured CUDA graphs can be
+// replayed for every step: kernels read the pass shape (rows, first
+// position, input tokens) from here instead of from launch arguments.
+struct DevState {
+  int32_t n;        // committed length; tokens[n-1] is pending
+  int32_t round;    // decoding round counter (Philox counter word 2)
+  int32_t j;        // draft steps run in the current round
+  int32_t d;        // draft tokens kept in the current round
+  int32_t stop;     // the confidence stop fired in the current round
+  int32_t M;        // rows of the current pass
+  int32_t pos0;     // position of row 0 of the current pass
+  int32_t slot;     // output slot of the current pass (draft step index)
+  int32_t n_emitted;
+  int32_t accepted;
+  int32_t pad[6];
+  int32_t in_tok[kMaxRows];
+  int32_t draft_tok[kMaxRows];
+  float draft_conf[kMaxRows];
+  int32_t emitted[kMaxRows + 1];
+  int32_t pad2[15];
+};
+
+// ---------------------------------------------------------------------------
+// loads / stores
+
+// Weights are read exactly once per pass: keep them out of L1.
+SSD_DI uint4 ld_stream_u4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+SSD_DI uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+SSD_DI float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+SSD_DI float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// D += A * B on the tensor cores, m16n8k16, bf16 inputs, fp32 accumulate.
+SSD_DI void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                     uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Programmatic dependent launch: wait for the preceding kernel's memory, and
+// let the following kernel start its launch.
+SSD_DI void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+SSD_DI void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+SSD_DI int rows_of(int M_static, const int32_t* M_dev) { return M_dev ? *M_dev : M_static; }
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two
+// 32x32->64 multiplies on a 128-bit counter with a Weyl-bumped 64-bit key.
+
+SSD_DI uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// Uniform in (0, 1), exact in fp32: ((r >> 9) + 0.5) * 2^-23.
+SSD_DI float u01(uint32_t r) { return (float(r >> 9) + 0.5f) * (1.0f / 8388608.0f); }
+
+SSD_DI uint32_t word_of(uint4 v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// Gumbel noise -log(-log u) for vocabulary entry v at (pos, round, stream).
+SSD_DI float gumbel_at(uint64_t seed, int v, int pos, int round, int stream) {
+  const uint4 r = philox4x32_10(make_uint4((uint32_t)(v >> 2), (uint32_t)pos, (uint32_t)round,
+                                           (uint32_t)stream),
+                                (uint32_t)seed, (uint32_t)(seed >> 32));
+  return -logf(-logf(u01(word_of(r, v & 3))));
+}
+
+// Total order used by every argmax: larger value first, then lower index.
+SSD_DI bool better(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+}  // namespace ssd

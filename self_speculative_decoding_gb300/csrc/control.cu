@@ -1,0 +1,382 @@
+// Pass set-up, draft control and acceptance kernels (sm_103a).
+//
+// These kernels keep the decoding state in device memory (DevState) so
+// that a captured CUDA graph of a draft step, a verify pass or an
+// autoregressive step can be replayed for every step without host-side
+// argument changes.
+#include "kernels.cuh"
+
+namespace ssd {
+
+namespace {
+
+constexpr int kBeginThreads = 512;
+constexpr int kAcceptThreads = 1024;
+
+// Embedding (or boundary copy) of the pass's rows, with the sum-of-squares
+// partials of every 16-column group (the same order the projection
+// epilogues use: ascending columns from zero).
+__global__ void __launch_bounds__(kBeginThreads) begin_kernel(BeginArgs a) {
+  __shared__ int s_M, s_tok[kMaxRows];
+  pdl_wait();
+  pdl_trigger();
+  DevState* st = a.st;
+  if (threadIdx.x == 0) {
+    int M = 1, pos0 = 0, slot = 0;
+    switch (a.mode) {
+      case BEGIN_TOKENS:
+        M = a.M;
+        pos0 = a.pos0;
+        for (int m = 0; m < M; ++m) s_tok[m] = a.toks_in[m];
+        if (a.reset_round) {
+          st->round = 0;
+          st->j = st->d = st->stop = 0;
+        }
+        break;
+      case BEGIN_AR:
+        st->round += 1;
+        pos0 = st->n - 1;
+        s_tok[0] = a.tokens[st->n - 1];
+        break;
+      case BEGIN_DRAFT:
+        if (st->j == 0) st->round += 1;
+        pos0 = st->n - 1 + st->j;
+        s_tok[0] = st->j == 0 ? a.tokens[st->n - 1] : st->draft_tok[st->j - 1];
+        slot = st->j;
+        break;
+      case BEGIN_EXTRA:
+        pos0 = st->n - 1 + st->d;
+        s_tok[0] = st->d > 0 ? st->draft_tok[st->d - 1] : a.tokens[st->n - 1];
+        break;
+      case BEGIN_VERIFY:
+        M = st->d + 1;
+        pos0 = st->n - 1;
+        break;
+    }
+    st->M = M;
+    st->pos0 = pos0;
+    st->slot = slot;
+    if (a.mode != BEGIN_VERIFY)
+      for (int m = 0; m < M; ++m) st->in_tok[m] = s_tok[m];
+    s_M = M;
+  }
+  __syncthreads();
+  const int M = s_M, D = a.D, NP = D / kSsGroup;
+  if (a.mode == BEGIN_VERIFY) {
+    for (int e = threadIdx.x; e < M * D; e += kBeginThreads) a.x[e] = a.bx[e];
+    for (int e = threadIdx.x; e < M * NP; e += kBeginThreads) a.ss[e] = a.bss[e];
+    return;
+  }
+  for (int e = threadIdx.x; e < M * NP; e += kBeginThreads) {
+    const int m = e / NP, grp = e % NP;
+    const bf16* src = a.embed + (size_t)s_tok[m] * D + grp * kSsGroup;
+    float* dst = a.x + (size_t)m * D + grp * kSsGroup;
+    float s = 0.f;
+    for (int i = 0; i < kSsGroup; ++i) {
+      const float v = __bfloat162float(src[i]);
+      dst[i] = v;
+      s += v * v;
+    }
+    a.ss[(size_t)m * NP + grp] = s;
+  }
+}
+
+__global__ void save_boundary_kernel(DevState* st, int use_d, const float* x, const float* ss,
+                                     float* bx, float* bss, int D) {
+  pdl_wait();
+  pdl_trigger();
+  const int slot = use_d ? st->d : st->j;
+  const int NP = D / kSsGroup;
+  for (int e = threadIdx.x; e < D; e += blockDim.x) bx[(size_t)slot * D + e] = x[e];
+  for (int e = threadIdx.x; e < NP; e += blockDim.x) bss[(size_t)slot * NP + e] = ss[e];
+}
+
+// SWIFT §4.2 confidence-aware stop: the draft token of step j is kept only
+// if its top-1 probability reaches tau.
+__global__ void draft_end_kernel(DevState* st, const RowStats* dstats, float tau, float T) {
+  pdl_wait();
+  pdl_trigger();
+  const int j = st->j;
+  const RowStats rs = dstats[j];
+  st->draft_conf[j] = rs.conf;
+  if (rs.conf < tau) {
+    st->stop = 1;
+  } else {
+    st->draft_tok[j] = T > 0.f ? rs.sample : rs.top1;
+    st->d = j + 1;
+  }
+  st->j = j + 1;
+}
+
+// Commit the token the full model produced for the last row of the pass.
+__global__ void ar_end_kernel(DevState* st, int32_t* tokens, const RowStats* vstats,
+                              int row_from_M, float T, int reset) {
+  pdl_wait();
+  pdl_trigger();
+  const int row = row_from_M ? st->M - 1 : 0;
+  const RowStats rs = vstats[row];
+  const int tok = T > 0.f ? rs.sample : rs.top1;
+  const int n = reset ? st->pos0 + st->M : st->n;
+  tokens[n] = tok;
+  st->n = n + 1;
+  st->emitted[0] = tok;
+  st->n_emitted = 1;
+  if (reset) st->j = st->d = st->stop = 0;
+}
+
+// Greedy acceptance: the longest prefix of drafts matching the full
+// model's argmax, then the full model's token after it.
+__global__ void accept_greedy_kernel(DevState* st, int32_t* tokens, const RowStats* vstats) {
+  pdl_wait();
+  pdl_trigger();
+  const int d = st->d, n = st->n;
+  int a = 0;
+  while (a < d && st->draft_tok[a] == vstats[a].top1) ++a;
+  for (int i = 0; i < a; ++i) st->emitted[i] = st->draft_tok[i];
+  st->emitted[a] = vstats[a].top1;
+  for (int i = 0; i <= a; ++i) tokens[n + i] = st->emitted[i];
+  st->n = n + a + 1;
+  st->n_emitted = a + 1;
+  st->accepted = a;
+  st->j = st->d = st->stop = 0;
+}
+
+// ---- stochastic acceptance (LayerSkip blog §3.3) ---------------------------
+
+SSD_DI float block_max(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float r = red[0];
+  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) r = fmaxf(r, red[w]);
+  return r;
+}
+
+SSD_DI float block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float r = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) r += red[w];
+  return r;
+}
+
+SSD_DI void block_argmax(float& v, int& i, float* redv, int* redi) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    if (better(ov, oi, v, i)) { v = ov; i = oi; }
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) { redv[warp] = v; redi[warp] = i; }
+  __syncthreads();
+  v = redv[0];
+  i = redi[0];
+  for (int w = 1; w < (int)(blockDim.x >> 5); ++w)
+    if (better(redv[w], redi[w], v, i)) { v = redv[w]; i = redi[w]; }
+}
+
+// log sum exp (z / T) over one row, fixed order.
+SSD_DI float row_lse_t(const float* z, int V, float T, float* red) {
+  float mx = -INFINITY;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) mx = fmaxf(mx, z[v] / T);
+  mx = block_max(mx, red);
+  float s = 0.f;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) s += expf(z[v] / T - mx);
+  s = block_sum(s, red);
+  return mx + logf(s);
+}
+
+__global__ void __launch_bounds__(kAcceptThreads) accept_stoch_kernel(AcceptArgs a) {
+  __shared__ float red[32];
+  __shared__ float redv[32];
+  __shared__ int redi[32];
+  __shared__ int s_dec;
+  pdl_wait();
+  pdl_trigger();
+  DevState* st = a.st;
+  const int d = st ? st->d : a.d_static;
+  const int n = st ? st->n : a.n_static;
+  const int round = st ? st->round : a.round_static;
+  const int32_t* drafts = st ? st->draft_tok : a.drafts;
+  const int V = a.V;
+  const float T = a.temperature;
+
+  int acc = 0;
+  float lseP = 0.f, lseQ = 0.f;
+  for (; acc < d; ++acc) {
+    const float* P = a.P + (size_t)acc * V;
+    const float* Q = a.Q + (size_t)acc * V;
+    lseP = a.pstats ? a.pstats[acc].lse_t : row_lse_t(P, V, T, red);
+    lseQ = a.qstats ? a.qstats[acc].lse_t : row_lse_t(Q, V, T, red);
+    if (threadIdx.x == 0) {
+      const int y = drafts[acc];
+      const float p = expf(P[y] / T - lseP);
+      const float q = expf(Q[y] / T - lseQ);
+      const uint4 r = philox4x32_10(make_uint4(0u, (uint32_t)(n + acc), (uint32_t)round, 1u),
+                                    (uint32_t)a.seed, (uint32_t)(a.seed >> 32));
+      s_dec = u01(r.x) < p / q;
+    }
+    __syncthreads();
+    const int ok = s_dec;
+    __syncthreads();
+    if (!ok) break;
+  }
+  // sample the token after the accepted prefix
+  float bv = -INFINITY, pv = -INFINITY;
+  int bi = 0x7fffffff, pi = 0x7fffffff;
+  const int row = acc;
+  const int pos = n + row;
+  const float* P = a.P + (size_t)row * V;
+  if (row < d) {
+    // residual norm(max(0, p - q)); p itself if the residual is empty
+    const float* Q = a.Q + (size_t)row * V;
+    for (int v = threadIdx.x; v < V; v += blockDim.x) {
+      const float lp = P[v] / T - lseP;
+      const float w = expf(lp) - expf(Q[v] / T - lseQ);
+      const float g = gumbel_at(a.seed, v, pos, round, 2);
+      if (w > 0.f) {
+        const float sc = logf(w) + g;
+        if (better(sc, v, bv, bi)) { bv = sc; bi = v; }
+      }
+      const float sp = lp + g;
+      if (better(sp, v, pv, pi)) { pv = sp; pi = v; }
+    }
+    block_argmax(bv, bi, redv, redi);
+    block_argmax(pv, pi, redv, redi);
+    if (bv == -INFINITY) bi = pi;
+  } else {
+    for (int v = threadIdx.x; v < V; v += blockDim.x) {
+      const float sc = P[v] / T + gumbel_at(a.seed, v, pos, round, 2);
+      if (better(sc, v, bv, bi)) { bv = sc; bi = v; }
+    }
+    block_argmax(bv, bi, redv, redi);
+  }
+  if (threadIdx.x == 0) {
+    if (st) {
+      for (int i = 0; i < acc; ++i) st->emitted[i] = drafts[i];
+      st->emitted[acc] = bi;
+      for (int i = 0; i <= acc; ++i) a.tokens[n + i] = st->emitted[i];
+      st->n = n + acc + 1;
+      st->n_emitted = acc + 1;
+      st->accepted = acc;
+      st->j = st->d = st->stop = 0;
+    } else {
+      for (int i = 0; i < acc; ++i) a.emitted[i] = drafts[i];
+      a.emitted[acc] = bi;
+      *a.n_emitted = acc + 1;
+    }
+  }
+}
+
+__global__ void philox_kernel(const uint32_t* ctr, int count, uint64_t key, uint32_t* out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= count) return;
+  const uint4 c = reinterpret_cast<const uint4*>(ctr)[i];
+  reinterpret_cast<uint4*>(out)[i] = philox4x32_10(c, (uint32_t)key, (uint32_t)(key >> 32));
+}
+
+__global__ void ss_partials_kernel(const float* x, int M, int D, float* ss) {
+  const int NP = D / kSsGroup;
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= M * NP) return;
+  const int m = e / NP, grp = e % NP;
+  const float* src = x + (size_t)m * D + grp * kSsGroup;
+  float s = 0.f;
+  for (int i = 0; i < kSsGroup; ++i) s += src[i] * src[i];
+  ss[e] = s;
+}
+
+__global__ void rope_table_kernel(float2* tab, int n_pos, int half, double theta) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= n_pos * half) return;
+  const int pos = e / half, i = e % half;
+  const double inv = pow(theta, -2.0 * (double)i / (double)(2 * half));
+  const double ang = (double)pos * inv;
+  tab[e] = make_float2((float)cos(ang), (float)sin(ang));
+}
+
+cudaLaunchConfig_t make_cfg(int grid, int block, cudaStream_t s, bool pdl,
+                            cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(grid);
+  lc.blockDim = dim3(block);
+  lc.stream = s;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = pdl ? 1 : 0;
+  return lc;
+}
+
+}  // namespace
+
+cudaError_t launch_begin(const BeginArgs& a, cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t lc = make_cfg(1, kBeginThreads, s, pdl, attr);
+  return cudaLaunchKernelEx(&lc, begin_kernel, a);
+}
+
+cudaError_t launch_save_boundary(DevState* st, int use_d, const float* x, const float* ss,
+                                 float* bx, float* bss, int D, cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t lc = make_cfg(1, 512, s, pdl, attr);
+  return cudaLaunchKernelEx(&lc, save_boundary_kernel, st, use_d, x, ss, bx, bss, D);
+}
+
+cudaError_t launch_draft_end(DevState* st, const RowStats* dstats, float tau, float temperature,
+                             cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t lc = make_cfg(1, 32, s, pdl, attr);
+  return cudaLaunchKernelEx(&lc, draft_end_kernel, st, dstats, tau, temperature);
+}
+
+cudaError_t launch_ar_end(DevState* st, int32_t* tokens, const RowStats* vstats, int row_from_M,
+                          float temperature, int reset, cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t lc = make_cfg(1, 32, s, pdl, attr);
+  return cudaLaunchKernelEx(&lc, ar_end_kernel, st, tokens, vstats, row_from_M, temperature,
+                            reset);
+}
+
+cudaError_t launch_accept_greedy(DevState* st, int32_t* tokens, const RowStats* vstats,
+                                 cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t lc = make_cfg(1, 32, s, pdl, attr);
+  return cudaLaunchKernelEx(&lc, accept_greedy_kernel, st, tokens, vstats);
+}
+
+cudaError_t launch_accept_stochastic(const AcceptArgs& a, cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t lc = make_cfg(1, kAcceptThreads, s, pdl, attr);
+  return cudaLaunchKernelEx(&lc, accept_stoch_kernel, a);
+}
+
+cudaError_t launch_philox(const uint32_t* ctr, int count, uint64_t key, uint32_t* out,
+                          cudaStream_t s) {
+  if (count <= 0) return cudaSuccess;
+  philox_kernel<<<(count + 255) / 256, 256, 0, s>>>(ctr, count, key, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_table(float2* tab, int n_pos, int half, double theta, cudaStream_t s) {
+  const int n = n_pos * half;
+  rope_table_kernel<<<(n + 255) / 256, 256, 0, s>>>(tab, n_pos, half, theta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ss_partials(const float* x, int M, int D, float* ss, cudaStream_t s) {
+  const int n = M * (D / kSsGroup);
+  ss_partials_kernel<<<(n + 255) / 256, 256, 0, s>>>(x, M, D, ss);
+  return cudaGetLastError();
+}
+
+}  // namespace ssd

@@ -1,0 +1,145 @@
+// Kernel launch interfaces shared by the context runtime and the op entry points.
+#pragma once
+
+#include "common.cuh"
+
+namespace ssd {
+
+enum InMode { IN_BF16 = 0, IN_NORM = 1 };
+enum EpiMode { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LMHEAD = 3 };
+
+// Arguments of the small-M GEMV family: y = W act over M <= 16 rows.
+struct LinearArgs {
+  const bf16* W0 = nullptr;   // [R][K] row-major
+  const bf16* W1 = nullptr;   // second matrix of the SwiGLU pair (up), [R][K]
+  int R = 0, K = 0;
+  // input
+  const bf16* act = nullptr;  // IN_BF16: [M][K]
+  const float* x = nullptr;   // IN_NORM: fp32 residual [M][K]
+  const float* ss = nullptr;  // IN_NORM: sum-of-squares partials [M][K/16]
+  const float* gain = nullptr;
+  float eps = 1e-5f;
+  int M_static = 1;
+  const int32_t* M_dev = nullptr;
+  // outputs
+  float* y = nullptr;         // EPI_STORE [M][R]
+  float* xres = nullptr;      // EPI_RESID [M][R], read and written
+  float* ss_out = nullptr;    // EPI_RESID [M][R/16]
+  bf16* u = nullptr;          // EPI_SWIGLU [M][R]
+  // EPI_LMHEAD
+  float* logits = nullptr;    // [slot + M][R] (nullable)
+  RowStats* stats = nullptr;  // [slot + M]
+  const int32_t* slot_dev = nullptr;
+  float* part = nullptr;      // per-CTA partials [nCTA][16][8]
+  unsigned* counter = nullptr;
+  float temperature = 0.f;
+  uint64_t seed = 0;
+  int round_static = 0;
+  const int32_t* round_dev = nullptr;
+  int sample_stream = 0;
+  int pos0_static = 0;
+  const int32_t* pos0_dev = nullptr;
+};
+
+struct GemvCfg {
+  int RG;  // 16-row groups per CTA
+  int KS;  // warps splitting K for each row group (RG * KS == 8)
+};
+
+// Launch shape for a matrix of `row_groups` 16-row groups and depth K.
+// Depends only on the shape, never on M.
+GemvCfg gemv_pick(int row_groups, int K, int epi);
+int gemv_grid(int row_groups, GemvCfg cfg, int epi);
+
+cudaError_t launch_gemv(int in_mode, int epi, const LinearArgs& a, GemvCfg cfg, cudaStream_t st,
+                        bool pdl);
+
+// Attention over the KV cache for the rows of a pass (see ssd_op_attention).
+struct AttnArgs {
+  const float* qkv = nullptr;  // [M][ld_qkv]
+  int ld_qkv = 0;
+  int M_static = 1;
+  const int32_t* M_dev = nullptr;
+  int pos0_static = 0;
+  const int32_t* pos0_dev = nullptr;
+  bf16* kc = nullptr;          // [Hkv][max_seq][dh]
+  bf16* vc = nullptr;
+  int max_seq = 0;
+  int H = 0, Hkv = 0, dh = 0;
+  const float2* rope = nullptr;  // [max_seq][dh/2] (cos, sin)
+  bf16* out = nullptr;         // [M][H dh]
+  float* part = nullptr;       // [Hkv][max_seq/kAttnChunk][G*16][dh+2]
+  unsigned* counters = nullptr;  // [Hkv]
+  float scale = 1.f;
+};
+
+int attn_grid(const AttnArgs& a);
+size_t attn_smem(const AttnArgs& a);
+size_t attn_part_floats(int Hkv, int H, int dh, int max_seq);
+// Sets the kernel's dynamic shared-memory limit for this head geometry
+// (call once before launching or capturing).
+cudaError_t attn_prepare(const AttnArgs& a);
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st, bool pdl);
+
+// RoPE (cos, sin) table [n_pos][half], angles pos * theta^(-2i/dh) evaluated
+// in double precision and rounded to fp32.
+cudaError_t launch_rope_table(float2* tab, int n_pos, int half, double theta, cudaStream_t s);
+
+// Embedding / pass set-up ("begin") kernel modes.
+enum BeginMode { BEGIN_TOKENS = 0, BEGIN_AR = 1, BEGIN_DRAFT = 2, BEGIN_EXTRA = 3, BEGIN_VERIFY = 4 };
+
+struct BeginArgs {
+  int mode = BEGIN_TOKENS;
+  DevState* st = nullptr;
+  const int32_t* tokens = nullptr;   // committed tokens [max_seq]
+  const int32_t* toks_in = nullptr;  // BEGIN_TOKENS: this pass's tokens
+  int M = 1, pos0 = 0;               // BEGIN_TOKENS
+  int reset_round = 0;               // BEGIN_TOKENS: set round = 0 (prefill)
+  const bf16* embed = nullptr;       // [V][D]
+  int D = 0;
+  float* x = nullptr;                // [16][D]
+  float* ss = nullptr;               // [16][D/16]
+  const float* bx = nullptr;         // boundary states [16][D] (BEGIN_VERIFY)
+  const float* bss = nullptr;
+};
+cudaError_t launch_begin(const BeginArgs& a, cudaStream_t st, bool pdl);
+
+// Copy row 0 of the residual (and its partials) into boundary slot j
+// (draft) or d (extra pass).
+cudaError_t launch_save_boundary(DevState* st, int use_d, const float* x, const float* ss,
+                                 float* bx, float* bss, int D, cudaStream_t s, bool pdl);
+
+cudaError_t launch_draft_end(DevState* st, const RowStats* dstats, float tau, float temperature,
+                             cudaStream_t s, bool pdl);
+cudaError_t launch_ar_end(DevState* st, int32_t* tokens, const RowStats* vstats, int row_from_M,
+                          float temperature, int reset, cudaStream_t s, bool pdl);
+cudaError_t launch_accept_greedy(DevState* st, int32_t* tokens, const RowStats* vstats,
+                                 cudaStream_t s, bool pdl);
+
+struct AcceptArgs {
+  const float* P = nullptr;       // [d+1][V]
+  const float* Q = nullptr;       // [d][V]
+  const int32_t* drafts = nullptr;
+  int d_static = 0;
+  const RowStats* pstats = nullptr;  // nullable: lse_t of P rows
+  const RowStats* qstats = nullptr;  // nullable: lse_t of Q rows
+  int V = 0;
+  float temperature = 1.f;
+  uint64_t seed = 0;
+  int round_static = 0;
+  int n_static = 0;
+  DevState* st = nullptr;         // state-driven mode when not NULL
+  int32_t* tokens = nullptr;      // state-driven: committed tokens
+  int32_t* emitted = nullptr;     // op mode outputs
+  int32_t* n_emitted = nullptr;
+};
+cudaError_t launch_accept_stochastic(const AcceptArgs& a, cudaStream_t s, bool pdl);
+
+cudaError_t launch_philox(const uint32_t* ctr, int count, uint64_t key, uint32_t* out,
+                          cudaStream_t s);
+
+// Sum-of-squares partials of fp32 rows (used by the op entry points to feed
+// the norm-fused GEMV from an arbitrary x).
+cudaError_t launch_ss_partials(const float* x, int M, int D, float* ss, cudaStream_t s);
+
+}  // namespace ssd

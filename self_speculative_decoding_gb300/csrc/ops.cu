@@ -1,0 +1,249 @@
+// Kernel-level C-ABI (ssd_ops.h): each call runs one hot-path kernel on
+// caller-provided device buffers, so that every kernel can be checked on
+// its own against the CPU oracle.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "../../include/ssd_ops.h"
+#include "kernels.cuh"
+
+using namespace ssd;
+
+namespace {
+
+thread_local std::string g_op_err;
+
+ssd_status op_fail(ssd_status s, const std::string& m) {
+  g_op_err = m;
+  return s;
+}
+
+bool al16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
+
+ssd_status check_linear(const void* W, int R, int K, int M) {
+  if (!al16(W)) return op_fail(SSD_ERR_INVALID_ARG, "W must be non-null and 16-byte aligned");
+  if (R <= 0 || R % 16) return op_fail(SSD_ERR_INVALID_ARG, "R must be a positive multiple of 16");
+  if (K <= 0 || K % 32) return op_fail(SSD_ERR_INVALID_ARG, "K must be a positive multiple of 32");
+  if (M < 1 || M > kMaxRows) return op_fail(SSD_ERR_INVALID_ARG, "M must be in 1..16");
+  return SSD_OK;
+}
+
+ssd_status cu(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return SSD_OK;
+  cudaGetLastError();
+  return op_fail(e == cudaErrorMemoryAllocation ? SSD_ERR_OOM : SSD_ERR_CUDA,
+                 std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+// Stream-ordered scratch that is freed on scope exit.
+struct Scratch {
+  cudaStream_t s;
+  void* p = nullptr;
+  Scratch(cudaStream_t st) : s(st) {}
+  cudaError_t alloc(size_t bytes) { return cudaMallocAsync(&p, bytes, s); }
+  ~Scratch() {
+    if (p) cudaFreeAsync(p, s);
+  }
+};
+
+}  // namespace
+
+extern "C" {
+
+const char* ssd_ops_last_error(void) { return g_op_err.c_str(); }
+
+ssd_status ssd_op_linear(const void* W, int32_t R, int32_t K, const void* act, int32_t M,
+                         float* y, void* stream) {
+  ssd_status r = check_linear(W, R, K, M);
+  if (r != SSD_OK) return r;
+  if (!al16(act) || !al16(y)) return op_fail(SSD_ERR_INVALID_ARG, "act / y alignment");
+  LinearArgs a;
+  a.W0 = (const bf16*)W;
+  a.R = R;
+  a.K = K;
+  a.act = (const bf16*)act;
+  a.M_static = M;
+  a.y = y;
+  return cu(launch_gemv(IN_BF16, EPI_STORE, a, gemv_pick(R / 16, K, EPI_STORE),
+                        (cudaStream_t)stream, false), "linear");
+}
+
+ssd_status ssd_op_rmsnorm_linear(const void* W, int32_t R, int32_t K, const float* x,
+                                 const float* gain, float eps, int32_t M, float* y, void* stream) {
+  ssd_status r = check_linear(W, R, K, M);
+  if (r != SSD_OK) return r;
+  if (!al16(x) || !al16(gain) || !al16(y) || !(eps > 0.f))
+    return op_fail(SSD_ERR_INVALID_ARG, "x / gain / y / eps");
+  cudaStream_t s = (cudaStream_t)stream;
+  Scratch ss(s);
+  if ((r = cu(ss.alloc((size_t)M * (K / kSsGroup) * 4), "scratch")) != SSD_OK) return r;
+  if ((r = cu(launch_ss_partials(x, M, K, (float*)ss.p, s), "ss")) != SSD_OK) return r;
+  LinearArgs a;
+  a.W0 = (const bf16*)W;
+  a.R = R;
+  a.K = K;
+  a.x = x;
+  a.ss = (const float*)ss.p;
+  a.gain = gain;
+  a.eps = eps;
+  a.M_static = M;
+  a.y = y;
+  return cu(launch_gemv(IN_NORM, EPI_STORE, a, gemv_pick(R / 16, K, EPI_STORE), s, false),
+            "rmsnorm_linear");
+}
+
+ssd_status ssd_op_residual_linear(const void* W, int32_t R, int32_t K, const void* act, int32_t M,
+                                  float* x, void* stream) {
+  ssd_status r = check_linear(W, R, K, M);
+  if (r != SSD_OK) return r;
+  if (!al16(act) || !al16(x)) return op_fail(SSD_ERR_INVALID_ARG, "act / x alignment");
+  cudaStream_t s = (cudaStream_t)stream;
+  Scratch ss(s);
+  if ((r = cu(ss.alloc((size_t)M * (R / kSsGroup) * 4), "scratch")) != SSD_OK) return r;
+  LinearArgs a;
+  a.W0 = (const bf16*)W;
+  a.R = R;
+  a.K = K;
+  a.act = (const bf16*)act;
+  a.M_static = M;
+  a.xres = x;
+  a.ss_out = (float*)ss.p;
+  return cu(launch_gemv(IN_BF16, EPI_RESID, a, gemv_pick(R / 16, K, EPI_RESID), s, false),
+            "residual_linear");
+}
+
+ssd_status ssd_op_swiglu(const void* Wg, const void* Wu, int32_t F, int32_t K, const float* x,
+                         const float* gain, float eps, int32_t M, void* u, void* stream) {
+  ssd_status r = check_linear(Wg, F, K, M);
+  if (r != SSD_OK) return r;
+  if (!al16(Wu) || !al16(x) || !al16(gain) || !al16(u) || !(eps > 0.f))
+    return op_fail(SSD_ERR_INVALID_ARG, "Wu / x / gain / u / eps");
+  cudaStream_t s = (cudaStream_t)stream;
+  Scratch ss(s);
+  if ((r = cu(ss.alloc((size_t)M * (K / kSsGroup) * 4), "scratch")) != SSD_OK) return r;
+  if ((r = cu(launch_ss_partials(x, M, K, (float*)ss.p, s), "ss")) != SSD_OK) return r;
+  LinearArgs a;
+  a.W0 = (const bf16*)Wg;
+  a.W1 = (const bf16*)Wu;
+  a.R = F;
+  a.K = K;
+  a.x = x;
+  a.ss = (const float*)ss.p;
+  a.gain = gain;
+  a.eps = eps;
+  a.M_static = M;
+  a.u = (bf16*)u;
+  return cu(launch_gemv(IN_NORM, EPI_SWIGLU, a, gemv_pick(F / 16, K, EPI_SWIGLU), s, false),
+            "swiglu");
+}
+
+ssd_status ssd_op_attention(const float* qkv, int32_t M, int32_t pos0, void* k_cache,
+                            void* v_cache, int32_t max_seq, int32_t H, int32_t Hkv, int32_t dh,
+                            float theta, void* out, void* stream) {
+  if (M < 1 || M > kMaxRows || pos0 < 0 || H <= 0 || Hkv <= 0 || H % Hkv || H / Hkv > 8 ||
+      (dh != 64 && dh != 128) || max_seq <= 0 || max_seq % kAttnChunk || pos0 + M > max_seq ||
+      !(theta > 0.f))
+    return op_fail(SSD_ERR_INVALID_ARG, "attention sizes");
+  if (!al16(qkv) || !al16(k_cache) || !al16(v_cache) || !al16(out))
+    return op_fail(SSD_ERR_INVALID_ARG, "attention pointers");
+  cudaStream_t s = (cudaStream_t)stream;
+  ssd_status r;
+  Scratch rope(s), part(s), cnt(s);
+  const int half = dh / 2;
+  if ((r = cu(rope.alloc((size_t)max_seq * half * sizeof(float2)), "scratch")) != SSD_OK) return r;
+  if ((r = cu(part.alloc(attn_part_floats(Hkv, H, dh, max_seq) * 4), "scratch")) != SSD_OK) return r;
+  if ((r = cu(cnt.alloc((size_t)Hkv * 4), "scratch")) != SSD_OK) return r;
+  if ((r = cu(cudaMemsetAsync(cnt.p, 0, (size_t)Hkv * 4, s), "memset")) != SSD_OK) return r;
+  if ((r = cu(launch_rope_table((float2*)rope.p, max_seq, half, (double)theta, s), "rope")) != SSD_OK)
+    return r;
+  AttnArgs a;
+  a.qkv = qkv;
+  a.ld_qkv = (H + 2 * Hkv) * dh;
+  a.M_static = M;
+  a.pos0_static = pos0;
+  a.kc = (bf16*)k_cache;
+  a.vc = (bf16*)v_cache;
+  a.max_seq = max_seq;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.dh = dh;
+  a.rope = (const float2*)rope.p;
+  a.out = (bf16*)out;
+  a.part = (float*)part.p;
+  a.counters = (unsigned*)cnt.p;
+  a.scale = (float)(1.0 / std::sqrt((double)dh));
+  if ((r = cu(attn_prepare(a), "attn_prepare")) != SSD_OK) return r;
+  return cu(launch_attention(a, s, false), "attention");
+}
+
+ssd_status ssd_op_lm_head(const void* W, int32_t V, int32_t D, const float* x, const float* gain,
+                          float eps, int32_t M, float temperature, uint64_t seed, int32_t round,
+                          int32_t stream_id, int32_t pos0, float* logits, ssd_row_stats* stats,
+                          void* stream) {
+  ssd_status r = check_linear(W, V, D, M);
+  if (r != SSD_OK) return r;
+  if (!al16(x) || !al16(gain) || !al16(stats) || (logits && !al16(logits)) || !(eps > 0.f) ||
+      !(temperature >= 0.f))
+    return op_fail(SSD_ERR_INVALID_ARG, "lm_head pointers / eps / temperature");
+  cudaStream_t s = (cudaStream_t)stream;
+  const GemvCfg cfg = gemv_pick(V / 16, D, EPI_LMHEAD);
+  const int ctas = gemv_grid(V / 16, cfg, EPI_LMHEAD);
+  Scratch ss(s), part(s), cnt(s);
+  if ((r = cu(ss.alloc((size_t)M * (D / kSsGroup) * 4), "scratch")) != SSD_OK) return r;
+  if ((r = cu(part.alloc((size_t)ctas * kMaxRows * 8 * 4), "scratch")) != SSD_OK) return r;
+  if ((r = cu(cnt.alloc(4), "scratch")) != SSD_OK) return r;
+  if ((r = cu(cudaMemsetAsync(cnt.p, 0, 4, s), "memset")) != SSD_OK) return r;
+  if ((r = cu(launch_ss_partials(x, M, D, (float*)ss.p, s), "ss")) != SSD_OK) return r;
+  LinearArgs a;
+  a.W0 = (const bf16*)W;
+  a.R = V;
+  a.K = D;
+  a.x = x;
+  a.ss = (const float*)ss.p;
+  a.gain = gain;
+  a.eps = eps;
+  a.M_static = M;
+  a.logits = logits;
+  a.stats = (RowStats*)stats;
+  a.part = (float*)part.p;
+  a.counter = (unsigned*)cnt.p;
+  a.temperature = temperature;
+  a.seed = seed;
+  a.round_static = round;
+  a.sample_stream = stream_id;
+  a.pos0_static = pos0;
+  return cu(launch_gemv(IN_NORM, EPI_LMHEAD, a, cfg, s, false), "lm_head");
+}
+
+ssd_status ssd_op_accept_stochastic(const float* P, const float* Q, const int32_t* drafts,
+                                    int32_t d, int32_t V, float temperature, uint64_t seed,
+                                    int32_t round, int32_t n, int32_t* emitted,
+                                    int32_t* n_emitted, void* stream) {
+  if (!P || (d > 0 && (!Q || !drafts)) || !emitted || !n_emitted || d < 0 || d > kMaxRows - 1 ||
+      V <= 0 || !(temperature > 0.f) || n < 0)
+    return op_fail(SSD_ERR_INVALID_ARG, "accept arguments");
+  AcceptArgs a;
+  a.P = P;
+  a.Q = Q;
+  a.drafts = drafts;
+  a.d_static = d;
+  a.V = V;
+  a.temperature = temperature;
+  a.seed = seed;
+  a.round_static = round;
+  a.n_static = n;
+  a.emitted = emitted;
+  a.n_emitted = n_emitted;
+  return cu(launch_accept_stochastic(a, (cudaStream_t)stream, false), "accept");
+}
+
+ssd_status ssd_op_philox(const uint32_t* ctr, int32_t count, uint64_t key, uint32_t* out,
+                         void* stream) {
+  if (count < 0 || (count > 0 && (!al16(ctr) || !al16(out))))
+    return op_fail(SSD_ERR_INVALID_ARG, "philox arguments");
+  return cu(launch_philox(ctr, count, key, out, (cudaStream_t)stream), "philox");
+}
+
+}  // extern "C"

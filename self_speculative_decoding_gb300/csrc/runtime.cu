@@ -1,0 +1,878 @@
+// libssd context runtime: KV cache, workspaces, CUDA graphs and the
+// draft / verify / accept loop (the C-ABI of ssd.h).
+//
+// One context drives one model on one GPU.  Every step's dynamic values
+// (rows, positions, tokens) live in a device-side DevState, so each kind of
+// pass is captured once as a CUDA graph and replayed:
+//   draft step  : begin(draft) -> layers < s0 -> save boundary -> kept layers
+//                 >= s0 -> LM head (+summary) -> draft end (confidence stop)
+//   extra pass  : begin(extra) -> layers < s0 -> save boundary
+//   verify pass : begin(verify) -> layers s0..L-1 over d+1 rows -> LM head
+//   accept      : greedy prefix or min(1, p/q) acceptance, commit, rollback
+//   AR step     : begin(ar) -> all layers -> LM head -> commit
+// The host reads back a few bytes per draft step (the confidence stop) and
+// per round (the emitted tokens).
+#include <chrono>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "../../include/ssd.h"
+#include "kernels.cuh"
+
+using namespace ssd;
+
+namespace {
+
+enum Phase { PH_NONE = 0, PH_IDLE = 1, PH_DRAFTED = 2, PH_VERIFIED = 3 };
+
+struct Graph {
+  cudaGraphExec_t exec = nullptr;
+  int nodes = 0;
+  void reset() {
+    if (exec) cudaGraphExecDestroy(exec);
+    exec = nullptr;
+    nodes = 0;
+  }
+};
+
+}  // namespace
+
+struct ssd_ctx {
+  ssd_config cfg{};
+  std::vector<ssd_layer_weights> layers;
+  const bf16* embed = nullptr;
+  const float* final_norm = nullptr;
+  const bf16* lm_head = nullptr;
+  cudaStream_t stream = nullptr;
+  cudaStream_t cap = nullptr;
+  cudaEvent_t ev = nullptr;
+  int timeout_ms = 120000;
+  bool pdl = true;
+
+  ssd_policy pol{};
+  bool has_policy = false;
+  int s0 = 0;
+  std::vector<int> pre, post, verify_layers;
+
+  // device buffers
+  bf16* kc = nullptr;
+  bf16* vc = nullptr;
+  float* x = nullptr;
+  float* ss = nullptr;
+  float* bx = nullptr;
+  float* bss = nullptr;
+  float* qkv = nullptr;
+  bf16* attn = nullptr;
+  bf16* u = nullptr;
+  float2* rope = nullptr;
+  float* attn_part = nullptr;
+  unsigned* attn_cnt = nullptr;
+  float* lm_part = nullptr;
+  unsigned* lm_cnt = nullptr;
+  RowStats* dstats = nullptr;
+  RowStats* vstats = nullptr;
+  float* dlogits = nullptr;
+  float* vlogits = nullptr;
+  int32_t* tokens = nullptr;
+  int32_t* toks_in = nullptr;
+  DevState* st = nullptr;
+  DevState* h_st = nullptr;  // pinned mirror
+  int32_t* h_tok = nullptr;  // pinned staging [max_seq]
+
+  GemvCfg c_qkv{}, c_o{}, c_gu{}, c_dn{}, c_lm{};
+  Graph g_draft, g_extra, g_verify, g_accept, g_ar;
+
+  Phase phase = PH_NONE;
+  // profiling: events recorded around every eager launch
+  bool profiling = false;
+  int prof_class = 6;
+  std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> prof_events;
+  int64_t launches = 0;
+  int capturing_nodes = 0;
+  bool capturing = false;
+  std::string err;
+};
+
+namespace {
+
+thread_local char g_static_err[256];
+
+ssd_status fail(ssd_ctx* c, ssd_status s, const std::string& msg) {
+  if (c) c->err = msg;
+  return s;
+}
+
+#define CK(call)                                                                          \
+  do {                                                                                    \
+    cudaError_t e_ = (call);                                                              \
+    if (e_ != cudaSuccess)                                                                \
+      return fail(c, SSD_ERR_CUDA, std::string(#call) + ": " + cudaGetErrorString(e_));  \
+  } while (0)
+
+size_t kv_elems(const ssd_config& g) {
+  return (size_t)g.n_layers * g.n_kv_heads * g.max_seq * g.head_dim;
+}
+size_t kv_layer_elems(const ssd_config& g) {
+  return (size_t)g.n_kv_heads * g.max_seq * g.head_dim;
+}
+int qkv_rows(const ssd_config& g) { return (g.n_heads + 2 * g.n_kv_heads) * g.head_dim; }
+
+bool skipped(const ssd_policy& p, int l) { return (p.skip_mask[l >> 6] >> (l & 63)) & 1ull; }
+
+// Bounded host wait on the context stream.
+ssd_status wait_stream(ssd_ctx* c) {
+  CK(cudaEventRecord(c->ev, c->stream));
+  const auto t0 = std::chrono::steady_clock::now();
+  int spins = 0;
+  for (;;) {
+    const cudaError_t e = cudaEventQuery(c->ev);
+    if (e == cudaSuccess) return SSD_OK;
+    if (e != cudaErrorNotReady)
+      return fail(c, SSD_ERR_CUDA, std::string("stream: ") + cudaGetErrorString(e));
+    if (++spins > 2000) {
+      const auto ms = std::chrono::duration_cast<std::chrono::milliseconds>(
+                          std::chrono::steady_clock::now() - t0)
+                          .count();
+      if (ms > c->timeout_ms) return fail(c, SSD_ERR_TIMEOUT, "timed out waiting for the GPU");
+      std::this_thread::sleep_for(std::chrono::microseconds(20));
+    }
+  }
+}
+
+ssd_status read_state(ssd_ctx* c) {
+  CK(cudaMemcpyAsync(c->h_st, c->st, sizeof(DevState), cudaMemcpyDeviceToHost, c->stream));
+  return wait_stream(c);
+}
+
+// ---------------------------------------------------------------------------
+// enqueue helpers (eager stream or capture stream)
+
+ssd_status note(ssd_ctx* c, cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return fail(c, SSD_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+  if (c->capturing) c->capturing_nodes++;
+  else c->launches++;
+  if (c->profiling) {
+    // close the event pair opened by prof_begin
+    cudaEventRecord(c->prof_events.back().second.second, c->stream);
+  }
+  return SSD_OK;
+}
+
+// Opens an event pair before an eager launch of kernel class `cls`.
+void prof_begin(ssd_ctx* c, int cls) {
+  if (!c->profiling) return;
+  cudaEvent_t a, b;
+  cudaEventCreate(&a);
+  cudaEventCreate(&b);
+  cudaEventRecord(a, c->stream);
+  c->prof_events.push_back({cls, {a, b}});
+}
+
+ssd_status enq_layer(ssd_ctx* c, int l, cudaStream_t s) {
+  const ssd_config& g = c->cfg;
+  const ssd_layer_weights& w = c->layers[l];
+  ssd_status r;
+  {
+    LinearArgs a;
+    a.W0 = (const bf16*)w.wqkv;
+    a.R = qkv_rows(g);
+    a.K = g.d_model;
+    a.x = c->x;
+    a.ss = c->ss;
+    a.gain = (const float*)w.attn_norm;
+    a.eps = g.norm_eps;
+    a.M_dev = &c->st->M;
+    a.y = c->qkv;
+    prof_begin(c, 0);
+    if ((r = note(c, launch_gemv(IN_NORM, EPI_STORE, a, c->c_qkv, s, c->pdl), "qkv")) != SSD_OK)
+      return r;
+  }
+  {
+    AttnArgs a;
+    a.qkv = c->qkv;
+    a.ld_qkv = qkv_rows(g);
+    a.M_dev = &c->st->M;
+    a.pos0_dev = &c->st->pos0;
+    a.kc = c->kc + (size_t)l * kv_layer_elems(g);
+    a.vc = c->vc + (size_t)l * kv_layer_elems(g);
+    a.max_seq = g.max_seq;
+    a.H = g.n_heads;
+    a.Hkv = g.n_kv_heads;
+    a.dh = g.head_dim;
+    a.rope = c->rope;
+    a.out = c->attn;
+    a.part = c->attn_part;
+    a.counters = c->attn_cnt;
+    a.scale = (float)(1.0 / std::sqrt((double)g.head_dim));
+    prof_begin(c, 1);
+    if ((r = note(c, launch_attention(a, s, c->pdl), "attention")) != SSD_OK) return r;
+  }
+  {
+    LinearArgs a;
+    a.W0 = (const bf16*)w.wo;
+    a.R = g.d_model;
+    a.K = g.n_heads * g.head_dim;
+    a.act = c->attn;
+    a.M_dev = &c->st->M;
+    a.xres = c->x;
+    a.ss_out = c->ss;
+    prof_begin(c, 2);
+    if ((r = note(c, launch_gemv(IN_BF16, EPI_RESID, a, c->c_o, s, c->pdl), "o_proj")) != SSD_OK)
+      return r;
+  }
+  {
+    LinearArgs a;
+    a.W0 = (const bf16*)w.w_gate;
+    a.W1 = (const bf16*)w.w_up;
+    a.R = g.ffn_dim;
+    a.K = g.d_model;
+    a.x = c->x;
+    a.ss = c->ss;
+    a.gain = (const float*)w.mlp_norm;
+    a.eps = g.norm_eps;
+    a.M_dev = &c->st->M;
+    a.u = c->u;
+    prof_begin(c, 3);
+    if ((r = note(c, launch_gemv(IN_NORM, EPI_SWIGLU, a, c->c_gu, s, c->pdl), "gate_up")) != SSD_OK)
+      return r;
+  }
+  {
+    LinearArgs a;
+    a.W0 = (const bf16*)w.w_down;
+    a.R = g.d_model;
+    a.K = g.ffn_dim;
+    a.act = c->u;
+    a.M_dev = &c->st->M;
+    a.xres = c->x;
+    a.ss_out = c->ss;
+    prof_begin(c, 4);
+    if ((r = note(c, launch_gemv(IN_BF16, EPI_RESID, a, c->c_dn, s, c->pdl), "down")) != SSD_OK)
+      return r;
+  }
+  return SSD_OK;
+}
+
+ssd_status enq_layers(ssd_ctx* c, const std::vector<int>& ls, cudaStream_t s) {
+  for (int l : ls) {
+    const ssd_status r = enq_layer(c, l, s);
+    if (r != SSD_OK) return r;
+  }
+  return SSD_OK;
+}
+
+ssd_status enq_lmhead(ssd_ctx* c, RowStats* stats, float* logits, const int32_t* slot_dev,
+                      int sample_stream, cudaStream_t s) {
+  const ssd_config& g = c->cfg;
+  LinearArgs a;
+  a.W0 = c->lm_head;
+  a.R = g.vocab;
+  a.K = g.d_model;
+  a.x = c->x;
+  a.ss = c->ss;
+  a.gain = c->final_norm;
+  a.eps = g.norm_eps;
+  a.M_dev = &c->st->M;
+  a.logits = logits;
+  a.stats = stats;
+  a.slot_dev = slot_dev;
+  a.part = c->lm_part;
+  a.counter = c->lm_cnt;
+  a.temperature = sample_stream >= 0 ? c->pol.temperature : 0.f;
+  a.seed = c->pol.seed;
+  a.round_dev = &c->st->round;
+  a.sample_stream = sample_stream < 0 ? 0 : sample_stream;
+  a.pos0_dev = &c->st->pos0;
+  prof_begin(c, 5);
+  return note(c, launch_gemv(IN_NORM, EPI_LMHEAD, a, c->c_lm, s, c->pdl), "lm_head");
+}
+
+ssd_status enq_begin(ssd_ctx* c, int mode, cudaStream_t s, int M = 1, int pos0 = 0,
+                     const int32_t* toks_in = nullptr, int reset = 0) {
+  BeginArgs b;
+  b.mode = mode;
+  b.st = c->st;
+  b.tokens = c->tokens;
+  b.toks_in = toks_in;
+  b.M = M;
+  b.pos0 = pos0;
+  b.reset_round = reset;
+  b.embed = c->embed;
+  b.D = c->cfg.d_model;
+  b.x = c->x;
+  b.ss = c->ss;
+  b.bx = c->bx;
+  b.bss = c->bss;
+  prof_begin(c, 6);
+  return note(c, launch_begin(b, s, c->pdl), "begin");
+}
+
+// ---------------------------------------------------------------------------
+// graphs
+
+typedef ssd_status (*Builder)(ssd_ctx*, cudaStream_t);
+
+ssd_status build_graph(ssd_ctx* c, Graph& g, Builder fn) {
+  g.reset();
+  CK(cudaStreamBeginCapture(c->cap, cudaStreamCaptureModeThreadLocal));
+  c->capturing = true;
+  c->capturing_nodes = 0;
+  ssd_status r = fn(c, c->cap);
+  c->capturing = false;
+  cudaGraph_t graph = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(c->cap, &graph);
+  if (r != SSD_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    return r;
+  }
+  if (e != cudaSuccess) return fail(c, SSD_ERR_CUDA, std::string("capture: ") + cudaGetErrorString(e));
+  const cudaError_t e2 = cudaGraphInstantiate(&g.exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (e2 != cudaSuccess)
+    return fail(c, SSD_ERR_CUDA, std::string("instantiate: ") + cudaGetErrorString(e2));
+  g.nodes = c->capturing_nodes;
+  return SSD_OK;
+}
+
+ssd_status b_draft(ssd_ctx* c, cudaStream_t s) {
+  ssd_status r;
+  if ((r = enq_begin(c, BEGIN_DRAFT, s)) != SSD_OK) return r;
+  if ((r = enq_layers(c, c->pre, s)) != SSD_OK) return r;
+  if ((r = note(c, launch_save_boundary(c->st, 0, c->x, c->ss, c->bx, c->bss, c->cfg.d_model, s,
+                                        c->pdl), "save_boundary")) != SSD_OK)
+    return r;
+  if ((r = enq_layers(c, c->post, s)) != SSD_OK) return r;
+  if ((r = enq_lmhead(c, c->dstats, c->dlogits, &c->st->slot, 0, s)) != SSD_OK) return r;
+  return note(c, launch_draft_end(c->st, c->dstats, c->pol.tau, c->pol.temperature, s, c->pdl),
+              "draft_end");
+}
+
+ssd_status b_extra(ssd_ctx* c, cudaStream_t s) {
+  ssd_status r;
+  if ((r = enq_begin(c, BEGIN_EXTRA, s)) != SSD_OK) return r;
+  if ((r = enq_layers(c, c->pre, s)) != SSD_OK) return r;
+  return note(c, launch_save_boundary(c->st, 1, c->x, c->ss, c->bx, c->bss, c->cfg.d_model, s,
+                                      c->pdl), "save_boundary");
+}
+
+ssd_status b_verify(ssd_ctx* c, cudaStream_t s) {
+  ssd_status r;
+  if ((r = enq_begin(c, BEGIN_VERIFY, s)) != SSD_OK) return r;
+  if ((r = enq_layers(c, c->verify_layers, s)) != SSD_OK) return r;
+  return enq_lmhead(c, c->vstats, c->vlogits, nullptr, -1, s);
+}
+
+ssd_status b_accept(ssd_ctx* c, cudaStream_t s) {
+  if (c->pol.temperature > 0.f) {
+    AcceptArgs a;
+    a.P = c->vlogits;
+    a.Q = c->dlogits;
+    a.pstats = c->vstats;
+    a.qstats = c->dstats;
+    a.V = c->cfg.vocab;
+    a.temperature = c->pol.temperature;
+    a.seed = c->pol.seed;
+    a.st = c->st;
+    a.tokens = c->tokens;
+    return note(c, launch_accept_stochastic(a, s, c->pdl), "accept");
+  }
+  return note(c, launch_accept_greedy(c->st, c->tokens, c->vstats, s, c->pdl), "accept");
+}
+
+ssd_status b_ar(ssd_ctx* c, cudaStream_t s) {
+  ssd_status r;
+  if ((r = enq_begin(c, BEGIN_AR, s)) != SSD_OK) return r;
+  std::vector<int> all(c->cfg.n_layers);
+  for (int l = 0; l < c->cfg.n_layers; ++l) all[l] = l;
+  if ((r = enq_layers(c, all, s)) != SSD_OK) return r;
+  if ((r = enq_lmhead(c, c->vstats, nullptr, nullptr, 2, s)) != SSD_OK) return r;
+  prof_begin(c, 6);
+  return note(c, launch_ar_end(c->st, c->tokens, c->vstats, 0, c->pol.temperature, 0, s, c->pdl),
+              "ar_end");
+}
+
+ssd_status build_graphs(ssd_ctx* c) {
+  ssd_status r;
+  if ((r = build_graph(c, c->g_draft, b_draft)) != SSD_OK) return r;
+  if ((r = build_graph(c, c->g_extra, b_extra)) != SSD_OK) return r;
+  if ((r = build_graph(c, c->g_verify, b_verify)) != SSD_OK) return r;
+  if ((r = build_graph(c, c->g_accept, b_accept)) != SSD_OK) return r;
+  return build_graph(c, c->g_ar, b_ar);
+}
+
+ssd_status replay(ssd_ctx* c, Graph& g) {
+  CK(cudaGraphLaunch(g.exec, c->stream));
+  c->launches += g.nodes;
+  return SSD_OK;
+}
+
+// algorithmic bytes of one pass: weights of the layers run (+ LM head), K/V
+// read for positions [0, pos0 + M) and written for M positions per layer.
+double pass_bytes(const ssd_ctx* c, int n_layers_run, bool lm, int pos0, int M) {
+  const ssd_config& g = c->cfg;
+  const double layer_w = 2.0 * ((double)qkv_rows(g) * g.d_model +
+                                (double)g.d_model * g.n_heads * g.head_dim +
+                                3.0 * g.d_model * g.ffn_dim);
+  const double kv_pos = 2.0 * 2.0 * g.n_kv_heads * g.head_dim;
+  double b = n_layers_run * (layer_w + kv_pos * (pos0 + M) + kv_pos * M);
+  if (lm) b += 2.0 * (double)g.vocab * g.d_model;
+  return b;
+}
+
+ssd_status check_capacity(ssd_ctx* c, int extra) {
+  if (c->h_st->n + extra > c->cfg.max_seq)
+    return fail(c, SSD_ERR_CAPACITY, "KV cache capacity (max_seq) exceeded");
+  return SSD_OK;
+}
+
+// Draft loop (host side of the confidence stop).  Returns with h_st read.
+ssd_status run_draft(ssd_ctx* c, ssd_stats* stats) {
+  ssd_status r;
+  const int n = c->h_st->n;
+  for (int j = 0; j < c->pol.d_max; ++j) {
+    if ((r = replay(c, c->g_draft)) != SSD_OK) return r;
+    if ((r = read_state(c)) != SSD_OK) return r;
+    if (stats) {
+      stats->draft_steps++;
+      stats->bytes_streamed += pass_bytes(c, (int)(c->pre.size() + c->post.size()), true, n - 1 + j, 1);
+    }
+    if (c->h_st->stop) break;
+  }
+  c->phase = PH_DRAFTED;
+  return SSD_OK;
+}
+
+ssd_status run_verify(ssd_ctx* c, ssd_stats* stats) {
+  ssd_status r;
+  const int n = c->h_st->n, d = c->h_st->d;
+  const bool extra = !c->h_st->stop;
+  if (extra) {
+    if ((r = replay(c, c->g_extra)) != SSD_OK) return r;
+    if (stats) stats->bytes_streamed += pass_bytes(c, (int)c->pre.size(), false, n - 1 + d, 1);
+  }
+  if ((r = replay(c, c->g_verify)) != SSD_OK) return r;
+  if (stats) stats->bytes_streamed += pass_bytes(c, (int)c->verify_layers.size(), true, n - 1, d + 1);
+  c->phase = PH_VERIFIED;
+  return SSD_OK;
+}
+
+ssd_status ensure_policy(ssd_ctx* c) {
+  if (!c->has_policy) return fail(c, SSD_ERR_STATE, "no policy set (ssd_set_policy)");
+  if (c->phase == PH_NONE) return fail(c, SSD_ERR_STATE, "no prefill");
+  return SSD_OK;
+}
+
+}  // namespace
+
+// ===========================================================================
+// C-ABI
+
+extern "C" {
+
+ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream, ssd_ctx** out) {
+  ssd_ctx* c = nullptr;
+  if (!cfg || !w || !out || !w->layers || !w->tok_embed || !w->lm_head || !w->final_norm)
+    return SSD_ERR_INVALID_ARG;
+  *out = nullptr;
+  const ssd_config& g = *cfg;
+  if (g.n_layers <= 0 || g.n_layers > 256 || g.d_model <= 0 || g.d_model % 64 ||
+      g.n_heads <= 0 || g.n_kv_heads <= 0 || g.n_heads % g.n_kv_heads ||
+      (g.head_dim != 64 && g.head_dim != 128) || g.ffn_dim <= 0 || g.ffn_dim % 32 ||
+      g.vocab <= 0 || g.vocab % 16 || g.max_seq <= 0 || g.max_seq % kAttnChunk ||
+      g.max_draft < 1 || g.max_draft > kMaxRows - 1 || g.max_score_rows < 0 ||
+      (g.n_heads * g.head_dim) % 32 || g.n_heads / g.n_kv_heads > 8 || !(g.norm_eps > 0.f) ||
+      !(g.rope_theta > 0.f))
+    return SSD_ERR_INVALID_ARG;
+  for (int l = 0; l < g.n_layers; ++l) {
+    const ssd_layer_weights& L = w->layers[l];
+    if (!L.attn_norm || !L.wqkv || !L.wo || !L.mlp_norm || !L.w_gate || !L.w_up || !L.w_down)
+      return SSD_ERR_INVALID_ARG;
+  }
+  c = new ssd_ctx();
+  c->cfg = g;
+  c->layers.assign(w->layers, w->layers + g.n_layers);
+  c->embed = (const bf16*)w->tok_embed;
+  c->final_norm = (const float*)w->final_norm;
+  c->lm_head = (const bf16*)w->lm_head;
+  c->stream = (cudaStream_t)stream;
+
+  auto alloc = [&](void** p, size_t bytes) -> bool {
+    if (cudaMalloc(p, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    return true;
+  };
+  const int D = g.d_model, F = g.ffn_dim, V = g.vocab;
+  const int nr = kMaxRows;
+  const GemvCfg lmc = gemv_pick(V / 16, D, EPI_LMHEAD);
+  const int lm_ctas = gemv_grid(V / 16, lmc, EPI_LMHEAD);
+  bool ok = alloc((void**)&c->kc, kv_elems(g) * sizeof(bf16)) &&
+            alloc((void**)&c->vc, kv_elems(g) * sizeof(bf16)) &&
+            alloc((void**)&c->x, (size_t)nr * D * 4) &&
+            alloc((void**)&c->ss, (size_t)nr * (D / kSsGroup) * 4) &&
+            alloc((void**)&c->bx, (size_t)nr * D * 4) &&
+            alloc((void**)&c->bss, (size_t)nr * (D / kSsGroup) * 4) &&
+            alloc((void**)&c->qkv, (size_t)nr * qkv_rows(g) * 4) &&
+            alloc((void**)&c->attn, (size_t)nr * g.n_heads * g.head_dim * 2) &&
+            alloc((void**)&c->u, (size_t)nr * F * 2) &&
+            alloc((void**)&c->rope, (size_t)g.max_seq * (g.head_dim / 2) * sizeof(float2)) &&
+            alloc((void**)&c->attn_part,
+                  attn_part_floats(g.n_kv_heads, g.n_heads, g.head_dim, g.max_seq) * 4) &&
+            alloc((void**)&c->attn_cnt, (size_t)g.n_kv_heads * 4) &&
+            alloc((void**)&c->lm_part, (size_t)lm_ctas * kMaxRows * 8 * 4) &&
+            alloc((void**)&c->lm_cnt, 4) &&
+            alloc((void**)&c->dstats, (size_t)nr * sizeof(RowStats)) &&
+            alloc((void**)&c->vstats, (size_t)nr * sizeof(RowStats)) &&
+            alloc((void**)&c->dlogits, (size_t)nr * V * 4) &&
+            alloc((void**)&c->vlogits, (size_t)nr * V * 4) &&
+            alloc((void**)&c->tokens, (size_t)g.max_seq * 4) &&
+            alloc((void**)&c->toks_in, (size_t)g.max_seq * 4) &&
+            alloc((void**)&c->st, sizeof(DevState));
+  if (!ok) {
+    ssd_destroy(c);
+    return SSD_ERR_OOM;
+  }
+  if (cudaMallocHost((void**)&c->h_st, sizeof(DevState)) != cudaSuccess ||
+      cudaMallocHost((void**)&c->h_tok, (size_t)g.max_seq * 4) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&c->cap, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->ev, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    ssd_destroy(c);
+    return SSD_ERR_OOM;
+  }
+  memset(c->h_st, 0, sizeof(DevState));
+  cudaMemsetAsync(c->st, 0, sizeof(DevState), c->stream);
+  cudaMemsetAsync(c->attn_cnt, 0, (size_t)g.n_kv_heads * 4, c->stream);
+  cudaMemsetAsync(c->lm_cnt, 0, 4, c->stream);
+  cudaMemsetAsync(c->tokens, 0, (size_t)g.max_seq * 4, c->stream);
+  const int half = g.head_dim / 2;
+  launch_rope_table(c->rope, g.max_seq, half, (double)g.rope_theta, c->stream);
+  {
+    AttnArgs probe;
+    probe.H = g.n_heads;
+    probe.Hkv = g.n_kv_heads;
+    probe.dh = g.head_dim;
+    attn_prepare(probe);
+  }
+  c->c_qkv = gemv_pick(qkv_rows(g) / 16, D, EPI_STORE);
+  c->c_o = gemv_pick(D / 16, g.n_heads * g.head_dim, EPI_RESID);
+  c->c_gu = gemv_pick(F / 16, D, EPI_SWIGLU);
+  c->c_dn = gemv_pick(D / 16, F, EPI_RESID);
+  c->c_lm = lmc;
+  const cudaError_t e = cudaStreamSynchronize(c->stream);
+  if (e != cudaSuccess) {
+    ssd_destroy(c);
+    return SSD_ERR_CUDA;
+  }
+  *out = c;
+  return SSD_OK;
+}
+
+ssd_status ssd_destroy(ssd_ctx* c) {
+  if (!c) return SSD_OK;
+  cudaStreamSynchronize(c->stream);
+  c->g_draft.reset();
+  c->g_extra.reset();
+  c->g_verify.reset();
+  c->g_accept.reset();
+  c->g_ar.reset();
+  void* bufs[] = {c->kc, c->vc, c->x, c->ss, c->bx, c->bss, c->qkv, c->attn, c->u, c->rope,
+                  c->attn_part, c->attn_cnt, c->lm_part, c->lm_cnt, c->dstats, c->vstats,
+                  c->dlogits, c->vlogits, c->tokens, c->toks_in, c->st};
+  for (void* p : bufs)
+    if (p) cudaFree(p);
+  if (c->h_st) cudaFreeHost(c->h_st);
+  if (c->h_tok) cudaFreeHost(c->h_tok);
+  if (c->cap) cudaStreamDestroy(c->cap);
+  if (c->ev) cudaEventDestroy(c->ev);
+  cudaGetLastError();
+  delete c;
+  return SSD_OK;
+}
+
+ssd_status ssd_set_policy(ssd_ctx* c, const ssd_policy* p) {
+  if (!c || !p) return SSD_ERR_INVALID_ARG;
+  const int L = c->cfg.n_layers;
+  if (p->mode != SSD_MODE_SKIP && p->mode != SSD_MODE_EXIT)
+    return fail(c, SSD_ERR_INVALID_ARG, "policy mode");
+  if (p->mode == SSD_MODE_EXIT && (p->exit_layer < 0 || p->exit_layer >= L))
+    return fail(c, SSD_ERR_INVALID_ARG, "exit_layer out of range");
+  if (p->d_max < 0) return fail(c, SSD_ERR_INVALID_ARG, "d_max < 0");
+  if (p->d_max > c->cfg.max_draft) return fail(c, SSD_ERR_CAPACITY, "d_max > max_draft");
+  if (!(p->temperature >= 0.f) || !std::isfinite(p->temperature))
+    return fail(c, SSD_ERR_INVALID_ARG, "temperature");
+  if (c->phase == PH_DRAFTED || c->phase == PH_VERIFIED)
+    return fail(c, SSD_ERR_STATE, "a round is in flight");
+  c->pol = *p;
+  c->pre.clear();
+  c->post.clear();
+  c->verify_layers.clear();
+  if (p->mode == SSD_MODE_SKIP) {
+    c->s0 = L;
+    for (int l = 0; l < L; ++l)
+      if (skipped(*p, l)) { c->s0 = l; break; }
+    for (int l = 0; l < L; ++l) {
+      if (l < c->s0) c->pre.push_back(l);
+      else if (!skipped(*p, l)) c->post.push_back(l);
+    }
+  } else {
+    c->s0 = p->exit_layer + 1;
+    for (int l = 0; l < c->s0; ++l) c->pre.push_back(l);
+  }
+  for (int l = c->s0; l < L; ++l) c->verify_layers.push_back(l);
+  c->has_policy = true;
+  const ssd_status r = build_graphs(c);
+  if (r != SSD_OK) c->has_policy = false;
+  return r;
+}
+
+ssd_status ssd_prefill(ssd_ctx* c, const int32_t* tokens, int32_t n, int32_t* first) {
+  if (!c || !tokens || n < 1) return c ? fail(c, SSD_ERR_INVALID_ARG, "prefill args") : SSD_ERR_INVALID_ARG;
+  if (!c->has_policy) return fail(c, SSD_ERR_STATE, "no policy set (ssd_set_policy)");
+  if (n + 1 > c->cfg.max_seq) return fail(c, SSD_ERR_CAPACITY, "prompt longer than max_seq - 1");
+  for (int i = 0; i < n; ++i)
+    if (tokens[i] < 0 || tokens[i] >= c->cfg.vocab) return fail(c, SSD_ERR_INVALID_ARG, "token id out of range");
+  memcpy(c->h_tok, tokens, (size_t)n * 4);
+  CK(cudaMemcpyAsync(c->toks_in, c->h_tok, (size_t)n * 4, cudaMemcpyHostToDevice, c->stream));
+  CK(cudaMemcpyAsync(c->tokens, c->h_tok, (size_t)n * 4, cudaMemcpyHostToDevice, c->stream));
+  std::vector<int> all(c->cfg.n_layers);
+  for (int l = 0; l < c->cfg.n_layers; ++l) all[l] = l;
+  ssd_status r;
+  for (int p0 = 0; p0 < n; p0 += kMaxRows) {
+    const int M = n - p0 < kMaxRows ? n - p0 : kMaxRows;
+    if ((r = enq_begin(c, BEGIN_TOKENS, c->stream, M, p0, c->toks_in + p0, p0 == 0)) != SSD_OK) return r;
+    if ((r = enq_layers(c, all, c->stream)) != SSD_OK) return r;
+  }
+  if ((r = enq_lmhead(c, c->vstats, nullptr, nullptr, 2, c->stream)) != SSD_OK) return r;
+  if ((r = note(c, launch_ar_end(c->st, c->tokens, c->vstats, 1, c->pol.temperature, 1, c->stream,
+                                 c->pdl), "prefill_end")) != SSD_OK)
+    return r;
+  if ((r = read_state(c)) != SSD_OK) return r;
+  if (first) *first = c->h_st->emitted[0];
+  c->phase = PH_IDLE;
+  return SSD_OK;
+}
+
+ssd_status ssd_draft(ssd_ctx* c, int32_t* draft_out, float* conf_out, int32_t* d_out) {
+  if (!c) return SSD_ERR_INVALID_ARG;
+  ssd_status r = ensure_policy(c);
+  if (r != SSD_OK) return r;
+  if (c->phase != PH_IDLE) return fail(c, SSD_ERR_STATE, "a draft is already pending");
+  if ((r = check_capacity(c, c->pol.d_max + 1)) != SSD_OK) return r;
+  if ((r = run_draft(c, nullptr)) != SSD_OK) return r;
+  const int d = c->h_st->d;
+  if (draft_out)
+    for (int i = 0; i < d; ++i) draft_out[i] = c->h_st->draft_tok[i];
+  if (conf_out)
+    for (int i = 0; i < c->h_st->j; ++i) conf_out[i] = c->h_st->draft_conf[i];
+  if (d_out) *d_out = d;
+  return SSD_OK;
+}
+
+ssd_status ssd_verify(ssd_ctx* c, float* logits_out) {
+  if (!c) return SSD_ERR_INVALID_ARG;
+  if (c->phase != PH_DRAFTED) return fail(c, SSD_ERR_STATE, "verify without a pending draft");
+  ssd_status r = run_verify(c, nullptr);
+  if (r != SSD_OK) return r;
+  if (logits_out) {
+    const int d = c->h_st->d;
+    CK(cudaMemcpyAsync(logits_out, c->vlogits, (size_t)(d + 1) * c->cfg.vocab * 4,
+                       cudaMemcpyDeviceToHost, c->stream));
+  }
+  return wait_stream(c);
+}
+
+ssd_status ssd_accept(ssd_ctx* c, int32_t* emitted_out, int32_t* n_out) {
+  if (!c) return SSD_ERR_INVALID_ARG;
+  if (c->phase != PH_VERIFIED) return fail(c, SSD_ERR_STATE, "accept without a verify");
+  ssd_status r = replay(c, c->g_accept);
+  if (r != SSD_OK) return r;
+  if ((r = read_state(c)) != SSD_OK) return r;
+  c->phase = PH_IDLE;
+  const int ne = c->h_st->n_emitted;
+  if (emitted_out)
+    for (int i = 0; i < ne; ++i) emitted_out[i] = c->h_st->emitted[i];
+  if (n_out) *n_out = ne;
+  return SSD_OK;
+}
+
+ssd_status ssd_generate(ssd_ctx* c, int32_t n_tokens, int32_t* out, ssd_stats* stats) {
+  if (!c || n_tokens < 0) return SSD_ERR_INVALID_ARG;
+  ssd_status r = ensure_policy(c);
+  if (r != SSD_OK) return r;
+  if (c->phase != PH_IDLE) return fail(c, SSD_ERR_STATE, "a round is in flight");
+  if (stats) memset(stats, 0, sizeof(*stats));
+  const int64_t l0 = c->launches;
+  if ((r = read_state(c)) != SSD_OK) return r;
+  const int n_start = c->h_st->n;
+  if (n_start + n_tokens + c->pol.d_max + 1 > c->cfg.max_seq)
+    return fail(c, SSD_ERR_CAPACITY, "n_tokens + d_max + 1 exceeds the KV capacity");
+  int got = 0;
+  while (got < n_tokens) {
+    if ((r = run_draft(c, stats)) != SSD_OK) return r;
+    const int d = c->pol.d_max == 0 ? 0 : c->h_st->d;
+    if ((r = run_verify(c, stats)) != SSD_OK) return r;
+    if ((r = replay(c, c->g_accept)) != SSD_OK) return r;
+    if ((r = read_state(c)) != SSD_OK) return r;
+    c->phase = PH_IDLE;
+    const int ne = c->h_st->n_emitted;
+    for (int i = 0; i < ne && got < n_tokens; ++i, ++got)
+      if (out) out[got] = c->h_st->emitted[i];
+    if (stats) {
+      stats->rounds++;
+      stats->drafted += d;
+      stats->accepted += c->h_st->accepted;
+      stats->emitted += ne;
+    }
+  }
+  if (c->h_st->n != n_start + n_tokens) {
+    const int32_t nn = n_start + n_tokens;
+    CK(cudaMemcpyAsync(&c->st->n, &nn, 4, cudaMemcpyHostToDevice, c->stream));
+    if ((r = read_state(c)) != SSD_OK) return r;
+  }
+  if (stats) stats->kernel_launches = c->launches - l0;
+  return SSD_OK;
+}
+
+ssd_status ssd_decode_ar(ssd_ctx* c, int32_t n_tokens, int32_t* out, ssd_stats* stats) {
+  if (!c || n_tokens < 0) return SSD_ERR_INVALID_ARG;
+  ssd_status r = ensure_policy(c);
+  if (r != SSD_OK) return r;
+  if (c->phase != PH_IDLE) return fail(c, SSD_ERR_STATE, "a round is in flight");
+  if (stats) memset(stats, 0, sizeof(*stats));
+  if ((r = read_state(c)) != SSD_OK) return r;
+  const int n0 = c->h_st->n;
+  if (n0 + n_tokens > c->cfg.max_seq) return fail(c, SSD_ERR_CAPACITY, "max_seq exceeded");
+  const int64_t l0 = c->launches;
+  for (int i = 0; i < n_tokens; ++i) {
+    if ((r = replay(c, c->g_ar)) != SSD_OK) return r;
+    if (stats) stats->bytes_streamed += pass_bytes(c, c->cfg.n_layers, true, n0 - 1 + i, 1);
+  }
+  if (out && n_tokens > 0) {
+    CK(cudaMemcpyAsync(c->h_tok, c->tokens + n0, (size_t)n_tokens * 4, cudaMemcpyDeviceToHost,
+                       c->stream));
+  }
+  if ((r = read_state(c)) != SSD_OK) return r;
+  if (out && n_tokens > 0) memcpy(out, c->h_tok, (size_t)n_tokens * 4);
+  if (stats) {
+    stats->rounds = n_tokens;
+    stats->emitted = n_tokens;
+    stats->kernel_launches = c->launches - l0;
+  }
+  return SSD_OK;
+}
+
+ssd_status ssd_rewind(ssd_ctx* c, int32_t n) {
+  if (!c) return SSD_ERR_INVALID_ARG;
+  if (c->phase == PH_NONE) return fail(c, SSD_ERR_STATE, "no prefill");
+  ssd_status r = read_state(c);
+  if (r != SSD_OK) return r;
+  if (n < 2 || n > c->h_st->n) return fail(c, SSD_ERR_INVALID_ARG, "rewind target out of range");
+  DevState* hs = c->h_st;
+  hs->n = n;
+  hs->j = hs->d = hs->stop = 0;
+  CK(cudaMemcpyAsync(c->st, hs, sizeof(DevState), cudaMemcpyHostToDevice, c->stream));
+  c->phase = PH_IDLE;
+  return wait_stream(c);
+}
+
+ssd_status ssd_get_tokens(ssd_ctx* c, int32_t* out, int32_t cap, int32_t* n_out) {
+  if (!c || !n_out) return SSD_ERR_INVALID_ARG;
+  ssd_status r = read_state(c);
+  if (r != SSD_OK) return r;
+  const int n = c->phase == PH_NONE ? 0 : c->h_st->n;
+  *n_out = n;
+  if (out && cap > 0 && n > 0) {
+    const int k = n < cap ? n : cap;
+    CK(cudaMemcpyAsync(c->h_tok, c->tokens, (size_t)k * 4, cudaMemcpyDeviceToHost, c->stream));
+    if ((r = wait_stream(c)) != SSD_OK) return r;
+    memcpy(out, c->h_tok, (size_t)k * 4);
+  }
+  return SSD_OK;
+}
+
+ssd_status ssd_profile_decode(ssd_ctx* c, int32_t n_steps, ssd_kernel_times* out) {
+  if (!c || !out || n_steps <= 0) return SSD_ERR_INVALID_ARG;
+  ssd_status r = ensure_policy(c);
+  if (r != SSD_OK) return r;
+  if (c->phase != PH_IDLE) return fail(c, SSD_ERR_STATE, "a round is in flight");
+  if ((r = read_state(c)) != SSD_OK) return r;
+  const int n0 = c->h_st->n;
+  if (n0 + n_steps > c->cfg.max_seq) return fail(c, SSD_ERR_CAPACITY, "max_seq exceeded");
+  memset(out, 0, sizeof(*out));
+  DevState saved = *c->h_st;
+  c->profiling = true;
+  c->prof_events.clear();
+  const ssd_config& g = c->cfg;
+  std::vector<double> kv_bytes;
+  for (int i = 0; i < n_steps; ++i) {
+    r = b_ar(c, c->stream);
+    if (r != SSD_OK) break;
+    // attention reads K/V of positions [0, pos] and writes one position per layer
+    kv_bytes.push_back(2.0 * 2.0 * g.n_kv_heads * g.head_dim * (double)(n0 + i + 1));
+  }
+  c->profiling = false;
+  if (r == SSD_OK) r = wait_stream(c);
+  const double w_qkv = 2.0 * qkv_rows(g) * g.d_model;
+  const double w_o = 2.0 * g.d_model * g.n_heads * g.head_dim;
+  const double w_gu = 2.0 * 2.0 * g.ffn_dim * g.d_model;
+  const double w_dn = 2.0 * g.d_model * g.ffn_dim;
+  const double w_lm = 2.0 * g.vocab * g.d_model;
+  int step = -1, layer_in_step = 0;
+  for (auto& pe : c->prof_events) {
+    const int cls = pe.first;
+    float ms = 0.f;
+    if (r == SSD_OK) cudaEventElapsedTime(&ms, pe.second.first, pe.second.second);
+    if (cls == 6 && layer_in_step == 0) step++;
+    out->ms[cls] += ms;
+    out->launches[cls]++;
+    double b = 0.0;
+    switch (cls) {
+      case 0: b = w_qkv; break;
+      case 1: b = step >= 0 && step < (int)kv_bytes.size() ? kv_bytes[step] : 0.0; break;
+      case 2: b = w_o; break;
+      case 3: b = w_gu; break;
+      case 4: b = w_dn; break;
+      case 5: b = w_lm; break;
+      default: b = 0.0;
+    }
+    out->bytes[cls] += b;
+    layer_in_step = (cls == 6) ? (layer_in_step ? 0 : 1) : layer_in_step;
+    cudaEventDestroy(pe.second.first);
+    cudaEventDestroy(pe.second.second);
+  }
+  c->prof_events.clear();
+  for (int k = 0; k < 8; ++k)
+    if (out->launches[k]) {
+      out->ms[k] /= (double)out->launches[k];
+      out->bytes[k] /= (double)out->launches[k];
+    }
+  if (r != SSD_OK) return r;
+  // restore the committed state
+  saved.j = saved.d = saved.stop = 0;
+  *c->h_st = saved;
+  CK(cudaMemcpyAsync(c->st, c->h_st, sizeof(DevState), cudaMemcpyHostToDevice, c->stream));
+  return wait_stream(c);
+}
+
+ssd_status ssd_set_timeout_ms(ssd_ctx* c, int32_t ms) {
+  if (!c || ms <= 0) return SSD_ERR_INVALID_ARG;
+  c->timeout_ms = ms;
+  return SSD_OK;
+}
+
+const char* ssd_last_error(const ssd_ctx* c) {
+  if (!c) {
+    snprintf(g_static_err, sizeof(g_static_err), "null context");
+    return g_static_err;
+  }
+  return c->err.c_str();
+}
+
+// Scoring lives in scoring.cu.
+
+}  // extern "C"

@@ -1,0 +1,29 @@
+"""Helpers for the GPU parity tests: seeded inputs on both sides."""
+
+import numpy as np
+import torch
+
+
+def rand_bf16(shape, seed, std=0.02):
+    """A seeded bf16 tensor on cuda:0 and its bit pattern (uint16) on the host."""
+    rng = np.random.default_rng(seed)
+    t = torch.from_numpy((rng.standard_normal(shape) * std).astype(np.float32)).to(torch.bfloat16)
+    bits = t.view(torch.int16).numpy().view(np.uint16).copy()
+    return t.cuda(), bits
+
+
+def rand_f32(shape, seed, std=1.0, mean=0.0):
+    rng = np.random.default_rng(seed)
+    a = (mean + rng.standard_normal(shape) * std).astype(np.float32)
+    return torch.from_numpy(a).cuda(), a.astype(np.float64)
+
+
+def bf16_values(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().to(torch.float64).numpy()
+
+
+def to_device_weights(wts):
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in wts.items()
+           if k != "layers"}
+    dev["layers"] = [{k: v.cuda() for k, v in lw.items()} for lw in wts["layers"]]
+    return dev

@@ -1,0 +1,245 @@
+"""End-to-end GPU tests through the context C-ABI.
+
+* The library's greedy self-speculative output is bit-identical to its own
+  autoregressive greedy output (no exclusions), for skip and exit policies,
+  MHA and GQA shapes, with and without the confidence stop.
+* GPU and oracle run the same seeded inputs independently and are compared
+  token by token and round by round until the oracle reports a near-tie
+  (top-1/top-2 logit gap <= 0.1, or a confidence within 1e-3 of tau), where
+  the two may legitimately diverge.  Logits must agree within 5e-2 and
+  confidences within 1e-3 on every compared row.
+"""
+
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+
+from synthetic import TINY, make_weights, weights_to_numpy, make_prompt, shrink
+from synthetic.configs import Policy, ModelShape, Workload
+from tests.gpu_util import to_device_weights
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ssd():
+    import __graft_entry__ as g
+    g.build()
+    import self_speculative_decoding_gb300 as m
+    return m
+
+
+SMALL_GQA = Workload(name="small-gqa", shape=ModelShape(
+    n_layers=6, d_model=512, n_heads=8, n_kv_heads=2, head_dim=64, ffn_dim=1408, vocab=2048),
+    scaled_layers=(2, 3), scale=0.1)
+MID = Workload(name="mid-dh128", shape=ModelShape(
+    n_layers=4, d_model=1024, n_heads=8, n_kv_heads=8, head_dim=128, ffn_dim=2816, vocab=4096),
+    scaled_layers=(1, 2), scale=0.1)
+
+CASES = [
+    (TINY, Policy(mode="skip", skip=(2,), d_max=4, tau=None)),
+    (TINY, Policy(mode="skip", skip=(2,), d_max=4, tau=0.5)),
+    (TINY, Policy(mode="skip", skip=(1, 2), d_max=7, tau=0.2)),
+    (TINY, Policy(mode="exit", exit_layer=1, d_max=12, tau=None)),
+    (TINY, Policy(mode="exit", exit_layer=3, d_max=3, tau=None)),
+    (TINY, Policy(mode="skip", skip=(), d_max=15, tau=None)),
+    (TINY, Policy(mode="skip", skip=(0,), d_max=1, tau=None)),
+    (SMALL_GQA, Policy(mode="skip", skip=(2, 3), d_max=8, tau=None)),
+    (SMALL_GQA, Policy(mode="exit", exit_layer=2, d_max=12, tau=None)),
+    (MID, Policy(mode="skip", skip=(1, 2), d_max=8, tau=0.1)),
+    (MID, Policy(mode="exit", exit_layer=0, d_max=6, tau=None)),
+]
+
+
+def _ctx(ssd, w, lm_head_scale=10.0, max_seq=256, seed_gains=True):
+    wts = make_weights(w, dtype="bf16", lm_head_scale=lm_head_scale, random_gains=seed_gains)
+    dev = to_device_weights(wts)
+    return ssd.SSDContext(w.shape, dev, max_seq=max_seq), wts
+
+
+@pytest.mark.parametrize("ci", range(len(CASES)))
+def test_greedy_ssd_is_bit_identical_to_ar(ssd, ci):
+    w, pol = CASES[ci]
+    ctx, _ = _ctx(ssd, w)
+    ctx.set_policy(pol)
+    prompt = make_prompt(w, 20)
+    f1 = ctx.prefill(prompt)
+    ar, _ = ctx.decode_ar(60)
+    f2 = ctx.prefill(prompt)
+    toks, stats = ctx.generate(60)
+    assert f1 == f2
+    assert toks == ar
+    assert stats["emitted"] >= 60 and stats["rounds"] >= 60 // (pol.d_max + 1)
+    assert ctx.tokens() == [int(t) for t in prompt] + [f1] + ar
+    ctx.close()
+
+
+def test_generation_continues_across_calls_and_rewind(ssd):
+    w, pol = CASES[0]
+    ctx, _ = _ctx(ssd, w)
+    ctx.set_policy(pol)
+    prompt = make_prompt(w, 20)
+    ctx.prefill(prompt)
+    full, _ = ctx.generate(40)
+    ctx.prefill(prompt)
+    a, _ = ctx.generate(13)
+    b, _ = ctx.generate(27)
+    assert a + b == full
+    n = len(ctx.tokens())
+    ctx.rewind(n - 10)
+    c, _ = ctx.generate(10)
+    assert c == full[-10:]
+    ctx.close()
+
+
+def _near_tie(z, thr=0.1):
+    s = np.sort(z)
+    return s[-1] - s[-2] <= thr
+
+
+def test_ar_greedy_matches_oracle(ssd):
+    from oracle import OracleModel, prefill, ar_generate
+    w = TINY
+    pol = Policy(mode="skip", skip=(2,), d_max=4, tau=None)
+    ctx, wts = _ctx(ssd, w, lm_head_scale=40.0)
+    ctx.set_policy(pol)
+    prompt = make_prompt(w)
+    first = ctx.prefill(prompt)
+    toks, _ = ctx.decode_ar(40)
+    m = OracleModel(w.shape, weights_to_numpy(wts))
+    st = prefill(m, prompt, pol, 128)
+    zs = [st.last_logits] + ar_generate(m, st, pol, 40)
+    ref = st.tokens[len(prompt):]
+    got = [first] + toks
+    compared = 0
+    for a, b, z in zip(got, ref, zs):
+        if _near_tie(z):
+            break
+        assert a == b
+        compared += 1
+    assert compared >= 8, compared
+    ctx.close()
+
+
+@pytest.mark.parametrize("w,pol", [
+    (TINY, Policy(mode="skip", skip=(2,), d_max=4, tau=None)),
+    (TINY, Policy(mode="skip", skip=(1, 2), d_max=5, tau=0.3)),
+    (SMALL_GQA, Policy(mode="exit", exit_layer=1, d_max=6, tau=None)),
+])
+def test_rounds_match_oracle_in_lockstep(ssd, w, pol):
+    from oracle import OracleModel, prefill, ssd_round
+    ctx, wts = _ctx(ssd, w, lm_head_scale=40.0)
+    ctx.set_policy(pol)
+    prompt = make_prompt(w)
+    first = ctx.prefill(prompt)
+    m = OracleModel(w.shape, weights_to_numpy(wts))
+    st = prefill(m, prompt, pol, 256)
+    if _near_tie(st.last_logits):
+        pytest.skip("near-tie at the first token")
+    assert first == st.tokens[-1]
+    rounds = 0
+    for _ in range(12):
+        drafts, confs = ctx.draft()
+        vlog = ctx.verify(d=len(drafts))
+        emitted = ctx.accept()
+        rec = ssd_round(m, st, pol)
+        # confidences of every draft step run (the stopping one included)
+        ref_conf = rec.conf + ([rec.stop_conf] if rec.stop_conf is not None else [])
+        for a, b in zip(confs, ref_conf):
+            assert abs(a - b) <= 1e-3
+        ties = any(_near_tie(z) for z in rec.draft_logits) or any(
+            pol.tau is not None and abs(c - pol.tau) <= 1e-3 for c in ref_conf)
+        if ties:
+            break
+        assert drafts == rec.draft
+        assert np.max(np.abs(vlog - rec.verify_logits)) <= 5e-2
+        if any(_near_tie(z) for z in rec.verify_logits[: rec.accepted + 1]):
+            break
+        assert emitted == rec.emitted
+        rounds += 1
+    assert rounds >= 2, rounds
+    ctx.close()
+
+
+def test_state_and_capacity_errors(ssd):
+    from self_speculative_decoding_gb300 import SSDError
+    w = TINY
+    ctx, _ = _ctx(ssd, w, max_seq=64)
+    with pytest.raises(SSDError, match="STATE"):
+        ctx.prefill([1, 2, 3])                      # no policy yet
+    with pytest.raises(SSDError, match="CAPACITY"):
+        ctx.set_policy(Policy(mode="skip", skip=(2,), d_max=16))
+    with pytest.raises(SSDError, match="INVALID_ARG"):
+        ctx.set_policy(Policy(mode="exit", exit_layer=9, d_max=4))
+    ctx.set_policy(Policy(mode="skip", skip=(2,), d_max=4))
+    with pytest.raises(SSDError, match="CAPACITY"):
+        ctx.prefill(list(range(64)))
+    with pytest.raises(SSDError, match="INVALID_ARG"):
+        ctx.prefill([5000])
+    ctx.prefill(list(range(10)))
+    with pytest.raises(SSDError, match="STATE"):
+        ctx.verify()
+    with pytest.raises(SSDError, match="STATE"):
+        ctx.accept()
+    ctx.draft()
+    with pytest.raises(SSDError, match="STATE"):
+        ctx.draft()
+    ctx.verify(want_logits=False)
+    ctx.accept()
+    with pytest.raises(SSDError, match="CAPACITY"):
+        ctx.generate(60)
+    ctx.close()
+
+
+def test_sampled_generation_follows_target_distribution(ssd):
+    # exit-mode drafting at T = 1 on a tiny vocabulary: the first emitted
+    # token of a round follows the full model's softmax (chi-square).
+    from scipy.stats import chisquare
+    from oracle import OracleModel, prefill
+    from oracle.model import softmax
+    w = Workload(name="tiny-v16", shape=ModelShape(n_layers=2, d_model=64, n_heads=1,
+                 n_kv_heads=1, head_dim=64, ffn_dim=128, vocab=16))
+    wts = make_weights(w, dtype="bf16", lm_head_scale=60.0, random_gains=True)
+    ctx = ssd.SSDContext(w.shape, to_device_weights(wts), max_seq=64)
+    prompt = make_prompt(w, 6)
+    m = OracleModel(w.shape, weights_to_numpy(wts))
+    p = softmax(prefill(m, prompt, Policy(), 64).last_logits)   # target after the prompt
+    ctx.set_policy(Policy(mode="exit", exit_layer=0, d_max=3, temperature=1.0, seed=7))
+    ctx.prefill(prompt)
+    counts = np.zeros(16)
+    n = 3000
+    for _ in range(n):
+        ctx.rewind(len(prompt))        # prompt[-1] pending again; the round counter moves on
+        ctx.draft()
+        ctx.verify(want_logits=False)
+        counts[ctx.accept()[0]] += 1
+    keep = p * n >= 5
+    exp = p[keep] * n
+    obs = counts[keep]
+    obs = obs * exp.sum() / obs.sum()
+    assert chisquare(obs, exp).pvalue > 1e-3
+    ctx.close()
+
+
+@pytest.mark.parametrize("literal_tau", [False, True])
+def test_llama7b_shape_ssd_equals_ar(ssd, literal_tau):
+    # the bench workload's shape and skip set, shortened: bit-identity at full size
+    from synthetic import LLAMA7B_SWIFT
+    w = LLAMA7B_SWIFT
+    pol = w.policy if literal_tau else replace(w.policy, tau=None)
+    wts = make_weights(w, device="cuda")
+    ctx = ssd.SSDContext(w.shape, wts, max_seq=512)
+    ctx.set_policy(pol)
+    prompt = make_prompt(w, 128)
+    f1 = ctx.prefill(prompt)
+    ar, _ = ctx.decode_ar(48)
+    f2 = ctx.prefill(prompt)
+    toks, stats = ctx.generate(48)
+    assert f1 == f2 and toks == ar
+    if not literal_tau:
+        assert stats["drafted"] > 0
+    ctx.close()
+    del wts
+    torch.cuda.empty_cache()
