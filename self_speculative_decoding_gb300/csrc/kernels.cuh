@@ -26,12 +26,15 @@ struct LinearArgs {
   float* xres = nullptr;      // EPI_RESID [M][R], read and written
   float* ss_out = nullptr;    // EPI_RESID [M][R/16]
   bf16* u = nullptr;          // EPI_SWIGLU [M][R]
+  // split-row-group combine scratch (see gemv_scratch); counters start at
+  // zero and are returned to zero by the kernel
+  float* part = nullptr;
+  unsigned* counter = nullptr;
+  float* rec = nullptr;       // EPI_LMHEAD summary records
   // EPI_LMHEAD
   float* logits = nullptr;    // [slot + M][R] (nullable)
   RowStats* stats = nullptr;  // [slot + M]
   const int32_t* slot_dev = nullptr;
-  float* part = nullptr;      // per-CTA partials [nCTA][16][8]
-  unsigned* counter = nullptr;
   float temperature = 0.f;
   uint64_t seed = 0;
   int round_static = 0;
@@ -41,18 +44,15 @@ struct LinearArgs {
   const int32_t* pos0_dev = nullptr;
 };
 
-struct GemvCfg {
-  int RG;  // 16-row groups per CTA
-  int KS;  // warps splitting K for each row group (RG * KS == 8)
+// Scratch one launch needs for a matrix of R rows and depth K (floats of
+// partial sums, counters, LM-head records).  Consecutive launches on one
+// stream may share the same scratch.
+struct GemvScratch {
+  size_t part_floats, counters, rec_floats;
 };
+GemvScratch gemv_scratch(int R, int K, int epi);
 
-// Launch shape for a matrix of `row_groups` 16-row groups and depth K.
-// Depends only on the shape, never on M.
-GemvCfg gemv_pick(int row_groups, int K, int epi);
-int gemv_grid(int row_groups, GemvCfg cfg, int epi);
-
-cudaError_t launch_gemv(int in_mode, int epi, const LinearArgs& a, GemvCfg cfg, cudaStream_t st,
-                        bool pdl);
+cudaError_t launch_gemv(int in_mode, int epi, const LinearArgs& a, cudaStream_t st, bool pdl);
 
 // Attention over the KV cache for the rows of a pass (see ssd_op_attention).
 struct AttnArgs {
@@ -70,6 +70,7 @@ struct AttnArgs {
   bf16* out = nullptr;         // [M][H dh]
   float* part = nullptr;       // [Hkv][max_seq/kAttnChunk][G*16][dh+2]
   unsigned* counters = nullptr;  // [Hkv]
+  int* err = nullptr;          // set to 1 if a bulk copy never completed
   float scale = 1.f;
 };
 

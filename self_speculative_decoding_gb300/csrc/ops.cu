@@ -48,6 +48,24 @@ struct Scratch {
   }
 };
 
+// Scratch for one GEMV launch (zeroed counters).
+struct GemvOpScratch {
+  Scratch part, cnt, rec;
+  explicit GemvOpScratch(cudaStream_t s) : part(s), cnt(s), rec(s) {}
+  ssd_status init(int R, int K, int epi, LinearArgs& a, cudaStream_t s) {
+    const GemvScratch gs = gemv_scratch(R, K, epi);
+    ssd_status r;
+    if ((r = cu(part.alloc(gs.part_floats * 4), "scratch")) != SSD_OK) return r;
+    if ((r = cu(cnt.alloc(gs.counters * 4), "scratch")) != SSD_OK) return r;
+    if ((r = cu(rec.alloc(gs.rec_floats ? gs.rec_floats * 4 : 16), "scratch")) != SSD_OK) return r;
+    if ((r = cu(cudaMemsetAsync(cnt.p, 0, gs.counters * 4, s), "memset")) != SSD_OK) return r;
+    a.part = (float*)part.p;
+    a.counter = (unsigned*)cnt.p;
+    a.rec = (float*)rec.p;
+    return SSD_OK;
+  }
+};
+
 }  // namespace
 
 extern "C" {
@@ -66,8 +84,9 @@ ssd_status ssd_op_linear(const void* W, int32_t R, int32_t K, const void* act, i
   a.act = (const bf16*)act;
   a.M_static = M;
   a.y = y;
-  return cu(launch_gemv(IN_BF16, EPI_STORE, a, gemv_pick(R / 16, K, EPI_STORE),
-                        (cudaStream_t)stream, false), "linear");
+  GemvOpScratch gs((cudaStream_t)stream);
+  if ((r = gs.init(R, K, EPI_STORE, a, (cudaStream_t)stream)) != SSD_OK) return r;
+  return cu(launch_gemv(IN_BF16, EPI_STORE, a, (cudaStream_t)stream, false), "linear");
 }
 
 ssd_status ssd_op_rmsnorm_linear(const void* W, int32_t R, int32_t K, const float* x,
@@ -90,8 +109,9 @@ ssd_status ssd_op_rmsnorm_linear(const void* W, int32_t R, int32_t K, const floa
   a.eps = eps;
   a.M_static = M;
   a.y = y;
-  return cu(launch_gemv(IN_NORM, EPI_STORE, a, gemv_pick(R / 16, K, EPI_STORE), s, false),
-            "rmsnorm_linear");
+  GemvOpScratch gs(s);
+  if ((r = gs.init(R, K, EPI_STORE, a, s)) != SSD_OK) return r;
+  return cu(launch_gemv(IN_NORM, EPI_STORE, a, s, false), "rmsnorm_linear");
 }
 
 ssd_status ssd_op_residual_linear(const void* W, int32_t R, int32_t K, const void* act, int32_t M,
@@ -110,8 +130,9 @@ ssd_status ssd_op_residual_linear(const void* W, int32_t R, int32_t K, const voi
   a.M_static = M;
   a.xres = x;
   a.ss_out = (float*)ss.p;
-  return cu(launch_gemv(IN_BF16, EPI_RESID, a, gemv_pick(R / 16, K, EPI_RESID), s, false),
-            "residual_linear");
+  GemvOpScratch gs(s);
+  if ((r = gs.init(R, K, EPI_RESID, a, s)) != SSD_OK) return r;
+  return cu(launch_gemv(IN_BF16, EPI_RESID, a, s, false), "residual_linear");
 }
 
 ssd_status ssd_op_swiglu(const void* Wg, const void* Wu, int32_t F, int32_t K, const float* x,
@@ -135,8 +156,9 @@ ssd_status ssd_op_swiglu(const void* Wg, const void* Wu, int32_t F, int32_t K, c
   a.eps = eps;
   a.M_static = M;
   a.u = (bf16*)u;
-  return cu(launch_gemv(IN_NORM, EPI_SWIGLU, a, gemv_pick(F / 16, K, EPI_SWIGLU), s, false),
-            "swiglu");
+  GemvOpScratch gs(s);
+  if ((r = gs.init(F, K, EPI_SWIGLU, a, s)) != SSD_OK) return r;
+  return cu(launch_gemv(IN_NORM, EPI_SWIGLU, a, s, false), "swiglu");
 }
 
 ssd_status ssd_op_attention(const float* qkv, int32_t M, int32_t pos0, void* k_cache,
@@ -150,12 +172,14 @@ ssd_status ssd_op_attention(const float* qkv, int32_t M, int32_t pos0, void* k_c
     return op_fail(SSD_ERR_INVALID_ARG, "attention pointers");
   cudaStream_t s = (cudaStream_t)stream;
   ssd_status r;
-  Scratch rope(s), part(s), cnt(s);
+  Scratch rope(s), part(s), cnt(s), err(s);
   const int half = dh / 2;
   if ((r = cu(rope.alloc((size_t)max_seq * half * sizeof(float2)), "scratch")) != SSD_OK) return r;
   if ((r = cu(part.alloc(attn_part_floats(Hkv, H, dh, max_seq) * 4), "scratch")) != SSD_OK) return r;
   if ((r = cu(cnt.alloc((size_t)Hkv * 4), "scratch")) != SSD_OK) return r;
+  if ((r = cu(err.alloc(4), "scratch")) != SSD_OK) return r;
   if ((r = cu(cudaMemsetAsync(cnt.p, 0, (size_t)Hkv * 4, s), "memset")) != SSD_OK) return r;
+  if ((r = cu(cudaMemsetAsync(err.p, 0, 4, s), "memset")) != SSD_OK) return r;
   if ((r = cu(launch_rope_table((float2*)rope.p, max_seq, half, (double)theta, s), "rope")) != SSD_OK)
     return r;
   AttnArgs a;
@@ -173,6 +197,7 @@ ssd_status ssd_op_attention(const float* qkv, int32_t M, int32_t pos0, void* k_c
   a.out = (bf16*)out;
   a.part = (float*)part.p;
   a.counters = (unsigned*)cnt.p;
+  a.err = (int*)err.p;
   a.scale = (float)(1.0 / std::sqrt((double)dh));
   if ((r = cu(attn_prepare(a), "attn_prepare")) != SSD_OK) return r;
   return cu(launch_attention(a, s, false), "attention");
@@ -188,13 +213,8 @@ ssd_status ssd_op_lm_head(const void* W, int32_t V, int32_t D, const float* x, c
       !(temperature >= 0.f))
     return op_fail(SSD_ERR_INVALID_ARG, "lm_head pointers / eps / temperature");
   cudaStream_t s = (cudaStream_t)stream;
-  const GemvCfg cfg = gemv_pick(V / 16, D, EPI_LMHEAD);
-  const int ctas = gemv_grid(V / 16, cfg, EPI_LMHEAD);
-  Scratch ss(s), part(s), cnt(s);
+  Scratch ss(s);
   if ((r = cu(ss.alloc((size_t)M * (D / kSsGroup) * 4), "scratch")) != SSD_OK) return r;
-  if ((r = cu(part.alloc((size_t)ctas * kMaxRows * 8 * 4), "scratch")) != SSD_OK) return r;
-  if ((r = cu(cnt.alloc(4), "scratch")) != SSD_OK) return r;
-  if ((r = cu(cudaMemsetAsync(cnt.p, 0, 4, s), "memset")) != SSD_OK) return r;
   if ((r = cu(launch_ss_partials(x, M, D, (float*)ss.p, s), "ss")) != SSD_OK) return r;
   LinearArgs a;
   a.W0 = (const bf16*)W;
@@ -207,14 +227,14 @@ ssd_status ssd_op_lm_head(const void* W, int32_t V, int32_t D, const float* x, c
   a.M_static = M;
   a.logits = logits;
   a.stats = (RowStats*)stats;
-  a.part = (float*)part.p;
-  a.counter = (unsigned*)cnt.p;
+  GemvOpScratch gs(s);
+  if ((r = gs.init(V, D, EPI_LMHEAD, a, s)) != SSD_OK) return r;
   a.temperature = temperature;
   a.seed = seed;
   a.round_static = round;
   a.sample_stream = stream_id;
   a.pos0_static = pos0;
-  return cu(launch_gemv(IN_NORM, EPI_LMHEAD, a, cfg, s, false), "lm_head");
+  return cu(launch_gemv(IN_NORM, EPI_LMHEAD, a, s, false), "lm_head");
 }
 
 ssd_status ssd_op_accept_stochastic(const float* P, const float* Q, const int32_t* drafts,

@@ -12,9 +12,11 @@
 //   AR step     : begin(ar) -> all layers -> LM head -> commit
 // The host reads back a few bytes per draft step (the confidence stop) and
 // per round (the emitted tokens).
+#include <algorithm>
 #include <chrono>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <thread>
@@ -71,8 +73,10 @@ struct ssd_ctx {
   float2* rope = nullptr;
   float* attn_part = nullptr;
   unsigned* attn_cnt = nullptr;
-  float* lm_part = nullptr;
-  unsigned* lm_cnt = nullptr;
+  int* attn_err = nullptr;
+  float* g_part = nullptr;      // GEMV split-row-group partials (shared by all GEMVs)
+  unsigned* g_cnt = nullptr;
+  float* g_rec = nullptr;
   RowStats* dstats = nullptr;
   RowStats* vstats = nullptr;
   float* dlogits = nullptr;
@@ -83,7 +87,6 @@ struct ssd_ctx {
   DevState* h_st = nullptr;  // pinned mirror
   int32_t* h_tok = nullptr;  // pinned staging [max_seq]
 
-  GemvCfg c_qkv{}, c_o{}, c_gu{}, c_dn{}, c_lm{};
   Graph g_draft, g_extra, g_verify, g_accept, g_ar;
 
   Phase phase = PH_NONE;
@@ -172,6 +175,12 @@ void prof_begin(ssd_ctx* c, int cls) {
   c->prof_events.push_back({cls, {a, b}});
 }
 
+void gemv_scratch_args(ssd_ctx* c, LinearArgs& a) {
+  a.part = c->g_part;
+  a.counter = c->g_cnt;
+  a.rec = c->g_rec;
+}
+
 ssd_status enq_layer(ssd_ctx* c, int l, cudaStream_t s) {
   const ssd_config& g = c->cfg;
   const ssd_layer_weights& w = c->layers[l];
@@ -187,8 +196,9 @@ ssd_status enq_layer(ssd_ctx* c, int l, cudaStream_t s) {
     a.eps = g.norm_eps;
     a.M_dev = &c->st->M;
     a.y = c->qkv;
+    gemv_scratch_args(c, a);
     prof_begin(c, 0);
-    if ((r = note(c, launch_gemv(IN_NORM, EPI_STORE, a, c->c_qkv, s, c->pdl), "qkv")) != SSD_OK)
+    if ((r = note(c, launch_gemv(IN_NORM, EPI_STORE, a, s, c->pdl), "qkv")) != SSD_OK)
       return r;
   }
   {
@@ -207,6 +217,7 @@ ssd_status enq_layer(ssd_ctx* c, int l, cudaStream_t s) {
     a.out = c->attn;
     a.part = c->attn_part;
     a.counters = c->attn_cnt;
+    a.err = c->attn_err;
     a.scale = (float)(1.0 / std::sqrt((double)g.head_dim));
     prof_begin(c, 1);
     if ((r = note(c, launch_attention(a, s, c->pdl), "attention")) != SSD_OK) return r;
@@ -220,8 +231,9 @@ ssd_status enq_layer(ssd_ctx* c, int l, cudaStream_t s) {
     a.M_dev = &c->st->M;
     a.xres = c->x;
     a.ss_out = c->ss;
+    gemv_scratch_args(c, a);
     prof_begin(c, 2);
-    if ((r = note(c, launch_gemv(IN_BF16, EPI_RESID, a, c->c_o, s, c->pdl), "o_proj")) != SSD_OK)
+    if ((r = note(c, launch_gemv(IN_BF16, EPI_RESID, a, s, c->pdl), "o_proj")) != SSD_OK)
       return r;
   }
   {
@@ -236,8 +248,9 @@ ssd_status enq_layer(ssd_ctx* c, int l, cudaStream_t s) {
     a.eps = g.norm_eps;
     a.M_dev = &c->st->M;
     a.u = c->u;
+    gemv_scratch_args(c, a);
     prof_begin(c, 3);
-    if ((r = note(c, launch_gemv(IN_NORM, EPI_SWIGLU, a, c->c_gu, s, c->pdl), "gate_up")) != SSD_OK)
+    if ((r = note(c, launch_gemv(IN_NORM, EPI_SWIGLU, a, s, c->pdl), "gate_up")) != SSD_OK)
       return r;
   }
   {
@@ -249,8 +262,9 @@ ssd_status enq_layer(ssd_ctx* c, int l, cudaStream_t s) {
     a.M_dev = &c->st->M;
     a.xres = c->x;
     a.ss_out = c->ss;
+    gemv_scratch_args(c, a);
     prof_begin(c, 4);
-    if ((r = note(c, launch_gemv(IN_BF16, EPI_RESID, a, c->c_dn, s, c->pdl), "down")) != SSD_OK)
+    if ((r = note(c, launch_gemv(IN_BF16, EPI_RESID, a, s, c->pdl), "down")) != SSD_OK)
       return r;
   }
   return SSD_OK;
@@ -279,15 +293,14 @@ ssd_status enq_lmhead(ssd_ctx* c, RowStats* stats, float* logits, const int32_t*
   a.logits = logits;
   a.stats = stats;
   a.slot_dev = slot_dev;
-  a.part = c->lm_part;
-  a.counter = c->lm_cnt;
+  gemv_scratch_args(c, a);
   a.temperature = sample_stream >= 0 ? c->pol.temperature : 0.f;
   a.seed = c->pol.seed;
   a.round_dev = &c->st->round;
   a.sample_stream = sample_stream < 0 ? 0 : sample_stream;
   a.pos0_dev = &c->st->pos0;
   prof_begin(c, 5);
-  return note(c, launch_gemv(IN_NORM, EPI_LMHEAD, a, c->c_lm, s, c->pdl), "lm_head");
+  return note(c, launch_gemv(IN_NORM, EPI_LMHEAD, a, s, c->pdl), "lm_head");
 }
 
 ssd_status enq_begin(ssd_ctx* c, int mode, cudaStream_t s, int M = 1, int pos0 = 0,
@@ -508,8 +521,19 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
   };
   const int D = g.d_model, F = g.ffn_dim, V = g.vocab;
   const int nr = kMaxRows;
-  const GemvCfg lmc = gemv_pick(V / 16, D, EPI_LMHEAD);
-  const int lm_ctas = gemv_grid(V / 16, lmc, EPI_LMHEAD);
+  // one scratch area serves every GEMV of the context (they run in stream order)
+  GemvScratch gs{0, 0, 0};
+  {
+    const GemvScratch all[5] = {gemv_scratch(qkv_rows(g), D, EPI_STORE),
+                                gemv_scratch(D, g.n_heads * g.head_dim, EPI_RESID),
+                                gemv_scratch(F, D, EPI_SWIGLU), gemv_scratch(D, F, EPI_RESID),
+                                gemv_scratch(V, D, EPI_LMHEAD)};
+    for (const GemvScratch& x : all) {
+      gs.part_floats = std::max(gs.part_floats, x.part_floats);
+      gs.counters = std::max(gs.counters, x.counters);
+      gs.rec_floats = std::max(gs.rec_floats, x.rec_floats);
+    }
+  }
   bool ok = alloc((void**)&c->kc, kv_elems(g) * sizeof(bf16)) &&
             alloc((void**)&c->vc, kv_elems(g) * sizeof(bf16)) &&
             alloc((void**)&c->x, (size_t)nr * D * 4) &&
@@ -523,8 +547,10 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
             alloc((void**)&c->attn_part,
                   attn_part_floats(g.n_kv_heads, g.n_heads, g.head_dim, g.max_seq) * 4) &&
             alloc((void**)&c->attn_cnt, (size_t)g.n_kv_heads * 4) &&
-            alloc((void**)&c->lm_part, (size_t)lm_ctas * kMaxRows * 8 * 4) &&
-            alloc((void**)&c->lm_cnt, 4) &&
+            alloc((void**)&c->attn_err, 4) &&
+            alloc((void**)&c->g_part, gs.part_floats * 4) &&
+            alloc((void**)&c->g_cnt, gs.counters * 4) &&
+            alloc((void**)&c->g_rec, gs.rec_floats * 4) &&
             alloc((void**)&c->dstats, (size_t)nr * sizeof(RowStats)) &&
             alloc((void**)&c->vstats, (size_t)nr * sizeof(RowStats)) &&
             alloc((void**)&c->dlogits, (size_t)nr * V * 4) &&
@@ -547,7 +573,8 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
   memset(c->h_st, 0, sizeof(DevState));
   cudaMemsetAsync(c->st, 0, sizeof(DevState), c->stream);
   cudaMemsetAsync(c->attn_cnt, 0, (size_t)g.n_kv_heads * 4, c->stream);
-  cudaMemsetAsync(c->lm_cnt, 0, 4, c->stream);
+  cudaMemsetAsync(c->g_cnt, 0, gs.counters * 4, c->stream);
+  cudaMemsetAsync(c->attn_err, 0, 4, c->stream);
   cudaMemsetAsync(c->tokens, 0, (size_t)g.max_seq * 4, c->stream);
   const int half = g.head_dim / 2;
   launch_rope_table(c->rope, g.max_seq, half, (double)g.rope_theta, c->stream);
@@ -556,13 +583,13 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
     probe.H = g.n_heads;
     probe.Hkv = g.n_kv_heads;
     probe.dh = g.head_dim;
-    attn_prepare(probe);
+    probe.max_seq = g.max_seq;
+    if (attn_prepare(probe) != cudaSuccess) {
+      cudaGetLastError();
+      ssd_destroy(c);
+      return SSD_ERR_INVALID_ARG;
+    }
   }
-  c->c_qkv = gemv_pick(qkv_rows(g) / 16, D, EPI_STORE);
-  c->c_o = gemv_pick(D / 16, g.n_heads * g.head_dim, EPI_RESID);
-  c->c_gu = gemv_pick(F / 16, D, EPI_SWIGLU);
-  c->c_dn = gemv_pick(D / 16, F, EPI_RESID);
-  c->c_lm = lmc;
   const cudaError_t e = cudaStreamSynchronize(c->stream);
   if (e != cudaSuccess) {
     ssd_destroy(c);
@@ -581,7 +608,7 @@ ssd_status ssd_destroy(ssd_ctx* c) {
   c->g_accept.reset();
   c->g_ar.reset();
   void* bufs[] = {c->kc, c->vc, c->x, c->ss, c->bx, c->bss, c->qkv, c->attn, c->u, c->rope,
-                  c->attn_part, c->attn_cnt, c->lm_part, c->lm_cnt, c->dstats, c->vstats,
+                  c->attn_part, c->attn_cnt, c->attn_err, c->g_part, c->g_cnt, c->g_rec, c->dstats, c->vstats,
                   c->dlogits, c->vlogits, c->tokens, c->toks_in, c->st};
   for (void* p : bufs)
     if (p) cudaFree(p);

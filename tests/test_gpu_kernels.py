@@ -134,8 +134,13 @@ def test_attention_matches_oracle(ops, H, Hkv, dh, pos0, M):
     assert _bf16_close(kg, Kr[:, pos0:pos0 + M], rel=1.0 / 128)
     # untouched cache stays untouched
     assert torch.equal(kc[:, :pos0].cpu(), kc0[:, :pos0])
+    # Outputs are bf16 on both sides and almost all bit-equal.  The rest
+    # differ because ~0.1% of the stored K values are one bf16 step apart
+    # (RoPE in fp32 on the GPU vs fp64 in the oracle), which moves a score by
+    # ~2^-9 |q_i k_i| and an output by a few bf16 steps at most.
+    assert np.mean(out != ref) < 0.02
     assert _bf16_close(out, ref, rel=1.0 / 32)
-    assert np.max(np.abs(out - ref)) < 3e-2
+    assert np.mean(np.abs(out - ref)) < 1e-4
 
 
 @pytest.mark.parametrize("H,Hkv,dh", [(32, 32, 128), (64, 8, 128), (4, 4, 64)])

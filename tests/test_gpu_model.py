@@ -123,14 +123,22 @@ def test_ar_greedy_matches_oracle(ssd):
     ctx.close()
 
 
-@pytest.mark.parametrize("w,pol", [
-    (TINY, Policy(mode="skip", skip=(2,), d_max=4, tau=None)),
-    (TINY, Policy(mode="skip", skip=(1, 2), d_max=5, tau=0.3)),
-    (SMALL_GQA, Policy(mode="exit", exit_layer=1, d_max=6, tau=None)),
+@pytest.mark.parametrize("w,pol,head", [
+    (TINY, Policy(mode="skip", skip=(2,), d_max=4, tau=None), 1.0),
+    (TINY, Policy(mode="skip", skip=(2,), d_max=4, tau=None), 10.0),
+    (TINY, Policy(mode="skip", skip=(1, 2), d_max=5, tau=0.15), 10.0),
+    (SMALL_GQA, Policy(mode="exit", exit_layer=1, d_max=6, tau=None), 1.0),
+    (SMALL_GQA, Policy(mode="exit", exit_layer=1, d_max=6, tau=None), 10.0),
 ])
-def test_rounds_match_oracle_in_lockstep(ssd, w, pol):
+def test_rounds_match_oracle_in_lockstep(ssd, w, pol, head):
+    # Tolerances: logits within 5e-2 and confidences within 1e-3 with the
+    # workloads' own LM head (head = 1).  GPU and oracle differ where a
+    # bf16-rounded activation lands on the other side of a rounding boundary;
+    # an LM head sharpened by `head` scales that logit deviation by `head`,
+    # and conf = exp(z1 - lse) moves by at most 2 conf max|dz|, so the
+    # confidence tolerance is scaled by `head` as well.
     from oracle import OracleModel, prefill, ssd_round
-    ctx, wts = _ctx(ssd, w, lm_head_scale=40.0)
+    ctx, wts = _ctx(ssd, w, lm_head_scale=head)
     ctx.set_policy(pol)
     prompt = make_prompt(w)
     first = ctx.prefill(prompt)
@@ -139,6 +147,7 @@ def test_rounds_match_oracle_in_lockstep(ssd, w, pol):
     if _near_tie(st.last_logits):
         pytest.skip("near-tie at the first token")
     assert first == st.tokens[-1]
+    conf_tol = 1e-3 * head
     rounds = 0
     for _ in range(12):
         drafts, confs = ctx.draft()
@@ -147,10 +156,15 @@ def test_rounds_match_oracle_in_lockstep(ssd, w, pol):
         rec = ssd_round(m, st, pol)
         # confidences of every draft step run (the stopping one included)
         ref_conf = rec.conf + ([rec.stop_conf] if rec.stop_conf is not None else [])
-        for a, b in zip(confs, ref_conf):
-            assert abs(a - b) <= 1e-3
-        ties = any(_near_tie(z) for z in rec.draft_logits) or any(
-            pol.tau is not None and abs(c - pol.tau) <= 1e-3 for c in ref_conf)
+        ties = False
+        for j, (a, b) in enumerate(zip(confs, ref_conf)):
+            assert abs(a - b) <= conf_tol
+            if pol.tau is not None and abs(b - pol.tau) <= conf_tol:
+                ties = True
+            if j < len(rec.draft_logits) and _near_tie(rec.draft_logits[j]):
+                ties = True
+            if ties:
+                break
         if ties:
             break
         assert drafts == rec.draft
@@ -159,7 +173,7 @@ def test_rounds_match_oracle_in_lockstep(ssd, w, pol):
             break
         assert emitted == rec.emitted
         rounds += 1
-    assert rounds >= 2, rounds
+    assert rounds >= (1 if head == 1.0 else 2), rounds
     ctx.close()
 
 
@@ -201,7 +215,7 @@ def test_sampled_generation_follows_target_distribution(ssd):
     from oracle.model import softmax
     w = Workload(name="tiny-v16", shape=ModelShape(n_layers=2, d_model=64, n_heads=1,
                  n_kv_heads=1, head_dim=64, ffn_dim=128, vocab=16))
-    wts = make_weights(w, dtype="bf16", lm_head_scale=60.0, random_gains=True)
+    wts = make_weights(w, dtype="bf16", lm_head_scale=4.0, random_gains=True)
     ctx = ssd.SSDContext(w.shape, to_device_weights(wts), max_seq=64)
     prompt = make_prompt(w, 6)
     m = OracleModel(w.shape, weights_to_numpy(wts))
@@ -216,9 +230,11 @@ def test_sampled_generation_follows_target_distribution(ssd):
         ctx.verify(want_logits=False)
         counts[ctx.accept()[0]] += 1
     keep = p * n >= 5
-    exp = p[keep] * n
-    obs = counts[keep]
-    obs = obs * exp.sum() / obs.sum()
+    assert keep.sum() >= 4                  # a spread target distribution
+    exp = np.append(p[keep] * n, p[~keep].sum() * n)
+    obs = np.append(counts[keep], counts[~keep].sum())
+    if exp[-1] == 0.0:
+        exp, obs = exp[:-1], obs[:-1]
     assert chisquare(obs, exp).pvalue > 1e-3
     ctx.close()
 
