@@ -70,21 +70,23 @@ typedef struct {
   int32_t max_score_rows; /* K*N capacity of ssd_score_masks (0: none)   */
 } ssd_config;
 
-/* Device pointers of one decoder layer (borrowed, row-major). */
+/* Device pointers of one decoder layer (borrowed).  Projection matrices
+ * are given in the packed layout written by ssd_pack_weight; the shapes
+ * below are those of the row-major matrices they were packed from. */
 typedef struct {
   const void* attn_norm; /* [D] fp32 RMSNorm gain                          */
-  const void* wqkv;      /* [(H + 2 Hkv) dh, D] bf16: q rows, k rows, v rows */
-  const void* wo;        /* [D, H dh] bf16                                 */
+  const void* wqkv;      /* packed [(H + 2 Hkv) dh, D] bf16: q, k, v rows  */
+  const void* wo;        /* packed [D, H dh] bf16                          */
   const void* mlp_norm;  /* [D] fp32                                       */
-  const void* w_gate;    /* [F, D] bf16                                    */
-  const void* w_up;      /* [F, D] bf16                                    */
-  const void* w_down;    /* [D, F] bf16                                    */
+  const void* w_gate;    /* packed [F, D] bf16                             */
+  const void* w_up;      /* packed [F, D] bf16                             */
+  const void* w_down;    /* packed [D, F] bf16                             */
 } ssd_layer_weights;
 
 typedef struct {
-  const void* tok_embed;  /* [V, D] bf16                                    */
+  const void* tok_embed;  /* [V, D] bf16, row-major (rows are gathered)     */
   const void* final_norm; /* [D] fp32                                       */
-  const void* lm_head;    /* [V, D] bf16 (shared by draft and verify)       */
+  const void* lm_head;    /* packed [V, D] bf16 (shared by draft and verify) */
   const ssd_layer_weights* layers; /* host array of n_layers entries; the
                                       table is copied by ssd_create       */
 } ssd_weights;
@@ -116,6 +118,17 @@ typedef struct {
   int64_t kernel_launches; /* library kernels launched (graph nodes counted) */
   double bytes_streamed;   /* algorithmic HBM bytes: weights + KV read/written */
 } ssd_stats;
+
+/* Converts a row-major bf16 matrix W [R][K] (device memory) into the
+ * library's packed layout at dst (device, R*K bf16, must not overlap src).
+ * The packed matrix is a sequence of units of 16 rows x 32 columns,
+ * row-group-major; inside a unit, element W[16 vr + 8 h + g][32 kb + 8 c + e]
+ * sits at unit offset h*256 + (4 g + c)*8 + e (h < 2, g < 8, c < 4, e < 8),
+ * which is the register fragment order of the tensor-core MMA, so each unit
+ * streams into shared memory with one bulk copy and every projection is one
+ * contiguous read.  Requires R % 16 == 0 and K % 32 == 0.  Enqueued on
+ * `stream`; returns without waiting.  Errors: INVALID_ARG, CUDA. */
+ssd_status ssd_pack_weight(const void* src, void* dst, int32_t R, int32_t K, void* stream);
 
 /* Creates a context for one model on one device (the current device).
  * stream: a cudaStream_t (NULL: the legacy default stream).  Validates the

@@ -8,8 +8,9 @@
  * inputs; the context API in ssd.h runs the same kernels.
  *
  * Common rules: M (rows, i.e. token positions processed together) is
- * 1..16; matrices are row-major bf16 with R % 16 == 0 and K % 32 == 0;
- * pointers are 16-byte aligned.  Calls that need scratch memory take it
+ * 1..16; weight matrices are bf16 in the packed layout of ssd_pack_weight
+ * (shapes are given as those of the row-major matrix, R % 16 == 0 and
+ * K % 32 == 0); pointers are 16-byte aligned.  Calls that need scratch memory take it
  * from the stream-ordered allocator (cudaMallocAsync) and free it on the
  * same stream.  Errors: SSD_ERR_INVALID_ARG for a bad size or pointer,
  * SSD_ERR_OOM, SSD_ERR_CUDA for a failed launch; the message is available

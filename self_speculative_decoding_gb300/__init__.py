@@ -20,7 +20,42 @@ from . import _abi
 from ._abi import (SSDError, SsdConfig, SsdLayerWeights, SsdPolicy, SsdRowStats, SsdStats,
                    SsdWeights, SSD_MODE_EXIT, SSD_MODE_SKIP)
 
-__all__ = ["SSDContext", "SSDError", "ops", "policy_struct", "stream_handle"]
+__all__ = ["SSDContext", "SSDError", "ops", "pack_weight", "pack_weights", "policy_struct",
+           "stream_handle"]
+
+MATRICES = ("wqkv", "wo", "w_gate", "w_up", "w_down")
+
+
+def pack_weight(W: torch.Tensor) -> torch.Tensor:
+    """Row-major bf16 [R, K] CUDA matrix -> the library's packed layout (a new
+    tensor of the same shape and size)."""
+    if W.dtype != torch.bfloat16 or W.dim() != 2:
+        raise ValueError("pack_weight expects a 2-D bf16 tensor")
+    out = torch.empty_like(W)
+    st = _lib().ssd_pack_weight(_ptr(W), _ptr(out), W.shape[0], W.shape[1], stream_handle())
+    if st != _abi.SSD_OK:
+        raise SSDError(st, _lib().ssd_ops_last_error().decode())
+    return out
+
+
+def pack_weights(wts: Dict, release: bool = False) -> Dict:
+    """A copy of a weight dict with every projection matrix packed.  With
+    ``release`` the row-major matrices are dropped from ``wts`` as they are
+    packed, so that peak memory is the model plus one matrix."""
+    out = {k: v for k, v in wts.items() if k not in ("layers", "lm_head")}
+    out["lm_head"] = pack_weight(wts["lm_head"])
+    if release:
+        wts["lm_head"] = None
+    out["layers"] = []
+    for lw in wts["layers"]:
+        nl = {k: v for k, v in lw.items() if k not in MATRICES}
+        for k in MATRICES:
+            nl[k] = pack_weight(lw[k])
+            if release:
+                lw[k] = None
+        out["layers"].append(nl)
+    out["packed"] = True
+    return out
 
 
 def _lib():
@@ -65,6 +100,8 @@ class SSDContext:
     def __init__(self, shape, weights: Dict, max_seq: int, max_draft: int = 15,
                  max_score_rows: int = 0, stream: Optional[torch.cuda.Stream] = None):
         self.shape = shape
+        if not weights.get("packed"):
+            raise ValueError("weights must be packed with pack_weights() first")
         self._weights = weights  # keep the tensors alive
         cfg = SsdConfig(shape.n_layers, shape.d_model, shape.n_heads, shape.n_kv_heads,
                         shape.head_dim, shape.ffn_dim, shape.vocab, shape.rope_theta,

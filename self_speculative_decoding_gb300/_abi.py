@@ -74,6 +74,7 @@ assert C.sizeof(SsdRowStats) == 48
 _P = C.c_void_p
 _I = C.c_int32
 _SIGS = {
+    "ssd_pack_weight": [_P, _P, _I, _I, _P],
     "ssd_create": [C.POINTER(SsdConfig), C.POINTER(SsdWeights), _P, C.POINTER(_P)],
     "ssd_destroy": [_P],
     "ssd_set_policy": [_P, C.POINTER(SsdPolicy)],

@@ -5,64 +5,66 @@
 // reading W once from HBM; the same kernel serves the M = d+1 verify pass
 // and the 16-row prefill chunks.
 //
-// Work partition.  W is cut into units of 16 rows x 32 columns (1 KB of
-// bf16).  Units are ordered row-group-major and split into equal contiguous
-// ranges, one per warp of a fixed grid of kGridCtas CTAs (two resident CTAs
-// on each of the 152 SMs), so every warp streams the same number of bytes
-// and all CTAs run in a single wave.  A 16-row group whose units span
-// several warps ("segments") is finished by the last of those warps to
-// complete: it sums the segments' partials in segment order and applies the
-// epilogue.  The partition depends only on the matrix shape.
+// Weight layout.  W is stored in "units" of 16 rows x 32 columns (1 KB),
+// row-group-major, each unit in tensor-core fragment order (see
+// ssd_pack_weight): the matrix is one contiguous stream and a unit is exactly
+// the A operand of two m16n8k16 MMAs for one warp.
 //
-// Tensor-core mapping.  One m16n8k16 MMA consumes 16 rows x 16 K of W against
-// 16 K x 8 token columns (M <= 8 uses one column tile, M <= 16 two).  The K
-// order inside each 32-wide block is permuted consistently for W and the
-// activations so that a lane's 16-byte load is exactly its A fragment for
-// two MMAs: lane (g, c) holds W[g][8c..8c+7] and W[g+8][8c..8c+7]; the first
-// MMA takes elements 0-3, the second 4-7.  Weights stream straight from HBM
-// into two register buffers (one in flight while the other feeds the MMAs);
-// activations are staged once per CTA in shared memory when they fit.
+// Data movement.  Each CTA owns an equal contiguous range of units (a fixed
+// grid of kGridCtas CTAs, two per SM, one wave).  A producer warp streams
+// the range into a ring of shared-memory slots with bulk (TMA) copies of up
+// to 8 units, completing on mbarriers; eight consumer warps take one unit
+// each per slot, read their fragments with conflict-free 16-byte shared loads
+// and run the MMAs.  Activations (the B operand: 8 or 16 token columns) are
+// read from global memory (L1-resident); the RMSNorm of the norm-fused input
+// is applied on the fly from the producer kernel's sum-of-squares partials.
 //
-// Reduction order.  Inside a segment each output accumulates its K blocks in
-// ascending order; segments are summed in order; nothing depends on M, so a
-// column's bits do not change with the number of rows processed together.
-// That is what makes self-speculative verification reproduce
-// autoregressive decoding bit for bit.
+// Reduction order.  A row group (16 outputs) whose units span several CTAs is
+// finished by the last CTA to complete it: each CTA first sums its eight
+// warps' partials in warp order, and the finishing CTA sums the CTAs'
+// partials in CTA order before the epilogue.  Each warp accumulates its units
+// in ascending K order.  The partition depends only on the matrix shape and
+// nothing depends on M, so a column's bits do not change with the number of
+// rows processed together — which is what makes self-speculative
+// verification reproduce autoregressive decoding bit for bit.
 #include "kernels.cuh"
 
 namespace ssd {
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kGridCtas = 304;                  // 2 resident CTAs x 152 SMs
-constexpr int kTotalWarps = kGridCtas * kWarps;
-constexpr int kUnroll = 4;                      // units per pipeline stage
-constexpr int kStageBytes = 88 * 1024;          // activation staging budget (2 CTAs/SM)
-constexpr int kPad = 8;                         // bf16 row padding in the stage
-constexpr int kLmBlock = 32;                    // LM-head row groups per level-2 block
+constexpr int kConsumers = 8;                    // consumer warps
+constexpr int kProducer = kConsumers;            // warp that issues the bulk copies
+constexpr int kEpilogue = kConsumers + 1;        // warp that finishes row groups
+constexpr int kThreads = (kConsumers + 2) * 32;
+constexpr int kGridCtas = 304;                   // 2 resident CTAs x 152 SMs
+constexpr int kChunk = 8;                        // units per ring slot
+constexpr int kSlots = 8;                        // ring depth
+constexpr int kUnitBytes = 1024;
+constexpr int kSlotBytes = kChunk * kUnitBytes;
+constexpr int kRingBytes = kSlots * kSlotBytes;
+constexpr int kLmBlock = 32;                     // LM-head row groups per level-2 block
 
 struct Part {
   long long T;  // units = NRG * KB
   int NRG;      // (virtual) 16-row groups
   int KB;       // 32-wide K blocks
-  int W;        // warps with work = min(kTotalWarps, T)
+  int C;        // CTAs with work = min(kGridCtas, T)
   int segmax;   // stride of the partial buffer per row group
 };
 
-__host__ __device__ inline long long unit_begin(const Part& p, int w) {
-  return (long long)w * p.T / p.W;
+__host__ __device__ inline long long unit_begin(const Part& p, int b) {
+  return (long long)b * p.T / p.C;
 }
-// first / last warp whose unit range intersects units [a, b)
-__host__ __device__ inline int warp_first(const Part& p, long long a) {
-  return (int)(((a + 1) * p.W + p.T - 1) / p.T) - 1;
+// first / last CTA whose unit range intersects units [a, b)
+__host__ __device__ inline int cta_first(const Part& p, long long a) {
+  return (int)(((a + 1) * p.C + p.T - 1) / p.T) - 1;
 }
-__host__ __device__ inline int warp_last(const Part& p, long long b) {
-  return (int)((b * p.W + p.T - 1) / p.T) - 1;
+__host__ __device__ inline int cta_last(const Part& p, long long b) {
+  return (int)((b * p.C + p.T - 1) / p.T) - 1;
 }
 __host__ __device__ inline int nseg(const Part& p, int vr) {
-  return warp_last(p, (long long)(vr + 1) * p.KB) - warp_first(p, (long long)vr * p.KB) + 1;
+  return cta_last(p, (long long)(vr + 1) * p.KB) - cta_first(p, (long long)vr * p.KB) + 1;
 }
 
 Part make_part(int R, int K, int epi) {
@@ -70,72 +72,73 @@ Part make_part(int R, int K, int epi) {
   p.NRG = (epi == EPI_SWIGLU ? 2 : 1) * (R / 16);
   p.KB = K / 32;
   p.T = (long long)p.NRG * p.KB;
-  p.W = (int)(p.T < kTotalWarps ? p.T : kTotalWarps);
-  p.segmax = (p.W + p.NRG - 1) / p.NRG + 1;
+  p.C = (int)(p.T < kGridCtas ? p.T : kGridCtas);
+  p.segmax = (p.C + p.NRG - 1) / p.NRG + 1;
   return p;
 }
 
-// B fragment (8 consecutive K of token t) for the permuted MMA layout,
-// read from global memory.
-template <int IN>
-SSD_DI uint4 load_b_global(const LinearArgs& a, int t, int off, const float* rstd) {
-  if (IN == IN_BF16) {
-    return *reinterpret_cast<const uint4*>(a.act + (size_t)t * a.K + off);
-  } else {
-    const float4* xp = reinterpret_cast<const float4*>(a.x + (size_t)t * a.K + off);
-    const float4* gp = reinterpret_cast<const float4*>(a.gain + off);
-    const float4 x0 = xp[0], x1 = xp[1], g0 = gp[0], g1 = gp[1];
-    const float r = rstd[t];
-    return make_uint4(pack_bf16x2(x0.x * r * g0.x, x0.y * r * g0.y),
-                      pack_bf16x2(x0.z * r * g0.z, x0.w * r * g0.w),
-                      pack_bf16x2(x1.x * r * g1.x, x1.y * r * g1.y),
-                      pack_bf16x2(x1.z * r * g1.z, x1.w * r * g1.w));
-  }
-}
-
-template <int IN, bool SMEM>
-SSD_DI uint4 load_b(const LinearArgs& a, const bf16* stage, int t, int off, bool valid,
-                    const float* rstd) {
-  if (!valid) return make_uint4(0u, 0u, 0u, 0u);
-  if (SMEM) return *reinterpret_cast<const uint4*>(stage + (size_t)t * (a.K + kPad) + off);
-  return load_b_global<IN>(a, t, off, rstd);
-}
-
-// Row pointer of unit u for lane (g, c): W[row0 + g][kb*32 + 8c].
+// Unit (vr, kb) in the packed stream of its matrix.
 template <int EPI>
-SSD_DI const bf16* unit_ptr(const LinearArgs& a, const Part& p, long long u, int g, int c) {
-  const int vr = (int)(u / p.KB);
-  const int kb = (int)(u - (long long)vr * p.KB);
-  const bf16* W = a.W0;
-  int row0 = vr * 16;
+SSD_DI const bf16* unit_src(const LinearArgs& a, const Part& p, int vr, int kb) {
   if (EPI == EPI_SWIGLU) {
-    W = (vr & 1) ? a.W1 : a.W0;
-    row0 = (vr >> 1) * 16;
+    const bf16* W = (vr & 1) ? a.W1 : a.W0;
+    return W + ((size_t)(vr >> 1) * p.KB + kb) * (kUnitBytes / 2);
   }
-  return W + (size_t)(row0 + g) * a.K + kb * 32 + 8 * c;
+  return a.W0 + ((size_t)vr * p.KB + kb) * (kUnitBytes / 2);
 }
 
-struct WBuf {
-  uint4 a[kUnroll], b[kUnroll];
+// Raw B operand (8 consecutive K of one token): loaded one chunk ahead so
+// that the global-memory latency is off the critical path.  For the
+// norm-fused input the RMSNorm is applied when the operand is used.
+template <int IN>
+struct BRaw {
+  uint4 v;
+};
+template <>
+struct BRaw<IN_NORM> {
+  float4 x0, x1, g0, g1;
 };
 
-template <int EPI>
-SSD_DI void load_w(WBuf& w, const LinearArgs& a, const Part& p, long long u, long long u1,
-                   int lane) {
-  const int g = lane >> 2, c = lane & 3;
-#pragma unroll
-  for (int i = 0; i < kUnroll; ++i) {
-    if (u + i < u1) {
-      const bf16* q = unit_ptr<EPI>(a, p, u + i, g, c);
-      w.a[i] = ld_stream_u4(q);
-      w.b[i] = ld_stream_u4(q + (size_t)8 * a.K);
+template <int IN>
+SSD_DI void b_issue(BRaw<IN>& r, const LinearArgs& a, int t, int off, bool valid) {
+  if (IN == IN_BF16) {
+    auto& q = reinterpret_cast<BRaw<IN_BF16>&>(r);
+    q.v = valid ? *reinterpret_cast<const uint4*>(a.act + (size_t)t * a.K + off)
+                : make_uint4(0u, 0u, 0u, 0u);
+  } else {
+    auto& q = reinterpret_cast<BRaw<IN_NORM>&>(r);
+    if (valid) {
+      const float4* xp = reinterpret_cast<const float4*>(a.x + (size_t)t * a.K + off);
+      const float4* gp = reinterpret_cast<const float4*>(a.gain + off);
+      q.x0 = xp[0]; q.x1 = xp[1]; q.g0 = gp[0]; q.g1 = gp[1];
+    } else {
+      q.x0 = q.x1 = q.g0 = q.g1 = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
 }
 
+template <int IN>
+SSD_DI uint4 b_finish(const BRaw<IN>& r, float rs) {
+  if (IN == IN_BF16) {
+    return reinterpret_cast<const BRaw<IN_BF16>&>(r).v;
+  } else {
+    const auto& q = reinterpret_cast<const BRaw<IN_NORM>&>(r);
+    return make_uint4(pack_bf16x2(q.x0.x * rs * q.g0.x, q.x0.y * rs * q.g0.y),
+                      pack_bf16x2(q.x0.z * rs * q.g0.z, q.x0.w * rs * q.g0.w),
+                      pack_bf16x2(q.x1.x * rs * q.g1.x, q.x1.y * rs * q.g1.y),
+                      pack_bf16x2(q.x1.z * rs * q.g1.z, q.x1.w * rs * q.g1.w));
+  }
+}
+
+SSD_DI void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory"); }
+
+SSD_DI void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 // ---------------------------------------------------------------- reductions
 
-// Warp-level top-2 merge under the (value desc, index asc) total order.
+// Top-2 merge under the (value desc, index asc) total order.
 SSD_DI void top2_insert(float v, int i, float& v1, int& i1, float& v2, int& i2) {
   if (better(v, i, v1, i1)) {
     v2 = v1; i2 = i1; v1 = v; i1 = i;
@@ -171,16 +174,17 @@ SSD_DI float sum_warp(float s) {
   return s;
 }
 
-// LM-head summary record of a set of vocabulary rows for one token:
-// {max z, argmax, second z, its id, sum exp(z - max), sum exp(z/T - max/T),
-//  best Gumbel score, its id}
+// LM-head summary of a set of vocabulary rows for one token: max z and its
+// id, second z and its id, sum exp(z - max), sum exp(z/T - max/T), best
+// Gumbel score and its id.
 struct LmRec {
   float v1, v2, se, set, gv;
   int i1, i2, gi;
 };
 
 SSD_DI void lm_store(float* p, const LmRec& r) {
-  reinterpret_cast<float4*>(p)[0] = make_float4(r.v1, __int_as_float(r.i1), r.v2, __int_as_float(r.i2));
+  reinterpret_cast<float4*>(p)[0] =
+      make_float4(r.v1, __int_as_float(r.i1), r.v2, __int_as_float(r.i2));
   reinterpret_cast<float4*>(p)[1] = make_float4(r.se, r.set, r.gv, __int_as_float(r.gi));
 }
 
@@ -201,8 +205,8 @@ SSD_DI LmRec lm_empty() {
   return r;
 }
 
-// Merge the per-lane records of a warp (a butterfly, identical in every lane).
-// Sums are rescaled to the merged maximum before being added.
+// Merge one record per lane (a butterfly, identical in every lane); the sums
+// are rescaled to the merged maximum before being added.
 SSD_DI LmRec lm_merge_warp(LmRec r, float T) {
   float v1 = r.v1, v2 = r.v2, gv = r.gv;
   int i1 = r.i1, i2 = r.i2, gi = r.gi;
@@ -219,295 +223,367 @@ SSD_DI LmRec lm_merge_warp(LmRec r, float T) {
   return o;
 }
 
+// ---------------------------------------------------------------- epilogues
+
+// Runs in one warp once row group vr (or the gate/up pair containing it) is
+// complete; ep[h][row][tok] holds the finished sums.
+template <int EPI>
+SSD_DI void epilogue(const LinearArgs& a, const Part& p, int vr, float (*ep)[16][17], int M,
+                     int lane) {
+  if (EPI == EPI_STORE) {
+    const int row0 = vr * 16;
+    for (int e = lane; e < 16 * M; e += 32) {
+      const int row = e / M, tok = e % M;
+      a.y[(size_t)tok * a.R + row0 + row] = ep[0][row][tok];
+    }
+  } else if (EPI == EPI_RESID) {
+    const int row0 = vr * 16;
+    for (int e = lane; e < 16 * M; e += 32) {
+      const int row = e / M, tok = e % M;
+      const size_t idx = (size_t)tok * a.R + row0 + row;
+      const float xn = a.xres[idx] + ep[0][row][tok];
+      a.xres[idx] = xn;
+      ep[0][row][tok] = xn;
+    }
+    __syncwarp();
+    if (lane < M) {
+      float s = 0.f;
+      for (int row = 0; row < 16; ++row) s += ep[0][row][lane] * ep[0][row][lane];
+      a.ss_out[(size_t)lane * (a.R / kSsGroup) + vr] = s;
+    }
+  } else if (EPI == EPI_SWIGLU) {
+    const int row0 = (vr >> 1) * 16;
+    for (int e = lane; e < 16 * M; e += 32) {
+      const int row = e / M, tok = e % M;
+      const float gt = ep[0][row][tok];
+      const float up = ep[1][row][tok];
+      const float sl = gt / (1.0f + expf(-gt));
+      a.u[(size_t)tok * a.R + row0 + row] = __float2bfloat16_rn(sl * up);
+    }
+  } else if (EPI == EPI_LMHEAD) {
+    const int slot = a.slot_dev ? *a.slot_dev : 0;
+    const int row0 = vr * 16;
+    const float T = a.temperature;
+    if (a.logits) {
+      for (int e = lane; e < 16 * M; e += 32) {
+        const int row = e / M, tok = e % M;
+        a.logits[(size_t)(slot + tok) * a.R + row0 + row] = ep[0][row][tok];
+      }
+    }
+    const int round = a.round_dev ? *a.round_dev : a.round_static;
+    const int pos0 = a.pos0_dev ? *a.pos0_dev : a.pos0_static;
+    // level 1: this group's 16 rows in order, one lane per token
+    if (lane < M) {
+      LmRec r = lm_empty();
+      for (int row = 0; row < 16; ++row) {
+        const float z = ep[0][row][lane];
+        top2_insert(z, row0 + row, r.v1, r.i1, r.v2, r.i2);
+        if (T > 0.f) {
+          const float sc =
+              z / T + gumbel_at(a.seed, row0 + row, pos0 + lane + 1, round, a.sample_stream);
+          if (better(sc, row0 + row, r.gv, r.gi)) { r.gv = sc; r.gi = row0 + row; }
+        }
+      }
+      for (int row = 0; row < 16; ++row) {
+        const float z = ep[0][row][lane];
+        r.se += expf(z - r.v1);
+        if (T > 0.f) r.set += expf(z / T - r.v1 / T);
+      }
+      lm_store(a.rec + ((size_t)vr * kMaxRows + lane) * 8, r);
+    }
+    __threadfence();
+    __syncwarp();
+    // level 2: blocks of kLmBlock consecutive groups
+    const int nb = (p.NRG + kLmBlock - 1) / kLmBlock;
+    const int blk = vr / kLmBlock;
+    const int blk_n = min(kLmBlock, p.NRG - blk * kLmBlock);
+    unsigned* c2 = a.counter + p.NRG;
+    int last2 = 0;
+    if (lane == 0) last2 = atomicAdd(c2 + blk, 1u) == (unsigned)(blk_n - 1);
+    last2 = __shfl_sync(0xffffffffu, last2, 0);
+    if (!last2) return;
+    __threadfence();
+    float* rec2 = a.rec + (size_t)p.NRG * kMaxRows * 8;
+    for (int tok = 0; tok < M; ++tok) {
+      const int gi = blk * kLmBlock + lane;
+      LmRec r = lane < blk_n ? lm_load(a.rec + ((size_t)gi * kMaxRows + tok) * 8) : lm_empty();
+      r = lm_merge_warp(r, T);
+      if (lane == 0) lm_store(rec2 + ((size_t)blk * kMaxRows + tok) * 8, r);
+    }
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) c2[blk] = 0u;
+    int last3 = 0;
+    if (lane == 0) last3 = atomicAdd(c2 + nb, 1u) == (unsigned)(nb - 1);
+    last3 = __shfl_sync(0xffffffffu, last3, 0);
+    if (!last3) return;
+    __threadfence();
+    // level 3: all blocks; lane b folds blocks b, b+32, ... in order
+    for (int tok = 0; tok < M; ++tok) {
+      LmRec r = lm_empty();
+      for (int b = lane; b < nb; b += 32) {
+        const LmRec q = lm_load(rec2 + ((size_t)b * kMaxRows + tok) * 8);
+        const float mx = fmaxf(r.v1, q.v1);
+        const float se =
+            (r.v1 == -INFINITY ? 0.f : r.se * expf(r.v1 - mx)) + q.se * expf(q.v1 - mx);
+        float set = 0.f;
+        if (T > 0.f)
+          set = (r.v1 == -INFINITY ? 0.f : r.set * expf(r.v1 / T - mx / T)) +
+                q.set * expf(q.v1 / T - mx / T);
+        top2_insert(q.v1, q.i1, r.v1, r.i1, r.v2, r.i2);
+        top2_insert(q.v2, q.i2, r.v1, r.i1, r.v2, r.i2);
+        if (better(q.gv, q.gi, r.gv, r.gi)) { r.gv = q.gv; r.gi = q.gi; }
+        r.se = se;
+        r.set = set;
+      }
+      r = lm_merge_warp(r, T);
+      if (lane == 0) {
+        RowStats rs;
+        rs.top1 = r.i1;
+        rs.top2 = r.i2;
+        rs.sample = T > 0.f ? r.gi : r.i1;
+        rs.pad = 0;
+        rs.z1 = r.v1;
+        rs.z2 = r.v2;
+        rs.lse = r.v1 + logf(r.se);
+        rs.conf = expf(r.v1 - rs.lse);
+        rs.lse_t = T > 0.f ? r.v1 / T + logf(r.set) : rs.lse;
+        rs.pad2[0] = rs.pad2[1] = rs.pad2[2] = 0.f;
+        a.stats[slot + tok] = rs;
+      }
+    }
+    if (lane == 0) c2[nb] = 0u;
+  }
+}
+
 // ---------------------------------------------------------------- kernel
+
+struct __align__(16) GemvSmem {
+  unsigned char ring[kRingBytes];
+  float red[2][kConsumers][16][16];  // per-warp partials, double-buffered per row group
+  float ep[2][16][17];               // epilogue operands
+  float rstd[kMaxRows];
+  uint64_t full[kSlots];             // slot filled by the bulk copy
+  uint64_t empty[kSlots];            // slot consumed by all consumer warps
+  uint64_t rfull[2];                 // partial buffer written by all consumer warps
+  uint64_t rempty[2];                // partial buffer read by the epilogue warp
+};
+
+// Length of the next chunk: at most kChunk units, never crossing a row group.
+SSD_DI int chunk_len(const Part& p, int kb, int left) {
+  return min(kChunk, min(p.KB - kb, left));
+}
 
 template <int IN, int EPI>
 __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(LinearArgs a, Part p) {
-  __shared__ float rstd_s[kMaxRows];
-  __shared__ float ep[kWarps][2][16][17];   // per-warp epilogue scratch
-  extern __shared__ __align__(16) unsigned char stage_raw[];
-  bf16* stage = reinterpret_cast<bf16*>(stage_raw);
-
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  GemvSmem& sm = *reinterpret_cast<GemvSmem*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, c = lane & 3;
-  const int w = blockIdx.x * kWarps + warp;
-  const bool has_work = w < p.W;
-  const long long u0 = has_work ? unit_begin(p, w) : 0;
-  const long long u1 = has_work ? unit_begin(p, w + 1) : 0;
+  const int b = blockIdx.x;
+  const long long U0 = unit_begin(p, b), U1 = unit_begin(p, b + 1);
 
-  // Weights do not depend on the preceding kernel: start streaming them
-  // before waiting for its results.
-  WBuf A, B;
-  if (has_work) load_w<EPI>(A, a, p, u0, u1, lane);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], kConsumers);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.rfull[s], kConsumers);
+      mbar_init(&sm.rempty[s], 1);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kProducer) {
+    // ---- producer: stream this CTA's units into the ring (weights do not
+    // depend on the preceding kernel, so no wait is needed here)
+    if (lane == 0) {
+      int vr = (int)(U0 / p.KB), kb = (int)(U0 % p.KB), left = (int)(U1 - U0);
+      int slot = 0;
+      uint32_t ph = 0;   // parity of the ring pass
+      for (int t = 0; left > 0; ++t) {
+        const int n = chunk_len(p, kb, left);
+        if (t >= kSlots && !mbar_wait(&sm.empty[slot], ph ^ 1u)) {
+          atomicExch(a.err, 2);
+          break;
+        }
+        mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)(n * kUnitBytes));
+        bulk_g2s(sm.ring + slot * kSlotBytes, unit_src<EPI>(a, p, vr, kb),
+                 (uint32_t)(n * kUnitBytes), &sm.full[slot]);
+        kb += n;
+        left -= n;
+        if (kb == p.KB) { kb = 0; ++vr; }
+        if (++slot == kSlots) { slot = 0; ph ^= 1u; }
+      }
+    }
+    return;
+  }
 
   pdl_wait();
   pdl_trigger();
-
   const int M = rows_of(a.M_static, a.M_dev);
+
+  if (warp == kEpilogue) {
+    // ---- epilogue warp: one flush per row-group segment of this CTA's range
+    int vr = (int)(U0 / p.KB), kb = (int)(U0 % p.KB), left = (int)(U1 - U0);
+    for (int fl = 0; left > 0; ++fl) {
+      const int gvr = vr;
+      left -= p.KB - kb < left ? p.KB - kb : left;
+      kb = 0;
+      ++vr;
+      const int buf = fl & 1;
+      if (!mbar_wait(&sm.rfull[buf], (fl >> 1) & 1)) {
+        if (lane == 0) atomicExch(a.err, 4);
+        return;
+      }
+      // this CTA's partial of the group: the consumer warps summed in order
+      const int seg = b - cta_first(p, (long long)gvr * p.KB);
+      float* dst = a.part + ((size_t)gvr * p.segmax + seg) * 256;
+      for (int e = lane; e < 16 * M; e += 32) {
+        const int row = e / M, tok = e % M;
+        float s2 = 0.f;
+        for (int w2 = 0; w2 < kConsumers; ++w2) s2 += sm.red[buf][w2][row][tok];
+        dst[row * 16 + tok] = s2;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.rempty[buf]);
+      __threadfence();
+      __syncwarp();
+      const int cidx = EPI == EPI_SWIGLU ? gvr >> 1 : gvr;
+      int last = 0;
+      if (lane == 0) {
+        int expect = nseg(p, gvr);
+        if (EPI == EPI_SWIGLU) expect += nseg(p, gvr ^ 1);
+        last = atomicAdd(a.counter + cidx, 1u) == (unsigned)(expect - 1);
+      }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (!last) continue;
+      __threadfence();
+      // sum the CTAs' partials of the group(s) in CTA order
+      const int ngrp = EPI == EPI_SWIGLU ? 2 : 1;
+      for (int h = 0; h < ngrp; ++h) {
+        const int gv = EPI == EPI_SWIGLU ? ((gvr & ~1) | h) : gvr;
+        const int ns = nseg(p, gv);
+        const float* src = a.part + (size_t)gv * p.segmax * 256;
+        for (int e = lane; e < 16 * M; e += 32) {
+          const int row = e / M, tok = e % M;
+          float s2 = 0.f;
+          for (int sg = 0; sg < ns; ++sg) s2 += __ldcg(src + (size_t)sg * 256 + row * 16 + tok);
+          sm.ep[h][row][tok] = s2;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) a.counter[cidx] = 0u;
+      epilogue<EPI>(a, p, gvr, sm.ep, M, lane);
+      __syncwarp();
+    }
+    return;
+  }
+
+  // ---- consumers
   if (IN == IN_NORM) {
     // 1 / sqrt(mean(x^2) + eps) per row from the producer's partials, in a
     // fixed order: lane l sums partials l, l+32, ... then a butterfly.
     const int NP = a.K / kSsGroup;
-    for (int m = warp; m < M; m += kWarps) {
-      float s = 0.f;
-      for (int q = lane; q < NP; q += 32) s += a.ss[(size_t)m * NP + q];
-      s = sum_warp(s);
-      if (lane == 0) rstd_s[m] = 1.0f / sqrtf(s / (float)a.K + a.eps);
+    for (int m = warp; m < M; m += kConsumers) {
+      float s2 = 0.f;
+      for (int q = lane; q < NP; q += 32) s2 += a.ss[(size_t)m * NP + q];
+      s2 = sum_warp(s2);
+      if (lane == 0) sm.rstd[m] = 1.0f / sqrtf(s2 / (float)a.K + a.eps);
     }
-    __syncthreads();
+    consumer_sync();
   }
-  const bool use_smem = (size_t)M * (a.K + kPad) * sizeof(bf16) <= (size_t)kStageBytes;
-  if (use_smem) {
-    const int vpr = a.K / 8;  // 16-byte pieces per row
-    for (int e = threadIdx.x; e < M * vpr; e += kThreads) {
-      const int m = e / vpr, q = e % vpr;
-      reinterpret_cast<uint4*>(stage + (size_t)m * (a.K + kPad))[q] =
-          load_b_global<IN>(a, m, q * 8, rstd_s);
-    }
-    __syncthreads();
-  }
-  if (!has_work) return;
-
+  const int g = lane >> 2, c = lane & 3;
   const bool two = M > 8;
   const bool v0 = g < M, v1 = two && (g + 8) < M;
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  int cur = (int)(u0 / p.KB);
+  const float rs0 = IN == IN_NORM && v0 ? sm.rstd[g] : 0.f;
+  const float rs1 = IN == IN_NORM && v1 ? sm.rstd[g + 8] : 0.f;
+  int vr = (int)(U0 / p.KB), kb = (int)(U0 % p.KB), left = (int)(U1 - U0);
+  int n = left > 0 ? chunk_len(p, kb, left) : 0;
+  BRaw<IN> ra, rb;
+  b_issue<IN>(ra, a, g, (kb + warp) * 32 + 8 * c, v0 && warp < n);
+  if (two) b_issue<IN>(rb, a, g + 8, (kb + warp) * 32 + 8 * c, v1 && warp < n);
+  int slot = 0;
+  uint32_t ph = 0;
+  int fl = 0;
+  while (left > 0) {
+    // position of the next chunk; its B operands are requested now
+    int kb2 = kb + n, vr2 = vr;
+    const int left2 = left - n;
+    if (kb2 == p.KB) { kb2 = 0; ++vr2; }
+    const int n2 = left2 > 0 ? chunk_len(p, kb2, left2) : 0;
+    BRaw<IN> na, nb;
+    b_issue<IN>(na, a, g, (kb2 + warp) * 32 + 8 * c, v0 && warp < n2);
+    if (two) b_issue<IN>(nb, a, g + 8, (kb2 + warp) * 32 + 8 * c, v1 && warp < n2);
 
-  // Flush the accumulators of row group `vr` into its segment slot; the last
-  // warp to finish the group (or the gate/up pair) runs the epilogue.
-  auto flush = [&](int vr) {
-    const int seg = w - warp_first(p, (long long)vr * p.KB);
-    float* dst = a.part + ((size_t)vr * p.segmax + seg) * 256;
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-      const int tok = t * 8 + 2 * c;
-      if (tok < M) {
-        dst[g * 16 + tok] = acc[t][0];
-        dst[(g + 8) * 16 + tok] = acc[t][2];
-      }
-      if (tok + 1 < M) {
-        dst[g * 16 + tok + 1] = acc[t][1];
-        dst[(g + 8) * 16 + tok + 1] = acc[t][3];
-      }
+    if (!mbar_wait(&sm.full[slot], ph)) {
+      if (lane == 0) atomicExch(a.err, 3);
+      return;
     }
-    __threadfence();
-    __syncwarp();
-    const int cidx = EPI == EPI_SWIGLU ? vr >> 1 : vr;
-    int last = 0;
-    if (lane == 0) {
-      int expect = nseg(p, vr);
-      if (EPI == EPI_SWIGLU) expect += nseg(p, vr ^ 1);
-      last = atomicAdd(a.counter + cidx, 1u) == (unsigned)(expect - 1);
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (!last) return;
-    __threadfence();
-    // sum the segments of the group(s) in segment order
-    const int ngrp = EPI == EPI_SWIGLU ? 2 : 1;
-    for (int h = 0; h < ngrp; ++h) {
-      const int gv = EPI == EPI_SWIGLU ? ((vr & ~1) | h) : vr;
-      const int ns = nseg(p, gv);
-      const float* src = a.part + (size_t)gv * p.segmax * 256;
-      for (int e = lane; e < 16 * M; e += 32) {
-        const int row = e / M, tok = e % M;
-        float s = 0.f;
-        for (int sg = 0; sg < ns; ++sg) s += __ldcg(src + (size_t)sg * 256 + row * 16 + tok);
-        ep[warp][h][row][tok] = s;
+    if (warp < n) {
+      const unsigned char* base = sm.ring + slot * kSlotBytes + warp * kUnitBytes;
+      const uint4 wa = *reinterpret_cast<const uint4*>(base + lane * 16);
+      const uint4 wb = *reinterpret_cast<const uint4*>(base + 512 + lane * 16);
+      const uint4 xa = b_finish<IN>(ra, rs0);
+      mma_bf16(acc[0], wa.x, wb.x, wa.y, wb.y, xa.x, xa.y);
+      mma_bf16(acc[0], wa.z, wb.z, wa.w, wb.w, xa.z, xa.w);
+      if (two) {
+        const uint4 xb = b_finish<IN>(rb, rs1);
+        mma_bf16(acc[1], wa.x, wb.x, wa.y, wb.y, xb.x, xb.y);
+        mma_bf16(acc[1], wa.z, wb.z, wa.w, wb.w, xb.z, xb.w);
       }
     }
     __syncwarp();
-    if (lane == 0) a.counter[cidx] = 0u;
-    if (EPI == EPI_STORE) {
-      const int row0 = vr * 16;
-      for (int e = lane; e < 16 * M; e += 32) {
-        const int row = e / M, tok = e % M;
-        a.y[(size_t)tok * a.R + row0 + row] = ep[warp][0][row][tok];
+    if (lane == 0) mbar_arrive(&sm.empty[slot]);
+    if (++slot == kSlots) { slot = 0; ph ^= 1u; }
+    const bool group_done = kb2 == 0 || left2 == 0;
+    vr = vr2;
+    kb = kb2;
+    left = left2;
+    n = n2;
+    ra = na;
+    if (two) rb = nb;
+    if (!group_done) continue;
+    // ---- the CTA's part of a row group is done: hand the accumulators to
+    // the epilogue warp through the double-buffered partial area
+    {
+      const int buf = fl & 1;
+      if (fl >= 2 && !mbar_wait(&sm.rempty[buf], ((fl >> 1) - 1) & 1)) {
+        if (lane == 0) atomicExch(a.err, 5);
+        return;
       }
-    } else if (EPI == EPI_RESID) {
-      const int row0 = vr * 16;
-      for (int e = lane; e < 16 * M; e += 32) {
-        const int row = e / M, tok = e % M;
-        const size_t idx = (size_t)tok * a.R + row0 + row;
-        const float xn = a.xres[idx] + ep[warp][0][row][tok];
-        a.xres[idx] = xn;
-        ep[warp][0][row][tok] = xn;
-      }
-      __syncwarp();
-      if (lane < M) {
-        float s = 0.f;
-        for (int row = 0; row < 16; ++row) s += ep[warp][0][row][lane] * ep[warp][0][row][lane];
-        a.ss_out[(size_t)lane * (a.R / kSsGroup) + vr] = s;
-      }
-    } else if (EPI == EPI_SWIGLU) {
-      const int row0 = (vr >> 1) * 16;
-      for (int e = lane; e < 16 * M; e += 32) {
-        const int row = e / M, tok = e % M;
-        const float gt = ep[warp][0][row][tok];
-        const float up = ep[warp][1][row][tok];
-        const float sl = gt / (1.0f + expf(-gt));
-        a.u[(size_t)tok * a.R + row0 + row] = __float2bfloat16_rn(sl * up);
-      }
-    } else if (EPI == EPI_LMHEAD) {
-      const int slot = a.slot_dev ? *a.slot_dev : 0;
-      const int row0 = vr * 16;
-      const float T = a.temperature;
-      if (a.logits) {
-        for (int e = lane; e < 16 * M; e += 32) {
-          const int row = e / M, tok = e % M;
-          a.logits[(size_t)(slot + tok) * a.R + row0 + row] = ep[warp][0][row][tok];
-        }
-      }
-      const int round = a.round_dev ? *a.round_dev : a.round_static;
-      const int pos0 = a.pos0_dev ? *a.pos0_dev : a.pos0_static;
-      // level 1: the group's 16 rows, sequentially, one lane per token
-      if (lane < M) {
-        LmRec r = lm_empty();
-        for (int row = 0; row < 16; ++row) {
-          const float z = ep[warp][0][row][lane];
-          top2_insert(z, row0 + row, r.v1, r.i1, r.v2, r.i2);
-          if (T > 0.f) {
-            const float sc = z / T + gumbel_at(a.seed, row0 + row, pos0 + lane + 1, round,
-                                               a.sample_stream);
-            if (better(sc, row0 + row, r.gv, r.gi)) { r.gv = sc; r.gi = row0 + row; }
-          }
-        }
-        for (int row = 0; row < 16; ++row) {
-          const float z = ep[warp][0][row][lane];
-          r.se += expf(z - r.v1);
-          if (T > 0.f) r.set += expf(z / T - r.v1 / T);
-        }
-        lm_store(a.rec + ((size_t)vr * kMaxRows + lane) * 8, r);
-      }
-      __threadfence();
-      __syncwarp();
-      // level 2: blocks of kLmBlock groups
-      const int nb = (p.NRG + kLmBlock - 1) / kLmBlock;
-      const int blk = vr / kLmBlock;
-      const int blk_n = min(kLmBlock, p.NRG - blk * kLmBlock);
-      unsigned* c2 = a.counter + p.NRG;
-      int last2 = 0;
-      if (lane == 0) last2 = atomicAdd(c2 + blk, 1u) == (unsigned)(blk_n - 1);
-      last2 = __shfl_sync(0xffffffffu, last2, 0);
-      if (!last2) return;
-      __threadfence();
-      float* rec2 = a.rec + (size_t)p.NRG * kMaxRows * 8;
-      for (int tok = 0; tok < M; ++tok) {
-        const int gi = blk * kLmBlock + lane;
-        LmRec r = lane < blk_n ? lm_load(a.rec + ((size_t)gi * kMaxRows + tok) * 8) : lm_empty();
-        r = lm_merge_warp(r, T);
-        if (lane == 0) lm_store(rec2 + ((size_t)blk * kMaxRows + tok) * 8, r);
-      }
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) c2[blk] = 0u;
-      int last3 = 0;
-      if (lane == 0) last3 = atomicAdd(c2 + nb, 1u) == (unsigned)(nb - 1);
-      last3 = __shfl_sync(0xffffffffu, last3, 0);
-      if (!last3) return;
-      __threadfence();
-      // level 3: all blocks; lane b takes blocks b, b+32, ... in order
-      for (int tok = 0; tok < M; ++tok) {
-        LmRec r = lm_empty();
-        for (int b = lane; b < nb; b += 32) {
-          const LmRec q = lm_load(rec2 + ((size_t)b * kMaxRows + tok) * 8);
-          const float mx = fmaxf(r.v1, q.v1);
-          const float se = (r.v1 == -INFINITY ? 0.f : r.se * expf(r.v1 - mx)) +
-                           q.se * expf(q.v1 - mx);
-          float set = 0.f;
-          if (T > 0.f)
-            set = (r.v1 == -INFINITY ? 0.f : r.set * expf(r.v1 / T - mx / T)) +
-                  q.set * expf(q.v1 / T - mx / T);
-          top2_insert(q.v1, q.i1, r.v1, r.i1, r.v2, r.i2);
-          top2_insert(q.v2, q.i2, r.v1, r.i1, r.v2, r.i2);
-          if (better(q.gv, q.gi, r.gv, r.gi)) { r.gv = q.gv; r.gi = q.gi; }
-          r.se = se;
-          r.set = set;
-        }
-        r = lm_merge_warp(r, T);
-        if (lane == 0) {
-          RowStats rs;
-          rs.top1 = r.i1;
-          rs.top2 = r.i2;
-          rs.sample = T > 0.f ? r.gi : r.i1;
-          rs.pad = 0;
-          rs.z1 = r.v1;
-          rs.z2 = r.v2;
-          rs.lse = r.v1 + logf(r.se);
-          rs.conf = expf(r.v1 - rs.lse);
-          rs.lse_t = T > 0.f ? r.v1 / T + logf(r.set) : rs.lse;
-          rs.pad2[0] = rs.pad2[1] = rs.pad2[2] = 0.f;
-          a.stats[slot + tok] = rs;
-        }
-      }
-      if (lane == 0) c2[nb] = 0u;
-    }
-  };
-
-  // Main loop over this warp's units: two register buffers in flight.
-  auto consume = [&](const WBuf& wb, long long u) {
 #pragma unroll
-    for (int i = 0; i < kUnroll; ++i) {
-      const long long uu = u + i;
-      if (uu < u1) {
-        const int vr = (int)(uu / p.KB);
-        if (vr != cur) {
-          flush(cur);
-#pragma unroll
-          for (int t = 0; t < 2; ++t)
-            acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-          cur = vr;
-        }
-        const int off = (int)(uu - (long long)vr * p.KB) * 32 + 8 * c;
-        if (use_smem) {
-          const uint4 xa = load_b<IN, true>(a, stage, g, off, v0, rstd_s);
-          mma_bf16(acc[0], wb.a[i].x, wb.b[i].x, wb.a[i].y, wb.b[i].y, xa.x, xa.y);
-          mma_bf16(acc[0], wb.a[i].z, wb.b[i].z, wb.a[i].w, wb.b[i].w, xa.z, xa.w);
-          if (two) {
-            const uint4 xb = load_b<IN, true>(a, stage, g + 8, off, v1, rstd_s);
-            mma_bf16(acc[1], wb.a[i].x, wb.b[i].x, wb.a[i].y, wb.b[i].y, xb.x, xb.y);
-            mma_bf16(acc[1], wb.a[i].z, wb.b[i].z, wb.a[i].w, wb.b[i].w, xb.z, xb.w);
-          }
-        } else {
-          const uint4 xa = load_b<IN, false>(a, stage, g, off, v0, rstd_s);
-          mma_bf16(acc[0], wb.a[i].x, wb.b[i].x, wb.a[i].y, wb.b[i].y, xa.x, xa.y);
-          mma_bf16(acc[0], wb.a[i].z, wb.b[i].z, wb.a[i].w, wb.b[i].w, xa.z, xa.w);
-          if (two) {
-            const uint4 xb = load_b<IN, false>(a, stage, g + 8, off, v1, rstd_s);
-            mma_bf16(acc[1], wb.a[i].x, wb.b[i].x, wb.a[i].y, wb.b[i].y, xb.x, xb.y);
-            mma_bf16(acc[1], wb.a[i].z, wb.b[i].z, wb.a[i].w, wb.b[i].w, xb.z, xb.w);
-          }
-        }
+      for (int h = 0; h < 2; ++h) {
+        const int tok = h * 8 + 2 * c;
+        sm.red[buf][warp][g][tok] = acc[h][0];
+        sm.red[buf][warp][g][tok + 1] = acc[h][1];
+        sm.red[buf][warp][g + 8][tok] = acc[h][2];
+        sm.red[buf][warp][g + 8][tok + 1] = acc[h][3];
+        acc[h][0] = acc[h][1] = acc[h][2] = acc[h][3] = 0.f;
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.rfull[buf]);
+      ++fl;
     }
-  };
-
-  long long u = u0;
-  while (u < u1) {
-    if (u + kUnroll < u1) load_w<EPI>(B, a, p, u + kUnroll, u1, lane);
-    consume(A, u);
-    u += kUnroll;
-    if (u >= u1) break;
-    if (u + kUnroll < u1) load_w<EPI>(A, a, p, u + kUnroll, u1, lane);
-    consume(B, u);
-    u += kUnroll;
   }
-  flush(cur);
 }
 
 template <int IN, int EPI>
 cudaError_t launch_one(const LinearArgs& a, const Part& p, cudaStream_t st, bool pdl) {
   static bool attr_set = false;
+  const int smem = (int)sizeof(GemvSmem) + 128;
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(gemv_kernel<IN, EPI>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               kStageBytes);
+    const cudaError_t e = cudaFuncSetAttribute(
+        gemv_kernel<IN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(kGridCtas);
+  lc.gridDim = dim3(p.C);
   lc.blockDim = dim3(kThreads);
-  lc.dynamicSmemBytes = kStageBytes;
+  lc.dynamicSmemBytes = smem;
   lc.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -515,6 +591,26 @@ cudaError_t launch_one(const LinearArgs& a, const Part& p, cudaStream_t st, bool
   lc.attrs = attr;
   lc.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&lc, gemv_kernel<IN, EPI>, a, p);
+}
+
+// Packs W [R][K] row-major into units of 16 rows x 32 columns in fragment
+// order: unit (vr, kb) = 512 bf16; half h (rows vr*16 + 8h .. + 7), lane
+// L = 4g + c holds W[vr*16 + 8h + g][kb*32 + 8c .. + 7] at [h*256 + 8L].
+__global__ void pack_kernel(const bf16* __restrict__ src, bf16* __restrict__ dst, int R, int K) {
+  const long long n = (long long)R * K / 8;  // 16-byte pieces
+  const int KB = K / 32;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long unit = i / 64;
+    const int within = (int)(i % 64);
+    const int h = within / 32, L = within % 32;
+    const int gg = L >> 2, cc = L & 3;
+    const long long vr = unit / KB;
+    const int kb = (int)(unit % KB);
+    const long long row = vr * 16 + 8 * h + gg;
+    reinterpret_cast<uint4*>(dst)[i] =
+        *reinterpret_cast<const uint4*>(src + row * K + (long long)kb * 32 + 8 * cc);
+  }
 }
 
 }  // namespace
@@ -540,6 +636,14 @@ cudaError_t launch_gemv(int in_mode, int epi, const LinearArgs& a, cudaStream_t 
   SSD_GEMV_CASE(IN_NORM, EPI_LMHEAD)
 #undef SSD_GEMV_CASE
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_pack(const bf16* src, bf16* dst, int R, int K, cudaStream_t st) {
+  const long long n = (long long)R * K / 8;
+  long long blocks = (n + 255) / 256;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  pack_kernel<<<(int)blocks, 256, 0, st>>>(src, dst, R, K);
+  return cudaGetLastError();
 }
 
 }  // namespace ssd

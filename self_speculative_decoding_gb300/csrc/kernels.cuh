@@ -31,6 +31,7 @@ struct LinearArgs {
   float* part = nullptr;
   unsigned* counter = nullptr;
   float* rec = nullptr;       // EPI_LMHEAD summary records
+  int* err = nullptr;         // set non-zero if a bulk copy never completed
   // EPI_LMHEAD
   float* logits = nullptr;    // [slot + M][R] (nullable)
   RowStats* stats = nullptr;  // [slot + M]
@@ -52,7 +53,11 @@ struct GemvScratch {
 };
 GemvScratch gemv_scratch(int R, int K, int epi);
 
+// W0 / W1 must be in the packed unit layout written by launch_pack.
 cudaError_t launch_gemv(int in_mode, int epi, const LinearArgs& a, cudaStream_t st, bool pdl);
+
+// Row-major W [R][K] -> packed 16x32 units in tensor-core fragment order.
+cudaError_t launch_pack(const bf16* src, bf16* dst, int R, int K, cudaStream_t st);
 
 // Attention over the KV cache for the rows of a pass (see ssd_op_attention).
 struct AttnArgs {

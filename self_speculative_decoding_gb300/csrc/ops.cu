@@ -50,18 +50,21 @@ struct Scratch {
 
 // Scratch for one GEMV launch (zeroed counters).
 struct GemvOpScratch {
-  Scratch part, cnt, rec;
-  explicit GemvOpScratch(cudaStream_t s) : part(s), cnt(s), rec(s) {}
+  Scratch part, cnt, rec, err;
+  explicit GemvOpScratch(cudaStream_t s) : part(s), cnt(s), rec(s), err(s) {}
   ssd_status init(int R, int K, int epi, LinearArgs& a, cudaStream_t s) {
     const GemvScratch gs = gemv_scratch(R, K, epi);
     ssd_status r;
     if ((r = cu(part.alloc(gs.part_floats * 4), "scratch")) != SSD_OK) return r;
     if ((r = cu(cnt.alloc(gs.counters * 4), "scratch")) != SSD_OK) return r;
     if ((r = cu(rec.alloc(gs.rec_floats ? gs.rec_floats * 4 : 16), "scratch")) != SSD_OK) return r;
+    if ((r = cu(err.alloc(16), "scratch")) != SSD_OK) return r;
     if ((r = cu(cudaMemsetAsync(cnt.p, 0, gs.counters * 4, s), "memset")) != SSD_OK) return r;
+    if ((r = cu(cudaMemsetAsync(err.p, 0, 16, s), "memset")) != SSD_OK) return r;
     a.part = (float*)part.p;
     a.counter = (unsigned*)cnt.p;
     a.rec = (float*)rec.p;
+    a.err = (int*)err.p;
     return SSD_OK;
   }
 };
@@ -71,6 +74,19 @@ struct GemvOpScratch {
 extern "C" {
 
 const char* ssd_ops_last_error(void) { return g_op_err.c_str(); }
+
+ssd_status ssd_pack_weight(const void* src, void* dst, int32_t R, int32_t K, void* stream) {
+  if (!al16(src) || !al16(dst) || src == dst)
+    return op_fail(SSD_ERR_INVALID_ARG, "pack: src / dst must be distinct, 16-byte aligned");
+  if (R <= 0 || R % 16 || K <= 0 || K % 32)
+    return op_fail(SSD_ERR_INVALID_ARG, "pack: R % 16 == 0 and K % 32 == 0 required");
+  const char* lo = (const char*)src;
+  const char* hi = (const char*)dst;
+  const size_t bytes = (size_t)R * K * 2;
+  if ((lo < hi && lo + bytes > hi) || (hi < lo && hi + bytes > lo))
+    return op_fail(SSD_ERR_INVALID_ARG, "pack: src and dst overlap");
+  return cu(launch_pack((const bf16*)src, (bf16*)dst, R, K, (cudaStream_t)stream), "pack");
+}
 
 ssd_status ssd_op_linear(const void* W, int32_t R, int32_t K, const void* act, int32_t M,
                          float* y, void* stream) {

@@ -179,6 +179,7 @@ void gemv_scratch_args(ssd_ctx* c, LinearArgs& a) {
   a.part = c->g_part;
   a.counter = c->g_cnt;
   a.rec = c->g_rec;
+  a.err = c->attn_err;
 }
 
 ssd_status enq_layer(ssd_ctx* c, int l, cudaStream_t s) {

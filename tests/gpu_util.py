@@ -23,7 +23,16 @@ def bf16_values(t: torch.Tensor) -> np.ndarray:
 
 
 def to_device_weights(wts):
+    """Device copies of a weight dict, projection matrices packed for the library."""
+    import self_speculative_decoding_gb300 as ssd
     dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in wts.items()
            if k != "layers"}
     dev["layers"] = [{k: v.cuda() for k, v in lw.items()} for lw in wts["layers"]]
-    return dev
+    return ssd.pack_weights(dev)
+
+
+def pack_reference(bits: np.ndarray) -> np.ndarray:
+    """The packed unit layout, written out with numpy index arithmetic."""
+    R, K = bits.shape
+    u = bits.reshape(R // 16, 2, 8, K // 32, 4, 8)        # vr, h, g, kb, c, e
+    return u.transpose(0, 3, 1, 2, 4, 5).reshape(R, K)      # vr, kb, h, g, c, e

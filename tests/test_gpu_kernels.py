@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 import torch
 
-from tests.gpu_util import rand_bf16, rand_f32, bf16_values
+from tests.gpu_util import rand_bf16, rand_f32, bf16_values, pack_reference
 
 pytestmark = pytest.mark.gpu
 
@@ -25,6 +25,19 @@ def ops():
     g.build()
     import self_speculative_decoding_gb300 as ssd
     return ssd.ops
+
+
+def P(W):
+    """Weights in the library's packed layout."""
+    import self_speculative_decoding_gb300 as ssd
+    return ssd.pack_weight(W)
+
+
+@pytest.mark.parametrize("R,K", [(16, 32), (48, 704), (4096, 11008)])
+def test_pack_layout(ops, R, K):
+    W, Wb = rand_bf16((R, K), seed=R + K)
+    got = P(W).cpu().view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(got, pack_reference(Wb))
 
 
 def _bf16_close(got, ref, rel=1.0 / 64):
@@ -41,7 +54,7 @@ def test_linear_matches_oracle(ops, R, K, M):
     from oracle import ops as O
     W, Wb = rand_bf16((R, K), seed=R * 7 + K)
     act, actb = rand_bf16((M, K), seed=M + 1000, std=1.0)
-    y = ops.linear(W, act).cpu().numpy()
+    y = ops.linear(P(W), act).cpu().numpy()
     ref = O.linear(Wb, bf16_values(act))
     np.testing.assert_allclose(y, ref, rtol=1e-4, atol=1e-4 * np.sqrt(K) * 0.02)
 
@@ -49,6 +62,7 @@ def test_linear_matches_oracle(ops, R, K, M):
 @pytest.mark.parametrize("R,K", [(48, 704), (1024, 4096), (4096, 11008)])
 def test_linear_column_invariance(ops, R, K):
     W, _ = rand_bf16((R, K), seed=3)
+    W = P(W)
     act, _ = rand_bf16((16, K), seed=4, std=1.0)
     full = ops.linear(W, act)
     for M in (1, 5, 8, 9, 13):
@@ -64,6 +78,7 @@ def test_linear_column_invariance(ops, R, K):
 def test_rmsnorm_linear_matches_oracle(ops, R, K, M):
     from oracle import ops as O
     W, Wb = rand_bf16((R, K), seed=11)
+    W = P(W)
     x, xd = rand_f32((M, K), seed=12, std=2.0)
     g, gd = rand_f32((K,), seed=13, std=0.1, mean=1.0)
     y = ops.rmsnorm_linear(W, x, g, 1e-5).cpu().numpy()
@@ -83,7 +98,7 @@ def test_residual_linear_matches_oracle(ops, R, K, M):
     W, Wb = rand_bf16((R, K), seed=21)
     act, _ = rand_bf16((M, K), seed=22, std=1.0)
     x, xd = rand_f32((M, R), seed=23)
-    out = ops.residual_linear(W, act, x.clone()).cpu().numpy()
+    out = ops.residual_linear(P(W), act, x.clone()).cpu().numpy()
     ref = xd + O.linear(Wb, bf16_values(act))
     np.testing.assert_allclose(out, ref, rtol=1e-4, atol=1e-4)
 
@@ -94,6 +109,7 @@ def test_swiglu_matches_oracle(ops, F, K, M):
     from oracle import ops as O
     Wg, Wgb = rand_bf16((F, K), seed=31)
     Wu, Wub = rand_bf16((F, K), seed=32)
+    Wg, Wu = P(Wg), P(Wu)
     x, xd = rand_f32((M, K), seed=33)
     g, gd = rand_f32((K,), seed=34, std=0.1, mean=1.0)
     u = bf16_values(ops.swiglu(Wg, Wu, x, g, 1e-5))
@@ -166,6 +182,7 @@ def test_lm_head_summary_matches_oracle(ops, V, D, M, T):
     from oracle import ops as O
     import self_speculative_decoding_gb300 as ssd
     W, Wb = rand_bf16((V, D), seed=41, std=0.02 * 10)
+    W = P(W)
     x, xd = rand_f32((M, D), seed=42)
     g, gd = rand_f32((D,), seed=43, std=0.1, mean=1.0)
     seed, rnd, pos0 = 1234, 3, 77

@@ -115,9 +115,9 @@ def test_ar_greedy_matches_oracle(ssd):
     got = [first] + toks
     compared = 0
     for a, b, z in zip(got, ref, zs):
-        if _near_tie(z):
+        if a != b:
+            assert _near_tie(z), f"token {compared} differs without a near-tie"
             break
-        assert a == b
         compared += 1
     assert compared >= 8, compared
     ctx.close()
@@ -134,9 +134,10 @@ def test_rounds_match_oracle_in_lockstep(ssd, w, pol, head):
     # Tolerances: logits within 5e-2 and confidences within 1e-3 with the
     # workloads' own LM head (head = 1).  GPU and oracle differ where a
     # bf16-rounded activation lands on the other side of a rounding boundary;
-    # an LM head sharpened by `head` scales that logit deviation by `head`,
-    # and conf = exp(z1 - lse) moves by at most 2 conf max|dz|, so the
-    # confidence tolerance is scaled by `head` as well.
+    # an LM head sharpened by `head` multiplies that logit deviation by
+    # `head` (measured: 0.003-0.006 at head 1, 0.03-0.06 at head 10), and
+    # conf = exp(z1 - lse) moves by at most 2 conf max|dz|, so both
+    # tolerances are multiplied by `head` for the sharpened parity models.
     from oracle import OracleModel, prefill, ssd_round
     ctx, wts = _ctx(ssd, w, lm_head_scale=head)
     ctx.set_policy(pol)
@@ -149,31 +150,37 @@ def test_rounds_match_oracle_in_lockstep(ssd, w, pol, head):
     assert first == st.tokens[-1]
     conf_tol = 1e-3 * head
     rounds = 0
+    checked = 0
     for _ in range(12):
         drafts, confs = ctx.draft()
         vlog = ctx.verify(d=len(drafts))
         emitted = ctx.accept()
         rec = ssd_round(m, st, pol)
-        # confidences of every draft step run (the stopping one included)
+        # confidences of every draft step run (the stopping one included),
+        # up to the first step whose draft token differs (later steps see
+        # different inputs)
         ref_conf = rec.conf + ([rec.stop_conf] if rec.stop_conf is not None else [])
-        ties = False
-        for j, (a, b) in enumerate(zip(confs, ref_conf)):
+        j = next(i for i in range(min(len(drafts), len(rec.draft)) + 1)
+                 if i >= len(drafts) or i >= len(rec.draft) or drafts[i] != rec.draft[i])
+        for a, b in list(zip(confs, ref_conf))[: j + 1]:
             assert abs(a - b) <= conf_tol
-            if pol.tau is not None and abs(b - pol.tau) <= conf_tol:
-                ties = True
-            if j < len(rec.draft_logits) and _near_tie(rec.draft_logits[j]):
-                ties = True
-            if ties:
-                break
-        if ties:
+            checked += 1
+        if drafts != rec.draft:
+            # a divergence is only allowed at a near-tie or a tau crossing
+            tie = (j < len(rec.draft_logits) and _near_tie(rec.draft_logits[j])) or (
+                pol.tau is not None and j < len(ref_conf) and abs(ref_conf[j] - pol.tau) <= conf_tol)
+            assert tie, f"drafts diverge at step {j} without a near-tie"
             break
-        assert drafts == rec.draft
-        assert np.max(np.abs(vlog - rec.verify_logits)) <= 5e-2
-        if any(_near_tie(z) for z in rec.verify_logits[: rec.accepted + 1]):
+        assert np.max(np.abs(vlog - rec.verify_logits)) <= 5e-2 * head
+        if emitted != rec.emitted:
+            j = next(i for i in range(len(emitted) + 1)
+                     if i >= len(emitted) or i >= len(rec.emitted) or emitted[i] != rec.emitted[i])
+            assert _near_tie(rec.verify_logits[min(j, len(rec.verify_logits) - 1)]), \
+                f"emitted tokens diverge at {j} without a near-tie"
             break
-        assert emitted == rec.emitted
         rounds += 1
-    assert rounds >= (1 if head == 1.0 else 2), rounds
+    assert checked >= 1
+    assert rounds >= (1 if head == 1.0 else 3), rounds
     ctx.close()
 
 
@@ -245,7 +252,7 @@ def test_llama7b_shape_ssd_equals_ar(ssd, literal_tau):
     from synthetic import LLAMA7B_SWIFT
     w = LLAMA7B_SWIFT
     pol = w.policy if literal_tau else replace(w.policy, tau=None)
-    wts = make_weights(w, device="cuda")
+    wts = ssd.pack_weights(make_weights(w, device="cuda"), release=True)
     ctx = ssd.SSDContext(w.shape, wts, max_seq=512)
     ctx.set_policy(pol)
     prompt = make_prompt(w, 128)
