@@ -70,5 +70,29 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     return LIB
 
 
+def build_variant(tag: str, flags) -> str:
+    """Builds a copy of the library with extra compile flags (tuning sweeps)
+    under _build/<tag>/; returns the path of its .so."""
+    out_dir = os.path.join(BUILD, tag)
+    os.makedirs(out_dir, exist_ok=True)
+    cc = nvcc()
+
+    def compile_one(src):
+        obj = os.path.join(out_dir, src[:-3] + ".o")
+        cmd = [cc, *ARCH, *FLAGS, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+        return obj
+
+    with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
+        objs = list(ex.map(compile_one, sources()))
+    lib = os.path.join(out_dir, "libssd.so")
+    r = subprocess.run([cc, *ARCH, "-shared", "-o", lib, *objs], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stderr}")
+    return lib
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose=True))

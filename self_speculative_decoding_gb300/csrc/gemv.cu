@@ -37,13 +37,28 @@ constexpr int kConsumers = 8;                    // consumer warps
 constexpr int kProducer = kConsumers;            // warp that issues the bulk copies
 constexpr int kEpilogue = kConsumers + 1;        // warp that finishes row groups
 constexpr int kThreads = (kConsumers + 2) * 32;
-constexpr int kGridCtas = 304;                   // 2 resident CTAs x 152 SMs
-constexpr int kChunk = 8;                        // units per ring slot
-constexpr int kSlots = 8;                        // ring depth
+#ifndef SSD_GEMV_CTAS
+#define SSD_GEMV_CTAS 304
+#endif
+#ifndef SSD_GEMV_CHUNK
+#define SSD_GEMV_CHUNK 8
+#endif
+#ifndef SSD_GEMV_SLOTS
+#define SSD_GEMV_SLOTS 5
+#endif
+constexpr int kGridCtas = SSD_GEMV_CTAS;         // 2 resident CTAs x 152 SMs
+constexpr int kChunk = SSD_GEMV_CHUNK;           // units per ring slot (<= kConsumers * k)
+constexpr int kSlots = SSD_GEMV_SLOTS;           // ring depth
+constexpr int kUPW = (kChunk + kConsumers - 1) / kConsumers;  // units per warp per chunk
 constexpr int kUnitBytes = 1024;
 constexpr int kSlotBytes = kChunk * kUnitBytes;
 constexpr int kRingBytes = kSlots * kSlotBytes;
 constexpr int kLmBlock = 32;                     // LM-head row groups per level-2 block
+// Activations (the B operand, bf16 and already normalised for the norm-fused
+// input) are staged once per CTA when M rows of K fit in this budget; this
+// covers every single-token pass of the 7B and 13B shapes.
+constexpr int kStageBytes = 52 * 1024;
+constexpr int kPad = 8;                          // bf16 row padding of the stage
 
 struct Part {
   long long T;  // units = NRG * KB
@@ -367,11 +382,119 @@ struct __align__(16) GemvSmem {
   uint64_t empty[kSlots];            // slot consumed by all consumer warps
   uint64_t rfull[2];                 // partial buffer written by all consumer warps
   uint64_t rempty[2];                // partial buffer read by the epilogue warp
+  __align__(16) bf16 stage[kStageBytes / 2];
 };
 
 // Length of the next chunk: at most kChunk units, never crossing a row group.
 SSD_DI int chunk_len(const Part& p, int kb, int left) {
   return min(kChunk, min(p.KB - kb, left));
+}
+
+// Consumer warps: take the ring's slots in order, one unit per warp per
+// slot, and hand each finished row-group segment to the epilogue warp.
+template <int IN, int EPI, bool STAGED>
+SSD_DI void consume(const LinearArgs& a, const Part& p, GemvSmem& sm, long long U0, long long U1,
+                    int M, int warp, int lane) {
+  const int g = lane >> 2, c = lane & 3;
+  const bool two = M > 8;
+  const bool v0 = g < M, v1 = two && (g + 8) < M;
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  const float rs0 = IN == IN_NORM && v0 && !STAGED ? sm.rstd[g] : 0.f;
+  const float rs1 = IN == IN_NORM && v1 && !STAGED ? sm.rstd[g + 8] : 0.f;
+  int vr = (int)(U0 / p.KB), kb = (int)(U0 % p.KB), left = (int)(U1 - U0);
+  int n = left > 0 ? chunk_len(p, kb, left) : 0;
+  BRaw<IN> ra[kUPW], rb[kUPW];
+  if (!STAGED) {
+#pragma unroll
+    for (int i = 0; i < kUPW; ++i) {
+      const int un = warp + i * kConsumers;
+      b_issue<IN>(ra[i], a, g, (kb + un) * 32 + 8 * c, v0 && un < n);
+      if (two) b_issue<IN>(rb[i], a, g + 8, (kb + un) * 32 + 8 * c, v1 && un < n);
+    }
+  }
+  int slot = 0;
+  uint32_t ph = 0;
+  int fl = 0;
+  while (left > 0) {
+    // position of the next chunk; its B operands are requested now
+    int kb2 = kb + n, vr2 = vr;
+    const int left2 = left - n;
+    if (kb2 == p.KB) { kb2 = 0; ++vr2; }
+    const int n2 = left2 > 0 ? chunk_len(p, kb2, left2) : 0;
+    BRaw<IN> na[kUPW], nb[kUPW];
+    if (!STAGED) {
+#pragma unroll
+      for (int i = 0; i < kUPW; ++i) {
+        const int un = warp + i * kConsumers;
+        b_issue<IN>(na[i], a, g, (kb2 + un) * 32 + 8 * c, v0 && un < n2);
+        if (two) b_issue<IN>(nb[i], a, g + 8, (kb2 + un) * 32 + 8 * c, v1 && un < n2);
+      }
+    }
+
+    if (!mbar_wait(&sm.full[slot], ph)) {
+      if (lane == 0) atomicExch(a.err, 3);
+      return;
+    }
+#pragma unroll
+    for (int i = 0; i < kUPW; ++i) {
+      const int un = warp + i * kConsumers;
+      if (un < n) {
+        const unsigned char* base = sm.ring + slot * kSlotBytes + un * kUnitBytes;
+        const uint4 wa = *reinterpret_cast<const uint4*>(base + lane * 16);
+        const uint4 wb = *reinterpret_cast<const uint4*>(base + 512 + lane * 16);
+        const int off = (kb + un) * 32 + 8 * c;
+        const uint4 xa = STAGED ? (v0 ? *reinterpret_cast<const uint4*>(sm.stage + (size_t)g * (a.K + kPad) + off)
+                                      : make_uint4(0u, 0u, 0u, 0u))
+                                : b_finish<IN>(ra[i], rs0);
+        mma_bf16(acc[0], wa.x, wb.x, wa.y, wb.y, xa.x, xa.y);
+        mma_bf16(acc[0], wa.z, wb.z, wa.w, wb.w, xa.z, xa.w);
+        if (two) {
+          const uint4 xb = STAGED ? (v1 ? *reinterpret_cast<const uint4*>(sm.stage + (size_t)(g + 8) * (a.K + kPad) + off)
+                                        : make_uint4(0u, 0u, 0u, 0u))
+                                  : b_finish<IN>(rb[i], rs1);
+          mma_bf16(acc[1], wa.x, wb.x, wa.y, wb.y, xb.x, xb.y);
+          mma_bf16(acc[1], wa.z, wb.z, wa.w, wb.w, xb.z, xb.w);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[slot]);
+    if (++slot == kSlots) { slot = 0; ph ^= 1u; }
+    const bool group_done = kb2 == 0 || left2 == 0;
+    vr = vr2;
+    kb = kb2;
+    left = left2;
+    n = n2;
+    if (!STAGED) {
+#pragma unroll
+      for (int i = 0; i < kUPW; ++i) {
+        ra[i] = na[i];
+        if (two) rb[i] = nb[i];
+      }
+    }
+    if (!group_done) continue;
+    // ---- the CTA's part of a row group is done: hand the accumulators to
+    // the epilogue warp through the double-buffered partial area
+    {
+      const int buf = fl & 1;
+      if (fl >= 2 && !mbar_wait(&sm.rempty[buf], ((fl >> 1) - 1) & 1)) {
+        if (lane == 0) atomicExch(a.err, 5);
+        return;
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int tok = h * 8 + 2 * c;
+        sm.red[buf][warp][g][tok] = acc[h][0];
+        sm.red[buf][warp][g][tok + 1] = acc[h][1];
+        sm.red[buf][warp][g + 8][tok] = acc[h][2];
+        sm.red[buf][warp][g + 8][tok + 1] = acc[h][3];
+        acc[h][0] = acc[h][1] = acc[h][2] = acc[h][3] = 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.rfull[buf]);
+      ++fl;
+    }
+  }
 }
 
 template <int IN, int EPI>
@@ -494,79 +617,20 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(LinearArgs a, Part p)
     }
     consumer_sync();
   }
-  const int g = lane >> 2, c = lane & 3;
-  const bool two = M > 8;
-  const bool v0 = g < M, v1 = two && (g + 8) < M;
-  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  const float rs0 = IN == IN_NORM && v0 ? sm.rstd[g] : 0.f;
-  const float rs1 = IN == IN_NORM && v1 ? sm.rstd[g + 8] : 0.f;
-  int vr = (int)(U0 / p.KB), kb = (int)(U0 % p.KB), left = (int)(U1 - U0);
-  int n = left > 0 ? chunk_len(p, kb, left) : 0;
-  BRaw<IN> ra, rb;
-  b_issue<IN>(ra, a, g, (kb + warp) * 32 + 8 * c, v0 && warp < n);
-  if (two) b_issue<IN>(rb, a, g + 8, (kb + warp) * 32 + 8 * c, v1 && warp < n);
-  int slot = 0;
-  uint32_t ph = 0;
-  int fl = 0;
-  while (left > 0) {
-    // position of the next chunk; its B operands are requested now
-    int kb2 = kb + n, vr2 = vr;
-    const int left2 = left - n;
-    if (kb2 == p.KB) { kb2 = 0; ++vr2; }
-    const int n2 = left2 > 0 ? chunk_len(p, kb2, left2) : 0;
-    BRaw<IN> na, nb;
-    b_issue<IN>(na, a, g, (kb2 + warp) * 32 + 8 * c, v0 && warp < n2);
-    if (two) b_issue<IN>(nb, a, g + 8, (kb2 + warp) * 32 + 8 * c, v1 && warp < n2);
-
-    if (!mbar_wait(&sm.full[slot], ph)) {
-      if (lane == 0) atomicExch(a.err, 3);
-      return;
+  const bool staged = (size_t)M * (a.K + kPad) * sizeof(bf16) <= (size_t)kStageBytes;
+  if (staged) {
+    const int vpr = a.K / 8;   // 16-byte pieces per row
+    for (int e = threadIdx.x; e < M * vpr; e += kConsumers * 32) {
+      const int m = e / vpr, q = e % vpr;
+      BRaw<IN> r;
+      b_issue<IN>(r, a, m, q * 8, true);
+      const float rs = IN == IN_NORM ? sm.rstd[m] : 0.f;
+      *reinterpret_cast<uint4*>(sm.stage + (size_t)m * (a.K + kPad) + q * 8) = b_finish<IN>(r, rs);
     }
-    if (warp < n) {
-      const unsigned char* base = sm.ring + slot * kSlotBytes + warp * kUnitBytes;
-      const uint4 wa = *reinterpret_cast<const uint4*>(base + lane * 16);
-      const uint4 wb = *reinterpret_cast<const uint4*>(base + 512 + lane * 16);
-      const uint4 xa = b_finish<IN>(ra, rs0);
-      mma_bf16(acc[0], wa.x, wb.x, wa.y, wb.y, xa.x, xa.y);
-      mma_bf16(acc[0], wa.z, wb.z, wa.w, wb.w, xa.z, xa.w);
-      if (two) {
-        const uint4 xb = b_finish<IN>(rb, rs1);
-        mma_bf16(acc[1], wa.x, wb.x, wa.y, wb.y, xb.x, xb.y);
-        mma_bf16(acc[1], wa.z, wb.z, wa.w, wb.w, xb.z, xb.w);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.empty[slot]);
-    if (++slot == kSlots) { slot = 0; ph ^= 1u; }
-    const bool group_done = kb2 == 0 || left2 == 0;
-    vr = vr2;
-    kb = kb2;
-    left = left2;
-    n = n2;
-    ra = na;
-    if (two) rb = nb;
-    if (!group_done) continue;
-    // ---- the CTA's part of a row group is done: hand the accumulators to
-    // the epilogue warp through the double-buffered partial area
-    {
-      const int buf = fl & 1;
-      if (fl >= 2 && !mbar_wait(&sm.rempty[buf], ((fl >> 1) - 1) & 1)) {
-        if (lane == 0) atomicExch(a.err, 5);
-        return;
-      }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int tok = h * 8 + 2 * c;
-        sm.red[buf][warp][g][tok] = acc[h][0];
-        sm.red[buf][warp][g][tok + 1] = acc[h][1];
-        sm.red[buf][warp][g + 8][tok] = acc[h][2];
-        sm.red[buf][warp][g + 8][tok + 1] = acc[h][3];
-        acc[h][0] = acc[h][1] = acc[h][2] = acc[h][3] = 0.f;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.rfull[buf]);
-      ++fl;
-    }
+    consumer_sync();
+    consume<IN, EPI, true>(a, p, sm, U0, U1, M, warp, lane);
+  } else {
+    consume<IN, EPI, false>(a, p, sm, U0, U1, M, warp, lane);
   }
 }
 
