@@ -89,19 +89,29 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(AttnArgs a) {
     const int n_old = max(0, min(p_end, pos0) - p_begin);
     bf16* kc = a.kc + kvh * head_stride;
     bf16* vc = a.vc + kvh * head_stride;
+    bf16* kc2 = a.kc2 ? a.kc2 + (size_t)kvh * a.scratch_len * dh : nullptr;
+    bf16* vc2 = a.vc2 ? a.vc2 + (size_t)kvh * a.scratch_len * dh : nullptr;
+    // row of position pos in the shared cache or in the scratch cache
+    auto krow = [&](int pos) { return pos < a.split ? kc + (size_t)pos * dh : kc2 + (size_t)(pos - a.split) * dh; };
+    auto vrow = [&](int pos) { return pos < a.split ? vc + (size_t)pos * dh : vc2 + (size_t)(pos - a.split) * dh; };
 
-    // (1) cached keys/values of the chunk: bulk copies (one per padded K
-    // row, one for the contiguous V rows), issued by warp 0
+    // (1) cached keys/values of the chunk: bulk copies issued by warp 0 (one
+    // per padded K row; V rows in one copy unless the chunk straddles the
+    // scratch split)
     if (n_old > 0 && warp == 0) {
+      const bool one_v = p_begin + n_old <= a.split || p_begin >= a.split;
       if (lane == 0) {
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(&bar, (uint32_t)(2 * n_old * dh * sizeof(bf16)));
-        bulk_g2s(sm.V, vc + (size_t)p_begin * dh, (uint32_t)(n_old * dh * sizeof(bf16)), &bar);
+        if (one_v)
+          bulk_g2s(sm.V, vrow(p_begin), (uint32_t)(n_old * dh * sizeof(bf16)), &bar);
       }
       __syncwarp();
-      for (int j = lane; j < n_old; j += 32)
-        bulk_g2s(sm.K + (size_t)j * krs, kc + (size_t)(p_begin + j) * dh,
-                 (uint32_t)(dh * sizeof(bf16)), &bar);
+      for (int j = lane; j < n_old; j += 32) {
+        bulk_g2s(sm.K + (size_t)j * krs, krow(p_begin + j), (uint32_t)(dh * sizeof(bf16)), &bar);
+        if (!one_v)
+          bulk_g2s(sm.V + (size_t)j * dh, vrow(p_begin + j), (uint32_t)(dh * sizeof(bf16)), &bar);
+      }
     }
     // (2) new keys of this chunk: RoPE, bf16, append to the cache
     const int first_new = max(p_begin, pos0);
@@ -120,10 +130,12 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(AttnArgs a) {
       sm.K[j * krs + i + half] = kb1;
       sm.V[j * dh + i] = vb0;
       sm.V[j * dh + i + half] = vb1;
-      kc[(size_t)pos * dh + i] = kb0;
-      kc[(size_t)pos * dh + i + half] = kb1;
-      vc[(size_t)pos * dh + i] = vb0;
-      vc[(size_t)pos * dh + i + half] = vb1;
+      bf16* kd = krow(pos);
+      bf16* vd = vrow(pos);
+      kd[i] = kb0;
+      kd[i + half] = kb1;
+      vd[i] = vb0;
+      vd[i + half] = vb1;
     }
     // (3) queries of the group, RoPE'd, fp32; row r = gh * 16 + m
     for (int e = tid; e < R * half; e += kThreads) {

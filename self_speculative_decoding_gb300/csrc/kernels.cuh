@@ -77,6 +77,14 @@ struct AttnArgs {
   unsigned* counters = nullptr;  // [Hkv]
   int* err = nullptr;          // set to 1 if a bulk copy never completed
   float scale = 1.f;
+  // Positions >= split live in a second (scratch) cache kc2 / vc2
+  // [Hkv][scratch_len][dh] at index pos - split; split >= max_seq disables it.
+  // Candidate-mask scoring uses it so that window K/V never touch the shared
+  // cache.
+  bf16* kc2 = nullptr;
+  bf16* vc2 = nullptr;
+  int split = 1 << 30;
+  int scratch_len = 0;
 };
 
 int attn_grid(const AttnArgs& a);
@@ -140,6 +148,10 @@ struct AcceptArgs {
   int32_t* n_emitted = nullptr;
 };
 cudaError_t launch_accept_stochastic(const AcceptArgs& a, cudaStream_t s, bool pdl);
+
+// matches[0] += #{m < M : stats[m].top1 == targets[m]} (M from the state).
+cudaError_t launch_match_count(const RowStats* stats, const int32_t* targets, const int32_t* M_dev,
+                               int32_t* matches, cudaStream_t s);
 
 cudaError_t launch_philox(const uint32_t* ctr, int count, uint64_t key, uint32_t* out,
                           cudaStream_t s);

@@ -83,6 +83,14 @@ struct ssd_ctx {
   float* vlogits = nullptr;
   int32_t* tokens = nullptr;
   int32_t* toks_in = nullptr;
+  // candidate-mask scoring: scratch K/V for the window positions and counters
+  bf16* sc_k = nullptr;
+  bf16* sc_v = nullptr;
+  int sc_len = 0;           // window capacity (positions)
+  int sc_split = -1;        // >= 0 while scoring: first window position
+  RowStats* sc_stats = nullptr;
+  int32_t* sc_counts = nullptr;
+  int32_t* h_counts = nullptr;
   DevState* st = nullptr;
   DevState* h_st = nullptr;  // pinned mirror
   int32_t* h_tok = nullptr;  // pinned staging [max_seq]
@@ -219,6 +227,12 @@ ssd_status enq_layer(ssd_ctx* c, int l, cudaStream_t s) {
     a.part = c->attn_part;
     a.counters = c->attn_cnt;
     a.err = c->attn_err;
+    if (c->sc_split >= 0) {
+      a.kc2 = c->sc_k + (size_t)l * g.n_kv_heads * c->sc_len * g.head_dim;
+      a.vc2 = c->sc_v + (size_t)l * g.n_kv_heads * c->sc_len * g.head_dim;
+      a.split = c->sc_split;
+      a.scratch_len = c->sc_len;
+    }
     a.scale = (float)(1.0 / std::sqrt((double)g.head_dim));
     prof_begin(c, 1);
     if ((r = note(c, launch_attention(a, s, c->pdl), "attention")) != SSD_OK) return r;
@@ -559,6 +573,15 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
             alloc((void**)&c->tokens, (size_t)g.max_seq * 4) &&
             alloc((void**)&c->toks_in, (size_t)g.max_seq * 4) &&
             alloc((void**)&c->st, sizeof(DevState));
+  if (ok && g.max_score_rows > 0) {
+    int w = g.max_score_rows < 512 ? g.max_score_rows : 512;
+    c->sc_len = ((w + 63) / 64) * 64;
+    const size_t e = (size_t)g.n_layers * g.n_kv_heads * c->sc_len * g.head_dim;
+    ok = alloc((void**)&c->sc_k, e * sizeof(bf16)) && alloc((void**)&c->sc_v, e * sizeof(bf16)) &&
+         alloc((void**)&c->sc_stats, (size_t)kMaxRows * sizeof(RowStats)) &&
+         alloc((void**)&c->sc_counts, 256 * sizeof(int32_t)) &&
+         cudaMallocHost((void**)&c->h_counts, 256 * sizeof(int32_t)) == cudaSuccess;
+  }
   if (!ok) {
     ssd_destroy(c);
     return SSD_ERR_OOM;
@@ -613,6 +636,11 @@ ssd_status ssd_destroy(ssd_ctx* c) {
                   c->dlogits, c->vlogits, c->tokens, c->toks_in, c->st};
   for (void* p : bufs)
     if (p) cudaFree(p);
+  if (c->sc_k) cudaFree(c->sc_k);
+  if (c->sc_v) cudaFree(c->sc_v);
+  if (c->sc_stats) cudaFree(c->sc_stats);
+  if (c->sc_counts) cudaFree(c->sc_counts);
+  if (c->h_counts) cudaFreeHost(c->h_counts);
   if (c->h_st) cudaFreeHost(c->h_st);
   if (c->h_tok) cudaFreeHost(c->h_tok);
   if (c->cap) cudaStreamDestroy(c->cap);
@@ -901,6 +929,53 @@ const char* ssd_last_error(const ssd_ctx* c) {
   return c->err.c_str();
 }
 
-// Scoring lives in scoring.cu.
+ssd_status ssd_score_masks(ssd_ctx* c, const uint64_t* masks, int32_t K, int32_t N,
+                           float* matchness_out, int32_t* best_out) {
+  if (!c) return SSD_ERR_INVALID_ARG;
+  if (!masks || K < 1 || K > 256 || N < 1 || !matchness_out)
+    return fail(c, SSD_ERR_INVALID_ARG, "score_masks arguments");
+  ssd_status r = ensure_policy(c);
+  if (r != SSD_OK) return r;
+  if (c->phase != PH_IDLE) return fail(c, SSD_ERR_STATE, "a round is in flight");
+  if (c->sc_len == 0 || (int64_t)K * N > c->cfg.max_score_rows || N > c->sc_len)
+    return fail(c, SSD_ERR_CAPACITY, "K*N exceeds max_score_rows (or the scoring window)");
+  if ((r = read_state(c)) != SSD_OK) return r;
+  const int n = c->h_st->n;
+  if (N + 2 > n) return fail(c, SSD_ERR_CAPACITY, "window longer than the committed context");
+  const int L = c->cfg.n_layers;
+  // SWIFT §4.1.2: candidate k predicts the committed tokens t[n-N..n-1] from
+  // t[n-N-1..n-2]; positions >= split use the scratch cache, so the shared
+  // full-model cache is only read.
+  const int split = n - N - 1;
+  CK(cudaMemsetAsync(c->sc_counts, 0, (size_t)K * sizeof(int32_t), c->stream));
+  c->sc_split = split;
+  for (int k = 0; k < K && r == SSD_OK; ++k) {
+    std::vector<int> keep;
+    for (int l = 0; l < L; ++l)
+      if (!((masks[4 * k + (l >> 6)] >> (l & 63)) & 1ull)) keep.push_back(l);
+    for (int c0 = 0; c0 < N && r == SSD_OK; c0 += kMaxRows) {
+      const int M = N - c0 < kMaxRows ? N - c0 : kMaxRows;
+      if ((r = enq_begin(c, BEGIN_TOKENS, c->stream, M, split + c0, c->tokens + split + c0)) != SSD_OK)
+        break;
+      if ((r = enq_layers(c, keep, c->stream)) != SSD_OK) break;
+      if ((r = enq_lmhead(c, c->sc_stats, nullptr, nullptr, -1, c->stream)) != SSD_OK) break;
+      r = note(c, launch_match_count(c->sc_stats, c->tokens + split + 1 + c0, &c->st->M,
+                                     c->sc_counts + k, c->stream),
+               "match_count");
+    }
+  }
+  c->sc_split = -1;
+  if (r != SSD_OK) return r;
+  CK(cudaMemcpyAsync(c->h_counts, c->sc_counts, (size_t)K * sizeof(int32_t), cudaMemcpyDeviceToHost,
+                     c->stream));
+  if ((r = wait_stream(c)) != SSD_OK) return r;
+  int best = 0;
+  for (int k = 0; k < K; ++k) {
+    matchness_out[k] = (float)c->h_counts[k] / (float)N;
+    if (c->h_counts[k] > c->h_counts[best]) best = k;
+  }
+  if (best_out) *best_out = best;
+  return SSD_OK;
+}
 
 }  // extern "C"
