@@ -108,6 +108,23 @@ ssd_status ssd_op_philox(const uint32_t* ctr, int32_t count, uint64_t key, uint3
 /* Description of the most recent failed op call on this host thread. */
 const char* ssd_ops_last_error(void);
 
+/* ssd_op_linear for callers that cannot allocate device memory (the pages
+ * have no counterpart; this is a library convenience).  Same arguments,
+ * layout and result as ssd_op_linear, but the GEMV's scratch (partial sums of
+ * row groups split across CTAs, completion counters) comes from a fixed
+ * 1 MiB + 4.25 KiB array that the library reserves on every GPU that loads it,
+ * held until the process exits; no cudaMalloc, cudaFree or other allocating
+ * routine is called.  R must be <= 8192 (SSD_ERR_CAPACITY otherwise).
+ * The first call on a device looks up the array's device address with that
+ * device current; make that first call before any stream capture.  Every
+ * call on a device shares the one array and clears its counters on entry, so
+ * calls whose kernels overlap on the GPU (different streams, or different
+ * host threads) race and must be serialised by the caller.  Errors are
+ * described by ssd_op_linear_noalloc_last_error(). */
+ssd_status ssd_op_linear_noalloc(const void* W, int32_t R, int32_t K, const void* act, int32_t M,
+                                 float* y, void* stream);
+const char* ssd_op_linear_noalloc_last_error(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -100,6 +100,8 @@ _SIGS = {
     "ssd_op_accept_stochastic": [_P, _P, _P, _I, _I, C.c_float, C.c_uint64, _I, _I, _P, _P, _P],
     "ssd_op_philox": [_P, _I, C.c_uint64, _P, _P],
     "ssd_ops_last_error": [],
+    "ssd_op_linear_noalloc": [_P, _I, _I, _P, _I, _P, _P],
+    "ssd_op_linear_noalloc_last_error": [],
 }
 
 EXPORTED = tuple(_SIGS)
@@ -114,7 +116,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     for name, args in _SIGS.items():
         fn = getattr(lib, name)
         fn.argtypes = args
-        fn.restype = C.c_char_p if name in ("ssd_last_error", "ssd_ops_last_error") else C.c_int
+        fn.restype = C.c_char_p if name.endswith("last_error") else C.c_int
     return lib
 
 
