@@ -293,7 +293,7 @@ SSD_DI void epilogue(const LinearArgs& a, const Part& p, int vr, float (*ep)[16]
       for (int row = 0; row < 16; ++row) {
         const float z = ep[0][row][lane];
         top2_insert(z, row0 + row, r.v1, r.i1, r.v2, r.i2);
-        if (T > 0.f) {
+        if (T > 0.f && a.sample) {
           const float sc =
               z / T + gumbel_at(a.seed, row0 + row, pos0 + lane + 1, round, a.sample_stream);
           if (better(sc, row0 + row, r.gv, r.gi)) { r.gv = sc; r.gi = row0 + row; }
@@ -356,7 +356,7 @@ SSD_DI void epilogue(const LinearArgs& a, const Part& p, int vr, float (*ep)[16]
         RowStats rs;
         rs.top1 = r.i1;
         rs.top2 = r.i2;
-        rs.sample = T > 0.f ? r.gi : r.i1;
+        rs.sample = T > 0.f && a.sample ? r.gi : r.i1;
         rs.pad = 0;
         rs.z1 = r.v1;
         rs.z2 = r.v2;

@@ -36,7 +36,8 @@ struct LinearArgs {
   float* logits = nullptr;    // [slot + M][R] (nullable)
   RowStats* stats = nullptr;  // [slot + M]
   const int32_t* slot_dev = nullptr;
-  float temperature = 0.f;
+  float temperature = 0.f;    // > 0: the summary includes lse of z / T
+  int sample = 0;             // 1: also draw a Gumbel-max sample of softmax(z / T)
   uint64_t seed = 0;
   int round_static = 0;
   const int32_t* round_dev = nullptr;

@@ -246,6 +246,7 @@ ssd_status ssd_op_lm_head(const void* W, int32_t V, int32_t D, const float* x, c
   GemvOpScratch gs(s);
   if ((r = gs.init(V, D, EPI_LMHEAD, a, s)) != SSD_OK) return r;
   a.temperature = temperature;
+  a.sample = temperature > 0.f ? 1 : 0;
   a.seed = seed;
   a.round_static = round;
   a.sample_stream = stream_id;

@@ -309,7 +309,9 @@ ssd_status enq_lmhead(ssd_ctx* c, RowStats* stats, float* logits, const int32_t*
   a.stats = stats;
   a.slot_dev = slot_dev;
   gemv_scratch_args(c, a);
-  a.temperature = sample_stream >= 0 ? c->pol.temperature : 0.f;
+  // every pass reports lse(z / T); only draft, AR and prefill passes draw
+  a.temperature = c->pol.temperature;
+  a.sample = sample_stream >= 0 ? 1 : 0;
   a.seed = c->pol.seed;
   a.round_dev = &c->st->round;
   a.sample_stream = sample_stream < 0 ? 0 : sample_stream;

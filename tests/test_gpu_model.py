@@ -184,6 +184,62 @@ def test_rounds_match_oracle_in_lockstep(ssd, w, pol, head):
     ctx.close()
 
 
+@pytest.mark.parametrize("w,pol,head", [
+    (SMALL_GQA, Policy(mode="exit", exit_layer=1, d_max=6, temperature=0.6, seed=1234), 4.0),
+    (TINY, Policy(mode="skip", skip=(1, 2), d_max=4, temperature=0.6, seed=99), 4.0),
+])
+def test_sampled_rounds_match_oracle_in_lockstep(ssd, w, pol, head):
+    # T > 0: both sides draw the same Philox numbers, so drafts, acceptance
+    # decisions and emitted tokens agree wherever the decision is not within
+    # the tolerance of its boundary (Gumbel score gap > 0.1, |log u - log(p/q)|
+    # > 0.05); the first legitimate divergence ends the comparison.
+    from oracle import OracleModel, prefill, ssd_round
+    from oracle.philox import uniforms
+    from oracle import ops as O
+    ctx, wts = _ctx(ssd, w, lm_head_scale=head)
+    ctx.set_policy(pol)
+    prompt = make_prompt(w)
+    first = ctx.prefill(prompt)
+    m = OracleModel(w.shape, weights_to_numpy(wts))
+    st = prefill(m, prompt, pol, 256)
+    if first != st.tokens[-1]:
+        pytest.skip("first sampled token sits on a Gumbel near-tie")
+    T, seed = pol.temperature, pol.seed
+    V = w.shape.vocab
+
+    def gumbel_gap(z, pos, rnd, stream):
+        sc = np.sort(z / T - np.log(-np.log(uniforms(seed, pos, rnd, stream, V))))
+        return sc[-1] - sc[-2]
+
+    rounds = accepted_total = rejected_total = 0
+    for _ in range(16):
+        n, rnd = st.n, st.round + 1
+        drafts, _ = ctx.draft()
+        vlog = ctx.verify(d=len(drafts))
+        emitted = ctx.accept()
+        rec = ssd_round(m, st, pol)
+        if drafts != rec.draft:
+            j = next(i for i in range(len(rec.draft)) if drafts[i] != rec.draft[i])
+            assert gumbel_gap(rec.draft_logits[j], n + j, rnd, 0) <= 0.1, "draft sample differs"
+            break
+        assert np.max(np.abs(vlog - rec.verify_logits)) <= 5e-2 * head
+        Q = np.stack(rec.draft_logits) if rec.draft else np.zeros((0, V))
+        margins = O.accept_margins(rec.verify_logits, Q, rec.draft, T, seed, rnd, n)
+        k = 0
+        while k < min(len(margins), rec.accepted + 1) and margins[k] > 0.05:
+            k += 1
+        if k <= rec.accepted and k < len(margins):
+            break        # a decision within tolerance of its boundary
+        if O.resample_gap(rec.verify_logits, Q, rec.accepted, T, seed, rnd, n) <= 0.1:
+            break
+        assert emitted == rec.emitted
+        rounds += 1
+        accepted_total += rec.accepted
+        rejected_total += int(rec.accepted < rec.d)
+    assert rounds >= 2, rounds
+    ctx.close()
+
+
 def test_state_and_capacity_errors(ssd):
     from self_speculative_decoding_gb300 import SSDError
     w = TINY
@@ -214,9 +270,11 @@ def test_state_and_capacity_errors(ssd):
     ctx.close()
 
 
-def test_sampled_generation_follows_target_distribution(ssd):
-    # exit-mode drafting at T = 1 on a tiny vocabulary: the first emitted
-    # token of a round follows the full model's softmax (chi-square).
+@pytest.mark.parametrize("T", [1.0, 0.6])
+def test_sampled_generation_follows_target_distribution(ssd, T):
+    # exit-mode drafting at temperature T on a tiny vocabulary: the first
+    # emitted token of a round follows the full model's softmax(z / T)
+    # (chi-square).
     from scipy.stats import chisquare
     from oracle import OracleModel, prefill
     from oracle.model import softmax
@@ -226,8 +284,8 @@ def test_sampled_generation_follows_target_distribution(ssd):
     ctx = ssd.SSDContext(w.shape, to_device_weights(wts), max_seq=64)
     prompt = make_prompt(w, 6)
     m = OracleModel(w.shape, weights_to_numpy(wts))
-    p = softmax(prefill(m, prompt, Policy(), 64).last_logits)   # target after the prompt
-    ctx.set_policy(Policy(mode="exit", exit_layer=0, d_max=3, temperature=1.0, seed=7))
+    p = softmax(prefill(m, prompt, Policy(), 64).last_logits / T)   # target after the prompt
+    ctx.set_policy(Policy(mode="exit", exit_layer=0, d_max=3, temperature=T, seed=7))
     ctx.prefill(prompt)
     counts = np.zeros(16)
     n = 3000
