@@ -1,0 +1,275 @@
+// Decode / verify attention: one work item = (KV head, 64-position chunk).
+// Shared by the standalone attention kernel and the persistent pass kernel.
+//
+// A pass carries M <= 16 query rows at consecutive positions pos0..pos0+M-1.
+// The item
+//   1. brings the chunk's cached keys / values into shared memory with bulk
+//      copies (the cached rows of positions >= split come from a scratch
+//      cache: candidate-mask scoring keeps its window there);
+//   2. applies rotate-half RoPE to the chunk's new keys, rounds k and v to
+//      bf16 and appends them to the cache (LayerSkip blog §3.2: every pass
+//      writes the K/V of the layers it runs);
+//   3. for every query head of the group and every row computes the chunk's
+//      maximum score, sum of exponentials and unnormalised output;
+//   4. the item that completes a head's last chunk combines that head's
+//      chunks in chunk order and writes bf16 outputs.
+// Causality is per row: row m sees keys <= pos0+m; masked keys contribute
+// exact zeros, and a row's values depend only on its own position, so a row
+// computed in a pass of M rows is bit-identical to the same row alone.
+#pragma once
+
+#include "kernels.cuh"
+
+namespace ssd {
+namespace attn {
+
+constexpr int kGroupThreads = 256;  // threads that execute an item
+constexpr int kGroupWarps = kGroupThreads / 32;
+constexpr int kKPad = 8;            // bf16 padding per cached key row
+
+// Shared memory of one item (offsets multiples of 16 B):
+//   K [64][dh + 8] bf16 | V [64][dh] bf16 | Q [16][dh] f32 | S [16][64] f32
+//   | combine scratch: m, l, w [nchunk] f32
+struct Smem {
+  bf16* K;
+  bf16* V;
+  float* Q;
+  float* S;
+  float* cm;
+  float* cl;
+  float* cw;
+};
+
+__host__ __device__ inline size_t smem_bytes(int dh, int nchunk) {
+  return (size_t)kAttnChunk * (dh + kKPad) * 2 + (size_t)kAttnChunk * dh * 2 +
+         (size_t)kMaxRows * dh * 4 + (size_t)kMaxRows * kAttnChunk * 4 + (size_t)3 * nchunk * 4;
+}
+
+SSD_DI Smem carve(unsigned char* raw, int dh, int nchunk) {
+  Smem sm;
+  sm.K = reinterpret_cast<bf16*>(raw);
+  sm.V = sm.K + kAttnChunk * (dh + kKPad);
+  sm.Q = reinterpret_cast<float*>(sm.V + kAttnChunk * dh);
+  sm.S = sm.Q + kMaxRows * dh;
+  sm.cm = sm.S + kMaxRows * kAttnChunk;
+  sm.cl = sm.cm + nchunk;
+  sm.cw = sm.cl + nchunk;
+  return sm;
+}
+
+// Executes work item `item` with threads tid < kGroupThreads; `sync()` is
+// the barrier of those threads.  `bar` is an initialised mbarrier whose
+// phase parity is tracked in `phase`; `flag` is one shared int.  Returns
+// true if this item combined its head (the head's output is complete).
+template <class Sync>
+SSD_DI bool item(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, uint64_t* bar,
+                 uint32_t& phase, int* flag, int tid, Sync sync) {
+  const int dh = a.dh, half = dh / 2, krs = dh + kKPad;
+  const int G = a.H / a.Hkv;
+  const int rows = G * kMaxRows;
+  const int nchunk_max = a.max_seq / kAttnChunk;
+  const int last_pos = pos0 + M - 1;
+  const int n_active = last_pos / kAttnChunk + 1;
+  const int warp = tid >> 5, lane = tid & 31;
+  const size_t head_stride = (size_t)a.max_seq * dh;
+  const int ld_out = a.H * dh;
+
+  const int c = item / a.Hkv, kvh = item % a.Hkv;
+  const int p_begin = c * kAttnChunk;
+  const int p_end = min(p_begin + kAttnChunk, last_pos + 1);
+  const int nk = p_end - p_begin;
+  const int n_old = max(0, min(p_end, pos0) - p_begin);
+  bf16* kc = a.kc + kvh * head_stride;
+  bf16* vc = a.vc + kvh * head_stride;
+  bf16* kc2 = a.kc2 ? a.kc2 + (size_t)kvh * a.scratch_len * dh : nullptr;
+  bf16* vc2 = a.vc2 ? a.vc2 + (size_t)kvh * a.scratch_len * dh : nullptr;
+  // row of position pos in the shared cache or in the scratch cache
+  auto krow = [&](int pos) {
+    return pos < a.split ? kc + (size_t)pos * dh : kc2 + (size_t)(pos - a.split) * dh;
+  };
+  auto vrow = [&](int pos) {
+    return pos < a.split ? vc + (size_t)pos * dh : vc2 + (size_t)(pos - a.split) * dh;
+  };
+
+  // (1) cached keys/values: bulk copies issued by warp 0 (one per padded K
+  // row; the V rows in one copy unless the chunk straddles the split)
+  if (n_old > 0 && warp == 0) {
+    const bool one_v = p_begin + n_old <= a.split || p_begin >= a.split;
+    if (lane == 0) {
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar, (uint32_t)(2 * n_old * dh * sizeof(bf16)));
+      if (one_v) bulk_g2s(sm.V, vrow(p_begin), (uint32_t)(n_old * dh * sizeof(bf16)), bar);
+    }
+    __syncwarp();
+    for (int j = lane; j < n_old; j += 32) {
+      bulk_g2s(sm.K + (size_t)j * krs, krow(p_begin + j), (uint32_t)(dh * sizeof(bf16)), bar);
+      if (!one_v)
+        bulk_g2s(sm.V + (size_t)j * dh, vrow(p_begin + j), (uint32_t)(dh * sizeof(bf16)), bar);
+    }
+  }
+  // (2) new keys of this chunk: RoPE, bf16, append to the cache
+  const int first_new = max(p_begin, pos0);
+  for (int e = tid; e < (p_end - first_new) * half; e += kGroupThreads) {
+    const int jj = e / half, i = e % half;
+    const int pos = first_new + jj, m = pos - pos0, j = pos - p_begin;
+    const float* kr = a.qkv + (size_t)m * a.ld_qkv + (size_t)(a.H + kvh) * dh;
+    const float* vr = kr + (size_t)a.Hkv * dh;
+    const float2 cs = a.rope[(size_t)pos * half + i];
+    const float k0 = __ldcg(kr + i), k1 = __ldcg(kr + i + half);
+    const bf16 kb0 = __float2bfloat16_rn(k0 * cs.x - k1 * cs.y);
+    const bf16 kb1 = __float2bfloat16_rn(k0 * cs.y + k1 * cs.x);
+    const bf16 vb0 = __float2bfloat16_rn(__ldcg(vr + i));
+    const bf16 vb1 = __float2bfloat16_rn(__ldcg(vr + i + half));
+    sm.K[j * krs + i] = kb0;
+    sm.K[j * krs + i + half] = kb1;
+    sm.V[j * dh + i] = vb0;
+    sm.V[j * dh + i + half] = vb1;
+    bf16* kd = krow(pos);
+    bf16* vd = vrow(pos);
+    kd[i] = kb0;
+    kd[i + half] = kb1;
+    vd[i] = vb0;
+    vd[i + half] = vb1;
+  }
+  if (n_old > 0) {
+    if (!mbar_wait(bar, phase & 1u)) {
+      if (tid == 0) atomicExch(a.err, 1);
+      return false;
+    }
+    ++phase;
+  }
+
+  float* part_base = a.part + ((size_t)kvh * nchunk_max + c) * rows * (dh + 2);
+  for (int gh = 0; gh < G; ++gh) {
+    sync();  // K/V complete; the previous head's S and Q are no longer read
+    // (3) queries of this head, RoPE'd, fp32
+    for (int e = tid; e < M * half; e += kGroupThreads) {
+      const int i = e % half, m = e / half;
+      const float* qr = a.qkv + (size_t)m * a.ld_qkv + (size_t)(kvh * G + gh) * dh;
+      const float2 cs = a.rope[(size_t)(pos0 + m) * half + i];
+      const float q0 = __ldcg(qr + i), q1 = __ldcg(qr + i + half);
+      float* qd = sm.Q + (size_t)m * dh;
+      qd[i] = q0 * cs.x - q1 * cs.y;
+      qd[i + half] = q0 * cs.y + q1 * cs.x;
+    }
+    sync();
+    // (4) scores: 4 lanes per (row, key), each lane a quarter of the head
+    // dimension in 8-wide pieces, then a 2-step butterfly (fixed order)
+    const int qd = dh / 4;
+    for (int u = tid; u < M * kAttnChunk * 4; u += kGroupThreads) {
+      const int qt = u & 3, key = (u >> 2) & (kAttnChunk - 1), m = u >> 8;
+      const bool valid = key < nk && p_begin + key <= pos0 + m;
+      float acc = 0.f;
+      if (valid) {
+        const float* q = sm.Q + (size_t)m * dh;
+        const bf16* k = sm.K + (size_t)key * krs;
+        for (int t = 0; t < qd; t += 8) {
+          const int d0 = t * 4 + qt * 8;
+          const uint4 kk = *reinterpret_cast<const uint4*>(k + d0);
+          const float4 qa = *reinterpret_cast<const float4*>(q + d0);
+          const float4 qb = *reinterpret_cast<const float4*>(q + d0 + 4);
+          acc = fmaf(qa.x, bf16_lo(kk.x), acc);
+          acc = fmaf(qa.y, bf16_hi(kk.x), acc);
+          acc = fmaf(qa.z, bf16_lo(kk.y), acc);
+          acc = fmaf(qa.w, bf16_hi(kk.y), acc);
+          acc = fmaf(qb.x, bf16_lo(kk.z), acc);
+          acc = fmaf(qb.y, bf16_hi(kk.z), acc);
+          acc = fmaf(qb.z, bf16_lo(kk.w), acc);
+          acc = fmaf(qb.w, bf16_hi(kk.w), acc);
+        }
+      }
+      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+      if (qt == 0) sm.S[(size_t)m * kAttnChunk + key] = valid ? acc * a.scale : -INFINITY;
+    }
+    sync();
+    // (5) per-row chunk softmax statistics; one warp per row
+    for (int m = warp; m < M; m += kGroupWarps) {
+      const int r = gh * kMaxRows + m;
+      float* srow = sm.S + (size_t)m * kAttnChunk;
+      const float s0 = srow[lane], s1 = srow[lane + 32];
+      float mx = fmaxf(s0, s1);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float p0 = s0 == -INFINITY ? 0.f : expf(s0 - mx);
+      const float p1 = s1 == -INFINITY ? 0.f : expf(s1 - mx);
+      float l = p0 + p1;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+      __syncwarp();
+      srow[lane] = p0;
+      srow[lane + 32] = p1;
+      if (lane == 0) {
+        part_base[(size_t)r * (dh + 2) + 0] = mx;
+        part_base[(size_t)r * (dh + 2) + 1] = l;
+      }
+    }
+    sync();
+    // (6) unnormalised output of the chunk: sequential over keys
+    for (int e = tid; e < M * dh; e += kGroupThreads) {
+      const int dd = e % dh, m = e / dh;
+      const int r = gh * kMaxRows + m;
+      const float* p = sm.S + (size_t)m * kAttnChunk;
+      float o = 0.f;
+      for (int j = 0; j < nk; ++j) o = fmaf(p[j], __bfloat162float(sm.V[j * dh + dd]), o);
+      part_base[(size_t)r * (dh + 2) + 2 + dd] = o;
+    }
+  }
+  __threadfence();
+  sync();
+  if (tid == 0) {
+    const unsigned prev = atomicAdd(a.counters + kvh, 1u);
+    *flag = prev == (unsigned)(n_active - 1);
+  }
+  sync();
+  const bool last = *flag != 0;
+  if (last) {
+    __threadfence();
+    // (7) combine this head's chunks in chunk order, one row at a time:
+    // stage (m_c, l_c), weights w_c = exp(m_c - max), then each output
+    // dimension sums o_c * w_c over chunks.
+    const float* hb = a.part + (size_t)kvh * nchunk_max * rows * (dh + 2);
+    for (int rr = 0; rr < G * M; ++rr) {
+      const int m = rr % M, gh = rr / M, r = gh * kMaxRows + m;
+      const int nc = (pos0 + m) / kAttnChunk + 1;
+      for (int cc = tid; cc < nc; cc += kGroupThreads) {
+        const float* pc = hb + ((size_t)cc * rows + r) * (dh + 2);
+        sm.cm[cc] = __ldcg(pc);
+        sm.cl[cc] = __ldcg(pc + 1);
+      }
+      sync();
+      float mx = -INFINITY;
+      for (int cc = 0; cc < nc; ++cc) mx = fmaxf(mx, sm.cm[cc]);
+      for (int cc = tid; cc < nc; cc += kGroupThreads) sm.cw[cc] = expf(sm.cm[cc] - mx);
+      sync();
+      float L = 0.f;
+      for (int cc = 0; cc < nc; ++cc) L = fmaf(sm.cl[cc], sm.cw[cc], L);
+      for (int dd = tid; dd < dh; dd += kGroupThreads) {
+        float O = 0.f;
+        int cc = 0;
+        for (; cc + 4 <= nc; cc += 4) {
+          const float o0 = __ldcg(hb + ((size_t)(cc + 0) * rows + r) * (dh + 2) + 2 + dd);
+          const float o1 = __ldcg(hb + ((size_t)(cc + 1) * rows + r) * (dh + 2) + 2 + dd);
+          const float o2 = __ldcg(hb + ((size_t)(cc + 2) * rows + r) * (dh + 2) + 2 + dd);
+          const float o3 = __ldcg(hb + ((size_t)(cc + 3) * rows + r) * (dh + 2) + 2 + dd);
+          O = fmaf(o0, sm.cw[cc + 0], O);
+          O = fmaf(o1, sm.cw[cc + 1], O);
+          O = fmaf(o2, sm.cw[cc + 2], O);
+          O = fmaf(o3, sm.cw[cc + 3], O);
+        }
+        for (; cc < nc; ++cc)
+          O = fmaf(__ldcg(hb + ((size_t)cc * rows + r) * (dh + 2) + 2 + dd), sm.cw[cc], O);
+        a.out[(size_t)m * ld_out + (size_t)(kvh * G + gh) * dh + dd] = __float2bfloat16_rn(O / L);
+      }
+      sync();
+    }
+    if (tid == 0) a.counters[kvh] = 0u;
+  }
+  // the next item's bulk copies overwrite this item's shared memory
+  fence_proxy_async_smem();
+  sync();
+  return last;
+}
+
+}  // namespace attn
+}  // namespace ssd

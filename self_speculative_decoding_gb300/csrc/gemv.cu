@@ -27,475 +27,13 @@
 // nothing depends on M, so a column's bits do not change with the number of
 // rows processed together — which is what makes self-speculative
 // verification reproduce autoregressive decoding bit for bit.
-#include "kernels.cuh"
+#include "gemv_dev.cuh"
 
 namespace ssd {
 
+using namespace gemv;
+
 namespace {
-
-constexpr int kConsumers = 8;                    // consumer warps
-constexpr int kProducer = kConsumers;            // warp that issues the bulk copies
-constexpr int kEpilogue = kConsumers + 1;        // warp that finishes row groups
-constexpr int kThreads = (kConsumers + 2) * 32;
-#ifndef SSD_GEMV_CTAS
-#define SSD_GEMV_CTAS 304
-#endif
-#ifndef SSD_GEMV_CHUNK
-#define SSD_GEMV_CHUNK 8
-#endif
-#ifndef SSD_GEMV_SLOTS
-#define SSD_GEMV_SLOTS 5
-#endif
-constexpr int kGridCtas = SSD_GEMV_CTAS;         // 2 resident CTAs x 152 SMs
-constexpr int kChunk = SSD_GEMV_CHUNK;           // units per ring slot (<= kConsumers * k)
-constexpr int kSlots = SSD_GEMV_SLOTS;           // ring depth
-constexpr int kUPW = (kChunk + kConsumers - 1) / kConsumers;  // units per warp per chunk
-constexpr int kUnitBytes = 1024;
-constexpr int kSlotBytes = kChunk * kUnitBytes;
-constexpr int kRingBytes = kSlots * kSlotBytes;
-constexpr int kLmBlock = 32;                     // LM-head row groups per level-2 block
-// Activations (the B operand, bf16 and already normalised for the norm-fused
-// input) are staged once per CTA when M rows of K fit in this budget; this
-// covers every single-token pass of the 7B and 13B shapes.
-constexpr int kStageBytes = 52 * 1024;
-constexpr int kPad = 8;                          // bf16 row padding of the stage
-
-struct Part {
-  long long T;  // units = NRG * KB
-  int NRG;      // (virtual) 16-row groups
-  int KB;       // 32-wide K blocks
-  int C;        // CTAs with work = min(kGridCtas, T)
-  int segmax;   // stride of the partial buffer per row group
-};
-
-__host__ __device__ inline long long unit_begin(const Part& p, int b) {
-  return (long long)b * p.T / p.C;
-}
-// first / last CTA whose unit range intersects units [a, b)
-__host__ __device__ inline int cta_first(const Part& p, long long a) {
-  return (int)(((a + 1) * p.C + p.T - 1) / p.T) - 1;
-}
-__host__ __device__ inline int cta_last(const Part& p, long long b) {
-  return (int)((b * p.C + p.T - 1) / p.T) - 1;
-}
-__host__ __device__ inline int nseg(const Part& p, int vr) {
-  return cta_last(p, (long long)(vr + 1) * p.KB) - cta_first(p, (long long)vr * p.KB) + 1;
-}
-
-Part make_part(int R, int K, int epi) {
-  Part p;
-  p.NRG = (epi == EPI_SWIGLU ? 2 : 1) * (R / 16);
-  p.KB = K / 32;
-  p.T = (long long)p.NRG * p.KB;
-  p.C = (int)(p.T < kGridCtas ? p.T : kGridCtas);
-  p.segmax = (p.C + p.NRG - 1) / p.NRG + 1;
-  return p;
-}
-
-// Unit (vr, kb) in the packed stream of its matrix.
-template <int EPI>
-SSD_DI const bf16* unit_src(const LinearArgs& a, const Part& p, int vr, int kb) {
-  if (EPI == EPI_SWIGLU) {
-    const bf16* W = (vr & 1) ? a.W1 : a.W0;
-    return W + ((size_t)(vr >> 1) * p.KB + kb) * (kUnitBytes / 2);
-  }
-  return a.W0 + ((size_t)vr * p.KB + kb) * (kUnitBytes / 2);
-}
-
-// Raw B operand (8 consecutive K of one token): loaded one chunk ahead so
-// that the global-memory latency is off the critical path.  For the
-// norm-fused input the RMSNorm is applied when the operand is used.
-template <int IN>
-struct BRaw {
-  uint4 v;
-};
-template <>
-struct BRaw<IN_NORM> {
-  float4 x0, x1, g0, g1;
-};
-
-template <int IN>
-SSD_DI void b_issue(BRaw<IN>& r, const LinearArgs& a, int t, int off, bool valid) {
-  if (IN == IN_BF16) {
-    auto& q = reinterpret_cast<BRaw<IN_BF16>&>(r);
-    q.v = valid ? *reinterpret_cast<const uint4*>(a.act + (size_t)t * a.K + off)
-                : make_uint4(0u, 0u, 0u, 0u);
-  } else {
-    auto& q = reinterpret_cast<BRaw<IN_NORM>&>(r);
-    if (valid) {
-      const float4* xp = reinterpret_cast<const float4*>(a.x + (size_t)t * a.K + off);
-      const float4* gp = reinterpret_cast<const float4*>(a.gain + off);
-      q.x0 = xp[0]; q.x1 = xp[1]; q.g0 = gp[0]; q.g1 = gp[1];
-    } else {
-      q.x0 = q.x1 = q.g0 = q.g1 = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  }
-}
-
-template <int IN>
-SSD_DI uint4 b_finish(const BRaw<IN>& r, float rs) {
-  if (IN == IN_BF16) {
-    return reinterpret_cast<const BRaw<IN_BF16>&>(r).v;
-  } else {
-    const auto& q = reinterpret_cast<const BRaw<IN_NORM>&>(r);
-    return make_uint4(pack_bf16x2(q.x0.x * rs * q.g0.x, q.x0.y * rs * q.g0.y),
-                      pack_bf16x2(q.x0.z * rs * q.g0.z, q.x0.w * rs * q.g0.w),
-                      pack_bf16x2(q.x1.x * rs * q.g1.x, q.x1.y * rs * q.g1.y),
-                      pack_bf16x2(q.x1.z * rs * q.g1.z, q.x1.w * rs * q.g1.w));
-  }
-}
-
-SSD_DI void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory"); }
-
-SSD_DI void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-// ---------------------------------------------------------------- reductions
-
-// Top-2 merge under the (value desc, index asc) total order.
-SSD_DI void top2_insert(float v, int i, float& v1, int& i1, float& v2, int& i2) {
-  if (better(v, i, v1, i1)) {
-    v2 = v1; i2 = i1; v1 = v; i1 = i;
-  } else if (better(v, i, v2, i2)) {
-    v2 = v; i2 = i;
-  }
-}
-
-SSD_DI void top2_warp(float& v1, int& i1, float& v2, int& i2) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov1 = __shfl_xor_sync(0xffffffffu, v1, o);
-    const int oi1 = __shfl_xor_sync(0xffffffffu, i1, o);
-    const float ov2 = __shfl_xor_sync(0xffffffffu, v2, o);
-    const int oi2 = __shfl_xor_sync(0xffffffffu, i2, o);
-    top2_insert(ov1, oi1, v1, i1, v2, i2);
-    top2_insert(ov2, oi2, v1, i1, v2, i2);
-  }
-}
-
-SSD_DI void argmax_warp(float& v, int& i) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-    if (better(ov, oi, v, i)) { v = ov; i = oi; }
-  }
-}
-
-SSD_DI float sum_warp(float s) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  return s;
-}
-
-// LM-head summary of a set of vocabulary rows for one token: max z and its
-// id, second z and its id, sum exp(z - max), sum exp(z/T - max/T), best
-// Gumbel score and its id.
-struct LmRec {
-  float v1, v2, se, set, gv;
-  int i1, i2, gi;
-};
-
-SSD_DI void lm_store(float* p, const LmRec& r) {
-  reinterpret_cast<float4*>(p)[0] =
-      make_float4(r.v1, __int_as_float(r.i1), r.v2, __int_as_float(r.i2));
-  reinterpret_cast<float4*>(p)[1] = make_float4(r.se, r.set, r.gv, __int_as_float(r.gi));
-}
-
-SSD_DI LmRec lm_load(const float* p) {
-  const float4 a = __ldcg(reinterpret_cast<const float4*>(p));
-  const float4 b = __ldcg(reinterpret_cast<const float4*>(p) + 1);
-  LmRec r;
-  r.v1 = a.x; r.i1 = __float_as_int(a.y); r.v2 = a.z; r.i2 = __float_as_int(a.w);
-  r.se = b.x; r.set = b.y; r.gv = b.z; r.gi = __float_as_int(b.w);
-  return r;
-}
-
-SSD_DI LmRec lm_empty() {
-  LmRec r;
-  r.v1 = r.v2 = r.gv = -INFINITY;
-  r.i1 = r.i2 = r.gi = 0x7fffffff;
-  r.se = r.set = 0.f;
-  return r;
-}
-
-// Merge one record per lane (a butterfly, identical in every lane); the sums
-// are rescaled to the merged maximum before being added.
-SSD_DI LmRec lm_merge_warp(LmRec r, float T) {
-  float v1 = r.v1, v2 = r.v2, gv = r.gv;
-  int i1 = r.i1, i2 = r.i2, gi = r.gi;
-  top2_warp(v1, i1, v2, i2);
-  argmax_warp(gv, gi);
-  const float mx = v1;
-  float s = r.v1 == -INFINITY ? 0.f : r.se * expf(r.v1 - mx);
-  float st = 0.f;
-  if (T > 0.f) st = r.v1 == -INFINITY ? 0.f : r.set * expf(r.v1 / T - mx / T);
-  s = sum_warp(s);
-  st = sum_warp(st);
-  LmRec o;
-  o.v1 = v1; o.i1 = i1; o.v2 = v2; o.i2 = i2; o.gv = gv; o.gi = gi; o.se = s; o.set = st;
-  return o;
-}
-
-// ---------------------------------------------------------------- epilogues
-
-// Runs in one warp once row group vr (or the gate/up pair containing it) is
-// complete; ep[h][row][tok] holds the finished sums.
-template <int EPI>
-SSD_DI void epilogue(const LinearArgs& a, const Part& p, int vr, float (*ep)[16][17], int M,
-                     int lane) {
-  if (EPI == EPI_STORE) {
-    const int row0 = vr * 16;
-    for (int e = lane; e < 16 * M; e += 32) {
-      const int row = e / M, tok = e % M;
-      a.y[(size_t)tok * a.R + row0 + row] = ep[0][row][tok];
-    }
-  } else if (EPI == EPI_RESID) {
-    const int row0 = vr * 16;
-    for (int e = lane; e < 16 * M; e += 32) {
-      const int row = e / M, tok = e % M;
-      const size_t idx = (size_t)tok * a.R + row0 + row;
-      const float xn = a.xres[idx] + ep[0][row][tok];
-      a.xres[idx] = xn;
-      ep[0][row][tok] = xn;
-    }
-    __syncwarp();
-    if (lane < M) {
-      float s = 0.f;
-      for (int row = 0; row < 16; ++row) s += ep[0][row][lane] * ep[0][row][lane];
-      a.ss_out[(size_t)lane * (a.R / kSsGroup) + vr] = s;
-    }
-  } else if (EPI == EPI_SWIGLU) {
-    const int row0 = (vr >> 1) * 16;
-    for (int e = lane; e < 16 * M; e += 32) {
-      const int row = e / M, tok = e % M;
-      const float gt = ep[0][row][tok];
-      const float up = ep[1][row][tok];
-      const float sl = gt / (1.0f + expf(-gt));
-      a.u[(size_t)tok * a.R + row0 + row] = __float2bfloat16_rn(sl * up);
-    }
-  } else if (EPI == EPI_LMHEAD) {
-    const int slot = a.slot_dev ? *a.slot_dev : 0;
-    const int row0 = vr * 16;
-    const float T = a.temperature;
-    if (a.logits) {
-      for (int e = lane; e < 16 * M; e += 32) {
-        const int row = e / M, tok = e % M;
-        a.logits[(size_t)(slot + tok) * a.R + row0 + row] = ep[0][row][tok];
-      }
-    }
-    const int round = a.round_dev ? *a.round_dev : a.round_static;
-    const int pos0 = a.pos0_dev ? *a.pos0_dev : a.pos0_static;
-    // level 1: this group's 16 rows in order, one lane per token
-    if (lane < M) {
-      LmRec r = lm_empty();
-      for (int row = 0; row < 16; ++row) {
-        const float z = ep[0][row][lane];
-        top2_insert(z, row0 + row, r.v1, r.i1, r.v2, r.i2);
-        if (T > 0.f && a.sample) {
-          const float sc =
-              z / T + gumbel_at(a.seed, row0 + row, pos0 + lane + 1, round, a.sample_stream);
-          if (better(sc, row0 + row, r.gv, r.gi)) { r.gv = sc; r.gi = row0 + row; }
-        }
-      }
-      for (int row = 0; row < 16; ++row) {
-        const float z = ep[0][row][lane];
-        r.se += expf(z - r.v1);
-        if (T > 0.f) r.set += expf(z / T - r.v1 / T);
-      }
-      lm_store(a.rec + ((size_t)vr * kMaxRows + lane) * 8, r);
-    }
-    __threadfence();
-    __syncwarp();
-    // level 2: blocks of kLmBlock consecutive groups
-    const int nb = (p.NRG + kLmBlock - 1) / kLmBlock;
-    const int blk = vr / kLmBlock;
-    const int blk_n = min(kLmBlock, p.NRG - blk * kLmBlock);
-    unsigned* c2 = a.counter + p.NRG;
-    int last2 = 0;
-    if (lane == 0) last2 = atomicAdd(c2 + blk, 1u) == (unsigned)(blk_n - 1);
-    last2 = __shfl_sync(0xffffffffu, last2, 0);
-    if (!last2) return;
-    __threadfence();
-    float* rec2 = a.rec + (size_t)p.NRG * kMaxRows * 8;
-    for (int tok = 0; tok < M; ++tok) {
-      const int gi = blk * kLmBlock + lane;
-      LmRec r = lane < blk_n ? lm_load(a.rec + ((size_t)gi * kMaxRows + tok) * 8) : lm_empty();
-      r = lm_merge_warp(r, T);
-      if (lane == 0) lm_store(rec2 + ((size_t)blk * kMaxRows + tok) * 8, r);
-    }
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) c2[blk] = 0u;
-    int last3 = 0;
-    if (lane == 0) last3 = atomicAdd(c2 + nb, 1u) == (unsigned)(nb - 1);
-    last3 = __shfl_sync(0xffffffffu, last3, 0);
-    if (!last3) return;
-    __threadfence();
-    // level 3: all blocks; lane b folds blocks b, b+32, ... in order
-    for (int tok = 0; tok < M; ++tok) {
-      LmRec r = lm_empty();
-      for (int b = lane; b < nb; b += 32) {
-        const LmRec q = lm_load(rec2 + ((size_t)b * kMaxRows + tok) * 8);
-        const float mx = fmaxf(r.v1, q.v1);
-        const float se =
-            (r.v1 == -INFINITY ? 0.f : r.se * expf(r.v1 - mx)) + q.se * expf(q.v1 - mx);
-        float set = 0.f;
-        if (T > 0.f)
-          set = (r.v1 == -INFINITY ? 0.f : r.set * expf(r.v1 / T - mx / T)) +
-                q.set * expf(q.v1 / T - mx / T);
-        top2_insert(q.v1, q.i1, r.v1, r.i1, r.v2, r.i2);
-        top2_insert(q.v2, q.i2, r.v1, r.i1, r.v2, r.i2);
-        if (better(q.gv, q.gi, r.gv, r.gi)) { r.gv = q.gv; r.gi = q.gi; }
-        r.se = se;
-        r.set = set;
-      }
-      r = lm_merge_warp(r, T);
-      if (lane == 0) {
-        RowStats rs;
-        rs.top1 = r.i1;
-        rs.top2 = r.i2;
-        rs.sample = T > 0.f && a.sample ? r.gi : r.i1;
-        rs.pad = 0;
-        rs.z1 = r.v1;
-        rs.z2 = r.v2;
-        rs.lse = r.v1 + logf(r.se);
-        rs.conf = expf(r.v1 - rs.lse);
-        rs.lse_t = T > 0.f ? r.v1 / T + logf(r.set) : rs.lse;
-        rs.pad2[0] = rs.pad2[1] = rs.pad2[2] = 0.f;
-        a.stats[slot + tok] = rs;
-      }
-    }
-    if (lane == 0) c2[nb] = 0u;
-  }
-}
-
-// ---------------------------------------------------------------- kernel
-
-struct __align__(16) GemvSmem {
-  unsigned char ring[kRingBytes];
-  float red[2][kConsumers][16][16];  // per-warp partials, double-buffered per row group
-  float ep[2][16][17];               // epilogue operands
-  float rstd[kMaxRows];
-  uint64_t full[kSlots];             // slot filled by the bulk copy
-  uint64_t empty[kSlots];            // slot consumed by all consumer warps
-  uint64_t rfull[2];                 // partial buffer written by all consumer warps
-  uint64_t rempty[2];                // partial buffer read by the epilogue warp
-  __align__(16) bf16 stage[kStageBytes / 2];
-};
-
-// Length of the next chunk: at most kChunk units, never crossing a row group.
-SSD_DI int chunk_len(const Part& p, int kb, int left) {
-  return min(kChunk, min(p.KB - kb, left));
-}
-
-// Consumer warps: take the ring's slots in order, one unit per warp per
-// slot, and hand each finished row-group segment to the epilogue warp.
-template <int IN, int EPI, bool STAGED>
-SSD_DI void consume(const LinearArgs& a, const Part& p, GemvSmem& sm, long long U0, long long U1,
-                    int M, int warp, int lane) {
-  const int g = lane >> 2, c = lane & 3;
-  const bool two = M > 8;
-  const bool v0 = g < M, v1 = two && (g + 8) < M;
-  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  const float rs0 = IN == IN_NORM && v0 && !STAGED ? sm.rstd[g] : 0.f;
-  const float rs1 = IN == IN_NORM && v1 && !STAGED ? sm.rstd[g + 8] : 0.f;
-  int vr = (int)(U0 / p.KB), kb = (int)(U0 % p.KB), left = (int)(U1 - U0);
-  int n = left > 0 ? chunk_len(p, kb, left) : 0;
-  BRaw<IN> ra[kUPW], rb[kUPW];
-  if (!STAGED) {
-#pragma unroll
-    for (int i = 0; i < kUPW; ++i) {
-      const int un = warp + i * kConsumers;
-      b_issue<IN>(ra[i], a, g, (kb + un) * 32 + 8 * c, v0 && un < n);
-      if (two) b_issue<IN>(rb[i], a, g + 8, (kb + un) * 32 + 8 * c, v1 && un < n);
-    }
-  }
-  int slot = 0;
-  uint32_t ph = 0;
-  int fl = 0;
-  while (left > 0) {
-    // position of the next chunk; its B operands are requested now
-    int kb2 = kb + n, vr2 = vr;
-    const int left2 = left - n;
-    if (kb2 == p.KB) { kb2 = 0; ++vr2; }
-    const int n2 = left2 > 0 ? chunk_len(p, kb2, left2) : 0;
-    BRaw<IN> na[kUPW], nb[kUPW];
-    if (!STAGED) {
-#pragma unroll
-      for (int i = 0; i < kUPW; ++i) {
-        const int un = warp + i * kConsumers;
-        b_issue<IN>(na[i], a, g, (kb2 + un) * 32 + 8 * c, v0 && un < n2);
-        if (two) b_issue<IN>(nb[i], a, g + 8, (kb2 + un) * 32 + 8 * c, v1 && un < n2);
-      }
-    }
-
-    if (!mbar_wait(&sm.full[slot], ph)) {
-      if (lane == 0) atomicExch(a.err, 3);
-      return;
-    }
-#pragma unroll
-    for (int i = 0; i < kUPW; ++i) {
-      const int un = warp + i * kConsumers;
-      if (un < n) {
-        const unsigned char* base = sm.ring + slot * kSlotBytes + un * kUnitBytes;
-        const uint4 wa = *reinterpret_cast<const uint4*>(base + lane * 16);
-        const uint4 wb = *reinterpret_cast<const uint4*>(base + 512 + lane * 16);
-        const int off = (kb + un) * 32 + 8 * c;
-        const uint4 xa = STAGED ? (v0 ? *reinterpret_cast<const uint4*>(sm.stage + (size_t)g * (a.K + kPad) + off)
-                                      : make_uint4(0u, 0u, 0u, 0u))
-                                : b_finish<IN>(ra[i], rs0);
-        mma_bf16(acc[0], wa.x, wb.x, wa.y, wb.y, xa.x, xa.y);
-        mma_bf16(acc[0], wa.z, wb.z, wa.w, wb.w, xa.z, xa.w);
-        if (two) {
-          const uint4 xb = STAGED ? (v1 ? *reinterpret_cast<const uint4*>(sm.stage + (size_t)(g + 8) * (a.K + kPad) + off)
-                                        : make_uint4(0u, 0u, 0u, 0u))
-                                  : b_finish<IN>(rb[i], rs1);
-          mma_bf16(acc[1], wa.x, wb.x, wa.y, wb.y, xb.x, xb.y);
-          mma_bf16(acc[1], wa.z, wb.z, wa.w, wb.w, xb.z, xb.w);
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.empty[slot]);
-    if (++slot == kSlots) { slot = 0; ph ^= 1u; }
-    const bool group_done = kb2 == 0 || left2 == 0;
-    vr = vr2;
-    kb = kb2;
-    left = left2;
-    n = n2;
-    if (!STAGED) {
-#pragma unroll
-      for (int i = 0; i < kUPW; ++i) {
-        ra[i] = na[i];
-        if (two) rb[i] = nb[i];
-      }
-    }
-    if (!group_done) continue;
-    // ---- the CTA's part of a row group is done: hand the accumulators to
-    // the epilogue warp through the double-buffered partial area
-    {
-      const int buf = fl & 1;
-      if (fl >= 2 && !mbar_wait(&sm.rempty[buf], ((fl >> 1) - 1) & 1)) {
-        if (lane == 0) atomicExch(a.err, 5);
-        return;
-      }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int tok = h * 8 + 2 * c;
-        sm.red[buf][warp][g][tok] = acc[h][0];
-        sm.red[buf][warp][g][tok + 1] = acc[h][1];
-        sm.red[buf][warp][g + 8][tok] = acc[h][2];
-        sm.red[buf][warp][g + 8][tok + 1] = acc[h][3];
-        acc[h][0] = acc[h][1] = acc[h][2] = acc[h][3] = 0.f;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.rfull[buf]);
-      ++fl;
-    }
-  }
-}
 
 template <int IN, int EPI>
 __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(LinearArgs a, Part p) {
@@ -503,8 +41,6 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(LinearArgs a, Part p)
   GemvSmem& sm = *reinterpret_cast<GemvSmem*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x;
-  const long long U0 = unit_begin(p, b), U1 = unit_begin(p, b + 1);
-
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&sm.full[s], 1);
@@ -517,121 +53,20 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(LinearArgs a, Part p)
     fence_mbar_init();
   }
   __syncthreads();
-
+  RingPos rp;
   if (warp == kProducer) {
-    // ---- producer: stream this CTA's units into the ring (weights do not
-    // depend on the preceding kernel, so no wait is needed here)
-    if (lane == 0) {
-      int vr = (int)(U0 / p.KB), kb = (int)(U0 % p.KB), left = (int)(U1 - U0);
-      int slot = 0;
-      uint32_t ph = 0;   // parity of the ring pass
-      for (int t = 0; left > 0; ++t) {
-        const int n = chunk_len(p, kb, left);
-        if (t >= kSlots && !mbar_wait(&sm.empty[slot], ph ^ 1u)) {
-          atomicExch(a.err, 2);
-          break;
-        }
-        mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)(n * kUnitBytes));
-        bulk_g2s(sm.ring + slot * kSlotBytes, unit_src<EPI>(a, p, vr, kb),
-                 (uint32_t)(n * kUnitBytes), &sm.full[slot]);
-        kb += n;
-        left -= n;
-        if (kb == p.KB) { kb = 0; ++vr; }
-        if (++slot == kSlots) { slot = 0; ph ^= 1u; }
-      }
-    }
+    // weights do not depend on the preceding kernel: no wait before streaming
+    producer_phase<EPI>(a, p, sm, b, lane, rp);
     return;
   }
-
   pdl_wait();
   pdl_trigger();
   const int M = rows_of(a.M_static, a.M_dev);
-
   if (warp == kEpilogue) {
-    // ---- epilogue warp: one flush per row-group segment of this CTA's range
-    int vr = (int)(U0 / p.KB), kb = (int)(U0 % p.KB), left = (int)(U1 - U0);
-    for (int fl = 0; left > 0; ++fl) {
-      const int gvr = vr;
-      left -= p.KB - kb < left ? p.KB - kb : left;
-      kb = 0;
-      ++vr;
-      const int buf = fl & 1;
-      if (!mbar_wait(&sm.rfull[buf], (fl >> 1) & 1)) {
-        if (lane == 0) atomicExch(a.err, 4);
-        return;
-      }
-      // this CTA's partial of the group: the consumer warps summed in order
-      const int seg = b - cta_first(p, (long long)gvr * p.KB);
-      float* dst = a.part + ((size_t)gvr * p.segmax + seg) * 256;
-      for (int e = lane; e < 16 * M; e += 32) {
-        const int row = e / M, tok = e % M;
-        float s2 = 0.f;
-        for (int w2 = 0; w2 < kConsumers; ++w2) s2 += sm.red[buf][w2][row][tok];
-        dst[row * 16 + tok] = s2;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.rempty[buf]);
-      __threadfence();
-      __syncwarp();
-      const int cidx = EPI == EPI_SWIGLU ? gvr >> 1 : gvr;
-      int last = 0;
-      if (lane == 0) {
-        int expect = nseg(p, gvr);
-        if (EPI == EPI_SWIGLU) expect += nseg(p, gvr ^ 1);
-        last = atomicAdd(a.counter + cidx, 1u) == (unsigned)(expect - 1);
-      }
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (!last) continue;
-      __threadfence();
-      // sum the CTAs' partials of the group(s) in CTA order
-      const int ngrp = EPI == EPI_SWIGLU ? 2 : 1;
-      for (int h = 0; h < ngrp; ++h) {
-        const int gv = EPI == EPI_SWIGLU ? ((gvr & ~1) | h) : gvr;
-        const int ns = nseg(p, gv);
-        const float* src = a.part + (size_t)gv * p.segmax * 256;
-        for (int e = lane; e < 16 * M; e += 32) {
-          const int row = e / M, tok = e % M;
-          float s2 = 0.f;
-          for (int sg = 0; sg < ns; ++sg) s2 += __ldcg(src + (size_t)sg * 256 + row * 16 + tok);
-          sm.ep[h][row][tok] = s2;
-        }
-      }
-      __syncwarp();
-      if (lane == 0) a.counter[cidx] = 0u;
-      epilogue<EPI>(a, p, gvr, sm.ep, M, lane);
-      __syncwarp();
-    }
+    epilogue_phase<EPI>(a, p, sm, b, M, lane, rp, nullptr);
     return;
   }
-
-  // ---- consumers
-  if (IN == IN_NORM) {
-    // 1 / sqrt(mean(x^2) + eps) per row from the producer's partials, in a
-    // fixed order: lane l sums partials l, l+32, ... then a butterfly.
-    const int NP = a.K / kSsGroup;
-    for (int m = warp; m < M; m += kConsumers) {
-      float s2 = 0.f;
-      for (int q = lane; q < NP; q += 32) s2 += a.ss[(size_t)m * NP + q];
-      s2 = sum_warp(s2);
-      if (lane == 0) sm.rstd[m] = 1.0f / sqrtf(s2 / (float)a.K + a.eps);
-    }
-    consumer_sync();
-  }
-  const bool staged = (size_t)M * (a.K + kPad) * sizeof(bf16) <= (size_t)kStageBytes;
-  if (staged) {
-    const int vpr = a.K / 8;   // 16-byte pieces per row
-    for (int e = threadIdx.x; e < M * vpr; e += kConsumers * 32) {
-      const int m = e / vpr, q = e % vpr;
-      BRaw<IN> r;
-      b_issue<IN>(r, a, m, q * 8, true);
-      const float rs = IN == IN_NORM ? sm.rstd[m] : 0.f;
-      *reinterpret_cast<uint4*>(sm.stage + (size_t)m * (a.K + kPad) + q * 8) = b_finish<IN>(r, rs);
-    }
-    consumer_sync();
-    consume<IN, EPI, true>(a, p, sm, U0, U1, M, warp, lane);
-  } else {
-    consume<IN, EPI, false>(a, p, sm, U0, U1, M, warp, lane);
-  }
+  consumer_phase<IN, EPI>(a, p, sm, b, M, warp, lane, rp);
 }
 
 template <int IN, int EPI>
