@@ -124,17 +124,31 @@ SSD_DI void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) 
 
 // Bounded wait for the phase with the given parity; false if it never
 // completed (the caller records an error instead of hanging).
+#ifndef SSD_MBAR_SUSPEND_NS
+#define SSD_MBAR_SUSPEND_NS 0
+#endif
 SSD_DI bool mbar_wait(uint64_t* bar, uint32_t parity) {
   const uint32_t addr = smem_addr(bar);
   for (int i = 0; i < (1 << 22); ++i) {
     uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(addr), "r"(parity)
-        : "memory");
+    if (SSD_MBAR_SUSPEND_NS > 0) {
+      // the waiting thread may be suspended up to the hint (ns) per poll
+      asm volatile(
+          "{\n\t.reg .pred p;\n\t"
+          "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+          "selp.u32 %0, 1, 0, p;\n\t}"
+          : "=r"(done)
+          : "r"(addr), "r"(parity), "n"(SSD_MBAR_SUSPEND_NS)
+          : "memory");
+    } else {
+      asm volatile(
+          "{\n\t.reg .pred p;\n\t"
+          "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+          "selp.u32 %0, 1, 0, p;\n\t}"
+          : "=r"(done)
+          : "r"(addr), "r"(parity)
+          : "memory");
+    }
     if (done) return true;
   }
   return false;

@@ -36,7 +36,7 @@ using namespace gemv;
 namespace {
 
 template <int IN, int EPI>
-__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(LinearArgs a, Part p) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(LinearArgs a, Part p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   GemvSmem& sm = *reinterpret_cast<GemvSmem*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

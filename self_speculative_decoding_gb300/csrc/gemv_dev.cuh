@@ -14,20 +14,30 @@
 namespace ssd {
 namespace gemv {
 
-constexpr int kConsumers = 8;                    // consumer warps
+#ifndef SSD_GEMV_CONSUMERS
+#define SSD_GEMV_CONSUMERS 8
+#endif
+#ifndef SSD_GEMV_CPS
+#define SSD_GEMV_CPS 2
+#endif
+#ifndef SSD_GEMV_CTAS
+#define SSD_GEMV_CTAS (152 * SSD_GEMV_CPS)
+#endif
+#ifndef SSD_GEMV_STAGE_KB
+#define SSD_GEMV_STAGE_KB 52
+#endif
+constexpr int kConsumers = SSD_GEMV_CONSUMERS;   // consumer warps
 constexpr int kProducer = kConsumers;            // warp that issues the bulk copies
 constexpr int kEpilogue = kConsumers + 1;        // warp that finishes row groups
 constexpr int kThreads = (kConsumers + 2) * 32;
-#ifndef SSD_GEMV_CTAS
-#define SSD_GEMV_CTAS 304
-#endif
+constexpr int kCtasPerSm = SSD_GEMV_CPS;         // resident CTAs per SM
 #ifndef SSD_GEMV_CHUNK
 #define SSD_GEMV_CHUNK 8
 #endif
 #ifndef SSD_GEMV_SLOTS
 #define SSD_GEMV_SLOTS 5
 #endif
-constexpr int kGridCtas = SSD_GEMV_CTAS;         // 2 resident CTAs x 152 SMs
+constexpr int kGridCtas = SSD_GEMV_CTAS;         // kCtasPerSm resident CTAs x 152 SMs
 constexpr int kChunk = SSD_GEMV_CHUNK;           // units per ring slot (<= kConsumers * k)
 constexpr int kSlots = SSD_GEMV_SLOTS;           // ring depth
 constexpr int kUPW = (kChunk + kConsumers - 1) / kConsumers;  // units per warp per chunk
@@ -38,7 +48,7 @@ constexpr int kLmBlock = 32;                     // LM-head row groups per level
 // Activations (the B operand, bf16 and already normalised for the norm-fused
 // input) are staged once per CTA when M rows of K fit in this budget; this
 // covers every single-token pass of the 7B and 13B shapes.
-constexpr int kStageBytes = 52 * 1024;
+constexpr int kStageBytes = SSD_GEMV_STAGE_KB * 1024;
 constexpr int kPad = 8;                          // bf16 row padding of the stage
 
 struct Part {
