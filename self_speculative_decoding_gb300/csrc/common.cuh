@@ -122,6 +122,11 @@ SSD_DI void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) 
       : "memory");
 }
 
+// Bulk prefetch of global memory into L2 (address and size multiples of 16).
+SSD_DI void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Bounded wait for the phase with the given parity; false if it never
 // completed (the caller records an error instead of hanging).
 #ifndef SSD_MBAR_SUSPEND_NS
@@ -150,6 +155,22 @@ SSD_DI bool mbar_wait(uint64_t* bar, uint32_t parity) {
           : "memory");
     }
     if (done) return true;
+  }
+  return false;
+}
+
+// Adds v to a global counter with release semantics (no value returned).
+SSD_DI void red_release_add(unsigned* c, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(c), "r"(v) : "memory");
+}
+
+// Bounded wait until a global counter reaches target (acquire); false if it
+// never did (the caller records an error instead of hanging).
+SSD_DI bool wait_count(const unsigned* c, unsigned target) {
+  for (int i = 0; i < (1 << 24); ++i) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+    if (v >= target) return true;
   }
   return false;
 }

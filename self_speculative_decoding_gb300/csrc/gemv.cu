@@ -118,13 +118,13 @@ GemvScratch gemv_scratch(int R, int K, int epi) {
   const Part p = make_part(R, K, epi);
   GemvScratch s;
   s.part_floats = (size_t)p.NRG * p.segmax * 256;
-  const int nb = (p.NRG + kLmBlock - 1) / kLmBlock;
-  s.counters = (size_t)p.NRG + nb + 1;
-  s.rec_floats = epi == EPI_LMHEAD ? (size_t)(p.NRG + nb) * kMaxRows * 8 : 0;
+  s.counters = (size_t)p.NRG + 1;
+  s.rec_floats = epi == EPI_LMHEAD ? (size_t)p.C * kMaxRows * 8 : 0;
   return s;
 }
 
 cudaError_t launch_gemv(int in_mode, int epi, const LinearArgs& a, cudaStream_t st, bool pdl) {
+  if (!part_fits(a.R, a.K)) return cudaErrorInvalidValue;
   const Part p = make_part(a.R, a.K, epi);
 #define SSD_GEMV_CASE(I, E) \
   if (in_mode == I && epi == E) return launch_one<I, E>(a, p, st, pdl);

@@ -44,43 +44,65 @@ constexpr int kUPW = (kChunk + kConsumers - 1) / kConsumers;  // units per warp 
 constexpr int kUnitBytes = 1024;
 constexpr int kSlotBytes = kChunk * kUnitBytes;
 constexpr int kRingBytes = kSlots * kSlotBytes;
-constexpr int kLmBlock = 32;                     // LM-head row groups per level-2 block
 // Activations (the B operand, bf16 and already normalised for the norm-fused
 // input) are staged once per CTA when M rows of K fit in this budget; this
 // covers every single-token pass of the 7B and 13B shapes.
 constexpr int kStageBytes = SSD_GEMV_STAGE_KB * 1024;
 constexpr int kPad = 8;                          // bf16 row padding of the stage
 
+// Partition of a GEMV's T units over C CTAs: CTA b owns the contiguous
+// granules [b*Tg/C, (b+1)*Tg/C), a granule being G units.  Projections use
+// single units (G = 1: equal shares, row groups may straddle CTAs); the LM
+// head uses whole row groups (G = KB) so that every CTA summarises complete
+// vocabulary rows on its own.
 struct Part {
-  long long T;  // units = NRG * KB
-  int NRG;      // (virtual) 16-row groups
-  int KB;       // 32-wide K blocks
-  int C;        // CTAs with work = min(kGridCtas, T)
-  int segmax;   // stride of the partial buffer per row group
+  int T;       // units = NRG * KB
+  int Tg;      // granules = T / G
+  int NRG;     // (virtual) 16-row groups
+  int KB;      // 32-wide K blocks
+  int G;       // units per granule
+  int C;       // CTAs with work = min(kGridCtas, Tg)
+  int segmax;  // stride of the partial buffer per row group
 };
 
-__host__ __device__ inline long long unit_begin(const Part& p, int b) {
-  return (long long)b * p.T / p.C;
+// All partition arithmetic is 32-bit unsigned: launch_gemv refuses shapes
+// with T * (kGridCtas + 1) >= 2^32 (far beyond any decoder projection).
+__host__ __device__ inline int unit_begin(const Part& p, int b) {
+  return (int)((unsigned)b * (unsigned)p.Tg / (unsigned)p.C) * p.G;
 }
-// first / last CTA whose unit range intersects units [a, b)
-__host__ __device__ inline int cta_first(const Part& p, long long a) {
-  return (int)(((a + 1) * p.C + p.T - 1) / p.T) - 1;
+// first CTA whose range contains unit a / last CTA whose range meets [.., b)
+__host__ __device__ inline int cta_first(const Part& p, int a) {
+  const unsigned ga = (unsigned)(a / p.G);
+  return (int)(((ga + 1u) * (unsigned)p.C + (unsigned)p.Tg - 1u) / (unsigned)p.Tg) - 1;
 }
-__host__ __device__ inline int cta_last(const Part& p, long long b) {
-  return (int)((b * p.C + p.T - 1) / p.T) - 1;
+__host__ __device__ inline int cta_last(const Part& p, int b) {
+  const unsigned gb = (unsigned)((b + p.G - 1) / p.G);
+  return (int)((gb * (unsigned)p.C + (unsigned)p.Tg - 1u) / (unsigned)p.Tg) - 1;
 }
 __host__ __device__ inline int nseg(const Part& p, int vr) {
-  return cta_last(p, (long long)(vr + 1) * p.KB) - cta_first(p, (long long)vr * p.KB) + 1;
+  return cta_last(p, (vr + 1) * p.KB) - cta_first(p, vr * p.KB) + 1;
+}
+// row group vr lies entirely in CTA b's range
+__host__ __device__ inline bool owns(const Part& p, int vr, int b) {
+  return cta_first(p, vr * p.KB) == b && cta_last(p, (vr + 1) * p.KB) == b;
 }
 
 __host__ __device__ inline Part make_part(int R, int K, int epi) {
   Part p;
   p.NRG = (epi == EPI_SWIGLU ? 2 : 1) * (R / 16);
   p.KB = K / 32;
-  p.T = (long long)p.NRG * p.KB;
-  p.C = (int)(p.T < kGridCtas ? p.T : kGridCtas);
+  p.T = p.NRG * p.KB;
+  p.G = epi == EPI_LMHEAD ? p.KB : 1;
+  p.Tg = p.T / p.G;
+  p.C = p.Tg < kGridCtas ? p.Tg : kGridCtas;
   p.segmax = (p.C + p.NRG - 1) / p.NRG + 1;
   return p;
+}
+
+// Shapes whose partition arithmetic fits 32 bits.
+inline bool part_fits(int R, int K) {
+  const unsigned long long T = 2ull * (unsigned long long)(R / 16) * (unsigned long long)(K / 32);
+  return T * (unsigned long long)(kGridCtas + 1) < (1ull << 32);
 }
 
 // Unit (vr, kb) in the packed stream of its matrix.
@@ -233,11 +255,32 @@ SSD_DI LmRec lm_merge_warp(LmRec r, float T) {
 
 // Runs in one warp once row group vr (or the gate/up pair containing it) is
 // complete; ep[h][row][tok] holds the finished sums.
-// Returns true when the call completes one signalled unit of the phase (a
-// row group, a gate/up pair, or the whole LM-head summary).
+// (Projections only; the LM head goes through lm_group / lm_finish.)
+// Returns true: the call completes one signalled unit of the phase (a row
+// group or a gate/up pair).
+// Residual entries lane + 32 i of a row group (EPI_RESID), loaded ahead of
+// the group's completion so that their latency is off the tail.
+struct XPre {
+  float v[kMaxRows * 16 / 32];
+};
+
+template <int EPI>
+SSD_DI void xres_prefetch(const LinearArgs& a, int vr, int M, int lane, XPre& xp) {
+  if (EPI == EPI_RESID) {
+#pragma unroll
+    for (int i = 0; i < kMaxRows * 16 / 32; ++i) {
+      const int e = lane + 32 * i;
+      if (e < 16 * M) {
+        const int row = e / M, tok = e % M;
+        xp.v[i] = __ldcg(a.xres + (size_t)tok * a.R + vr * 16 + row);
+      }
+    }
+  }
+}
+
 template <int EPI>
 SSD_DI bool epilogue(const LinearArgs& a, const Part& p, int vr, float (*ep)[16][17], int M,
-                     int lane) {
+                     int lane, const XPre& xp) {
   if (EPI == EPI_STORE) {
     const int row0 = vr * 16;
     for (int e = lane; e < 16 * M; e += 32) {
@@ -246,12 +289,15 @@ SSD_DI bool epilogue(const LinearArgs& a, const Part& p, int vr, float (*ep)[16]
     }
   } else if (EPI == EPI_RESID) {
     const int row0 = vr * 16;
-    for (int e = lane; e < 16 * M; e += 32) {
-      const int row = e / M, tok = e % M;
-      const size_t idx = (size_t)tok * a.R + row0 + row;
-      const float xn = __ldcg(a.xres + idx) + ep[0][row][tok];
-      a.xres[idx] = xn;
-      ep[0][row][tok] = xn;
+#pragma unroll
+    for (int i = 0; i < kMaxRows * 16 / 32; ++i) {
+      const int e = lane + 32 * i;
+      if (e < 16 * M) {
+        const int row = e / M, tok = e % M;
+        const float xn = xp.v[i] + ep[0][row][tok];
+        a.xres[(size_t)tok * a.R + row0 + row] = xn;
+        ep[0][row][tok] = xn;
+      }
     }
     __syncwarp();
     if (lane < M) {
@@ -268,101 +314,109 @@ SSD_DI bool epilogue(const LinearArgs& a, const Part& p, int vr, float (*ep)[16]
       const float sl = gt / (1.0f + expf(-gt));
       a.u[(size_t)tok * a.R + row0 + row] = __float2bfloat16_rn(sl * up);
     }
-  } else if (EPI == EPI_LMHEAD) {
-    const int slot = a.slot_dev ? *a.slot_dev : 0;
-    const int row0 = vr * 16;
-    const float T = a.temperature;
-    if (a.logits) {
-      for (int e = lane; e < 16 * M; e += 32) {
-        const int row = e / M, tok = e % M;
-        a.logits[(size_t)(slot + tok) * a.R + row0 + row] = ep[0][row][tok];
-      }
-    }
-    const int round = a.round_dev ? *a.round_dev : a.round_static;
-    const int pos0 = a.pos0_dev ? *a.pos0_dev : a.pos0_static;
-    // level 1: this group's 16 rows in order, one lane per token
-    if (lane < M) {
-      LmRec r = lm_empty();
-      for (int row = 0; row < 16; ++row) {
-        const float z = ep[0][row][lane];
-        top2_insert(z, row0 + row, r.v1, r.i1, r.v2, r.i2);
-        if (T > 0.f && a.sample) {
-          const float sc =
-              z / T + gumbel_at(a.seed, row0 + row, pos0 + lane + 1, round, a.sample_stream);
-          if (better(sc, row0 + row, r.gv, r.gi)) { r.gv = sc; r.gi = row0 + row; }
-        }
-      }
-      for (int row = 0; row < 16; ++row) {
-        const float z = ep[0][row][lane];
-        r.se += expf(z - r.v1);
-        if (T > 0.f) r.set += expf(z / T - r.v1 / T);
-      }
-      lm_store(a.rec + ((size_t)vr * kMaxRows + lane) * 8, r);
-    }
-    __threadfence();
-    __syncwarp();
-    // level 2: blocks of kLmBlock consecutive groups
-    const int nb = (p.NRG + kLmBlock - 1) / kLmBlock;
-    const int blk = vr / kLmBlock;
-    const int blk_n = min(kLmBlock, p.NRG - blk * kLmBlock);
-    unsigned* c2 = a.counter + p.NRG;
-    int last2 = 0;
-    if (lane == 0) last2 = atomicAdd(c2 + blk, 1u) == (unsigned)(blk_n - 1);
-    last2 = __shfl_sync(0xffffffffu, last2, 0);
-    if (!last2) return false;
-    __threadfence();
-    float* rec2 = a.rec + (size_t)p.NRG * kMaxRows * 8;
-    for (int tok = 0; tok < M; ++tok) {
-      const int gi = blk * kLmBlock + lane;
-      LmRec r = lane < blk_n ? lm_load(a.rec + ((size_t)gi * kMaxRows + tok) * 8) : lm_empty();
-      r = lm_merge_warp(r, T);
-      if (lane == 0) lm_store(rec2 + ((size_t)blk * kMaxRows + tok) * 8, r);
-    }
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) c2[blk] = 0u;
-    int last3 = 0;
-    if (lane == 0) last3 = atomicAdd(c2 + nb, 1u) == (unsigned)(nb - 1);
-    last3 = __shfl_sync(0xffffffffu, last3, 0);
-    if (!last3) return false;
-    __threadfence();
-    // level 3: all blocks; lane b folds blocks b, b+32, ... in order
-    for (int tok = 0; tok < M; ++tok) {
-      LmRec r = lm_empty();
-      for (int b = lane; b < nb; b += 32) {
-        const LmRec q = lm_load(rec2 + ((size_t)b * kMaxRows + tok) * 8);
-        const float mx = fmaxf(r.v1, q.v1);
-        const float se =
-            (r.v1 == -INFINITY ? 0.f : r.se * expf(r.v1 - mx)) + q.se * expf(q.v1 - mx);
-        float set = 0.f;
-        if (T > 0.f)
-          set = (r.v1 == -INFINITY ? 0.f : r.set * expf(r.v1 / T - mx / T)) +
-                q.set * expf(q.v1 / T - mx / T);
-        top2_insert(q.v1, q.i1, r.v1, r.i1, r.v2, r.i2);
-        top2_insert(q.v2, q.i2, r.v1, r.i1, r.v2, r.i2);
-        if (better(q.gv, q.gi, r.gv, r.gi)) { r.gv = q.gv; r.gi = q.gi; }
-        r.se = se;
-        r.set = set;
-      }
-      r = lm_merge_warp(r, T);
-      if (lane == 0) {
-        RowStats rs;
-        rs.top1 = r.i1;
-        rs.top2 = r.i2;
-        rs.sample = T > 0.f && a.sample ? r.gi : r.i1;
-        rs.pad = 0;
-        rs.z1 = r.v1;
-        rs.z2 = r.v2;
-        rs.lse = r.v1 + logf(r.se);
-        rs.conf = expf(r.v1 - rs.lse);
-        rs.lse_t = T > 0.f ? r.v1 / T + logf(r.set) : rs.lse;
-        rs.pad2[0] = rs.pad2[1] = rs.pad2[2] = 0.f;
-        a.stats[slot + tok] = rs;
-      }
-    }
-    if (lane == 0) c2[nb] = 0u;
-    return true;
   }
+  return true;
+}
+
+// Folds record q into r: top-2 and the Gumbel argmax under the total order,
+// the exponential sums rescaled to the larger maximum.
+SSD_DI void lm_combine(LmRec& r, const LmRec& q, float T) {
+  if (q.v1 == -INFINITY) return;
+  const float mx = fmaxf(r.v1, q.v1);
+  const float se = (r.v1 == -INFINITY ? 0.f : r.se * expf(r.v1 - mx)) + q.se * expf(q.v1 - mx);
+  float set = 0.f;
+  if (T > 0.f)
+    set = (r.v1 == -INFINITY ? 0.f : r.set * expf(r.v1 / T - mx / T)) +
+          q.set * expf(q.v1 / T - mx / T);
+  top2_insert(q.v1, q.i1, r.v1, r.i1, r.v2, r.i2);
+  top2_insert(q.v2, q.i2, r.v1, r.i1, r.v2, r.i2);
+  if (better(q.gv, q.gi, r.gv, r.gi)) { r.gv = q.gv; r.gi = q.gi; }
+  r.se = se;
+  r.set = set;
+}
+
+// LM head, one finished row group (16 vocabulary rows in ep[0]): optional
+// logits, then lane tok < M folds the group's rows, in row order, into its
+// running record `run` (the CTA's vocabulary range so far).
+SSD_DI void lm_group(const LinearArgs& a, int vr, float (*ep)[16][17], int M, int lane, int slot,
+                     int round, int pos0, LmRec& run) {
+  const int row0 = vr * 16;
+  const float T = a.temperature;
+  if (a.logits) {
+    for (int e = lane; e < 16 * M; e += 32) {
+      const int row = e / M, tok = e % M;
+      a.logits[(size_t)(slot + tok) * a.R + row0 + row] = ep[0][row][tok];
+    }
+  }
+  if (lane < M) {
+    LmRec r = lm_empty();
+    for (int row = 0; row < 16; ++row) {
+      const float z = ep[0][row][lane];
+      top2_insert(z, row0 + row, r.v1, r.i1, r.v2, r.i2);
+      if (T > 0.f && a.sample) {
+        const float sc =
+            z / T + gumbel_at(a.seed, row0 + row, pos0 + lane + 1, round, a.sample_stream);
+        if (better(sc, row0 + row, r.gv, r.gi)) { r.gv = sc; r.gi = row0 + row; }
+      }
+    }
+    for (int row = 0; row < 16; ++row) {
+      const float z = ep[0][row][lane];
+      r.se += expf(z - r.v1);
+      if (T > 0.f) r.set += expf(z / T - r.v1 / T);
+    }
+    lm_combine(run, r, T);
+  }
+}
+
+// LM head, end of CTA b's range: publish the CTA's records (one per token,
+// stored [tok][b]); the CTA that publishes last folds all CTAs' records in
+// CTA order and writes the row summaries.  `stage` holds C records.
+// Returns true in the CTA that wrote the summaries.
+SSD_DI bool lm_finish(const LinearArgs& a, const Part& p, int b, int M, int lane, int slot,
+                      const LmRec& run, float* stage) {
+  const float T = a.temperature;
+  if (lane < M) lm_store(a.rec + ((size_t)lane * p.C + b) * 8, run);
+  __threadfence();
+  __syncwarp();
+  int last = 0;
+  if (lane == 0) last = atomicAdd(a.counter, 1u) == (unsigned)(p.C - 1);
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return false;
+  __threadfence();
+  for (int tok = 0; tok < M; ++tok) {
+    // all C records of this token into shared memory (independent loads)
+    const float4* src = reinterpret_cast<const float4*>(a.rec + (size_t)tok * p.C * 8);
+    float4* dst = reinterpret_cast<float4*>(stage);
+#pragma unroll 4
+    for (int i = lane; i < 2 * p.C; i += 32) dst[i] = __ldcg(src + i);
+    __syncwarp();
+    // lane l folds CTAs l, l+32, ... in order, then a butterfly
+    LmRec r = lm_empty();
+    for (int c = lane; c < p.C; c += 32) {
+      const float4 x0 = dst[2 * c], x1 = dst[2 * c + 1];
+      LmRec q;
+      q.v1 = x0.x; q.i1 = __float_as_int(x0.y); q.v2 = x0.z; q.i2 = __float_as_int(x0.w);
+      q.se = x1.x; q.set = x1.y; q.gv = x1.z; q.gi = __float_as_int(x1.w);
+      lm_combine(r, q, T);
+    }
+    r = lm_merge_warp(r, T);
+    if (lane == 0) {
+      RowStats rs;
+      rs.top1 = r.i1;
+      rs.top2 = r.i2;
+      rs.sample = T > 0.f && a.sample ? r.gi : r.i1;
+      rs.pad = 0;
+      rs.z1 = r.v1;
+      rs.z2 = r.v2;
+      rs.lse = r.v1 + logf(r.se);
+      rs.conf = expf(r.v1 - rs.lse);
+      rs.lse_t = T > 0.f ? r.v1 / T + logf(r.set) : rs.lse;
+      rs.pad2[0] = rs.pad2[1] = rs.pad2[2] = 0.f;
+      a.stats[slot + tok] = rs;
+    }
+    __syncwarp();
+  }
+  if (lane == 0) a.counter[0] = 0u;
   return true;
 }
 
@@ -398,7 +452,7 @@ SSD_DI int chunk_len(const Part& p, int kb, int left) {
 // Consumer warps: take the ring's slots in order, one unit per warp per
 // slot, and hand each finished row-group segment to the epilogue warp.
 template <int IN, int EPI, bool STAGED>
-SSD_DI void consume(const LinearArgs& a, const Part& p, GemvSmem& sm, long long U0, long long U1,
+SSD_DI void consume(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0, int U1,
                     int M, int warp, int lane, RingPos& rp) {
   const int g = lane >> 2, c = lane & 3;
   const bool two = M > 8;
@@ -406,7 +460,7 @@ SSD_DI void consume(const LinearArgs& a, const Part& p, GemvSmem& sm, long long 
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
   const float rs0 = IN == IN_NORM && v0 && !STAGED ? sm.rstd[g] : 0.f;
   const float rs1 = IN == IN_NORM && v1 && !STAGED ? sm.rstd[g + 8] : 0.f;
-  int vr = (int)(U0 / p.KB), kb = (int)(U0 % p.KB), left = (int)(U1 - U0);
+  int vr = U0 / p.KB, kb = U0 % p.KB, left = U1 - U0;
   int n = left > 0 ? chunk_len(p, kb, left) : 0;
   BRaw<IN> ra[kUPW], rb[kUPW];
   if (!STAGED) {
@@ -514,8 +568,11 @@ template <int EPI>
 SSD_DI void producer_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int b, int lane,
                            RingPos& rp) {
   if (b >= p.C || lane != 0 || !rp.ok) return;
-  const long long U0 = unit_begin(p, b), U1 = unit_begin(p, b + 1);
-  int vr = (int)(U0 / p.KB), kb = (int)(U0 % p.KB), left = (int)(U1 - U0);
+  // the RMSNorm gain is the one input the consumers read from DRAM: bring
+  // it into L2 ahead of this CTA's weight stream
+  if (a.gain && b == 0) bulk_prefetch_l2(a.gain, (uint32_t)(a.K * sizeof(float)));
+  const int U0 = unit_begin(p, b), U1 = unit_begin(p, b + 1);
+  int vr = U0 / p.KB, kb = U0 % p.KB, left = U1 - U0;
   while (left > 0) {
     const int n = chunk_len(p, kb, left);
     if (rp.t >= kSlots && !mbar_wait(&sm.empty[rp.slot], rp.ph ^ 1u)) {
@@ -534,73 +591,150 @@ SSD_DI void producer_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int
   }
 }
 
-// Epilogue warp: receives CTA b's row-group segments of one GEMV in order,
-// writes the CTA's partial, and finishes the groups it completes last.
+// Epilogue warp: receives CTA b's row-group segments of one GEMV in order.
+// A row group that lies wholly in this CTA (for SwiGLU: both groups of the
+// gate/up pair) is finished straight from shared memory.  A group split
+// across CTAs is finished by the last CTA to complete it: each CTA stores its
+// partial, and the finisher sums the partials in CTA order.  Either way a
+// group's sum is its CTAs' partials added in CTA order, each partial being
+// the consumer warps' sums added in warp order, so the result depends on the
+// matrix shape only.  The LM head (whole-group partition) folds its groups
+// into one running record per token and publishes it at the end.
 // `done` (nullable) counts finished row groups (gate/up pairs; 1 for the LM
 // head) for the persistent pass kernel.
 template <int EPI>
 SSD_DI void epilogue_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int b, int M,
                            int lane, RingPos& rp, unsigned* done) {
-  if (b >= p.C) return;
-  const long long U0 = unit_begin(p, b), U1 = unit_begin(p, b + 1);
-  if (!rp.ok) return;
-  int vr = (int)(U0 / p.KB), kb = (int)(U0 % p.KB), left = (int)(U1 - U0);
+  if (b >= p.C || !rp.ok) return;
+  const int U0 = unit_begin(p, b), U1 = unit_begin(p, b + 1);
+  int vr = U0 / p.KB, kb = U0 % p.KB, left = U1 - U0;
+  LmRec run = lm_empty();
+  int slot = 0, round = 0, pos0 = 0;
+  if (EPI == EPI_LMHEAD) {
+    slot = a.slot_dev ? __ldcg(a.slot_dev) : 0;
+    round = a.round_dev ? __ldcg(a.round_dev) : a.round_static;
+    pos0 = a.pos0_dev ? __ldcg(a.pos0_dev) : a.pos0_static;
+  }
   for (; left > 0; ++rp.fl) {
-      const int fl = rp.fl;
-      const int gvr = vr;
-      left -= p.KB - kb < left ? p.KB - kb : left;
-      kb = 0;
-      ++vr;
-      const int buf = fl & 1;
-      if (!mbar_wait(&sm.rfull[buf], (fl >> 1) & 1)) {
-        if (lane == 0) atomicExch(a.err, 4);
-        rp.ok = false;
-        return;
-      }
-      // this CTA's partial of the group: the consumer warps summed in order
-      const int seg = b - cta_first(p, (long long)gvr * p.KB);
-      float* dst = a.part + ((size_t)gvr * p.segmax + seg) * 256;
+    const int fl = rp.fl;
+    const int gvr = vr;
+    left -= p.KB - kb < left ? p.KB - kb : left;
+    kb = 0;
+    ++vr;
+    const int buf = fl & 1;
+    XPre xp;
+    xres_prefetch<EPI>(a, gvr, M, lane, xp);
+    if (!mbar_wait(&sm.rfull[buf], (fl >> 1) & 1)) {
+      if (lane == 0) atomicExch(a.err, 4);
+      rp.ok = false;
+      return;
+    }
+    const bool whole = EPI == EPI_LMHEAD ||
+                       (owns(p, gvr, b) && (EPI != EPI_SWIGLU || owns(p, gvr ^ 1, b)));
+    if (whole) {
+      const int h = EPI == EPI_SWIGLU ? (gvr & 1) : 0;
       for (int e = lane; e < 16 * M; e += 32) {
         const int row = e / M, tok = e % M;
         float s2 = 0.f;
         for (int w2 = 0; w2 < kConsumers; ++w2) s2 += sm.red[buf][w2][row][tok];
-        dst[row * 16 + tok] = s2;
+        sm.ep[h][row][tok] = 0.f + s2;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.rempty[buf]);
-      __threadfence();
-      __syncwarp();
-      const int cidx = EPI == EPI_SWIGLU ? gvr >> 1 : gvr;
-      int last = 0;
-      if (lane == 0) {
-        int expect = nseg(p, gvr);
-        if (EPI == EPI_SWIGLU) expect += nseg(p, gvr ^ 1);
-        last = atomicAdd(a.counter + cidx, 1u) == (unsigned)(expect - 1);
-      }
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (!last) continue;
-      __threadfence();
-      // sum the CTAs' partials of the group(s) in CTA order
-      const int ngrp = EPI == EPI_SWIGLU ? 2 : 1;
-      for (int h = 0; h < ngrp; ++h) {
-        const int gv = EPI == EPI_SWIGLU ? ((gvr & ~1) | h) : gvr;
-        const int ns = nseg(p, gv);
-        const float* src = a.part + (size_t)gv * p.segmax * 256;
-        for (int e = lane; e < 16 * M; e += 32) {
-          const int row = e / M, tok = e % M;
-          float s2 = 0.f;
-          for (int sg = 0; sg < ns; ++sg) s2 += __ldcg(src + (size_t)sg * 256 + row * 16 + tok);
-          sm.ep[h][row][tok] = s2;
-        }
+      if (EPI == EPI_SWIGLU && h == 0) continue;  // the up group follows
+      bool fin;
+      if (EPI == EPI_LMHEAD) {
+        lm_group(a, gvr, sm.ep, M, lane, slot, round, pos0, run);
+        fin = false;
+      } else {
+        fin = epilogue<EPI>(a, p, gvr, sm.ep, M, lane, xp);
       }
       __syncwarp();
-      if (lane == 0) a.counter[cidx] = 0u;
-      const bool fin = epilogue<EPI>(a, p, gvr, sm.ep, M, lane);
-      __syncwarp();
-      if (done && fin && lane == 0) {
+      if (done && fin) {
         __threadfence();
-        atomicAdd(done, 1u);
+        if (lane == 0) atomicAdd(done, 1u);
       }
+      continue;
+    }
+    // ---- split group (pair): every CTA stores its partial; the CTA that
+    // holds the first unit (F) finishes, the others only publish.  F's own
+    // segments of the group are its last ones and the others' are their
+    // first ones, so F waits for work that needs nothing from F.
+    const int seg = b - cta_first(p, gvr * p.KB);
+    float* dst = a.part + ((size_t)gvr * p.segmax + seg) * 256;
+    for (int e = lane; e < 16 * M; e += 32) {
+      const int row = e / M, tok = e % M;
+      float s2 = 0.f;
+      for (int w2 = 0; w2 < kConsumers; ++w2) s2 += sm.red[buf][w2][row][tok];
+      dst[row * 16 + tok] = s2;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.rempty[buf]);
+    const int g0 = EPI == EPI_SWIGLU ? (gvr & ~1) : gvr;
+    const int F = cta_first(p, g0 * p.KB);
+    const int cidx = EPI == EPI_SWIGLU ? gvr >> 1 : gvr;
+    if (b != F) {
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) red_release_add(a.counter + cidx, 1u);
+      continue;
+    }
+    if (EPI == EPI_SWIGLU && (gvr & 1) == 0 && left > 0) continue;  // F's up segment follows
+    const int ngrp = EPI == EPI_SWIGLU ? 2 : 1;
+    int expect = 0;
+    for (int hh = 0; hh < ngrp; ++hh) {
+      const int gv = g0 + hh;
+      expect += nseg(p, gv) - (cta_first(p, gv * p.KB) == F ? 1 : 0);
+    }
+    int ok = 1;
+    if (lane == 0) ok = wait_count(a.counter + cidx, (unsigned)expect);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) {
+      if (lane == 0) atomicExch(a.err, 6);
+      rp.ok = false;
+      return;
+    }
+    // sum the CTAs' partials of the group(s) in CTA order; the loads of up
+    // to four segments of both groups are issued before any is used
+    int ns[2];
+    ns[0] = nseg(p, g0);
+    ns[1] = ngrp > 1 ? nseg(p, g0 + 1) : 0;
+    for (int e = lane; e < 16 * M; e += 32) {
+      const int row = e / M, tok = e % M;
+      float v[2][4];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const float* src = a.part + (size_t)(g0 + hh) * p.segmax * 256 + row * 16 + tok;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[hh][q] = q < ns[hh] ? __ldcg(src + (size_t)q * 256) : 0.f;
+      }
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        if (hh >= ngrp) break;
+        const float* src = a.part + (size_t)(g0 + hh) * p.segmax * 256 + row * 16 + tok;
+        float s2 = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (q < ns[hh]) s2 += v[hh][q];
+        for (int q = 4; q < ns[hh]; ++q) s2 += __ldcg(src + (size_t)q * 256);
+        sm.ep[hh][row][tok] = s2;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) a.counter[cidx] = 0u;
+    const bool fin = epilogue<EPI>(a, p, gvr, sm.ep, M, lane, xp);
+    __syncwarp();
+    if (done && fin) {
+      __threadfence();
+      if (lane == 0) atomicAdd(done, 1u);
+    }
+  }
+  if (EPI == EPI_LMHEAD) {
+    const bool fin = lm_finish(a, p, b, M, lane, slot, run, reinterpret_cast<float*>(sm.stage));
+    if (done && fin && lane == 0) {
+      __threadfence();
+      atomicAdd(done, 1u);
+    }
   }
 }
 
@@ -610,29 +744,53 @@ template <int IN, int EPI>
 SSD_DI void consumer_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int b, int M,
                            int warp, int lane, RingPos& rp) {
   if (b >= p.C) return;
-  const long long U0 = unit_begin(p, b), U1 = unit_begin(p, b + 1);
+  const int U0 = unit_begin(p, b), U1 = unit_begin(p, b + 1);
   if (!rp.ok) return;
+  const bool staged = (size_t)M * (a.K + kPad) * sizeof(bf16) <= (size_t)kStageBytes;
+  const int vpr = a.K / 8;  // 16-byte pieces per row
+  const int nst = staged ? M * vpr : 0;
+  constexpr int kPre = IN == IN_NORM ? 2 : 4;
+  constexpr int kStride = kConsumers * 32;
+  // the first pieces' loads go out together with the statistics' loads
+  BRaw<IN> pre[kPre];
+  int e0 = threadIdx.x;
+#pragma unroll
+  for (int i = 0; i < kPre; ++i) {
+    const int e = e0 + i * kStride;
+    if (e < nst) b_issue<IN>(pre[i], a, e / vpr, (e % vpr) * 8, true);
+  }
   if (IN == IN_NORM) {
     // 1 / sqrt(mean(x^2) + eps) per row from the producer's partials, in a
     // fixed order: lane l sums partials l, l+32, ... then a butterfly.
     const int NP = a.K / kSsGroup;
     for (int m = warp; m < M; m += kConsumers) {
       float s2 = 0.f;
+#pragma unroll 8
       for (int q = lane; q < NP; q += 32) s2 += __ldcg(a.ss + (size_t)m * NP + q);
       s2 = sum_warp(s2);
       if (lane == 0) sm.rstd[m] = 1.0f / sqrtf(s2 / (float)a.K + a.eps);
     }
     consumer_sync();
   }
-  const bool staged = (size_t)M * (a.K + kPad) * sizeof(bf16) <= (size_t)kStageBytes;
   if (staged) {
-    const int vpr = a.K / 8;   // 16-byte pieces per row
-    for (int e = threadIdx.x; e < M * vpr; e += kConsumers * 32) {
-      const int m = e / vpr, q = e % vpr;
-      BRaw<IN> r;
-      b_issue<IN>(r, a, m, q * 8, true);
-      const float rs = IN == IN_NORM ? sm.rstd[m] : 0.f;
-      *reinterpret_cast<uint4*>(sm.stage + (size_t)m * (a.K + kPad) + q * 8) = b_finish<IN>(r, rs);
+    for (;;) {
+#pragma unroll
+      for (int i = 0; i < kPre; ++i) {
+        const int e = e0 + i * kStride;
+        if (e < nst) {
+          const int m = e / vpr;
+          const float rs = IN == IN_NORM ? sm.rstd[m] : 0.f;
+          *reinterpret_cast<uint4*>(sm.stage + (size_t)m * (a.K + kPad) + (e % vpr) * 8) =
+              b_finish<IN>(pre[i], rs);
+        }
+      }
+      e0 += kPre * kStride;
+      if (e0 >= nst) break;
+#pragma unroll
+      for (int i = 0; i < kPre; ++i) {
+        const int e = e0 + i * kStride;
+        if (e < nst) b_issue<IN>(pre[i], a, e / vpr, (e % vpr) * 8, true);
+      }
     }
     consumer_sync();
     consume<IN, EPI, true>(a, p, sm, U0, U1, M, warp, lane, rp);
