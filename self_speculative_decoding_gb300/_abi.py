@@ -88,6 +88,7 @@ _SIGS = {
     "ssd_rewind": [_P, _I],
     "ssd_get_tokens": [_P, C.POINTER(_I), _I, C.POINTER(_I)],
     "ssd_set_timeout_ms": [_P, _I],
+    "ssd_set_pass_kernel": [_P, _I, C.POINTER(C.c_int32)],
     "ssd_profile_decode": [_P, _I, C.POINTER(SsdKernelTimes)],
     "ssd_last_error": [_P],
     "ssd_op_linear": [_P, _I, _I, _P, _I, _P, _P],

@@ -43,7 +43,8 @@ struct DevState {
   int32_t slot;     // output slot of the current pass (draft step index)
   int32_t n_emitted;
   int32_t accepted;
-  int32_t pad[6];
+  int32_t err;      // non-zero: a device-side wait gave up (its code)
+  int32_t pad[5];
   int32_t in_tok[kMaxRows];
   int32_t draft_tok[kMaxRows];
   float draft_conf[kMaxRows];

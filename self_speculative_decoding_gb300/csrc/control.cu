@@ -4,7 +4,7 @@
 // that a captured CUDA graph of a draft step, a verify pass or an
 // autoregressive step can be replayed for every step without host-side
 // argument changes.
-#include "kernels.cuh"
+#include "control_dev.cuh"
 
 namespace ssd {
 
@@ -13,115 +13,31 @@ namespace {
 constexpr int kBeginThreads = 512;
 constexpr int kAcceptThreads = 1024;
 
-// Embedding (or boundary copy) of the pass's rows, with the sum-of-squares
-// partials of every 16-column group (the same order the projection
-// epilogues use: ascending columns from zero).
 __global__ void __launch_bounds__(kBeginThreads) begin_kernel(BeginArgs a) {
   __shared__ int s_M, s_tok[kMaxRows];
   pdl_wait();
   pdl_trigger();
-  DevState* st = a.st;
-  if (threadIdx.x == 0) {
-    int M = 1, pos0 = 0, slot = 0;
-    switch (a.mode) {
-      case BEGIN_TOKENS:
-        M = a.M;
-        pos0 = a.pos0;
-        for (int m = 0; m < M; ++m) s_tok[m] = a.toks_in[m];
-        if (a.reset_round) {
-          st->round = 0;
-          st->j = st->d = st->stop = 0;
-        }
-        break;
-      case BEGIN_AR:
-        st->round += 1;
-        pos0 = st->n - 1;
-        s_tok[0] = a.tokens[st->n - 1];
-        break;
-      case BEGIN_DRAFT:
-        if (st->j == 0) st->round += 1;
-        pos0 = st->n - 1 + st->j;
-        s_tok[0] = st->j == 0 ? a.tokens[st->n - 1] : st->draft_tok[st->j - 1];
-        slot = st->j;
-        break;
-      case BEGIN_EXTRA:
-        pos0 = st->n - 1 + st->d;
-        s_tok[0] = st->d > 0 ? st->draft_tok[st->d - 1] : a.tokens[st->n - 1];
-        break;
-      case BEGIN_VERIFY:
-        M = st->d + 1;
-        pos0 = st->n - 1;
-        break;
-    }
-    st->M = M;
-    st->pos0 = pos0;
-    st->slot = slot;
-    if (a.mode != BEGIN_VERIFY)
-      for (int m = 0; m < M; ++m) st->in_tok[m] = s_tok[m];
-    s_M = M;
-  }
-  __syncthreads();
-  const int M = s_M, D = a.D, NP = D / kSsGroup;
-  if (a.mode == BEGIN_VERIFY) {
-    for (int e = threadIdx.x; e < M * D; e += kBeginThreads) a.x[e] = a.bx[e];
-    for (int e = threadIdx.x; e < M * NP; e += kBeginThreads) a.ss[e] = a.bss[e];
-    return;
-  }
-  for (int e = threadIdx.x; e < M * NP; e += kBeginThreads) {
-    const int m = e / NP, grp = e % NP;
-    const bf16* src = a.embed + (size_t)s_tok[m] * D + grp * kSsGroup;
-    float* dst = a.x + (size_t)m * D + grp * kSsGroup;
-    float s = 0.f;
-    for (int i = 0; i < kSsGroup; ++i) {
-      const float v = __bfloat162float(src[i]);
-      dst[i] = v;
-      s += v * v;
-    }
-    a.ss[(size_t)m * NP + grp] = s;
-  }
+  ctl::begin(a, threadIdx.x, kBeginThreads, &s_M, s_tok, [] { __syncthreads(); });
 }
 
 __global__ void save_boundary_kernel(DevState* st, int use_d, const float* x, const float* ss,
                                      float* bx, float* bss, int D) {
   pdl_wait();
   pdl_trigger();
-  const int slot = use_d ? st->d : st->j;
-  const int NP = D / kSsGroup;
-  for (int e = threadIdx.x; e < D; e += blockDim.x) bx[(size_t)slot * D + e] = x[e];
-  for (int e = threadIdx.x; e < NP; e += blockDim.x) bss[(size_t)slot * NP + e] = ss[e];
+  ctl::save_boundary(st, use_d, x, ss, bx, bss, D, threadIdx.x, blockDim.x);
 }
 
-// SWIFT §4.2 confidence-aware stop: the draft token of step j is kept only
-// if its top-1 probability reaches tau.
 __global__ void draft_end_kernel(DevState* st, const RowStats* dstats, float tau, float T) {
   pdl_wait();
   pdl_trigger();
-  const int j = st->j;
-  const RowStats rs = dstats[j];
-  st->draft_conf[j] = rs.conf;
-  if (rs.conf < tau) {
-    st->stop = 1;
-  } else {
-    st->draft_tok[j] = T > 0.f ? rs.sample : rs.top1;
-    st->d = j + 1;
-  }
-  st->j = j + 1;
+  if (threadIdx.x == 0) ctl::draft_end(st, dstats, tau, T);
 }
 
-// Commit the token the full model produced for the last row of the pass.
 __global__ void ar_end_kernel(DevState* st, int32_t* tokens, const RowStats* vstats,
                               int row_from_M, float T, int reset) {
   pdl_wait();
   pdl_trigger();
-  const int row = row_from_M ? st->M - 1 : 0;
-  const RowStats rs = vstats[row];
-  const int tok = T > 0.f ? rs.sample : rs.top1;
-  const int n = reset ? st->pos0 + st->M : st->n;
-  tokens[n] = tok;
-  st->n = n + 1;
-  st->emitted[0] = tok;
-  st->n_emitted = 1;
-  if (reset) st->j = st->d = st->stop = 0;
+  if (threadIdx.x == 0) ctl::ar_end(st, tokens, vstats, row_from_M, T, reset);
 }
 
 // Greedy acceptance: the longest prefix of drafts matching the full

@@ -10,23 +10,24 @@
 // ssd_pack_weight): the matrix is one contiguous stream and a unit is exactly
 // the A operand of two m16n8k16 MMAs for one warp.
 //
-// Data movement.  Each CTA owns an equal contiguous range of units (a fixed
-// grid of kGridCtas CTAs, two per SM, one wave).  A producer warp streams
-// the range into a ring of shared-memory slots with bulk (TMA) copies of up
-// to 8 units, completing on mbarriers; eight consumer warps take one unit
-// each per slot, read their fragments with conflict-free 16-byte shared loads
-// and run the MMAs.  Activations (the B operand: 8 or 16 token columns) are
-// read from global memory (L1-resident); the RMSNorm of the norm-fused input
-// is applied on the fly from the producer kernel's sum-of-squares partials.
+// Data movement.  Each CTA owns a contiguous range of units: whole row
+// groups (whole gate/up pairs) in equal numbers where the matrix has enough
+// of them, else an equal share of single units (at most kGridCtas CTAs, two
+// per SM, one wave).  A producer warp streams the range into a ring of
+// shared-memory slots with bulk (TMA) copies of up to 8 units, completing on
+// mbarriers; eight consumer warps take one unit each per slot, read their
+// fragments with conflict-free 16-byte shared loads and run the MMAs.
+// Activations (the B operand: 8 or 16 token columns) are staged once per CTA
+// in shared memory (normalised with the RMSNorm statistics for the norm-fused
+// input) or, for wide passes, read from global memory a chunk ahead.
 //
-// Reduction order.  A row group (16 outputs) whose units span several CTAs is
-// finished by the last CTA to complete it: each CTA first sums its eight
-// warps' partials in warp order, and the finishing CTA sums the CTAs'
-// partials in CTA order before the epilogue.  Each warp accumulates its units
-// in ascending K order.  The partition depends only on the matrix shape and
-// nothing depends on M, so a column's bits do not change with the number of
-// rows processed together — which is what makes self-speculative
-// verification reproduce autoregressive decoding bit for bit.
+// Reduction order.  A row group's sum is the sum, in CTA order, of its CTAs'
+// partials; a partial is the sum, in warp order, of the consumer warps'
+// accumulators; each warp accumulates its units in ascending K order.  The
+// partition depends only on the matrix shape and nothing depends on M, so a
+// column's bits do not change with the number of rows processed together —
+// which is what makes self-speculative verification reproduce
+// autoregressive decoding bit for bit.
 #include "gemv_dev.cuh"
 
 namespace ssd {

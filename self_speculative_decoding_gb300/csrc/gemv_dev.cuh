@@ -51,10 +51,14 @@ constexpr int kStageBytes = SSD_GEMV_STAGE_KB * 1024;
 constexpr int kPad = 8;                          // bf16 row padding of the stage
 
 // Partition of a GEMV's T units over C CTAs: CTA b owns the contiguous
-// granules [b*Tg/C, (b+1)*Tg/C), a granule being G units.  Projections use
-// single units (G = 1: equal shares, row groups may straddle CTAs); the LM
-// head uses whole row groups (G = KB) so that every CTA summarises complete
-// vocabulary rows on its own.
+// granules [b*Tg/C, (b+1)*Tg/C), a granule being G units.  Where the matrix
+// has enough row groups, a granule is a whole row group (a whole gate/up
+// pair for SwiGLU) and C is chosen so that every CTA gets the same number of
+// granules: no row group is then split across CTAs and every epilogue runs
+// from shared memory.  Matrices with too few row groups for that use single
+// units (G = 1, C = kGridCtas) and combine split groups across CTAs.
+constexpr int kMinWholeCtas = 200;
+
 struct Part {
   int T;       // units = NRG * KB
   int Tg;      // granules = T / G
@@ -92,9 +96,19 @@ __host__ __device__ inline Part make_part(int R, int K, int epi) {
   p.NRG = (epi == EPI_SWIGLU ? 2 : 1) * (R / 16);
   p.KB = K / 32;
   p.T = p.NRG * p.KB;
-  p.G = epi == EPI_LMHEAD ? p.KB : 1;
-  p.Tg = p.T / p.G;
-  p.C = p.Tg < kGridCtas ? p.Tg : kGridCtas;
+  const int gu = (epi == EPI_SWIGLU ? 2 : 1) * p.KB;  // units of a whole group / pair
+  const int ng = p.T / gu;
+  const int per = (ng + kGridCtas - 1) / kGridCtas;   // granules per CTA
+  const int cw = (ng + per - 1) / per;                // CTAs with equal shares
+  if (epi == EPI_LMHEAD || cw >= kMinWholeCtas) {
+    p.G = gu;
+    p.Tg = ng;
+    p.C = cw;
+  } else {
+    p.G = 1;
+    p.Tg = p.T;
+    p.C = p.T < kGridCtas ? p.T : kGridCtas;
+  }
   p.segmax = (p.C + p.NRG - 1) / p.NRG + 1;
   return p;
 }
@@ -253,11 +267,6 @@ SSD_DI LmRec lm_merge_warp(LmRec r, float T) {
 
 // ---------------------------------------------------------------- epilogues
 
-// Runs in one warp once row group vr (or the gate/up pair containing it) is
-// complete; ep[h][row][tok] holds the finished sums.
-// (Projections only; the LM head goes through lm_group / lm_finish.)
-// Returns true: the call completes one signalled unit of the phase (a row
-// group or a gate/up pair).
 // Residual entries lane + 32 i of a row group (EPI_RESID), loaded ahead of
 // the group's completion so that their latency is off the tail.
 struct XPre {
@@ -278,6 +287,10 @@ SSD_DI void xres_prefetch(const LinearArgs& a, int vr, int M, int lane, XPre& xp
   }
 }
 
+// Runs in one warp once row group vr (or the gate/up pair containing it) is
+// complete; ep[h][row][tok] holds the finished sums.  Projections only (the
+// LM head goes through lm_group / lm_finish).  Returns true: the call
+// completes one signalled unit of the phase (a row group or a gate/up pair).
 template <int EPI>
 SSD_DI bool epilogue(const LinearArgs& a, const Part& p, int vr, float (*ep)[16][17], int M,
                      int lane, const XPre& xp) {
@@ -609,6 +622,7 @@ SSD_DI void epilogue_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int
   const int U0 = unit_begin(p, b), U1 = unit_begin(p, b + 1);
   int vr = U0 / p.KB, kb = U0 % p.KB, left = U1 - U0;
   LmRec run = lm_empty();
+  unsigned nfin = 0;  // signalled units finished by this CTA
   int slot = 0, round = 0, pos0 = 0;
   if (EPI == EPI_LMHEAD) {
     slot = a.slot_dev ? __ldcg(a.slot_dev) : 0;
@@ -650,10 +664,7 @@ SSD_DI void epilogue_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int
         fin = epilogue<EPI>(a, p, gvr, sm.ep, M, lane, xp);
       }
       __syncwarp();
-      if (done && fin) {
-        __threadfence();
-        if (lane == 0) atomicAdd(done, 1u);
-      }
+      nfin += fin ? 1u : 0u;
       continue;
     }
     // ---- split group (pair): every CTA stores its partial; the CTA that
@@ -724,17 +735,15 @@ SSD_DI void epilogue_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int
     if (lane == 0) a.counter[cidx] = 0u;
     const bool fin = epilogue<EPI>(a, p, gvr, sm.ep, M, lane, xp);
     __syncwarp();
-    if (done && fin) {
-      __threadfence();
-      if (lane == 0) atomicAdd(done, 1u);
-    }
+    nfin += fin ? 1u : 0u;
   }
-  if (EPI == EPI_LMHEAD) {
-    const bool fin = lm_finish(a, p, b, M, lane, slot, run, reinterpret_cast<float*>(sm.stage));
-    if (done && fin && lane == 0) {
-      __threadfence();
-      atomicAdd(done, 1u);
-    }
+  if (EPI == EPI_LMHEAD)
+    nfin = lm_finish(a, p, b, M, lane, slot, run, reinterpret_cast<float*>(sm.stage)) ? 1u : 0u;
+  // one completion signal per CTA and phase: all of this CTA's finished
+  // units at once
+  if (done && nfin) {
+    __threadfence();
+    if (lane == 0) atomicAdd(done, nfin);
   }
 }
 

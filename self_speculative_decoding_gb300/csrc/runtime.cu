@@ -31,6 +31,18 @@ namespace {
 
 enum Phase { PH_NONE = 0, PH_IDLE = 1, PH_DRAFTED = 2, PH_VERIFIED = 3 };
 
+// A pass program in device memory: phases, their arguments, the completion
+// counters and the abort flag (one allocation).
+struct PassDev {
+  void* buf = nullptr;
+  PassProg prog;
+  void reset() {
+    if (buf) cudaFree(buf);
+    buf = nullptr;
+    prog = PassProg();
+  }
+};
+
 struct Graph {
   cudaGraphExec_t exec = nullptr;
   int nodes = 0;
@@ -73,7 +85,6 @@ struct ssd_ctx {
   float2* rope = nullptr;
   float* attn_part = nullptr;
   unsigned* attn_cnt = nullptr;
-  int* attn_err = nullptr;
   float* g_part = nullptr;      // GEMV split-row-group partials (shared by all GEMVs)
   unsigned* g_cnt = nullptr;
   float* g_rec = nullptr;
@@ -96,6 +107,11 @@ struct ssd_ctx {
   int32_t* h_tok = nullptr;  // pinned staging [max_seq]
 
   Graph g_draft, g_extra, g_verify, g_accept, g_ar;
+  // persistent pass kernel programs (one launch per draft step / extra pass /
+  // verify pass / AR step) and whether they are used
+  bool use_pass = false;
+  bool pass_ok = false;
+  PassDev p_draft, p_extra, p_verify, p_ar;
 
   Phase phase = PH_NONE;
   // profiling: events recorded around every eager launch
@@ -156,7 +172,13 @@ ssd_status wait_stream(ssd_ctx* c) {
 
 ssd_status read_state(ssd_ctx* c) {
   CK(cudaMemcpyAsync(c->h_st, c->st, sizeof(DevState), cudaMemcpyDeviceToHost, c->stream));
-  return wait_stream(c);
+  const ssd_status r = wait_stream(c);
+  if (r != SSD_OK) return r;
+  if (c->h_st->err != 0)
+    return fail(c, SSD_ERR_TIMEOUT,
+                "a device-side wait gave up (code " + std::to_string(c->h_st->err) +
+                    "); the context must be destroyed");
+  return SSD_OK;
 }
 
 // ---------------------------------------------------------------------------
@@ -187,114 +209,106 @@ void gemv_scratch_args(ssd_ctx* c, LinearArgs& a) {
   a.part = c->g_part;
   a.counter = c->g_cnt;
   a.rec = c->g_rec;
-  a.err = c->attn_err;
+  a.err = &c->st->err;
 }
 
-ssd_status enq_layer(ssd_ctx* c, int l, cudaStream_t s) {
+// Arguments of layer l's five steps (shared by the eager / captured launches
+// and by the pass programs).
+LinearArgs qkv_args(ssd_ctx* c, int l) {
   const ssd_config& g = c->cfg;
   const ssd_layer_weights& w = c->layers[l];
-  ssd_status r;
-  {
-    LinearArgs a;
-    a.W0 = (const bf16*)w.wqkv;
-    a.R = qkv_rows(g);
-    a.K = g.d_model;
-    a.x = c->x;
-    a.ss = c->ss;
-    a.gain = (const float*)w.attn_norm;
-    a.eps = g.norm_eps;
-    a.M_dev = &c->st->M;
-    a.y = c->qkv;
-    gemv_scratch_args(c, a);
-    prof_begin(c, 0);
-    if ((r = note(c, launch_gemv(IN_NORM, EPI_STORE, a, s, c->pdl), "qkv")) != SSD_OK)
-      return r;
-  }
-  {
-    AttnArgs a;
-    a.qkv = c->qkv;
-    a.ld_qkv = qkv_rows(g);
-    a.M_dev = &c->st->M;
-    a.pos0_dev = &c->st->pos0;
-    a.kc = c->kc + (size_t)l * kv_layer_elems(g);
-    a.vc = c->vc + (size_t)l * kv_layer_elems(g);
-    a.max_seq = g.max_seq;
-    a.H = g.n_heads;
-    a.Hkv = g.n_kv_heads;
-    a.dh = g.head_dim;
-    a.rope = c->rope;
-    a.out = c->attn;
-    a.part = c->attn_part;
-    a.counters = c->attn_cnt;
-    a.err = c->attn_err;
-    if (c->sc_split >= 0) {
-      a.kc2 = c->sc_k + (size_t)l * g.n_kv_heads * c->sc_len * g.head_dim;
-      a.vc2 = c->sc_v + (size_t)l * g.n_kv_heads * c->sc_len * g.head_dim;
-      a.split = c->sc_split;
-      a.scratch_len = c->sc_len;
-    }
-    a.scale = (float)(1.0 / std::sqrt((double)g.head_dim));
-    prof_begin(c, 1);
-    if ((r = note(c, launch_attention(a, s, c->pdl), "attention")) != SSD_OK) return r;
-  }
-  {
-    LinearArgs a;
-    a.W0 = (const bf16*)w.wo;
-    a.R = g.d_model;
-    a.K = g.n_heads * g.head_dim;
-    a.act = c->attn;
-    a.M_dev = &c->st->M;
-    a.xres = c->x;
-    a.ss_out = c->ss;
-    gemv_scratch_args(c, a);
-    prof_begin(c, 2);
-    if ((r = note(c, launch_gemv(IN_BF16, EPI_RESID, a, s, c->pdl), "o_proj")) != SSD_OK)
-      return r;
-  }
-  {
-    LinearArgs a;
-    a.W0 = (const bf16*)w.w_gate;
-    a.W1 = (const bf16*)w.w_up;
-    a.R = g.ffn_dim;
-    a.K = g.d_model;
-    a.x = c->x;
-    a.ss = c->ss;
-    a.gain = (const float*)w.mlp_norm;
-    a.eps = g.norm_eps;
-    a.M_dev = &c->st->M;
-    a.u = c->u;
-    gemv_scratch_args(c, a);
-    prof_begin(c, 3);
-    if ((r = note(c, launch_gemv(IN_NORM, EPI_SWIGLU, a, s, c->pdl), "gate_up")) != SSD_OK)
-      return r;
-  }
-  {
-    LinearArgs a;
-    a.W0 = (const bf16*)w.w_down;
-    a.R = g.d_model;
-    a.K = g.ffn_dim;
-    a.act = c->u;
-    a.M_dev = &c->st->M;
-    a.xres = c->x;
-    a.ss_out = c->ss;
-    gemv_scratch_args(c, a);
-    prof_begin(c, 4);
-    if ((r = note(c, launch_gemv(IN_BF16, EPI_RESID, a, s, c->pdl), "down")) != SSD_OK)
-      return r;
-  }
-  return SSD_OK;
+  LinearArgs a;
+  a.W0 = (const bf16*)w.wqkv;
+  a.R = qkv_rows(g);
+  a.K = g.d_model;
+  a.x = c->x;
+  a.ss = c->ss;
+  a.gain = (const float*)w.attn_norm;
+  a.eps = g.norm_eps;
+  a.M_dev = &c->st->M;
+  a.y = c->qkv;
+  gemv_scratch_args(c, a);
+  return a;
 }
 
-ssd_status enq_layers(ssd_ctx* c, const std::vector<int>& ls, cudaStream_t s) {
-  for (int l : ls) {
-    const ssd_status r = enq_layer(c, l, s);
-    if (r != SSD_OK) return r;
+AttnArgs attn_args(ssd_ctx* c, int l) {
+  const ssd_config& g = c->cfg;
+  AttnArgs a;
+  a.qkv = c->qkv;
+  a.ld_qkv = qkv_rows(g);
+  a.M_dev = &c->st->M;
+  a.pos0_dev = &c->st->pos0;
+  a.kc = c->kc + (size_t)l * kv_layer_elems(g);
+  a.vc = c->vc + (size_t)l * kv_layer_elems(g);
+  a.max_seq = g.max_seq;
+  a.H = g.n_heads;
+  a.Hkv = g.n_kv_heads;
+  a.dh = g.head_dim;
+  a.rope = c->rope;
+  a.out = c->attn;
+  a.part = c->attn_part;
+  a.counters = c->attn_cnt;
+  a.err = &c->st->err;
+  if (c->sc_split >= 0) {
+    a.kc2 = c->sc_k + (size_t)l * g.n_kv_heads * c->sc_len * g.head_dim;
+    a.vc2 = c->sc_v + (size_t)l * g.n_kv_heads * c->sc_len * g.head_dim;
+    a.split = c->sc_split;
+    a.scratch_len = c->sc_len;
   }
-  return SSD_OK;
+  a.scale = (float)(1.0 / std::sqrt((double)g.head_dim));
+  return a;
 }
 
-ssd_status enq_lmhead(ssd_ctx* c, RowStats* stats, float* logits, const int32_t* slot_dev,
-                      int sample_stream, cudaStream_t s) {
+LinearArgs oproj_args(ssd_ctx* c, int l) {
+  const ssd_config& g = c->cfg;
+  LinearArgs a;
+  a.W0 = (const bf16*)c->layers[l].wo;
+  a.R = g.d_model;
+  a.K = g.n_heads * g.head_dim;
+  a.act = c->attn;
+  a.M_dev = &c->st->M;
+  a.xres = c->x;
+  a.ss_out = c->ss;
+  gemv_scratch_args(c, a);
+  return a;
+}
+
+LinearArgs gateup_args(ssd_ctx* c, int l) {
+  const ssd_config& g = c->cfg;
+  const ssd_layer_weights& w = c->layers[l];
+  LinearArgs a;
+  a.W0 = (const bf16*)w.w_gate;
+  a.W1 = (const bf16*)w.w_up;
+  a.R = g.ffn_dim;
+  a.K = g.d_model;
+  a.x = c->x;
+  a.ss = c->ss;
+  a.gain = (const float*)w.mlp_norm;
+  a.eps = g.norm_eps;
+  a.M_dev = &c->st->M;
+  a.u = c->u;
+  gemv_scratch_args(c, a);
+  return a;
+}
+
+LinearArgs down_args(ssd_ctx* c, int l) {
+  const ssd_config& g = c->cfg;
+  LinearArgs a;
+  a.W0 = (const bf16*)c->layers[l].w_down;
+  a.R = g.d_model;
+  a.K = g.ffn_dim;
+  a.act = c->u;
+  a.M_dev = &c->st->M;
+  a.xres = c->x;
+  a.ss_out = c->ss;
+  gemv_scratch_args(c, a);
+  return a;
+}
+
+// LM head over the pass's rows; every pass reports lse(z / T), only draft,
+// AR and prefill passes draw (sample_stream >= 0).
+LinearArgs lm_args(ssd_ctx* c, RowStats* stats, float* logits, const int32_t* slot_dev,
+                   int sample_stream) {
   const ssd_config& g = c->cfg;
   LinearArgs a;
   a.W0 = c->lm_head;
@@ -309,19 +323,16 @@ ssd_status enq_lmhead(ssd_ctx* c, RowStats* stats, float* logits, const int32_t*
   a.stats = stats;
   a.slot_dev = slot_dev;
   gemv_scratch_args(c, a);
-  // every pass reports lse(z / T); only draft, AR and prefill passes draw
   a.temperature = c->pol.temperature;
   a.sample = sample_stream >= 0 ? 1 : 0;
   a.seed = c->pol.seed;
   a.round_dev = &c->st->round;
   a.sample_stream = sample_stream < 0 ? 0 : sample_stream;
   a.pos0_dev = &c->st->pos0;
-  prof_begin(c, 5);
-  return note(c, launch_gemv(IN_NORM, EPI_LMHEAD, a, s, c->pdl), "lm_head");
+  return a;
 }
 
-ssd_status enq_begin(ssd_ctx* c, int mode, cudaStream_t s, int M = 1, int pos0 = 0,
-                     const int32_t* toks_in = nullptr, int reset = 0) {
+BeginArgs begin_args(ssd_ctx* c, int mode, int M, int pos0, const int32_t* toks_in, int reset) {
   BeginArgs b;
   b.mode = mode;
   b.st = c->st;
@@ -336,9 +347,196 @@ ssd_status enq_begin(ssd_ctx* c, int mode, cudaStream_t s, int M = 1, int pos0 =
   b.ss = c->ss;
   b.bx = c->bx;
   b.bss = c->bss;
-  prof_begin(c, 6);
-  return note(c, launch_begin(b, s, c->pdl), "begin");
+  return b;
 }
+
+ssd_status enq_layer(ssd_ctx* c, int l, cudaStream_t s) {
+  ssd_status r;
+  prof_begin(c, 0);
+  if ((r = note(c, launch_gemv(IN_NORM, EPI_STORE, qkv_args(c, l), s, c->pdl), "qkv")) != SSD_OK)
+    return r;
+  prof_begin(c, 1);
+  if ((r = note(c, launch_attention(attn_args(c, l), s, c->pdl), "attention")) != SSD_OK) return r;
+  prof_begin(c, 2);
+  if ((r = note(c, launch_gemv(IN_BF16, EPI_RESID, oproj_args(c, l), s, c->pdl), "o_proj")) !=
+      SSD_OK)
+    return r;
+  prof_begin(c, 3);
+  if ((r = note(c, launch_gemv(IN_NORM, EPI_SWIGLU, gateup_args(c, l), s, c->pdl), "gate_up")) !=
+      SSD_OK)
+    return r;
+  prof_begin(c, 4);
+  return note(c, launch_gemv(IN_BF16, EPI_RESID, down_args(c, l), s, c->pdl), "down");
+}
+
+ssd_status enq_layers(ssd_ctx* c, const std::vector<int>& ls, cudaStream_t s) {
+  for (int l : ls) {
+    const ssd_status r = enq_layer(c, l, s);
+    if (r != SSD_OK) return r;
+  }
+  return SSD_OK;
+}
+
+ssd_status enq_lmhead(ssd_ctx* c, RowStats* stats, float* logits, const int32_t* slot_dev,
+                      int sample_stream, cudaStream_t s) {
+  prof_begin(c, 5);
+  return note(c, launch_gemv(IN_NORM, EPI_LMHEAD, lm_args(c, stats, logits, slot_dev, sample_stream),
+                             s, c->pdl),
+              "lm_head");
+}
+
+ssd_status enq_begin(ssd_ctx* c, int mode, cudaStream_t s, int M = 1, int pos0 = 0,
+                     const int32_t* toks_in = nullptr, int reset = 0) {
+  prof_begin(c, 6);
+  return note(c, launch_begin(begin_args(c, mode, M, pos0, toks_in, reset), s, c->pdl), "begin");
+}
+
+// ---------------------------------------------------------------------------
+// pass programs
+
+struct PassBuilder {
+  std::vector<PassPhase> ph;
+  std::vector<LinearArgs> lin;
+  std::vector<AttnArgs> att;
+  std::vector<BeginArgs> beg;
+
+  void gemv(int in, int epi, const LinearArgs& a, unsigned target) {
+    PassPhase p;
+    p.kind = PK_GEMV;
+    p.in = in;
+    p.epi = epi;
+    p.idx = (int)lin.size();
+    p.target = target;
+    lin.push_back(a);
+    ph.push_back(p);
+  }
+  void attention(const AttnArgs& a) {
+    PassPhase p;
+    p.kind = PK_ATTN;
+    p.idx = (int)att.size();
+    p.target = (unsigned)a.Hkv;  // one completion per combined KV head
+    att.push_back(a);
+    ph.push_back(p);
+  }
+  void begin(const BeginArgs& b) {
+    PassPhase p;
+    p.kind = PK_BEGIN;
+    p.idx = (int)beg.size();
+    beg.push_back(b);
+    ph.push_back(p);
+  }
+  void control(const PassPhase& p) { ph.push_back(p); }
+};
+
+void pb_layers(ssd_ctx* c, PassBuilder& B, const std::vector<int>& ls) {
+  const ssd_config& g = c->cfg;
+  for (int l : ls) {
+    B.gemv(IN_NORM, EPI_STORE, qkv_args(c, l), (unsigned)(qkv_rows(g) / 16));
+    B.attention(attn_args(c, l));
+    B.gemv(IN_BF16, EPI_RESID, oproj_args(c, l), (unsigned)(g.d_model / 16));
+    B.gemv(IN_NORM, EPI_SWIGLU, gateup_args(c, l), (unsigned)(g.ffn_dim / 16));
+    B.gemv(IN_BF16, EPI_RESID, down_args(c, l), (unsigned)(g.d_model / 16));
+  }
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Uploads a built program (one device allocation).
+ssd_status pass_upload(ssd_ctx* c, const PassBuilder& B, PassDev& d) {
+  d.reset();
+  const size_t n = B.ph.size();
+  const size_t o_ph = 0;
+  const size_t o_lin = align256(o_ph + n * sizeof(PassPhase));
+  const size_t o_att = align256(o_lin + B.lin.size() * sizeof(LinearArgs));
+  const size_t o_beg = align256(o_att + B.att.size() * sizeof(AttnArgs));
+  const size_t o_done = align256(o_beg + B.beg.size() * sizeof(BeginArgs));
+  const size_t o_flags = align256(o_done + n * sizeof(unsigned));
+  const size_t total = o_flags + 256;
+  CK(cudaMalloc(&d.buf, total));
+  std::vector<unsigned char> h(total, 0);
+  memcpy(h.data() + o_ph, B.ph.data(), n * sizeof(PassPhase));
+  if (!B.lin.empty()) memcpy(h.data() + o_lin, B.lin.data(), B.lin.size() * sizeof(LinearArgs));
+  if (!B.att.empty()) memcpy(h.data() + o_att, B.att.data(), B.att.size() * sizeof(AttnArgs));
+  if (!B.beg.empty()) memcpy(h.data() + o_beg, B.beg.data(), B.beg.size() * sizeof(BeginArgs));
+  CK(cudaMemcpy(d.buf, h.data(), total, cudaMemcpyHostToDevice));
+  unsigned char* base = static_cast<unsigned char*>(d.buf);
+  PassProg& P = d.prog;
+  P.n = (int)n;
+  P.ph = reinterpret_cast<const PassPhase*>(base + o_ph);
+  P.lin = reinterpret_cast<const LinearArgs*>(base + o_lin);
+  P.att = reinterpret_cast<const AttnArgs*>(base + o_att);
+  P.beg = reinterpret_cast<const BeginArgs*>(base + o_beg);
+  P.done = reinterpret_cast<unsigned*>(base + o_done);
+  P.exit_count = reinterpret_cast<unsigned*>(base + o_flags);
+  P.abort = reinterpret_cast<int*>(base + o_flags + 64);
+  P.st = c->st;
+  P.tokens = c->tokens;
+  P.dstats = c->dstats;
+  P.vstats = c->vstats;
+  P.x = c->x;
+  P.ss = c->ss;
+  P.bx = c->bx;
+  P.bss = c->bss;
+  P.D = c->cfg.d_model;
+  P.err = &c->st->err;
+  return SSD_OK;
+}
+
+ssd_status build_pass_programs(ssd_ctx* c) {
+  ssd_status r;
+  {  // draft step
+    PassBuilder B;
+    B.begin(begin_args(c, BEGIN_DRAFT, 1, 0, nullptr, 0));
+    pb_layers(c, B, c->pre);
+    PassPhase sv;
+    sv.kind = PK_SAVE;
+    sv.use_d = 0;
+    B.control(sv);
+    pb_layers(c, B, c->post);
+    B.gemv(IN_NORM, EPI_LMHEAD, lm_args(c, c->dstats, c->dlogits, &c->st->slot, 0), 1u);
+    PassPhase de;
+    de.kind = PK_DRAFT_END;
+    de.tau = c->pol.tau;
+    de.temperature = c->pol.temperature;
+    B.control(de);
+    if ((r = pass_upload(c, B, c->p_draft)) != SSD_OK) return r;
+  }
+  {  // extra pass (layers below the first skipped one for the last draft)
+    PassBuilder B;
+    B.begin(begin_args(c, BEGIN_EXTRA, 1, 0, nullptr, 0));
+    pb_layers(c, B, c->pre);
+    PassPhase sv;
+    sv.kind = PK_SAVE;
+    sv.use_d = 1;
+    B.control(sv);
+    if ((r = pass_upload(c, B, c->p_extra)) != SSD_OK) return r;
+  }
+  {  // verify pass
+    PassBuilder B;
+    B.begin(begin_args(c, BEGIN_VERIFY, 1, 0, nullptr, 0));
+    pb_layers(c, B, c->verify_layers);
+    B.gemv(IN_NORM, EPI_LMHEAD, lm_args(c, c->vstats, c->vlogits, nullptr, -1), 1u);
+    if ((r = pass_upload(c, B, c->p_verify)) != SSD_OK) return r;
+  }
+  {  // autoregressive step
+    PassBuilder B;
+    B.begin(begin_args(c, BEGIN_AR, 1, 0, nullptr, 0));
+    std::vector<int> all(c->cfg.n_layers);
+    for (int l = 0; l < c->cfg.n_layers; ++l) all[l] = l;
+    pb_layers(c, B, all);
+    B.gemv(IN_NORM, EPI_LMHEAD, lm_args(c, c->vstats, nullptr, nullptr, 2), 1u);
+    PassPhase ae;
+    ae.kind = PK_AR_END;
+    ae.temperature = c->pol.temperature;
+    ae.row_from_M = 0;
+    ae.reset = 0;
+    B.control(ae);
+    if ((r = pass_upload(c, B, c->p_ar)) != SSD_OK) return r;
+  }
+  return SSD_OK;
+}
+
+bool pass_active(const ssd_ctx* c) { return c->use_pass && c->pass_ok && !c->profiling; }
 
 // ---------------------------------------------------------------------------
 // graphs
@@ -368,6 +566,7 @@ ssd_status build_graph(ssd_ctx* c, Graph& g, Builder fn) {
 }
 
 ssd_status b_draft(ssd_ctx* c, cudaStream_t s) {
+  if (pass_active(c)) return note(c, launch_pass(c->p_draft.prog, s), "draft pass");
   ssd_status r;
   if ((r = enq_begin(c, BEGIN_DRAFT, s)) != SSD_OK) return r;
   if ((r = enq_layers(c, c->pre, s)) != SSD_OK) return r;
@@ -381,6 +580,7 @@ ssd_status b_draft(ssd_ctx* c, cudaStream_t s) {
 }
 
 ssd_status b_extra(ssd_ctx* c, cudaStream_t s) {
+  if (pass_active(c)) return note(c, launch_pass(c->p_extra.prog, s), "extra pass");
   ssd_status r;
   if ((r = enq_begin(c, BEGIN_EXTRA, s)) != SSD_OK) return r;
   if ((r = enq_layers(c, c->pre, s)) != SSD_OK) return r;
@@ -389,6 +589,7 @@ ssd_status b_extra(ssd_ctx* c, cudaStream_t s) {
 }
 
 ssd_status b_verify(ssd_ctx* c, cudaStream_t s) {
+  if (pass_active(c)) return note(c, launch_pass(c->p_verify.prog, s), "verify pass");
   ssd_status r;
   if ((r = enq_begin(c, BEGIN_VERIFY, s)) != SSD_OK) return r;
   if ((r = enq_layers(c, c->verify_layers, s)) != SSD_OK) return r;
@@ -413,6 +614,7 @@ ssd_status b_accept(ssd_ctx* c, cudaStream_t s) {
 }
 
 ssd_status b_ar(ssd_ctx* c, cudaStream_t s) {
+  if (pass_active(c)) return note(c, launch_pass(c->p_ar.prog, s), "ar pass");
   ssd_status r;
   if ((r = enq_begin(c, BEGIN_AR, s)) != SSD_OK) return r;
   std::vector<int> all(c->cfg.n_layers);
@@ -424,13 +626,27 @@ ssd_status b_ar(ssd_ctx* c, cudaStream_t s) {
               "ar_end");
 }
 
-ssd_status build_graphs(ssd_ctx* c) {
+ssd_status build_graphs_once(ssd_ctx* c) {
   ssd_status r;
   if ((r = build_graph(c, c->g_draft, b_draft)) != SSD_OK) return r;
   if ((r = build_graph(c, c->g_extra, b_extra)) != SSD_OK) return r;
   if ((r = build_graph(c, c->g_verify, b_verify)) != SSD_OK) return r;
   if ((r = build_graph(c, c->g_accept, b_accept)) != SSD_OK) return r;
   return build_graph(c, c->g_ar, b_ar);
+}
+
+// Builds the graphs with the pass kernel when it is enabled and usable on
+// this device, else (or if that fails) with one kernel per step.
+ssd_status build_graphs(ssd_ctx* c) {
+  c->pass_ok = false;
+  if (c->use_pass && pass_supported(c->cfg.head_dim, c->cfg.max_seq) &&
+      pass_prepare() == cudaSuccess && build_pass_programs(c) == SSD_OK) {
+    c->pass_ok = true;
+    if (build_graphs_once(c) == SSD_OK) return SSD_OK;
+    c->pass_ok = false;
+  }
+  cudaGetLastError();
+  return build_graphs_once(c);
 }
 
 ssd_status replay(ssd_ctx* c, Graph& g) {
@@ -564,7 +780,6 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
             alloc((void**)&c->attn_part,
                   attn_part_floats(g.n_kv_heads, g.n_heads, g.head_dim, g.max_seq) * 4) &&
             alloc((void**)&c->attn_cnt, (size_t)g.n_kv_heads * 4) &&
-            alloc((void**)&c->attn_err, 4) &&
             alloc((void**)&c->g_part, gs.part_floats * 4) &&
             alloc((void**)&c->g_cnt, gs.counters * 4) &&
             alloc((void**)&c->g_rec, gs.rec_floats * 4) &&
@@ -600,7 +815,6 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
   cudaMemsetAsync(c->st, 0, sizeof(DevState), c->stream);
   cudaMemsetAsync(c->attn_cnt, 0, (size_t)g.n_kv_heads * 4, c->stream);
   cudaMemsetAsync(c->g_cnt, 0, gs.counters * 4, c->stream);
-  cudaMemsetAsync(c->attn_err, 0, 4, c->stream);
   cudaMemsetAsync(c->tokens, 0, (size_t)g.max_seq * 4, c->stream);
   const int half = g.head_dim / 2;
   launch_rope_table(c->rope, g.max_seq, half, (double)g.rope_theta, c->stream);
@@ -633,8 +847,12 @@ ssd_status ssd_destroy(ssd_ctx* c) {
   c->g_verify.reset();
   c->g_accept.reset();
   c->g_ar.reset();
+  c->p_draft.reset();
+  c->p_extra.reset();
+  c->p_verify.reset();
+  c->p_ar.reset();
   void* bufs[] = {c->kc, c->vc, c->x, c->ss, c->bx, c->bss, c->qkv, c->attn, c->u, c->rope,
-                  c->attn_part, c->attn_cnt, c->attn_err, c->g_part, c->g_cnt, c->g_rec, c->dstats, c->vstats,
+                  c->attn_part, c->attn_cnt, c->g_part, c->g_cnt, c->g_rec, c->dstats, c->vstats,
                   c->dlogits, c->vlogits, c->tokens, c->toks_in, c->st};
   for (void* p : bufs)
     if (p) cudaFree(p);
@@ -915,6 +1133,19 @@ ssd_status ssd_profile_decode(ssd_ctx* c, int32_t n_steps, ssd_kernel_times* out
   *c->h_st = saved;
   CK(cudaMemcpyAsync(c->st, c->h_st, sizeof(DevState), cudaMemcpyHostToDevice, c->stream));
   return wait_stream(c);
+}
+
+ssd_status ssd_set_pass_kernel(ssd_ctx* c, int32_t enable, int32_t* active_out) {
+  if (!c) return SSD_ERR_INVALID_ARG;
+  if (c->phase == PH_DRAFTED || c->phase == PH_VERIFIED)
+    return fail(c, SSD_ERR_STATE, "a round is in flight");
+  c->use_pass = enable != 0;
+  if (c->has_policy) {
+    const ssd_status r = build_graphs(c);
+    if (r != SSD_OK) return r;
+  }
+  if (active_out) *active_out = c->use_pass && c->pass_ok ? 1 : 0;
+  return SSD_OK;
 }
 
 ssd_status ssd_set_timeout_ms(ssd_ctx* c, int32_t ms) {

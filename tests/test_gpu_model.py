@@ -321,6 +321,11 @@ def test_llama7b_shape_ssd_equals_ar(ssd, literal_tau):
     assert f1 == f2 and toks == ar
     if not literal_tau:
         assert stats["drafted"] > 0
+    # one kernel per step computes the same bits as the persistent pass kernel
+    ctx.set_pass_kernel(False)
+    assert ctx.prefill(prompt) == f1
+    toks2, _ = ctx.generate(48)
+    assert toks2 == toks
     ctx.close()
     del wts
     torch.cuda.empty_cache()
