@@ -22,7 +22,7 @@ namespace ssd {
 
 namespace {
 
-__global__ void __launch_bounds__(attn::kGroupThreads) attn_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(attn::kGroupThreads, 3) attn_kernel(AttnArgs a) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bar;
   __shared__ int flag;
@@ -31,16 +31,23 @@ __global__ void __launch_bounds__(attn::kGroupThreads) attn_kernel(AttnArgs a) {
     mbar_init(&bar, 1);
     fence_mbar_init();
   }
-  pdl_wait();
-  pdl_trigger();
-  const int M = rows_of(a.M_static, a.M_dev);
-  const int pos0 = a.pos0_dev ? *a.pos0_dev : a.pos0_static;
+  __syncthreads();
+  // The pass shape was written by kernels that completed before this one was
+  // launched, and the cached rows before pos0 by earlier passes: the first
+  // item's bulk copies go out before the wait on the preceding kernel (the
+  // projection that produces q, k, v).
+  const int M = a.M_dev ? __ldcg(a.M_dev) : a.M_static;
+  const int pos0 = a.pos0_dev ? __ldcg(a.pos0_dev) : a.pos0_static;
   const attn::Smem sm = attn::carve(smem_raw, a.dh, a.max_seq / kAttnChunk);
   const int n_items = ((pos0 + M - 1) / kAttnChunk + 1) * a.Hkv;
   uint32_t phase = 0;
-  __syncthreads();
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x)
-    attn::item(a, M, pos0, it, sm, &bar, phase, &flag, tid, [] { __syncthreads(); });
+  if ((int)blockIdx.x < n_items) attn::issue(a, M, pos0, blockIdx.x, sm, &bar, tid);
+  pdl_wait();
+  pdl_trigger();
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    if (it != (int)blockIdx.x) attn::issue(a, M, pos0, it, sm, &bar, tid);
+    attn::body(a, M, pos0, it, sm, &bar, phase, &flag, tid, [] { __syncthreads(); });
+  }
 }
 
 }  // namespace
@@ -68,7 +75,7 @@ int attn_grid(const AttnArgs& a) {
   // Grid size only sets how many CTAs loop over the (head, chunk) items; it
   // does not change any reduction order.
   const int items = a.Hkv * (a.max_seq / kAttnChunk);
-  const int cap = sm_count() * 4;
+  const int cap = sm_count() * 3;  // resident CTAs per SM (launch bounds)
   return items < cap ? items : cap;
 }
 

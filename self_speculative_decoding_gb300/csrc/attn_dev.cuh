@@ -57,12 +57,53 @@ SSD_DI Smem carve(unsigned char* raw, int dh, int nchunk) {
   return sm;
 }
 
-// Executes work item `item` with threads tid < kGroupThreads; `sync()` is
-// the barrier of those threads.  `bar` is an initialised mbarrier whose
-// phase parity is tracked in `phase`; `flag` is one shared int.  Returns
-// true if this item combined its head (the head's output is complete).
+// Position p's cached key / value row: the shared cache below a.split, the
+// scratch cache from a.split on.
+SSD_DI const bf16* cache_row(const bf16* c, const bf16* c2, const AttnArgs& a, int kvh, int pos) {
+  return pos < a.split ? c + (size_t)kvh * a.max_seq * a.dh + (size_t)pos * a.dh
+                       : c2 + ((size_t)kvh * a.scratch_len + (pos - a.split)) * a.dh;
+}
+
+// Step (1) of work item `item`: the bulk copies of the chunk's cached keys
+// and values (positions before pos0), issued by warp 0 (one copy per padded
+// K row; the V rows in one copy unless the chunk straddles the split) and
+// completing on `bar`.  The cache rows before pos0 were written by earlier
+// passes, so this may run before the wait on the preceding kernel.
+SSD_DI void issue(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, uint64_t* bar,
+                  int tid) {
+  const int dh = a.dh, krs = dh + kKPad;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int c = item / a.Hkv, kvh = item % a.Hkv;
+  const int p_begin = c * kAttnChunk;
+  const int p_end = min(p_begin + kAttnChunk, pos0 + M);
+  const int n_old = max(0, min(p_end, pos0) - p_begin);
+  if (n_old > 0 && warp == 0) {
+    const bool one_v = p_begin + n_old <= a.split || p_begin >= a.split;
+    if (lane == 0) {
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar, (uint32_t)(2 * n_old * dh * sizeof(bf16)));
+      if (one_v)
+        bulk_g2s(sm.V, cache_row(a.vc, a.vc2, a, kvh, p_begin),
+                 (uint32_t)(n_old * dh * sizeof(bf16)), bar);
+    }
+    __syncwarp();
+    for (int j = lane; j < n_old; j += 32) {
+      bulk_g2s(sm.K + (size_t)j * krs, cache_row(a.kc, a.kc2, a, kvh, p_begin + j),
+               (uint32_t)(dh * sizeof(bf16)), bar);
+      if (!one_v)
+        bulk_g2s(sm.V + (size_t)j * dh, cache_row(a.vc, a.vc2, a, kvh, p_begin + j),
+                 (uint32_t)(dh * sizeof(bf16)), bar);
+    }
+  }
+}
+
+// Steps (2)-(4) of work item `item`, after issue() for the same item, with
+// threads tid < kGroupThreads; `sync()` is the barrier of those threads.
+// `bar` is an initialised mbarrier whose phase parity is tracked in `phase`;
+// `flag` is one shared int.  Returns true if this item combined its head
+// (the head's output is complete).
 template <class Sync>
-SSD_DI bool item(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, uint64_t* bar,
+SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, uint64_t* bar,
                  uint32_t& phase, int* flag, int tid, Sync sync) {
   const int dh = a.dh, half = dh / 2, krs = dh + kKPad;
   const int G = a.H / a.Hkv;
@@ -71,7 +112,6 @@ SSD_DI bool item(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
   const int last_pos = pos0 + M - 1;
   const int n_active = last_pos / kAttnChunk + 1;
   const int warp = tid >> 5, lane = tid & 31;
-  const size_t head_stride = (size_t)a.max_seq * dh;
   const int ld_out = a.H * dh;
 
   const int c = item / a.Hkv, kvh = item % a.Hkv;
@@ -79,34 +119,6 @@ SSD_DI bool item(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
   const int p_end = min(p_begin + kAttnChunk, last_pos + 1);
   const int nk = p_end - p_begin;
   const int n_old = max(0, min(p_end, pos0) - p_begin);
-  bf16* kc = a.kc + kvh * head_stride;
-  bf16* vc = a.vc + kvh * head_stride;
-  bf16* kc2 = a.kc2 ? a.kc2 + (size_t)kvh * a.scratch_len * dh : nullptr;
-  bf16* vc2 = a.vc2 ? a.vc2 + (size_t)kvh * a.scratch_len * dh : nullptr;
-  // row of position pos in the shared cache or in the scratch cache
-  auto krow = [&](int pos) {
-    return pos < a.split ? kc + (size_t)pos * dh : kc2 + (size_t)(pos - a.split) * dh;
-  };
-  auto vrow = [&](int pos) {
-    return pos < a.split ? vc + (size_t)pos * dh : vc2 + (size_t)(pos - a.split) * dh;
-  };
-
-  // (1) cached keys/values: bulk copies issued by warp 0 (one per padded K
-  // row; the V rows in one copy unless the chunk straddles the split)
-  if (n_old > 0 && warp == 0) {
-    const bool one_v = p_begin + n_old <= a.split || p_begin >= a.split;
-    if (lane == 0) {
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(bar, (uint32_t)(2 * n_old * dh * sizeof(bf16)));
-      if (one_v) bulk_g2s(sm.V, vrow(p_begin), (uint32_t)(n_old * dh * sizeof(bf16)), bar);
-    }
-    __syncwarp();
-    for (int j = lane; j < n_old; j += 32) {
-      bulk_g2s(sm.K + (size_t)j * krs, krow(p_begin + j), (uint32_t)(dh * sizeof(bf16)), bar);
-      if (!one_v)
-        bulk_g2s(sm.V + (size_t)j * dh, vrow(p_begin + j), (uint32_t)(dh * sizeof(bf16)), bar);
-    }
-  }
   // (2) new keys of this chunk: RoPE, bf16, append to the cache
   const int first_new = max(p_begin, pos0);
   for (int e = tid; e < (p_end - first_new) * half; e += kGroupThreads) {
@@ -124,8 +136,8 @@ SSD_DI bool item(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
     sm.K[j * krs + i + half] = kb1;
     sm.V[j * dh + i] = vb0;
     sm.V[j * dh + i + half] = vb1;
-    bf16* kd = krow(pos);
-    bf16* vd = vrow(pos);
+    bf16* kd = const_cast<bf16*>(cache_row(a.kc, a.kc2, a, kvh, pos));
+    bf16* vd = const_cast<bf16*>(cache_row(a.vc, a.vc2, a, kvh, pos));
     kd[i] = kb0;
     kd[i + half] = kb1;
     vd[i] = vb0;
@@ -225,43 +237,89 @@ SSD_DI bool item(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
   const bool last = *flag != 0;
   if (last) {
     __threadfence();
-    // (7) combine this head's chunks in chunk order, one row at a time:
-    // stage (m_c, l_c), weights w_c = exp(m_c - max), then each output
-    // dimension sums o_c * w_c over chunks.
+    // (7) combine this head's chunks in chunk order.  Per row: w_c =
+    // exp(m_c - max_c m_c), L = sum_c l_c w_c and O = sum_c o_c w_c, each sum
+    // in chunk order.  All rows at once when their (m, l, w) fit in this
+    // item's shared memory, else one row at a time.
     const float* hb = a.part + (size_t)kvh * nchunk_max * rows * (dh + 2);
-    for (int rr = 0; rr < G * M; ++rr) {
-      const int m = rr % M, gh = rr / M, r = gh * kMaxRows + m;
-      const int nc = (pos0 + m) / kAttnChunk + 1;
-      for (int cc = tid; cc < nc; cc += kGroupThreads) {
-        const float* pc = hb + ((size_t)cc * rows + r) * (dh + 2);
-        sm.cm[cc] = __ldcg(pc);
-        sm.cl[cc] = __ldcg(pc + 1);
+    const int R = G * M;
+    float* CM = reinterpret_cast<float*>(sm.K);
+    float* CL = CM + R * n_active;
+    float* CW = CL + R * n_active;
+    float* LR = CW + R * n_active;
+    const size_t need = ((size_t)3 * R * n_active + R) * sizeof(float);
+    if (need <= smem_bytes(dh, nchunk_max)) {
+      for (int e = tid; e < R * n_active; e += kGroupThreads) {
+        const int rr = e / n_active, cc = e % n_active;
+        const int m = rr % M, r = (rr / M) * kMaxRows + m;
+        if (cc <= (pos0 + m) / kAttnChunk) {
+          const float* pc = hb + ((size_t)cc * rows + r) * (dh + 2);
+          CM[e] = __ldcg(pc);
+          CL[e] = __ldcg(pc + 1);
+        }
       }
       sync();
-      float mx = -INFINITY;
-      for (int cc = 0; cc < nc; ++cc) mx = fmaxf(mx, sm.cm[cc]);
-      for (int cc = tid; cc < nc; cc += kGroupThreads) sm.cw[cc] = expf(sm.cm[cc] - mx);
+      for (int rr = tid; rr < R; rr += kGroupThreads) {
+        const int m = rr % M;
+        const int nc = (pos0 + m) / kAttnChunk + 1;
+        const float* cm = CM + rr * n_active;
+        float mx = -INFINITY;
+        for (int cc = 0; cc < nc; ++cc) mx = fmaxf(mx, cm[cc]);
+        float L = 0.f;
+        for (int cc = 0; cc < nc; ++cc) {
+          const float w = expf(cm[cc] - mx);
+          CW[rr * n_active + cc] = w;
+          L = fmaf(CL[rr * n_active + cc], w, L);
+        }
+        LR[rr] = L;
+      }
       sync();
-      float L = 0.f;
-      for (int cc = 0; cc < nc; ++cc) L = fmaf(sm.cl[cc], sm.cw[cc], L);
-      for (int dd = tid; dd < dh; dd += kGroupThreads) {
+      for (int e = tid; e < R * dh; e += kGroupThreads) {
+        const int rr = e / dh, dd = e % dh;
+        const int m = rr % M, gh = rr / M, r = gh * kMaxRows + m;
+        const int nc = (pos0 + m) / kAttnChunk + 1;
+        const float* w = CW + rr * n_active;
+        const float* ob = hb + (size_t)r * (dh + 2) + 2 + dd;
+        const size_t cs = (size_t)rows * (dh + 2);
         float O = 0.f;
         int cc = 0;
         for (; cc + 4 <= nc; cc += 4) {
-          const float o0 = __ldcg(hb + ((size_t)(cc + 0) * rows + r) * (dh + 2) + 2 + dd);
-          const float o1 = __ldcg(hb + ((size_t)(cc + 1) * rows + r) * (dh + 2) + 2 + dd);
-          const float o2 = __ldcg(hb + ((size_t)(cc + 2) * rows + r) * (dh + 2) + 2 + dd);
-          const float o3 = __ldcg(hb + ((size_t)(cc + 3) * rows + r) * (dh + 2) + 2 + dd);
-          O = fmaf(o0, sm.cw[cc + 0], O);
-          O = fmaf(o1, sm.cw[cc + 1], O);
-          O = fmaf(o2, sm.cw[cc + 2], O);
-          O = fmaf(o3, sm.cw[cc + 3], O);
+          float o[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) o[q] = __ldcg(ob + (size_t)(cc + q) * cs);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) O = fmaf(o[q], w[cc + q], O);
         }
-        for (; cc < nc; ++cc)
-          O = fmaf(__ldcg(hb + ((size_t)cc * rows + r) * (dh + 2) + 2 + dd), sm.cw[cc], O);
-        a.out[(size_t)m * ld_out + (size_t)(kvh * G + gh) * dh + dd] = __float2bfloat16_rn(O / L);
+        for (; cc < nc; ++cc) O = fmaf(__ldcg(ob + (size_t)cc * cs), w[cc], O);
+        a.out[(size_t)m * ld_out + (size_t)(kvh * G + gh) * dh + dd] =
+            __float2bfloat16_rn(O / LR[rr]);
       }
       sync();
+    } else {
+      for (int rr = 0; rr < R; ++rr) {
+        const int m = rr % M, gh = rr / M, r = gh * kMaxRows + m;
+        const int nc = (pos0 + m) / kAttnChunk + 1;
+        for (int cc = tid; cc < nc; cc += kGroupThreads) {
+          const float* pc = hb + ((size_t)cc * rows + r) * (dh + 2);
+          sm.cm[cc] = __ldcg(pc);
+          sm.cl[cc] = __ldcg(pc + 1);
+        }
+        sync();
+        float mx = -INFINITY;
+        for (int cc = 0; cc < nc; ++cc) mx = fmaxf(mx, sm.cm[cc]);
+        for (int cc = tid; cc < nc; cc += kGroupThreads) sm.cw[cc] = expf(sm.cm[cc] - mx);
+        sync();
+        float L = 0.f;
+        for (int cc = 0; cc < nc; ++cc) L = fmaf(sm.cl[cc], sm.cw[cc], L);
+        for (int dd = tid; dd < dh; dd += kGroupThreads) {
+          float O = 0.f;
+          for (int cc = 0; cc < nc; ++cc)
+            O = fmaf(__ldcg(hb + ((size_t)cc * rows + r) * (dh + 2) + 2 + dd), sm.cw[cc], O);
+          a.out[(size_t)m * ld_out + (size_t)(kvh * G + gh) * dh + dd] =
+              __float2bfloat16_rn(O / L);
+        }
+        sync();
+      }
     }
     if (tid == 0) a.counters[kvh] = 0u;
   }
@@ -269,6 +327,14 @@ SSD_DI bool item(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
   fence_proxy_async_smem();
   sync();
   return last;
+}
+
+// A whole work item: issue() then body().
+template <class Sync>
+SSD_DI bool item(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, uint64_t* bar,
+                 uint32_t& phase, int* flag, int tid, Sync sync) {
+  issue(a, M, pos0, item, sm, bar, tid);
+  return body(a, M, pos0, item, sm, bar, phase, flag, tid, sync);
 }
 
 }  // namespace attn
