@@ -110,11 +110,22 @@ class OracleModel:
             out[h] = (e @ V) / np.sum(e)
         return out.reshape(-1)
 
-    def layer(self, l: int, X: np.ndarray, positions: Sequence[int], kv: KVCache) -> np.ndarray:
-        """Run rows X ([M, D], consecutive positions) through layer l; writes K/V."""
+    def layer(self, l: int, X: np.ndarray, positions: Sequence[int], kv: KVCache,
+              attn: bool = True, mlp: bool = True) -> np.ndarray:
+        """Run rows X ([M, D], consecutive positions) through layer l; writes K/V.
+        ``attn`` / ``mlp`` False leave that sublayer's residual branch out (an
+        attention sublayer that does not run writes no K/V)."""
+        X = X.copy()
+        if attn:
+            X = self._attention_sublayer(l, X, positions, kv)
+        if mlp:
+            X = self._mlp_sublayer(l, X)
+        return X
+
+    def _attention_sublayer(self, l: int, X: np.ndarray, positions: Sequence[int],
+                            kv: KVCache) -> np.ndarray:
         s = self.s
         H, Hkv, dh = s.n_heads, s.n_kv_heads, s.head_dim
-        X = X.copy()
         g1 = self.mat(l, "attn_norm")
         Wqkv = self.mat(l, "wqkv")
         qs = []
@@ -131,9 +142,12 @@ class OracleModel:
         for m, pos in enumerate(positions):
             a = self.rnd(self.attention_row(qs[m], kv, l, pos))
             X[m] = X[m] + Wo @ a
+        return X
+
+    def _mlp_sublayer(self, l: int, X: np.ndarray) -> np.ndarray:
         g2 = self.mat(l, "mlp_norm")
         Wg, Wu, Wd = self.mat(l, "w_gate"), self.mat(l, "w_up"), self.mat(l, "w_down")
-        for m in range(len(positions)):
+        for m in range(X.shape[0]):
             h2 = self.rnd(self.rmsnorm(X[m], g2))
             gate = Wg @ h2
             up = Wu @ h2
@@ -148,9 +162,11 @@ class OracleModel:
         return np.stack([W @ self.rnd(self.rmsnorm(x, g)) for x in X])
 
     def run_layers(self, X: np.ndarray, positions: Sequence[int], kv: KVCache,
-                   layers: Sequence[int]) -> np.ndarray:
+                   layers: Sequence[int], parts=None) -> np.ndarray:
+        """``parts`` (optional): layer -> (attention runs, MLP runs)."""
         for l in layers:
-            X = self.layer(l, X, positions, kv)
+            a, m = parts(l) if parts is not None else (True, True)
+            X = self.layer(l, X, positions, kv, attn=a, mlp=m)
         return X
 
     def new_cache(self, max_seq: int) -> KVCache:

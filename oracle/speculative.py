@@ -28,7 +28,11 @@ reason in the design notes):
   the target distribution).
 * In skip mode the draft's kept layers above s0 write their (draft) K/V for
   the draft positions; the verify overwrites every position it runs in every
-  layer >= s0.  Skipped layers write nothing.
+  layer >= s0.  Skipped layers write nothing.  A policy may also drop only the
+  attention or only the MLP sublayer of a layer (SWIFT Fig. 10 treats them
+  separately): the dropped sublayer's residual branch is left out, and a
+  layer whose attention does not run writes no K/V; s0 is then the first
+  layer with any dropped sublayer.
 * Verify: when the draft filled d_max without feeding y_{d-1}, that token is
   first run through layers 0..s0-1 at position n-1+d.  Then the d+1 boundary
   states (positions n-1..n-1+d) run through layers s0..L-1 and the LM head.
@@ -174,7 +178,8 @@ def ssd_round(model: OracleModel, st: SSDState, policy) -> RoundRecord:
         X = model.embed_rows([tok])
         X = model.run_layers(X, [pos], st.kv, range(s0))
         bnd.append(X[0].copy())
-        X = model.run_layers(X, [pos], st.kv, post)
+        X = model.run_layers(X, [pos], st.kv, post,
+                             parts=policy.sublayers if policy.mode == "skip" else None)
         z = model.lm_head(X)[0]
         conf = float(np.exp(np.max(z) - logsumexp(z)))
         y = _pick(z, T, seed, pos + 1, rnd, STREAM_DRAFT)

@@ -53,7 +53,10 @@ class ModelShape:
 class Policy:
     """Draft policy: which layers the draft runs and when it stops.
 
-    mode "skip": the draft runs every layer not in ``skip`` (SWIFT / Self-SD).
+    mode "skip": the draft runs every layer not in ``skip`` (SWIFT / Self-SD);
+    ``skip_attn`` / ``skip_mlp`` additionally drop only the attention or only
+    the MLP sublayer of the listed layers (SWIFT Fig. 10 skips the two
+    sublayers separately).  A layer in ``skip`` drops both.
     mode "exit": the draft runs layers 0..exit_layer and applies the shared
     final norm + LM head to that hidden state (LayerSkip).
     ``tau`` is the top-1 confidence threshold of the early stop (None: no
@@ -67,17 +70,26 @@ class Policy:
     tau: Optional[float] = None
     temperature: float = 0.0
     seed: int = 0
+    skip_attn: Tuple[int, ...] = ()
+    skip_mlp: Tuple[int, ...] = ()
+
+    def sublayers(self, layer: int) -> Tuple[bool, bool]:
+        """(attention runs, MLP runs) for ``layer`` in the draft (skip mode)."""
+        whole = layer in self.skip
+        return (not whole and layer not in self.skip_attn,
+                not whole and layer not in self.skip_mlp)
 
     def draft_layers(self, n_layers: int) -> Tuple[int, ...]:
+        """Layers the draft runs at least one sublayer of."""
         if self.mode == "skip":
-            s = set(self.skip)
-            return tuple(l for l in range(n_layers) if l not in s)
+            return tuple(l for l in range(n_layers) if any(self.sublayers(l)))
         return tuple(range(self.exit_layer + 1))
 
     def first_recomputed(self, n_layers: int) -> int:
         """s0: the first layer the verify pass recomputes."""
         if self.mode == "skip":
-            return min(self.skip) if self.skip else n_layers
+            dropped = set(self.skip) | set(self.skip_attn) | set(self.skip_mlp)
+            return min(dropped) if dropped else n_layers
         return self.exit_layer + 1
 
 
