@@ -107,6 +107,14 @@ typedef struct {
   float temperature;     /* 0: greedy draft and acceptance; > 0: sampled
                             draft from softmax(z/T), min(1,p/q) acceptance  */
   uint64_t seed;         /* Philox4x32-10 key                                */
+  /* Skip mode only (SWIFT Fig. 10 skips the two sublayers of a layer
+   * separately): bit l set drops only the attention sublayer (attn) or only
+   * the MLP sublayer (mlp) of layer l from the draft; a dropped sublayer's
+   * residual branch is left out and a layer whose attention is dropped
+   * writes no K/V at the draft positions.  A layer in skip_mask drops both.
+   * The verify recomputes from the first layer with any dropped sublayer.  */
+  uint64_t skip_attn_mask[4];
+  uint64_t skip_mlp_mask[4];
 } ssd_policy;
 
 typedef struct {

@@ -78,12 +78,15 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
 
 
 def policy_struct(policy) -> SsdPolicy:
-    """Marshals a policy (attributes mode, skip, exit_layer, d_max, tau,
-    temperature, seed — e.g. ``synthetic.Policy``) into ``ssd_policy``."""
+    """Marshals a policy (attributes mode, skip, skip_attn, skip_mlp,
+    exit_layer, d_max, tau, temperature, seed — e.g. ``synthetic.Policy``)
+    into ``ssd_policy``."""
     p = SsdPolicy()
     p.mode = SSD_MODE_SKIP if policy.mode == "skip" else SSD_MODE_EXIT
-    for l in getattr(policy, "skip", ()):
-        p.skip_mask[l // 64] |= 1 << (l % 64)
+    for field, mask in (("skip", p.skip_mask), ("skip_attn", p.skip_attn_mask),
+                        ("skip_mlp", p.skip_mlp_mask)):
+        for l in getattr(policy, field, ()):
+            mask[l // 64] |= 1 << (l % 64)
     p.exit_layer = int(getattr(policy, "exit_layer", -1))
     p.d_max = int(policy.d_max)
     tau = getattr(policy, "tau", None)

@@ -41,7 +41,8 @@ class SsdWeights(C.Structure):
 class SsdPolicy(C.Structure):
     _fields_ = [("mode", C.c_int32), ("skip_mask", C.c_uint64 * 4), ("exit_layer", C.c_int32),
                 ("d_max", C.c_int32), ("tau", C.c_float), ("temperature", C.c_float),
-                ("seed", C.c_uint64)]
+                ("seed", C.c_uint64), ("skip_attn_mask", C.c_uint64 * 4),
+                ("skip_mlp_mask", C.c_uint64 * 4)]
 
 
 class SsdStats(C.Structure):

@@ -71,6 +71,7 @@ struct ssd_ctx {
   bool has_policy = false;
   int s0 = 0;
   std::vector<int> pre, post, verify_layers;
+  std::vector<int> post_parts;  // per post layer: 1 attention runs, 2 MLP runs
 
   // device buffers
   bf16* kc = nullptr;
@@ -148,7 +149,13 @@ size_t kv_layer_elems(const ssd_config& g) {
 }
 int qkv_rows(const ssd_config& g) { return (g.n_heads + 2 * g.n_kv_heads) * g.head_dim; }
 
-bool skipped(const ssd_policy& p, int l) { return (p.skip_mask[l >> 6] >> (l & 63)) & 1ull; }
+bool bit(const uint64_t* m, int l) { return (m[l >> 6] >> (l & 63)) & 1ull; }
+bool skipped(const ssd_policy& p, int l) { return bit(p.skip_mask, l); }
+// Sublayers of layer l the draft runs (skip mode): 1 attention, 2 MLP.
+int draft_parts(const ssd_policy& p, int l) {
+  if (skipped(p, l)) return 0;
+  return (bit(p.skip_attn_mask, l) ? 0 : 1) | (bit(p.skip_mlp_mask, l) ? 0 : 2);
+}
 
 // Bounded host wait on the context stream.
 ssd_status wait_stream(ssd_ctx* c) {
@@ -350,8 +357,9 @@ BeginArgs begin_args(ssd_ctx* c, int mode, int M, int pos0, const int32_t* toks_
   return b;
 }
 
-ssd_status enq_layer(ssd_ctx* c, int l, cudaStream_t s) {
+ssd_status enq_layer(ssd_ctx* c, int l, cudaStream_t s, int parts = 3) {
   ssd_status r;
+  if (!(parts & 1)) goto mlp;
   prof_begin(c, 0);
   if ((r = note(c, launch_gemv(IN_NORM, EPI_STORE, qkv_args(c, l), s, c->pdl), "qkv")) != SSD_OK)
     return r;
@@ -361,6 +369,8 @@ ssd_status enq_layer(ssd_ctx* c, int l, cudaStream_t s) {
   if ((r = note(c, launch_gemv(IN_BF16, EPI_RESID, oproj_args(c, l), s, c->pdl), "o_proj")) !=
       SSD_OK)
     return r;
+mlp:
+  if (!(parts & 2)) return SSD_OK;
   prof_begin(c, 3);
   if ((r = note(c, launch_gemv(IN_NORM, EPI_SWIGLU, gateup_args(c, l), s, c->pdl), "gate_up")) !=
       SSD_OK)
@@ -369,9 +379,10 @@ ssd_status enq_layer(ssd_ctx* c, int l, cudaStream_t s) {
   return note(c, launch_gemv(IN_BF16, EPI_RESID, down_args(c, l), s, c->pdl), "down");
 }
 
-ssd_status enq_layers(ssd_ctx* c, const std::vector<int>& ls, cudaStream_t s) {
-  for (int l : ls) {
-    const ssd_status r = enq_layer(c, l, s);
+ssd_status enq_layers(ssd_ctx* c, const std::vector<int>& ls, cudaStream_t s,
+                      const std::vector<int>* parts = nullptr) {
+  for (size_t i = 0; i < ls.size(); ++i) {
+    const ssd_status r = enq_layer(c, ls[i], s, parts ? (*parts)[i] : 3);
     if (r != SSD_OK) return r;
   }
   return SSD_OK;
@@ -428,14 +439,20 @@ struct PassBuilder {
   void control(const PassPhase& p) { ph.push_back(p); }
 };
 
-void pb_layers(ssd_ctx* c, PassBuilder& B, const std::vector<int>& ls) {
+void pb_layers(ssd_ctx* c, PassBuilder& B, const std::vector<int>& ls,
+               const std::vector<int>* parts = nullptr) {
   const ssd_config& g = c->cfg;
-  for (int l : ls) {
-    B.gemv(IN_NORM, EPI_STORE, qkv_args(c, l), (unsigned)(qkv_rows(g) / 16));
-    B.attention(attn_args(c, l));
-    B.gemv(IN_BF16, EPI_RESID, oproj_args(c, l), (unsigned)(g.d_model / 16));
-    B.gemv(IN_NORM, EPI_SWIGLU, gateup_args(c, l), (unsigned)(g.ffn_dim / 16));
-    B.gemv(IN_BF16, EPI_RESID, down_args(c, l), (unsigned)(g.d_model / 16));
+  for (size_t i = 0; i < ls.size(); ++i) {
+    const int l = ls[i], pt = parts ? (*parts)[i] : 3;
+    if (pt & 1) {
+      B.gemv(IN_NORM, EPI_STORE, qkv_args(c, l), (unsigned)(qkv_rows(g) / 16));
+      B.attention(attn_args(c, l));
+      B.gemv(IN_BF16, EPI_RESID, oproj_args(c, l), (unsigned)(g.d_model / 16));
+    }
+    if (pt & 2) {
+      B.gemv(IN_NORM, EPI_SWIGLU, gateup_args(c, l), (unsigned)(g.ffn_dim / 16));
+      B.gemv(IN_BF16, EPI_RESID, down_args(c, l), (unsigned)(g.d_model / 16));
+    }
   }
 }
 
@@ -492,7 +509,7 @@ ssd_status build_pass_programs(ssd_ctx* c) {
     sv.kind = PK_SAVE;
     sv.use_d = 0;
     B.control(sv);
-    pb_layers(c, B, c->post);
+    pb_layers(c, B, c->post, &c->post_parts);
     B.gemv(IN_NORM, EPI_LMHEAD, lm_args(c, c->dstats, c->dlogits, &c->st->slot, 0), 1u);
     PassPhase de;
     de.kind = PK_DRAFT_END;
@@ -573,7 +590,7 @@ ssd_status b_draft(ssd_ctx* c, cudaStream_t s) {
   if ((r = note(c, launch_save_boundary(c->st, 0, c->x, c->ss, c->bx, c->bss, c->cfg.d_model, s,
                                         c->pdl), "save_boundary")) != SSD_OK)
     return r;
-  if ((r = enq_layers(c, c->post, s)) != SSD_OK) return r;
+  if ((r = enq_layers(c, c->post, s, &c->post_parts)) != SSD_OK) return r;
   if ((r = enq_lmhead(c, c->dstats, c->dlogits, &c->st->slot, 0, s)) != SSD_OK) return r;
   return note(c, launch_draft_end(c->st, c->dstats, c->pol.tau, c->pol.temperature, s, c->pdl),
               "draft_end");
@@ -668,6 +685,18 @@ double pass_bytes(const ssd_ctx* c, int n_layers_run, bool lm, int pos0, int M) 
   return b;
 }
 
+// algorithmic bytes of one draft step at position pos: the layers below s0,
+// the sublayers the draft runs above it, and the LM head
+double draft_bytes(const ssd_ctx* c, int pos) {
+  const ssd_config& g = c->cfg;
+  const double attn_w = 2.0 * ((double)qkv_rows(g) * g.d_model + (double)g.d_model * g.n_heads * g.head_dim);
+  const double mlp_w = 2.0 * 3.0 * g.d_model * g.ffn_dim;
+  const double kv = 2.0 * 2.0 * g.n_kv_heads * g.head_dim * (double)(pos + 2);
+  double b = c->pre.size() * (attn_w + kv + mlp_w);
+  for (int pt : c->post_parts) b += ((pt & 1) ? attn_w + kv : 0.0) + ((pt & 2) ? mlp_w : 0.0);
+  return b + 2.0 * (double)g.vocab * g.d_model;
+}
+
 ssd_status check_capacity(ssd_ctx* c, int extra) {
   if (c->h_st->n + extra > c->cfg.max_seq)
     return fail(c, SSD_ERR_CAPACITY, "KV cache capacity (max_seq) exceeded");
@@ -683,7 +712,7 @@ ssd_status run_draft(ssd_ctx* c, ssd_stats* stats) {
     if ((r = read_state(c)) != SSD_OK) return r;
     if (stats) {
       stats->draft_steps++;
-      stats->bytes_streamed += pass_bytes(c, (int)(c->pre.size() + c->post.size()), true, n - 1 + j, 1);
+      stats->bytes_streamed += draft_bytes(c, n - 1 + j);
     }
     if (c->h_st->stop) break;
   }
@@ -883,17 +912,30 @@ ssd_status ssd_set_policy(ssd_ctx* c, const ssd_policy* p) {
     return fail(c, SSD_ERR_INVALID_ARG, "temperature");
   if (c->phase == PH_DRAFTED || c->phase == PH_VERIFIED)
     return fail(c, SSD_ERR_STATE, "a round is in flight");
+  for (int l = L; l < 256; ++l)
+    if (bit(p->skip_mask, l) || bit(p->skip_attn_mask, l) || bit(p->skip_mlp_mask, l))
+      return fail(c, SSD_ERR_INVALID_ARG, "skip masks name layers >= n_layers");
+  if (p->mode == SSD_MODE_EXIT)
+    for (int w = 0; w < 4; ++w)
+      if (p->skip_attn_mask[w] || p->skip_mlp_mask[w])
+        return fail(c, SSD_ERR_INVALID_ARG, "sublayer masks need skip mode");
   c->pol = *p;
   c->pre.clear();
   c->post.clear();
+  c->post_parts.clear();
   c->verify_layers.clear();
   if (p->mode == SSD_MODE_SKIP) {
     c->s0 = L;
     for (int l = 0; l < L; ++l)
-      if (skipped(*p, l)) { c->s0 = l; break; }
+      if (draft_parts(*p, l) != 3) { c->s0 = l; break; }
     for (int l = 0; l < L; ++l) {
-      if (l < c->s0) c->pre.push_back(l);
-      else if (!skipped(*p, l)) c->post.push_back(l);
+      const int pt = draft_parts(*p, l);
+      if (l < c->s0) {
+        c->pre.push_back(l);
+      } else if (pt) {
+        c->post.push_back(l);
+        c->post_parts.push_back(pt);
+      }
     }
   } else {
     c->s0 = p->exit_layer + 1;

@@ -146,6 +146,20 @@ LLAMA7B_SWIFT = Workload(
     policy=Policy(mode="skip", skip=_odd(9, 31), d_max=8, tau=0.8),
 )
 
+LLAMA7B_SUBLAYER = Workload(
+    # sub-layer drafting on the 7B shape (SWIFT Fig. 10): the draft drops the
+    # attention sublayer of the odd layers 9..31 and the MLP sublayer of the
+    # even layers 10..30 (as many sublayers as the whole-layer c1 set)
+    name="llama2-7b-swift-sublayer",
+    shape=_LLAMA7B,
+    scaled_layers=_odd(9, 31),
+    scale=0.1,
+    prompt_len=512,
+    gen_len=256,
+    policy=Policy(mode="skip", skip_attn=_odd(9, 31),
+                  skip_mlp=tuple(l for l in range(10, 31) if l % 2 == 0), d_max=8, tau=None),
+)
+
 LLAMA7B_LAYERSKIP = Workload(
     name="llama2-7b-layerskip-exit8",
     shape=_LLAMA7B,
@@ -183,7 +197,7 @@ LLAMA70B_SWIFT = Workload(
 )
 
 WORKLOADS = {w.name: w for w in (TINY, LLAMA7B_SWIFT, LLAMA7B_LAYERSKIP, LLAMA13B_SCORE,
-                                 LLAMA70B_SWIFT)}
+                                 LLAMA70B_SWIFT, LLAMA7B_SUBLAYER)}
 
 
 def shrink(w: Workload, **shape_changes) -> Workload:

@@ -50,6 +50,11 @@ CASES = [
     (SMALL_GQA, Policy(mode="exit", exit_layer=2, d_max=12, tau=None)),
     (MID, Policy(mode="skip", skip=(1, 2), d_max=8, tau=0.1)),
     (MID, Policy(mode="exit", exit_layer=0, d_max=6, tau=None)),
+    # sub-layer drops (SWIFT Fig. 10): attention-only, MLP-only and mixed
+    (TINY, Policy(mode="skip", skip_attn=(2,), d_max=4, tau=None)),
+    (TINY, Policy(mode="skip", skip_mlp=(1, 3), d_max=5, tau=0.2)),
+    (SMALL_GQA, Policy(mode="skip", skip=(4,), skip_attn=(2,), skip_mlp=(3,), d_max=6, tau=None)),
+    (MID, Policy(mode="skip", skip_attn=(1,), skip_mlp=(2,), d_max=8, tau=None)),
 ]
 
 
@@ -129,6 +134,8 @@ def test_ar_greedy_matches_oracle(ssd):
     (TINY, Policy(mode="skip", skip=(1, 2), d_max=5, tau=0.15), 10.0),
     (SMALL_GQA, Policy(mode="exit", exit_layer=1, d_max=6, tau=None), 1.0),
     (SMALL_GQA, Policy(mode="exit", exit_layer=1, d_max=6, tau=None), 10.0),
+    (TINY, Policy(mode="skip", skip_attn=(1,), skip_mlp=(2,), d_max=5, tau=None), 10.0),
+    (SMALL_GQA, Policy(mode="skip", skip_mlp=(2, 3), d_max=6, tau=None), 10.0),
 ])
 def test_rounds_match_oracle_in_lockstep(ssd, w, pol, head):
     # Tolerances: logits within 5e-2 and confidences within 1e-3 with the
@@ -237,6 +244,16 @@ def test_sampled_rounds_match_oracle_in_lockstep(ssd, w, pol, head):
         accepted_total += rec.accepted
         rejected_total += int(rec.accepted < rec.d)
     assert rounds >= 2, rounds
+    ctx.close()
+
+
+def test_sublayer_masks_are_validated(ssd):
+    from self_speculative_decoding_gb300 import SSDError
+    ctx, _ = _ctx(ssd, TINY)
+    with pytest.raises(SSDError, match="INVALID_ARG"):
+        ctx.set_policy(Policy(mode="skip", skip_mlp=(7,), d_max=2))       # layer >= n_layers
+    with pytest.raises(SSDError, match="INVALID_ARG"):
+        ctx.set_policy(Policy(mode="exit", exit_layer=1, skip_attn=(0,), d_max=2))
     ctx.close()
 
 

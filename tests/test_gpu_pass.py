@@ -30,6 +30,7 @@ CASES = [
     (SMALL_GQA, Policy(mode="skip", skip=(2, 3), d_max=8, tau=0.1)),
     (MID, Policy(mode="skip", skip=(1, 2), d_max=5, tau=None, temperature=0.8, seed=3)),
     (MID, Policy(mode="exit", exit_layer=0, d_max=3, tau=0.05)),
+    (SMALL_GQA, Policy(mode="skip", skip_attn=(2,), skip_mlp=(3, 4), d_max=6, tau=None)),
 ]
 
 
