@@ -35,3 +35,11 @@ from .speculative import (  # noqa: F401
     accept_stochastic,
 )
 from .scoring import score_masks, score_masks_bruteforce  # noqa: F401
+from .swift import (  # noqa: F401
+    SplitMix64,
+    SwiftParams,
+    SwiftTrace,
+    swift_generate,
+    uniform_set,
+    propose,
+)
