@@ -228,6 +228,57 @@ ssd_status ssd_profile_decode(ssd_ctx* ctx, int32_t n_steps, ssd_kernel_times* o
  * (default 120000). */
 ssd_status ssd_set_timeout_ms(ssd_ctx* ctx, int32_t ms);
 
+/* SWIFT on-the-fly layer-set optimisation (SWIFT §4: optimisation
+ * alternates with confidence-aware acceleration; §4.1.1: uniform layer
+ * skipping until the context window is filled; §4.1.2: candidate layer sets
+ * proposed by random search, scored by parallel prediction of prior context
+ * tokens, the best matchness kept, the phase ending at its step limit or
+ * when the best candidate stays unchanged; §B.2: S = 1000, 300 unchanged
+ * steps, matchness > 0.95, gamma = 32).  Bayesian optimisation is not
+ * included. */
+typedef struct {
+  int32_t skip_count; /* layers every candidate skips (skip ratio x L), >= 1    */
+  int32_t lo_layer;   /* candidates skip layers in [lo_layer, n_layers)          */
+  int32_t window;     /* gamma: committed tokens a candidate is scored on       */
+  int32_t candidates; /* K per step: the incumbent, then K-1 random proposals;
+                         K * window <= max_score_rows                           */
+  int32_t max_steps;  /* step limit S                                            */
+  int32_t patience;   /* stop after this many consecutive steps the incumbent wins */
+  float target;       /* stop after a step whose best matchness exceeds this     */
+  uint64_t seed;      /* SplitMix64 (Steele, Lea, Flood 2014) seed of the proposals */
+} ssd_swift_params;
+
+typedef struct {
+  int32_t steps;        /* optimisation steps run                                */
+  int32_t stopped_by;   /* 0: still optimising when the tokens ran out;
+                           1: target; 2: step limit; 3: patience                 */
+  uint64_t final_mask[4]; /* the incumbent skip set at the end                   */
+  int64_t rounds, drafted, accepted, emitted;
+  double opt_seconds;   /* host wall time spent in scoring steps                */
+  double total_seconds; /* host wall time of the call                           */
+} ssd_swift_report;
+
+/* Generates n_tokens after the committed context with SWIFT.  The draft
+ * starts from the uniform set (layer lo + floor((2i+1)(L-lo) / (2 count)),
+ * i < count); every decoding round with the incumbent set is followed, once
+ * window + 1 tokens have been generated and while optimising, by one step
+ * that scores the incumbent and K-1 proposals (a partial Fisher-Yates shuffle
+ * of the allowed layers per proposal, one SplitMix64 stream drawn in
+ * proposal order) with ssd_score_masks over the last `window` committed
+ * tokens; the highest matchness wins, the lowest index on ties (the
+ * incumbent survives ties).  Optimisation stops after a step whose best
+ * exceeds target, after max_steps steps, or after `patience` steps the
+ * incumbent won.  Drafting uses the context's policy (skip mode: d_max,
+ * tau, temperature, seed) with the incumbent as its skip set, which stays
+ * set afterwards.  out (nullable): n_tokens ids.  Per step s < trace_cap
+ * (arrays nullable): trace_masks [s][K][4] candidates, trace_scores [s][K]
+ * matchness, trace_best [s] the winner.  Errors: INVALID_ARG, STATE (exit
+ * mode, no prefill, a round in flight), CAPACITY (tokens or K * window),
+ * CUDA, TIMEOUT. */
+ssd_status ssd_swift_generate(ssd_ctx* ctx, const ssd_swift_params* params, int32_t n_tokens,
+                              int32_t* out, uint64_t* trace_masks, float* trace_scores,
+                              int32_t* trace_best, int32_t trace_cap, ssd_swift_report* report);
+
 /* Selects how the decode passes run (the draft step, the extra pass, the
  * verify pass and the autoregressive step of LayerSkip §3 / SWIFT §4).
  * enable = 1: each pass is one launch of a persistent kernel that keeps

@@ -18,7 +18,7 @@ import torch
 
 from . import _abi
 from ._abi import (SSDError, SsdConfig, SsdLayerWeights, SsdPolicy, SsdRowStats, SsdStats,
-                   SsdWeights, SSD_MODE_EXIT, SSD_MODE_SKIP)
+                   SsdSwiftParams, SsdSwiftReport, SsdWeights, SSD_MODE_EXIT, SSD_MODE_SKIP)
 
 __all__ = ["SSDContext", "SSDError", "ops", "pack_weight", "pack_weights", "policy_struct",
            "stream_handle"]
@@ -225,6 +225,37 @@ class SSDContext:
 
     def set_timeout_ms(self, ms: int):
         self._check(_lib().ssd_set_timeout_ms(self._h, ms))
+
+    def swift_generate(self, params, n_tokens: int, trace_cap: int = 0):
+        """SWIFT layer-set optimisation while generating n_tokens (ssd.h:
+        ssd_swift_generate).  ``params`` has the fields of ssd_swift_params
+        (e.g. a ``types.SimpleNamespace``).  Returns (tokens,
+        report dict, trace) with trace = (candidate masks [steps][K] as
+        layer tuples, scores [steps][K], winners [steps]) for the first
+        ``trace_cap`` steps."""
+        p = SsdSwiftParams()
+        for f, _ in SsdSwiftParams._fields_:
+            setattr(p, f, getattr(params, f))
+        K = int(params.candidates)
+        out = np.zeros(max(n_tokens, 1), dtype=np.int32)
+        tm = np.zeros((max(trace_cap, 1), K, 4), dtype=np.uint64)
+        tsc = np.zeros((max(trace_cap, 1), K), dtype=np.float32)
+        tb = np.zeros(max(trace_cap, 1), dtype=np.int32)
+        rep = SsdSwiftReport()
+        self._check(_lib().ssd_swift_generate(
+            self._h, C.byref(p), n_tokens, out.ctypes.data, tm.ctypes.data, tsc.ctypes.data,
+            tb.ctypes.data, trace_cap, C.byref(rep)))
+        steps = min(rep.steps, trace_cap)
+        L = self.shape.n_layers
+
+        def layers(m):
+            return tuple(l for l in range(L) if (int(m[l // 64]) >> (l % 64)) & 1)
+
+        trace = ([[layers(tm[s, k]) for k in range(K)] for s in range(steps)],
+                 tsc[:steps].tolist(), tb[:steps].tolist())
+        report = {f: getattr(rep, f) for f, _ in SsdSwiftReport._fields_ if f != "final_mask"}
+        report["final"] = layers(rep.final_mask)
+        return out[:n_tokens].tolist(), report, trace
 
     def set_pass_kernel(self, enable: bool) -> bool:
         """One persistent launch per decode pass (True) or one kernel per

@@ -45,6 +45,18 @@ class SsdPolicy(C.Structure):
                 ("skip_mlp_mask", C.c_uint64 * 4)]
 
 
+class SsdSwiftParams(C.Structure):
+    _fields_ = [("skip_count", C.c_int32), ("lo_layer", C.c_int32), ("window", C.c_int32),
+                ("candidates", C.c_int32), ("max_steps", C.c_int32), ("patience", C.c_int32),
+                ("target", C.c_float), ("seed", C.c_uint64)]
+
+
+class SsdSwiftReport(C.Structure):
+    _fields_ = [("steps", C.c_int32), ("stopped_by", C.c_int32), ("final_mask", C.c_uint64 * 4),
+                ("rounds", C.c_int64), ("drafted", C.c_int64), ("accepted", C.c_int64),
+                ("emitted", C.c_int64), ("opt_seconds", C.c_double), ("total_seconds", C.c_double)]
+
+
 class SsdStats(C.Structure):
     _fields_ = [("rounds", C.c_int64), ("drafted", C.c_int64), ("accepted", C.c_int64),
                 ("emitted", C.c_int64), ("draft_steps", C.c_int64),
@@ -90,6 +102,8 @@ _SIGS = {
     "ssd_get_tokens": [_P, C.POINTER(_I), _I, C.POINTER(_I)],
     "ssd_set_timeout_ms": [_P, _I],
     "ssd_set_pass_kernel": [_P, _I, C.POINTER(C.c_int32)],
+    "ssd_swift_generate": [_P, C.POINTER(SsdSwiftParams), _I, _P, _P, _P, _P, _I,
+                           C.POINTER(SsdSwiftReport)],
     "ssd_profile_decode": [_P, _I, C.POINTER(SsdKernelTimes)],
     "ssd_last_error": [_P],
     "ssd_op_linear": [_P, _I, _I, _P, _I, _P, _P],

@@ -1177,6 +1177,137 @@ ssd_status ssd_profile_decode(ssd_ctx* c, int32_t n_steps, ssd_kernel_times* out
   return wait_stream(c);
 }
 
+ssd_status ssd_swift_generate(ssd_ctx* c, const ssd_swift_params* pp, int32_t n_tokens,
+                              int32_t* out, uint64_t* trace_masks, float* trace_scores,
+                              int32_t* trace_best, int32_t trace_cap, ssd_swift_report* rep) {
+  if (!c) return SSD_ERR_INVALID_ARG;
+  if (!pp || n_tokens < 0 || trace_cap < 0) return fail(c, SSD_ERR_INVALID_ARG, "swift arguments");
+  const ssd_swift_params P = *pp;
+  const int L = c->cfg.n_layers;
+  if (P.lo_layer < 0 || P.lo_layer >= L || P.skip_count < 1 || P.skip_count > L - P.lo_layer ||
+      P.window < 1 || P.candidates < 1 || P.candidates > 256 || P.max_steps < 0 || P.patience < 1)
+    return fail(c, SSD_ERR_INVALID_ARG, "swift parameters out of range");
+  ssd_status r = ensure_policy(c);
+  if (r != SSD_OK) return r;
+  if (c->pol.mode != SSD_MODE_SKIP) return fail(c, SSD_ERR_STATE, "swift needs a skip-mode policy");
+  if (c->phase != PH_IDLE) return fail(c, SSD_ERR_STATE, "a round is in flight");
+  if ((int64_t)P.candidates * P.window > c->cfg.max_score_rows || P.window > c->sc_len)
+    return fail(c, SSD_ERR_CAPACITY, "candidates * window exceeds max_score_rows");
+  if ((r = read_state(c)) != SSD_OK) return r;
+  const int n_start = c->h_st->n;
+  if (n_start + n_tokens + c->pol.d_max + 1 > c->cfg.max_seq)
+    return fail(c, SSD_ERR_CAPACITY, "n_tokens + d_max + 1 exceeds the KV capacity");
+  if (rep) memset(rep, 0, sizeof(*rep));
+  const auto t_begin = std::chrono::steady_clock::now();
+
+  // SplitMix64 (Steele, Lea, Flood, OOPSLA 2014)
+  uint64_t rng = P.seed;
+  auto next = [&rng]() {
+    rng += 0x9E3779B97F4A7C15ull;
+    uint64_t z = rng;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+  };
+  const int span = L - P.lo_layer;
+  auto propose = [&]() {
+    std::vector<int> pool(span);
+    for (int i = 0; i < span; ++i) pool[i] = P.lo_layer + i;
+    for (int i = 0; i < P.skip_count; ++i) {
+      const int j = i + (int)(next() % (uint64_t)(span - i));
+      std::swap(pool[i], pool[j]);
+    }
+    pool.resize(P.skip_count);
+    std::sort(pool.begin(), pool.end());
+    return pool;
+  };
+  std::vector<int> inc(P.skip_count);
+  for (int i = 0; i < P.skip_count; ++i) inc[i] = P.lo_layer + (2 * i + 1) * span / (2 * P.skip_count);
+  ssd_policy pol = c->pol;
+  auto apply = [&](const std::vector<int>& set) {
+    memset(pol.skip_mask, 0, sizeof(pol.skip_mask));
+    memset(pol.skip_attn_mask, 0, sizeof(pol.skip_attn_mask));
+    memset(pol.skip_mlp_mask, 0, sizeof(pol.skip_mlp_mask));
+    for (int l : set) pol.skip_mask[l >> 6] |= 1ull << (l & 63);
+    return ssd_set_policy(c, &pol);
+  };
+  if ((r = apply(inc)) != SSD_OK) return r;
+
+  const int K = P.candidates;
+  std::vector<uint64_t> masks((size_t)K * 4);
+  std::vector<float> scores(K);
+  std::vector<std::vector<int>> cands(K);
+  bool optimizing = true;
+  int steps = 0, unchanged = 0, stopped_by = 0, got = 0;
+  double opt_seconds = 0.0;
+  ssd_stats st{};
+  while (got < n_tokens) {
+    if ((r = run_draft(c, &st)) != SSD_OK) return r;
+    const int d = c->pol.d_max == 0 ? 0 : c->h_st->d;
+    if ((r = run_verify(c, &st)) != SSD_OK) return r;
+    if ((r = replay(c, c->g_accept)) != SSD_OK) return r;
+    if ((r = read_state(c)) != SSD_OK) return r;
+    c->phase = PH_IDLE;
+    const int ne = c->h_st->n_emitted;
+    for (int i = 0; i < ne && got < n_tokens; ++i, ++got)
+      if (out) out[got] = c->h_st->emitted[i];
+    st.rounds++;
+    st.drafted += d;
+    st.accepted += c->h_st->accepted;
+    st.emitted += ne;
+    const int generated = c->h_st->n - n_start;
+    if (!optimizing || generated < P.window + 1 || generated >= n_tokens) continue;
+    // one optimisation step: the incumbent, then K-1 proposals
+    const auto t0 = std::chrono::steady_clock::now();
+    cands[0] = inc;
+    for (int k = 1; k < K; ++k) cands[k] = propose();
+    std::fill(masks.begin(), masks.end(), 0ull);
+    for (int k = 0; k < K; ++k)
+      for (int l : cands[k]) masks[(size_t)k * 4 + (l >> 6)] |= 1ull << (l & 63);
+    if ((r = ssd_score_masks(c, masks.data(), K, P.window, scores.data(), nullptr)) != SSD_OK)
+      return r;
+    int best = 0;
+    for (int k = 1; k < K; ++k)
+      if (scores[k] > scores[best]) best = k;
+    if (steps < trace_cap) {
+      if (trace_masks) memcpy(trace_masks + (size_t)steps * K * 4, masks.data(), masks.size() * 8);
+      if (trace_scores) memcpy(trace_scores + (size_t)steps * K, scores.data(), (size_t)K * 4);
+      if (trace_best) trace_best[steps] = best;
+    }
+    ++steps;
+    if (best == 0) {
+      ++unchanged;
+    } else {
+      unchanged = 0;
+      inc = cands[best];
+      if ((r = apply(inc)) != SSD_OK) return r;
+    }
+    if (scores[best] > P.target) stopped_by = 1;
+    else if (steps >= P.max_steps) stopped_by = 2;
+    else if (unchanged >= P.patience) stopped_by = 3;
+    if (stopped_by) optimizing = false;
+    opt_seconds += std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count();
+  }
+  if (c->h_st->n != n_start + n_tokens) {   // the last round may emit past the budget
+    const int32_t nn = n_start + n_tokens;
+    CK(cudaMemcpyAsync(&c->st->n, &nn, 4, cudaMemcpyHostToDevice, c->stream));
+    if ((r = read_state(c)) != SSD_OK) return r;
+  }
+  if (rep) {
+    rep->steps = steps;
+    rep->stopped_by = stopped_by;
+    for (int l : inc) rep->final_mask[l >> 6] |= 1ull << (l & 63);
+    rep->rounds = st.rounds;
+    rep->drafted = st.drafted;
+    rep->accepted = st.accepted;
+    rep->emitted = st.emitted;
+    rep->opt_seconds = opt_seconds;
+    rep->total_seconds =
+        std::chrono::duration<double>(std::chrono::steady_clock::now() - t_begin).count();
+  }
+  return SSD_OK;
+}
+
 ssd_status ssd_set_pass_kernel(ssd_ctx* c, int32_t enable, int32_t* active_out) {
   if (!c) return SSD_ERR_INVALID_ARG;
   if (c->phase == PH_DRAFTED || c->phase == PH_VERIFIED)
