@@ -51,7 +51,10 @@ ssd_status ssd_op_linear(const void* W, int32_t R, int32_t K, const void* act, i
                          float* y, void* stream);
 
 /* y = W bf16(rmsnorm(x) * gain): the norm-fused input of the QKV projection
- * and the LM head.  x fp32 [M][K]; gain fp32 [K]; y fp32 [M][R]. */
+ * and the LM head.  x fp32 [M][K]; gain fp32 [K]; y fp32 [M][R].  When M
+ * rows of K do not fit the GEMV's per-CTA activation stage, a RMSNorm pass
+ * first writes the bf16 rows (scratch) and the projection reads them; the
+ * result is the same.  The same holds for ssd_op_swiglu and ssd_op_lm_head. */
 ssd_status ssd_op_rmsnorm_linear(const void* W, int32_t R, int32_t K, const float* x,
                                  const float* gain, float eps, int32_t M, float* y, void* stream);
 

@@ -113,7 +113,57 @@ __global__ void pack_kernel(const bf16* __restrict__ src, bf16* __restrict__ dst
   }
 }
 
+// RMSNorm of the pass's rows into bf16: out[m][k] = bf16(x[m][k] * r_m * g[k])
+// with r_m = 1 / sqrt(mean(x_m^2) + eps) from the sum-of-squares partials.
+// Every warp of a block computes r_m itself, in the consumer warps' order
+// (lane l sums partials l, l+32, ..., then a butterfly), and the products are
+// rounded as the staged layout rounds them, so a projection fed from this
+// buffer computes the bits the norm-fused input computes.
+__global__ void __launch_bounds__(256) norm_rows_kernel(const float* x, const float* ss,
+                                                        const float* gain, float eps, int M_static,
+                                                        const int32_t* M_dev, int K, bf16* out) {
+  pdl_wait();
+  pdl_trigger();
+  const int M = M_dev ? __ldcg(M_dev) : M_static;
+  const int m = blockIdx.x;
+  if (m >= M) return;
+  const int lane = threadIdx.x & 31;
+  const int NP = K / kSsGroup;
+  float s2 = 0.f;
+#pragma unroll 8
+  for (int q = lane; q < NP; q += 32) s2 += __ldcg(ss + (size_t)m * NP + q);
+  s2 = sum_warp(s2);
+  const float rs = 1.0f / sqrtf(s2 / (float)K + eps);
+  const int k0 = (blockIdx.y * 256 + threadIdx.x) * 8;
+  if (k0 >= K) return;
+  const float4* xp = reinterpret_cast<const float4*>(x + (size_t)m * K + k0);
+  const float4* gp = reinterpret_cast<const float4*>(gain + k0);
+  const float4 x0 = __ldcg(xp), x1 = __ldcg(xp + 1), g0 = gp[0], g1 = gp[1];
+  *reinterpret_cast<uint4*>(out + (size_t)m * K + k0) =
+      make_uint4(pack_bf16x2(x0.x * rs * g0.x, x0.y * rs * g0.y),
+                 pack_bf16x2(x0.z * rs * g0.z, x0.w * rs * g0.w),
+                 pack_bf16x2(x1.x * rs * g1.x, x1.y * rs * g1.y),
+                 pack_bf16x2(x1.z * rs * g1.z, x1.w * rs * g1.w));
+}
+
 }  // namespace
+
+int gemv_stage_rows(int K) { return kStageBytes / ((K + kPad) * (int)sizeof(bf16)); }
+
+cudaError_t launch_norm_rows(const float* x, const float* ss, const float* gain, float eps,
+                             int M_static, const int32_t* M_dev, int K, bf16* out, cudaStream_t st,
+                             bool pdl) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(kMaxRows, (K + 2047) / 2048);
+  lc.blockDim = dim3(256);
+  lc.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&lc, norm_rows_kernel, x, ss, gain, eps, M_static, M_dev, K, out);
+}
 
 GemvScratch gemv_scratch(int R, int K, int epi) {
   const Part p = make_part(R, K, epi);
@@ -134,6 +184,8 @@ cudaError_t launch_gemv(int in_mode, int epi, const LinearArgs& a, cudaStream_t 
   SSD_GEMV_CASE(IN_BF16, EPI_RESID)
   SSD_GEMV_CASE(IN_NORM, EPI_SWIGLU)
   SSD_GEMV_CASE(IN_NORM, EPI_LMHEAD)
+  SSD_GEMV_CASE(IN_BF16, EPI_SWIGLU)
+  SSD_GEMV_CASE(IN_BF16, EPI_LMHEAD)
 #undef SSD_GEMV_CASE
   return cudaErrorInvalidValue;
 }

@@ -574,6 +574,144 @@ SSD_DI void consume(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0, in
   rp.fl = fl;
 }
 
+// Windowed activations (bf16 input, whole-group partition, rows that do not
+// fit the stage at once): the consumer warps stage the activations of 16
+// units (512 K-columns) at a time in two shared buffers.  The loads of
+// window w + 2 are issued while window w is consumed; at the end of window w
+// they are stored into the buffer window w - 1 used, and one consumer
+// barrier publishes them.  B values and the MMA order are those of the
+// other layouts, so a row's result does not depend on the layout.
+constexpr int kWinUnits = 16;
+constexpr int kWinRow = kWinUnits * 32 * 2 + 64;   // bytes per row; rows 16 banks apart
+constexpr int kWinBytes = kMaxRows * kWinRow;
+constexpr int kWinPieces = kMaxRows * kWinUnits * 4 / (kConsumers * 32);  // 16-byte pieces per thread
+static_assert(2 * kWinBytes <= kStageBytes, "two activation windows fit the stage");
+static_assert(kWinUnits % kChunk == 0, "windows hold whole chunks");
+
+template <int EPI>
+SSD_DI void consume_win(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0, int U1, int M,
+                        int warp, int lane, RingPos& rp) {
+  const int tid = threadIdx.x;  // consumer threads are 0 .. kConsumers * 32 - 1
+  const int g = lane >> 2, c = lane & 3;
+  const bool two = M > 8;
+  const bool v0 = g < M, v1 = two && (g + 8) < M;
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  unsigned char* wb = reinterpret_cast<unsigned char*>(sm.stage);
+  const int KB = p.KB;
+  const int nwin = (KB + kWinUnits - 1) / kWinUnits;  // windows per row group
+  const int vr_end = U1 / KB;
+  uint4 pre[kWinPieces];
+  // window (vr, kw) -> registers: row m, K columns kw*512 + 8q .. + 7
+  auto load = [&](int kw) {
+    const int wu = min(kWinUnits, KB - kw * kWinUnits);
+#pragma unroll
+    for (int i = 0; i < kWinPieces; ++i) {
+      const int e = tid + i * kConsumers * 32;
+      const int m = e / (kWinUnits * 4), q = e % (kWinUnits * 4);
+      pre[i] = m < M && q < wu * 4
+                   ? __ldcg(reinterpret_cast<const uint4*>(a.act + (size_t)m * a.K +
+                                                           (size_t)kw * kWinUnits * 32 + q * 8))
+                   : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  auto store = [&](int buf) {
+#pragma unroll
+    for (int i = 0; i < kWinPieces; ++i) {
+      const int e = tid + i * kConsumers * 32;
+      const int m = e / (kWinUnits * 4), q = e % (kWinUnits * 4);
+      if (m < M) *reinterpret_cast<uint4*>(wb + buf * kWinBytes + m * kWinRow + q * 16) = pre[i];
+    }
+  };
+  // the window after (vr, kw) in this CTA's sequence, as (vr, kw); vr == vr_end: none
+  auto advance = [&](int& vr, int& kw) {
+    if (++kw == nwin) { kw = 0; ++vr; }
+  };
+  int vr = U0 / KB, kw = 0, wseq = 0;
+  load(0);
+  store(0);
+  consumer_sync();
+  int nvr = vr, nkw = kw;  // the window whose loads are in flight in `pre`
+  advance(nvr, nkw);
+  if (nvr < vr_end) load(nkw);
+
+  int kb = 0, left = U1 - U0;
+  int slot = rp.slot;
+  uint32_t ph = rp.ph;
+  int fl = rp.fl;
+  // A failed wait does not leave the loop: every consumer warp must take part
+  // in every window barrier, so a warp that gave up runs on without waiting.
+  bool okw = rp.ok;
+  while (left > 0) {
+    const int n = chunk_len(p, kb, left);
+    if (okw && !mbar_wait(&sm.full[slot], ph)) {
+      if (lane == 0) atomicExch(a.err, 3);
+      okw = false;
+    }
+    const unsigned char* wbase = wb + (wseq & 1) * kWinBytes;
+#pragma unroll
+    for (int i = 0; i < kUPW; ++i) {
+      const int un = warp + i * kConsumers;
+      if (un < n) {
+        const unsigned char* base = sm.ring + slot * kSlotBytes + un * kUnitBytes;
+        const uint4 wa = *reinterpret_cast<const uint4*>(base + lane * 16);
+        const uint4 wbv = *reinterpret_cast<const uint4*>(base + 512 + lane * 16);
+        const int col = ((kb - kw * kWinUnits) + un) * 64 + c * 16;  // bytes into the row
+        const uint4 xa = v0 ? *reinterpret_cast<const uint4*>(wbase + g * kWinRow + col)
+                            : make_uint4(0u, 0u, 0u, 0u);
+        mma_bf16(acc[0], wa.x, wbv.x, wa.y, wbv.y, xa.x, xa.y);
+        mma_bf16(acc[0], wa.z, wbv.z, wa.w, wbv.w, xa.z, xa.w);
+        if (two) {
+          const uint4 xb = v1 ? *reinterpret_cast<const uint4*>(wbase + (g + 8) * kWinRow + col)
+                              : make_uint4(0u, 0u, 0u, 0u);
+          mma_bf16(acc[1], wa.x, wbv.x, wa.y, wbv.y, xb.x, xb.y);
+          mma_bf16(acc[1], wa.z, wbv.z, wa.w, wbv.w, xb.z, xb.w);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[slot]);
+    if (++slot == kSlots) { slot = 0; ph ^= 1u; }
+    kb += n;
+    left -= n;
+    const bool group_done = kb == KB;
+    const bool win_done = group_done || kb % kWinUnits == 0;
+    if (win_done && left > 0) {
+      // the next window (loaded one window ago) goes into the other buffer
+      store((wseq + 1) & 1);
+      consumer_sync();
+      ++wseq;
+      advance(vr, kw);
+      advance(nvr, nkw);
+      if (nvr < vr_end) load(nkw);
+    }
+    if (group_done) kb = 0;
+    if (!group_done) continue;
+    {
+      const int buf = fl & 1;
+      if (okw && fl >= 2 && !mbar_wait(&sm.rempty[buf], ((fl >> 1) - 1) & 1)) {
+        if (lane == 0) atomicExch(a.err, 5);
+        okw = false;
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int tok = h * 8 + 2 * c;
+        sm.red[buf][warp][g][tok] = acc[h][0];
+        sm.red[buf][warp][g][tok + 1] = acc[h][1];
+        sm.red[buf][warp][g + 8][tok] = acc[h][2];
+        sm.red[buf][warp][g + 8][tok + 1] = acc[h][3];
+        acc[h][0] = acc[h][1] = acc[h][2] = acc[h][3] = 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.rfull[buf]);
+      ++fl;
+    }
+  }
+  rp.slot = slot;
+  rp.ph = ph;
+  rp.fl = fl;
+  rp.ok = okw;
+}
+
 // Producer warp (lane 0 issues): streams CTA b's units of one GEMV into the
 // ring.  Weights never depend on earlier phases, so the producer runs ahead
 // of the consumers, bounded only by free ring slots.
@@ -803,6 +941,8 @@ SSD_DI void consumer_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int
     }
     consumer_sync();
     consume<IN, EPI, true>(a, p, sm, U0, U1, M, warp, lane, rp);
+  } else if (IN == IN_BF16 && p.G == p.KB * (EPI == EPI_SWIGLU ? 2 : 1)) {
+    consume_win<EPI>(a, p, sm, U0, U1, M, warp, lane, rp);
   } else {
     consume<IN, EPI, false>(a, p, sm, U0, U1, M, warp, lane, rp);
   }

@@ -57,6 +57,16 @@ GemvScratch gemv_scratch(int R, int K, int epi);
 // W0 / W1 must be in the packed unit layout written by launch_pack.
 cudaError_t launch_gemv(int in_mode, int epi, const LinearArgs& a, cudaStream_t st, bool pdl);
 
+// Rows whose activations (K columns) fit the per-CTA stage at once.
+int gemv_stage_rows(int K);
+
+// out[m][k] = bf16(rmsnorm(x_m)[k] * gain[k]) for the pass's rows, computed
+// exactly as the norm-fused GEMV input computes it (for passes whose rows do
+// not fit the stage: the projection then reads bf16 activations).
+cudaError_t launch_norm_rows(const float* x, const float* ss, const float* gain, float eps,
+                             int M_static, const int32_t* M_dev, int K, bf16* out, cudaStream_t st,
+                             bool pdl);
+
 // Row-major W [R][K] -> packed 16x32 units in tensor-core fragment order.
 cudaError_t launch_pack(const bf16* src, bf16* dst, int R, int K, cudaStream_t st);
 

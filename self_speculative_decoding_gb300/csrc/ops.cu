@@ -69,6 +69,24 @@ struct GemvOpScratch {
   }
 };
 
+// A norm-fused projection: when the rows do not fit the GEMV's activation
+// stage, a RMSNorm pre-pass writes bf16 rows and the projection reads those
+// (the same bits; what the context runtime does for wide passes).
+ssd_status launch_norm_fused(int epi, LinearArgs a, cudaStream_t s, Scratch& xn, const char* what) {
+  if (a.M_static <= gemv_stage_rows(a.K)) return cu(launch_gemv(IN_NORM, epi, a, s, false), what);
+  ssd_status r;
+  if ((r = cu(xn.alloc((size_t)a.M_static * a.K * sizeof(bf16)), "scratch")) != SSD_OK) return r;
+  if ((r = cu(launch_norm_rows(a.x, a.ss, a.gain, a.eps, a.M_static, nullptr, a.K, (bf16*)xn.p, s,
+                               false),
+              "rmsnorm")) != SSD_OK)
+    return r;
+  a.act = (const bf16*)xn.p;
+  a.x = nullptr;
+  a.ss = nullptr;
+  a.gain = nullptr;
+  return cu(launch_gemv(IN_BF16, epi, a, s, false), what);
+}
+
 }  // namespace
 
 extern "C" {
@@ -127,7 +145,8 @@ ssd_status ssd_op_rmsnorm_linear(const void* W, int32_t R, int32_t K, const floa
   a.y = y;
   GemvOpScratch gs(s);
   if ((r = gs.init(R, K, EPI_STORE, a, s)) != SSD_OK) return r;
-  return cu(launch_gemv(IN_NORM, EPI_STORE, a, s, false), "rmsnorm_linear");
+  Scratch xn(s);
+  return launch_norm_fused(EPI_STORE, a, s, xn, "rmsnorm_linear");
 }
 
 ssd_status ssd_op_residual_linear(const void* W, int32_t R, int32_t K, const void* act, int32_t M,
@@ -174,7 +193,8 @@ ssd_status ssd_op_swiglu(const void* Wg, const void* Wu, int32_t F, int32_t K, c
   a.u = (bf16*)u;
   GemvOpScratch gs(s);
   if ((r = gs.init(F, K, EPI_SWIGLU, a, s)) != SSD_OK) return r;
-  return cu(launch_gemv(IN_NORM, EPI_SWIGLU, a, s, false), "swiglu");
+  Scratch xn(s);
+  return launch_norm_fused(EPI_SWIGLU, a, s, xn, "swiglu");
 }
 
 ssd_status ssd_op_attention(const float* qkv, int32_t M, int32_t pos0, void* k_cache,
@@ -251,7 +271,8 @@ ssd_status ssd_op_lm_head(const void* W, int32_t V, int32_t D, const float* x, c
   a.round_static = round;
   a.sample_stream = stream_id;
   a.pos0_static = pos0;
-  return cu(launch_gemv(IN_NORM, EPI_LMHEAD, a, s, false), "lm_head");
+  Scratch xn(s);
+  return launch_norm_fused(EPI_LMHEAD, a, s, xn, "lm_head");
 }
 
 ssd_status ssd_op_accept_stochastic(const float* P, const float* Q, const int32_t* drafts,

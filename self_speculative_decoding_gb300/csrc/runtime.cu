@@ -83,6 +83,7 @@ struct ssd_ctx {
   float* qkv = nullptr;
   bf16* attn = nullptr;
   bf16* u = nullptr;
+  bf16* xn = nullptr;           // normalised bf16 rows for passes too wide for the GEMV stage
   float2* rope = nullptr;
   float* attn_part = nullptr;
   unsigned* attn_cnt = nullptr;
@@ -110,6 +111,8 @@ struct ssd_ctx {
   Graph g_draft, g_extra, g_verify, g_accept, g_ar;
   // persistent pass kernel programs (one launch per draft step / extra pass /
   // verify pass / AR step) and whether they are used
+  // static row bound of the passes being enqueued (0: up to 16 rows)
+  int mmax = 0;
   bool use_pass = false;
   bool pass_ok = false;
   PassDev p_draft, p_extra, p_verify, p_ar;
@@ -357,12 +360,31 @@ BeginArgs begin_args(ssd_ctx* c, int mode, int M, int pos0, const int32_t* toks_
   return b;
 }
 
+// A norm-fused projection of a pass whose rows may not fit the GEMV's
+// activation stage runs as a RMSNorm pre-pass into bf16 rows plus a bf16-input
+// projection (same bits, bounded shared memory).
+ssd_status enq_norm_gemv(ssd_ctx* c, int epi, const LinearArgs& a, cudaStream_t s,
+                         const char* what) {
+  const int mm = c->mmax ? c->mmax : kMaxRows;
+  if (mm <= gemv_stage_rows(a.K)) return note(c, launch_gemv(IN_NORM, epi, a, s, c->pdl), what);
+  ssd_status r = note(c, launch_norm_rows(a.x, a.ss, a.gain, a.eps, a.M_static, a.M_dev, a.K, c->xn,
+                                          s, c->pdl),
+                      "rmsnorm");
+  if (r != SSD_OK) return r;
+  if (c->profiling) prof_begin(c, 6);
+  LinearArgs b = a;
+  b.act = c->xn;
+  b.x = nullptr;
+  b.ss = nullptr;
+  b.gain = nullptr;
+  return note(c, launch_gemv(IN_BF16, epi, b, s, c->pdl), what);
+}
+
 ssd_status enq_layer(ssd_ctx* c, int l, cudaStream_t s, int parts = 3) {
   ssd_status r;
   if (!(parts & 1)) goto mlp;
   prof_begin(c, 0);
-  if ((r = note(c, launch_gemv(IN_NORM, EPI_STORE, qkv_args(c, l), s, c->pdl), "qkv")) != SSD_OK)
-    return r;
+  if ((r = enq_norm_gemv(c, EPI_STORE, qkv_args(c, l), s, "qkv")) != SSD_OK) return r;
   prof_begin(c, 1);
   if ((r = note(c, launch_attention(attn_args(c, l), s, c->pdl), "attention")) != SSD_OK) return r;
   prof_begin(c, 2);
@@ -372,9 +394,7 @@ ssd_status enq_layer(ssd_ctx* c, int l, cudaStream_t s, int parts = 3) {
 mlp:
   if (!(parts & 2)) return SSD_OK;
   prof_begin(c, 3);
-  if ((r = note(c, launch_gemv(IN_NORM, EPI_SWIGLU, gateup_args(c, l), s, c->pdl), "gate_up")) !=
-      SSD_OK)
-    return r;
+  if ((r = enq_norm_gemv(c, EPI_SWIGLU, gateup_args(c, l), s, "gate_up")) != SSD_OK) return r;
   prof_begin(c, 4);
   return note(c, launch_gemv(IN_BF16, EPI_RESID, down_args(c, l), s, c->pdl), "down");
 }
@@ -391,9 +411,8 @@ ssd_status enq_layers(ssd_ctx* c, const std::vector<int>& ls, cudaStream_t s,
 ssd_status enq_lmhead(ssd_ctx* c, RowStats* stats, float* logits, const int32_t* slot_dev,
                       int sample_stream, cudaStream_t s) {
   prof_begin(c, 5);
-  return note(c, launch_gemv(IN_NORM, EPI_LMHEAD, lm_args(c, stats, logits, slot_dev, sample_stream),
-                             s, c->pdl),
-              "lm_head");
+  return enq_norm_gemv(c, EPI_LMHEAD, lm_args(c, stats, logits, slot_dev, sample_stream), s,
+                       "lm_head");
 }
 
 ssd_status enq_begin(ssd_ctx* c, int mode, cudaStream_t s, int M = 1, int pos0 = 0,
@@ -582,7 +601,14 @@ ssd_status build_graph(ssd_ctx* c, Graph& g, Builder fn) {
   return SSD_OK;
 }
 
+ssd_status b_draft_body(ssd_ctx* c, cudaStream_t s);
 ssd_status b_draft(ssd_ctx* c, cudaStream_t s) {
+  c->mmax = 1;
+  const ssd_status r = b_draft_body(c, s);
+  c->mmax = 0;
+  return r;
+}
+ssd_status b_draft_body(ssd_ctx* c, cudaStream_t s) {
   if (pass_active(c)) return note(c, launch_pass(c->p_draft.prog, s), "draft pass");
   ssd_status r;
   if ((r = enq_begin(c, BEGIN_DRAFT, s)) != SSD_OK) return r;
@@ -596,7 +622,14 @@ ssd_status b_draft(ssd_ctx* c, cudaStream_t s) {
               "draft_end");
 }
 
+ssd_status b_extra_body(ssd_ctx* c, cudaStream_t s);
 ssd_status b_extra(ssd_ctx* c, cudaStream_t s) {
+  c->mmax = 1;
+  const ssd_status r = b_extra_body(c, s);
+  c->mmax = 0;
+  return r;
+}
+ssd_status b_extra_body(ssd_ctx* c, cudaStream_t s) {
   if (pass_active(c)) return note(c, launch_pass(c->p_extra.prog, s), "extra pass");
   ssd_status r;
   if ((r = enq_begin(c, BEGIN_EXTRA, s)) != SSD_OK) return r;
@@ -605,7 +638,14 @@ ssd_status b_extra(ssd_ctx* c, cudaStream_t s) {
                                       c->pdl), "save_boundary");
 }
 
+ssd_status b_verify_body(ssd_ctx* c, cudaStream_t s);
 ssd_status b_verify(ssd_ctx* c, cudaStream_t s) {
+  c->mmax = c->pol.d_max + 1;
+  const ssd_status r = b_verify_body(c, s);
+  c->mmax = 0;
+  return r;
+}
+ssd_status b_verify_body(ssd_ctx* c, cudaStream_t s) {
   if (pass_active(c)) return note(c, launch_pass(c->p_verify.prog, s), "verify pass");
   ssd_status r;
   if ((r = enq_begin(c, BEGIN_VERIFY, s)) != SSD_OK) return r;
@@ -630,7 +670,14 @@ ssd_status b_accept(ssd_ctx* c, cudaStream_t s) {
   return note(c, launch_accept_greedy(c->st, c->tokens, c->vstats, s, c->pdl), "accept");
 }
 
+ssd_status b_ar_body(ssd_ctx* c, cudaStream_t s);
 ssd_status b_ar(ssd_ctx* c, cudaStream_t s) {
+  c->mmax = 1;
+  const ssd_status r = b_ar_body(c, s);
+  c->mmax = 0;
+  return r;
+}
+ssd_status b_ar_body(ssd_ctx* c, cudaStream_t s) {
   if (pass_active(c)) return note(c, launch_pass(c->p_ar.prog, s), "ar pass");
   ssd_status r;
   if ((r = enq_begin(c, BEGIN_AR, s)) != SSD_OK) return r;
@@ -805,6 +852,7 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
             alloc((void**)&c->qkv, (size_t)nr * qkv_rows(g) * 4) &&
             alloc((void**)&c->attn, (size_t)nr * g.n_heads * g.head_dim * 2) &&
             alloc((void**)&c->u, (size_t)nr * F * 2) &&
+            alloc((void**)&c->xn, (size_t)nr * D * 2) &&
             alloc((void**)&c->rope, (size_t)g.max_seq * (g.head_dim / 2) * sizeof(float2)) &&
             alloc((void**)&c->attn_part,
                   attn_part_floats(g.n_kv_heads, g.n_heads, g.head_dim, g.max_seq) * 4) &&
@@ -880,7 +928,7 @@ ssd_status ssd_destroy(ssd_ctx* c) {
   c->p_extra.reset();
   c->p_verify.reset();
   c->p_ar.reset();
-  void* bufs[] = {c->kc, c->vc, c->x, c->ss, c->bx, c->bss, c->qkv, c->attn, c->u, c->rope,
+  void* bufs[] = {c->kc, c->vc, c->x, c->ss, c->bx, c->bss, c->qkv, c->attn, c->u, c->xn, c->rope,
                   c->attn_part, c->attn_cnt, c->g_part, c->g_cnt, c->g_rec, c->dstats, c->vstats,
                   c->dlogits, c->vlogits, c->tokens, c->toks_in, c->st};
   for (void* p : bufs)

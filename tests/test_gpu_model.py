@@ -38,6 +38,12 @@ MID = Workload(name="mid-dh128", shape=ModelShape(
     n_layers=4, d_model=1024, n_heads=8, n_kv_heads=8, head_dim=128, ffn_dim=2816, vocab=4096),
     scaled_layers=(1, 2), scale=0.1)
 
+# wide enough that a verify pass of more than 6 rows does not fit the GEMV's
+# activation stage: the norm pre-pass and the windowed activation layout run
+WIDE = Workload(name="wide-d4096", shape=ModelShape(
+    n_layers=3, d_model=4096, n_heads=32, n_kv_heads=8, head_dim=128, ffn_dim=2048, vocab=4096),
+    scaled_layers=(1,), scale=0.1)
+
 CASES = [
     (TINY, Policy(mode="skip", skip=(2,), d_max=4, tau=None)),
     (TINY, Policy(mode="skip", skip=(2,), d_max=4, tau=0.5)),
@@ -55,6 +61,8 @@ CASES = [
     (TINY, Policy(mode="skip", skip_mlp=(1, 3), d_max=5, tau=0.2)),
     (SMALL_GQA, Policy(mode="skip", skip=(4,), skip_attn=(2,), skip_mlp=(3,), d_max=6, tau=None)),
     (MID, Policy(mode="skip", skip_attn=(1,), skip_mlp=(2,), d_max=8, tau=None)),
+    (WIDE, Policy(mode="skip", skip=(1,), d_max=8, tau=None)),
+    (WIDE, Policy(mode="exit", exit_layer=0, d_max=12, tau=None)),
 ]
 
 
@@ -136,6 +144,7 @@ def test_ar_greedy_matches_oracle(ssd):
     (SMALL_GQA, Policy(mode="exit", exit_layer=1, d_max=6, tau=None), 10.0),
     (TINY, Policy(mode="skip", skip_attn=(1,), skip_mlp=(2,), d_max=5, tau=None), 10.0),
     (SMALL_GQA, Policy(mode="skip", skip_mlp=(2, 3), d_max=6, tau=None), 10.0),
+    (WIDE, Policy(mode="exit", exit_layer=0, d_max=10, tau=None), 1.0),
 ])
 def test_rounds_match_oracle_in_lockstep(ssd, w, pol, head):
     # Tolerances: logits within 5e-2 and confidences within 1e-3 with the
