@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(attn::kGroupThreads, 3) attn_kernel(AttnArgs a
 size_t attn_smem(const AttnArgs& a) { return attn::smem_bytes(a.dh, a.max_seq / kAttnChunk); }
 
 size_t attn_part_floats(int Hkv, int H, int dh, int max_seq) {
-  return (size_t)Hkv * (max_seq / kAttnChunk) * (H / Hkv) * kMaxRows * (dh + 2);
+  return (size_t)Hkv * (max_seq / kAttnChunk) * (H / Hkv) * kMaxRows * (dh + attn::kRecPad);
 }
 
 static int sm_count() {

@@ -26,6 +26,9 @@ namespace attn {
 constexpr int kGroupThreads = 256;  // threads that execute an item
 constexpr int kGroupWarps = kGroupThreads / 32;
 constexpr int kKPad = 8;            // bf16 padding per cached key row
+// A chunk's partial record per (head, row): max score, sum of exponentials,
+// two pad words, then the unnormalised output (16-byte aligned).
+constexpr int kRecPad = 4;
 
 // Shared memory of one item (offsets multiples of 16 B):
 //   K [64][dh + 8] bf16 | V [64][dh] bf16 | Q [16][dh] f32 | S [16][64] f32
@@ -151,7 +154,7 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
     ++phase;
   }
 
-  float* part_base = a.part + ((size_t)kvh * nchunk_max + c) * rows * (dh + 2);
+  float* part_base = a.part + ((size_t)kvh * nchunk_max + c) * rows * (dh + kRecPad);
   for (int gh = 0; gh < G; ++gh) {
     sync();  // K/V complete; the previous head's S and Q are no longer read
     // (3) queries of this head, RoPE'd, fp32
@@ -212,8 +215,8 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
       srow[lane] = p0;
       srow[lane + 32] = p1;
       if (lane == 0) {
-        part_base[(size_t)r * (dh + 2) + 0] = mx;
-        part_base[(size_t)r * (dh + 2) + 1] = l;
+        part_base[(size_t)r * (dh + kRecPad) + 0] = mx;
+        part_base[(size_t)r * (dh + kRecPad) + 1] = l;
       }
     }
     sync();
@@ -224,7 +227,7 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
       const float* p = sm.S + (size_t)m * kAttnChunk;
       float o = 0.f;
       for (int j = 0; j < nk; ++j) o = fmaf(p[j], __bfloat162float(sm.V[j * dh + dd]), o);
-      part_base[(size_t)r * (dh + 2) + 2 + dd] = o;
+      part_base[(size_t)r * (dh + kRecPad) + kRecPad + dd] = o;
     }
   }
   __threadfence();
@@ -241,7 +244,7 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
     // exp(m_c - max_c m_c), L = sum_c l_c w_c and O = sum_c o_c w_c, each sum
     // in chunk order.  All rows at once when their (m, l, w) fit in this
     // item's shared memory, else one row at a time.
-    const float* hb = a.part + (size_t)kvh * nchunk_max * rows * (dh + 2);
+    const float* hb = a.part + (size_t)kvh * nchunk_max * rows * (dh + kRecPad);
     const int R = G * M;
     float* CM = reinterpret_cast<float*>(sm.K);
     float* CL = CM + R * n_active;
@@ -253,7 +256,7 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
         const int rr = e / n_active, cc = e % n_active;
         const int m = rr % M, r = (rr / M) * kMaxRows + m;
         if (cc <= (pos0 + m) / kAttnChunk) {
-          const float* pc = hb + ((size_t)cc * rows + r) * (dh + 2);
+          const float* pc = hb + ((size_t)cc * rows + r) * (dh + kRecPad);
           CM[e] = __ldcg(pc);
           CL[e] = __ldcg(pc + 1);
         }
@@ -274,33 +277,72 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
         LR[rr] = L;
       }
       sync();
-      for (int e = tid; e < R * dh; e += kGroupThreads) {
-        const int rr = e / dh, dd = e % dh;
-        const int m = rr % M, gh = rr / M, r = gh * kMaxRows + m;
-        const int nc = (pos0 + m) / kAttnChunk + 1;
-        const float* w = CW + rr * n_active;
-        const float* ob = hb + (size_t)r * (dh + 2) + 2 + dd;
-        const size_t cs = (size_t)rows * (dh + 2);
-        float O = 0.f;
-        int cc = 0;
-        for (; cc + 4 <= nc; cc += 4) {
-          float o[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) o[q] = __ldcg(ob + (size_t)(cc + q) * cs);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) O = fmaf(o[q], w[cc + q], O);
+      // the chunks' output vectors of a batch of rows go to shared memory in
+      // one parallel pass, then every output sums them in chunk order
+      const size_t cs = (size_t)rows * (dh + kRecPad);
+      const size_t used = ((size_t)3 * R * n_active + R + 3) & ~(size_t)3;  // floats, 16 B aligned
+      float* OB = CM + used;
+      const size_t row_floats = (size_t)n_active * dh;
+      const int per_batch = (int)((smem_bytes(dh, nchunk_max) / sizeof(float) - used) / row_floats);
+      if (per_batch >= 1) {
+        for (int r0 = 0; r0 < R; r0 += per_batch) {
+          const int nb = min(per_batch, R - r0);
+          // 16-byte asynchronous copies, all in flight at once: thread t
+          // copies piece t % (dh/4) of (row, chunk) records t / (dh/4), ...
+          const int h4 = dh / 4;
+          const int q = tid % h4;
+          for (int rc = tid / h4; rc < nb * n_active; rc += kGroupThreads / h4) {
+            const int rb = rc / n_active, cc = rc % n_active;
+            const int rr = r0 + rb;
+            const int m = rr % M, r = (rr / M) * kMaxRows + m;
+            if (cc <= (pos0 + m) / kAttnChunk)
+              cp_async16(OB + (size_t)rb * row_floats + (size_t)cc * dh + 4 * q,
+                         hb + cc * cs + (size_t)r * (dh + kRecPad) + kRecPad + 4 * q);
+          }
+          cp_async_wait_all();
+          sync();
+          for (int e = tid; e < nb * dh; e += kGroupThreads) {
+            const int rb = e / dh, dd = e % dh;
+            const int rr = r0 + rb;
+            const int m = rr % M, gh = rr / M;
+            const int nc = (pos0 + m) / kAttnChunk + 1;
+            const float* w = CW + rr * n_active;
+            const float* ob = OB + (size_t)rb * row_floats + dd;
+            float O = 0.f;
+            for (int cc = 0; cc < nc; ++cc) O = fmaf(ob[(size_t)cc * dh], w[cc], O);
+            a.out[(size_t)m * ld_out + (size_t)(kvh * G + gh) * dh + dd] =
+                __float2bfloat16_rn(O / LR[rr]);
+          }
+          sync();
         }
-        for (; cc < nc; ++cc) O = fmaf(__ldcg(ob + (size_t)cc * cs), w[cc], O);
-        a.out[(size_t)m * ld_out + (size_t)(kvh * G + gh) * dh + dd] =
-            __float2bfloat16_rn(O / LR[rr]);
+      } else {
+        for (int e = tid; e < R * dh; e += kGroupThreads) {
+          const int rr = e / dh, dd = e % dh;
+          const int m = rr % M, gh = rr / M, r = gh * kMaxRows + m;
+          const int nc = (pos0 + m) / kAttnChunk + 1;
+          const float* w = CW + rr * n_active;
+          const float* ob = hb + (size_t)r * (dh + kRecPad) + kRecPad + dd;
+          float O = 0.f;
+          int cc = 0;
+          for (; cc + 4 <= nc; cc += 4) {
+            float o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) o[q] = __ldcg(ob + (size_t)(cc + q) * cs);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) O = fmaf(o[q], w[cc + q], O);
+          }
+          for (; cc < nc; ++cc) O = fmaf(__ldcg(ob + (size_t)cc * cs), w[cc], O);
+          a.out[(size_t)m * ld_out + (size_t)(kvh * G + gh) * dh + dd] =
+              __float2bfloat16_rn(O / LR[rr]);
+        }
+        sync();
       }
-      sync();
     } else {
       for (int rr = 0; rr < R; ++rr) {
         const int m = rr % M, gh = rr / M, r = gh * kMaxRows + m;
         const int nc = (pos0 + m) / kAttnChunk + 1;
         for (int cc = tid; cc < nc; cc += kGroupThreads) {
-          const float* pc = hb + ((size_t)cc * rows + r) * (dh + 2);
+          const float* pc = hb + ((size_t)cc * rows + r) * (dh + kRecPad);
           sm.cm[cc] = __ldcg(pc);
           sm.cl[cc] = __ldcg(pc + 1);
         }
@@ -314,7 +356,7 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
         for (int dd = tid; dd < dh; dd += kGroupThreads) {
           float O = 0.f;
           for (int cc = 0; cc < nc; ++cc)
-            O = fmaf(__ldcg(hb + ((size_t)cc * rows + r) * (dh + 2) + 2 + dd), sm.cw[cc], O);
+            O = fmaf(__ldcg(hb + ((size_t)cc * rows + r) * (dh + kRecPad) + kRecPad + dd), sm.cw[cc], O);
           a.out[(size_t)m * ld_out + (size_t)(kvh * G + gh) * dh + dd] =
               __float2bfloat16_rn(O / L);
         }

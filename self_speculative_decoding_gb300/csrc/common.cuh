@@ -123,6 +123,14 @@ SSD_DI void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) 
       : "memory");
 }
 
+// 16-byte asynchronous global -> shared copy through L2 (both addresses
+// 16-byte aligned); completes at cp_async_wait_all().
+SSD_DI void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+SSD_DI void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Bulk prefetch of global memory into L2 (address and size multiples of 16).
 SSD_DI void bulk_prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
