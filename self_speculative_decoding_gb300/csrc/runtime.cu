@@ -109,6 +109,9 @@ struct ssd_ctx {
   int32_t* h_tok = nullptr;  // pinned staging [max_seq]
 
   Graph g_draft, g_extra, g_verify, g_accept, g_ar;
+  // verify pass for rounds whose d + 1 rows do not fit the GEMV activation
+  // stage (norm pre-pass + bf16 projections); g_verify covers the others
+  Graph g_verify_wide;
   // persistent pass kernel programs (one launch per draft step / extra pass /
   // verify pass / AR step) and whether they are used
   // static row bound of the passes being enqueued (0: up to 16 rows)
@@ -639,7 +642,18 @@ ssd_status b_extra_body(ssd_ctx* c, cudaStream_t s) {
 }
 
 ssd_status b_verify_body(ssd_ctx* c, cudaStream_t s);
+// Rows the verify graphs are built for: the narrow one up to what the stage
+// holds at d_model, the wide one up to d_max + 1.
+int verify_narrow_rows(const ssd_ctx* c) {
+  return std::min(c->pol.d_max + 1, std::max(1, gemv_stage_rows(c->cfg.d_model)));
+}
 ssd_status b_verify(ssd_ctx* c, cudaStream_t s) {
+  c->mmax = verify_narrow_rows(c);
+  const ssd_status r = b_verify_body(c, s);
+  c->mmax = 0;
+  return r;
+}
+ssd_status b_verify_wide(ssd_ctx* c, cudaStream_t s) {
   c->mmax = c->pol.d_max + 1;
   const ssd_status r = b_verify_body(c, s);
   c->mmax = 0;
@@ -695,6 +709,10 @@ ssd_status build_graphs_once(ssd_ctx* c) {
   if ((r = build_graph(c, c->g_draft, b_draft)) != SSD_OK) return r;
   if ((r = build_graph(c, c->g_extra, b_extra)) != SSD_OK) return r;
   if ((r = build_graph(c, c->g_verify, b_verify)) != SSD_OK) return r;
+  c->g_verify_wide.reset();
+  if (verify_narrow_rows(c) < c->pol.d_max + 1 &&
+      (r = build_graph(c, c->g_verify_wide, b_verify_wide)) != SSD_OK)
+    return r;
   if ((r = build_graph(c, c->g_accept, b_accept)) != SSD_OK) return r;
   return build_graph(c, c->g_ar, b_ar);
 }
@@ -775,7 +793,8 @@ ssd_status run_verify(ssd_ctx* c, ssd_stats* stats) {
     if ((r = replay(c, c->g_extra)) != SSD_OK) return r;
     if (stats) stats->bytes_streamed += pass_bytes(c, (int)c->pre.size(), false, n - 1 + d, 1);
   }
-  if ((r = replay(c, c->g_verify)) != SSD_OK) return r;
+  const bool wide = d + 1 > verify_narrow_rows(c) && c->g_verify_wide.exec;
+  if ((r = replay(c, wide ? c->g_verify_wide : c->g_verify)) != SSD_OK) return r;
   if (stats) stats->bytes_streamed += pass_bytes(c, (int)c->verify_layers.size(), true, n - 1, d + 1);
   c->phase = PH_VERIFIED;
   return SSD_OK;
@@ -922,6 +941,7 @@ ssd_status ssd_destroy(ssd_ctx* c) {
   c->g_draft.reset();
   c->g_extra.reset();
   c->g_verify.reset();
+  c->g_verify_wide.reset();
   c->g_accept.reset();
   c->g_ar.reset();
   c->p_draft.reset();
