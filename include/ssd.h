@@ -125,7 +125,18 @@ typedef struct {
   int64_t draft_steps;     /* draft forward passes run                      */
   int64_t kernel_launches; /* library kernels launched (graph nodes counted) */
   double bytes_streamed;   /* algorithmic HBM bytes: weights + KV read/written */
+  /* Device time (CUDA events around each pass; the SWIFT cost coefficient c
+   * is draft_ms / draft_steps over ar_ms / AR steps, SWIFT §B.3): */
+  double draft_ms;         /* draft steps                                   */
+  double verify_ms;        /* extra passes, verify passes and acceptance    */
+  double ar_ms;            /* ssd_decode_ar: the autoregressive steps       */
 } ssd_stats;
+
+/* Fault injection for failure-detection tests: the n-th device allocation
+ * (counting from 0) of the calling thread's next ssd_create fails as if the
+ * device were out of memory; n < 0 disables it.  ssd_create must then return
+ * SSD_ERR_OOM having released everything it allocated. */
+ssd_status ssd_debug_fail_alloc(int32_t n);
 
 /* Converts a row-major bf16 matrix W [R][K] (device memory) into the
  * library's packed layout at dst (device, R*K bf16, must not overlap src).

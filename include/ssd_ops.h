@@ -111,6 +111,14 @@ ssd_status ssd_op_philox(const uint32_t* ctr, int32_t count, uint64_t key, uint3
 /* Description of the most recent failed op call on this host thread. */
 const char* ssd_ops_last_error(void);
 
+/* Failure detection self-test: runs the device-side bounded waits the
+ * kernels use (an mbarrier wait, a global-counter wait) against conditions
+ * that never come true, each limited to `polls` polls (1..2^20).  Every wait
+ * must give up and report instead of hanging: *code_out (host) receives bit
+ * 0 if the mbarrier wait gave up and bit 1 if the counter wait did (3 when
+ * both behave).  Synchronises the stream.  Errors: INVALID_ARG, CUDA. */
+ssd_status ssd_op_wait_selftest(int32_t polls, int32_t* code_out, void* stream);
+
 /* ssd_op_linear for callers that cannot allocate device memory (the pages
  * have no counterpart; this is a library convenience).  Same arguments,
  * layout and result as ssd_op_linear, but the GEMV's scratch (partial sums of

@@ -335,6 +335,13 @@ class _Ops:
                                                     stream_handle()))
         return emitted, n_em
 
+    def wait_selftest(self, polls: int = 4096) -> int:
+        """Device bounded waits made to run out (ssd_op_wait_selftest);
+        returns the code (3 = both waits gave up and reported)."""
+        code = C.c_int32(-1)
+        self._check(_lib().ssd_op_wait_selftest(polls, C.byref(code), stream_handle()))
+        return code.value
+
     def philox(self, ctr: torch.Tensor, key: int) -> torch.Tensor:
         out = torch.empty_like(ctr)
         self._check(_lib().ssd_op_philox(_ptr(ctr), ctr.shape[0], key, _ptr(out),

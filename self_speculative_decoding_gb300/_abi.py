@@ -60,7 +60,8 @@ class SsdSwiftReport(C.Structure):
 class SsdStats(C.Structure):
     _fields_ = [("rounds", C.c_int64), ("drafted", C.c_int64), ("accepted", C.c_int64),
                 ("emitted", C.c_int64), ("draft_steps", C.c_int64),
-                ("kernel_launches", C.c_int64), ("bytes_streamed", C.c_double)]
+                ("kernel_launches", C.c_int64), ("bytes_streamed", C.c_double),
+                ("draft_ms", C.c_double), ("verify_ms", C.c_double), ("ar_ms", C.c_double)]
 
     def as_dict(self) -> dict:
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -102,6 +103,7 @@ _SIGS = {
     "ssd_get_tokens": [_P, C.POINTER(_I), _I, C.POINTER(_I)],
     "ssd_set_timeout_ms": [_P, _I],
     "ssd_set_pass_kernel": [_P, _I, C.POINTER(C.c_int32)],
+    "ssd_debug_fail_alloc": [_I],
     "ssd_swift_generate": [_P, C.POINTER(SsdSwiftParams), _I, _P, _P, _P, _P, _I,
                            C.POINTER(SsdSwiftReport)],
     "ssd_profile_decode": [_P, _I, C.POINTER(SsdKernelTimes)],
@@ -117,6 +119,7 @@ _SIGS = {
     "ssd_op_philox": [_P, _I, C.c_uint64, _P, _P],
     "ssd_ops_last_error": [],
     "ssd_op_linear_noalloc": [_P, _I, _I, _P, _I, _P, _P],
+    "ssd_op_wait_selftest": [_I, C.POINTER(C.c_int32), _P],
     "ssd_op_linear_noalloc_last_error": [],
 }
 

@@ -138,35 +138,22 @@ SSD_DI void bulk_prefetch_l2(const void* src, uint32_t bytes) {
 
 // Bounded wait for the phase with the given parity; false if it never
 // completed (the caller records an error instead of hanging).
-#ifndef SSD_MBAR_SUSPEND_NS
-#define SSD_MBAR_SUSPEND_NS 0
-#endif
-SSD_DI bool mbar_wait(uint64_t* bar, uint32_t parity) {
+SSD_DI bool mbar_wait_n(uint64_t* bar, uint32_t parity, int polls) {
   const uint32_t addr = smem_addr(bar);
-  for (int i = 0; i < (1 << 22); ++i) {
+  for (int i = 0; i < polls; ++i) {
     uint32_t done;
-    if (SSD_MBAR_SUSPEND_NS > 0) {
-      // the waiting thread may be suspended up to the hint (ns) per poll
-      asm volatile(
-          "{\n\t.reg .pred p;\n\t"
-          "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-          "selp.u32 %0, 1, 0, p;\n\t}"
-          : "=r"(done)
-          : "r"(addr), "r"(parity), "n"(SSD_MBAR_SUSPEND_NS)
-          : "memory");
-    } else {
-      asm volatile(
-          "{\n\t.reg .pred p;\n\t"
-          "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-          "selp.u32 %0, 1, 0, p;\n\t}"
-          : "=r"(done)
-          : "r"(addr), "r"(parity)
-          : "memory");
-    }
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(addr), "r"(parity)
+        : "memory");
     if (done) return true;
   }
   return false;
 }
+SSD_DI bool mbar_wait(uint64_t* bar, uint32_t parity) { return mbar_wait_n(bar, parity, 1 << 22); }
 
 // Adds v to a global counter with release semantics (no value returned).
 SSD_DI void red_release_add(unsigned* c, unsigned v) {
@@ -175,14 +162,15 @@ SSD_DI void red_release_add(unsigned* c, unsigned v) {
 
 // Bounded wait until a global counter reaches target (acquire); false if it
 // never did (the caller records an error instead of hanging).
-SSD_DI bool wait_count(const unsigned* c, unsigned target) {
-  for (int i = 0; i < (1 << 24); ++i) {
+SSD_DI bool wait_count_n(const unsigned* c, unsigned target, int polls) {
+  for (int i = 0; i < polls; ++i) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
     if (v >= target) return true;
   }
   return false;
 }
+SSD_DI bool wait_count(const unsigned* c, unsigned target) { return wait_count_n(c, target, 1 << 24); }
 
 // ---------------------------------------------------------------------------
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two

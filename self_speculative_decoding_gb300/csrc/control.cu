@@ -231,6 +231,20 @@ __global__ void rope_table_kernel(float2* tab, int n_pos, int half, double theta
   tab[e] = make_float2((float)cos(ang), (float)sin(ang));
 }
 
+// Device-side bounded waits, made to run out: an mbarrier nothing arrives on
+// and a counter nothing increments.  Each wait must give up after `polls`
+// polls and the kernel records which did (bit 0: mbarrier, bit 1: counter).
+__global__ void wait_selftest_kernel(const unsigned* never, int polls, int32_t* code) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  int c = 0;
+  if (!mbar_wait_n(&bar, 0u, polls)) c |= 1;
+  if (!wait_count_n(never, 1u, polls)) c |= 2;
+  *code = c;
+}
+
 cudaLaunchConfig_t make_cfg(int grid, int block, cudaStream_t s, bool pdl,
                             cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t lc = {};
@@ -290,6 +304,11 @@ cudaError_t launch_accept_stochastic(const AcceptArgs& a, cudaStream_t s, bool p
 cudaError_t launch_match_count(const RowStats* stats, const int32_t* targets, const int32_t* M_dev,
                                int32_t* matches, cudaStream_t s) {
   match_count_kernel<<<1, 32, 0, s>>>(stats, targets, M_dev, matches);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(const unsigned* never, int polls, int32_t* code, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(never, polls, code);
   return cudaGetLastError();
 }
 

@@ -211,6 +211,11 @@ cudaError_t launch_match_count(const RowStats* stats, const int32_t* targets, co
 cudaError_t launch_philox(const uint32_t* ctr, int count, uint64_t key, uint32_t* out,
                           cudaStream_t s);
 
+// Runs the device's bounded waits against conditions that never come true
+// (never[0] must be 0); *code gets bit 0 if the mbarrier wait gave up, bit 1
+// if the counter wait did.
+cudaError_t launch_wait_selftest(const unsigned* never, int polls, int32_t* code, cudaStream_t s);
+
 // Sum-of-squares partials of fp32 rows (used by the op entry points to feed
 // the norm-fused GEMV from an arbitrary x).
 cudaError_t launch_ss_partials(const float* x, int M, int D, float* ss, cudaStream_t s);

@@ -297,6 +297,24 @@ ssd_status ssd_op_accept_stochastic(const float* P, const float* Q, const int32_
   return cu(launch_accept_stochastic(a, (cudaStream_t)stream, false), "accept");
 }
 
+ssd_status ssd_op_wait_selftest(int32_t polls, int32_t* code_out, void* stream) {
+  if (polls < 1 || polls > (1 << 20) || !code_out)
+    return op_fail(SSD_ERR_INVALID_ARG, "polls in 1..2^20 and code_out required");
+  cudaStream_t s = (cudaStream_t)stream;
+  Scratch never(s), code(s);
+  ssd_status r;
+  if ((r = cu(never.alloc(16), "scratch")) != SSD_OK) return r;
+  if ((r = cu(code.alloc(16), "scratch")) != SSD_OK) return r;
+  if ((r = cu(cudaMemsetAsync(never.p, 0, 16, s), "memset")) != SSD_OK) return r;
+  if ((r = cu(cudaMemsetAsync(code.p, 0xff, 16, s), "memset")) != SSD_OK) return r;
+  if ((r = cu(launch_wait_selftest((const unsigned*)never.p, polls, (int32_t*)code.p, s),
+              "selftest")) != SSD_OK)
+    return r;
+  if ((r = cu(cudaMemcpyAsync(code_out, code.p, 4, cudaMemcpyDeviceToHost, s), "copy")) != SSD_OK)
+    return r;
+  return cu(cudaStreamSynchronize(s), "synchronize");
+}
+
 ssd_status ssd_op_philox(const uint32_t* ctr, int32_t count, uint64_t key, uint32_t* out,
                          void* stream) {
   if (count < 0 || (count > 0 && (!al16(ctr) || !al16(out))))

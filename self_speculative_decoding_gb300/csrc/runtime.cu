@@ -22,6 +22,8 @@
 #include <thread>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/ssd.h"
 #include "kernels.cuh"
 
@@ -64,6 +66,7 @@ struct ssd_ctx {
   cudaStream_t stream = nullptr;
   cudaStream_t cap = nullptr;
   cudaEvent_t ev = nullptr;
+  cudaEvent_t t0 = nullptr, t1 = nullptr;  // pass timing for ssd_stats
   int timeout_ms = 120000;
   bool pdl = true;
 
@@ -139,6 +142,15 @@ ssd_status fail(ssd_ctx* c, ssd_status s, const std::string& msg) {
   if (c) c->err = msg;
   return s;
 }
+
+// NVTX range over the host enqueue of a pass (the device work of graph
+// replays is attributed by the profiler's correlation).
+struct Range {
+  explicit Range(const char* name) { nvtxRangePushA(name); }
+  ~Range() { nvtxRangePop(); }
+};
+
+thread_local int g_fail_alloc = -1;  // fault injection: fail the n-th allocation
 
 #define CK(call)                                                                          \
   do {                                                                                    \
@@ -773,9 +785,15 @@ ssd_status run_draft(ssd_ctx* c, ssd_stats* stats) {
   ssd_status r;
   const int n = c->h_st->n;
   for (int j = 0; j < c->pol.d_max; ++j) {
+    Range nv("ssd draft step");
+    if (stats) CK(cudaEventRecord(c->t0, c->stream));
     if ((r = replay(c, c->g_draft)) != SSD_OK) return r;
+    if (stats) CK(cudaEventRecord(c->t1, c->stream));
     if ((r = read_state(c)) != SSD_OK) return r;
     if (stats) {
+      float ms = 0.f;
+      cudaEventElapsedTime(&ms, c->t0, c->t1);
+      stats->draft_ms += ms;
       stats->draft_steps++;
       stats->bytes_streamed += draft_bytes(c, n - 1 + j);
     }
@@ -786,8 +804,10 @@ ssd_status run_draft(ssd_ctx* c, ssd_stats* stats) {
 }
 
 ssd_status run_verify(ssd_ctx* c, ssd_stats* stats) {
+  Range nv("ssd verify");
   ssd_status r;
   const int n = c->h_st->n, d = c->h_st->d;
+  if (stats) CK(cudaEventRecord(c->t0, c->stream));
   const bool extra = !c->h_st->stop;
   if (extra) {
     if ((r = replay(c, c->g_extra)) != SSD_OK) return r;
@@ -841,6 +861,10 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
   c->stream = (cudaStream_t)stream;
 
   auto alloc = [&](void** p, size_t bytes) -> bool {
+    if (g_fail_alloc >= 0 && g_fail_alloc-- == 0) {  // injected failure (ssd_debug_fail_alloc)
+      g_fail_alloc = -1;
+      return false;
+    }
     if (cudaMalloc(p, bytes) != cudaSuccess) {
       cudaGetLastError();
       return false;
@@ -902,7 +926,8 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
   if (cudaMallocHost((void**)&c->h_st, sizeof(DevState)) != cudaSuccess ||
       cudaMallocHost((void**)&c->h_tok, (size_t)g.max_seq * 4) != cudaSuccess ||
       cudaStreamCreateWithFlags(&c->cap, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaEventCreateWithFlags(&c->ev, cudaEventDisableTiming) != cudaSuccess) {
+      cudaEventCreateWithFlags(&c->ev, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreate(&c->t0) != cudaSuccess || cudaEventCreate(&c->t1) != cudaSuccess) {
     cudaGetLastError();
     ssd_destroy(c);
     return SSD_ERR_OOM;
@@ -962,6 +987,8 @@ ssd_status ssd_destroy(ssd_ctx* c) {
   if (c->h_tok) cudaFreeHost(c->h_tok);
   if (c->cap) cudaStreamDestroy(c->cap);
   if (c->ev) cudaEventDestroy(c->ev);
+  if (c->t0) cudaEventDestroy(c->t0);
+  if (c->t1) cudaEventDestroy(c->t1);
   cudaGetLastError();
   delete c;
   return SSD_OK;
@@ -1018,6 +1045,7 @@ ssd_status ssd_set_policy(ssd_ctx* c, const ssd_policy* p) {
 
 ssd_status ssd_prefill(ssd_ctx* c, const int32_t* tokens, int32_t n, int32_t* first) {
   if (!c || !tokens || n < 1) return c ? fail(c, SSD_ERR_INVALID_ARG, "prefill args") : SSD_ERR_INVALID_ARG;
+  Range nv("ssd prefill");
   if (!c->has_policy) return fail(c, SSD_ERR_STATE, "no policy set (ssd_set_policy)");
   if (n + 1 > c->cfg.max_seq) return fail(c, SSD_ERR_CAPACITY, "prompt longer than max_seq - 1");
   for (int i = 0; i < n; ++i)
@@ -1103,7 +1131,13 @@ ssd_status ssd_generate(ssd_ctx* c, int32_t n_tokens, int32_t* out, ssd_stats* s
     const int d = c->pol.d_max == 0 ? 0 : c->h_st->d;
     if ((r = run_verify(c, stats)) != SSD_OK) return r;
     if ((r = replay(c, c->g_accept)) != SSD_OK) return r;
+    if (stats) CK(cudaEventRecord(c->t1, c->stream));
     if ((r = read_state(c)) != SSD_OK) return r;
+    if (stats) {
+      float ms = 0.f;
+      cudaEventElapsedTime(&ms, c->t0, c->t1);
+      stats->verify_ms += ms;
+    }
     c->phase = PH_IDLE;
     const int ne = c->h_st->n_emitted;
     for (int i = 0; i < ne && got < n_tokens; ++i, ++got)
@@ -1134,10 +1168,13 @@ ssd_status ssd_decode_ar(ssd_ctx* c, int32_t n_tokens, int32_t* out, ssd_stats* 
   const int n0 = c->h_st->n;
   if (n0 + n_tokens > c->cfg.max_seq) return fail(c, SSD_ERR_CAPACITY, "max_seq exceeded");
   const int64_t l0 = c->launches;
+  Range nv("ssd decode_ar");
+  if (stats) CK(cudaEventRecord(c->t0, c->stream));
   for (int i = 0; i < n_tokens; ++i) {
     if ((r = replay(c, c->g_ar)) != SSD_OK) return r;
     if (stats) stats->bytes_streamed += pass_bytes(c, c->cfg.n_layers, true, n0 - 1 + i, 1);
   }
+  if (stats) CK(cudaEventRecord(c->t1, c->stream));
   if (out && n_tokens > 0) {
     CK(cudaMemcpyAsync(c->h_tok, c->tokens + n0, (size_t)n_tokens * 4, cudaMemcpyDeviceToHost,
                        c->stream));
@@ -1148,6 +1185,9 @@ ssd_status ssd_decode_ar(ssd_ctx* c, int32_t n_tokens, int32_t* out, ssd_stats* 
     stats->rounds = n_tokens;
     stats->emitted = n_tokens;
     stats->kernel_launches = c->launches - l0;
+    float ms = 0.f;
+    if (n_tokens > 0) cudaEventElapsedTime(&ms, c->t0, c->t1);
+    stats->ar_ms = ms;
   }
   return SSD_OK;
 }
@@ -1314,7 +1354,13 @@ ssd_status ssd_swift_generate(ssd_ctx* c, const ssd_swift_params* pp, int32_t n_
     const int d = c->pol.d_max == 0 ? 0 : c->h_st->d;
     if ((r = run_verify(c, &st)) != SSD_OK) return r;
     if ((r = replay(c, c->g_accept)) != SSD_OK) return r;
+    CK(cudaEventRecord(c->t1, c->stream));
     if ((r = read_state(c)) != SSD_OK) return r;
+    {
+      float ms = 0.f;
+      cudaEventElapsedTime(&ms, c->t0, c->t1);
+      st.verify_ms += ms;
+    }
     c->phase = PH_IDLE;
     const int ne = c->h_st->n_emitted;
     for (int i = 0; i < ne && got < n_tokens; ++i, ++got)
@@ -1389,6 +1435,11 @@ ssd_status ssd_set_pass_kernel(ssd_ctx* c, int32_t enable, int32_t* active_out) 
   return SSD_OK;
 }
 
+ssd_status ssd_debug_fail_alloc(int32_t n) {
+  g_fail_alloc = n < 0 ? -1 : n;
+  return SSD_OK;
+}
+
 ssd_status ssd_set_timeout_ms(ssd_ctx* c, int32_t ms) {
   if (!c || ms <= 0) return SSD_ERR_INVALID_ARG;
   c->timeout_ms = ms;
@@ -1421,6 +1472,7 @@ ssd_status ssd_score_masks(ssd_ctx* c, const uint64_t* masks, int32_t K, int32_t
   // t[n-N-1..n-2]; positions >= split use the scratch cache, so the shared
   // full-model cache is only read.
   const int split = n - N - 1;
+  Range nv("ssd score_masks");
   CK(cudaMemsetAsync(c->sc_counts, 0, (size_t)K * sizeof(int32_t), c->stream));
   c->sc_split = split;
   for (int k = 0; k < K && r == SSD_OK; ++k) {
