@@ -108,6 +108,35 @@ ssd_status ssd_op_accept_stochastic(const float* P, const float* Q, const int32_
 ssd_status ssd_op_philox(const uint32_t* ctr, int32_t count, uint64_t key, uint32_t* out,
                          void* stream);
 
+/* Many-row projection on the tensor cores (the batched candidate-mask
+ * scoring forward of SWIFT §4.1.2, where K candidates x N window positions
+ * give hundreds of rows): for T >= 1 rows of act (bf16 [T][K]),
+ *   epi 0 (store):  out fp32 [T][R] = W act
+ *   epi 1 (resid):  out fp32 [*][R]: out[map[t]] += W act[t] (map: device
+ *                   int32 [T], NULL = identity; rows not named stay as they are)
+ *   epi 2 (swiglu): out bf16 [T][R] = bf16(silu(W act) * (W1 act)), W1 the
+ *                   up matrix (same shape as W)
+ *   epi 3 (argmax): out int32 [T] = argmax_r (W act)[r], lowest r on ties
+ * W, W1 packed (ssd_pack_weight).  Every output sums K in ascending 32-wide
+ * steps, whatever T.  This call has no limit of 16 rows. */
+ssd_status ssd_op_linear_rows(const void* W, const void* W1, int32_t R, int32_t K,
+                              const void* act, int32_t T, int32_t epi, void* out,
+                              const int32_t* map, void* stream);
+
+/* Attention of candidate-mask scoring windows.  For each candidate k in
+ * cand (device int32 [n_cand]) and window row i < N (query position
+ * split + i), with q bf16 [n_cand N][H][dh] (RoPE applied, row ja N + i for
+ * the ja-th candidate of the list):
+ *   out[ja N + i][h dh ..] = bf16(softmax(q K^T / sqrt(dh)) V)
+ * over the keys of the shared cache k_cache / v_cache ([Hkv][max_seq][dh]
+ * bf16) at positions 0..split-1, then candidate k's own window keys
+ * wk / wv (bf16 [rows][Hkv][dh], row k N + w) for w <= i.  split >= 1,
+ * split <= max_seq; dh 64 or 128. */
+ssd_status ssd_op_score_attention(const void* q, const int32_t* cand, int32_t n_cand, int32_t N,
+                                  int32_t split, const void* k_cache, const void* v_cache,
+                                  int32_t max_seq, const void* wk, const void* wv, int32_t H,
+                                  int32_t Hkv, int32_t dh, void* out, void* stream);
+
 /* Description of the most recent failed op call on this host thread. */
 const char* ssd_ops_last_error(void);
 

@@ -44,6 +44,41 @@ def swiglu(Wg_bits, Wu_bits, x, g, eps) -> np.ndarray:
     return np.stack(out)
 
 
+def silu_product(Wg_bits, Wu_bits, act) -> np.ndarray:
+    """u[m] = bf16(silu(Wg act[m]) * (Wu act[m])): the SwiGLU activation of
+    already-normalised bf16 rows."""
+    Wg, Wu = widen(Wg_bits), widen(Wu_bits)
+    out = []
+    for a in act:
+        gate, up = Wg @ a, Wu @ a
+        out.append(bf16_round(gate / (1.0 + np.exp(-gate)) * up))
+    return np.stack(out)
+
+
+def score_attention(q: np.ndarray, cand, N: int, split: int, K: np.ndarray, V: np.ndarray,
+                    WK: np.ndarray, WV: np.ndarray, H: int, Hkv: int) -> np.ndarray:
+    """Attention of candidate-mask scoring windows (SWIFT §4.1.2 parallel
+    prediction): query row (candidate cand[j], window row i) sits at position
+    split + i and sees the shared cache's keys 0..split-1 (K, V: [Hkv,
+    max_seq, dh]) followed by its own candidate's window keys 0..i (WK, WV:
+    [rows, Hkv, dh], row k N + w).  q: [len(cand) N, H, dh] after RoPE.
+    Returns bf16-rounded outputs [len(cand) N, H dh]."""
+    dh = q.shape[2]
+    group = H // Hkv
+    out = np.zeros((len(cand) * N, H * dh))
+    for j, k in enumerate(cand):
+        for i in range(N):
+            t = j * N + i
+            for h in range(H):
+                kvh = h // group
+                keys = np.concatenate([K[kvh, :split], WK[k * N: k * N + i + 1, kvh]])
+                vals = np.concatenate([V[kvh, :split], WV[k * N: k * N + i + 1, kvh]])
+                sc = keys @ q[t, h] / np.sqrt(dh)
+                e = np.exp(sc - np.max(sc))
+                out[t, h * dh:(h + 1) * dh] = (e @ vals) / np.sum(e)
+    return bf16_round(out)
+
+
 def _shape(H, Hkv, dh, theta):
     return SimpleNamespace(n_heads=H, n_kv_heads=Hkv, head_dim=dh, rope_theta=theta,
                            norm_eps=1e-5)

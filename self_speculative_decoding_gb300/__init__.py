@@ -335,6 +335,39 @@ class _Ops:
                                                     stream_handle()))
         return emitted, n_em
 
+    LINEAR_ROWS_EPI = {"store": 0, "resid": 1, "swiglu": 2, "argmax": 3}
+
+    def linear_rows(self, W, act, epi="store", W1=None, out=None, rowmap=None):
+        """Many-row projection (ssd_op_linear_rows).  epi "store" -> fp32
+        [T, R]; "resid" adds into out (fp32) at rows rowmap (or 0..T-1);
+        "swiglu" -> bf16 [T, R] with W1 the up matrix; "argmax" -> int32 [T]."""
+        R, K = W.shape
+        T = act.shape[0]
+        e = self.LINEAR_ROWS_EPI[epi]
+        if out is None:
+            if epi == "store":
+                out = torch.empty(T, R, dtype=torch.float32, device=W.device)
+            elif epi == "swiglu":
+                out = torch.empty(T, R, dtype=torch.bfloat16, device=W.device)
+            elif epi == "argmax":
+                out = torch.empty(T, dtype=torch.int32, device=W.device)
+            else:
+                raise ValueError("epi 'resid' needs out")
+        self._check(_lib().ssd_op_linear_rows(_ptr(W), _ptr(W1), R, K, _ptr(act), T, e, _ptr(out),
+                                              _ptr(rowmap), stream_handle()))
+        return out
+
+    def score_attention(self, q, cand, N, split, k_cache, v_cache, wk, wv, H, Hkv, dh):
+        """Window attention of candidate-mask scoring (ssd_op_score_attention);
+        q bf16 [len(cand) N, H, dh]; returns bf16 [len(cand) N, H dh]."""
+        nc = cand.shape[0]
+        out = torch.empty(nc * N, H * dh, dtype=torch.bfloat16, device=q.device)
+        self._check(_lib().ssd_op_score_attention(_ptr(q), _ptr(cand), nc, N, split,
+                                                  _ptr(k_cache), _ptr(v_cache), k_cache.shape[1],
+                                                  _ptr(wk), _ptr(wv), H, Hkv, dh, _ptr(out),
+                                                  stream_handle()))
+        return out
+
     def wait_selftest(self, polls: int = 4096) -> int:
         """Device bounded waits made to run out (ssd_op_wait_selftest);
         returns the code (3 = both waits gave up and reported)."""

@@ -4,8 +4,7 @@
 // A pass carries M <= 16 query rows at consecutive positions pos0..pos0+M-1.
 // The item
 //   1. brings the chunk's cached keys / values into shared memory with bulk
-//      copies (the cached rows of positions >= split come from a scratch
-//      cache: candidate-mask scoring keeps its window there);
+//      copies;
 //   2. applies rotate-half RoPE to the chunk's new keys, rounds k and v to
 //      bf16 and appends them to the cache (LayerSkip blog §3.2: every pass
 //      writes the K/V of the layers it runs);
@@ -60,16 +59,14 @@ SSD_DI Smem carve(unsigned char* raw, int dh, int nchunk) {
   return sm;
 }
 
-// Position p's cached key / value row: the shared cache below a.split, the
-// scratch cache from a.split on.
-SSD_DI const bf16* cache_row(const bf16* c, const bf16* c2, const AttnArgs& a, int kvh, int pos) {
-  return pos < a.split ? c + (size_t)kvh * a.max_seq * a.dh + (size_t)pos * a.dh
-                       : c2 + ((size_t)kvh * a.scratch_len + (pos - a.split)) * a.dh;
+// Position p's cached key / value row.
+SSD_DI const bf16* cache_row(const bf16* c, const AttnArgs& a, int kvh, int pos) {
+  return c + (size_t)kvh * a.max_seq * a.dh + (size_t)pos * a.dh;
 }
 
 // Step (1) of work item `item`: the bulk copies of the chunk's cached keys
 // and values (positions before pos0), issued by warp 0 (one copy per padded
-// K row; the V rows in one copy unless the chunk straddles the split) and
+// K row; the V rows in one copy) and
 // completing on `bar`.  The cache rows before pos0 were written by earlier
 // passes, so this may run before the wait on the preceding kernel.
 SSD_DI void issue(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, uint64_t* bar,
@@ -81,22 +78,16 @@ SSD_DI void issue(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, 
   const int p_end = min(p_begin + kAttnChunk, pos0 + M);
   const int n_old = max(0, min(p_end, pos0) - p_begin);
   if (n_old > 0 && warp == 0) {
-    const bool one_v = p_begin + n_old <= a.split || p_begin >= a.split;
     if (lane == 0) {
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(bar, (uint32_t)(2 * n_old * dh * sizeof(bf16)));
-      if (one_v)
-        bulk_g2s(sm.V, cache_row(a.vc, a.vc2, a, kvh, p_begin),
-                 (uint32_t)(n_old * dh * sizeof(bf16)), bar);
+      bulk_g2s(sm.V, cache_row(a.vc, a, kvh, p_begin), (uint32_t)(n_old * dh * sizeof(bf16)),
+               bar);
     }
     __syncwarp();
-    for (int j = lane; j < n_old; j += 32) {
-      bulk_g2s(sm.K + (size_t)j * krs, cache_row(a.kc, a.kc2, a, kvh, p_begin + j),
+    for (int j = lane; j < n_old; j += 32)
+      bulk_g2s(sm.K + (size_t)j * krs, cache_row(a.kc, a, kvh, p_begin + j),
                (uint32_t)(dh * sizeof(bf16)), bar);
-      if (!one_v)
-        bulk_g2s(sm.V + (size_t)j * dh, cache_row(a.vc, a.vc2, a, kvh, p_begin + j),
-                 (uint32_t)(dh * sizeof(bf16)), bar);
-    }
   }
 }
 
@@ -139,8 +130,8 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
     sm.K[j * krs + i + half] = kb1;
     sm.V[j * dh + i] = vb0;
     sm.V[j * dh + i + half] = vb1;
-    bf16* kd = const_cast<bf16*>(cache_row(a.kc, a.kc2, a, kvh, pos));
-    bf16* vd = const_cast<bf16*>(cache_row(a.vc, a.vc2, a, kvh, pos));
+    bf16* kd = const_cast<bf16*>(cache_row(a.kc, a, kvh, pos));
+    bf16* vd = const_cast<bf16*>(cache_row(a.vc, a, kvh, pos));
     kd[i] = kb0;
     kd[i + half] = kb1;
     vd[i] = vb0;

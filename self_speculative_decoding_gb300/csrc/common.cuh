@@ -203,6 +203,14 @@ SSD_DI float gumbel_at(uint64_t seed, int v, int pos, int round, int stream) {
   return -logf(-logf(u01(word_of(r, v & 3))));
 }
 
+// Packed weight unit (16 rows x 32 columns bf16, 1 KB): each 8-row half is
+// row-major with 64-byte rows whose four 16-byte chunks are stored in the
+// 64-byte swizzle order (chunk c of row r at position c ^ ((r >> 1) & 3)),
+// which the tensor cores' shared-memory descriptors read directly.  Byte
+// offset, within a half, of the chunk that mma.sync lane L = 4g + c needs
+// (row g, columns 8c .. 8c + 7).
+SSD_DI int unit_slot(int lane) { return (lane ^ ((lane >> 3) & 3)) << 4; }
+
 // Total order used by every argmax: larger value first, then lower index.
 SSD_DI bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);

@@ -193,17 +193,6 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_stoch_kernel(AcceptArgs
   }
 }
 
-__global__ void match_count_kernel(const RowStats* stats, const int32_t* targets,
-                                   const int32_t* M_dev, int32_t* matches) {
-  pdl_wait();
-  pdl_trigger();
-  if (threadIdx.x == 0) {
-    int cnt = 0;
-    for (int m = 0; m < *M_dev; ++m) cnt += stats[m].top1 == targets[m];
-    matches[0] += cnt;
-  }
-}
-
 __global__ void philox_kernel(const uint32_t* ctr, int count, uint64_t key, uint32_t* out) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= count) return;
@@ -299,12 +288,6 @@ cudaError_t launch_accept_stochastic(const AcceptArgs& a, cudaStream_t s, bool p
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t lc = make_cfg(1, kAcceptThreads, s, pdl, attr);
   return cudaLaunchKernelEx(&lc, accept_stoch_kernel, a);
-}
-
-cudaError_t launch_match_count(const RowStats* stats, const int32_t* targets, const int32_t* M_dev,
-                               int32_t* matches, cudaStream_t s) {
-  match_count_kernel<<<1, 32, 0, s>>>(stats, targets, M_dev, matches);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_wait_selftest(const unsigned* never, int polls, int32_t* code, cudaStream_t s) {

@@ -93,9 +93,10 @@ cudaError_t launch_one(const LinearArgs& a, const Part& p, cudaStream_t st, bool
   return cudaLaunchKernelEx(&lc, gemv_kernel<IN, EPI>, a, p);
 }
 
-// Packs W [R][K] row-major into units of 16 rows x 32 columns in fragment
-// order: unit (vr, kb) = 512 bf16; half h (rows vr*16 + 8h .. + 7), lane
-// L = 4g + c holds W[vr*16 + 8h + g][kb*32 + 8c .. + 7] at [h*256 + 8L].
+// Packs W [R][K] row-major into units of 16 rows x 32 columns: unit
+// (vr, kb) = 512 bf16; half h holds rows vr*16 + 8h .. + 7, row g at
+// [h*256 + 32g], its 16-byte chunk c (columns kb*32 + 8c .. + 7) at
+// position c ^ ((g >> 1) & 3) of the row (the 64-byte swizzle).
 __global__ void pack_kernel(const bf16* __restrict__ src, bf16* __restrict__ dst, int R, int K) {
   const long long n = (long long)R * K / 8;  // 16-byte pieces
   const int KB = K / 32;
@@ -104,7 +105,7 @@ __global__ void pack_kernel(const bf16* __restrict__ src, bf16* __restrict__ dst
     const long long unit = i / 64;
     const int within = (int)(i % 64);
     const int h = within / 32, L = within % 32;
-    const int gg = L >> 2, cc = L & 3;
+    const int gg = L >> 2, cc = (L & 3) ^ ((gg >> 1) & 3);
     const long long vr = unit / KB;
     const int kb = (int)(unit % KB);
     const long long row = vr * 16 + 8 * h + gg;

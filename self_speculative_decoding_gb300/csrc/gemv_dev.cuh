@@ -513,8 +513,8 @@ SSD_DI void consume(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0, in
       const int un = warp + i * kConsumers;
       if (un < n) {
         const unsigned char* base = sm.ring + slot * kSlotBytes + un * kUnitBytes;
-        const uint4 wa = *reinterpret_cast<const uint4*>(base + lane * 16);
-        const uint4 wb = *reinterpret_cast<const uint4*>(base + 512 + lane * 16);
+        const uint4 wa = *reinterpret_cast<const uint4*>(base + unit_slot(lane));
+        const uint4 wb = *reinterpret_cast<const uint4*>(base + 512 + unit_slot(lane));
         const int off = (kb + un) * 32 + 8 * c;
         const uint4 xa = STAGED ? (v0 ? *reinterpret_cast<const uint4*>(sm.stage + (size_t)g * (a.K + kPad) + off)
                                       : make_uint4(0u, 0u, 0u, 0u))
@@ -653,8 +653,8 @@ SSD_DI void consume_win(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0
       const int un = warp + i * kConsumers;
       if (un < n) {
         const unsigned char* base = sm.ring + slot * kSlotBytes + un * kUnitBytes;
-        const uint4 wa = *reinterpret_cast<const uint4*>(base + lane * 16);
-        const uint4 wbv = *reinterpret_cast<const uint4*>(base + 512 + lane * 16);
+        const uint4 wa = *reinterpret_cast<const uint4*>(base + unit_slot(lane));
+        const uint4 wbv = *reinterpret_cast<const uint4*>(base + 512 + unit_slot(lane));
         const int col = ((kb - kw * kWinUnits) + un) * 64 + c * 16;  // bytes into the row
         const uint4 xa = v0 ? *reinterpret_cast<const uint4*>(wbase + g * kWinRow + col)
                             : make_uint4(0u, 0u, 0u, 0u);

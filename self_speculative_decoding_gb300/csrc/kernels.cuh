@@ -88,14 +88,6 @@ struct AttnArgs {
   unsigned* counters = nullptr;  // [Hkv]
   int* err = nullptr;          // set to 1 if a bulk copy never completed
   float scale = 1.f;
-  // Positions >= split live in a second (scratch) cache kc2 / vc2
-  // [Hkv][scratch_len][dh] at index pos - split; split >= max_seq disables it.
-  // Candidate-mask scoring uses it so that window K/V never touch the shared
-  // cache.
-  bf16* kc2 = nullptr;
-  bf16* vc2 = nullptr;
-  int split = 1 << 30;
-  int scratch_len = 0;
 };
 
 int attn_grid(const AttnArgs& a);
@@ -204,12 +196,57 @@ bool pass_supported(int dh, int max_seq);
 cudaError_t pass_prepare();
 cudaError_t launch_pass(const PassProg& p, cudaStream_t s);
 
-// matches[0] += #{m < M : stats[m].top1 == targets[m]} (M from the state).
-cudaError_t launch_match_count(const RowStats* stats, const int32_t* targets, const int32_t* M_dev,
-                               int32_t* matches, cudaStream_t s);
-
 cudaError_t launch_philox(const uint32_t* ctr, int count, uint64_t key, uint32_t* out,
                           cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Batched candidate-mask scoring: many-row projections on the tensor cores
+// and the scoring forward's other steps (gemm.cu, score.cu).
+
+enum GemmEpi { GEMM_STORE = 0, GEMM_RESID = 1, GEMM_SWIGLU = 2, GEMM_ARGMAX = 3 };
+
+// out[t][r] = sum_k act[t][k] W[r][k] for T rows; W (and W1, the up matrix of
+// a SwiGLU pair) in the packed unit layout of launch_pack.
+struct GemmArgs {
+  const bf16* W0 = nullptr;
+  const bf16* W1 = nullptr;
+  int R = 0, K = 0, T = 0;
+  const bf16* act = nullptr;           // [T][K]
+  int epi = GEMM_STORE;
+  float* y = nullptr;                  // GEMM_STORE [T][R]
+  float* x = nullptr;                  // GEMM_RESID: x[rowmap[t]][r] += out[t][r]
+  const int32_t* rowmap = nullptr;     // nullable: identity
+  bf16* u = nullptr;                   // GEMM_SWIGLU [T][R]: silu(gate) * up
+  unsigned long long* best = nullptr;  // GEMM_ARGMAX [T]: atomic max of (value, -index) keys, zero before
+  int* err = nullptr;                  // set non-zero if a bounded wait gave up (nullable)
+};
+cudaError_t launch_gemm_rows(const GemmArgs& a, cudaStream_t s);
+// idx[t] = the index of argmax key best[t] (-1 for a row that saw no value)
+cudaError_t launch_argmax_index(const unsigned long long* best, int T, int32_t* idx,
+                                cudaStream_t s);
+
+struct ScoreAttnArgs {
+  const bf16* q = nullptr;    // [T][H][dh] compact rows (RoPE applied)
+  const bf16* kc = nullptr;   // the layer's shared cache [Hkv][max_seq][dh]
+  const bf16* vc = nullptr;
+  const bf16* sk = nullptr;   // window K/V [K * N][Hkv][dh] by physical row
+  const bf16* sv = nullptr;
+  const int32_t* cand = nullptr;  // [n_active] candidates that keep the layer
+  int N = 0, split = 0, max_seq = 0, H = 0, Hkv = 0, dh = 0;
+  float scale_log2 = 0.f;     // log2(e) / sqrt(dh)
+  bf16* out = nullptr;        // [T][H dh]
+};
+cudaError_t launch_score_attn(const ScoreAttnArgs& a, int n_active, cudaStream_t s);
+size_t score_attn_smem(int dh);
+cudaError_t launch_score_embed(const bf16* embed, const int32_t* tokens, int split, int N, int rows,
+                               int D, float* x, cudaStream_t s);
+cudaError_t launch_score_norm(const float* x, const int32_t* map, const float* gain, float eps,
+                              int T, int D, bf16* out, cudaStream_t s);
+cudaError_t launch_score_rope(const float* qkv, int T, const int32_t* map, int N, int split, int H,
+                              int Hkv, int dh, const float2* rope, bf16* q, bf16* sk, bf16* sv,
+                              cudaStream_t s);
+cudaError_t launch_score_match(unsigned long long* best, const int32_t* tokens, int split, int N,
+                               int rows, int32_t* counts, cudaStream_t s);
 
 // Runs the device's bounded waits against conditions that never come true
 // (never[0] must be 0); *code gets bit 0 if the mbarrier wait gave up, bit 1

@@ -322,4 +322,67 @@ ssd_status ssd_op_philox(const uint32_t* ctr, int32_t count, uint64_t key, uint3
   return cu(launch_philox(ctr, count, key, out, (cudaStream_t)stream), "philox");
 }
 
+ssd_status ssd_op_linear_rows(const void* W, const void* W1, int32_t R, int32_t K,
+                              const void* act, int32_t T, int32_t epi, void* out,
+                              const int32_t* map, void* stream) {
+  if (!al16(W) || (epi == GEMM_SWIGLU && !al16(W1)) || R <= 0 || R % 16 || K <= 0 || K % 32 ||
+      T < 1 || !al16(act) || !al16(out) || epi < GEMM_STORE || epi > GEMM_ARGMAX)
+    return op_fail(SSD_ERR_INVALID_ARG, "linear_rows arguments");
+  cudaStream_t s = (cudaStream_t)stream;
+  GemmArgs a;
+  a.W0 = (const bf16*)W;
+  a.W1 = (const bf16*)W1;
+  a.R = R;
+  a.K = K;
+  a.T = T;
+  a.act = (const bf16*)act;
+  a.epi = epi;
+  Scratch best(s), err(s);
+  ssd_status r;
+  if ((r = cu(err.alloc(16), "scratch")) != SSD_OK) return r;
+  if ((r = cu(cudaMemsetAsync(err.p, 0, 16, s), "memset")) != SSD_OK) return r;
+  a.err = (int*)err.p;
+  if (epi == GEMM_STORE) a.y = (float*)out;
+  if (epi == GEMM_RESID) {
+    a.x = (float*)out;
+    a.rowmap = map;
+  }
+  if (epi == GEMM_SWIGLU) a.u = (bf16*)out;
+  if (epi == GEMM_ARGMAX) {
+    if ((r = cu(best.alloc((size_t)T * 8), "scratch")) != SSD_OK) return r;
+    if ((r = cu(cudaMemsetAsync(best.p, 0, (size_t)T * 8, s), "memset")) != SSD_OK) return r;
+    a.best = (unsigned long long*)best.p;
+  }
+  if ((r = cu(launch_gemm_rows(a, s), "linear_rows")) != SSD_OK) return r;
+  if (epi == GEMM_ARGMAX)
+    return cu(launch_argmax_index(a.best, T, (int32_t*)out, s), "argmax_index");
+  return SSD_OK;
+}
+
+ssd_status ssd_op_score_attention(const void* q, const int32_t* cand, int32_t n_cand, int32_t N,
+                                  int32_t split, const void* k_cache, const void* v_cache,
+                                  int32_t max_seq, const void* wk, const void* wv, int32_t H,
+                                  int32_t Hkv, int32_t dh, void* out, void* stream) {
+  if (!al16(q) || !cand || n_cand < 1 || N < 1 || split < 1 || split > max_seq ||
+      !al16(k_cache) || !al16(v_cache) || !al16(wk) || !al16(wv) || !al16(out) || H < 1 ||
+      Hkv < 1 || H % Hkv || (dh != 64 && dh != 128))
+    return op_fail(SSD_ERR_INVALID_ARG, "score_attention arguments");
+  ScoreAttnArgs a;
+  a.q = (const bf16*)q;
+  a.kc = (const bf16*)k_cache;
+  a.vc = (const bf16*)v_cache;
+  a.sk = (const bf16*)wk;
+  a.sv = (const bf16*)wv;
+  a.cand = cand;
+  a.N = N;
+  a.split = split;
+  a.max_seq = max_seq;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.dh = dh;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)dh));
+  a.out = (bf16*)out;
+  return cu(launch_score_attn(a, n_cand, (cudaStream_t)stream), "score_attention");
+}
+
 }  // extern "C"

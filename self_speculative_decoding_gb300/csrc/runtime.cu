@@ -99,12 +99,21 @@ struct ssd_ctx {
   float* vlogits = nullptr;
   int32_t* tokens = nullptr;
   int32_t* toks_in = nullptr;
-  // candidate-mask scoring: scratch K/V for the window positions and counters
-  bf16* sc_k = nullptr;
-  bf16* sc_v = nullptr;
-  int sc_len = 0;           // window capacity (positions)
-  int sc_split = -1;        // >= 0 while scoring: first window position
-  RowStats* sc_stats = nullptr;
+  // candidate-mask scoring: rows (candidate-major, up to max_score_rows) of
+  // the batched forward, per-layer candidate lists and compact row maps
+  float* sc_x = nullptr;          // [rows][D] residual stream
+  bf16* sc_xn = nullptr;          // [rows][D] normalised activations
+  float* sc_qkv = nullptr;        // [rows][(H + 2 Hkv) dh]
+  bf16* sc_q = nullptr;           // [rows][H dh] after RoPE
+  bf16* sc_sk = nullptr;          // [rows][Hkv dh] window keys (RoPE applied)
+  bf16* sc_sv = nullptr;          // [rows][Hkv dh] window values
+  bf16* sc_attn = nullptr;        // [rows][H dh]
+  bf16* sc_u = nullptr;           // [rows][FFN]
+  unsigned long long* sc_best = nullptr;  // [rows] argmax keys
+  int32_t* sc_cand = nullptr;     // [L][256]
+  int32_t* sc_map = nullptr;      // [L][rows]
+  int32_t* h_sc_cand = nullptr;   // pinned mirrors
+  int32_t* h_sc_map = nullptr;
   int32_t* sc_counts = nullptr;
   int32_t* h_counts = nullptr;
   DevState* st = nullptr;
@@ -274,12 +283,6 @@ AttnArgs attn_args(ssd_ctx* c, int l) {
   a.part = c->attn_part;
   a.counters = c->attn_cnt;
   a.err = &c->st->err;
-  if (c->sc_split >= 0) {
-    a.kc2 = c->sc_k + (size_t)l * g.n_kv_heads * c->sc_len * g.head_dim;
-    a.vc2 = c->sc_v + (size_t)l * g.n_kv_heads * c->sc_len * g.head_dim;
-    a.split = c->sc_split;
-    a.scratch_len = c->sc_len;
-  }
   a.scale = (float)(1.0 / std::sqrt((double)g.head_dim));
   return a;
 }
@@ -826,6 +829,132 @@ ssd_status ensure_policy(ssd_ctx* c) {
   return SSD_OK;
 }
 
+// SWIFT §4.1.2: the K candidate layer sets predict the committed tokens
+// t[split+1 .. split+N] from t[split .. split+N-1] in one batched forward.
+// Row p = k N + i is candidate k's window position split + i; a layer runs
+// the rows of the candidates that keep it (compact row t -> p through the
+// layer's row map), attending to the shared cache's positions below split
+// and to the candidate's own window K/V.  Leaves the match counts in
+// sc_counts; the shared cache is only read.
+ssd_status enq_score(ssd_ctx* c, const uint64_t* masks, int K, int N, int split) {
+  const ssd_config& g = c->cfg;
+  const int L = g.n_layers, D = g.d_model, rows = K * N, R = g.max_score_rows;
+  std::vector<int> nact(L, 0);
+  for (int l = 0; l < L; ++l) {
+    int32_t* cand = c->h_sc_cand + (size_t)l * 256;
+    int32_t* map = c->h_sc_map + (size_t)l * R;
+    for (int k = 0; k < K; ++k)
+      if (!((masks[4 * k + (l >> 6)] >> (l & 63)) & 1ull)) {
+        for (int i = 0; i < N; ++i) map[nact[l] * N + i] = k * N + i;
+        cand[nact[l]++] = k;
+      }
+  }
+  CK(cudaMemcpyAsync(c->sc_cand, c->h_sc_cand, (size_t)L * 256 * 4, cudaMemcpyHostToDevice,
+                     c->stream));
+  CK(cudaMemcpyAsync(c->sc_map, c->h_sc_map, (size_t)L * R * 4, cudaMemcpyHostToDevice, c->stream));
+  CK(cudaMemsetAsync(c->sc_counts, 0, (size_t)K * sizeof(int32_t), c->stream));
+  CK(cudaMemsetAsync(c->sc_best, 0, (size_t)rows * 8, c->stream));
+  ssd_status r;
+  cudaStream_t s = c->stream;
+  if ((r = note(c, launch_score_embed(c->embed, c->tokens, split, N, rows, D, c->sc_x, s),
+                "score_embed")) != SSD_OK)
+    return r;
+  const int HD = g.n_heads * g.head_dim;
+  for (int l = 0; l < L; ++l) {
+    const int T = nact[l] * N;
+    if (T == 0) continue;
+    const ssd_layer_weights& w = c->layers[l];
+    const int32_t* map = c->sc_map + (size_t)l * R;
+    if ((r = note(c, launch_score_norm(c->sc_x, map, (const float*)w.attn_norm, g.norm_eps, T, D,
+                                       c->sc_xn, s),
+                  "score_norm")) != SSD_OK)
+      return r;
+    GemmArgs q;
+    q.W0 = (const bf16*)w.wqkv;
+    q.R = qkv_rows(g);
+    q.K = D;
+    q.T = T;
+    q.act = c->sc_xn;
+    q.epi = GEMM_STORE;
+    q.err = &c->st->err;
+    q.y = c->sc_qkv;
+    if ((r = note(c, launch_gemm_rows(q, s), "score_qkv")) != SSD_OK) return r;
+    if ((r = note(c, launch_score_rope(c->sc_qkv, T, map, N, split, g.n_heads, g.n_kv_heads,
+                                       g.head_dim, c->rope, c->sc_q, c->sc_sk, c->sc_sv, s),
+                  "score_rope")) != SSD_OK)
+      return r;
+    ScoreAttnArgs at;
+    at.q = c->sc_q;
+    at.kc = c->kc + (size_t)l * kv_layer_elems(g);
+    at.vc = c->vc + (size_t)l * kv_layer_elems(g);
+    at.sk = c->sc_sk;
+    at.sv = c->sc_sv;
+    at.cand = c->sc_cand + (size_t)l * 256;
+    at.N = N;
+    at.split = split;
+    at.max_seq = g.max_seq;
+    at.H = g.n_heads;
+    at.Hkv = g.n_kv_heads;
+    at.dh = g.head_dim;
+    at.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)g.head_dim));
+    at.out = c->sc_attn;
+    if ((r = note(c, launch_score_attn(at, nact[l], s), "score_attn")) != SSD_OK) return r;
+    GemmArgs o;
+    o.W0 = (const bf16*)w.wo;
+    o.R = D;
+    o.K = HD;
+    o.T = T;
+    o.act = c->sc_attn;
+    o.epi = GEMM_RESID;
+    o.err = &c->st->err;
+    o.x = c->sc_x;
+    o.rowmap = map;
+    if ((r = note(c, launch_gemm_rows(o, s), "score_oproj")) != SSD_OK) return r;
+    if ((r = note(c, launch_score_norm(c->sc_x, map, (const float*)w.mlp_norm, g.norm_eps, T, D,
+                                       c->sc_xn, s),
+                  "score_norm")) != SSD_OK)
+      return r;
+    GemmArgs gu;
+    gu.W0 = (const bf16*)w.w_gate;
+    gu.W1 = (const bf16*)w.w_up;
+    gu.R = g.ffn_dim;
+    gu.K = D;
+    gu.T = T;
+    gu.act = c->sc_xn;
+    gu.epi = GEMM_SWIGLU;
+    gu.err = &c->st->err;
+    gu.u = c->sc_u;
+    if ((r = note(c, launch_gemm_rows(gu, s), "score_gate_up")) != SSD_OK) return r;
+    GemmArgs dn;
+    dn.W0 = (const bf16*)w.w_down;
+    dn.R = D;
+    dn.K = g.ffn_dim;
+    dn.T = T;
+    dn.act = c->sc_u;
+    dn.epi = GEMM_RESID;
+    dn.err = &c->st->err;
+    dn.x = c->sc_x;
+    dn.rowmap = map;
+    if ((r = note(c, launch_gemm_rows(dn, s), "score_down")) != SSD_OK) return r;
+  }
+  if ((r = note(c, launch_score_norm(c->sc_x, nullptr, c->final_norm, g.norm_eps, rows, D,
+                                     c->sc_xn, s),
+                "score_norm")) != SSD_OK)
+    return r;
+  GemmArgs lm;
+  lm.W0 = c->lm_head;
+  lm.R = g.vocab;
+  lm.K = D;
+  lm.T = rows;
+  lm.act = c->sc_xn;
+  lm.epi = GEMM_ARGMAX;
+  lm.err = &c->st->err;
+  lm.best = c->sc_best;
+  if ((r = note(c, launch_gemm_rows(lm, s), "score_lm_head")) != SSD_OK) return r;
+  return note(c, launch_score_match(c->sc_best, c->tokens, split, N, rows, c->sc_counts, s),
+              "score_match");
+}
+
 }  // namespace
 
 // ===========================================================================
@@ -911,13 +1040,20 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
             alloc((void**)&c->toks_in, (size_t)g.max_seq * 4) &&
             alloc((void**)&c->st, sizeof(DevState));
   if (ok && g.max_score_rows > 0) {
-    int w = g.max_score_rows < 512 ? g.max_score_rows : 512;
-    c->sc_len = ((w + 63) / 64) * 64;
-    const size_t e = (size_t)g.n_layers * g.n_kv_heads * c->sc_len * g.head_dim;
-    ok = alloc((void**)&c->sc_k, e * sizeof(bf16)) && alloc((void**)&c->sc_v, e * sizeof(bf16)) &&
-         alloc((void**)&c->sc_stats, (size_t)kMaxRows * sizeof(RowStats)) &&
+    const size_t r = (size_t)g.max_score_rows, D = g.d_model, HD = (size_t)g.n_heads * g.head_dim;
+    const size_t KV = (size_t)g.n_kv_heads * g.head_dim;
+    ok = alloc((void**)&c->sc_x, r * D * 4) && alloc((void**)&c->sc_xn, r * D * 2) &&
+         alloc((void**)&c->sc_qkv, r * qkv_rows(g) * 4) && alloc((void**)&c->sc_q, r * HD * 2) &&
+         alloc((void**)&c->sc_sk, r * KV * 2) && alloc((void**)&c->sc_sv, r * KV * 2) &&
+         alloc((void**)&c->sc_attn, r * HD * 2) && alloc((void**)&c->sc_u, r * g.ffn_dim * 2) &&
+         alloc((void**)&c->sc_best, r * 8) &&
+         alloc((void**)&c->sc_cand, (size_t)g.n_layers * 256 * 4) &&
+         alloc((void**)&c->sc_map, (size_t)g.n_layers * r * 4) &&
          alloc((void**)&c->sc_counts, 256 * sizeof(int32_t)) &&
-         cudaMallocHost((void**)&c->h_counts, 256 * sizeof(int32_t)) == cudaSuccess;
+         cudaMallocHost((void**)&c->h_counts, 256 * sizeof(int32_t)) == cudaSuccess &&
+         cudaMallocHost((void**)&c->h_sc_cand, (size_t)g.n_layers * 256 * 4) == cudaSuccess &&
+         cudaMallocHost((void**)&c->h_sc_map, (size_t)g.n_layers * r * 4) == cudaSuccess;
+    if (ok) cudaMemsetAsync(c->sc_best, 0, r * 8, c->stream);
   }
   if (!ok) {
     ssd_destroy(c);
@@ -978,11 +1114,13 @@ ssd_status ssd_destroy(ssd_ctx* c) {
                   c->dlogits, c->vlogits, c->tokens, c->toks_in, c->st};
   for (void* p : bufs)
     if (p) cudaFree(p);
-  if (c->sc_k) cudaFree(c->sc_k);
-  if (c->sc_v) cudaFree(c->sc_v);
-  if (c->sc_stats) cudaFree(c->sc_stats);
-  if (c->sc_counts) cudaFree(c->sc_counts);
+  void* sc[] = {c->sc_x,    c->sc_xn,   c->sc_qkv,  c->sc_q,   c->sc_sk,  c->sc_sv,
+                c->sc_attn, c->sc_u,    c->sc_best, c->sc_cand, c->sc_map, c->sc_counts};
+  for (void* p : sc)
+    if (p) cudaFree(p);
   if (c->h_counts) cudaFreeHost(c->h_counts);
+  if (c->h_sc_cand) cudaFreeHost(c->h_sc_cand);
+  if (c->h_sc_map) cudaFreeHost(c->h_sc_map);
   if (c->h_st) cudaFreeHost(c->h_st);
   if (c->h_tok) cudaFreeHost(c->h_tok);
   if (c->cap) cudaStreamDestroy(c->cap);
@@ -1299,7 +1437,7 @@ ssd_status ssd_swift_generate(ssd_ctx* c, const ssd_swift_params* pp, int32_t n_
   if (r != SSD_OK) return r;
   if (c->pol.mode != SSD_MODE_SKIP) return fail(c, SSD_ERR_STATE, "swift needs a skip-mode policy");
   if (c->phase != PH_IDLE) return fail(c, SSD_ERR_STATE, "a round is in flight");
-  if ((int64_t)P.candidates * P.window > c->cfg.max_score_rows || P.window > c->sc_len)
+  if ((int64_t)P.candidates * P.window > c->cfg.max_score_rows)
     return fail(c, SSD_ERR_CAPACITY, "candidates * window exceeds max_score_rows");
   if ((r = read_state(c)) != SSD_OK) return r;
   const int n_start = c->h_st->n;
@@ -1462,39 +1600,16 @@ ssd_status ssd_score_masks(ssd_ctx* c, const uint64_t* masks, int32_t K, int32_t
   ssd_status r = ensure_policy(c);
   if (r != SSD_OK) return r;
   if (c->phase != PH_IDLE) return fail(c, SSD_ERR_STATE, "a round is in flight");
-  if (c->sc_len == 0 || (int64_t)K * N > c->cfg.max_score_rows || N > c->sc_len)
-    return fail(c, SSD_ERR_CAPACITY, "K*N exceeds max_score_rows (or the scoring window)");
+  if ((int64_t)K * N > c->cfg.max_score_rows)
+    return fail(c, SSD_ERR_CAPACITY, "K*N exceeds max_score_rows");
   if ((r = read_state(c)) != SSD_OK) return r;
   const int n = c->h_st->n;
   if (N + 2 > n) return fail(c, SSD_ERR_CAPACITY, "window longer than the committed context");
-  const int L = c->cfg.n_layers;
-  // SWIFT §4.1.2: candidate k predicts the committed tokens t[n-N..n-1] from
-  // t[n-N-1..n-2]; positions >= split use the scratch cache, so the shared
-  // full-model cache is only read.
-  const int split = n - N - 1;
   Range nv("ssd score_masks");
-  CK(cudaMemsetAsync(c->sc_counts, 0, (size_t)K * sizeof(int32_t), c->stream));
-  c->sc_split = split;
-  for (int k = 0; k < K && r == SSD_OK; ++k) {
-    std::vector<int> keep;
-    for (int l = 0; l < L; ++l)
-      if (!((masks[4 * k + (l >> 6)] >> (l & 63)) & 1ull)) keep.push_back(l);
-    for (int c0 = 0; c0 < N && r == SSD_OK; c0 += kMaxRows) {
-      const int M = N - c0 < kMaxRows ? N - c0 : kMaxRows;
-      if ((r = enq_begin(c, BEGIN_TOKENS, c->stream, M, split + c0, c->tokens + split + c0)) != SSD_OK)
-        break;
-      if ((r = enq_layers(c, keep, c->stream)) != SSD_OK) break;
-      if ((r = enq_lmhead(c, c->sc_stats, nullptr, nullptr, -1, c->stream)) != SSD_OK) break;
-      r = note(c, launch_match_count(c->sc_stats, c->tokens + split + 1 + c0, &c->st->M,
-                                     c->sc_counts + k, c->stream),
-               "match_count");
-    }
-  }
-  c->sc_split = -1;
-  if (r != SSD_OK) return r;
+  if ((r = enq_score(c, masks, K, N, n - N - 1)) != SSD_OK) return r;
   CK(cudaMemcpyAsync(c->h_counts, c->sc_counts, (size_t)K * sizeof(int32_t), cudaMemcpyDeviceToHost,
                      c->stream));
-  if ((r = wait_stream(c)) != SSD_OK) return r;
+  if ((r = read_state(c)) != SSD_OK) return r;
   int best = 0;
   for (int k = 0; k < K; ++k) {
     matchness_out[k] = (float)c->h_counts[k] / (float)N;

@@ -1,0 +1,359 @@
+// Batched candidate-mask scoring (SWIFT §4.1.2): K candidate layer sets each
+// predict the last N committed tokens in one parallel forward.  Rows are laid
+// out candidate-major: physical row p = k * N + i is candidate k's window
+// position split + i.  A layer runs only the rows of the candidates that keep
+// it; those rows are packed densely (compact row t, row map t -> p) so that
+// the projections (gemm.cu) do no work for a skipped layer.
+//
+// This file holds everything of the scoring forward that is not a
+// projection: the embedding of the window tokens, the RMSNorm of mapped rows
+// into bf16 activations, RoPE with the window K/V write, the attention of the
+// window queries (tensor cores, flash-style online softmax) and the match
+// count of the argmax against the committed tokens.
+#include "kernels.cuh"
+
+namespace ssd {
+
+namespace {
+
+// x[p] = E[tokens[split + p % N]] (fp32) for p < rows.
+__global__ void score_embed_kernel(const bf16* embed, const int32_t* tokens, int split, int N,
+                                   int rows, int D, float* x) {
+  const size_t n = (size_t)rows * D;
+  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < n;
+       e += (size_t)gridDim.x * blockDim.x) {
+    const int p = (int)(e / D), k = (int)(e % D);
+    x[e] = __bfloat162float(embed[(size_t)tokens[split + p % N] * D + k]);
+  }
+}
+
+// out[t] = bf16(rmsnorm(x[map[t]]) * gain): one warp per row; lane l sums
+// the squares of elements 2l, 2l + 1, 2l + 64, ... in that order, then a
+// butterfly over the warp.
+__global__ void __launch_bounds__(256) score_norm_kernel(const float* x, const int32_t* map,
+                                                         const float* gain, float eps, int T,
+                                                         int D, bf16* out) {
+  const int t = (blockIdx.x * 256 + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const float* xr = x + (size_t)(map ? map[t] : t) * D;
+  float s = 0.f;
+  for (int k = 2 * lane; k < D; k += 64) {
+    const float2 v = *reinterpret_cast<const float2*>(xr + k);
+    s += v.x * v.x;
+    s += v.y * v.y;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  const float rs = 1.0f / sqrtf(s / (float)D + eps);
+  for (int k = 2 * lane; k < D; k += 64) {
+    const float2 v = *reinterpret_cast<const float2*>(xr + k);
+    *reinterpret_cast<uint32_t*>(out + (size_t)t * D + k) =
+        pack_bf16x2(v.x * rs * gain[k], v.y * rs * gain[k + 1]);
+  }
+}
+
+// RoPE (rotate-half pairs (j, j + dh/2)) of the compact rows' q and k at
+// position split + p % N; q -> q[t] bf16, k and v -> the window cache row p.
+__global__ void score_rope_kernel(const float* qkv, int T, const int32_t* map, int N, int split,
+                                  int H, int Hkv, int dh, const float2* rope, bf16* q, bf16* sk,
+                                  bf16* sv) {
+  const int half = dh / 2;
+  const int per_row = (H + Hkv) * half + Hkv * half;  // rotations + v pairs
+  const int ld = (H + 2 * Hkv) * dh;
+  const size_t n = (size_t)T * per_row;
+  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < n;
+       e += (size_t)gridDim.x * blockDim.x) {
+    const int t = (int)(e / per_row);
+    int r = (int)(e % per_row);
+    const int p = map[t];
+    const int pos = split + p % N;
+    const float* row = qkv + (size_t)t * ld;
+    if (r < (H + Hkv) * half) {
+      const int hh = r / half, j = r % half;
+      const float* v = row + (size_t)hh * dh;
+      const float2 cs = rope[(size_t)pos * half + j];
+      const float a = v[j], b = v[j + half];
+      const float ra = a * cs.x - b * cs.y, rb = a * cs.y + b * cs.x;
+      if (hh < H) {
+        bf16* d = q + (size_t)t * H * dh + (size_t)hh * dh;
+        d[j] = __float2bfloat16_rn(ra);
+        d[j + half] = __float2bfloat16_rn(rb);
+      } else {
+        bf16* d = sk + ((size_t)p * Hkv + (hh - H)) * dh;
+        d[j] = __float2bfloat16_rn(ra);
+        d[j + half] = __float2bfloat16_rn(rb);
+      }
+    } else {
+      r -= (H + Hkv) * half;
+      const int kvh = r / half, j2 = 2 * (r % half);
+      const float* v = row + (size_t)(H + Hkv) * dh + (size_t)kvh * dh;
+      *reinterpret_cast<uint32_t*>(sv + ((size_t)p * Hkv + kvh) * dh + j2) =
+          pack_bf16x2(v[j2], v[j2 + 1]);
+    }
+  }
+}
+
+SSD_DI void cp_async16_z(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+SSD_DI void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+SSD_DI void cp_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+SSD_DI void ldsm_x4_trans(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_addr(p)));
+}
+
+constexpr int kSaKeys = 64;  // keys per block
+
+// Window-query attention.  CTA (row block, head h, active candidate ja):
+// warps own 16 query rows each.  Keys: the shared cache's positions
+// [0, split) then the candidate's own window rows w <= i.  S = Q K^T and
+// O += P V run on the tensor cores (bf16 operands, fp32 accumulation); the
+// softmax is the online form in base 2 with the running max per row.  Every
+// row sums its key blocks in ascending key order.
+template <int DH>
+__global__ void __launch_bounds__(128) score_attn_kernel(ScoreAttnArgs a) {
+  extern __shared__ __align__(16) unsigned char sm_raw[];
+  constexpr int KT = DH / 16;      // k16 steps of Q K^T
+  constexpr int NT = DH / 8;       // n8 tiles of the output
+  constexpr int RS = DH + 8;       // padded smem row (bf16)
+  bf16* smK = reinterpret_cast<bf16*>(sm_raw);          // [2][64][RS]
+  bf16* smV = smK + 2 * kSaKeys * RS;                   // [2][64][RS]
+  const int nw = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int h = blockIdx.y, ja = blockIdx.z;
+  const int kvh = h / (a.H / a.Hkv);
+  const int cand = a.cand[ja];
+  const int r0 = blockIdx.x * nw * 16;                 // first window row of the CTA
+  const int i0 = r0 + warp * 16;                       // first row of the warp
+  const int N = a.N;
+
+  // Q fragments (rows beyond N are zero)
+  uint32_t qf[KT][4];
+  {
+    const int ia = i0 + g, ib = i0 + g + 8;
+    const bf16* qa = a.q + ((size_t)(ja * N + ia) * a.H + h) * DH;
+    const bf16* qb = a.q + ((size_t)(ja * N + ib) * a.H + h) * DH;
+#pragma unroll
+    for (int kt = 0; kt < KT; ++kt) {
+      const int k0 = kt * 16 + 2 * c;
+      qf[kt][0] = ia < N ? *reinterpret_cast<const uint32_t*>(qa + k0) : 0u;
+      qf[kt][1] = ib < N ? *reinterpret_cast<const uint32_t*>(qb + k0) : 0u;
+      qf[kt][2] = ia < N ? *reinterpret_cast<const uint32_t*>(qa + k0 + 8) : 0u;
+      qf[kt][3] = ib < N ? *reinterpret_cast<const uint32_t*>(qb + k0 + 8) : 0u;
+    }
+  }
+  float o[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+
+  const int nb_pre = (a.split + kSaKeys - 1) / kSaKeys;
+  const int wmax = min(N, r0 + nw * 16);               // window keys the CTA needs
+  const int nb = nb_pre + (wmax + kSaKeys - 1) / kSaKeys;
+  const bf16* kc = a.kc + (size_t)kvh * a.max_seq * DH;
+  const bf16* vc = a.vc + (size_t)kvh * a.max_seq * DH;
+
+  auto load_block = [&](int b, int buf) {
+    constexpr int PR = DH / 8;                         // 16-byte pieces per row
+    for (int e = threadIdx.x; e < kSaKeys * PR; e += blockDim.x) {
+      const int key = e / PR, q = e % PR;
+      const bf16 *ks, *vs;
+      bool ok;
+      if (b < nb_pre) {
+        const int pos = b * kSaKeys + key;
+        ok = pos < a.split;
+        ks = kc + (size_t)(ok ? pos : 0) * DH;
+        vs = vc + (size_t)(ok ? pos : 0) * DH;
+      } else {
+        const int w = (b - nb_pre) * kSaKeys + key;
+        ok = w < wmax;
+        const size_t row = ((size_t)cand * N + (ok ? w : 0)) * a.Hkv + kvh;
+        ks = a.sk + row * DH;
+        vs = a.sv + row * DH;
+      }
+      cp_async16_z(smK + ((size_t)buf * kSaKeys + key) * RS + q * 8, ks + q * 8, ok);
+      cp_async16_z(smV + ((size_t)buf * kSaKeys + key) * RS + q * 8, vs + q * 8, ok);
+    }
+  };
+
+  load_block(0, 0);
+  cp_commit();
+  for (int b = 0; b < nb; ++b) {
+    const int buf = b & 1;
+    if (b + 1 < nb) load_block(b + 1, buf ^ 1);
+    cp_commit();
+    cp_wait1();
+    __syncthreads();
+    const bf16* Kb = smK + (size_t)buf * kSaKeys * RS;
+    const bf16* Vb = smV + (size_t)buf * kSaKeys * RS;
+    // S = Q K^T for 64 keys
+    float s[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+      const bf16* kr = Kb + (size_t)(nt * 8 + g) * RS + 2 * c;
+#pragma unroll
+      for (int kt = 0; kt < KT; ++kt) {
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(kr + kt * 16);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(kr + kt * 16 + 8);
+        mma_bf16(s[nt], qf[kt][0], qf[kt][1], qf[kt][2], qf[kt][3], b0, b1);
+      }
+    }
+    // mask, scale, online softmax
+    const bool pre = b < nb_pre;
+    const int kbase = pre ? b * kSaKeys : (b - nb_pre) * kSaKeys;
+    float bm[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = kbase + nt * 8 + 2 * c + (e & 1);
+        const int i = i0 + g + 8 * (e >> 1);
+        const bool valid = pre ? key < a.split : key <= i && key < N;
+        const float v = valid ? s[nt][e] * a.scale_log2 : -INFINITY;
+        s[nt][e] = v;
+        bm[e >> 1] = fmaxf(bm[e >> 1], v);
+      }
+    float corr[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      bm[r] = fmaxf(bm[r], __shfl_xor_sync(0xffffffffu, bm[r], 1));
+      bm[r] = fmaxf(bm[r], __shfl_xor_sync(0xffffffffu, bm[r], 2));
+      const float mn = fmaxf(mrow[r], bm[r]);
+      corr[r] = mn == -INFINITY ? 1.f : exp2f(mrow[r] - mn);
+      mrow[r] = mn;
+    }
+    float ls[2] = {0.f, 0.f};
+    uint32_t pf[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      float pv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float m = mrow[e >> 1];
+        pv[e] = m == -INFINITY ? 0.f : exp2f(s[nt][e] - m);
+        ls[e >> 1] += pv[e];
+      }
+      pf[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(pv[0], pv[1]);
+      pf[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) lrow[r] = lrow[r] * corr[r] + ls[r];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      o[j][0] *= corr[0];
+      o[j][1] *= corr[0];
+      o[j][2] *= corr[1];
+      o[j][3] *= corr[1];
+    }
+    // O += P V: k16 step kk covers keys 16kk .. 16kk + 15
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      // A fragment order: (row g, keys 2c..), (row g+8, keys 2c..),
+      // (row g, keys 2c+8..), (row g+8, keys 2c+8..)
+      const uint32_t a0 = pf[kk][0], a1 = pf[kk][1], a2 = pf[kk][2], a3 = pf[kk][3];
+      const int mi = lane >> 3, rr = lane & 7;
+#pragma unroll
+      for (int j = 0; j < NT; j += 2) {
+        uint32_t vb[4];
+        ldsm_x4_trans(vb, Vb + (size_t)(kk * 16 + (mi & 1) * 8 + rr) * RS + j * 8 + (mi >> 1) * 8);
+        mma_bf16(o[j], a0, a1, a2, a3, vb[0], vb[1]);
+        mma_bf16(o[j + 1], a0, a1, a2, a3, vb[2], vb[3]);
+      }
+    }
+    __syncthreads();
+  }
+  // row sums over the 4 lanes of a row, normalise, store
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
+    lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
+  }
+  const int ia = i0 + g, ib = i0 + g + 8;
+  const float inva = 1.0f / lrow[0], invb = 1.0f / lrow[1];
+  bf16* oa = a.out + (size_t)(ja * N + ia) * a.H * DH + (size_t)h * DH;
+  bf16* ob = a.out + (size_t)(ja * N + ib) * a.H * DH + (size_t)h * DH;
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    const int d = j * 8 + 2 * c;
+    if (ia < N) *reinterpret_cast<uint32_t*>(oa + d) = pack_bf16x2(o[j][0] * inva, o[j][1] * inva);
+    if (ib < N) *reinterpret_cast<uint32_t*>(ob + d) = pack_bf16x2(o[j][2] * invb, o[j][3] * invb);
+  }
+}
+
+// counts[p / N] += (argmax of row p == tokens[split + 1 + p % N]); best[p]
+// is returned to zero for the next call.
+__global__ void score_match_kernel(unsigned long long* best, const int32_t* tokens, int split,
+                                   int N, int rows, int32_t* counts) {
+  const int p = blockIdx.x * blockDim.x + threadIdx.x;
+  if (p >= rows) return;
+  const unsigned long long key = best[p];
+  const int idx = (int)(0xffffffffu - (uint32_t)(key & 0xffffffffull));
+  if (key != 0ull && idx == tokens[split + 1 + p % N]) atomicAdd(counts + p / N, 1);
+  best[p] = 0ull;
+}
+
+}  // namespace
+
+cudaError_t launch_score_embed(const bf16* embed, const int32_t* tokens, int split, int N, int rows,
+                               int D, float* x, cudaStream_t s) {
+  score_embed_kernel<<<1216, 256, 0, s>>>(embed, tokens, split, N, rows, D, x);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_score_norm(const float* x, const int32_t* map, const float* gain, float eps,
+                              int T, int D, bf16* out, cudaStream_t s) {
+  if (D % 64) return cudaErrorInvalidValue;
+  score_norm_kernel<<<(T * 32 + 255) / 256, 256, 0, s>>>(x, map, gain, eps, T, D, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_score_rope(const float* qkv, int T, const int32_t* map, int N, int split, int H,
+                              int Hkv, int dh, const float2* rope, bf16* q, bf16* sk, bf16* sv,
+                              cudaStream_t s) {
+  score_rope_kernel<<<1216, 256, 0, s>>>(qkv, T, map, N, split, H, Hkv, dh, rope, q, sk, sv);
+  return cudaGetLastError();
+}
+
+size_t score_attn_smem(int dh) { return (size_t)4 * kSaKeys * (dh + 8) * sizeof(bf16); }
+
+cudaError_t launch_score_attn(const ScoreAttnArgs& a, int n_active, cudaStream_t s) {
+  if (n_active <= 0) return cudaSuccess;
+  const int nw = a.N >= 64 ? 4 : (a.N + 15) / 16;
+  dim3 grid((a.N + nw * 16 - 1) / (nw * 16), a.H, n_active);
+  const size_t smem = score_attn_smem(a.dh);
+  static bool ready128 = false, ready64 = false;
+  cudaError_t e = cudaSuccess;
+  if (a.dh == 128) {
+    if (!ready128)
+      e = cudaFuncSetAttribute(score_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
+    if (e != cudaSuccess) return e;
+    ready128 = true;
+    score_attn_kernel<128><<<grid, nw * 32, smem, s>>>(a);
+  } else if (a.dh == 64) {
+    if (!ready64)
+      e = cudaFuncSetAttribute(score_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
+    if (e != cudaSuccess) return e;
+    ready64 = true;
+    score_attn_kernel<64><<<grid, nw * 32, smem, s>>>(a);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_score_match(unsigned long long* best, const int32_t* tokens, int split, int N,
+                               int rows, int32_t* counts, cudaStream_t s) {
+  score_match_kernel<<<(rows + 255) / 256, 256, 0, s>>>(best, tokens, split, N, rows, counts);
+  return cudaGetLastError();
+}
+
+}  // namespace ssd

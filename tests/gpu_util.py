@@ -32,7 +32,14 @@ def to_device_weights(wts):
 
 
 def pack_reference(bits: np.ndarray) -> np.ndarray:
-    """The packed unit layout, written out with numpy index arithmetic."""
+    """The packed unit layout, written out with numpy index arithmetic:
+    16 x 32 tiles ordered (row group, K block), each 8-row half row-major with
+    the 16-byte chunks of row g at positions c ^ ((g >> 1) & 3)."""
     R, K = bits.shape
     u = bits.reshape(R // 16, 2, 8, K // 32, 4, 8)        # vr, h, g, kb, c, e
-    return u.transpose(0, 3, 1, 2, 4, 5).reshape(R, K)      # vr, kb, h, g, c, e
+    u = u.transpose(0, 3, 1, 2, 4, 5).copy()               # vr, kb, h, g, c, e
+    out = np.empty_like(u)
+    for g in range(8):
+        for c in range(4):
+            out[:, :, :, g, c ^ ((g >> 1) & 3), :] = u[:, :, :, g, c, :]
+    return out.reshape(R, K)

@@ -5,8 +5,8 @@
   candidate the match counts may differ only at window rows where the
   oracle's top-1/top-2 gap is <= 0.1.
 * The empty candidate reproduces the full model, so on the library's own
-  greedy window it scores exactly 1.0 (scoring passes of up to 16 rows are
-  bit-identical to the single-row decode that produced the window).
+  greedy window it scores 1.0, except at rows with a near tie (the batched
+  scoring forward sums in its own fixed order, not the decode GEMV's).
 * Scoring reads the shared KV cache but never writes it.
 """
 
@@ -69,14 +69,25 @@ def test_scoring_matches_oracle(ssd, N):
 
 @pytest.mark.parametrize("w", [TINY, SMALL])
 def test_empty_mask_scores_one_on_own_greedy_window(ssd, w):
+    from oracle import OracleModel, prefill, score_masks
     wts = make_weights(w, dtype="bf16", random_gains=True)
     ctx = ssd.SSDContext(w.shape, to_device_weights(wts), max_seq=256, max_score_rows=256)
-    ctx.set_policy(Policy(mode="skip", skip=(), d_max=4))
+    pol = Policy(mode="skip", skip=(), d_max=4)
+    ctx.set_policy(pol)
     ctx.prefill(make_prompt(w, 10))
     ctx.decode_ar(40)
     scores, best = ctx.score_masks([(), (1,), (0, 2)], 32)
-    assert scores[0] == 1.0
-    assert best == 0
+    # the full model predicts its own greedy tokens; the batched pass sums in
+    # another order than the decode, so a miss is allowed only at a row whose
+    # (oracle) top-1/top-2 gap is <= 0.1
+    seq = ctx.tokens()
+    m = OracleModel(w.shape, weights_to_numpy(wts))
+    st = prefill(m, seq, pol, 256)
+    _, _, logits = score_masks(m, seq, st.kv, [()], 32)
+    ties = sum(_near_tie(z) for z in logits[0])
+    assert round(scores[0] * 32) >= 32 - ties
+    if ties == 0:
+        assert scores[0] == 1.0 and best == 0
     ctx.close()
 
 

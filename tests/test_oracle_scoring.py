@@ -50,3 +50,34 @@ def test_scoring_does_not_touch_the_shared_cache():
     score_masks(m, st.tokens, st.kv, [(1,), (2,)], N=8)
     for a, b in zip(before, st.kv.K):
         np.testing.assert_array_equal(a, b)
+
+
+def test_score_attention_equals_model_attention_on_forked_caches():
+    """oracle.ops.score_attention equals the decoder's own attention row when
+    candidate k's window keys are written into a copy of the shared cache at
+    positions split + w (the per-candidate fork of oracle.scoring)."""
+    from oracle.ops import score_attention
+    from oracle.model import OracleModel, KVCache
+    from types import SimpleNamespace
+    rng = np.random.default_rng(7)
+    H, Hkv, dh, N, split, max_seq = 4, 2, 16, 5, 9, 32
+    K = rng.standard_normal((Hkv, max_seq, dh))
+    V = rng.standard_normal((Hkv, max_seq, dh))
+    rows = 3 * N
+    WK = rng.standard_normal((rows, Hkv, dh))
+    WV = rng.standard_normal((rows, Hkv, dh))
+    cand = [2, 0]
+    q = rng.standard_normal((len(cand) * N, H, dh))
+    got = score_attention(q, cand, N, split, K, V, WK, WV, H, Hkv)
+    m = OracleModel.__new__(OracleModel)
+    m.s = SimpleNamespace(n_heads=H, n_kv_heads=Hkv, head_dim=dh)
+    from oracle.numerics import bf16_round
+    for j, k in enumerate(cand):
+        kv = KVCache.__new__(KVCache)
+        kv.K, kv.V = [K.copy()], [V.copy()]
+        for w in range(N):
+            kv.K[0][:, split + w] = WK[k * N + w]
+            kv.V[0][:, split + w] = WV[k * N + w]
+        for i in range(N):
+            ref = bf16_round(m.attention_row(q[j * N + i], kv, 0, split + i))
+            np.testing.assert_array_equal(got[j * N + i], ref)
