@@ -204,6 +204,35 @@ ssd_status ssd_generate(ssd_ctx* ctx, int32_t n_tokens, int32_t* out, ssd_stats*
  * speedup is measured against), same kernels.  out (host, nullable). */
 ssd_status ssd_decode_ar(ssd_ctx* ctx, int32_t n_tokens, int32_t* out, ssd_stats* stats);
 
+/* Lossy early exit (LayerSkip blog §3, inference mode one): each step runs
+ * the pending token through the policy's draft layers only (exit mode:
+ * layers 0..E; skip mode: the kept layers and sublayers) and commits the
+ * shared final RMSNorm + LM head's pick (greedy, or at temperature > 0 the
+ * Gumbel-max sample an autoregressive step would draw).  No verification:
+ * the output is the early model's.  The dropped layers' K/V of those
+ * positions are not written, so until the context is rewound to before the
+ * first of them (ssd_rewind) or prefilled again, the lossless entry points
+ * (ssd_draft, ssd_generate, ssd_decode_ar, ssd_score_masks,
+ * ssd_swift_generate, ssd_layer_features) return SSD_ERR_STATE.  A policy
+ * whose draft runs every sublayer decodes losslessly and sets no such mark.
+ * out (host, nullable, >= n_tokens); stats (host, nullable): rounds =
+ * emitted = n_tokens, draft_ms = device time of the steps.
+ * Errors: CAPACITY, STATE, CUDA, TIMEOUT. */
+ssd_status ssd_decode_lossy(ssd_ctx* ctx, int32_t n_tokens, int32_t* out, ssd_stats* stats);
+
+/* AdaInfer exit features (EE-structure page, steps 1-2): one
+ * autoregressive step of the pending token (it commits what ssd_decode_ar
+ * would) with the early-exit head (final RMSNorm + LM head) applied to the
+ * hidden state after every layer l = min_layer .. L-1.  For entry
+ * i = l - min_layer (host arrays of L - min_layer entries): top1[i] = the
+ * argmax, top_prob[i] = p1 = max softmax, gap[i] = p1 - p2 (the two largest
+ * probabilities).  The label of layer l is top1[i] == top1[L-1-min_layer].
+ * Costs one LM-head pass per layer.
+ * Errors: INVALID_ARG (min_layer outside 0..L-1, NULL outputs), CAPACITY,
+ * STATE, CUDA, TIMEOUT. */
+ssd_status ssd_layer_features(ssd_ctx* ctx, int32_t min_layer, int32_t* top1, float* top_prob,
+                              float* gap);
+
 /* SWIFT §4.1.2: scores K candidate skip sets by matchness.  Candidate k
  * (masks[4k..4k+3], host, bit l = layer l skipped) runs the window inputs
  * t[n-N-1..n-2] causally through its kept layers, attending to the

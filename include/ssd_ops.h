@@ -117,8 +117,13 @@ ssd_status ssd_op_philox(const uint32_t* ctr, int32_t count, uint64_t key, uint3
  *   epi 2 (swiglu): out bf16 [T][R] = bf16(silu(W act) * (W1 act)), W1 the
  *                   up matrix (same shape as W)
  *   epi 3 (argmax): out int32 [T] = argmax_r (W act)[r], lowest r on ties
- * W, W1 packed (ssd_pack_weight).  Every output sums K in ascending 32-wide
- * steps, whatever T.  This call has no limit of 16 rows. */
+ * W, W1 packed (ssd_pack_weight).  With epi | SSD_ROWS_ACT_PACKED, act is
+ * already in the packed layout: ssd_pack_weight of the [T'][K] matrix, T'
+ * = T rounded up to 16 (the rows beyond T are read and their results
+ * dropped); otherwise the call packs a scratch copy first.  Every output
+ * sums K in ascending 32-wide steps, whatever T.  This call has no limit of
+ * 16 rows. */
+#define SSD_ROWS_ACT_PACKED 16
 ssd_status ssd_op_linear_rows(const void* W, const void* W1, int32_t R, int32_t K,
                               const void* act, int32_t T, int32_t epi, void* out,
                               const int32_t* map, void* stream);

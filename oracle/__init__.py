@@ -10,7 +10,9 @@ from the pages' description of the method:
 * LayerSkip blog (marsggbo.github.io, "ACL'24 | LayerSkip ...") — early-exit
   drafting through the shared LM head (§3.1), verify over d+1 positions with
   KV reuse (§3.2), min(1, p/q) acceptance with residual resampling and the
-  bonus token (§3.3).
+  bonus token (§3.3), lossy early exit (§3, inference mode one).
+* The early-exit structure page on AdaInfer — per-layer gap / top-prob exit
+  features and their labels (steps 1-2).
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
 leg may import this package.  The CUDA library never calls it and shares no
@@ -35,6 +37,13 @@ from .speculative import (  # noqa: F401
     accept_stochastic,
 )
 from .scoring import score_masks, score_masks_bruteforce  # noqa: F401
+from .adaptive import (  # noqa: F401
+    lossy_step,
+    lossy_generate,
+    layer_features,
+    exit_features,
+    LayerFeatures,
+)
 from .swift import (  # noqa: F401
     SplitMix64,
     SwiftParams,

@@ -194,6 +194,27 @@ class SSDContext:
         self._check(_lib().ssd_decode_ar(self._h, n_tokens, ptr, C.byref(stats)))
         return (out[:n_tokens].tolist() if want_tokens else None), stats.as_dict()
 
+    def decode_lossy(self, n_tokens: int, want_tokens: bool = True):
+        """Lossy early exit (ssd_decode_lossy): the draft layers alone decide."""
+        out = np.zeros(max(n_tokens, 1), dtype=np.int32)
+        stats = SsdStats()
+        ptr = out.ctypes.data_as(C.POINTER(C.c_int32)) if want_tokens else None
+        self._check(_lib().ssd_decode_lossy(self._h, n_tokens, ptr, C.byref(stats)))
+        return (out[:n_tokens].tolist() if want_tokens else None), stats.as_dict()
+
+    def layer_features(self, min_layer: int = 0):
+        """AdaInfer exit features of one AR step (ssd_layer_features):
+        (top1, top_prob, gap) lists over layers min_layer .. L-1."""
+        nl = self.shape.n_layers - min_layer
+        t = np.zeros(max(nl, 1), dtype=np.int32)
+        p = np.zeros(max(nl, 1), dtype=np.float32)
+        g = np.zeros(max(nl, 1), dtype=np.float32)
+        self._check(_lib().ssd_layer_features(self._h, min_layer,
+                                              t.ctypes.data_as(C.POINTER(C.c_int32)),
+                                              p.ctypes.data_as(C.POINTER(C.c_float)),
+                                              g.ctypes.data_as(C.POINTER(C.c_float))))
+        return t[:nl].tolist(), p[:nl].tolist(), g[:nl].tolist()
+
     def score_masks(self, masks: Sequence[Sequence[int]], N: int):
         K = len(masks)
         words = np.zeros((K, 4), dtype=np.uint64)

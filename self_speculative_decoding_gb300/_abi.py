@@ -99,6 +99,8 @@ _SIGS = {
     "ssd_generate": [_P, _I, C.POINTER(_I), C.POINTER(SsdStats)],
     "ssd_decode_ar": [_P, _I, C.POINTER(_I), C.POINTER(SsdStats)],
     "ssd_score_masks": [_P, C.POINTER(C.c_uint64), _I, _I, C.POINTER(C.c_float), C.POINTER(_I)],
+    "ssd_decode_lossy": [_P, _I, C.POINTER(_I), C.POINTER(SsdStats)],
+    "ssd_layer_features": [_P, _I, C.POINTER(_I), C.POINTER(C.c_float), C.POINTER(C.c_float)],
     "ssd_rewind": [_P, _I],
     "ssd_get_tokens": [_P, C.POINTER(_I), _I, C.POINTER(_I)],
     "ssd_set_timeout_ms": [_P, _I],

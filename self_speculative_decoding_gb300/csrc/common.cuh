@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#define SSD_HD __host__ __device__ __forceinline__
 #define SSD_DI __device__ __forceinline__
 
 namespace ssd {
@@ -210,6 +211,16 @@ SSD_DI float gumbel_at(uint64_t seed, int v, int pos, int round, int stream) {
 // offset, within a half, of the chunk that mma.sync lane L = 4g + c needs
 // (row g, columns 8c .. 8c + 7).
 SSD_DI int unit_slot(int lane) { return (lane ^ ((lane >> 3) & 3)) << 4; }
+
+// Element offset of (row t, column k) of a [T][K] bf16 matrix stored in the
+// packed unit layout (units ordered (t / 16, k / 32); T padded to 16 rows).
+// The many-row projection reads its activations in this layout, one bulk
+// copy per unit.
+SSD_HD size_t packed_off(int t, int k, int K) {
+  const int r = t & 15;
+  return ((size_t)(t >> 4) * (size_t)(K >> 5) + (size_t)(k >> 5)) * 512 + (size_t)r * 32 +
+         (size_t)(((((k >> 3) & 3) ^ (((r & 7) >> 1) & 3))) << 3) + (size_t)(k & 7);
+}
 
 // Total order used by every argmax: larger value first, then lower index.
 SSD_DI bool better(float va, int ia, float vb, int ib) {

@@ -290,6 +290,24 @@ cudaError_t launch_accept_stochastic(const AcceptArgs& a, cudaStream_t s, bool p
   return cudaLaunchKernelEx(&lc, accept_stoch_kernel, a);
 }
 
+// AdaInfer exit features of n exit-head summaries: out[0][l] = top1 (int
+// bits), out[1][l] = p1 = exp(z1 - lse), out[2][l] = p1 - p2 with
+// p2 = exp(z2 - lse).
+__global__ void exit_features_kernel(const RowStats* st, int n, float* out) {
+  const int l = blockIdx.x * blockDim.x + threadIdx.x;
+  if (l >= n) return;
+  const RowStats r = st[l];
+  const float p1 = expf(r.z1 - r.lse), p2 = expf(r.z2 - r.lse);
+  out[l] = __int_as_float(r.top1);
+  out[n + l] = p1;
+  out[2 * n + l] = p1 - p2;
+}
+
+cudaError_t launch_exit_features(const RowStats* st, int n, float* out, cudaStream_t s) {
+  exit_features_kernel<<<(n + 127) / 128, 128, 0, s>>>(st, n, out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_wait_selftest(const unsigned* never, int polls, int32_t* code, cudaStream_t s) {
   wait_selftest_kernel<<<1, 32, 0, s>>>(never, polls, code);
   return cudaGetLastError();

@@ -7,31 +7,43 @@
 // With hundreds of rows every weight tile is used by every token tile, so the
 // work is a dense contraction.
 //
-// CTA tile: 128 outputs (8 packed row groups; for SwiGLU 4 gate/up pairs,
-// virtual group 2p = gate, 2p + 1 = up) x NT tokens (NT <= 256, a multiple
-// of 16 chosen per launch so that the token tiles split T evenly).  The
-// accumulator lives in tensor memory: 128 lanes (outputs) x NT columns
-// (tokens) of fp32.
+// CTA tile: 128 outputs (8 packed row groups) x NT tokens (NT <= 256, a
+// multiple of 16 chosen per launch from a cost model of CTA rounds and bytes
+// streamed).  Accumulators live in tensor memory: 128 lanes (outputs) x NT
+// columns (tokens) of fp32, two of them side by side.  A SwiGLU tile holds
+// 128 features: the gate rows accumulate in columns [0, NT), the up rows of
+// the same features in [NT, 2 NT), so one thread sees both halves of its
+// feature.  Other tiles accumulate the even K16 steps of every K block in
+// [0, NT) and the odd ones in [NT, 2 NT) and add the two in the epilogue.
 //
-// Operands are staged in shared memory in the K-major 64-byte-swizzle
-// layout the MMA descriptors read: the weights' packed units already are in
-// that layout (an 8-row half of a unit is one 512-byte swizzle atom), so a
-// unit is copied as is; activation rows are placed chunk by chunk with the
-// same swizzle.  A stage holds 64 K columns; all 128 threads fill stages
-// with 16-byte cp.async copies, one thread issues the MMAs of a stage
-// (4 x K16) and commits them to the stage's mbarrier, which frees the stage
-// for the copies three stages ahead.  Every output sums its K in ascending
-// order in one accumulator, so the result depends on the shapes only.
+// Operands are staged in shared memory in the K-major 64-byte-swizzle layout
+// the MMA descriptors read.  Weights and activations are both stored in the
+// packed unit layout (16 rows x 32 columns; each 8-row half is one 512-byte
+// swizzle atom), which a tensor map views as a 3-D tensor (256 elements of a
+// half unit, half units along K, 16-row groups): one tiled TMA copy brings 8
+// row groups of one K block (8 KB), another the token tile's K block
+// (NT x 64 bytes), rows beyond the matrix zero-filled.  A stage holds two
+// 32-wide K blocks; thread 0 issues the copies (stage barrier `full`,
+// transaction bytes).  Two threads in different warps issue the MMAs, one
+// per accumulator: a single thread's issue rate (about 150 cycles per MMA,
+// measured) cannot keep the tensor core busy at N < 256.  Each commits its
+// MMAs of a stage to the stage's `empty` barrier (two arrivals free it for
+// the copies `stages` steps ahead), and last to `done`.  All loops advance
+// their slot and phase parity incrementally (no division in the issue
+// path).  Every accumulator sums its K steps in ascending order, so the
+// result depends on the shapes only.
 //
 // Epilogue: each warp reads its 32 TMEM lanes (tcgen05.ld, 16 columns at a
 // time): store fp32; residual add into the rows named by a row map; SwiGLU to
-// bf16 (gate and up rows exchanged across half-warps); per-token argmax
-// (largest value, lowest index) through a 64-bit atomic max of an
-// order-preserving key, independent of the order CTAs finish in.
+// bf16; per-token argmax (largest value, lowest index) through a 64-bit
+// atomic max of an order-preserving key, independent of the order CTAs
+// finish in.
 //
-// Waits are bounded: a stage barrier that never completes sets the error
-// word, and the CTA drains its own copies, frees its tensor memory and
+// Waits are bounded: a barrier that never completes sets the error word,
+// and the CTA waits (bounded) for its own copies, frees its tensor memory and
 // returns.
+#include <cuda.h>
+
 #include "kernels.cuh"
 
 namespace ssd {
@@ -40,22 +52,21 @@ namespace {
 
 constexpr int kTcM = 128;          // outputs per tile
 constexpr int kTcGroups = 8;       // 16-row groups per tile
+constexpr int kTcMaxStages = 16;
 constexpr int kTcKbs = 2;          // 32-wide K blocks per stage
-constexpr int kTcStages = 4;
 constexpr int kTcThreads = 128;
 constexpr int kTcMaxN = 256;
-constexpr int kTcABytes = kTcKbs * kTcGroups * 1024;   // weights of one stage
+constexpr int kTcSmemBudget = 216 * 1024;  // per SM, split among resident CTAs
 constexpr int kWaitPolls = 1 << 24;
 
-SSD_DI void cp16(void* dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
-               "r"(valid ? 16 : 0)
-               : "memory");
+// Tiled TMA load of a 3-D box at (c0, c1, c2), completing on `bar`.
+SSD_DI void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+      : "memory");
 }
-SSD_DI void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-SSD_DI void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-SSD_DI void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // ---- tcgen05 helpers
 SSD_DI void tmem_alloc(uint32_t* slot, uint32_t ncols) {
@@ -124,45 +135,87 @@ SSD_DI uint32_t order_key(float v) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+
 struct TcShape {
-  int NT;        // tokens per tile (multiple of 16, <= 256)
-  int tiles;     // token tiles
-  int ncols;     // tensor-memory columns allocated (power of 2, >= 32)
-  size_t smem;   // dynamic shared memory
+  int NT;          // tokens per tile (multiple of 16, <= 256)
+  int tiles;       // token tiles
+  int ncols;       // tensor-memory columns allocated (power of 2, >= 32)
+  int nacc;        // accumulators = MMA-issuing threads (1 or 2)
+  int stages;      // pipeline depth
+  int stage_bytes; // kTcKbs x (weights (8 KB, 16 KB for SwiGLU) + activations (NT x 64 B))
+  size_t smem;     // dynamic shared memory
 };
 
-TcShape tc_shape(int T) {
+// Token tiling: among the tile counts from the fewest the 256-column limit
+// allows up to tiles of 32 tokens, the one with the least (CTA rounds x
+// bytes a CTA streams per K block: its weights plus NT tokens).
+TcShape tc_shape(int T, bool swiglu, int m_tiles, int sms) {
   TcShape s;
-  s.tiles = (T + kTcMaxN - 1) / kTcMaxN;
-  const int per = (T + s.tiles - 1) / s.tiles;
-  s.NT = ((per + 15) / 16) * 16;
-  s.ncols = 32;
-  while (s.ncols < s.NT) s.ncols <<= 1;
-  const size_t stage = (size_t)kTcABytes + (size_t)kTcKbs * s.NT * 64;
-  s.smem = 1024 + kTcStages * stage + 256;
+  const int wcols = (swiglu ? 2 : 1) * 128;   // weight bytes per K block / 64
+  long best = -1;
+  for (int tiles = (T + kTcMaxN - 1) / kTcMaxN;; ++tiles) {
+    const int NT = ((T + tiles - 1) / tiles + 15) / 16 * 16;
+    const int n = (T + NT - 1) / NT;
+    const long cost = (long)((m_tiles * n + sms - 1) / sms) * (NT + wcols);
+    if (best < 0 || cost < best) {
+      best = cost;
+      s.NT = NT;
+      s.tiles = n;
+    }
+    if (NT <= 32) break;
+  }
+  // two accumulators (gate / up, or even / odd K16 steps) and two issuing
+  // threads, unless the second accumulator would keep a second CTA off an SM
+  // that the grid needs: issuing threads per SM are what count
+  auto pow2 = [](int c) { int n = 32; while (n < c) n <<= 1; return n; };
+  const int want = (m_tiles * s.tiles + sms - 1) / sms >= 2 ? 2 : 1;
+  s.nacc = (swiglu || want == 1 || pow2(2 * s.NT) <= 256) ? 2 : 1;
+  s.ncols = pow2(s.nacc * s.NT);
+  s.stage_bytes = kTcKbs * ((swiglu ? 2 : 1) * kTcGroups * 1024 + s.NT * 64);
+  // shared memory sized so that the whole grid is resident at once when it
+  // fits (up to 2 CTAs per SM; tensor memory allows 512 / ncols)
+  int per_sm = (m_tiles * s.tiles + sms - 1) / sms;
+  if (per_sm > 2) per_sm = 2;
+  if (per_sm > 512 / s.ncols) per_sm = 512 / s.ncols;
+  if (per_sm < 1) per_sm = 1;
+  s.stages = (kTcSmemBudget / per_sm) / s.stage_bytes;
+  if (s.stages > kTcMaxStages) s.stages = kTcMaxStages;
+  if (s.stages < 2) s.stages = 2;
+  s.smem = 1024 + (size_t)s.stages * s.stage_bytes + 512;
   return s;
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(GemmArgs a, int NT, int ncols) {
+__global__ void __launch_bounds__(kTcThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ CUtensorMap mW1,
+                   const __grid_constant__ CUtensorMap mAct, GemmArgs a, int NT, int ncols,
+                   int stages, int stage_bytes, int tx_kb, int nacc) {
   extern __shared__ unsigned char sm_raw[];
   // 1024-byte aligned stage area (the swizzle pattern repeats every 512 bytes
   // of the absolute shared-memory address)
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~(uintptr_t)1023);
-  const int stage_bytes = kTcABytes + kTcKbs * NT * 64;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kTcStages * stage_bytes);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + kTcStages);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + stages * stage_bytes);
+  uint64_t* empty = full + kTcMaxStages;
+  uint64_t* done = empty + kTcMaxStages;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 1);
+  int* fail = reinterpret_cast<int*>(tslot + 1);
+  int* issued = fail + 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int KB = a.K / 32;
-  const int nkb = (KB + kTcKbs - 1) / kTcKbs;                         // stages of K
   const bool swiglu = a.epi == GEMM_SWIGLU;
-  const int NRG = (swiglu ? 2 : 1) * (a.R / 16);
+  const int a_kb = (swiglu ? 2 : 1) * kTcGroups * 1024;   // weight bytes per K block
   const int rg0 = blockIdx.y * kTcGroups;
   const int t0 = blockIdx.x * NT;
 
   if (tid == 0) {
-    for (int s = 0; s < kTcStages; ++s) mbar_init(&bar[s], 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], nacc);   // one commit per MMA issuer
+    }
+    mbar_init(done, nacc);
+    *fail = 0;
+    *issued = 0;
+    fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tslot, (uint32_t)ncols);
   tc_fence_before();
@@ -170,84 +223,99 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(GemmArgs a, int 
   tc_fence_after();
   const uint32_t tmem = *tslot;
 
-  auto unit_src = [&](int v, int kb) -> const unsigned char* {
-    if (swiglu) {
-      const bf16* W = (v & 1) ? a.W1 : a.W0;
-      return reinterpret_cast<const unsigned char*>(W) + ((size_t)(v >> 1) * KB + kb) * 1024;
+  // A stage holds kTcKbs K blocks: weights [kbl][a_kb] then activations
+  // [kbl][NT x 64 B].  Slots and phase parities advance incrementally.
+  const int nst = (KB + kTcKbs - 1) / kTcKbs;
+  if (warp == 0 && lane == 0) {
+    // producer: per K block one box of 8 weight row groups (two for SwiGLU)
+    // and one box of the tile's tokens
+    int s = 0, st = 0;
+    uint32_t par = 0;
+    unsigned char* S = sm;
+    for (; s < nst; ++s) {
+      if (s >= stages && !mbar_wait_n(&empty[st], par ^ 1u, kWaitPolls)) {
+        atomicExch(fail, 1);
+        break;
+      }
+      const int kb0 = s * kTcKbs, nk = min(kTcKbs, KB - kb0);
+      mbar_arrive_expect_tx(&full[st], (uint32_t)(nk * tx_kb));
+      for (int kbl = 0; kbl < nk; ++kbl) {
+        unsigned char* A = S + kbl * a_kb;
+        const int c1 = 2 * (kb0 + kbl);
+        tma_load_3d(A, &mW0, 0, c1, rg0, &full[st]);
+        if (swiglu) tma_load_3d(A + kTcGroups * 1024, &mW1, 0, c1, rg0, &full[st]);
+        tma_load_3d(S + kTcKbs * a_kb + kbl * (NT * 64), &mAct, 0, c1, t0 / 16, &full[st]);
+      }
+      if (++st == stages) {
+        st = 0;
+        par ^= 1u;
+        S = sm;
+      } else {
+        S += stage_bytes;
+      }
     }
-    return reinterpret_cast<const unsigned char*>(a.W0) + ((size_t)v * KB + kb) * 1024;
-  };
-  // fill stage st with the K blocks of step s
-  auto load_stage = [&](int s, int st) {
-    unsigned char* A = sm + st * stage_bytes;
-    unsigned char* B = A + kTcABytes;
-    for (int e = tid; e < kTcKbs * kTcGroups * 64; e += kTcThreads) {
-      const int kbl = e / (kTcGroups * 64), rem = e % (kTcGroups * 64);
-      const int u = rem / 64, q = rem % 64;
-      const int kb = s * kTcKbs + kbl, v = rg0 + u;
-      const bool ok = kb < KB && v < NRG;
-      cp16(A + kbl * (kTcGroups * 1024) + u * 1024 + q * 16,
-           ok ? unit_src(v, kb) + q * 16 : reinterpret_cast<const unsigned char*>(a.W0), ok);
-    }
-    for (int e = tid; e < kTcKbs * NT * 4; e += kTcThreads) {
-      const int kbl = e / (NT * 4), rem = e % (NT * 4);
-      const int n = rem / 4, c = rem % 4;
-      const int kb = s * kTcKbs + kbl, t = t0 + n;
-      const bool ok = kb < KB && t < a.T;
-      const int r8 = n & 7;
-      cp16(B + kbl * (NT * 64) + (n >> 3) * 512 + r8 * 64 + ((c ^ ((r8 >> 1) & 3)) << 4),
-           ok ? a.act + (size_t)t * a.K + (size_t)kb * 32 + c * 8 : a.act, ok);
-    }
-  };
-
-  const uint32_t idesc = idesc_bf16(kTcM, NT);
-  bool ok = true;
-#pragma unroll
-  for (int s = 0; s < kTcStages - 1; ++s) {
-    if (s < nkb) load_stage(s, s);
-    cp_commit();
-  }
-  for (int s = 0; s < nkb; ++s) {
-    const int st = s % kTcStages;
-    cp_wait<kTcStages - 2>();
-    fence_async_smem();
-    ok = __syncthreads_and(ok) != 0;
-    if (!ok) break;
-    if (tid == 0) {
+    *issued = s;
+  } else if ((warp == 1 || (warp == 2 && nacc == 2)) && lane == 0) {
+    // two MMA issuers (one thread's issue rate alone cannot keep the tensor
+    // core busy), each into its own accumulator: SwiGLU issuer 0 the gate
+    // rows into columns [0, NT), issuer 1 the up rows into [NT, 2 NT); other
+    // epilogues: issuer i the K16 steps ks = i of every K block into columns
+    // [i NT, (i + 1) NT), the two partial sums added in the epilogue.
+    // Descriptors advance by adding the byte offset / 16 to the start field.
+    const int who = warp - 1;
+    const uint32_t idesc = idesc_bf16(kTcM, NT);
+    const uint64_t d0 = sw64_desc(smem_addr(sm));
+    const uint32_t dcol = tmem + (uint32_t)(who * NT);
+    const uint32_t wofs = swiglu && who ? (uint32_t)(kTcGroups * 1024 >> 4) : 0u;
+    int st = 0;
+    uint32_t par = 0, off = 0;
+    for (int s = 0; s < nst; ++s) {
+      if (!mbar_wait_n(&full[st], par, kWaitPolls)) {
+        atomicExch(fail, 1);
+        break;
+      }
       tc_fence_after();
-      const uint32_t A = smem_addr(sm + st * stage_bytes);
-      const uint32_t B = A + kTcABytes;
+      const int nk = min(kTcKbs, KB - s * kTcKbs);
 #pragma unroll
       for (int kbl = 0; kbl < kTcKbs; ++kbl) {
-        if (s * kTcKbs + kbl < KB) {
-#pragma unroll
-          for (int ks = 0; ks < 2; ++ks) {
-            const uint64_t ad = sw64_desc(A + kbl * (kTcGroups * 1024) + ks * 32);
-            const uint64_t bd = sw64_desc(B + kbl * (NT * 64) + ks * 32);
-            mma_bf16_tc(tmem, ad, bd, idesc, (s | kbl | ks) != 0);
+        if (kbl < nk) {
+          const uint64_t da = d0 + ((off + kbl * a_kb) >> 4) + wofs;
+          const uint64_t db = d0 + ((off + kTcKbs * a_kb + kbl * (NT * 64)) >> 4);
+          if (swiglu) {
+            mma_bf16_tc(dcol, da, db, idesc, (s | kbl) != 0);
+            mma_bf16_tc(dcol, da + 2, db + 2, idesc, 1u);
+          } else if (nacc == 2) {
+            mma_bf16_tc(dcol, da + 2 * who, db + 2 * who, idesc, (s | kbl) != 0);
+          } else {
+            mma_bf16_tc(dcol, da, db, idesc, (s | kbl) != 0);
+            mma_bf16_tc(dcol, da + 2, db + 2, idesc, 1u);
           }
         }
       }
-      mma_commit(&bar[st]);
+      mma_commit(&empty[st]);
+      if (++st == stages) {
+        st = 0;
+        par ^= 1u;
+        off = 0;
+      } else {
+        off += stage_bytes;
+      }
     }
-    // the stage refilled next was read by the MMAs of step s - 1
-    const int nxt = s + kTcStages - 1;
-    if (s >= 1 && nxt < nkb) {
-      const int ps = (s - 1) % kTcStages;
-      if (!mbar_wait_n(&bar[ps], (uint32_t)(((s - 1) / kTcStages) & 1), kWaitPolls)) ok = false;
-    }
-    if (ok && nxt < nkb) load_stage(nxt, nxt % kTcStages);
-    cp_commit();
+    // arrives once every MMA this thread issued has completed
+    mma_commit(done);
   }
-  // every MMA done (a commit tracks all MMAs issued before it)
-  if (ok) {
-    const int ls = (nkb - 1) % kTcStages;
-    if (!mbar_wait_n(&bar[ls], (uint32_t)(((nkb - 1) / kTcStages) & 1), kWaitPolls)) ok = false;
-  }
-  ok = __syncthreads_and(ok) != 0;
+  __syncwarp();
+  bool ok = mbar_wait_n(done, 0u, kWaitPolls);
+  __syncthreads();
+  ok = __syncthreads_and(ok && *reinterpret_cast<volatile int*>(fail) == 0) != 0;
   if (!ok) {
-    if (tid == 0 && a.err) atomicExch(a.err, 5);
-    cp_wait<0>();
+    if (tid == 0) {
+      if (a.err) atomicExch(a.err, 5);
+      // let this CTA's copies still in flight land before the memory is released
+      const int n = *issued;
+      for (int s = n - 1; s >= 0 && s >= n - stages; --s)  // stage steps issued last
+        mbar_wait_n(&full[s % stages], (uint32_t)((s / stages) & 1), 1 << 20);
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, (uint32_t)ncols);
@@ -257,17 +325,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(GemmArgs a, int 
 
   // ---- epilogue: warp w owns tile rows 32w .. 32w + 31 (TMEM lanes)
   const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-  const int vrow = rg0 * 16 + warp * 32 + lane;   // (virtual) output row
+  const int row = rg0 * 16 + warp * 32 + lane;   // output row (feature for SwiGLU)
+  const bool rv = row < a.R;
   for (int c0 = 0; c0 < NT; c0 += 16) {
     float v[16];
     tmem_ld16(trow + (uint32_t)c0, v);
+    if (!swiglu && nacc == 2) {
+      float v1[16];
+      tmem_ld16(trow + (uint32_t)(NT + c0), v1);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] += v1[j];
+    }
     if (a.epi == GEMM_ARGMAX) {
-      const bool rv = vrow < a.R;
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const int tok = t0 + c0 + j;
         float bv = rv ? v[j] : -INFINITY;
-        int bi = rv ? vrow : 0x7fffffff;
+        int bi = rv ? row : 0x7fffffff;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -279,29 +353,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(GemmArgs a, int 
                                       (unsigned long long)(0xffffffffu - (uint32_t)bi));
       }
     } else if (swiglu) {
-      // lanes 0-15: gate rows of pair p, lanes 16-31: the matching up rows
-      const int pair = (rg0 >> 1) + warp;
-      const bool pv = 2 * pair + 1 < NRG;
+      float up[16];
+      tmem_ld16(trow + (uint32_t)(NT + c0), up);
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        const float up = __shfl_xor_sync(0xffffffffu, v[j], 16);
         const int tok = t0 + c0 + j;
-        if (lane < 16 && pv && tok < a.T) {
+        if (rv && tok < a.T) {
           const float gt = v[j];
           const float sl = gt / (1.0f + expf(-gt));
-          a.u[(size_t)tok * a.R + pair * 16 + lane] = __float2bfloat16_rn(sl * up);
+          a.u[a.u_packed ? packed_off(tok, row, a.R) : (size_t)tok * a.R + row] =
+              __float2bfloat16_rn(sl * up[j]);
         }
       }
-    } else if (vrow < a.R) {
+    } else if (rv) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const int tok = t0 + c0 + j;
         if (tok < a.T) {
           if (a.epi == GEMM_STORE) {
-            a.y[(size_t)tok * a.R + vrow] = v[j];
+            a.y[(size_t)tok * a.R + row] = v[j];
           } else {
             const size_t orow = a.rowmap ? (size_t)a.rowmap[tok] : (size_t)tok;
-            a.x[orow * a.R + vrow] += v[j];
+            a.x[orow * a.R + row] += v[j];
           }
         }
       }
@@ -318,7 +391,65 @@ __global__ void argmax_index_kernel(const unsigned long long* best, int T, int32
   if (t < T) idx[t] = best[t] ? (int)(0xffffffffu - (uint32_t)(best[t] & 0xffffffffull)) : -1;
 }
 
+// dst (packed unit layout) = src [T][K] row-major; rows T .. 16-padded are zero.
+__global__ void pack_act_kernel(const bf16* src, int T, int K, bf16* dst) {
+  const int Tp = (T + 15) & ~15;
+  const size_t n = (size_t)Tp * K / 8;  // 16-byte chunks
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / (K / 8)), k = (int)(i % (K / 8)) * 8;
+    const uint4 v = t < T ? *reinterpret_cast<const uint4*>(src + (size_t)t * K + k)
+                          : make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(dst + packed_off(t, k, K)) = v;
+  }
+}
+
+// ---- host: tensor maps over the packed layout
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+  static EncodeTiled fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
+// A packed [groups * 16][K] bf16 matrix seen as (256 elements, 2 K / 32 half
+// units, groups); boxes of (256, 2, box_groups): one K block of box_groups
+// row groups, landing as consecutive 1 KB units.
+bool packed_map(CUtensorMap* m, const void* base, int K, int groups, int box_groups) {
+  EncodeTiled enc = encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {256, (cuuint64_t)(2 * (K / 32)), (cuuint64_t)groups};
+  const cuuint64_t strides[2] = {512, (cuuint64_t)(K / 32) * 1024};
+  const cuuint32_t box[3] = {256, 2, (cuuint32_t)box_groups};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
+
+cudaError_t launch_pack_act(const bf16* src, int T, int K, bf16* dst, cudaStream_t s) {
+  if (K % 32 || T <= 0) return cudaErrorInvalidValue;
+  pack_act_kernel<<<1216, 256, 0, s>>>(src, T, K, dst);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_argmax_index(const unsigned long long* best, int T, int32_t* idx,
                                 cudaStream_t s) {
@@ -328,7 +459,28 @@ cudaError_t launch_argmax_index(const unsigned long long* best, int T, int32_t* 
 
 cudaError_t launch_gemm_rows(const GemmArgs& a, cudaStream_t s) {
   if (a.R % 16 || a.K % 32 || a.T <= 0) return cudaErrorInvalidValue;
-  const TcShape sh = tc_shape(a.T);
+  const bool swiglu = a.epi == GEMM_SWIGLU;
+  if (((uintptr_t)a.W0 | (uintptr_t)a.act | (swiglu ? (uintptr_t)a.W1 : 0)) & 15)
+    return cudaErrorInvalidValue;
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+      sms = 1;
+  }
+  const int m_tiles = (a.R / 16 + kTcGroups - 1) / kTcGroups;
+  const TcShape sh = tc_shape(a.T, swiglu, m_tiles, sms);
+  // boxes no larger than the tensors; the bytes a stage receives
+  CUtensorMap m0, m1, mx;
+  const int groups = a.R / 16, tgroups = (a.T + 15) / 16;
+  const int wbox = groups < kTcGroups ? groups : kTcGroups;
+  const int xbox = tgroups < sh.NT / 16 ? tgroups : sh.NT / 16;
+  if (!packed_map(&m0, a.W0, a.K, groups, wbox) ||
+      !packed_map(&m1, swiglu ? a.W1 : a.W0, a.K, groups, wbox) ||
+      !packed_map(&mx, a.act, a.K, tgroups, xbox))
+    return cudaErrorInvalidValue;
+  const int tx = ((swiglu ? 2 : 1) * wbox + xbox) * 1024;
   static size_t smem_set = 0;
   if (sh.smem > smem_set) {
     const cudaError_t e = cudaFuncSetAttribute(
@@ -336,9 +488,9 @@ cudaError_t launch_gemm_rows(const GemmArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     smem_set = sh.smem;
   }
-  const int NRG = (a.epi == GEMM_SWIGLU ? 2 : 1) * (a.R / 16);
-  dim3 grid(sh.tiles, (NRG + kTcGroups - 1) / kTcGroups);
-  gemm_tc_kernel<<<grid, kTcThreads, sh.smem, s>>>(a, sh.NT, sh.ncols);
+  dim3 grid(sh.tiles, (groups + kTcGroups - 1) / kTcGroups);
+  gemm_tc_kernel<<<grid, kTcThreads, sh.smem, s>>>(m0, m1, mx, a, sh.NT, sh.ncols, sh.stages,
+                                                   sh.stage_bytes, tx, sh.nacc);
   return cudaGetLastError();
 }
 

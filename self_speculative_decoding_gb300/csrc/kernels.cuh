@@ -211,12 +211,13 @@ struct GemmArgs {
   const bf16* W0 = nullptr;
   const bf16* W1 = nullptr;
   int R = 0, K = 0, T = 0;
-  const bf16* act = nullptr;           // [T][K]
+  const bf16* act = nullptr;           // [T][K] in the packed unit layout (packed_off), T padded to 16
   int epi = GEMM_STORE;
   float* y = nullptr;                  // GEMM_STORE [T][R]
   float* x = nullptr;                  // GEMM_RESID: x[rowmap[t]][r] += out[t][r]
   const int32_t* rowmap = nullptr;     // nullable: identity
   bf16* u = nullptr;                   // GEMM_SWIGLU [T][R]: silu(gate) * up
+  int u_packed = 0;                    // 1: u in the packed unit layout
   unsigned long long* best = nullptr;  // GEMM_ARGMAX [T]: atomic max of (value, -index) keys, zero before
   int* err = nullptr;                  // set non-zero if a bounded wait gave up (nullable)
 };
@@ -235,18 +236,26 @@ struct ScoreAttnArgs {
   int N = 0, split = 0, max_seq = 0, H = 0, Hkv = 0, dh = 0;
   float scale_log2 = 0.f;     // log2(e) / sqrt(dh)
   bf16* out = nullptr;        // [T][H dh]
+  int out_packed = 0;         // 1: out in the packed unit layout (packed_off)
 };
 cudaError_t launch_score_attn(const ScoreAttnArgs& a, int n_active, cudaStream_t s);
 size_t score_attn_smem(int dh);
 cudaError_t launch_score_embed(const bf16* embed, const int32_t* tokens, int split, int N, int rows,
                                int D, float* x, cudaStream_t s);
+// out in the packed unit layout (packed_off)
 cudaError_t launch_score_norm(const float* x, const int32_t* map, const float* gain, float eps,
                               int T, int D, bf16* out, cudaStream_t s);
+// dst = src [T][K] row-major in the packed unit layout, rows T .. 16-padded zero
+cudaError_t launch_pack_act(const bf16* src, int T, int K, bf16* dst, cudaStream_t s);
 cudaError_t launch_score_rope(const float* qkv, int T, const int32_t* map, int N, int split, int H,
                               int Hkv, int dh, const float2* rope, bf16* q, bf16* sk, bf16* sv,
                               cudaStream_t s);
 cudaError_t launch_score_match(unsigned long long* best, const int32_t* tokens, int split, int N,
                                int rows, int32_t* counts, cudaStream_t s);
+
+// AdaInfer exit features of n exit-head row summaries: out [3][n] = top1
+// (int bits), top prob p1, gap p1 - p2.
+cudaError_t launch_exit_features(const RowStats* st, int n, float* out, cudaStream_t s);
 
 // Runs the device's bounded waits against conditions that never come true
 // (never[0] must be 0); *code gets bit 0 if the mbarrier wait gave up, bit 1

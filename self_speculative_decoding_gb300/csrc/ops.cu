@@ -325,6 +325,8 @@ ssd_status ssd_op_philox(const uint32_t* ctr, int32_t count, uint64_t key, uint3
 ssd_status ssd_op_linear_rows(const void* W, const void* W1, int32_t R, int32_t K,
                               const void* act, int32_t T, int32_t epi, void* out,
                               const int32_t* map, void* stream) {
+  const bool act_packed = (epi & SSD_ROWS_ACT_PACKED) != 0;
+  epi &= ~SSD_ROWS_ACT_PACKED;
   if (!al16(W) || (epi == GEMM_SWIGLU && !al16(W1)) || R <= 0 || R % 16 || K <= 0 || K % 32 ||
       T < 1 || !al16(act) || !al16(out) || epi < GEMM_STORE || epi > GEMM_ARGMAX)
     return op_fail(SSD_ERR_INVALID_ARG, "linear_rows arguments");
@@ -337,11 +339,20 @@ ssd_status ssd_op_linear_rows(const void* W, const void* W1, int32_t R, int32_t 
   a.T = T;
   a.act = (const bf16*)act;
   a.epi = epi;
-  Scratch best(s), err(s);
+  Scratch best(s), err(s), packed(s);
   ssd_status r;
   if ((r = cu(err.alloc(16), "scratch")) != SSD_OK) return r;
   if ((r = cu(cudaMemsetAsync(err.p, 0, 16, s), "memset")) != SSD_OK) return r;
   a.err = (int*)err.p;
+  // the projection reads its activations in the packed unit layout
+  if (!act_packed) {
+    const size_t Tp = ((size_t)T + 15) / 16 * 16;
+    if ((r = cu(packed.alloc(Tp * K * sizeof(bf16)), "scratch")) != SSD_OK) return r;
+    if ((r = cu(launch_pack_act((const bf16*)act, T, K, (bf16*)packed.p, s), "pack_act")) !=
+        SSD_OK)
+      return r;
+    a.act = (const bf16*)packed.p;
+  }
   if (epi == GEMM_STORE) a.y = (float*)out;
   if (epi == GEMM_RESID) {
     a.x = (float*)out;

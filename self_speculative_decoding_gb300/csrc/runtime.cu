@@ -102,13 +102,13 @@ struct ssd_ctx {
   // candidate-mask scoring: rows (candidate-major, up to max_score_rows) of
   // the batched forward, per-layer candidate lists and compact row maps
   float* sc_x = nullptr;          // [rows][D] residual stream
-  bf16* sc_xn = nullptr;          // [rows][D] normalised activations
+  bf16* sc_xn = nullptr;          // [rows][D] normalised activations (packed units)
   float* sc_qkv = nullptr;        // [rows][(H + 2 Hkv) dh]
   bf16* sc_q = nullptr;           // [rows][H dh] after RoPE
   bf16* sc_sk = nullptr;          // [rows][Hkv dh] window keys (RoPE applied)
   bf16* sc_sv = nullptr;          // [rows][Hkv dh] window values
-  bf16* sc_attn = nullptr;        // [rows][H dh]
-  bf16* sc_u = nullptr;           // [rows][FFN]
+  bf16* sc_attn = nullptr;        // [rows][H dh] (packed units)
+  bf16* sc_u = nullptr;           // [rows][FFN] (packed units)
   unsigned long long* sc_best = nullptr;  // [rows] argmax keys
   int32_t* sc_cand = nullptr;     // [L][256]
   int32_t* sc_map = nullptr;      // [L][rows]
@@ -121,6 +121,15 @@ struct ssd_ctx {
   int32_t* h_tok = nullptr;  // pinned staging [max_seq]
 
   Graph g_draft, g_extra, g_verify, g_accept, g_ar;
+  // lossy early-exit step: the AR step over the draft layer set only
+  Graph g_lossy;
+  // first position whose K/V a lossy step left incomplete (-1: none); the
+  // lossless entry points refuse to run until it is rewound or re-prefilled
+  int lossy_from = -1;
+  // per-layer exit-head summaries and features (ssd_layer_features)
+  RowStats* fstats = nullptr;
+  float* ffeat = nullptr;         // [3][L]: top1 (as int bits), p1, p1 - p2
+  float* h_ffeat = nullptr;
   // verify pass for rounds whose d + 1 rows do not fit the GEMV activation
   // stage (norm pre-pass + bf16 projections); g_verify covers the others
   Graph g_verify_wide;
@@ -719,6 +728,20 @@ ssd_status b_ar_body(ssd_ctx* c, cudaStream_t s) {
               "ar_end");
 }
 
+// LayerSkip blog §3, inference mode one: the pending token through the draft
+// layer set only, the shared head, and the AR step's commit.
+ssd_status b_lossy(ssd_ctx* c, cudaStream_t s) {
+  c->mmax = 1;
+  ssd_status r;
+  if ((r = enq_begin(c, BEGIN_AR, s)) == SSD_OK && (r = enq_layers(c, c->pre, s)) == SSD_OK &&
+      (r = enq_layers(c, c->post, s, &c->post_parts)) == SSD_OK &&
+      (r = enq_lmhead(c, c->vstats, nullptr, nullptr, 2, s)) == SSD_OK)
+    r = note(c, launch_ar_end(c->st, c->tokens, c->vstats, 0, c->pol.temperature, 0, s, c->pdl),
+             "ar_end");
+  c->mmax = 0;
+  return r;
+}
+
 ssd_status build_graphs_once(ssd_ctx* c) {
   ssd_status r;
   if ((r = build_graph(c, c->g_draft, b_draft)) != SSD_OK) return r;
@@ -729,6 +752,7 @@ ssd_status build_graphs_once(ssd_ctx* c) {
       (r = build_graph(c, c->g_verify_wide, b_verify_wide)) != SSD_OK)
     return r;
   if ((r = build_graph(c, c->g_accept, b_accept)) != SSD_OK) return r;
+  if ((r = build_graph(c, c->g_lossy, b_lossy)) != SSD_OK) return r;
   return build_graph(c, c->g_ar, b_ar);
 }
 
@@ -823,9 +847,14 @@ ssd_status run_verify(ssd_ctx* c, ssd_stats* stats) {
   return SSD_OK;
 }
 
-ssd_status ensure_policy(ssd_ctx* c) {
+ssd_status ensure_policy(ssd_ctx* c, bool lossless = true) {
   if (!c->has_policy) return fail(c, SSD_ERR_STATE, "no policy set (ssd_set_policy)");
   if (c->phase == PH_NONE) return fail(c, SSD_ERR_STATE, "no prefill");
+  if (lossless && c->lossy_from >= 0)
+    return fail(c, SSD_ERR_STATE,
+                "positions from " + std::to_string(c->lossy_from) +
+                    " were decoded lossily (skipped layers' K/V missing); rewind to <= " +
+                    std::to_string(c->lossy_from + 1) + " or prefill again");
   return SSD_OK;
 }
 
@@ -898,6 +927,7 @@ ssd_status enq_score(ssd_ctx* c, const uint64_t* masks, int K, int N, int split)
     at.dh = g.head_dim;
     at.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)g.head_dim));
     at.out = c->sc_attn;
+    at.out_packed = 1;
     if ((r = note(c, launch_score_attn(at, nact[l], s), "score_attn")) != SSD_OK) return r;
     GemmArgs o;
     o.W0 = (const bf16*)w.wo;
@@ -924,6 +954,7 @@ ssd_status enq_score(ssd_ctx* c, const uint64_t* masks, int K, int N, int split)
     gu.epi = GEMM_SWIGLU;
     gu.err = &c->st->err;
     gu.u = c->sc_u;
+    gu.u_packed = 1;
     if ((r = note(c, launch_gemm_rows(gu, s), "score_gate_up")) != SSD_OK) return r;
     GemmArgs dn;
     dn.W0 = (const bf16*)w.w_down;
@@ -1038,14 +1069,18 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
             alloc((void**)&c->vlogits, (size_t)nr * V * 4) &&
             alloc((void**)&c->tokens, (size_t)g.max_seq * 4) &&
             alloc((void**)&c->toks_in, (size_t)g.max_seq * 4) &&
-            alloc((void**)&c->st, sizeof(DevState));
+            alloc((void**)&c->st, sizeof(DevState)) &&
+            alloc((void**)&c->fstats, (size_t)g.n_layers * sizeof(RowStats)) &&
+            alloc((void**)&c->ffeat, (size_t)3 * g.n_layers * 4);
   if (ok && g.max_score_rows > 0) {
+    // rows of the projections' packed bf16 inputs are padded to 16
     const size_t r = (size_t)g.max_score_rows, D = g.d_model, HD = (size_t)g.n_heads * g.head_dim;
+    const size_t rp = (r + 15) / 16 * 16;
     const size_t KV = (size_t)g.n_kv_heads * g.head_dim;
-    ok = alloc((void**)&c->sc_x, r * D * 4) && alloc((void**)&c->sc_xn, r * D * 2) &&
+    ok = alloc((void**)&c->sc_x, r * D * 4) && alloc((void**)&c->sc_xn, rp * D * 2) &&
          alloc((void**)&c->sc_qkv, r * qkv_rows(g) * 4) && alloc((void**)&c->sc_q, r * HD * 2) &&
          alloc((void**)&c->sc_sk, r * KV * 2) && alloc((void**)&c->sc_sv, r * KV * 2) &&
-         alloc((void**)&c->sc_attn, r * HD * 2) && alloc((void**)&c->sc_u, r * g.ffn_dim * 2) &&
+         alloc((void**)&c->sc_attn, rp * HD * 2) && alloc((void**)&c->sc_u, rp * g.ffn_dim * 2) &&
          alloc((void**)&c->sc_best, r * 8) &&
          alloc((void**)&c->sc_cand, (size_t)g.n_layers * 256 * 4) &&
          alloc((void**)&c->sc_map, (size_t)g.n_layers * r * 4) &&
@@ -1060,6 +1095,7 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
     return SSD_ERR_OOM;
   }
   if (cudaMallocHost((void**)&c->h_st, sizeof(DevState)) != cudaSuccess ||
+      cudaMallocHost((void**)&c->h_ffeat, (size_t)3 * g.n_layers * 4) != cudaSuccess ||
       cudaMallocHost((void**)&c->h_tok, (size_t)g.max_seq * 4) != cudaSuccess ||
       cudaStreamCreateWithFlags(&c->cap, cudaStreamNonBlocking) != cudaSuccess ||
       cudaEventCreateWithFlags(&c->ev, cudaEventDisableTiming) != cudaSuccess ||
@@ -1105,13 +1141,14 @@ ssd_status ssd_destroy(ssd_ctx* c) {
   c->g_verify_wide.reset();
   c->g_accept.reset();
   c->g_ar.reset();
+  c->g_lossy.reset();
   c->p_draft.reset();
   c->p_extra.reset();
   c->p_verify.reset();
   c->p_ar.reset();
   void* bufs[] = {c->kc, c->vc, c->x, c->ss, c->bx, c->bss, c->qkv, c->attn, c->u, c->xn, c->rope,
                   c->attn_part, c->attn_cnt, c->g_part, c->g_cnt, c->g_rec, c->dstats, c->vstats,
-                  c->dlogits, c->vlogits, c->tokens, c->toks_in, c->st};
+                  c->dlogits, c->vlogits, c->tokens, c->toks_in, c->st, c->fstats, c->ffeat};
   for (void* p : bufs)
     if (p) cudaFree(p);
   void* sc[] = {c->sc_x,    c->sc_xn,   c->sc_qkv,  c->sc_q,   c->sc_sk,  c->sc_sv,
@@ -1122,6 +1159,7 @@ ssd_status ssd_destroy(ssd_ctx* c) {
   if (c->h_sc_cand) cudaFreeHost(c->h_sc_cand);
   if (c->h_sc_map) cudaFreeHost(c->h_sc_map);
   if (c->h_st) cudaFreeHost(c->h_st);
+  if (c->h_ffeat) cudaFreeHost(c->h_ffeat);
   if (c->h_tok) cudaFreeHost(c->h_tok);
   if (c->cap) cudaStreamDestroy(c->cap);
   if (c->ev) cudaEventDestroy(c->ev);
@@ -1206,6 +1244,7 @@ ssd_status ssd_prefill(ssd_ctx* c, const int32_t* tokens, int32_t n, int32_t* fi
   if ((r = read_state(c)) != SSD_OK) return r;
   if (first) *first = c->h_st->emitted[0];
   c->phase = PH_IDLE;
+  c->lossy_from = -1;
   return SSD_OK;
 }
 
@@ -1330,6 +1369,85 @@ ssd_status ssd_decode_ar(ssd_ctx* c, int32_t n_tokens, int32_t* out, ssd_stats* 
   return SSD_OK;
 }
 
+ssd_status ssd_decode_lossy(ssd_ctx* c, int32_t n_tokens, int32_t* out, ssd_stats* stats) {
+  if (!c || n_tokens < 0) return SSD_ERR_INVALID_ARG;
+  ssd_status r = ensure_policy(c, false);
+  if (r != SSD_OK) return r;
+  if (c->phase != PH_IDLE) return fail(c, SSD_ERR_STATE, "a round is in flight");
+  if (stats) memset(stats, 0, sizeof(*stats));
+  if ((r = read_state(c)) != SSD_OK) return r;
+  const int n0 = c->h_st->n;
+  if (n0 + n_tokens > c->cfg.max_seq) return fail(c, SSD_ERR_CAPACITY, "max_seq exceeded");
+  const int64_t l0 = c->launches;
+  Range nv("ssd decode_lossy");
+  if (stats) CK(cudaEventRecord(c->t0, c->stream));
+  for (int i = 0; i < n_tokens; ++i) {
+    if ((r = replay(c, c->g_lossy)) != SSD_OK) return r;
+    if (stats) stats->bytes_streamed += pass_bytes(c, (int)(c->pre.size() + c->post.size()), true,
+                                                   n0 - 1 + i, 1);
+  }
+  if (stats) CK(cudaEventRecord(c->t1, c->stream));
+  // a draft set that drops any sublayer leaves those layers' K/V unwritten
+  if (n_tokens > 0 && c->s0 < c->cfg.n_layers && c->lossy_from < 0) c->lossy_from = n0 - 1;
+  if (out && n_tokens > 0)
+    CK(cudaMemcpyAsync(c->h_tok, c->tokens + n0, (size_t)n_tokens * 4, cudaMemcpyDeviceToHost,
+                       c->stream));
+  if ((r = read_state(c)) != SSD_OK) return r;
+  if (out && n_tokens > 0) memcpy(out, c->h_tok, (size_t)n_tokens * 4);
+  if (stats) {
+    stats->rounds = n_tokens;
+    stats->emitted = n_tokens;
+    stats->kernel_launches = c->launches - l0;
+    float ms = 0.f;
+    if (n_tokens > 0) cudaEventElapsedTime(&ms, c->t0, c->t1);
+    stats->draft_ms = ms;
+  }
+  return SSD_OK;
+}
+
+ssd_status ssd_layer_features(ssd_ctx* c, int32_t min_layer, int32_t* top1, float* top_prob,
+                              float* gap) {
+  if (!c) return SSD_ERR_INVALID_ARG;
+  const int L = c->cfg.n_layers;
+  if (min_layer < 0 || min_layer >= L || !top1 || !top_prob || !gap)
+    return fail(c, SSD_ERR_INVALID_ARG, "layer_features arguments");
+  ssd_status r = ensure_policy(c);
+  if (r != SSD_OK) return r;
+  if (c->phase != PH_IDLE) return fail(c, SSD_ERR_STATE, "a round is in flight");
+  if ((r = read_state(c)) != SSD_OK) return r;
+  if (c->h_st->n + 1 > c->cfg.max_seq) return fail(c, SSD_ERR_CAPACITY, "max_seq exceeded");
+  Range nv("ssd layer_features");
+  cudaStream_t s = c->stream;
+  // one autoregressive step with the exit head after every layer >= min_layer
+  c->mmax = 1;
+  if ((r = enq_begin(c, BEGIN_AR, s)) != SSD_OK) { c->mmax = 0; return r; }
+  for (int l = 0; l < L && r == SSD_OK; ++l) {
+    r = enq_layer(c, l, s);
+    if (r == SSD_OK && l >= min_layer && l < L - 1)
+      r = enq_lmhead(c, c->fstats + l, nullptr, nullptr, -1, s);
+  }
+  if (r == SSD_OK) r = enq_lmhead(c, c->vstats, nullptr, nullptr, 2, s);
+  if (r == SSD_OK)
+    r = note(c, launch_ar_end(c->st, c->tokens, c->vstats, 0, c->pol.temperature, 0, s, c->pdl),
+             "ar_end");
+  c->mmax = 0;
+  if (r != SSD_OK) return r;
+  const int nl = L - min_layer;
+  CK(cudaMemcpyAsync(c->fstats + (L - 1), c->vstats, sizeof(RowStats), cudaMemcpyDeviceToDevice,
+                     s));
+  if ((r = note(c, launch_exit_features(c->fstats + min_layer, nl, c->ffeat, s),
+                "exit_features")) != SSD_OK)
+    return r;
+  CK(cudaMemcpyAsync(c->h_ffeat, c->ffeat, (size_t)3 * nl * 4, cudaMemcpyDeviceToHost, s));
+  if ((r = read_state(c)) != SSD_OK) return r;
+  for (int i = 0; i < nl; ++i) {
+    memcpy(&top1[i], &c->h_ffeat[i], 4);
+    top_prob[i] = c->h_ffeat[nl + i];
+    gap[i] = c->h_ffeat[2 * nl + i];
+  }
+  return SSD_OK;
+}
+
 ssd_status ssd_rewind(ssd_ctx* c, int32_t n) {
   if (!c) return SSD_ERR_INVALID_ARG;
   if (c->phase == PH_NONE) return fail(c, SSD_ERR_STATE, "no prefill");
@@ -1339,6 +1457,8 @@ ssd_status ssd_rewind(ssd_ctx* c, int32_t n) {
   DevState* hs = c->h_st;
   hs->n = n;
   hs->j = hs->d = hs->stop = 0;
+  // the next pass writes position n - 1 and on: incomplete K/V before it stay
+  if (c->lossy_from >= 0 && n - 1 <= c->lossy_from) c->lossy_from = -1;
   CK(cudaMemcpyAsync(c->st, hs, sizeof(DevState), cudaMemcpyHostToDevice, c->stream));
   c->phase = PH_IDLE;
   return wait_stream(c);

@@ -27,27 +27,38 @@ __global__ void score_embed_kernel(const bf16* embed, const int32_t* tokens, int
   }
 }
 
-// out[t] = bf16(rmsnorm(x[map[t]]) * gain): one warp per row; lane l sums
-// the squares of elements 2l, 2l + 1, 2l + 64, ... in that order, then a
-// butterfly over the warp.
+// out[t] = bf16(rmsnorm(x[map[t]]) * gain), written in the packed unit
+// layout the projections read.  One 256-thread block per row: thread i sums
+// the squares of the pairs (2i, 2i + 1), (2i + 512, 2i + 513), ... in that
+// order; the block reduces the 256 partial sums in a fixed tree (butterfly
+// within each warp, then warp 0 over the 8 warp sums).
 __global__ void __launch_bounds__(256) score_norm_kernel(const float* x, const int32_t* map,
                                                          const float* gain, float eps, int T,
                                                          int D, bf16* out) {
-  const int t = (blockIdx.x * 256 + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (t >= T) return;
+  __shared__ float wsum[8];
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float* xr = x + (size_t)(map ? map[t] : t) * D;
   float s = 0.f;
-  for (int k = 2 * lane; k < D; k += 64) {
+  for (int k = 2 * tid; k < D; k += 512) {
     const float2 v = *reinterpret_cast<const float2*>(xr + k);
     s += v.x * v.x;
     s += v.y * v.y;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  const float rs = 1.0f / sqrtf(s / (float)D + eps);
-  for (int k = 2 * lane; k < D; k += 64) {
+  if (lane == 0) wsum[warp] = s;
+  __syncthreads();
+  if (warp == 0) {
+    float w = lane < 8 ? wsum[lane] : 0.f;
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+    if (lane == 0) wsum[0] = w;
+  }
+  __syncthreads();
+  const float rs = 1.0f / sqrtf(wsum[0] / (float)D + eps);
+  for (int k = 2 * tid; k < D; k += 512) {
     const float2 v = *reinterpret_cast<const float2*>(xr + k);
-    *reinterpret_cast<uint32_t*>(out + (size_t)t * D + k) =
+    *reinterpret_cast<uint32_t*>(out + packed_off(t, k, D)) =
         pack_bf16x2(v.x * rs * gain[k], v.y * rs * gain[k + 1]);
   }
 }
@@ -277,13 +288,15 @@ __global__ void __launch_bounds__(128) score_attn_kernel(ScoreAttnArgs a) {
   }
   const int ia = i0 + g, ib = i0 + g + 8;
   const float inva = 1.0f / lrow[0], invb = 1.0f / lrow[1];
-  bf16* oa = a.out + (size_t)(ja * N + ia) * a.H * DH + (size_t)h * DH;
-  bf16* ob = a.out + (size_t)(ja * N + ib) * a.H * DH + (size_t)h * DH;
+  const int HD = a.H * DH;
+  const int ta = ja * N + ia, tb = ja * N + ib;
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
-    const int d = j * 8 + 2 * c;
-    if (ia < N) *reinterpret_cast<uint32_t*>(oa + d) = pack_bf16x2(o[j][0] * inva, o[j][1] * inva);
-    if (ib < N) *reinterpret_cast<uint32_t*>(ob + d) = pack_bf16x2(o[j][2] * invb, o[j][3] * invb);
+    const int d = h * DH + j * 8 + 2 * c;
+    const size_t offa = a.out_packed ? packed_off(ta, d, HD) : (size_t)ta * HD + d;
+    const size_t offb = a.out_packed ? packed_off(tb, d, HD) : (size_t)tb * HD + d;
+    if (ia < N) *reinterpret_cast<uint32_t*>(a.out + offa) = pack_bf16x2(o[j][0] * inva, o[j][1] * inva);
+    if (ib < N) *reinterpret_cast<uint32_t*>(a.out + offb) = pack_bf16x2(o[j][2] * invb, o[j][3] * invb);
   }
 }
 
@@ -310,7 +323,7 @@ cudaError_t launch_score_embed(const bf16* embed, const int32_t* tokens, int spl
 cudaError_t launch_score_norm(const float* x, const int32_t* map, const float* gain, float eps,
                               int T, int D, bf16* out, cudaStream_t s) {
   if (D % 64) return cudaErrorInvalidValue;
-  score_norm_kernel<<<(T * 32 + 255) / 256, 256, 0, s>>>(x, map, gain, eps, T, D, out);
+  score_norm_kernel<<<T, 256, 0, s>>>(x, map, gain, eps, T, D, out);
   return cudaGetLastError();
 }
 

@@ -8,7 +8,8 @@ kernel: rows processed, algorithmic bytes per launch (the weights, plus the
 K/V read for attention), mean microseconds per launch and GB/s.
 
     python -m self_speculative_decoding_gb300.kernel_bench \
-        [--kernel qkv,o_proj,gate_up,down,lm_head,attention] [--model 7b|13b|70b] \
+        [--kernel qkv,o_proj,gate_up,down,lm_head,attention,gate_up_rows,...]
+        [--model 7b|13b|70b] \
         [--rows M] [--iters N] [--context L] [--lib path/to/libssd.so]
 
 ``--lib`` times another build of the library (e.g. one compiled with a
@@ -35,6 +36,8 @@ MODELS = {
     "70b": (8192, 64, 8, 128, 28672, 32000),
 }
 KERNELS = ("qkv", "o_proj", "gate_up", "down", "lm_head", "attention")
+# many-row projections (tcgen05 GEMM) of the batched scoring forward
+ROW_KERNELS = ("qkv_rows", "o_proj_rows", "gate_up_rows", "down_rows", "lm_head_rows")
 
 
 def _packed(lib, R, K, n, st):
@@ -108,6 +111,32 @@ def bench_kernel(lib, name: str, model: str, M: int, iters: int, context: int) -
                                                        v.data_ptr(), max_seq, H, Hkv, dh,
                                                        C.c_float(1e4), out.data_ptr(), st)
                  for k, v in zip(kc, vc)]
+    elif name in ROW_KERNELS:
+        # activations pre-packed (rows padded to 16), as the scoring forward keeps them
+        K = {"o_proj_rows": H * dh, "down_rows": F}.get(name, D)
+        R = {"qkv_rows": (H + 2 * Hkv) * dh, "gate_up_rows": F, "lm_head_rows": V}.get(name, D)
+        epi = {"qkv_rows": 0, "o_proj_rows": 1, "down_rows": 1, "gate_up_rows": 2,
+               "lm_head_rows": 3}[name]
+        Tp = (M + 15) // 16 * 16
+        a_rm = (torch.randn(Tp, K, device="cuda") * 0.1).to(torch.bfloat16)
+        act = torch.empty_like(a_rm)
+        lib.ssd_pack_weight(a_rm.data_ptr(), act.data_ptr(), Tp, K, st)
+        nmat = 2 if epi == 2 else 1
+        n = _copies(nmat * R * K * 2)
+        Ws = _packed(lib, R, K, n, st)
+        W1 = _packed(lib, R, K, n, st) if epi == 2 else [None] * n
+        if epi == 2:
+            out = torch.empty(M, R, dtype=torch.bfloat16, device="cuda")
+        elif epi == 3:
+            out = torch.empty(M, dtype=torch.int32, device="cuda")
+        else:
+            out = torch.zeros(M, R, device="cuda")
+        nbytes = nmat * R * K * 2
+        flop = 2.0 * M * nmat * R * K
+        calls = [lambda W=W, U=U: lib.ssd_op_linear_rows(
+                     W.data_ptr(), U.data_ptr() if U is not None else None, R, K, act.data_ptr(),
+                     M, epi | 16, out.data_ptr(), None, st)
+                 for W, U in zip(Ws, W1)]
     else:
         raise ValueError(f"unknown kernel {name}")
     for i in range(3):
@@ -121,8 +150,11 @@ def bench_kernel(lib, name: str, model: str, M: int, iters: int, context: int) -
     e1.record()
     torch.cuda.synchronize()
     us = e0.elapsed_time(e1) * 1000.0 / iters
-    return {"kernel": name, "model": model, "rows": M, "bytes": nbytes, "us": round(us, 2),
-            "GBps": round(nbytes / us / 1e3, 1)}
+    r = {"kernel": name, "model": model, "rows": M, "bytes": nbytes, "us": round(us, 2),
+         "GBps": round(nbytes / us / 1e3, 1)}
+    if name in ROW_KERNELS:
+        r["TFLOPs"] = round(flop / us / 1e6, 1)
+    return r
 
 
 def main(argv=None):
