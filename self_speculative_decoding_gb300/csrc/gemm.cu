@@ -53,8 +53,7 @@ namespace {
 constexpr int kTcM = 128;          // outputs per tile
 constexpr int kTcGroups = 8;       // 16-row groups per tile
 constexpr int kTcMaxStages = 16;
-constexpr int kTcKbs = 2;          // 32-wide K blocks per stage
-constexpr int kTcThreads = 128;
+constexpr int kTcThreads = 160;    // warp 0: copies; warps 1-4: MMA issuers; warps 0-3: epilogue
 constexpr int kTcMaxN = 256;
 constexpr int kTcSmemBudget = 216 * 1024;  // per SM, split among resident CTAs
 constexpr int kWaitPolls = 1 << 24;
@@ -140,7 +139,8 @@ struct TcShape {
   int NT;          // tokens per tile (multiple of 16, <= 256)
   int tiles;       // token tiles
   int ncols;       // tensor-memory columns allocated (power of 2, >= 32)
-  int nacc;        // accumulators = MMA-issuing threads (1 or 2)
+  int nacc;        // accumulators = MMA-issuing threads (1, 2 or 4)
+  int kbs;         // 32-wide K blocks per stage (2 or 4)
   int stages;      // pipeline depth
   int stage_bytes; // kTcKbs x (weights (8 KB, 16 KB for SwiGLU) + activations (NT x 64 B))
   size_t smem;     // dynamic shared memory
@@ -169,15 +169,22 @@ TcShape tc_shape(int T, bool swiglu, int m_tiles, int sms) {
   // that the grid needs: issuing threads per SM are what count
   auto pow2 = [](int c) { int n = 32; while (n < c) n <<= 1; return n; };
   const int want = (m_tiles * s.tiles + sms - 1) / sms >= 2 ? 2 : 1;
-  s.nacc = (swiglu || want == 1 || pow2(2 * s.NT) <= 256) ? 2 : 1;
+  const int cap = want == 2 ? 256 : 512;      // columns that keep `want` CTAs per SM
+  if (pow2(4 * s.NT) <= cap) s.nacc = 4;
+  else if (swiglu || pow2(2 * s.NT) <= cap) s.nacc = 2;
+  else s.nacc = 1;
   s.ncols = pow2(s.nacc * s.NT);
-  s.stage_bytes = kTcKbs * ((swiglu ? 2 : 1) * kTcGroups * 1024 + s.NT * 64);
+  const int kb_bytes = (swiglu ? 2 : 1) * kTcGroups * 1024 + s.NT * 64;
   // shared memory sized so that the whole grid is resident at once when it
   // fits (up to 2 CTAs per SM; tensor memory allows 512 / ncols)
   int per_sm = (m_tiles * s.tiles + sms - 1) / sms;
   if (per_sm > 2) per_sm = 2;
   if (per_sm > 512 / s.ncols) per_sm = 512 / s.ncols;
   if (per_sm < 1) per_sm = 1;
+  // deeper stages (4 K blocks) amortise each issuer's per-stage barrier
+  // wait, fence and commit when at least 3 of them still fit
+  s.kbs = (kTcSmemBudget / per_sm) / (4 * kb_bytes) >= 3 ? 4 : 2;
+  s.stage_bytes = s.kbs * kb_bytes;
   s.stages = (kTcSmemBudget / per_sm) / s.stage_bytes;
   if (s.stages > kTcMaxStages) s.stages = kTcMaxStages;
   if (s.stages < 2) s.stages = 2;
@@ -188,7 +195,7 @@ TcShape tc_shape(int T, bool swiglu, int m_tiles, int sms) {
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ CUtensorMap mW1,
                    const __grid_constant__ CUtensorMap mAct, GemmArgs a, int NT, int ncols,
-                   int stages, int stage_bytes, int tx_kb, int nacc) {
+                   int stages, int stage_bytes, int tx_kb, int nacc, int kbs) {
   extern __shared__ unsigned char sm_raw[];
   // 1024-byte aligned stage area (the swizzle pattern repeats every 512 bytes
   // of the absolute shared-memory address)
@@ -223,9 +230,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tslot;
 
-  // A stage holds kTcKbs K blocks: weights [kbl][a_kb] then activations
+  // A stage holds kbs K blocks: weights [kbl][a_kb] then activations
   // [kbl][NT x 64 B].  Slots and phase parities advance incrementally.
-  const int nst = (KB + kTcKbs - 1) / kTcKbs;
+  const int nst = (KB + kbs - 1) / kbs;
   if (warp == 0 && lane == 0) {
     // producer: per K block one box of 8 weight row groups (two for SwiGLU)
     // and one box of the tile's tokens
@@ -237,14 +244,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         atomicExch(fail, 1);
         break;
       }
-      const int kb0 = s * kTcKbs, nk = min(kTcKbs, KB - kb0);
+      const int kb0 = s * kbs, nk = min(kbs, KB - kb0);
       mbar_arrive_expect_tx(&full[st], (uint32_t)(nk * tx_kb));
       for (int kbl = 0; kbl < nk; ++kbl) {
         unsigned char* A = S + kbl * a_kb;
         const int c1 = 2 * (kb0 + kbl);
         tma_load_3d(A, &mW0, 0, c1, rg0, &full[st]);
         if (swiglu) tma_load_3d(A + kTcGroups * 1024, &mW1, 0, c1, rg0, &full[st]);
-        tma_load_3d(S + kTcKbs * a_kb + kbl * (NT * 64), &mAct, 0, c1, t0 / 16, &full[st]);
+        tma_load_3d(S + kbs * a_kb + kbl * (NT * 64), &mAct, 0, c1, t0 / 16, &full[st]);
       }
       if (++st == stages) {
         st = 0;
@@ -255,18 +262,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
     *issued = s;
-  } else if ((warp == 1 || (warp == 2 && nacc == 2)) && lane == 0) {
-    // two MMA issuers (one thread's issue rate alone cannot keep the tensor
-    // core busy), each into its own accumulator: SwiGLU issuer 0 the gate
-    // rows into columns [0, NT), issuer 1 the up rows into [NT, 2 NT); other
-    // epilogues: issuer i the K16 steps ks = i of every K block into columns
-    // [i NT, (i + 1) NT), the two partial sums added in the epilogue.
-    // Descriptors advance by adding the byte offset / 16 to the start field.
+  } else if (warp >= 1 && warp <= nacc && lane == 0) {
+    // MMA issuers (one thread's issue rate alone cannot keep the tensor core
+    // busy), each into its own accumulator of NT columns: the K16 steps j
+    // of a stage (j = 2 kbl + ks) are dealt to the `per` issuers of a matrix
+    // by j mod per; for SwiGLU issuers 0 .. per-1 take the gate rows and
+    // per .. 2 per-1 the up rows.  Descriptors advance by adding the byte
+    // offset / 16 to the start field.
     const int who = warp - 1;
+    const int per = swiglu ? nacc / 2 : nacc;
+    const int r = who % per;
     const uint32_t idesc = idesc_bf16(kTcM, NT);
     const uint64_t d0 = sw64_desc(smem_addr(sm));
     const uint32_t dcol = tmem + (uint32_t)(who * NT);
-    const uint32_t wofs = swiglu && who ? (uint32_t)(kTcGroups * 1024 >> 4) : 0u;
+    const uint32_t wofs = swiglu && who >= per ? (uint32_t)(kTcGroups * 1024 >> 4) : 0u;
     int st = 0;
     uint32_t par = 0, off = 0;
     for (int s = 0; s < nst; ++s) {
@@ -275,22 +284,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc_fence_after();
-      const int nk = min(kTcKbs, KB - s * kTcKbs);
-#pragma unroll
-      for (int kbl = 0; kbl < kTcKbs; ++kbl) {
-        if (kbl < nk) {
-          const uint64_t da = d0 + ((off + kbl * a_kb) >> 4) + wofs;
-          const uint64_t db = d0 + ((off + kTcKbs * a_kb + kbl * (NT * 64)) >> 4);
-          if (swiglu) {
-            mma_bf16_tc(dcol, da, db, idesc, (s | kbl) != 0);
-            mma_bf16_tc(dcol, da + 2, db + 2, idesc, 1u);
-          } else if (nacc == 2) {
-            mma_bf16_tc(dcol, da + 2 * who, db + 2 * who, idesc, (s | kbl) != 0);
-          } else {
-            mma_bf16_tc(dcol, da, db, idesc, (s | kbl) != 0);
-            mma_bf16_tc(dcol, da + 2, db + 2, idesc, 1u);
-          }
-        }
+      const int nj = 2 * min(kbs, KB - s * kbs);
+      for (int j = r; j < nj; j += per) {
+        const int kbl = j >> 1, ks = j & 1;
+        const uint64_t da = d0 + ((off + kbl * a_kb) >> 4) + wofs + 2 * ks;
+        const uint64_t db = d0 + ((off + kbs * a_kb + kbl * (NT * 64)) >> 4) + 2 * ks;
+        mma_bf16_tc(dcol, da, db, idesc, (s != 0 || j != r) ? 1u : 0u);
       }
       mma_commit(&empty[st]);
       if (++st == stages) {
@@ -323,16 +322,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   tc_fence_after();
 
-  // ---- epilogue: warp w owns tile rows 32w .. 32w + 31 (TMEM lanes)
+  // ---- epilogue: warp w < 4 owns tile rows 32w .. 32w + 31 (TMEM lanes).
+  // A matrix's value is the sum of its issuers' accumulators in issuer
+  // order; an issuer that received no K16 step (2 KB < per) holds nothing.
+  if (warp >= 4) {
+    tc_fence_before();
+    __syncthreads();
+    return;
+  }
+  const int per = swiglu ? nacc / 2 : nacc;
+  const int nsum = min(per, 2 * KB);
   const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
   const int row = rg0 * 16 + warp * 32 + lane;   // output row (feature for SwiGLU)
   const bool rv = row < a.R;
   for (int c0 = 0; c0 < NT; c0 += 16) {
     float v[16];
     tmem_ld16(trow + (uint32_t)c0, v);
-    if (!swiglu && nacc == 2) {
+    for (int q = 1; q < nsum; ++q) {
       float v1[16];
-      tmem_ld16(trow + (uint32_t)(NT + c0), v1);
+      tmem_ld16(trow + (uint32_t)(q * NT + c0), v1);
 #pragma unroll
       for (int j = 0; j < 16; ++j) v[j] += v1[j];
     }
@@ -354,7 +362,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     } else if (swiglu) {
       float up[16];
-      tmem_ld16(trow + (uint32_t)(NT + c0), up);
+      tmem_ld16(trow + (uint32_t)(per * NT + c0), up);
+      for (int q = 1; q < nsum; ++q) {
+        float v1[16];
+        tmem_ld16(trow + (uint32_t)((per + q) * NT + c0), v1);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) up[j] += v1[j];
+      }
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const int tok = t0 + c0 + j;
@@ -490,7 +504,7 @@ cudaError_t launch_gemm_rows(const GemmArgs& a, cudaStream_t s) {
   }
   dim3 grid(sh.tiles, (groups + kTcGroups - 1) / kTcGroups);
   gemm_tc_kernel<<<grid, kTcThreads, sh.smem, s>>>(m0, m1, mx, a, sh.NT, sh.ncols, sh.stages,
-                                                   sh.stage_bytes, tx, sh.nacc);
+                                                   sh.stage_bytes, tx, sh.nacc, sh.kbs);
   return cudaGetLastError();
 }
 
