@@ -10,11 +10,12 @@
 // CTA tile: 128 outputs (8 packed row groups) x NT tokens (NT <= 256, a
 // multiple of 16 chosen per launch from a cost model of CTA rounds and bytes
 // streamed).  Accumulators live in tensor memory: 128 lanes (outputs) x NT
-// columns (tokens) of fp32, two of them side by side.  A SwiGLU tile holds
-// 128 features: the gate rows accumulate in columns [0, NT), the up rows of
-// the same features in [NT, 2 NT), so one thread sees both halves of its
-// feature.  Other tiles accumulate the even K16 steps of every K block in
-// [0, NT) and the odd ones in [NT, 2 NT) and add the two in the epilogue.
+// columns (tokens) of fp32, up to four side by side, their number fixed by
+// the matrix (not by T).  A SwiGLU tile holds 128 features: the gate rows
+// accumulate in columns [0, NT), the up rows of the same features in
+// [NT, 2 NT), so one thread sees both halves of its feature.  Other tiles use
+// one accumulator, or four that take the K16 steps j of every stage by
+// j mod 4 and are added in order in the epilogue.
 //
 // Operands are staged in shared memory in the K-major 64-byte-swizzle layout
 // the MMA descriptors read.  Weights and activations are both stored in the
@@ -24,11 +25,11 @@
 // row groups of one K block (8 KB), another the token tile's K block
 // (NT x 64 bytes), rows beyond the matrix zero-filled.  A stage holds two
 // 32-wide K blocks; thread 0 issues the copies (stage barrier `full`,
-// transaction bytes).  Two threads in different warps issue the MMAs, one
-// per accumulator: a single thread's issue rate (about 150 cycles per MMA,
+// transaction bytes).  One thread per accumulator, each in its own warp,
+// issues the MMAs: a single thread's issue rate (about 150 cycles per MMA,
 // measured) cannot keep the tensor core busy at N < 256.  Each commits its
-// MMAs of a stage to the stage's `empty` barrier (two arrivals free it for
-// the copies `stages` steps ahead), and last to `done`.  All loops advance
+// MMAs of a stage to the stage's `empty` barrier (one arrival per issuer
+// frees it for the copies `stages` steps ahead), and last to `done`.  All loops advance
 // their slot and phase parity incrementally (no division in the issue
 // path).  Every accumulator sums its K steps in ascending order, so the
 // result depends on the shapes only.
@@ -55,6 +56,7 @@ constexpr int kTcGroups = 8;       // 16-row groups per tile
 constexpr int kTcMaxStages = 16;
 constexpr int kTcThreads = 160;    // warp 0: copies; warps 1-4: MMA issuers; warps 0-3: epilogue
 constexpr int kTcMaxN = 256;
+constexpr int kTcManyTiles = 100;  // 128-row tiles from which a matrix uses one accumulator
 constexpr int kTcSmemBudget = 216 * 1024;  // per SM, split among resident CTAs
 constexpr int kWaitPolls = 1 << 24;
 
@@ -146,14 +148,22 @@ struct TcShape {
   size_t smem;     // dynamic shared memory
 };
 
-// Token tiling: among the tile counts from the fewest the 256-column limit
+// Accumulators (= MMA-issuing threads) depend on the matrix only, never on
+// T, so that a row's bits do not depend on how many rows are processed
+// together: SwiGLU 2 (gate, up); matrices with few 128-row tiles 4 (the K16
+// steps dealt by j mod 4; tiles of at most 128 tokens keep 4 accumulators in
+// tensor memory); matrices with many tiles 1 (their grids want two CTAs per
+// SM, which one accumulator of up to 256 columns allows).
+// Token tiling: among the tile counts from the fewest the column limit
 // allows up to tiles of 32 tokens, the one with the least (CTA rounds x
 // bytes a CTA streams per K block: its weights plus NT tokens).
 TcShape tc_shape(int T, bool swiglu, int m_tiles, int sms) {
   TcShape s;
+  s.nacc = swiglu ? 2 : (m_tiles < kTcManyTiles ? 4 : 1);
+  const int max_n = s.nacc == 4 ? 128 : kTcMaxN;
   const int wcols = (swiglu ? 2 : 1) * 128;   // weight bytes per K block / 64
   long best = -1;
-  for (int tiles = (T + kTcMaxN - 1) / kTcMaxN;; ++tiles) {
+  for (int tiles = (T + max_n - 1) / max_n;; ++tiles) {
     const int NT = ((T + tiles - 1) / tiles + 15) / 16 * 16;
     const int n = (T + NT - 1) / NT;
     const long cost = (long)((m_tiles * n + sms - 1) / sms) * (NT + wcols);
@@ -164,15 +174,7 @@ TcShape tc_shape(int T, bool swiglu, int m_tiles, int sms) {
     }
     if (NT <= 32) break;
   }
-  // two accumulators (gate / up, or even / odd K16 steps) and two issuing
-  // threads, unless the second accumulator would keep a second CTA off an SM
-  // that the grid needs: issuing threads per SM are what count
   auto pow2 = [](int c) { int n = 32; while (n < c) n <<= 1; return n; };
-  const int want = (m_tiles * s.tiles + sms - 1) / sms >= 2 ? 2 : 1;
-  const int cap = want == 2 ? 256 : 512;      // columns that keep `want` CTAs per SM
-  if (pow2(4 * s.NT) <= cap) s.nacc = 4;
-  else if (swiglu || pow2(2 * s.NT) <= cap) s.nacc = 2;
-  else s.nacc = 1;
   s.ncols = pow2(s.nacc * s.NT);
   const int kb_bytes = (swiglu ? 2 : 1) * kTcGroups * 1024 + s.NT * 64;
   // shared memory sized so that the whole grid is resident at once when it

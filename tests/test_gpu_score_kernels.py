@@ -7,7 +7,7 @@ through the C-ABI (ssd_op_linear_rows, ssd_op_score_attention).
   (exact wherever the top-2 gap exceeds 1e-3).  Sizes span several row and
   output tiles with ragged tails.
 * A row's result does not depend on how many rows are processed together
-  (bit for bit).
+  (bit for bit), across token-tile widths from 16 to 256 columns.
 * The window attention equals oracle.ops.score_attention within bf16
   rounding of its operands (P and the output are bf16).
 """
@@ -94,15 +94,17 @@ def test_rows_argmax(ops, V, K, T):
             assert z[t][idx[t]] >= s[-1] - 1e-3
 
 
-def test_rows_count_invariance(ops):
-    R, K = 528, 704
+@pytest.mark.parametrize("R,K", [(528, 704), (1600, 512), (16384, 256)])
+def test_rows_count_invariance(ops, R, K):
+    # token tiles of different widths (16 .. 256 columns) for different T; the
+    # number of accumulators depends on the matrix only
     W, _ = rand_bf16((R, K), seed=11)
     Wp = P(W)
-    act, _ = rand_bf16((300, K), seed=12, std=1.0)
+    act, _ = rand_bf16((513, K), seed=12, std=1.0)
     full = ops.linear_rows(Wp, act)
-    for T in (1, 17, 128, 129, 257):
+    for T in (1, 17, 128, 129, 257, 300):
         part = ops.linear_rows(Wp, act[:T].contiguous())
-        assert torch.equal(part, full[:T])
+        assert torch.equal(part, full[:T]), T
     one = ops.linear_rows(Wp, act[200:201].contiguous())
     assert torch.equal(one[0], full[200])
 
