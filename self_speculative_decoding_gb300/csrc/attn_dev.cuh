@@ -24,13 +24,12 @@ namespace attn {
 
 constexpr int kGroupThreads = 256;  // threads that execute an item
 constexpr int kGroupWarps = kGroupThreads / 32;
-constexpr int kKPad = 8;            // bf16 padding per cached key row
 // A chunk's partial record per (head, row): max score, sum of exponentials,
 // two pad words, then the unnormalised output (16-byte aligned).
 constexpr int kRecPad = 4;
 
 // Shared memory of one item (offsets multiples of 16 B):
-//   K [64][dh + 8] bf16 | V [64][dh] bf16 | Q [16][dh] f32 | S [16][64] f32
+//   K [64][dh] bf16 | V [64][dh] bf16 | Q [16][dh] f32 | S [16][64] f32
 //   | combine scratch: m, l, w [nchunk] f32
 struct Smem {
   bf16* K;
@@ -43,14 +42,14 @@ struct Smem {
 };
 
 __host__ __device__ inline size_t smem_bytes(int dh, int nchunk) {
-  return (size_t)kAttnChunk * (dh + kKPad) * 2 + (size_t)kAttnChunk * dh * 2 +
+  return (size_t)kAttnChunk * dh * 2 + (size_t)kAttnChunk * dh * 2 +
          (size_t)kMaxRows * dh * 4 + (size_t)kMaxRows * kAttnChunk * 4 + (size_t)3 * nchunk * 4;
 }
 
 SSD_DI Smem carve(unsigned char* raw, int dh, int nchunk) {
   Smem sm;
   sm.K = reinterpret_cast<bf16*>(raw);
-  sm.V = sm.K + kAttnChunk * (dh + kKPad);
+  sm.V = sm.K + kAttnChunk * dh;
   sm.Q = reinterpret_cast<float*>(sm.V + kAttnChunk * dh);
   sm.S = sm.Q + kMaxRows * dh;
   sm.cm = sm.S + kMaxRows * kAttnChunk;
@@ -65,29 +64,23 @@ SSD_DI const bf16* cache_row(const bf16* c, const AttnArgs& a, int kvh, int pos)
 }
 
 // Step (1) of work item `item`: the bulk copies of the chunk's cached keys
-// and values (positions before pos0), issued by warp 0 (one copy per padded
-// K row; the V rows in one copy) and
-// completing on `bar`.  The cache rows before pos0 were written by earlier
+// and values (positions before pos0): one copy each for the K rows and the V
+// rows (consecutive positions are contiguous in the cache), issued by one
+// thread and completing on `bar`.  The cache rows before pos0 were written by earlier
 // passes, so this may run before the wait on the preceding kernel.
 SSD_DI void issue(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, uint64_t* bar,
                   int tid) {
-  const int dh = a.dh, krs = dh + kKPad;
-  const int warp = tid >> 5, lane = tid & 31;
+  const int dh = a.dh;
   const int c = item / a.Hkv, kvh = item % a.Hkv;
   const int p_begin = c * kAttnChunk;
   const int p_end = min(p_begin + kAttnChunk, pos0 + M);
   const int n_old = max(0, min(p_end, pos0) - p_begin);
-  if (n_old > 0 && warp == 0) {
-    if (lane == 0) {
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(bar, (uint32_t)(2 * n_old * dh * sizeof(bf16)));
-      bulk_g2s(sm.V, cache_row(a.vc, a, kvh, p_begin), (uint32_t)(n_old * dh * sizeof(bf16)),
-               bar);
-    }
-    __syncwarp();
-    for (int j = lane; j < n_old; j += 32)
-      bulk_g2s(sm.K + (size_t)j * krs, cache_row(a.kc, a, kvh, p_begin + j),
-               (uint32_t)(dh * sizeof(bf16)), bar);
+  if (n_old > 0 && tid == 0) {
+    const uint32_t bytes = (uint32_t)(n_old * dh * sizeof(bf16));
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar, 2 * bytes);
+    bulk_g2s(sm.K, cache_row(a.kc, a, kvh, p_begin), bytes, bar);
+    bulk_g2s(sm.V, cache_row(a.vc, a, kvh, p_begin), bytes, bar);
   }
 }
 
@@ -99,7 +92,7 @@ SSD_DI void issue(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, 
 template <class Sync>
 SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, uint64_t* bar,
                  uint32_t& phase, int* flag, int tid, Sync sync) {
-  const int dh = a.dh, half = dh / 2, krs = dh + kKPad;
+  const int dh = a.dh, half = dh / 2;
   const int G = a.H / a.Hkv;
   const int rows = G * kMaxRows;
   const int nchunk_max = a.max_seq / kAttnChunk;
@@ -126,8 +119,8 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
     const bf16 kb1 = __float2bfloat16_rn(k0 * cs.y + k1 * cs.x);
     const bf16 vb0 = __float2bfloat16_rn(__ldcg(vr + i));
     const bf16 vb1 = __float2bfloat16_rn(__ldcg(vr + i + half));
-    sm.K[j * krs + i] = kb0;
-    sm.K[j * krs + i + half] = kb1;
+    sm.K[j * dh + i] = kb0;
+    sm.K[j * dh + i + half] = kb1;
     sm.V[j * dh + i] = vb0;
     sm.V[j * dh + i + half] = vb1;
     bf16* kd = const_cast<bf16*>(cache_row(a.kc, a, kvh, pos));
@@ -159,18 +152,18 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
       qd[i + half] = q0 * cs.y + q1 * cs.x;
     }
     sync();
-    // (4) scores: 4 lanes per (row, key), each lane a quarter of the head
-    // dimension in 8-wide pieces, then a 2-step butterfly (fixed order)
-    const int qd = dh / 4;
-    for (int u = tid; u < M * kAttnChunk * 4; u += kGroupThreads) {
-      const int qt = u & 3, key = (u >> 2) & (kAttnChunk - 1), m = u >> 8;
+    // (4) scores: 8 lanes per (row, key); lane q8 takes the 8-element chunks
+    // q8, q8 + 8, ... of the head dimension, so one warp instruction reads 4
+    // key rows of 128 contiguous bytes (no bank conflict without row
+    // padding); then a 3-step butterfly (fixed order)
+    for (int u = tid; u < M * kAttnChunk * 8; u += kGroupThreads) {
+      const int q8 = u & 7, key = (u >> 3) & (kAttnChunk - 1), m = u >> 9;
       const bool valid = key < nk && p_begin + key <= pos0 + m;
       float acc = 0.f;
       if (valid) {
         const float* q = sm.Q + (size_t)m * dh;
-        const bf16* k = sm.K + (size_t)key * krs;
-        for (int t = 0; t < qd; t += 8) {
-          const int d0 = t * 4 + qt * 8;
+        const bf16* k = sm.K + (size_t)key * dh;
+        for (int d0 = q8 * 8; d0 < dh; d0 += 64) {
           const uint4 kk = *reinterpret_cast<const uint4*>(k + d0);
           const float4 qa = *reinterpret_cast<const float4*>(q + d0);
           const float4 qb = *reinterpret_cast<const float4*>(q + d0 + 4);
@@ -186,7 +179,8 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
       }
       acc += __shfl_xor_sync(0xffffffffu, acc, 1);
       acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-      if (qt == 0) sm.S[(size_t)m * kAttnChunk + key] = valid ? acc * a.scale : -INFINITY;
+      acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+      if (q8 == 0) sm.S[(size_t)m * kAttnChunk + key] = valid ? acc * a.scale : -INFINITY;
     }
     sync();
     // (5) per-row chunk softmax statistics; one warp per row

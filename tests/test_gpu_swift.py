@@ -104,8 +104,19 @@ def test_swift_lockstep_with_oracle(ssd):
     assert [s.best for s in tr.steps] == g_best
     assert tr.stopped_by == rep["stopped_by"]
     assert tuple(tr.final) == rep["final"]
-    # greedy tokens agree until the oracle's first near-tie, if there is one
-    assert st.tokens[len(prompt) + 1:][:len(toks)][:20] == toks[:20]
+    # greedy tokens (SWIFT is lossless: the model's greedy tokens) agree with
+    # the oracle's autoregressive tokens until the oracle's first near-tie
+    from oracle import ar_step
+    ost = prefill(m, prompt, pol, 256)
+    gpu = ctx.tokens()[len(prompt):]
+    assert ost.tokens[-1] == gpu[0] or _near_tie(ost.last_logits)
+    for i in range(1, min(20, len(gpu))):
+        if ost.tokens[-1] != gpu[i - 1]:
+            break
+        z = ar_step(m, ost, pol)
+        if _near_tie(z):
+            break
+        assert ost.tokens[-1] == gpu[i], i
     ctx.close()
 
 
