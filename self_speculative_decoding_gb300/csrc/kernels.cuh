@@ -250,8 +250,9 @@ cudaError_t launch_pack_act(const bf16* src, int T, int K, bf16* dst, cudaStream
 cudaError_t launch_score_rope(const float* qkv, int T, const int32_t* map, int N, int split, int H,
                               int Hkv, int dh, const float2* rope, bf16* q, bf16* sk, bf16* sv,
                               cudaStream_t s);
-cudaError_t launch_score_match(unsigned long long* best, const int32_t* tokens, int split, int N,
-                               int rows, int32_t* counts, cudaStream_t s);
+// compact rows t < T of physical rows map[t] (nullable: identity)
+cudaError_t launch_score_match(unsigned long long* best, const int32_t* map, const int32_t* tokens,
+                               int split, int N, int T, int32_t* counts, cudaStream_t s);
 
 // AdaInfer exit features of n exit-head row summaries: out [3][n] = top1
 // (int bits), top prob p1, gap p1 - p2.

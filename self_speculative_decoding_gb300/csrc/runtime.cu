@@ -116,6 +116,7 @@ struct ssd_ctx {
   int32_t* h_sc_map = nullptr;
   int32_t* sc_counts = nullptr;
   int32_t* h_counts = nullptr;
+  std::vector<int> sc_owner;      // per candidate of the last call: the row block it shares
   DevState* st = nullptr;
   DevState* h_st = nullptr;  // pinned mirror
   int32_t* h_tok = nullptr;  // pinned staging [max_seq]
@@ -868,19 +869,53 @@ ssd_status ensure_policy(ssd_ctx* c, bool lossless = true) {
 ssd_status enq_score(ssd_ctx* c, const uint64_t* masks, int K, int N, int split) {
   const ssd_config& g = c->cfg;
   const int L = g.n_layers, D = g.d_model, rows = K * N, R = g.max_score_rows;
-  std::vector<int> nact(L, 0);
+  // Candidates whose skip decisions agree on every layer so far hold the same
+  // rows (all steps of the forward are row-count invariant), so each group
+  // computes one block of rows, held by its owner (a member).  At the first
+  // layer a group's members disagree on, the subset without the owner takes
+  // a copy of the owner's rows before the layer runs.  Scores are identical
+  // to computing every candidate on its own.
+  auto skips = [&](int k, int l) { return ((masks[4 * k + (l >> 6)] >> (l & 63)) & 1ull) != 0; };
+  std::vector<int> owner(K, 0), nact(L, 0);
+  std::vector<std::vector<std::pair<int, int>>> copies(L);  // per layer: (from, to) owners
   for (int l = 0; l < L; ++l) {
     int32_t* cand = c->h_sc_cand + (size_t)l * 256;
     int32_t* map = c->h_sc_map + (size_t)l * R;
-    for (int k = 0; k < K; ++k)
-      if (!((masks[4 * k + (l >> 6)] >> (l & 63)) & 1ull)) {
-        for (int i = 0; i < N; ++i) map[nact[l] * N + i] = k * N + i;
-        cand[nact[l]++] = k;
+    std::vector<int> next = owner;
+    for (int o = 0; o < K; ++o) {
+      if (owner[o] != o) continue;  // o is not an owner
+      std::vector<int> keep, skip;
+      for (int k = o; k < K; ++k)
+        if (owner[k] == o) (skips(k, l) ? skip : keep).push_back(k);
+      if (keep.empty()) continue;
+      int run = o;
+      if (!skip.empty()) {
+        const bool o_keeps = !skips(o, l);
+        const std::vector<int>& moved = o_keeps ? skip : keep;
+        copies[l].push_back({o, moved[0]});
+        for (int k : moved) next[k] = moved[0];
+        if (!o_keeps) run = moved[0];
+      }
+      for (int i = 0; i < N; ++i) map[nact[l] * N + i] = run * N + i;
+      cand[nact[l]++] = run;
+    }
+    owner = next;
+  }
+  // final owners: the LM head and the match count run on their rows
+  int nfin = 0;
+  {
+    int32_t* map = c->h_sc_map + (size_t)L * R;
+    for (int o = 0; o < K; ++o)
+      if (owner[o] == o) {
+        for (int i = 0; i < N; ++i) map[nfin * N + i] = o * N + i;
+        ++nfin;
       }
   }
+  c->sc_owner.assign(owner.begin(), owner.end());
   CK(cudaMemcpyAsync(c->sc_cand, c->h_sc_cand, (size_t)L * 256 * 4, cudaMemcpyHostToDevice,
                      c->stream));
-  CK(cudaMemcpyAsync(c->sc_map, c->h_sc_map, (size_t)L * R * 4, cudaMemcpyHostToDevice, c->stream));
+  CK(cudaMemcpyAsync(c->sc_map, c->h_sc_map, (size_t)(L + 1) * R * 4, cudaMemcpyHostToDevice,
+                     c->stream));
   CK(cudaMemsetAsync(c->sc_counts, 0, (size_t)K * sizeof(int32_t), c->stream));
   CK(cudaMemsetAsync(c->sc_best, 0, (size_t)rows * 8, c->stream));
   ssd_status r;
@@ -890,6 +925,9 @@ ssd_status enq_score(ssd_ctx* c, const uint64_t* masks, int K, int N, int split)
     return r;
   const int HD = g.n_heads * g.head_dim;
   for (int l = 0; l < L; ++l) {
+    for (const auto& cp : copies[l])
+      CK(cudaMemcpyAsync(c->sc_x + (size_t)cp.second * N * D, c->sc_x + (size_t)cp.first * N * D,
+                         (size_t)N * D * sizeof(float), cudaMemcpyDeviceToDevice, s));
     const int T = nact[l] * N;
     if (T == 0) continue;
     const ssd_layer_weights& w = c->layers[l];
@@ -968,7 +1006,8 @@ ssd_status enq_score(ssd_ctx* c, const uint64_t* masks, int K, int N, int split)
     dn.rowmap = map;
     if ((r = note(c, launch_gemm_rows(dn, s), "score_down")) != SSD_OK) return r;
   }
-  if ((r = note(c, launch_score_norm(c->sc_x, nullptr, c->final_norm, g.norm_eps, rows, D,
+  const int32_t* fmap = c->sc_map + (size_t)L * R;
+  if ((r = note(c, launch_score_norm(c->sc_x, fmap, c->final_norm, g.norm_eps, nfin * N, D,
                                      c->sc_xn, s),
                 "score_norm")) != SSD_OK)
     return r;
@@ -976,13 +1015,14 @@ ssd_status enq_score(ssd_ctx* c, const uint64_t* masks, int K, int N, int split)
   lm.W0 = c->lm_head;
   lm.R = g.vocab;
   lm.K = D;
-  lm.T = rows;
+  lm.T = nfin * N;
   lm.act = c->sc_xn;
   lm.epi = GEMM_ARGMAX;
   lm.err = &c->st->err;
   lm.best = c->sc_best;
   if ((r = note(c, launch_gemm_rows(lm, s), "score_lm_head")) != SSD_OK) return r;
-  return note(c, launch_score_match(c->sc_best, c->tokens, split, N, rows, c->sc_counts, s),
+  return note(c, launch_score_match(c->sc_best, fmap, c->tokens, split, N, nfin * N,
+                                    c->sc_counts, s),
               "score_match");
 }
 
@@ -1083,11 +1123,11 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
          alloc((void**)&c->sc_attn, rp * HD * 2) && alloc((void**)&c->sc_u, rp * g.ffn_dim * 2) &&
          alloc((void**)&c->sc_best, r * 8) &&
          alloc((void**)&c->sc_cand, (size_t)g.n_layers * 256 * 4) &&
-         alloc((void**)&c->sc_map, (size_t)g.n_layers * r * 4) &&
+         alloc((void**)&c->sc_map, (size_t)(g.n_layers + 1) * r * 4) &&
          alloc((void**)&c->sc_counts, 256 * sizeof(int32_t)) &&
          cudaMallocHost((void**)&c->h_counts, 256 * sizeof(int32_t)) == cudaSuccess &&
          cudaMallocHost((void**)&c->h_sc_cand, (size_t)g.n_layers * 256 * 4) == cudaSuccess &&
-         cudaMallocHost((void**)&c->h_sc_map, (size_t)g.n_layers * r * 4) == cudaSuccess;
+         cudaMallocHost((void**)&c->h_sc_map, (size_t)(g.n_layers + 1) * r * 4) == cudaSuccess;
     if (ok) cudaMemsetAsync(c->sc_best, 0, r * 8, c->stream);
   }
   if (!ok) {
@@ -1732,8 +1772,9 @@ ssd_status ssd_score_masks(ssd_ctx* c, const uint64_t* masks, int32_t K, int32_t
   if ((r = read_state(c)) != SSD_OK) return r;
   int best = 0;
   for (int k = 0; k < K; ++k) {
-    matchness_out[k] = (float)c->h_counts[k] / (float)N;
-    if (c->h_counts[k] > c->h_counts[best]) best = k;
+    const int cnt = c->h_counts[c->sc_owner[k]];
+    matchness_out[k] = (float)cnt / (float)N;
+    if (cnt > c->h_counts[c->sc_owner[best]]) best = k;
   }
   if (best_out) *best_out = best;
   return SSD_OK;

@@ -300,16 +300,18 @@ __global__ void __launch_bounds__(128) score_attn_kernel(ScoreAttnArgs a) {
   }
 }
 
-// counts[p / N] += (argmax of row p == tokens[split + 1 + p % N]); best[p]
-// is returned to zero for the next call.
-__global__ void score_match_kernel(unsigned long long* best, const int32_t* tokens, int split,
-                                   int N, int rows, int32_t* counts) {
-  const int p = blockIdx.x * blockDim.x + threadIdx.x;
-  if (p >= rows) return;
-  const unsigned long long key = best[p];
+// For compact row t of physical row p = map[t]: counts[p / N] += (argmax of
+// row t == tokens[split + 1 + p % N]); best[t] is returned to zero.
+__global__ void score_match_kernel(unsigned long long* best, const int32_t* map,
+                                   const int32_t* tokens, int split, int N, int T,
+                                   int32_t* counts) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  const int p = map ? map[t] : t;
+  const unsigned long long key = best[t];
   const int idx = (int)(0xffffffffu - (uint32_t)(key & 0xffffffffull));
   if (key != 0ull && idx == tokens[split + 1 + p % N]) atomicAdd(counts + p / N, 1);
-  best[p] = 0ull;
+  best[t] = 0ull;
 }
 
 }  // namespace
@@ -363,9 +365,9 @@ cudaError_t launch_score_attn(const ScoreAttnArgs& a, int n_active, cudaStream_t
   return cudaGetLastError();
 }
 
-cudaError_t launch_score_match(unsigned long long* best, const int32_t* tokens, int split, int N,
-                               int rows, int32_t* counts, cudaStream_t s) {
-  score_match_kernel<<<(rows + 255) / 256, 256, 0, s>>>(best, tokens, split, N, rows, counts);
+cudaError_t launch_score_match(unsigned long long* best, const int32_t* map, const int32_t* tokens,
+                               int split, int N, int T, int32_t* counts, cudaStream_t s) {
+  score_match_kernel<<<(T + 255) / 256, 256, 0, s>>>(best, map, tokens, split, N, T, counts);
   return cudaGetLastError();
 }
 

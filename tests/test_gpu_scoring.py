@@ -121,3 +121,21 @@ def test_scoring_capacity_errors(ssd):
     with pytest.raises(SSDError, match="CAPACITY"):
         ctx.score_masks([()], 20)                # window longer than the context
     ctx.close()
+
+
+def test_scoring_together_equals_alone(ssd):
+    # candidates that agree on the first layers share those rows; every step is
+    # row-count invariant, so a candidate's matchness is bit-identical whether
+    # it is scored with others (shared prefixes, duplicates) or alone
+    w = SMALL
+    wts = make_weights(w, dtype="bf16", lm_head_scale=10.0, random_gains=True)
+    ctx = ssd.SSDContext(w.shape, to_device_weights(wts), max_seq=256, max_score_rows=512)
+    ctx.set_policy(Policy(mode="skip", skip=(), d_max=4))
+    ctx.prefill(make_prompt(w, 12))
+    ctx.decode_ar(40)
+    masks = [(), (5,), (2, 5), (2, 6), (2, 5), (6, 7), (2, 3, 4)] + make_masks(w)
+    together, best = ctx.score_masks(masks, 24)
+    alone = [ctx.score_masks([m], 24)[0][0] for m in masks]
+    assert list(together) == alone
+    assert best == int(np.argmax(together))
+    ctx.close()
