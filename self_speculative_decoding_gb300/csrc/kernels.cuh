@@ -247,9 +247,10 @@ cudaError_t launch_score_norm(const float* x, const int32_t* map, const float* g
                               int T, int D, bf16* out, cudaStream_t s);
 // dst = src [T][K] row-major in the packed unit layout, rows T .. 16-padded zero
 cudaError_t launch_pack_act(const bf16* src, int T, int K, bf16* dst, cudaStream_t s);
+// map nullable (identity); kc / vc nullable: also store k, v into that cache
 cudaError_t launch_score_rope(const float* qkv, int T, const int32_t* map, int N, int split, int H,
                               int Hkv, int dh, const float2* rope, bf16* q, bf16* sk, bf16* sv,
-                              cudaStream_t s);
+                              bf16* kc, bf16* vc, int max_seq, cudaStream_t s);
 // compact rows t < T of physical rows map[t] (nullable: identity)
 cudaError_t launch_score_match(unsigned long long* best, const int32_t* map, const int32_t* tokens,
                                int split, int N, int T, int32_t* counts, cudaStream_t s);

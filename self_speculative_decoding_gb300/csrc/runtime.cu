@@ -117,6 +117,7 @@ struct ssd_ctx {
   int32_t* sc_counts = nullptr;
   int32_t* h_counts = nullptr;
   std::vector<int> sc_owner;      // per candidate of the last call: the row block it shares
+  int pf_chunk = 0;               // prompt rows per batched prefill chunk
   DevState* st = nullptr;
   DevState* h_st = nullptr;  // pinned mirror
   int32_t* h_tok = nullptr;  // pinned staging [max_seq]
@@ -169,7 +170,9 @@ struct Range {
   ~Range() { nvtxRangePop(); }
 };
 
-thread_local int g_fail_alloc = -1;  // fault injection: fail the n-th allocation
+thread_local int g_fail_alloc = -1;
+
+constexpr int kPrefillChunk = 512;  // prompt rows per batched prefill chunk  // fault injection: fail the n-th allocation
 
 #define CK(call)                                                                          \
   do {                                                                                    \
@@ -859,6 +862,99 @@ ssd_status ensure_policy(ssd_ctx* c, bool lossless = true) {
   return SSD_OK;
 }
 
+// One layer of the batched forward over T compact rows of the scoring
+// buffers (compact row t = row map[t] of sc_x, map nullable = identity):
+// RMSNorm, QKV projection, RoPE with the window K/V (and, with kv_write, the
+// cache at positions split + p % N), attention of the n_active candidates'
+// window rows (cand, device), o_proj + residual, RMSNorm, SwiGLU, down +
+// residual.
+ssd_status enq_rows_layer(ssd_ctx* c, int l, int T, const int32_t* map, const int32_t* cand,
+                          int n_active, int N, int split, bool kv_write) {
+  const ssd_config& g = c->cfg;
+  const int D = g.d_model, HD = g.n_heads * g.head_dim;
+  cudaStream_t s = c->stream;
+  ssd_status r;
+  bf16* at_kc = c->kc + (size_t)l * kv_layer_elems(g);
+  bf16* at_vc = c->vc + (size_t)l * kv_layer_elems(g);
+  const ssd_layer_weights& w = c->layers[l];
+  if ((r = note(c, launch_score_norm(c->sc_x, map, (const float*)w.attn_norm, g.norm_eps, T, D,
+                                     c->sc_xn, s),
+                "score_norm")) != SSD_OK)
+    return r;
+  GemmArgs q;
+  q.W0 = (const bf16*)w.wqkv;
+  q.R = qkv_rows(g);
+  q.K = D;
+  q.T = T;
+  q.act = c->sc_xn;
+  q.epi = GEMM_STORE;
+  q.err = &c->st->err;
+  q.y = c->sc_qkv;
+  if ((r = note(c, launch_gemm_rows(q, s), "score_qkv")) != SSD_OK) return r;
+  if ((r = note(c, launch_score_rope(c->sc_qkv, T, map, N, split, g.n_heads, g.n_kv_heads,
+                                     g.head_dim, c->rope, c->sc_q, c->sc_sk, c->sc_sv,
+                                     kv_write ? at_kc : nullptr, kv_write ? at_vc : nullptr,
+                                     g.max_seq, s),
+                "score_rope")) != SSD_OK)
+    return r;
+  ScoreAttnArgs at;
+  at.q = c->sc_q;
+  at.kc = at_kc;
+  at.vc = at_vc;
+  at.sk = c->sc_sk;
+  at.sv = c->sc_sv;
+  at.cand = cand;
+  at.N = N;
+  at.split = split;
+  at.max_seq = g.max_seq;
+  at.H = g.n_heads;
+  at.Hkv = g.n_kv_heads;
+  at.dh = g.head_dim;
+  at.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)g.head_dim));
+  at.out = c->sc_attn;
+  at.out_packed = 1;
+  if ((r = note(c, launch_score_attn(at, n_active, s), "score_attn")) != SSD_OK) return r;
+  GemmArgs o;
+  o.W0 = (const bf16*)w.wo;
+  o.R = D;
+  o.K = HD;
+  o.T = T;
+  o.act = c->sc_attn;
+  o.epi = GEMM_RESID;
+  o.err = &c->st->err;
+  o.x = c->sc_x;
+  o.rowmap = map;
+  if ((r = note(c, launch_gemm_rows(o, s), "score_oproj")) != SSD_OK) return r;
+  if ((r = note(c, launch_score_norm(c->sc_x, map, (const float*)w.mlp_norm, g.norm_eps, T, D,
+                                     c->sc_xn, s),
+                "score_norm")) != SSD_OK)
+    return r;
+  GemmArgs gu;
+  gu.W0 = (const bf16*)w.w_gate;
+  gu.W1 = (const bf16*)w.w_up;
+  gu.R = g.ffn_dim;
+  gu.K = D;
+  gu.T = T;
+  gu.act = c->sc_xn;
+  gu.epi = GEMM_SWIGLU;
+  gu.err = &c->st->err;
+  gu.u = c->sc_u;
+  gu.u_packed = 1;
+  if ((r = note(c, launch_gemm_rows(gu, s), "score_gate_up")) != SSD_OK) return r;
+  GemmArgs dn;
+  dn.W0 = (const bf16*)w.w_down;
+  dn.R = D;
+  dn.K = g.ffn_dim;
+  dn.T = T;
+  dn.act = c->sc_u;
+  dn.epi = GEMM_RESID;
+  dn.err = &c->st->err;
+  dn.x = c->sc_x;
+  dn.rowmap = map;
+  if ((r = note(c, launch_gemm_rows(dn, s), "score_down")) != SSD_OK) return r;
+    return SSD_OK;
+}
+
 // SWIFT §4.1.2: the K candidate layer sets predict the committed tokens
 // t[split+1 .. split+N] from t[split .. split+N-1] in one batched forward.
 // Row p = k N + i is candidate k's window position split + i; a layer runs
@@ -923,88 +1019,15 @@ ssd_status enq_score(ssd_ctx* c, const uint64_t* masks, int K, int N, int split)
   if ((r = note(c, launch_score_embed(c->embed, c->tokens, split, N, rows, D, c->sc_x, s),
                 "score_embed")) != SSD_OK)
     return r;
-  const int HD = g.n_heads * g.head_dim;
   for (int l = 0; l < L; ++l) {
     for (const auto& cp : copies[l])
       CK(cudaMemcpyAsync(c->sc_x + (size_t)cp.second * N * D, c->sc_x + (size_t)cp.first * N * D,
                          (size_t)N * D * sizeof(float), cudaMemcpyDeviceToDevice, s));
     const int T = nact[l] * N;
     if (T == 0) continue;
-    const ssd_layer_weights& w = c->layers[l];
-    const int32_t* map = c->sc_map + (size_t)l * R;
-    if ((r = note(c, launch_score_norm(c->sc_x, map, (const float*)w.attn_norm, g.norm_eps, T, D,
-                                       c->sc_xn, s),
-                  "score_norm")) != SSD_OK)
+    if ((r = enq_rows_layer(c, l, T, c->sc_map + (size_t)l * R, c->sc_cand + (size_t)l * 256,
+                            nact[l], N, split, false)) != SSD_OK)
       return r;
-    GemmArgs q;
-    q.W0 = (const bf16*)w.wqkv;
-    q.R = qkv_rows(g);
-    q.K = D;
-    q.T = T;
-    q.act = c->sc_xn;
-    q.epi = GEMM_STORE;
-    q.err = &c->st->err;
-    q.y = c->sc_qkv;
-    if ((r = note(c, launch_gemm_rows(q, s), "score_qkv")) != SSD_OK) return r;
-    if ((r = note(c, launch_score_rope(c->sc_qkv, T, map, N, split, g.n_heads, g.n_kv_heads,
-                                       g.head_dim, c->rope, c->sc_q, c->sc_sk, c->sc_sv, s),
-                  "score_rope")) != SSD_OK)
-      return r;
-    ScoreAttnArgs at;
-    at.q = c->sc_q;
-    at.kc = c->kc + (size_t)l * kv_layer_elems(g);
-    at.vc = c->vc + (size_t)l * kv_layer_elems(g);
-    at.sk = c->sc_sk;
-    at.sv = c->sc_sv;
-    at.cand = c->sc_cand + (size_t)l * 256;
-    at.N = N;
-    at.split = split;
-    at.max_seq = g.max_seq;
-    at.H = g.n_heads;
-    at.Hkv = g.n_kv_heads;
-    at.dh = g.head_dim;
-    at.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)g.head_dim));
-    at.out = c->sc_attn;
-    at.out_packed = 1;
-    if ((r = note(c, launch_score_attn(at, nact[l], s), "score_attn")) != SSD_OK) return r;
-    GemmArgs o;
-    o.W0 = (const bf16*)w.wo;
-    o.R = D;
-    o.K = HD;
-    o.T = T;
-    o.act = c->sc_attn;
-    o.epi = GEMM_RESID;
-    o.err = &c->st->err;
-    o.x = c->sc_x;
-    o.rowmap = map;
-    if ((r = note(c, launch_gemm_rows(o, s), "score_oproj")) != SSD_OK) return r;
-    if ((r = note(c, launch_score_norm(c->sc_x, map, (const float*)w.mlp_norm, g.norm_eps, T, D,
-                                       c->sc_xn, s),
-                  "score_norm")) != SSD_OK)
-      return r;
-    GemmArgs gu;
-    gu.W0 = (const bf16*)w.w_gate;
-    gu.W1 = (const bf16*)w.w_up;
-    gu.R = g.ffn_dim;
-    gu.K = D;
-    gu.T = T;
-    gu.act = c->sc_xn;
-    gu.epi = GEMM_SWIGLU;
-    gu.err = &c->st->err;
-    gu.u = c->sc_u;
-    gu.u_packed = 1;
-    if ((r = note(c, launch_gemm_rows(gu, s), "score_gate_up")) != SSD_OK) return r;
-    GemmArgs dn;
-    dn.W0 = (const bf16*)w.w_down;
-    dn.R = D;
-    dn.K = g.ffn_dim;
-    dn.T = T;
-    dn.act = c->sc_u;
-    dn.epi = GEMM_RESID;
-    dn.err = &c->st->err;
-    dn.x = c->sc_x;
-    dn.rowmap = map;
-    if ((r = note(c, launch_gemm_rows(dn, s), "score_down")) != SSD_OK) return r;
   }
   const int32_t* fmap = c->sc_map + (size_t)L * R;
   if ((r = note(c, launch_score_norm(c->sc_x, fmap, c->final_norm, g.norm_eps, nfin * N, D,
@@ -1112,9 +1135,13 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
             alloc((void**)&c->st, sizeof(DevState)) &&
             alloc((void**)&c->fstats, (size_t)g.n_layers * sizeof(RowStats)) &&
             alloc((void**)&c->ffeat, (size_t)3 * g.n_layers * 4);
-  if (ok && g.max_score_rows > 0) {
-    // rows of the projections' packed bf16 inputs are padded to 16
-    const size_t r = (size_t)g.max_score_rows, D = g.d_model, HD = (size_t)g.n_heads * g.head_dim;
+  if (ok) {
+    // the batched forward's rows: candidate-mask scoring (max_score_rows) and
+    // the prefill chunks share them; rows of the projections' packed bf16
+    // inputs are padded to 16
+    c->pf_chunk = g.max_seq < kPrefillChunk ? g.max_seq : kPrefillChunk;
+    const size_t r = (size_t)std::max(g.max_score_rows, c->pf_chunk), D = g.d_model,
+                 HD = (size_t)g.n_heads * g.head_dim;
     const size_t rp = (r + 15) / 16 * 16;
     const size_t KV = (size_t)g.n_kv_heads * g.head_dim;
     ok = alloc((void**)&c->sc_x, r * D * 4) && alloc((void**)&c->sc_xn, rp * D * 2) &&
@@ -1269,16 +1296,31 @@ ssd_status ssd_prefill(ssd_ctx* c, const int32_t* tokens, int32_t n, int32_t* fi
   memcpy(c->h_tok, tokens, (size_t)n * 4);
   CK(cudaMemcpyAsync(c->toks_in, c->h_tok, (size_t)n * 4, cudaMemcpyHostToDevice, c->stream));
   CK(cudaMemcpyAsync(c->tokens, c->h_tok, (size_t)n * 4, cudaMemcpyHostToDevice, c->stream));
-  std::vector<int> all(c->cfg.n_layers);
-  for (int l = 0; l < c->cfg.n_layers; ++l) all[l] = l;
+  // The prompt in chunks of up to pf_chunk rows through the batched forward
+  // (tensor-core projections; each chunk attends causally to itself and to
+  // the cache of the chunks before it, and writes its K/V into the cache).
+  const int D = c->cfg.d_model;
+  cudaStream_t s = c->stream;
   ssd_status r;
-  for (int p0 = 0; p0 < n; p0 += kMaxRows) {
-    const int M = n - p0 < kMaxRows ? n - p0 : kMaxRows;
-    if ((r = enq_begin(c, BEGIN_TOKENS, c->stream, M, p0, c->toks_in + p0, p0 == 0)) != SSD_OK) return r;
-    if ((r = enq_layers(c, all, c->stream)) != SSD_OK) return r;
+  CK(cudaMemsetAsync(c->sc_cand, 0, sizeof(int32_t), s));  // the one "candidate"
+  int last = 0;
+  for (int c0 = 0; c0 < n; c0 += c->pf_chunk) {
+    const int m = std::min(c->pf_chunk, n - c0);
+    if ((r = note(c, launch_score_embed(c->embed, c->toks_in, c0, m, m, D, c->sc_x, s),
+                  "prefill_embed")) != SSD_OK)
+      return r;
+    for (int l = 0; l < c->cfg.n_layers; ++l)
+      if ((r = enq_rows_layer(c, l, m, nullptr, c->sc_cand, 1, m, c0, true)) != SSD_OK) return r;
+    last = m;
   }
-  if ((r = enq_lmhead(c, c->vstats, nullptr, nullptr, 2, c->stream)) != SSD_OK) return r;
-  if ((r = note(c, launch_ar_end(c->st, c->tokens, c->vstats, 1, c->pol.temperature, 1, c->stream,
+  // the last prompt position's state through the decode path's final norm and
+  // LM head (row summary; the first token committed as an AR step commits it)
+  if ((r = enq_begin(c, BEGIN_TOKENS, s, 1, n - 1, c->toks_in + n - 1, 1)) != SSD_OK) return r;
+  CK(cudaMemcpyAsync(c->x, c->sc_x + (size_t)(last - 1) * D, (size_t)D * sizeof(float),
+                     cudaMemcpyDeviceToDevice, s));
+  if ((r = note(c, launch_ss_partials(c->x, 1, D, c->ss, s), "prefill_ss")) != SSD_OK) return r;
+  if ((r = enq_lmhead(c, c->vstats, nullptr, nullptr, 2, s)) != SSD_OK) return r;
+  if ((r = note(c, launch_ar_end(c->st, c->tokens, c->vstats, 1, c->pol.temperature, 1, s,
                                  c->pdl), "prefill_end")) != SSD_OK)
     return r;
   if ((r = read_state(c)) != SSD_OK) return r;

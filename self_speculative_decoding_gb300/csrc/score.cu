@@ -64,10 +64,12 @@ __global__ void __launch_bounds__(256) score_norm_kernel(const float* x, const i
 }
 
 // RoPE (rotate-half pairs (j, j + dh/2)) of the compact rows' q and k at
-// position split + p % N; q -> q[t] bf16, k and v -> the window cache row p.
+// position split + p % N (p = map[t], or t without a map); q -> q[t] bf16,
+// k and v -> the window cache row p and, when kc is given, also the layer's
+// cache [Hkv][max_seq][dh] at that position (the batched prefill).
 __global__ void score_rope_kernel(const float* qkv, int T, const int32_t* map, int N, int split,
                                   int H, int Hkv, int dh, const float2* rope, bf16* q, bf16* sk,
-                                  bf16* sv) {
+                                  bf16* sv, bf16* kc, bf16* vc, int max_seq) {
   const int half = dh / 2;
   const int per_row = (H + Hkv) * half + Hkv * half;  // rotations + v pairs
   const int ld = (H + 2 * Hkv) * dh;
@@ -76,7 +78,7 @@ __global__ void score_rope_kernel(const float* qkv, int T, const int32_t* map, i
        e += (size_t)gridDim.x * blockDim.x) {
     const int t = (int)(e / per_row);
     int r = (int)(e % per_row);
-    const int p = map[t];
+    const int p = map ? map[t] : t;
     const int pos = split + p % N;
     const float* row = qkv + (size_t)t * ld;
     if (r < (H + Hkv) * half) {
@@ -93,13 +95,19 @@ __global__ void score_rope_kernel(const float* qkv, int T, const int32_t* map, i
         bf16* d = sk + ((size_t)p * Hkv + (hh - H)) * dh;
         d[j] = __float2bfloat16_rn(ra);
         d[j + half] = __float2bfloat16_rn(rb);
+        if (kc) {
+          bf16* e2 = kc + ((size_t)(hh - H) * max_seq + pos) * dh;
+          e2[j] = d[j];
+          e2[j + half] = d[j + half];
+        }
       }
     } else {
       r -= (H + Hkv) * half;
       const int kvh = r / half, j2 = 2 * (r % half);
       const float* v = row + (size_t)(H + Hkv) * dh + (size_t)kvh * dh;
-      *reinterpret_cast<uint32_t*>(sv + ((size_t)p * Hkv + kvh) * dh + j2) =
-          pack_bf16x2(v[j2], v[j2 + 1]);
+      const uint32_t vv = pack_bf16x2(v[j2], v[j2 + 1]);
+      *reinterpret_cast<uint32_t*>(sv + ((size_t)p * Hkv + kvh) * dh + j2) = vv;
+      if (vc) *reinterpret_cast<uint32_t*>(vc + ((size_t)kvh * max_seq + pos) * dh + j2) = vv;
     }
   }
 }
@@ -331,8 +339,9 @@ cudaError_t launch_score_norm(const float* x, const int32_t* map, const float* g
 
 cudaError_t launch_score_rope(const float* qkv, int T, const int32_t* map, int N, int split, int H,
                               int Hkv, int dh, const float2* rope, bf16* q, bf16* sk, bf16* sv,
-                              cudaStream_t s) {
-  score_rope_kernel<<<1216, 256, 0, s>>>(qkv, T, map, N, split, H, Hkv, dh, rope, q, sk, sv);
+                              bf16* kc, bf16* vc, int max_seq, cudaStream_t s) {
+  score_rope_kernel<<<1216, 256, 0, s>>>(qkv, T, map, N, split, H, Hkv, dh, rope, q, sk, sv, kc, vc,
+                                         max_seq);
   return cudaGetLastError();
 }
 
