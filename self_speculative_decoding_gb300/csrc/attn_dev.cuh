@@ -152,35 +152,43 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
       qd[i + half] = q0 * cs.y + q1 * cs.x;
     }
     sync();
-    // (4) scores: 8 lanes per (row, key); lane q8 takes the 8-element chunks
-    // q8, q8 + 8, ... of the head dimension, so one warp instruction reads 4
-    // key rows of 128 contiguous bytes (no bank conflict without row
-    // padding); then a 3-step butterfly (fixed order)
-    for (int u = tid; u < M * kAttnChunk * 8; u += kGroupThreads) {
-      const int q8 = u & 7, key = (u >> 3) & (kAttnChunk - 1), m = u >> 9;
-      const bool valid = key < nk && p_begin + key <= pos0 + m;
-      float acc = 0.f;
-      if (valid) {
-        const float* q = sm.Q + (size_t)m * dh;
-        const bf16* k = sm.K + (size_t)key * dh;
-        for (int d0 = q8 * 8; d0 < dh; d0 += 64) {
-          const uint4 kk = *reinterpret_cast<const uint4*>(k + d0);
-          const float4 qa = *reinterpret_cast<const float4*>(q + d0);
-          const float4 qb = *reinterpret_cast<const float4*>(q + d0 + 4);
-          acc = fmaf(qa.x, bf16_lo(kk.x), acc);
-          acc = fmaf(qa.y, bf16_hi(kk.x), acc);
-          acc = fmaf(qa.z, bf16_lo(kk.y), acc);
-          acc = fmaf(qa.w, bf16_hi(kk.y), acc);
-          acc = fmaf(qb.x, bf16_lo(kk.z), acc);
-          acc = fmaf(qb.y, bf16_hi(kk.z), acc);
-          acc = fmaf(qb.z, bf16_lo(kk.w), acc);
-          acc = fmaf(qb.w, bf16_hi(kk.w), acc);
+    // (4) scores.  Row m's dot product with key j is taken by an aligned
+    // group of 8 lanes: lane q8 sums the 8-element pieces q8, q8 + 8, ... of
+    // the head dimension in that order, then a 3-step butterfly (fixed
+    // order).  One warp instruction reads 4 key rows of 128 contiguous bytes
+    // (no bank conflict).  A warp task is one row and a run of 4-key groups;
+    // the row's query pieces stay in registers over the run.  Only the
+    // assignment of tasks to warps depends on M, never the order of a sum.
+    {
+      const int gpt = M <= 4 ? 2 : 4;        // 4-key groups per task
+      const int tpr = kAttnChunk / 4 / gpt;  // tasks per row
+      const int q8 = lane & 7, ks = lane >> 3;
+      const bool two = dh > 64;              // pieces per lane: 1 (dh 64) or 2 (dh 128)
+      for (int task = warp; task < M * tpr; task += kGroupWarps) {
+        const int m = task / tpr, kg0 = (task % tpr) * gpt;
+        const float* q = sm.Q + (size_t)m * dh + q8 * 8;
+        const float4 qa0 = *reinterpret_cast<const float4*>(q);
+        const float4 qb0 = *reinterpret_cast<const float4*>(q + 4);
+        float4 qa1 = qa0, qb1 = qb0;
+        if (two) {
+          qa1 = *reinterpret_cast<const float4*>(q + 64);
+          qb1 = *reinterpret_cast<const float4*>(q + 68);
+        }
+        for (int kg = kg0; kg < kg0 + gpt; ++kg) {
+          const int key = kg * 4 + ks;
+          const bool valid = key < nk && p_begin + key <= pos0 + m;
+          float acc = 0.f;
+          if (valid) {
+            const bf16* k = sm.K + (size_t)key * dh + q8 * 8;
+            acc = dot8(qa0, qb0, *reinterpret_cast<const uint4*>(k), acc);
+            if (two) acc = dot8(qa1, qb1, *reinterpret_cast<const uint4*>(k + 64), acc);
+          }
+          acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+          acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+          acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+          if (q8 == 0) sm.S[(size_t)m * kAttnChunk + key] = valid ? acc * a.scale : -INFINITY;
         }
       }
-      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-      if (q8 == 0) sm.S[(size_t)m * kAttnChunk + key] = valid ? acc * a.scale : -INFINITY;
     }
     sync();
     // (5) per-row chunk softmax statistics; one warp per row
@@ -205,14 +213,77 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
       }
     }
     sync();
-    // (6) unnormalised output of the chunk: sequential over keys
-    for (int e = tid; e < M * dh; e += kGroupThreads) {
-      const int dd = e % dh, m = e / dh;
-      const int r = gh * kMaxRows + m;
-      const float* p = sm.S + (size_t)m * kAttnChunk;
-      float o = 0.f;
-      for (int j = 0; j < nk; ++j) o = fmaf(p[j], __bfloat162float(sm.V[j * dh + dd]), o);
-      part_base[(size_t)r * (dh + kRecPad) + kRecPad + dd] = o;
+    // (6) unnormalised output of the chunk: output (m, dd) sums p_j v_j[dd]
+    // over the keys in order.  When every output has a thread of its own
+    // (M dh <= threads), thread t takes column t % dh of row t / dh.
+    // Otherwise thread t takes the column pair t % (dh/2) and the rows
+    // t / (dh/2) + r (kGroupThreads / (dh/2)), r = 0, 1, ...; per 4 keys it
+    // reads one bf16 pair per key and one float4 of p per row.
+    if (M * dh <= kGroupThreads) {
+      const int dd = tid % dh, m = tid / dh;
+      if (m < M) {
+        const bf16* vcol = sm.V + dd;
+        const float* p = sm.S + (size_t)m * kAttnChunk;
+        float o = 0.f;
+        int j = 0;
+        for (; j + 4 <= nk; j += 4) {
+          const float4 pp = *reinterpret_cast<const float4*>(p + j);
+          o = fmaf(pp.x, __bfloat162float(vcol[(size_t)j * dh]), o);
+          o = fmaf(pp.y, __bfloat162float(vcol[(size_t)(j + 1) * dh]), o);
+          o = fmaf(pp.z, __bfloat162float(vcol[(size_t)(j + 2) * dh]), o);
+          o = fmaf(pp.w, __bfloat162float(vcol[(size_t)(j + 3) * dh]), o);
+        }
+        for (; j < nk; ++j) o = fmaf(p[j], __bfloat162float(vcol[(size_t)j * dh]), o);
+        part_base[(size_t)(gh * kMaxRows + m) * (dh + kRecPad) + kRecPad + dd] = o;
+      }
+    } else {
+      const int h2 = dh / 2;
+      const int nrg = kGroupThreads / h2;    // 4 (dh 128) or 8 (dh 64)
+      const int cp = tid % h2, rg = tid / h2;
+      const int nr = M > rg ? (M - rg + nrg - 1) / nrg : 0;  // <= kMaxRows / 4
+      float o[kMaxRows / 4][2];
+#pragma unroll
+      for (int r = 0; r < kMaxRows / 4; ++r) o[r][0] = o[r][1] = 0.f;
+      const __nv_bfloat162* vcol = reinterpret_cast<const __nv_bfloat162*>(sm.V) + cp;
+      int j = 0;
+      for (; j + 4 <= nk; j += 4) {
+        float2 v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[q] = __bfloat1622float2(vcol[(size_t)(j + q) * h2]);
+#pragma unroll
+        for (int r = 0; r < kMaxRows / 4; ++r) {
+          if (r < nr) {
+            const float4 p = *reinterpret_cast<const float4*>(sm.S + (size_t)(rg + r * nrg) * kAttnChunk + j);
+            o[r][0] = fmaf(p.x, v[0].x, o[r][0]);
+            o[r][1] = fmaf(p.x, v[0].y, o[r][1]);
+            o[r][0] = fmaf(p.y, v[1].x, o[r][0]);
+            o[r][1] = fmaf(p.y, v[1].y, o[r][1]);
+            o[r][0] = fmaf(p.z, v[2].x, o[r][0]);
+            o[r][1] = fmaf(p.z, v[2].y, o[r][1]);
+            o[r][0] = fmaf(p.w, v[3].x, o[r][0]);
+            o[r][1] = fmaf(p.w, v[3].y, o[r][1]);
+          }
+        }
+      }
+      for (; j < nk; ++j) {
+        const float2 v = __bfloat1622float2(vcol[(size_t)j * h2]);
+#pragma unroll
+        for (int r = 0; r < kMaxRows / 4; ++r) {
+          if (r < nr) {
+            const float p = sm.S[(size_t)(rg + r * nrg) * kAttnChunk + j];
+            o[r][0] = fmaf(p, v.x, o[r][0]);
+            o[r][1] = fmaf(p, v.y, o[r][1]);
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kMaxRows / 4; ++r) {
+        if (r < nr) {
+          const int rr = gh * kMaxRows + rg + r * nrg;
+          *reinterpret_cast<float2*>(part_base + (size_t)rr * (dh + kRecPad) + kRecPad + 2 * cp) =
+              make_float2(o[r][0], o[r][1]);
+        }
+      }
     }
   }
   __threadfence();

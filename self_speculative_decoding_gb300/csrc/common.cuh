@@ -73,6 +73,19 @@ SSD_DI uint32_t pack_bf16x2(float lo, float hi) {
 SSD_DI float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 SSD_DI float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
+// acc + sum_i q_i k_i over 8 elements (q = qa, qb; k = 8 bf16), in element order.
+SSD_DI float dot8(const float4& qa, const float4& qb, const uint4& k, float acc) {
+  acc = fmaf(qa.x, bf16_lo(k.x), acc);
+  acc = fmaf(qa.y, bf16_hi(k.x), acc);
+  acc = fmaf(qa.z, bf16_lo(k.y), acc);
+  acc = fmaf(qa.w, bf16_hi(k.y), acc);
+  acc = fmaf(qb.x, bf16_lo(k.z), acc);
+  acc = fmaf(qb.y, bf16_hi(k.z), acc);
+  acc = fmaf(qb.z, bf16_lo(k.w), acc);
+  acc = fmaf(qb.w, bf16_hi(k.w), acc);
+  return acc;
+}
+
 // D += A * B on the tensor cores, m16n8k16, bf16 inputs, fp32 accumulate.
 SSD_DI void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                      uint32_t b0, uint32_t b1) {
