@@ -115,6 +115,20 @@ typedef struct {
    * The verify recomputes from the first layer with any dropped sublayer.  */
   uint64_t skip_attn_mask[4];
   uint64_t skip_mlp_mask[4];
+  /* Dynamic verification (SWIFT §4.2: the draft's confidence also sets how
+   * many candidates are verified; greedy decoding only).  tree_tau <= 0:
+   * off.  Otherwise a kept draft y_j whose top-1 probability is below
+   * tree_tau gets the draft's second choice s_j as a sibling candidate (at
+   * most tree_max per round, 1..8, in depth order; d_max + 1 + tree_max
+   * <= 16).  A sibling runs as a side row of the next draft step (or the
+   * extra pass) through the layers below s0 and of the verify pass through
+   * the rest, attending to the context before its position and to itself.
+   * When y_a is rejected and the full model's token there equals s_a, the
+   * sibling is taken and the full model's token after it is emitted too
+   * (one more token in that round; the output stays the greedy output).
+   * Requires temperature 0 (else SSD_ERR_INVALID_ARG).                    */
+  float tree_tau;
+  int32_t tree_max;
 } ssd_policy;
 
 typedef struct {
@@ -130,6 +144,8 @@ typedef struct {
   double draft_ms;         /* draft steps                                   */
   double verify_ms;        /* extra passes, verify passes and acceptance    */
   double ar_ms;            /* ssd_decode_ar: the autoregressive steps       */
+  int64_t side_rows;       /* dynamic verification: siblings verified        */
+  int64_t side_accepted;   /* rounds that took a sibling (one more token)   */
 } ssd_stats;
 
 /* Fault injection for failure-detection tests: the n-th device allocation

@@ -44,16 +44,28 @@ reason in the design notes):
   the committed length becomes n + a + 1 (the blog's context update line is
   garbled); K/V beyond the new pending position is stale and is overwritten
   before it is read, which is the rollback.
+* Dynamic verification (SWIFT §4.2 and §3.2.1: the draft's confidence also
+  sets how many candidates go to the verify; top-k drafts raise the accepted
+  length).  Read for greedy decoding as one-level siblings off the drafted
+  chain: a kept draft y_j whose confidence is below ``tree_tau`` also sends
+  the draft's second choice s_j (at most ``tree_max`` per round, in depth
+  order).  The verify computes, besides the chain rows, the full model's
+  logits for each sibling at its position n + j given the accepted-so-far
+  prefix (tokens before n + j) -- one full-model step on a fork of the
+  cache.  Acceptance walks the chain; at the first rejected depth a, when a
+  sibling at depth a is the full model's token there, the sibling is taken
+  and the full model's token after it is emitted as well, and the cache
+  becomes that sibling's fork.  The emitted sequence stays the greedy one.
 """
 
 from __future__ import annotations
 
 from dataclasses import dataclass, field
-from typing import Callable, List, Optional
+from typing import Callable, List, Optional, Tuple
 
 import numpy as np
 
-from .model import OracleModel, KVCache, softmax, logsumexp
+from .model import OracleModel, KVCache, softmax, logsumexp, top2
 from .philox import (gumbel_argmax, uniform, STREAM_DRAFT, STREAM_ACCEPT,
                      STREAM_RESAMPLE)
 
@@ -80,6 +92,9 @@ class RoundRecord:
     accepted: int
     emitted: List[int]
     extra_pass: bool = False
+    siblings: List[Tuple[int, int]] = field(default_factory=list)   # (depth j, token)
+    sibling_logits: List[np.ndarray] = field(default_factory=list)
+    sibling_taken: Optional[int] = None
 
     @property
     def d(self) -> int:
@@ -156,6 +171,15 @@ def accept_stochastic(P: np.ndarray, Q: List[np.ndarray], ys: List[int], T: floa
     return d, list(ys) + [draw_tok(d, P[d] / T)]
 
 
+def sibling_step(model: OracleModel, kv: KVCache, pos: int, tok: int):
+    """A sibling candidate's verify row: one full-model step of ``tok`` at
+    ``pos`` on a fork of ``kv`` (which holds the full-model K/V of the
+    tokens before ``pos``).  Returns (logits, fork)."""
+    kv_s = kv.fork()
+    X = model.run_layers(model.embed_rows([tok]), [pos], kv_s, range(model.s.n_layers))
+    return model.lm_head(X)[0], kv_s
+
+
 def ssd_round(model: OracleModel, st: SSDState, policy) -> RoundRecord:
     s = model.s
     L = s.n_layers
@@ -167,6 +191,9 @@ def ssd_round(model: OracleModel, st: SSDState, policy) -> RoundRecord:
     s0 = policy.first_recomputed(L)
     post = [l for l in policy.draft_layers(L) if l >= s0]
 
+    tree_tau = getattr(policy, "tree_tau", None)
+    tree = tree_tau is not None and tree_tau > 0.0 and T == 0.0 and policy.tree_max > 0
+    sibs: List[Tuple[int, int]] = []
     ys: List[int] = []
     confs: List[float] = []
     zs: List[np.ndarray] = []
@@ -189,6 +216,8 @@ def ssd_round(model: OracleModel, st: SSDState, policy) -> RoundRecord:
         ys.append(y)
         confs.append(conf)
         zs.append(z)
+        if tree and conf < tree_tau and len(sibs) < policy.tree_max:
+            sibs.append((j, top2(z)[2]))
     d = len(ys)
     extra = False
     if len(bnd) == d:
@@ -201,12 +230,25 @@ def ssd_round(model: OracleModel, st: SSDState, policy) -> RoundRecord:
 
     Xv = model.run_layers(np.stack(bnd), range(n - 1, n + d), st.kv, range(s0, L))
     P = model.lm_head(Xv)
+    forks, sib_logits = [], []
+    for j, s_tok in sibs:
+        z_s, kv_s = sibling_step(model, st.kv, n + j, s_tok)
+        forks.append(kv_s)
+        sib_logits.append(z_s)
+    taken = None
 
     if T == 0.0:
         a = 0
         while a < d and ys[a] == int(np.argmax(P[a])):
             a += 1
-        emitted = ys[:a] + [int(np.argmax(P[a]))]
+        t = int(np.argmax(P[a]))
+        emitted = ys[:a] + [t]
+        for i, (j, s_tok) in enumerate(sibs):
+            if a < d and j == a and s_tok == t:
+                taken = i
+        if taken is not None:
+            emitted.append(int(np.argmax(sib_logits[taken])))
+            st.kv = forks[taken]
     else:
         a, emitted = accept_stochastic(
             P, zs, ys, T,
@@ -215,7 +257,8 @@ def ssd_round(model: OracleModel, st: SSDState, policy) -> RoundRecord:
     st.tokens.extend(int(t) for t in emitted)
     return RoundRecord(n_before=n, draft=ys, conf=confs, stop_conf=stop_conf,
                        draft_logits=zs, verify_logits=P, accepted=a, emitted=emitted,
-                       extra_pass=extra)
+                       extra_pass=extra, siblings=sibs, sibling_logits=sib_logits,
+                       sibling_taken=taken)
 
 
 @dataclass
@@ -224,6 +267,8 @@ class GenStats:
     drafted: int = 0
     accepted: int = 0
     emitted: int = 0
+    side_rows: int = 0       # dynamic verification: siblings verified
+    side_accepted: int = 0   # rounds that took a sibling
     records: List[RoundRecord] = field(default_factory=list)
 
     @property
@@ -247,6 +292,8 @@ def ssd_generate(model: OracleModel, st: SSDState, policy, n_new: int) -> GenSta
         stats.drafted += r.d
         stats.accepted += r.accepted
         stats.emitted += len(r.emitted)
+        stats.side_rows += len(r.siblings)
+        stats.side_accepted += r.sibling_taken is not None
         stats.records.append(r)
     del st.tokens[target:]
     return stats

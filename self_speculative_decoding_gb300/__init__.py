@@ -79,8 +79,8 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
 
 def policy_struct(policy) -> SsdPolicy:
     """Marshals a policy (attributes mode, skip, skip_attn, skip_mlp,
-    exit_layer, d_max, tau, temperature, seed — e.g. ``synthetic.Policy``)
-    into ``ssd_policy``."""
+    exit_layer, d_max, tau, temperature, seed, tree_tau, tree_max — e.g.
+    ``synthetic.Policy``) into ``ssd_policy``."""
     p = SsdPolicy()
     p.mode = SSD_MODE_SKIP if policy.mode == "skip" else SSD_MODE_EXIT
     for field, mask in (("skip", p.skip_mask), ("skip_attn", p.skip_attn_mask),
@@ -93,6 +93,9 @@ def policy_struct(policy) -> SsdPolicy:
     p.tau = -1.0 if tau is None else float(tau)
     p.temperature = float(getattr(policy, "temperature", 0.0))
     p.seed = int(getattr(policy, "seed", 0)) & ((1 << 64) - 1)
+    tree_tau = getattr(policy, "tree_tau", None)
+    p.tree_tau = 0.0 if tree_tau is None else float(tree_tau)
+    p.tree_max = int(getattr(policy, "tree_max", 0))
     return p
 
 

@@ -42,7 +42,8 @@ class SsdPolicy(C.Structure):
     _fields_ = [("mode", C.c_int32), ("skip_mask", C.c_uint64 * 4), ("exit_layer", C.c_int32),
                 ("d_max", C.c_int32), ("tau", C.c_float), ("temperature", C.c_float),
                 ("seed", C.c_uint64), ("skip_attn_mask", C.c_uint64 * 4),
-                ("skip_mlp_mask", C.c_uint64 * 4)]
+                ("skip_mlp_mask", C.c_uint64 * 4), ("tree_tau", C.c_float),
+                ("tree_max", C.c_int32)]
 
 
 class SsdSwiftParams(C.Structure):
@@ -61,7 +62,8 @@ class SsdStats(C.Structure):
     _fields_ = [("rounds", C.c_int64), ("drafted", C.c_int64), ("accepted", C.c_int64),
                 ("emitted", C.c_int64), ("draft_steps", C.c_int64),
                 ("kernel_launches", C.c_int64), ("bytes_streamed", C.c_double),
-                ("draft_ms", C.c_double), ("verify_ms", C.c_double), ("ar_ms", C.c_double)]
+                ("draft_ms", C.c_double), ("verify_ms", C.c_double), ("ar_ms", C.c_double),
+                ("side_rows", C.c_int64), ("side_accepted", C.c_int64)]
 
     def as_dict(self) -> dict:
         return {k: getattr(self, k) for k, _ in self._fields_}

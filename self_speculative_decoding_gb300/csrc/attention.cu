@@ -38,15 +38,16 @@ __global__ void __launch_bounds__(attn::kGroupThreads, 3) attn_kernel(AttnArgs a
   // projection that produces q, k, v).
   const int M = a.M_dev ? __ldcg(a.M_dev) : a.M_static;
   const int pos0 = a.pos0_dev ? __ldcg(a.pos0_dev) : a.pos0_static;
+  const int ns = a.ns_dev ? __ldcg(a.ns_dev) : 0;  // side rows (after the chain rows)
   const attn::Smem sm = attn::carve(smem_raw, a.dh, a.max_seq / kAttnChunk);
-  const int n_items = ((pos0 + M - 1) / kAttnChunk + 1) * a.Hkv;
+  const int n_items = ((pos0 + M - ns - 1) / kAttnChunk + 1) * a.Hkv;
   uint32_t phase = 0;
-  if ((int)blockIdx.x < n_items) attn::issue(a, M, pos0, blockIdx.x, sm, &bar, tid);
+  if ((int)blockIdx.x < n_items) attn::issue(a, M - ns, pos0, blockIdx.x, sm, &bar, tid);
   pdl_wait();
   pdl_trigger();
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-    if (it != (int)blockIdx.x) attn::issue(a, M, pos0, it, sm, &bar, tid);
-    attn::body(a, M, pos0, it, sm, &bar, phase, &flag, tid, [] { __syncthreads(); });
+    if (it != (int)blockIdx.x) attn::issue(a, M - ns, pos0, it, sm, &bar, tid);
+    attn::body(a, M, ns, pos0, it, sm, &bar, phase, &flag, tid, [] { __syncthreads(); });
   }
 }
 

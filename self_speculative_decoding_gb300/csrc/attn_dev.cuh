@@ -31,6 +31,10 @@ constexpr int kRecPad = 4;
 // Shared memory of one item (offsets multiples of 16 B):
 //   K [64][dh] bf16 | V [64][dh] bf16 | Q [16][dh] f32 | S [16][64] f32
 //   | combine scratch: m, l, w [nchunk] f32
+//   | rows' positions [16] i32 | side rows' own-key weights [16] f32
+//   | side rows' own keys / values [kMaxSide][dh] bf16 each
+// The combine reuses the region from K up to the end of the scratch arrays;
+// the tail after it survives the combine.
 struct Smem {
   bf16* K;
   bf16* V;
@@ -39,11 +43,21 @@ struct Smem {
   float* cm;
   float* cl;
   float* cw;
+  int* rpos;
+  float* sp;
+  bf16* SK;
+  bf16* SV;
 };
 
+__host__ __device__ inline size_t main_bytes(int dh, int nchunk) {
+  const size_t b = (size_t)kAttnChunk * dh * 2 + (size_t)kAttnChunk * dh * 2 +
+                   (size_t)kMaxRows * dh * 4 + (size_t)kMaxRows * kAttnChunk * 4 +
+                   (size_t)3 * nchunk * 4;
+  return (b + 15) & ~(size_t)15;
+}
+
 __host__ __device__ inline size_t smem_bytes(int dh, int nchunk) {
-  return (size_t)kAttnChunk * dh * 2 + (size_t)kAttnChunk * dh * 2 +
-         (size_t)kMaxRows * dh * 4 + (size_t)kMaxRows * kAttnChunk * 4 + (size_t)3 * nchunk * 4;
+  return main_bytes(dh, nchunk) + (size_t)kMaxRows * 4 * 2 + (size_t)kMaxSide * dh * 2 * 2;
 }
 
 SSD_DI Smem carve(unsigned char* raw, int dh, int nchunk) {
@@ -55,6 +69,10 @@ SSD_DI Smem carve(unsigned char* raw, int dh, int nchunk) {
   sm.cm = sm.S + kMaxRows * kAttnChunk;
   sm.cl = sm.cm + nchunk;
   sm.cw = sm.cl + nchunk;
+  sm.rpos = reinterpret_cast<int*>(raw + main_bytes(dh, nchunk));
+  sm.sp = reinterpret_cast<float*>(sm.rpos + kMaxRows);
+  sm.SK = reinterpret_cast<bf16*>(sm.sp + kMaxRows);
+  sm.SV = sm.SK + kMaxSide * dh;
   return sm;
 }
 
@@ -89,14 +107,23 @@ SSD_DI void issue(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, 
 // `bar` is an initialised mbarrier whose phase parity is tracked in `phase`;
 // `flag` is one shared int.  Returns true if this item combined its head
 // (the head's output is complete).
+//
+// Side rows (the pass's last ns rows, dynamic verification): row Mc + i sits
+// at position side_pos[i] <= the last chain position.  It sees the keys
+// before its position (cache and chain keys) and its own key, which stands
+// where the cache would hold it; its own value enters the chunk's output as
+// the last term, after the masked keys' exact zeros, so the row gets the
+// bits the same token would get as an ordinary row at that position.  Its
+// K/V go to its side slot, not to the cache.
 template <class Sync>
-SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, uint64_t* bar,
-                 uint32_t& phase, int* flag, int tid, Sync sync) {
+SSD_DI bool body(const AttnArgs& a, int M, int ns, int pos0, int item, const Smem& sm,
+                 uint64_t* bar, uint32_t& phase, int* flag, int tid, Sync sync) {
   const int dh = a.dh, half = dh / 2;
   const int G = a.H / a.Hkv;
   const int rows = G * kMaxRows;
   const int nchunk_max = a.max_seq / kAttnChunk;
-  const int last_pos = pos0 + M - 1;
+  const int Mc = M - ns;                    // chain rows
+  const int last_pos = pos0 + Mc - 1;
   const int n_active = last_pos / kAttnChunk + 1;
   const int warp = tid >> 5, lane = tid & 31;
   const int ld_out = a.H * dh;
@@ -106,6 +133,7 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
   const int p_end = min(p_begin + kAttnChunk, last_pos + 1);
   const int nk = p_end - p_begin;
   const int n_old = max(0, min(p_end, pos0) - p_begin);
+  if (tid < M) sm.rpos[tid] = tid < Mc ? pos0 + tid : __ldcg(a.side_pos + (tid - Mc));
   // (2) new keys of this chunk: RoPE, bf16, append to the cache
   const int first_new = max(p_begin, pos0);
   for (int e = tid; e < (p_end - first_new) * half; e += kGroupThreads) {
@@ -130,6 +158,34 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
     vd[i] = vb0;
     vd[i + half] = vb1;
   }
+  // (2') side rows whose position lies in this chunk: own key and value
+  // (same RoPE and rounding) to shared memory and to the side slot
+  if (ns > 0) {
+    const int side0 = __ldcg(a.side0);
+    for (int e = tid; e < ns * half; e += kGroupThreads) {
+      const int si = e / half, i = e % half;
+      const int pos = __ldcg(a.side_pos + si);
+      if (pos / kAttnChunk != c) continue;
+      const float* kr = a.qkv + (size_t)(Mc + si) * a.ld_qkv + (size_t)(a.H + kvh) * dh;
+      const float* vr = kr + (size_t)a.Hkv * dh;
+      const float2 cs = a.rope[(size_t)pos * half + i];
+      const float k0 = __ldcg(kr + i), k1 = __ldcg(kr + i + half);
+      const bf16 kb0 = __float2bfloat16_rn(k0 * cs.x - k1 * cs.y);
+      const bf16 kb1 = __float2bfloat16_rn(k0 * cs.y + k1 * cs.x);
+      const bf16 vb0 = __float2bfloat16_rn(__ldcg(vr + i));
+      const bf16 vb1 = __float2bfloat16_rn(__ldcg(vr + i + half));
+      sm.SK[si * dh + i] = kb0;
+      sm.SK[si * dh + i + half] = kb1;
+      sm.SV[si * dh + i] = vb0;
+      sm.SV[si * dh + i + half] = vb1;
+      bf16* kd = a.ks + ((size_t)kvh * kMaxSide + side0 + si) * dh;
+      bf16* vd = a.vs + ((size_t)kvh * kMaxSide + side0 + si) * dh;
+      kd[i] = kb0;
+      kd[i + half] = kb1;
+      vd[i] = vb0;
+      vd[i + half] = vb1;
+    }
+  }
   if (n_old > 0) {
     if (!mbar_wait(bar, phase & 1u)) {
       if (tid == 0) atomicExch(a.err, 1);
@@ -145,7 +201,7 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
     for (int e = tid; e < M * half; e += kGroupThreads) {
       const int i = e % half, m = e / half;
       const float* qr = a.qkv + (size_t)m * a.ld_qkv + (size_t)(kvh * G + gh) * dh;
-      const float2 cs = a.rope[(size_t)(pos0 + m) * half + i];
+      const float2 cs = a.rope[(size_t)sm.rpos[m] * half + i];
       const float q0 = __ldcg(qr + i), q1 = __ldcg(qr + i + half);
       float* qd = sm.Q + (size_t)m * dh;
       qd[i] = q0 * cs.x - q1 * cs.y;
@@ -174,12 +230,14 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
           qa1 = *reinterpret_cast<const float4*>(q + 64);
           qb1 = *reinterpret_cast<const float4*>(q + 68);
         }
+        const int pm = sm.rpos[m];
+        const bf16* own = sm.SK + (size_t)(m >= Mc ? m - Mc : 0) * dh + q8 * 8;  // side rows
         for (int kg = kg0; kg < kg0 + gpt; ++kg) {
           const int key = kg * 4 + ks;
-          const bool valid = key < nk && p_begin + key <= pos0 + m;
+          const bool valid = key < nk && p_begin + key <= pm;
           float acc = 0.f;
           if (valid) {
-            const bf16* k = sm.K + (size_t)key * dh + q8 * 8;
+            const bf16* k = m >= Mc && p_begin + key == pm ? own : sm.K + (size_t)key * dh + q8 * 8;
             acc = dot8(qa0, qb0, *reinterpret_cast<const uint4*>(k), acc);
             if (two) acc = dot8(qa1, qb1, *reinterpret_cast<const uint4*>(k + 64), acc);
           }
@@ -199,12 +257,19 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
       float mx = fmaxf(s0, s1);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      const float p0 = s0 == -INFINITY ? 0.f : expf(s0 - mx);
-      const float p1 = s1 == -INFINITY ? 0.f : expf(s1 - mx);
+      float p0 = s0 == -INFINITY ? 0.f : expf(s0 - mx);
+      float p1 = s1 == -INFINITY ? 0.f : expf(s1 - mx);
       float l = p0 + p1;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
       __syncwarp();
+      if (m >= Mc) {
+        // a side row's own-key weight is kept aside; its slot in the row's
+        // weights becomes an exact zero for the chain value there
+        const int jo = sm.rpos[m] - p_begin;
+        if (jo == lane) { sm.sp[m] = p0; p0 = 0.f; }
+        if (jo == lane + 32) { sm.sp[m] = p1; p1 = 0.f; }
+      }
       srow[lane] = p0;
       srow[lane + 32] = p1;
       if (lane == 0) {
@@ -234,6 +299,11 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
           o = fmaf(pp.w, __bfloat162float(vcol[(size_t)(j + 3) * dh]), o);
         }
         for (; j < nk; ++j) o = fmaf(p[j], __bfloat162float(vcol[(size_t)j * dh]), o);
+        if (m >= Mc) {
+          const int jo = sm.rpos[m] - p_begin;
+          if (jo >= 0 && jo < kAttnChunk)
+            o = fmaf(sm.sp[m], __bfloat162float(sm.SV[(size_t)(m - Mc) * dh + dd]), o);
+        }
         part_base[(size_t)(gh * kMaxRows + m) * (dh + kRecPad) + kRecPad + dd] = o;
       }
     } else {
@@ -278,8 +348,19 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
       }
 #pragma unroll
       for (int r = 0; r < kMaxRows / 4; ++r) {
+        const int m = rg + r * nrg;
+        if (r < nr && m >= Mc) {
+          const int jo = sm.rpos[m] - p_begin;
+          if (jo >= 0 && jo < kAttnChunk) {
+            const __nv_bfloat162 sv =
+                reinterpret_cast<const __nv_bfloat162*>(sm.SV + (size_t)(m - Mc) * dh)[cp];
+            const float2 v = __bfloat1622float2(sv);
+            o[r][0] = fmaf(sm.sp[m], v.x, o[r][0]);
+            o[r][1] = fmaf(sm.sp[m], v.y, o[r][1]);
+          }
+        }
         if (r < nr) {
-          const int rr = gh * kMaxRows + rg + r * nrg;
+          const int rr = gh * kMaxRows + m;
           *reinterpret_cast<float2*>(part_base + (size_t)rr * (dh + kRecPad) + kRecPad + 2 * cp) =
               make_float2(o[r][0], o[r][1]);
         }
@@ -307,11 +388,11 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
     float* CW = CL + R * n_active;
     float* LR = CW + R * n_active;
     const size_t need = ((size_t)3 * R * n_active + R) * sizeof(float);
-    if (need <= smem_bytes(dh, nchunk_max)) {
+    if (need <= main_bytes(dh, nchunk_max)) {
       for (int e = tid; e < R * n_active; e += kGroupThreads) {
         const int rr = e / n_active, cc = e % n_active;
         const int m = rr % M, r = (rr / M) * kMaxRows + m;
-        if (cc <= (pos0 + m) / kAttnChunk) {
+        if (cc <= sm.rpos[m] / kAttnChunk) {
           const float* pc = hb + ((size_t)cc * rows + r) * (dh + kRecPad);
           CM[e] = __ldcg(pc);
           CL[e] = __ldcg(pc + 1);
@@ -320,7 +401,7 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
       sync();
       for (int rr = tid; rr < R; rr += kGroupThreads) {
         const int m = rr % M;
-        const int nc = (pos0 + m) / kAttnChunk + 1;
+        const int nc = sm.rpos[m] / kAttnChunk + 1;
         const float* cm = CM + rr * n_active;
         float mx = -INFINITY;
         for (int cc = 0; cc < nc; ++cc) mx = fmaxf(mx, cm[cc]);
@@ -339,7 +420,7 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
       const size_t used = ((size_t)3 * R * n_active + R + 3) & ~(size_t)3;  // floats, 16 B aligned
       float* OB = CM + used;
       const size_t row_floats = (size_t)n_active * dh;
-      const int per_batch = (int)((smem_bytes(dh, nchunk_max) / sizeof(float) - used) / row_floats);
+      const int per_batch = (int)((main_bytes(dh, nchunk_max) / sizeof(float) - used) / row_floats);
       if (per_batch >= 1) {
         for (int r0 = 0; r0 < R; r0 += per_batch) {
           const int nb = min(per_batch, R - r0);
@@ -351,7 +432,7 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
             const int rb = rc / n_active, cc = rc % n_active;
             const int rr = r0 + rb;
             const int m = rr % M, r = (rr / M) * kMaxRows + m;
-            if (cc <= (pos0 + m) / kAttnChunk)
+            if (cc <= sm.rpos[m] / kAttnChunk)
               cp_async16(OB + (size_t)rb * row_floats + (size_t)cc * dh + 4 * q,
                          hb + cc * cs + (size_t)r * (dh + kRecPad) + kRecPad + 4 * q);
           }
@@ -361,7 +442,7 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
             const int rb = e / dh, dd = e % dh;
             const int rr = r0 + rb;
             const int m = rr % M, gh = rr / M;
-            const int nc = (pos0 + m) / kAttnChunk + 1;
+            const int nc = sm.rpos[m] / kAttnChunk + 1;
             const float* w = CW + rr * n_active;
             const float* ob = OB + (size_t)rb * row_floats + dd;
             float O = 0.f;
@@ -375,7 +456,7 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
         for (int e = tid; e < R * dh; e += kGroupThreads) {
           const int rr = e / dh, dd = e % dh;
           const int m = rr % M, gh = rr / M, r = gh * kMaxRows + m;
-          const int nc = (pos0 + m) / kAttnChunk + 1;
+          const int nc = sm.rpos[m] / kAttnChunk + 1;
           const float* w = CW + rr * n_active;
           const float* ob = hb + (size_t)r * (dh + kRecPad) + kRecPad + dd;
           float O = 0.f;
@@ -396,7 +477,7 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
     } else {
       for (int rr = 0; rr < R; ++rr) {
         const int m = rr % M, gh = rr / M, r = gh * kMaxRows + m;
-        const int nc = (pos0 + m) / kAttnChunk + 1;
+        const int nc = sm.rpos[m] / kAttnChunk + 1;
         for (int cc = tid; cc < nc; cc += kGroupThreads) {
           const float* pc = hb + ((size_t)cc * rows + r) * (dh + kRecPad);
           sm.cm[cc] = __ldcg(pc);
@@ -429,10 +510,10 @@ SSD_DI bool body(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, u
 
 // A whole work item: issue() then body().
 template <class Sync>
-SSD_DI bool item(const AttnArgs& a, int M, int pos0, int item, const Smem& sm, uint64_t* bar,
-                 uint32_t& phase, int* flag, int tid, Sync sync) {
-  issue(a, M, pos0, item, sm, bar, tid);
-  return body(a, M, pos0, item, sm, bar, phase, flag, tid, sync);
+SSD_DI bool item(const AttnArgs& a, int M, int ns, int pos0, int item, const Smem& sm,
+                 uint64_t* bar, uint32_t& phase, int* flag, int tid, Sync sync) {
+  issue(a, M - ns, pos0, item, sm, bar, tid);
+  return body(a, M, ns, pos0, item, sm, bar, phase, flag, tid, sync);
 }
 
 }  // namespace attn

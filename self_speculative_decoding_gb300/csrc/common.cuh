@@ -22,6 +22,9 @@ constexpr int kAttnChunk = 64;
 // Columns of the residual stream covered by one sum-of-squares partial (one
 // 16-row group of the producing projection).
 constexpr int kSsGroup = 16;
+// Dynamic verification (SWIFT §4.2): at most this many sibling candidates per
+// round, each a side row of the passes that carry it.
+constexpr int kMaxSide = 8;
 
 // Per-row logits summary (same layout as ssd_row_stats in ssd_ops.h).
 struct RowStats {
@@ -39,19 +42,28 @@ struct DevState {
   int32_t j;        // draft steps run in the current round
   int32_t d;        // draft tokens kept in the current round
   int32_t stop;     // the confidence stop fired in the current round
-  int32_t M;        // rows of the current pass
+  int32_t M;        // rows of the current pass (chain rows, then side rows)
   int32_t pos0;     // position of row 0 of the current pass
   int32_t slot;     // output slot of the current pass (draft step index)
   int32_t n_emitted;
   int32_t accepted;
   int32_t err;      // non-zero: a device-side wait gave up (its code)
-  int32_t pad[5];
+  int32_t ns;       // side rows of the current pass (its last ns rows)
+  int32_t side0;    // sibling index (side K/V slot) of the first side row
+  int32_t n_sib;    // siblings recorded in the current round
+  int32_t sib_acc;  // sibling taken by the last acceptance (-1: none)
+  int32_t sib_pos;  // its position
   int32_t in_tok[kMaxRows];
   int32_t draft_tok[kMaxRows];
   float draft_conf[kMaxRows];
   int32_t emitted[kMaxRows + 1];
-  int32_t pad2[15];
+  int32_t sib_depth[kMaxSide];  // sibling i stands for draft y_j, j = sib_depth[i] (position n + j)
+  int32_t sib_tok[kMaxSide];
+  int32_t side_pos[kMaxSide];   // positions of the current pass's side rows
+  int32_t pad2[7];
 };
+static_assert(sizeof(DevState) % 16 == 0, "DevState layout");
+
 
 // ---------------------------------------------------------------------------
 // loads / stores

@@ -4,6 +4,8 @@
 // that a captured CUDA graph of a draft step, a verify pass or an
 // autoregressive step can be replayed for every step without host-side
 // argument changes.
+#include <algorithm>
+
 #include "control_dev.cuh"
 
 namespace ssd {
@@ -14,23 +16,22 @@ constexpr int kBeginThreads = 512;
 constexpr int kAcceptThreads = 1024;
 
 __global__ void __launch_bounds__(kBeginThreads) begin_kernel(BeginArgs a) {
-  __shared__ int s_M, s_tok[kMaxRows];
+  __shared__ int s_M[2], s_tok[kMaxRows];
   pdl_wait();
   pdl_trigger();
-  ctl::begin(a, threadIdx.x, kBeginThreads, &s_M, s_tok, [] { __syncthreads(); });
+  ctl::begin(a, threadIdx.x, kBeginThreads, s_M, s_tok, [] { __syncthreads(); });
 }
 
-__global__ void save_boundary_kernel(DevState* st, int use_d, const float* x, const float* ss,
-                                     float* bx, float* bss, int D) {
+__global__ void save_boundary_kernel(SaveArgs a) {
   pdl_wait();
   pdl_trigger();
-  ctl::save_boundary(st, use_d, x, ss, bx, bss, D, threadIdx.x, blockDim.x);
+  ctl::save_boundary(a, threadIdx.x, blockDim.x, [] { __syncthreads(); });
 }
 
-__global__ void draft_end_kernel(DevState* st, const RowStats* dstats, float tau, float T) {
+__global__ void draft_end_kernel(DraftEndArgs a) {
   pdl_wait();
   pdl_trigger();
-  if (threadIdx.x == 0) ctl::draft_end(st, dstats, tau, T);
+  if (threadIdx.x == 0) ctl::draft_end(a);
 }
 
 __global__ void ar_end_kernel(DevState* st, int32_t* tokens, const RowStats* vstats,
@@ -41,20 +42,54 @@ __global__ void ar_end_kernel(DevState* st, int32_t* tokens, const RowStats* vst
 }
 
 // Greedy acceptance: the longest prefix of drafts matching the full
-// model's argmax, then the full model's token after it.
+// model's argmax, then the full model's token after it.  Dynamic
+// verification (SWIFT §4.2): when draft y_a is rejected and a sibling
+// candidate at depth a is the full model's token there, the sibling is
+// taken and the full model's token after it (its own verify row) is
+// emitted as well.
 __global__ void accept_greedy_kernel(DevState* st, int32_t* tokens, const RowStats* vstats) {
   pdl_wait();
   pdl_trigger();
-  const int d = st->d, n = st->n;
+  if (threadIdx.x != 0) return;
+  const int d = st->d, n = st->n, ns = st->n_sib;
   int a = 0;
   while (a < d && st->draft_tok[a] == vstats[a].top1) ++a;
   for (int i = 0; i < a; ++i) st->emitted[i] = st->draft_tok[i];
-  st->emitted[a] = vstats[a].top1;
-  for (int i = 0; i <= a; ++i) tokens[n + i] = st->emitted[i];
-  st->n = n + a + 1;
-  st->n_emitted = a + 1;
+  const int t = vstats[a].top1;
+  st->emitted[a] = t;
+  int sib = -1;
+  if (a < d)
+    for (int i = 0; i < ns; ++i)
+      if (st->sib_depth[i] == a && st->sib_tok[i] == t) sib = i;
+  int ne = a + 1;
+  if (sib >= 0) st->emitted[ne++] = vstats[d + 1 + sib].top1;
+  for (int i = 0; i < ne; ++i) tokens[n + i] = st->emitted[i];
+  st->n = n + ne;
+  st->n_emitted = ne;
   st->accepted = a;
+  st->sib_acc = sib;
+  st->sib_pos = n + a;
   st->j = st->d = st->stop = 0;
+}
+
+// The taken sibling's K/V rows (every layer and KV head) into the cache at
+// its position; 16-byte pieces, grid-stride.
+__global__ void side_commit_kernel(const DevState* st, bf16* kc, bf16* vc, const bf16* ks,
+                                   const bf16* vs, int L, int Hkv, int max_seq, int dh) {
+  pdl_wait();
+  pdl_trigger();
+  const int sib = __ldcg(&st->sib_acc);
+  if (sib < 0) return;
+  const int pos = __ldcg(&st->sib_pos);
+  const int per_row = dh / 8;                       // 16-byte pieces per row
+  const int total = 2 * L * Hkv * per_row;
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += gridDim.x * blockDim.x) {
+    const int q = e % per_row, r = e / per_row;     // r = (kv, l, h)
+    const int lh = r % (L * Hkv), kv = r / (L * Hkv);
+    const bf16* src = (kv ? vs : ks) + ((size_t)lh * kMaxSide + sib) * dh + 8 * q;
+    bf16* dst = (kv ? vc : kc) + ((size_t)lh * max_seq + pos) * dh + 8 * q;
+    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+  }
 }
 
 // ---- stochastic acceptance (LayerSkip blog §3.3) ---------------------------
@@ -255,18 +290,26 @@ cudaError_t launch_begin(const BeginArgs& a, cudaStream_t s, bool pdl) {
   return cudaLaunchKernelEx(&lc, begin_kernel, a);
 }
 
-cudaError_t launch_save_boundary(DevState* st, int use_d, const float* x, const float* ss,
-                                 float* bx, float* bss, int D, cudaStream_t s, bool pdl) {
+cudaError_t launch_save_boundary(const SaveArgs& a, cudaStream_t s, bool pdl) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t lc = make_cfg(1, 512, s, pdl, attr);
-  return cudaLaunchKernelEx(&lc, save_boundary_kernel, st, use_d, x, ss, bx, bss, D);
+  return cudaLaunchKernelEx(&lc, save_boundary_kernel, a);
 }
 
-cudaError_t launch_draft_end(DevState* st, const RowStats* dstats, float tau, float temperature,
-                             cudaStream_t s, bool pdl) {
+cudaError_t launch_draft_end(const DraftEndArgs& a, cudaStream_t s, bool pdl) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t lc = make_cfg(1, 32, s, pdl, attr);
-  return cudaLaunchKernelEx(&lc, draft_end_kernel, st, dstats, tau, temperature);
+  return cudaLaunchKernelEx(&lc, draft_end_kernel, a);
+}
+
+cudaError_t launch_side_commit(const DevState* st, bf16* kc, bf16* vc, const bf16* ks,
+                               const bf16* vs, int L, int Hkv, int max_seq, int dh,
+                               cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute attr[1];
+  const int total = 2 * L * Hkv * (dh / 8);
+  const int grid = std::min(152, std::max(1, (total + 255) / 256));
+  cudaLaunchConfig_t lc = make_cfg(grid, 256, s, pdl, attr);
+  return cudaLaunchKernelEx(&lc, side_commit_kernel, st, kc, vc, ks, vs, L, Hkv, max_seq, dh);
 }
 
 cudaError_t launch_ar_end(DevState* st, int32_t* tokens, const RowStats* vstats, int row_from_M,

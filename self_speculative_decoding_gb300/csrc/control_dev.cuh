@@ -12,12 +12,12 @@ namespace ctl {
 // Embedding (or boundary copy) of the pass's rows, with the sum-of-squares
 // partials of every 16-column group (the same order the projection
 // epilogues use: ascending columns from zero).  Threads tid < nthr of one
-// CTA; s_M / s_tok are shared scratch; sync() is their barrier.
+// CTA; s_M (two ints) / s_tok are shared scratch; sync() is their barrier.
 template <class Sync>
 SSD_DI void begin(const BeginArgs& a, int tid, int nthr, int* s_M, int* s_tok, Sync sync) {
   DevState* st = a.st;
   if (tid == 0) {
-    int M = 1, pos0 = 0, slot = 0;
+    int M = 1, pos0 = 0, slot = 0, ns = 0, side0 = 0;
     switch (a.mode) {
       case BEGIN_TOKENS:
         M = a.M;
@@ -26,6 +26,7 @@ SSD_DI void begin(const BeginArgs& a, int tid, int nthr, int* s_M, int* s_tok, S
         if (a.reset_round) {
           st->round = 0;
           st->j = st->d = st->stop = 0;
+          st->n_sib = 0;
         }
         break;
       case BEGIN_AR:
@@ -34,32 +35,59 @@ SSD_DI void begin(const BeginArgs& a, int tid, int nthr, int* s_M, int* s_tok, S
         s_tok[0] = a.tokens[st->n - 1];
         break;
       case BEGIN_DRAFT:
-        if (st->j == 0) st->round += 1;
-        pos0 = st->n - 1 + st->j;
-        s_tok[0] = st->j == 0 ? a.tokens[st->n - 1] : st->draft_tok[st->j - 1];
-        slot = st->j;
+      case BEGIN_EXTRA: {
+        // draft step j feeds y_{j-1} (the pending token at j = 0); the extra
+        // pass feeds y_{d-1}.  A sibling recorded for that draft rides along
+        // as a side row at the same position.
+        int fed;
+        if (a.mode == BEGIN_DRAFT) {
+          if (st->j == 0) {
+            st->round += 1;
+            st->n_sib = 0;
+          }
+          fed = st->j - 1;
+          slot = st->j;
+        } else {
+          fed = st->d - 1;
+        }
+        pos0 = st->n + fed;
+        s_tok[0] = fed < 0 ? a.tokens[st->n - 1] : st->draft_tok[fed];
+        const int k = st->n_sib - 1;
+        if (fed >= 0 && k >= 0 && st->sib_depth[k] == fed) {
+          M = 2;
+          ns = 1;
+          side0 = k;
+          s_tok[1] = st->sib_tok[k];
+          st->side_pos[0] = pos0;
+        }
         break;
-      case BEGIN_EXTRA:
-        pos0 = st->n - 1 + st->d;
-        s_tok[0] = st->d > 0 ? st->draft_tok[st->d - 1] : a.tokens[st->n - 1];
-        break;
+      }
       case BEGIN_VERIFY:
-        M = st->d + 1;
+        // chain rows n-1 .. n-1+d, then every sibling at its own position
+        ns = st->n_sib;
+        M = st->d + 1 + ns;
         pos0 = st->n - 1;
+        for (int i = 0; i < ns; ++i) st->side_pos[i] = st->n + st->sib_depth[i];
         break;
     }
     st->M = M;
     st->pos0 = pos0;
     st->slot = slot;
+    st->ns = ns;
+    st->side0 = side0;
     if (a.mode != BEGIN_VERIFY)
       for (int m = 0; m < M; ++m) st->in_tok[m] = s_tok[m];
-    *s_M = M;
+    s_M[0] = M;
+    s_M[1] = ns;
   }
   sync();
-  const int M = *s_M, D = a.D, NP = D / kSsGroup;
+  const int M = s_M[0], D = a.D, NP = D / kSsGroup;
   if (a.mode == BEGIN_VERIFY) {
-    for (int e = tid; e < M * D; e += nthr) a.x[e] = __ldcg(a.bx + e);
-    for (int e = tid; e < M * NP; e += nthr) a.ss[e] = __ldcg(a.bss + e);
+    const int mc = M - s_M[1];
+    for (int e = tid; e < mc * D; e += nthr) a.x[e] = __ldcg(a.bx + e);
+    for (int e = tid; e < mc * NP; e += nthr) a.ss[e] = __ldcg(a.bss + e);
+    for (int e = tid; e < (M - mc) * D; e += nthr) a.x[mc * D + e] = __ldcg(a.bxs + e);
+    for (int e = tid; e < (M - mc) * NP; e += nthr) a.ss[mc * NP + e] = __ldcg(a.bsss + e);
     return;
   }
   for (int e = tid; e < M * NP; e += nthr) {
@@ -76,14 +104,26 @@ SSD_DI void begin(const BeginArgs& a, int tid, int nthr, int* s_M, int* s_tok, S
   }
 }
 
-// Copy row 0 of the residual (and its partials) into boundary slot j
-// (draft step) or d (extra pass).
-SSD_DI void save_boundary(DevState* st, int use_d, const float* x, const float* ss, float* bx,
-                          float* bss, int D, int tid, int nthr) {
-  const int slot = use_d ? st->d : st->j;
-  const int NP = D / kSsGroup;
-  for (int e = tid; e < D; e += nthr) bx[(size_t)slot * D + e] = __ldcg(x + e);
-  for (int e = tid; e < NP; e += nthr) bss[(size_t)slot * NP + e] = __ldcg(ss + e);
+// Copy row 0 of the residual (and its partials) into boundary slot j (draft
+// step) or d (extra pass), and a side row into the siblings' boundary slot
+// of its sibling index; the rest of the pass runs the chain row alone.
+template <class Sync>
+SSD_DI void save_boundary(const SaveArgs& a, int tid, int nthr, Sync sync) {
+  DevState* st = a.st;
+  const int slot = a.use_d ? __ldcg(&st->d) : __ldcg(&st->j);
+  const int ns = __ldcg(&st->ns), side0 = __ldcg(&st->side0);
+  const int D = a.D, NP = D / kSsGroup;
+  for (int e = tid; e < D; e += nthr) a.bx[(size_t)slot * D + e] = __ldcg(a.x + e);
+  for (int e = tid; e < NP; e += nthr) a.bss[(size_t)slot * NP + e] = __ldcg(a.ss + e);
+  if (ns > 0) {
+    for (int e = tid; e < D; e += nthr) a.bxs[(size_t)side0 * D + e] = __ldcg(a.x + D + e);
+    for (int e = tid; e < NP; e += nthr) a.bsss[(size_t)side0 * NP + e] = __ldcg(a.ss + NP + e);
+  }
+  sync();  // every thread has read ns before it is cleared
+  if (tid == 0 && ns > 0) {
+    st->M = 1;
+    st->ns = 0;
+  }
 }
 
 SSD_DI RowStats load_stats(const RowStats* p) {
@@ -98,16 +138,26 @@ SSD_DI RowStats load_stats(const RowStats* p) {
 }
 
 // SWIFT §4.2 confidence-aware stop: the draft token of step j is kept only
-// if its top-1 probability reaches tau.  One thread.
-SSD_DI void draft_end(DevState* st, const RowStats* dstats, float tau, float T) {
+// if its top-1 probability reaches tau.  Dynamic verification (greedy): a
+// kept draft whose top-1 probability is below tree_tau also gets the
+// draft's second choice as a sibling candidate, up to tree_max per round.
+// One thread.
+SSD_DI void draft_end(const DraftEndArgs& a) {
+  DevState* st = a.st;
   const int j = st->j;
-  const RowStats rs = load_stats(dstats + j);
+  const RowStats rs = load_stats(a.dstats + j);
   st->draft_conf[j] = rs.conf;
-  if (rs.conf < tau) {
+  if (rs.conf < a.tau) {
     st->stop = 1;
   } else {
-    st->draft_tok[j] = T > 0.f ? rs.sample : rs.top1;
+    st->draft_tok[j] = a.temperature > 0.f ? rs.sample : rs.top1;
     st->d = j + 1;
+    const int k = st->n_sib;
+    if (rs.conf < a.tree_tau && k < a.tree_max) {
+      st->sib_depth[k] = j;
+      st->sib_tok[k] = rs.top2;
+      st->n_sib = k + 1;
+    }
   }
   st->j = j + 1;
 }

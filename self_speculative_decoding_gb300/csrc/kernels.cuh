@@ -88,6 +88,16 @@ struct AttnArgs {
   unsigned* counters = nullptr;  // [Hkv]
   int* err = nullptr;          // set to 1 if a bulk copy never completed
   float scale = 1.f;
+  // Side rows (dynamic verification): the pass's last *ns_dev rows are
+  // sibling candidates at positions side_pos[i] (not pos0 + m).  A side row
+  // attends to the cache and chain keys before its position plus its own
+  // key; its K/V go to side slot side0 + i of this layer instead of the
+  // cache.  ns_dev NULL: no side rows.
+  const int32_t* ns_dev = nullptr;
+  const int32_t* side_pos = nullptr;  // [kMaxSide]
+  const int32_t* side0 = nullptr;
+  bf16* ks = nullptr;                 // [Hkv][kMaxSide][dh]
+  bf16* vs = nullptr;
 };
 
 int attn_grid(const AttnArgs& a);
@@ -118,20 +128,47 @@ struct BeginArgs {
   float* ss = nullptr;               // [16][D/16]
   const float* bx = nullptr;         // boundary states [16][D] (BEGIN_VERIFY)
   const float* bss = nullptr;
+  const float* bxs = nullptr;        // siblings' boundary states [kMaxSide][D]
+  const float* bsss = nullptr;
 };
 cudaError_t launch_begin(const BeginArgs& a, cudaStream_t st, bool pdl);
 
-// Copy row 0 of the residual (and its partials) into boundary slot j
-// (draft) or d (extra pass).
-cudaError_t launch_save_boundary(DevState* st, int use_d, const float* x, const float* ss,
-                                 float* bx, float* bss, int D, cudaStream_t s, bool pdl);
+// Boundary buffers of the draft / extra passes: the chain row's state goes
+// to bx slot j (draft) or d (extra pass), a side row's to bxs at its sibling
+// index; the pass then continues with the chain row alone.
+struct SaveArgs {
+  DevState* st = nullptr;
+  int use_d = 0;
+  const float* x = nullptr;
+  const float* ss = nullptr;
+  float* bx = nullptr;
+  float* bss = nullptr;
+  float* bxs = nullptr;
+  float* bsss = nullptr;
+  int D = 0;
+};
+cudaError_t launch_save_boundary(const SaveArgs& a, cudaStream_t s, bool pdl);
 
-cudaError_t launch_draft_end(DevState* st, const RowStats* dstats, float tau, float temperature,
-                             cudaStream_t s, bool pdl);
+// Draft-step control: the confidence stop (tau) and, for dynamic
+// verification, the sibling rule (tree_tau, tree_max).
+struct DraftEndArgs {
+  DevState* st = nullptr;
+  const RowStats* dstats = nullptr;
+  float tau = 0.f, temperature = 0.f;
+  float tree_tau = 0.f;
+  int tree_max = 0;
+};
+cudaError_t launch_draft_end(const DraftEndArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_ar_end(DevState* st, int32_t* tokens, const RowStats* vstats, int row_from_M,
                           float temperature, int reset, cudaStream_t s, bool pdl);
 cudaError_t launch_accept_greedy(DevState* st, int32_t* tokens, const RowStats* vstats,
                                  cudaStream_t s, bool pdl);
+// After a greedy acceptance that took a sibling: its K/V of every layer
+// (side slot sib_acc) into the cache at sib_pos.  kc / vc [L][Hkv][max_seq][dh],
+// ks / vs [L][Hkv][kMaxSide][dh].  No-op when no sibling was taken.
+cudaError_t launch_side_commit(const DevState* st, bf16* kc, bf16* vc, const bf16* ks,
+                               const bf16* vs, int L, int Hkv, int max_seq, int dh,
+                               cudaStream_t s, bool pdl);
 
 struct AcceptArgs {
   const float* P = nullptr;       // [d+1][V]
@@ -166,6 +203,8 @@ struct PassPhase {
   unsigned target = 1;                // completions that finish the phase
   int use_d = 0;                      // PK_SAVE: boundary slot d (extra pass) or j
   float tau = 0.f, temperature = 0.f; // PK_DRAFT_END / PK_AR_END
+  float tree_tau = 0.f;               // PK_DRAFT_END: sibling rule
+  int tree_max = 0;
   int row_from_M = 0, reset = 0;      // PK_AR_END
 };
 
@@ -183,6 +222,8 @@ struct PassProg {
   const float* ss = nullptr;
   float* bx = nullptr;
   float* bss = nullptr;
+  float* bxs = nullptr;
+  float* bsss = nullptr;
   int D = 0;
   unsigned* done = nullptr;           // [n], zero between launches
   unsigned* exit_count = nullptr;     // zero between launches

@@ -36,7 +36,7 @@ struct __align__(16) PassSmem {
   int flag;        // attention: this item combined its head
   int epoch;       // last phase this CTA has seen complete
   int epoch_ok;
-  int s_M;
+  int s_M[2];
   int s_tok[kMaxRows];
 };
 
@@ -215,27 +215,47 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) pass_kernel(PassProg P) 
       } else if (ph.kind == PK_ATTN) {
         const AttnArgs& a = P.att[ph.idx];
         const int M = __ldcg(&P.st->M), pos0 = __ldcg(&P.st->pos0);
+        const int ns = a.ns_dev ? __ldcg(a.ns_dev) : 0;
         const attn::Smem asm_ = attn::carve(reinterpret_cast<unsigned char*>(sm.stage), a.dh,
                                             a.max_seq / kAttnChunk);
         // the staging area was last written through the generic proxy
         fence_proxy_async_smem();
         consumer_sync();
-        const int n_items = ((pos0 + M - 1) / kAttnChunk + 1) * a.Hkv;
+        const int n_items = ((pos0 + M - ns - 1) / kAttnChunk + 1) * a.Hkv;
         for (int it = b; it < n_items; it += gridDim.x) {
-          const bool fin = attn::item(a, M, pos0, it, asm_, &S.abar, aphase, &S.flag, tid,
+          const bool fin = attn::item(a, M, ns, pos0, it, asm_, &S.abar, aphase, &S.flag, tid,
                                       [] { consumer_sync(); });
           if (fin && tid == 0) signal(P, k);
         }
       } else if (b == 0) {
         if (ph.kind == PK_BEGIN) {
-          ctl::begin(P.beg[ph.idx], tid, kConsumers * 32, &S.s_M, S.s_tok,
+          ctl::begin(P.beg[ph.idx], tid, kConsumers * 32, S.s_M, S.s_tok,
                      [] { consumer_sync(); });
           consumer_sync();
         } else if (ph.kind == PK_SAVE) {
-          ctl::save_boundary(P.st, ph.use_d, P.x, P.ss, P.bx, P.bss, P.D, tid, kConsumers * 32);
+          SaveArgs sa;
+          sa.st = P.st;
+          sa.use_d = ph.use_d;
+          sa.x = P.x;
+          sa.ss = P.ss;
+          sa.bx = P.bx;
+          sa.bss = P.bss;
+          sa.bxs = P.bxs;
+          sa.bsss = P.bsss;
+          sa.D = P.D;
+          ctl::save_boundary(sa, tid, kConsumers * 32, [] { consumer_sync(); });
           consumer_sync();
         } else if (ph.kind == PK_DRAFT_END) {
-          if (tid == 0) ctl::draft_end(P.st, P.dstats, ph.tau, ph.temperature);
+          if (tid == 0) {
+            DraftEndArgs da;
+            da.st = P.st;
+            da.dstats = P.dstats;
+            da.tau = ph.tau;
+            da.temperature = ph.temperature;
+            da.tree_tau = ph.tree_tau;
+            da.tree_max = ph.tree_max;
+            ctl::draft_end(da);
+          }
         } else if (ph.kind == PK_AR_END) {
           if (tid == 0)
             ctl::ar_end(P.st, P.tokens, P.vstats, ph.row_from_M, ph.temperature, ph.reset);

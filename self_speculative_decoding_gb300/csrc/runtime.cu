@@ -83,6 +83,12 @@ struct ssd_ctx {
   float* ss = nullptr;
   float* bx = nullptr;
   float* bss = nullptr;
+  // dynamic verification: the siblings' boundary states [kMaxSide][D] and
+  // side K/V slots [L][Hkv][kMaxSide][dh]
+  float* bxs = nullptr;
+  float* bsss = nullptr;
+  bf16* ks = nullptr;
+  bf16* vs = nullptr;
   float* qkv = nullptr;
   bf16* attn = nullptr;
   bf16* u = nullptr;
@@ -297,6 +303,11 @@ AttnArgs attn_args(ssd_ctx* c, int l) {
   a.counters = c->attn_cnt;
   a.err = &c->st->err;
   a.scale = (float)(1.0 / std::sqrt((double)g.head_dim));
+  a.ns_dev = &c->st->ns;
+  a.side_pos = c->st->side_pos;
+  a.side0 = &c->st->side0;
+  a.ks = c->ks + (size_t)l * g.n_kv_heads * kMaxSide * g.head_dim;
+  a.vs = c->vs + (size_t)l * g.n_kv_heads * kMaxSide * g.head_dim;
   return a;
 }
 
@@ -388,7 +399,37 @@ BeginArgs begin_args(ssd_ctx* c, int mode, int M, int pos0, const int32_t* toks_
   b.ss = c->ss;
   b.bx = c->bx;
   b.bss = c->bss;
+  b.bxs = c->bxs;
+  b.bsss = c->bsss;
   return b;
+}
+
+// Dynamic verification is on: siblings ride in the draft / extra passes.
+bool tree_on(const ssd_ctx* c) { return c->pol.tree_tau > 0.f && c->pol.tree_max > 0; }
+
+SaveArgs save_args(ssd_ctx* c, int use_d) {
+  SaveArgs a;
+  a.st = c->st;
+  a.use_d = use_d;
+  a.x = c->x;
+  a.ss = c->ss;
+  a.bx = c->bx;
+  a.bss = c->bss;
+  a.bxs = c->bxs;
+  a.bsss = c->bsss;
+  a.D = c->cfg.d_model;
+  return a;
+}
+
+DraftEndArgs draft_end_args(ssd_ctx* c) {
+  DraftEndArgs a;
+  a.st = c->st;
+  a.dstats = c->dstats;
+  a.tau = c->pol.tau;
+  a.temperature = c->pol.temperature;
+  a.tree_tau = tree_on(c) ? c->pol.tree_tau : 0.f;
+  a.tree_max = tree_on(c) ? c->pol.tree_max : 0;
+  return a;
 }
 
 // A norm-fused projection of a pass whose rows may not fit the GEMV's
@@ -544,6 +585,8 @@ ssd_status pass_upload(ssd_ctx* c, const PassBuilder& B, PassDev& d) {
   P.ss = c->ss;
   P.bx = c->bx;
   P.bss = c->bss;
+  P.bxs = c->bxs;
+  P.bsss = c->bsss;
   P.D = c->cfg.d_model;
   P.err = &c->st->err;
   return SSD_OK;
@@ -563,8 +606,11 @@ ssd_status build_pass_programs(ssd_ctx* c) {
     B.gemv(IN_NORM, EPI_LMHEAD, lm_args(c, c->dstats, c->dlogits, &c->st->slot, 0), 1u);
     PassPhase de;
     de.kind = PK_DRAFT_END;
-    de.tau = c->pol.tau;
-    de.temperature = c->pol.temperature;
+    const DraftEndArgs da = draft_end_args(c);
+    de.tau = da.tau;
+    de.temperature = da.temperature;
+    de.tree_tau = da.tree_tau;
+    de.tree_max = da.tree_max;
     B.control(de);
     if ((r = pass_upload(c, B, c->p_draft)) != SSD_OK) return r;
   }
@@ -634,7 +680,7 @@ ssd_status build_graph(ssd_ctx* c, Graph& g, Builder fn) {
 
 ssd_status b_draft_body(ssd_ctx* c, cudaStream_t s);
 ssd_status b_draft(ssd_ctx* c, cudaStream_t s) {
-  c->mmax = 1;
+  c->mmax = tree_on(c) ? 2 : 1;
   const ssd_status r = b_draft_body(c, s);
   c->mmax = 0;
   return r;
@@ -644,18 +690,16 @@ ssd_status b_draft_body(ssd_ctx* c, cudaStream_t s) {
   ssd_status r;
   if ((r = enq_begin(c, BEGIN_DRAFT, s)) != SSD_OK) return r;
   if ((r = enq_layers(c, c->pre, s)) != SSD_OK) return r;
-  if ((r = note(c, launch_save_boundary(c->st, 0, c->x, c->ss, c->bx, c->bss, c->cfg.d_model, s,
-                                        c->pdl), "save_boundary")) != SSD_OK)
+  if ((r = note(c, launch_save_boundary(save_args(c, 0), s, c->pdl), "save_boundary")) != SSD_OK)
     return r;
   if ((r = enq_layers(c, c->post, s, &c->post_parts)) != SSD_OK) return r;
   if ((r = enq_lmhead(c, c->dstats, c->dlogits, &c->st->slot, 0, s)) != SSD_OK) return r;
-  return note(c, launch_draft_end(c->st, c->dstats, c->pol.tau, c->pol.temperature, s, c->pdl),
-              "draft_end");
+  return note(c, launch_draft_end(draft_end_args(c), s, c->pdl), "draft_end");
 }
 
 ssd_status b_extra_body(ssd_ctx* c, cudaStream_t s);
 ssd_status b_extra(ssd_ctx* c, cudaStream_t s) {
-  c->mmax = 1;
+  c->mmax = tree_on(c) ? 2 : 1;
   const ssd_status r = b_extra_body(c, s);
   c->mmax = 0;
   return r;
@@ -665,15 +709,18 @@ ssd_status b_extra_body(ssd_ctx* c, cudaStream_t s) {
   ssd_status r;
   if ((r = enq_begin(c, BEGIN_EXTRA, s)) != SSD_OK) return r;
   if ((r = enq_layers(c, c->pre, s)) != SSD_OK) return r;
-  return note(c, launch_save_boundary(c->st, 1, c->x, c->ss, c->bx, c->bss, c->cfg.d_model, s,
-                                      c->pdl), "save_boundary");
+  return note(c, launch_save_boundary(save_args(c, 1), s, c->pdl), "save_boundary");
 }
 
 ssd_status b_verify_body(ssd_ctx* c, cudaStream_t s);
 // Rows the verify graphs are built for: the narrow one up to what the stage
-// holds at d_model, the wide one up to d_max + 1.
+// holds at d_model, the wide one up to d_max + 1 chain rows plus the
+// siblings of dynamic verification.
+int verify_max_rows(const ssd_ctx* c) {
+  return c->pol.d_max + 1 + (tree_on(c) ? c->pol.tree_max : 0);
+}
 int verify_narrow_rows(const ssd_ctx* c) {
-  return std::min(c->pol.d_max + 1, std::max(1, gemv_stage_rows(c->cfg.d_model)));
+  return std::min(verify_max_rows(c), std::max(1, gemv_stage_rows(c->cfg.d_model)));
 }
 ssd_status b_verify(ssd_ctx* c, cudaStream_t s) {
   c->mmax = verify_narrow_rows(c);
@@ -682,7 +729,7 @@ ssd_status b_verify(ssd_ctx* c, cudaStream_t s) {
   return r;
 }
 ssd_status b_verify_wide(ssd_ctx* c, cudaStream_t s) {
-  c->mmax = c->pol.d_max + 1;
+  c->mmax = verify_max_rows(c);
   const ssd_status r = b_verify_body(c, s);
   c->mmax = 0;
   return r;
@@ -709,7 +756,12 @@ ssd_status b_accept(ssd_ctx* c, cudaStream_t s) {
     a.tokens = c->tokens;
     return note(c, launch_accept_stochastic(a, s, c->pdl), "accept");
   }
-  return note(c, launch_accept_greedy(c->st, c->tokens, c->vstats, s, c->pdl), "accept");
+  ssd_status r = note(c, launch_accept_greedy(c->st, c->tokens, c->vstats, s, c->pdl), "accept");
+  if (r != SSD_OK || !tree_on(c)) return r;
+  const ssd_config& g = c->cfg;
+  return note(c, launch_side_commit(c->st, c->kc, c->vc, c->ks, c->vs, g.n_layers, g.n_kv_heads,
+                                    g.max_seq, g.head_dim, s, c->pdl),
+              "side_commit");
 }
 
 ssd_status b_ar_body(ssd_ctx* c, cudaStream_t s);
@@ -752,7 +804,7 @@ ssd_status build_graphs_once(ssd_ctx* c) {
   if ((r = build_graph(c, c->g_extra, b_extra)) != SSD_OK) return r;
   if ((r = build_graph(c, c->g_verify, b_verify)) != SSD_OK) return r;
   c->g_verify_wide.reset();
-  if (verify_narrow_rows(c) < c->pol.d_max + 1 &&
+  if (verify_narrow_rows(c) < verify_max_rows(c) &&
       (r = build_graph(c, c->g_verify_wide, b_verify_wide)) != SSD_OK)
     return r;
   if ((r = build_graph(c, c->g_accept, b_accept)) != SSD_OK) return r;
@@ -837,16 +889,17 @@ ssd_status run_draft(ssd_ctx* c, ssd_stats* stats) {
 ssd_status run_verify(ssd_ctx* c, ssd_stats* stats) {
   Range nv("ssd verify");
   ssd_status r;
-  const int n = c->h_st->n, d = c->h_st->d;
+  const int n = c->h_st->n, d = c->h_st->d, nsib = c->h_st->n_sib;
   if (stats) CK(cudaEventRecord(c->t0, c->stream));
   const bool extra = !c->h_st->stop;
   if (extra) {
     if ((r = replay(c, c->g_extra)) != SSD_OK) return r;
     if (stats) stats->bytes_streamed += pass_bytes(c, (int)c->pre.size(), false, n - 1 + d, 1);
   }
-  const bool wide = d + 1 > verify_narrow_rows(c) && c->g_verify_wide.exec;
+  const bool wide = d + 1 + nsib > verify_narrow_rows(c) && c->g_verify_wide.exec;
   if ((r = replay(c, wide ? c->g_verify_wide : c->g_verify)) != SSD_OK) return r;
-  if (stats) stats->bytes_streamed += pass_bytes(c, (int)c->verify_layers.size(), true, n - 1, d + 1);
+  if (stats)
+    stats->bytes_streamed += pass_bytes(c, (int)c->verify_layers.size(), true, n - 1, d + 1 + nsib);
   c->phase = PH_VERIFIED;
   return SSD_OK;
 }
@@ -1115,6 +1168,10 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
             alloc((void**)&c->ss, (size_t)nr * (D / kSsGroup) * 4) &&
             alloc((void**)&c->bx, (size_t)nr * D * 4) &&
             alloc((void**)&c->bss, (size_t)nr * (D / kSsGroup) * 4) &&
+            alloc((void**)&c->bxs, (size_t)kMaxSide * D * 4) &&
+            alloc((void**)&c->bsss, (size_t)kMaxSide * (D / kSsGroup) * 4) &&
+            alloc((void**)&c->ks, (size_t)g.n_layers * g.n_kv_heads * kMaxSide * g.head_dim * 2) &&
+            alloc((void**)&c->vs, (size_t)g.n_layers * g.n_kv_heads * kMaxSide * g.head_dim * 2) &&
             alloc((void**)&c->qkv, (size_t)nr * qkv_rows(g) * 4) &&
             alloc((void**)&c->attn, (size_t)nr * g.n_heads * g.head_dim * 2) &&
             alloc((void**)&c->u, (size_t)nr * F * 2) &&
@@ -1215,7 +1272,8 @@ ssd_status ssd_destroy(ssd_ctx* c) {
   c->p_ar.reset();
   void* bufs[] = {c->kc, c->vc, c->x, c->ss, c->bx, c->bss, c->qkv, c->attn, c->u, c->xn, c->rope,
                   c->attn_part, c->attn_cnt, c->g_part, c->g_cnt, c->g_rec, c->dstats, c->vstats,
-                  c->dlogits, c->vlogits, c->tokens, c->toks_in, c->st, c->fstats, c->ffeat};
+                  c->dlogits, c->vlogits, c->tokens, c->toks_in, c->st, c->fstats, c->ffeat,
+                  c->bxs, c->bsss, c->ks, c->vs};
   for (void* p : bufs)
     if (p) cudaFree(p);
   void* sc[] = {c->sc_x,    c->sc_xn,   c->sc_qkv,  c->sc_q,   c->sc_sk,  c->sc_sv,
@@ -1257,6 +1315,15 @@ ssd_status ssd_set_policy(ssd_ctx* c, const ssd_policy* p) {
     for (int w = 0; w < 4; ++w)
       if (p->skip_attn_mask[w] || p->skip_mlp_mask[w])
         return fail(c, SSD_ERR_INVALID_ARG, "sublayer masks need skip mode");
+  if (!std::isfinite(p->tree_tau)) return fail(c, SSD_ERR_INVALID_ARG, "tree_tau");
+  if (p->tree_tau > 0.f) {
+    if (p->temperature != 0.f)
+      return fail(c, SSD_ERR_INVALID_ARG, "dynamic verification (tree_tau > 0) needs temperature 0");
+    if (p->tree_max < 1 || p->tree_max > kMaxSide)
+      return fail(c, SSD_ERR_INVALID_ARG, "tree_max must be 1..8 when tree_tau > 0");
+    if (p->d_max + 1 + p->tree_max > kMaxRows)
+      return fail(c, SSD_ERR_INVALID_ARG, "d_max + 1 + tree_max exceeds 16 verify rows");
+  }
   c->pol = *p;
   c->pre.clear();
   c->post.clear();
@@ -1406,6 +1473,10 @@ ssd_status ssd_generate(ssd_ctx* c, int32_t n_tokens, int32_t* out, ssd_stats* s
       stats->drafted += d;
       stats->accepted += c->h_st->accepted;
       stats->emitted += ne;
+      if (tree_on(c)) {
+        stats->side_rows += c->h_st->n_sib;
+        stats->side_accepted += c->h_st->sib_acc >= 0 ? 1 : 0;
+      }
     }
   }
   if (c->h_st->n != n_start + n_tokens) {
@@ -1709,6 +1780,10 @@ ssd_status ssd_swift_generate(ssd_ctx* c, const ssd_swift_params* pp, int32_t n_
     st.drafted += d;
     st.accepted += c->h_st->accepted;
     st.emitted += ne;
+    if (tree_on(c)) {
+      st.side_rows += c->h_st->n_sib;
+      st.side_accepted += c->h_st->sib_acc >= 0 ? 1 : 0;
+    }
     const int generated = c->h_st->n - n_start;
     if (!optimizing || generated < P.window + 1 || generated >= n_tokens) continue;
     // one optimisation step: the incumbent, then K-1 proposals

@@ -61,6 +61,9 @@ class Policy:
     final norm + LM head to that hidden state (LayerSkip).
     ``tau`` is the top-1 confidence threshold of the early stop (None: no
     stop); ``temperature`` 0 means greedy drafting and acceptance.
+    ``tree_tau`` (None: off) turns on dynamic verification: a kept draft
+    whose top-1 confidence is below it also sends the draft's second choice
+    to the verify as a sibling candidate, at most ``tree_max`` per round.
     """
 
     mode: str = "skip"
@@ -72,6 +75,8 @@ class Policy:
     seed: int = 0
     skip_attn: Tuple[int, ...] = ()
     skip_mlp: Tuple[int, ...] = ()
+    tree_tau: Optional[float] = None
+    tree_max: int = 0
 
     def sublayers(self, layer: int) -> Tuple[bool, bool]:
         """(attention runs, MLP runs) for ``layer`` in the draft (skip mode)."""
@@ -114,6 +119,10 @@ class Workload:
     # greedy tokens generated after the prompt before scoring, so that the
     # scoring window holds full-model greedy tokens
     pre_generate: int = 0
+    # weight options (make_weights defaults): LM head multiplier, RMSNorm
+    # gains 1 + N(0, 0.1) instead of ones
+    lm_head_scale: float = 1.0
+    random_gains: bool = False
 
 
 def _odd(lo: int, hi: int) -> Tuple[int, ...]:
@@ -196,8 +205,15 @@ LLAMA70B_SWIFT = Workload(
     policy=Policy(mode="skip", skip=tuple(range(20, 80, 2)), d_max=8, tau=0.7),
 )
 
+# The tiny model with the parity tests' sharpened LM head (x10) and random
+# norm gains: drafts clear the confidence bar and are often accepted, so the
+# draft loop, rollback and dynamic verification do real work (with the plain
+# N(0, 0.02) head every literal threshold stops drafting at the first step).
+TINY_SHARP = replace(TINY, name="tiny-L4-d256-sharp", lm_head_scale=10.0, random_gains=True,
+                     policy=Policy(mode="skip", skip=(2,), d_max=4, tau=None))
+
 WORKLOADS = {w.name: w for w in (TINY, LLAMA7B_SWIFT, LLAMA7B_LAYERSKIP, LLAMA13B_SCORE,
-                                 LLAMA70B_SWIFT, LLAMA7B_SUBLAYER)}
+                                 LLAMA70B_SWIFT, LLAMA7B_SUBLAYER, TINY_SHARP)}
 
 
 def shrink(w: Workload, **shape_changes) -> Workload:

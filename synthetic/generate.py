@@ -49,15 +49,20 @@ def _normal(shape, seed: int, device, std: float, scale: float, dtype) -> torch.
 
 
 def make_weights(w: Workload, device="cpu", dtype: str | None = None,
-                 random_gains: bool = False, lm_head_scale: float = 1.0) -> Dict:
+                 random_gains: bool | None = None, lm_head_scale: float | None = None) -> Dict:
     """Seeded synthetic weights for workload ``w`` on ``device``.
 
     ``dtype`` overrides the workload dtype ("bf16" or "fp32").
     ``random_gains`` draws the RMSNorm gains 1 + N(0, 0.1) instead of ones
     (parity cases use it so that a dropped gain is caught).
     ``lm_head_scale`` multiplies the LM head (parity cases use a sharper head
-    so that greedy sequences have fewer near-ties).
+    so that greedy sequences have fewer near-ties).  Both default to the
+    workload's own setting.
     """
+    if random_gains is None:
+        random_gains = w.random_gains
+    if lm_head_scale is None:
+        lm_head_scale = w.lm_head_scale
     s = w.shape
     dt = dtype or s.dtype
     tdt = torch.bfloat16 if dt == "bf16" else torch.float32
