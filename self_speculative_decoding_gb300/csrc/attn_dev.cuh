@@ -389,6 +389,30 @@ SSD_DI bool body(const AttnArgs& a, int M, int ns, int pos0, int item, const Sme
     float* LR = CW + R * n_active;
     const size_t need = ((size_t)3 * R * n_active + R) * sizeof(float);
     if (need <= main_bytes(dh, nchunk_max)) {
+      // The chunks' output vectors of a batch of rows go to shared memory with
+      // 16-byte asynchronous copies, all in flight at once (thread t copies
+      // piece t % (dh/4) of (row, chunk) records t / (dh/4), ...); the first
+      // batch is requested before the (m, l) loads so that the two L2 round
+      // trips overlap.  Then every output sums its chunks in chunk order.
+      const size_t cs = (size_t)rows * (dh + kRecPad);
+      const size_t used = ((size_t)3 * R * n_active + R + 3) & ~(size_t)3;  // floats, 16 B aligned
+      float* OB = CM + used;
+      const size_t row_floats = (size_t)n_active * dh;
+      const int per_batch = (int)((main_bytes(dh, nchunk_max) / sizeof(float) - used) / row_floats);
+      auto fetch = [&](int r0) {
+        const int nb = min(per_batch, R - r0);
+        const int h4 = dh / 4;
+        const int q = tid % h4;
+        for (int rc = tid / h4; rc < nb * n_active; rc += kGroupThreads / h4) {
+          const int rb = rc / n_active, cc = rc % n_active;
+          const int rr = r0 + rb;
+          const int m = rr % M, r = (rr / M) * kMaxRows + m;
+          if (cc <= sm.rpos[m] / kAttnChunk)
+            cp_async16(OB + (size_t)rb * row_floats + (size_t)cc * dh + 4 * q,
+                       hb + cc * cs + (size_t)r * (dh + kRecPad) + kRecPad + 4 * q);
+        }
+      };
+      if (per_batch >= 1) fetch(0);
       for (int e = tid; e < R * n_active; e += kGroupThreads) {
         const int rr = e / n_active, cc = e % n_active;
         const int m = rr % M, r = (rr / M) * kMaxRows + m;
@@ -414,28 +438,10 @@ SSD_DI bool body(const AttnArgs& a, int M, int ns, int pos0, int item, const Sme
         LR[rr] = L;
       }
       sync();
-      // the chunks' output vectors of a batch of rows go to shared memory in
-      // one parallel pass, then every output sums them in chunk order
-      const size_t cs = (size_t)rows * (dh + kRecPad);
-      const size_t used = ((size_t)3 * R * n_active + R + 3) & ~(size_t)3;  // floats, 16 B aligned
-      float* OB = CM + used;
-      const size_t row_floats = (size_t)n_active * dh;
-      const int per_batch = (int)((main_bytes(dh, nchunk_max) / sizeof(float) - used) / row_floats);
       if (per_batch >= 1) {
         for (int r0 = 0; r0 < R; r0 += per_batch) {
           const int nb = min(per_batch, R - r0);
-          // 16-byte asynchronous copies, all in flight at once: thread t
-          // copies piece t % (dh/4) of (row, chunk) records t / (dh/4), ...
-          const int h4 = dh / 4;
-          const int q = tid % h4;
-          for (int rc = tid / h4; rc < nb * n_active; rc += kGroupThreads / h4) {
-            const int rb = rc / n_active, cc = rc % n_active;
-            const int rr = r0 + rb;
-            const int m = rr % M, r = (rr / M) * kMaxRows + m;
-            if (cc <= sm.rpos[m] / kAttnChunk)
-              cp_async16(OB + (size_t)rb * row_floats + (size_t)cc * dh + 4 * q,
-                         hb + cc * cs + (size_t)r * (dh + kRecPad) + kRecPad + 4 * q);
-          }
+          if (r0 > 0) fetch(r0);
           cp_async_wait_all();
           sync();
           for (int e = tid; e < nb * dh; e += kGroupThreads) {
