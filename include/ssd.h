@@ -213,8 +213,21 @@ ssd_status ssd_accept(ssd_ctx* ctx, int32_t* emitted_out, int32_t* n_emitted_out
  * are emitted; extra tokens of the last round are dropped (the committed
  * length ends exactly n_tokens further).  out (host, nullable, >= n_tokens)
  * receives the tokens; stats (host, nullable) is filled.
+ * With the device loop (ssd_set_device_loop, on by default where the device
+ * supports the conditional graph nodes it needs) the whole call is one
+ * graph launch: the draft loop's stop, the extra pass, the verify width and
+ * the next round are decided on the device, and the host reads back once.
+ * The tokens and counts are those of the host-driven loop; stats then has
+ * draft_ms = verify_ms = 0 and bytes_streamed counts the K/V at the
+ * generation's middle position.
  * Errors: CAPACITY, STATE (no prefill), CUDA, TIMEOUT. */
 ssd_status ssd_generate(ssd_ctx* ctx, int32_t n_tokens, int32_t* out, ssd_stats* stats);
+
+/* ssd_generate's device loop on (enable != 0, the default) or off (the host
+ * drives each draft step, verify and acceptance, and stats carries per-pass
+ * device times).  *active_out (host, nullable) = whether the loop graph
+ * exists and will be used.  Errors: INVALID_ARG (ctx NULL). */
+ssd_status ssd_set_device_loop(ssd_ctx* ctx, int32_t enable, int32_t* active_out);
 
 /* Plain autoregressive decoding with the full model (the baseline the
  * speedup is measured against), same kernels.  out (host, nullable). */

@@ -281,6 +281,19 @@ class SSDContext:
         report["final"] = layers(rep.final_mask)
         return out[:n_tokens].tolist(), report, trace
 
+    def last_error(self) -> str:
+        """The context's last error message (ssd_last_error)."""
+        return _lib().ssd_last_error(self._h).decode()
+
+    def set_device_loop(self, enable: bool) -> bool:
+        """generate() as one graph launch with device-side control (True,
+        the default where supported) or driven from the host (False; stats
+        then carry per-pass device times).  Returns whether the device loop
+        is in use.  Both produce the same tokens and counts."""
+        active = C.c_int32(0)
+        self._check(_lib().ssd_set_device_loop(self._h, 1 if enable else 0, C.byref(active)))
+        return bool(active.value)
+
     def set_pass_kernel(self, enable: bool) -> bool:
         """One persistent launch per decode pass (True) or one kernel per
         step (False, the default); returns whether the persistent kernel is

@@ -60,7 +60,13 @@ struct DevState {
   int32_t sib_depth[kMaxSide];  // sibling i stands for draft y_j, j = sib_depth[i] (position n + j)
   int32_t sib_tok[kMaxSide];
   int32_t side_pos[kMaxSide];   // positions of the current pass's side rows
-  int32_t pad2[7];
+  // device-side generation loop: its target length, the kept drafts of the
+  // last accepted round, and running counts of the loop's work
+  int32_t target_n;
+  int32_t last_d;
+  int32_t acc_rounds, acc_drafted, acc_accepted, acc_emitted;
+  int32_t acc_steps, acc_extra, acc_side_rows, acc_side_acc;
+  int32_t pad2[1];
 };
 static_assert(sizeof(DevState) % 16 == 0, "DevState layout");
 

@@ -69,7 +69,49 @@ __global__ void accept_greedy_kernel(DevState* st, int32_t* tokens, const RowSta
   st->accepted = a;
   st->sib_acc = sib;
   st->sib_pos = n + a;
+  st->last_d = d;
   st->j = st->d = st->stop = 0;
+}
+
+// Device-side generation loop: sets a graph conditional from the decoding
+// state (see LoopCond) and keeps the loop's running counts.  One thread.
+__global__ void loop_cond_kernel(DevState* st, cudaGraphConditionalHandle h, int what, int arg,
+                                 int limit) {
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x != 0) return;
+  unsigned v = 0;
+  switch (what) {
+    case LOOP_DRAFT_FIRST:  // arg = d_max
+      v = arg > 0;
+      break;
+    case LOOP_DRAFT_NEXT:   // after a draft step; arg = d_max
+      st->acc_steps += 1;
+      v = !st->stop && st->j < arg;
+      break;
+    case LOOP_EXTRA:
+      v = !st->stop;
+      st->acc_extra += v;
+      break;
+    case LOOP_EXTRA_NOP:    // leaves the condition as it is
+      return;
+    case LOOP_WIDE:         // arg = rows of the narrow verify graph
+      v = st->d + 1 + st->n_sib > arg;
+      break;
+    case LOOP_ROUND:        // after the acceptance; arg = 1: siblings counted
+      st->acc_rounds += 1;
+      st->acc_drafted += st->last_d;
+      st->acc_accepted += st->accepted;
+      st->acc_emitted += st->n_emitted;
+      if (arg) {
+        st->acc_side_rows += st->n_sib;
+        st->acc_side_acc += st->sib_acc >= 0;
+      }
+      // limit = max_seq - (d_max + 1): another round never writes past the cache
+      v = st->n < st->target_n && st->n <= limit && st->err == 0;
+      break;
+  }
+  cudaGraphSetConditional(h, v);
 }
 
 // The taken sibling's K/V rows (every layer and KV head) into the cache at
@@ -219,6 +261,7 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_stoch_kernel(AcceptArgs
       st->n = n + acc + 1;
       st->n_emitted = acc + 1;
       st->accepted = acc;
+      st->last_d = d;
       st->j = st->d = st->stop = 0;
     } else {
       for (int i = 0; i < acc; ++i) a.emitted[i] = drafts[i];
@@ -300,6 +343,13 @@ cudaError_t launch_draft_end(const DraftEndArgs& a, cudaStream_t s, bool pdl) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t lc = make_cfg(1, 32, s, pdl, attr);
   return cudaLaunchKernelEx(&lc, draft_end_kernel, a);
+}
+
+cudaError_t launch_loop_cond(DevState* st, cudaGraphConditionalHandle h, int what, int arg,
+                             int limit, cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t lc = make_cfg(1, 32, s, pdl, attr);
+  return cudaLaunchKernelEx(&lc, loop_cond_kernel, st, h, what, arg, limit);
 }
 
 cudaError_t launch_side_commit(const DevState* st, bf16* kc, bf16* vc, const bf16* ks,

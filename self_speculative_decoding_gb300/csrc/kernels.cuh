@@ -163,6 +163,19 @@ cudaError_t launch_ar_end(DevState* st, int32_t* tokens, const RowStats* vstats,
                           float temperature, int reset, cudaStream_t s, bool pdl);
 cudaError_t launch_accept_greedy(DevState* st, int32_t* tokens, const RowStats* vstats,
                                  cudaStream_t s, bool pdl);
+// Device-side generation loop (one graph launch per ssd_generate): the
+// conditions of its nodes, set by one-thread kernels from the decoding state.
+enum LoopCond {
+  LOOP_DRAFT_FIRST = 0,  // enter the draft loop: d_max > 0
+  LOOP_DRAFT_NEXT = 1,   // another draft step: no stop and j < d_max
+  LOOP_EXTRA = 2,        // the extra pass: the draft loop ended without a stop
+  LOOP_WIDE = 3,         // the wide verify graph: d + 1 + siblings > narrow rows
+  LOOP_ROUND = 4,        // another round: n < target, n <= limit, no device error
+  LOOP_EXTRA_NOP = 5,    // sets nothing (a plain launch that orders the graph)
+};
+cudaError_t launch_loop_cond(DevState* st, cudaGraphConditionalHandle h, int what, int arg,
+                             int limit, cudaStream_t s, bool pdl);
+
 // After a greedy acceptance that took a sibling: its K/V of every layer
 // (side slot sib_acc) into the cache at sib_pos.  kc / vc [L][Hkv][max_seq][dh],
 // ks / vs [L][Hkv][kMaxSide][dh].  No-op when no sibling was taken.

@@ -65,6 +65,7 @@ struct ssd_ctx {
   const bf16* lm_head = nullptr;
   cudaStream_t stream = nullptr;
   cudaStream_t cap = nullptr;
+  cudaStream_t cap2 = nullptr;  // captures the bodies of the loop graph's conditional nodes
   cudaEvent_t ev = nullptr;
   cudaEvent_t t0 = nullptr, t1 = nullptr;  // pass timing for ssd_stats
   int timeout_ms = 120000;
@@ -129,6 +130,13 @@ struct ssd_ctx {
   int32_t* h_tok = nullptr;  // pinned staging [max_seq]
 
   Graph g_draft, g_extra, g_verify, g_accept, g_ar;
+  // device-side generation loop: a whole ssd_generate in one graph launch
+  // (rounds, draft steps, the extra pass and the verify width decided on the
+  // device by conditional nodes); nodes of its bodies per iteration
+  Graph g_loop;
+  bool use_loop = true;
+  std::string loop_err;  // why the loop graph could not be built (empty: built)
+  int loop_nodes_draft = 0, loop_nodes_extra = 0, loop_nodes_round = 0;
   // lossy early-exit step: the AR step over the draft layer set only
   Graph g_lossy;
   // first position whose K/V a lossy step left incomplete (-1: none); the
@@ -812,9 +820,174 @@ ssd_status build_graphs_once(ssd_ctx* c) {
   return build_graph(c, c->g_ar, b_ar);
 }
 
+// ---------------------------------------------------------------------------
+// device-side generation loop
+
+// During a capture on `s`: appends a conditional node after the captured
+// work so far; returns its body graphs (owned by the node).
+cudaGraph_t* add_conditional(cudaStream_t s, cudaGraphConditionalHandle h,
+                             cudaGraphConditionalNodeType type, unsigned size, cudaError_t* err) {
+  cudaStreamCaptureStatus status;
+  cudaGraph_t g = nullptr;
+  const cudaGraphNode_t* deps = nullptr;
+  const cudaGraphEdgeData* edges = nullptr;
+  size_t nd = 0;
+  *err = cudaStreamGetCaptureInfo(s, &status, nullptr, &g, &deps, &edges, &nd);
+  if (*err != cudaSuccess) return nullptr;
+  cudaGraphNodeParams p = {};
+  p.type = cudaGraphNodeTypeConditional;
+  p.conditional.handle = h;
+  p.conditional.type = type;
+  p.conditional.size = size;
+  cudaGraphNode_t node = nullptr;
+  *err = cudaGraphAddNode(&node, g, deps, edges, nd, &p);
+  if (*err != cudaSuccess) return nullptr;
+  *err = cudaStreamUpdateCaptureDependencies(s, &node, nullptr, 1, cudaStreamSetCaptureDependencies);
+  return *err == cudaSuccess ? p.conditional.phGraph_out : nullptr;
+}
+
+// Captures builder `fn` (and optionally one condition kernel after it) into
+// body graph `g` on the second capture stream; returns the nodes captured.
+// Highest committed length from which another round stays inside the cache.
+int loop_limit(const ssd_ctx* c) { return c->cfg.max_seq - (c->pol.d_max + 1); }
+
+ssd_status capture_body(ssd_ctx* c, cudaGraph_t g, Builder fn, cudaGraphConditionalHandle h,
+                        int what, int arg, int* nodes) {
+  CK(cudaStreamBeginCaptureToGraph(c->cap2, g, nullptr, nullptr, 0,
+                                   cudaStreamCaptureModeThreadLocal));
+  const int n0 = c->capturing_nodes;
+  ssd_status r = fn ? fn(c, c->cap2) : SSD_OK;
+  if (r == SSD_OK && what >= 0)
+    r = note(c, launch_loop_cond(c->st, h, what, arg, loop_limit(c), c->cap2, false), "loop_cond");
+  cudaGraph_t out = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(c->cap2, &out);
+  if (r != SSD_OK) return r;
+  if (e != cudaSuccess) return fail(c, SSD_ERR_CUDA, std::string("capture: ") + cudaGetErrorString(e));
+  if (nodes) *nodes = c->capturing_nodes - n0;
+  return SSD_OK;
+}
+
+// The loop graph (one launch runs rounds until n reaches DevState::target_n):
+//   while (hR) {                       hR: default 1 at every launch
+//     hD = d_max > 0; while (hD) { draft step; hD = !stop && j < d_max }
+//     hE = !stop;     if (hE) { extra pass }
+//     hW = rows > narrow; if (hW) { wide verify } else { verify }
+//     accept; hR = n < target_n
+//   }
+ssd_status build_loop_graph(ssd_ctx* c) {
+  c->g_loop.reset();
+  cudaGraph_t G = nullptr;
+  CK(cudaGraphCreate(&G, 0));
+  cudaGraphConditionalHandle hR, hD, hE, hW;
+  cudaError_t e = cudaGraphConditionalHandleCreate(&hR, G, 1, cudaGraphCondAssignDefault);
+  ssd_status r = SSD_OK;
+  cudaGraph_t body = nullptr;
+  if (e == cudaSuccess) {
+    cudaGraphNodeParams p = {};
+    p.type = cudaGraphNodeTypeConditional;
+    p.conditional.handle = hR;
+    p.conditional.type = cudaGraphCondTypeWhile;
+    p.conditional.size = 1;
+    cudaGraphNode_t node = nullptr;
+    e = cudaGraphAddNode(&node, G, nullptr, nullptr, 0, &p);
+    if (e == cudaSuccess) body = p.conditional.phGraph_out[0];
+  }
+  if (e == cudaSuccess) e = cudaGraphConditionalHandleCreate(&hD, body, 0, 0);
+  if (e == cudaSuccess) e = cudaGraphConditionalHandleCreate(&hE, body, 0, 0);
+  if (e == cudaSuccess) e = cudaGraphConditionalHandleCreate(&hW, body, 0, 0);
+  if (e != cudaSuccess) {
+    cudaGraphDestroy(G);
+    return fail(c, SSD_ERR_CUDA, std::string("loop graph: ") + cudaGetErrorString(e));
+  }
+  const bool wide = c->g_verify_wide.exec != nullptr;
+  int n_draft = 0, n_extra = 0, n_v = 0, n_vw = 0;
+  c->capturing = true;
+  c->capturing_nodes = 0;
+  e = cudaStreamBeginCaptureToGraph(c->cap, body, nullptr, nullptr, 0,
+                                    cudaStreamCaptureModeThreadLocal);
+  bool open = e == cudaSuccess;
+  if (open)
+    r = note(c, launch_loop_cond(c->st, hD, LOOP_DRAFT_FIRST, c->pol.d_max, loop_limit(c), c->cap,
+                                 false),
+             "loop_cond");
+  cudaGraph_t* bd = nullptr;
+  if (open && r == SSD_OK) bd = add_conditional(c->cap, hD, cudaGraphCondTypeWhile, 1, &e);
+  if (bd) r = capture_body(c, bd[0], b_draft, hD, LOOP_DRAFT_NEXT, c->pol.d_max, &n_draft);
+  if (bd && r == SSD_OK)
+    r = note(c, launch_loop_cond(c->st, hE, LOOP_EXTRA, 0, loop_limit(c), c->cap, false), "loop_cond");
+  cudaGraph_t* be = nullptr;
+  if (bd && r == SSD_OK) be = add_conditional(c->cap, hE, cudaGraphCondTypeIf, 1, &e);
+  if (be) r = capture_body(c, be[0], b_extra, hE, -1, 0, &n_extra);
+  // the verify runs in the body of an IF node in both cases (without a wide
+  // graph its condition, rows > 0, always holds), so that every conditional
+  // node is followed by a plain-launched condition kernel or another
+  // conditional node and no programmatic launch depends on one directly
+  bool verified = false;
+  if (be && r == SSD_OK) {
+    r = note(c, launch_loop_cond(c->st, hW, LOOP_WIDE, wide ? verify_narrow_rows(c) : 0,
+                                 loop_limit(c), c->cap, false),
+             "loop_cond");
+    cudaGraph_t* bw =
+        r == SSD_OK ? add_conditional(c->cap, hW, cudaGraphCondTypeIf, wide ? 2 : 1, &e) : nullptr;
+    if (bw) r = capture_body(c, bw[0], wide ? b_verify_wide : b_verify, hW, -1, 0, &n_vw);
+    if (bw && wide && r == SSD_OK) r = capture_body(c, bw[1], b_verify, hW, -1, 0, &n_v);
+    verified = bw != nullptr && r == SSD_OK;
+  }
+  int n_acc = 0;
+  if (verified) {
+    const int n0 = c->capturing_nodes;
+    // a plain launch after the verify's IF node (see above)
+    r = note(c, launch_loop_cond(c->st, hE, LOOP_EXTRA_NOP, 0, loop_limit(c), c->cap, false),
+             "loop_cond");
+    if (r == SSD_OK) r = b_accept(c, c->cap);
+    if (r == SSD_OK)
+      r = note(c, launch_loop_cond(c->st, hR, LOOP_ROUND, tree_on(c) ? 1 : 0, loop_limit(c),
+                                   c->cap, false),
+               "loop_cond");
+    n_acc = c->capturing_nodes - n0;
+  }
+  cudaGraph_t out = nullptr;
+  if (open) {
+    const cudaError_t e2 = cudaStreamEndCapture(c->cap, &out);
+    if (e == cudaSuccess) e = e2;
+  }
+  c->capturing = false;
+  if (r == SSD_OK && (e != cudaSuccess || !verified)) {
+    r = fail(c, SSD_ERR_CUDA, std::string("loop graph capture: ") + cudaGetErrorString(e));
+  }
+  if (r == SSD_OK) {
+    e = cudaGraphInstantiate(&c->g_loop.exec, G, 0);
+    if (e != cudaSuccess) {
+      c->g_loop.exec = nullptr;
+      r = fail(c, SSD_ERR_CUDA, std::string("loop graph instantiate: ") + cudaGetErrorString(e));
+    }
+  }
+  cudaGraphDestroy(G);
+  c->loop_nodes_draft = n_draft;
+  c->loop_nodes_extra = n_extra;
+  c->loop_nodes_round = std::max(n_v, n_vw) + n_acc + 3;
+  return r;
+}
+
 // Builds the graphs with the pass kernel when it is enabled and usable on
 // this device, else (or if that fails) with one kernel per step.
+ssd_status build_graphs_and_loop(ssd_ctx* c);
 ssd_status build_graphs(ssd_ctx* c) {
+  const ssd_status r = build_graphs_and_loop(c);
+  if (r != SSD_OK) return r;
+  // the loop graph is an optimisation: without it generation runs the same
+  // graphs from the host
+  const std::string keep = c->err;
+  c->loop_err.clear();
+  if (build_loop_graph(c) != SSD_OK) {
+    c->g_loop.reset();
+    cudaGetLastError();
+    c->loop_err = c->err;
+    c->err = keep;
+  }
+  return SSD_OK;
+}
+ssd_status build_graphs_and_loop(ssd_ctx* c) {
   c->pass_ok = false;
   if (c->use_pass && pass_supported(c->cfg.head_dim, c->cfg.max_seq) &&
       pass_prepare() == cudaSuccess && build_pass_programs(c) == SSD_OK) {
@@ -1222,6 +1395,7 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
       cudaMallocHost((void**)&c->h_ffeat, (size_t)3 * g.n_layers * 4) != cudaSuccess ||
       cudaMallocHost((void**)&c->h_tok, (size_t)g.max_seq * 4) != cudaSuccess ||
       cudaStreamCreateWithFlags(&c->cap, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&c->cap2, cudaStreamNonBlocking) != cudaSuccess ||
       cudaEventCreateWithFlags(&c->ev, cudaEventDisableTiming) != cudaSuccess ||
       cudaEventCreate(&c->t0) != cudaSuccess || cudaEventCreate(&c->t1) != cudaSuccess) {
     cudaGetLastError();
@@ -1266,6 +1440,7 @@ ssd_status ssd_destroy(ssd_ctx* c) {
   c->g_accept.reset();
   c->g_ar.reset();
   c->g_lossy.reset();
+  c->g_loop.reset();
   c->p_draft.reset();
   c->p_extra.reset();
   c->p_verify.reset();
@@ -1287,6 +1462,7 @@ ssd_status ssd_destroy(ssd_ctx* c) {
   if (c->h_ffeat) cudaFreeHost(c->h_ffeat);
   if (c->h_tok) cudaFreeHost(c->h_tok);
   if (c->cap) cudaStreamDestroy(c->cap);
+  if (c->cap2) cudaStreamDestroy(c->cap2);
   if (c->ev) cudaEventDestroy(c->ev);
   if (c->t0) cudaEventDestroy(c->t0);
   if (c->t1) cudaEventDestroy(c->t1);
@@ -1440,6 +1616,59 @@ ssd_status ssd_accept(ssd_ctx* c, int32_t* emitted_out, int32_t* n_out) {
   return SSD_OK;
 }
 
+// ssd_generate on the device-side loop graph: one launch, one read-back.
+ssd_status generate_loop(ssd_ctx* c, int32_t n_tokens, int32_t* out, ssd_stats* stats,
+                         int n_start) {
+  Range nv("ssd generate (device loop)");
+  DevState* h = c->h_st;
+  h->target_n = n_start + n_tokens;
+  h->last_d = 0;
+  h->acc_rounds = h->acc_drafted = h->acc_accepted = h->acc_emitted = 0;
+  h->acc_steps = h->acc_extra = h->acc_side_rows = h->acc_side_acc = 0;
+  const size_t off = offsetof(DevState, target_n);
+  const size_t len = offsetof(DevState, pad2) - off;
+  CK(cudaMemcpyAsync(reinterpret_cast<char*>(c->st) + off, reinterpret_cast<char*>(h) + off, len,
+                     cudaMemcpyHostToDevice, c->stream));
+  CK(cudaGraphLaunch(c->g_loop.exec, c->stream));
+  ssd_status r = read_state(c);
+  c->phase = PH_IDLE;
+  if (r != SSD_OK) return r;
+  const int64_t launches = (int64_t)h->acc_steps * c->loop_nodes_draft +
+                           (int64_t)h->acc_extra * c->loop_nodes_extra +
+                           (int64_t)h->acc_rounds * c->loop_nodes_round;
+  c->launches += launches;
+  if (stats) {
+    stats->rounds = h->acc_rounds;
+    stats->drafted = h->acc_drafted;
+    stats->accepted = h->acc_accepted;
+    stats->emitted = h->acc_emitted;
+    stats->draft_steps = h->acc_steps;
+    stats->side_rows = h->acc_side_rows;
+    stats->side_accepted = h->acc_side_acc;
+    stats->kernel_launches = launches;
+    // K/V bytes at the generation's middle position
+    const int mid = n_start + n_tokens / 2;
+    const double rows = (double)h->acc_drafted + h->acc_rounds + h->acc_side_rows;
+    stats->bytes_streamed = h->acc_steps * draft_bytes(c, mid) +
+                            h->acc_extra * pass_bytes(c, (int)c->pre.size(), false, mid, 1) +
+                            h->acc_rounds * pass_bytes(c, (int)c->verify_layers.size(), true, mid, 0) +
+                            rows * (c->verify_layers.size() * 2.0 * 2.0 * 2.0 * c->cfg.n_kv_heads *
+                                    c->cfg.head_dim);
+  }
+  if (out && n_tokens > 0) {
+    CK(cudaMemcpyAsync(c->h_tok, c->tokens + n_start, (size_t)n_tokens * 4, cudaMemcpyDeviceToHost,
+                       c->stream));
+    if ((r = wait_stream(c)) != SSD_OK) return r;
+    memcpy(out, c->h_tok, (size_t)n_tokens * 4);
+  }
+  if (h->n != n_start + n_tokens) {
+    const int32_t nn = n_start + n_tokens;
+    CK(cudaMemcpyAsync(&c->st->n, &nn, 4, cudaMemcpyHostToDevice, c->stream));
+    if ((r = read_state(c)) != SSD_OK) return r;
+  }
+  return SSD_OK;
+}
+
 ssd_status ssd_generate(ssd_ctx* c, int32_t n_tokens, int32_t* out, ssd_stats* stats) {
   if (!c || n_tokens < 0) return SSD_ERR_INVALID_ARG;
   ssd_status r = ensure_policy(c);
@@ -1451,6 +1680,8 @@ ssd_status ssd_generate(ssd_ctx* c, int32_t n_tokens, int32_t* out, ssd_stats* s
   const int n_start = c->h_st->n;
   if (n_start + n_tokens + c->pol.d_max + 1 > c->cfg.max_seq)
     return fail(c, SSD_ERR_CAPACITY, "n_tokens + d_max + 1 exceeds the KV capacity");
+  if (c->use_loop && c->g_loop.exec && n_tokens > 0)
+    return generate_loop(c, n_tokens, out, stats, n_start);
   int got = 0;
   while (got < n_tokens) {
     if ((r = run_draft(c, stats)) != SSD_OK) return r;
@@ -1852,6 +2083,15 @@ ssd_status ssd_set_pass_kernel(ssd_ctx* c, int32_t enable, int32_t* active_out) 
 
 ssd_status ssd_debug_fail_alloc(int32_t n) {
   g_fail_alloc = n < 0 ? -1 : n;
+  return SSD_OK;
+}
+
+ssd_status ssd_set_device_loop(ssd_ctx* c, int32_t enable, int32_t* active_out) {
+  if (!c) return SSD_ERR_INVALID_ARG;
+  c->use_loop = enable != 0;
+  if (active_out) *active_out = c->use_loop && c->g_loop.exec ? 1 : 0;
+  // the reason the loop is unavailable, for ssd_last_error
+  if (c->use_loop && !c->g_loop.exec) c->err = "device loop unavailable: " + c->loop_err;
   return SSD_OK;
 }
 

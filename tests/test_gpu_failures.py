@@ -63,6 +63,7 @@ def test_pass_timing_statistics(ssd):
     wts = to_device_weights(make_weights(TINY, dtype="bf16", lm_head_scale=10.0))
     ctx = ssd.SSDContext(TINY.shape, wts, max_seq=128)
     ctx.set_policy(Policy(mode="skip", skip=(2,), d_max=3, tau=None))
+    ctx.set_device_loop(False)   # per-pass device times come from the host-driven loop
     ctx.prefill(make_prompt(TINY, 8))
     _, st = ctx.generate(20)
     assert st["draft_steps"] > 0 and st["draft_ms"] > 0 and st["verify_ms"] > 0
