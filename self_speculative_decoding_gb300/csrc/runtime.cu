@@ -1616,7 +1616,9 @@ ssd_status ssd_accept(ssd_ctx* c, int32_t* emitted_out, int32_t* n_out) {
   return SSD_OK;
 }
 
-// ssd_generate on the device-side loop graph: one launch, one read-back.
+// ssd_generate on the device-side loop graph: one launch and one read-back
+// per kLoopTokens generated tokens.
+constexpr int kLoopTokens = 512;
 ssd_status generate_loop(ssd_ctx* c, int32_t n_tokens, int32_t* out, ssd_stats* stats,
                          int n_start) {
   Range nv("ssd generate (device loop)");
@@ -1629,8 +1631,25 @@ ssd_status generate_loop(ssd_ctx* c, int32_t n_tokens, int32_t* out, ssd_stats* 
   const size_t len = offsetof(DevState, pad2) - off;
   CK(cudaMemcpyAsync(reinterpret_cast<char*>(c->st) + off, reinterpret_cast<char*>(h) + off, len,
                      cudaMemcpyHostToDevice, c->stream));
-  CK(cudaGraphLaunch(c->g_loop.exec, c->stream));
-  ssd_status r = read_state(c);
+  // one launch per kLoopTokens tokens, so that every bounded host wait covers
+  // a bounded amount of work; the rounds continue across launches unchanged
+  const int final_n = n_start + n_tokens;
+  ssd_status r = SSD_OK;
+  for (int n_cur = n_start; n_cur < final_n;) {
+    const int32_t target = std::min(final_n, n_cur + kLoopTokens);
+    if (target != h->target_n || n_cur != n_start) {
+      h->target_n = target;
+      CK(cudaMemcpyAsync(&c->st->target_n, &h->target_n, sizeof(int32_t),
+                         cudaMemcpyHostToDevice, c->stream));
+    }
+    CK(cudaGraphLaunch(c->g_loop.exec, c->stream));
+    if ((r = read_state(c)) != SSD_OK) break;
+    if (h->n <= n_cur) {
+      r = fail(c, SSD_ERR_CUDA, "device loop made no progress");
+      break;
+    }
+    n_cur = h->n;
+  }
   c->phase = PH_IDLE;
   if (r != SSD_OK) return r;
   const int64_t launches = (int64_t)h->acc_steps * c->loop_nodes_draft +

@@ -83,3 +83,21 @@ def test_device_loop_continues_across_calls(ssd):
     c, _ = ctx.generate(27)
     assert a + b + c == full
     ctx.close()
+
+
+def test_device_loop_in_several_launches(ssd):
+    # more than one launch's worth of tokens (512 per launch): the rounds
+    # continue across launches exactly as in the host-driven loop
+    w, pol = CASES[0]
+    wts = make_weights(w, dtype="bf16", lm_head_scale=10.0, random_gains=True)
+    ctx = ssd.SSDContext(w.shape, to_device_weights(wts), max_seq=1280)
+    ctx.set_policy(pol)
+    prompt = make_prompt(w, 20)
+    res = {}
+    for loop in (False, True):
+        assert ctx.set_device_loop(loop) == loop, ctx.last_error()
+        ctx.prefill(prompt)
+        toks, st = ctx.generate(1100)
+        res[loop] = (toks, ctx.tokens(), {k: st[k] for k in KEYS})
+    assert res[True] == res[False]
+    ctx.close()
