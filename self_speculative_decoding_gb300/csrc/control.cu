@@ -93,7 +93,7 @@ __global__ void loop_cond_kernel(DevState* st, cudaGraphConditionalHandle h, int
       v = !st->stop;
       st->acc_extra += v;
       break;
-    case LOOP_EXTRA_NOP:    // leaves the condition as it is
+    case LOOP_NOP:          // leaves the condition as it is
       return;
     case LOOP_WIDE:         // arg = rows of the narrow verify graph
       v = st->d + 1 + st->n_sib > arg;

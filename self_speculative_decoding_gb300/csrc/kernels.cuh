@@ -171,7 +171,7 @@ enum LoopCond {
   LOOP_EXTRA = 2,        // the extra pass: the draft loop ended without a stop
   LOOP_WIDE = 3,         // the wide verify graph: d + 1 + siblings > narrow rows
   LOOP_ROUND = 4,        // another round: n < target, n <= limit, no device error
-  LOOP_EXTRA_NOP = 5,    // sets nothing (a plain launch that orders the graph)
+  LOOP_NOP = 5,          // sets nothing (a plain launch that orders the graph)
 };
 cudaError_t launch_loop_cond(DevState* st, cudaGraphConditionalHandle h, int what, int arg,
                              int limit, cudaStream_t s, bool pdl);

@@ -937,7 +937,7 @@ ssd_status build_loop_graph(ssd_ctx* c) {
   if (verified) {
     const int n0 = c->capturing_nodes;
     // a plain launch after the verify's IF node (see above)
-    r = note(c, launch_loop_cond(c->st, hE, LOOP_EXTRA_NOP, 0, loop_limit(c), c->cap, false),
+    r = note(c, launch_loop_cond(c->st, hE, LOOP_NOP, 0, loop_limit(c), c->cap, false),
              "loop_cond");
     if (r == SSD_OK) r = b_accept(c, c->cap);
     if (r == SSD_OK)
@@ -969,11 +969,11 @@ ssd_status build_loop_graph(ssd_ctx* c) {
   return r;
 }
 
-// Builds the graphs with the pass kernel when it is enabled and usable on
-// this device, else (or if that fails) with one kernel per step.
-ssd_status build_graphs_and_loop(ssd_ctx* c);
+// Builds the per-pass graphs (build_pass_graphs), then the device-side
+// generation loop over them.
+ssd_status build_pass_graphs(ssd_ctx* c);
 ssd_status build_graphs(ssd_ctx* c) {
-  const ssd_status r = build_graphs_and_loop(c);
+  const ssd_status r = build_pass_graphs(c);
   if (r != SSD_OK) return r;
   // the loop graph is an optimisation: without it generation runs the same
   // graphs from the host
@@ -987,7 +987,10 @@ ssd_status build_graphs(ssd_ctx* c) {
   }
   return SSD_OK;
 }
-ssd_status build_graphs_and_loop(ssd_ctx* c) {
+
+// The per-pass graphs, with the persistent pass kernel when it is enabled and
+// usable on this device, else (or if that fails) with one kernel per step.
+ssd_status build_pass_graphs(ssd_ctx* c) {
   c->pass_ok = false;
   if (c->use_pass && pass_supported(c->cfg.head_dim, c->cfg.max_seq) &&
       pass_prepare() == cudaSuccess && build_pass_programs(c) == SSD_OK) {
