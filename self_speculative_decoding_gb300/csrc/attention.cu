@@ -22,7 +22,7 @@ namespace ssd {
 
 namespace {
 
-__global__ void __launch_bounds__(attn::kGroupThreads, 3) attn_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(attn::kGroupThreads, 4) attn_kernel(AttnArgs a) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bar;
   __shared__ int flag;
@@ -76,7 +76,7 @@ int attn_grid(const AttnArgs& a) {
   // Grid size only sets how many CTAs loop over the (head, chunk) items; it
   // does not change any reduction order.
   const int items = a.Hkv * (a.max_seq / kAttnChunk);
-  const int cap = sm_count() * 3;  // resident CTAs per SM (launch bounds)
+  const int cap = sm_count() * 4;  // resident CTAs per SM (launch bounds)
   return items < cap ? items : cap;
 }
 
