@@ -348,19 +348,6 @@ ssd_status ssd_swift_generate(ssd_ctx* ctx, const ssd_swift_params* params, int3
                               int32_t* out, uint64_t* trace_masks, float* trace_scores,
                               int32_t* trace_best, int32_t trace_cap, ssd_swift_report* report);
 
-/* Selects how the decode passes run (the draft step, the extra pass, the
- * verify pass and the autoregressive step of LayerSkip §3 / SWIFT §4).
- * enable = 1: each pass is one launch of a persistent kernel that keeps
- * every CTA resident and runs the pass's steps as dependent phases,
- * streaming the next step's weights while the current one finishes.
- * enable = 0 (the default, faster on GB300 today): one kernel per step,
- * chained with programmatic dependent launch.  Both compute the same bits.  The
- * persistent kernel is used only where the device holds its whole grid at
- * once; *active_out (nullable) reports whether it is in use.  Prefill, mask
- * scoring and ssd_profile_decode always use one kernel per step.  Rebuilds
- * the context's graphs.  Errors: STATE (a round is in flight), CUDA. */
-ssd_status ssd_set_pass_kernel(ssd_ctx* ctx, int32_t enable, int32_t* active_out);
-
 /* Human-readable description of the context's most recent error ("" if
  * none; a static string for a NULL context). */
 const char* ssd_last_error(const ssd_ctx* ctx);

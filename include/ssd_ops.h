@@ -161,7 +161,9 @@ ssd_status ssd_op_wait_selftest(int32_t polls, int32_t* code_out, void* stream);
  * held until the process exits; no cudaMalloc, cudaFree or other allocating
  * routine is called.  R must be <= 8192 (SSD_ERR_CAPACITY otherwise).
  * The first call on a device looks up the array's device address with that
- * device current; make that first call before any stream capture.  Every
+ * device current and keeps it; make that first call before any stream
+ * capture, and make no call on a device after cudaDeviceReset on it (the
+ * reset destroys the array the kept address points to).  Every
  * call on a device shares the one array and clears its counters on entry, so
  * calls whose kernels overlap on the GPU (different streams, or different
  * host threads) race and must be serialised by the caller.  Errors are

@@ -53,20 +53,33 @@ def _key(seed: int):
     return (seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF)
 
 
+def uniforms_table(seed: int, pos, rnd, stream: int, n: int) -> np.ndarray:
+    """u_v for v = 0..n-1 at every (position, round) of the broadcast arrays
+    ``pos`` and ``rnd``: shape [*broadcast shape, n] (fp64 holding values
+    exact in fp32).  Word w of vocabulary block b is u_{4b + w}."""
+    pos, rnd = np.broadcast_arrays(np.asarray(pos, dtype=np.uint64),
+                                   np.asarray(rnd, dtype=np.uint64))
+    blocks = np.arange((n + 3) // 4, dtype=np.uint64)
+    words = philox4x32_10((blocks, pos[..., None], rnd[..., None], stream), _key(seed))
+    r = np.stack(words, axis=-1).reshape(*pos.shape, -1)[..., :n]
+    return ((r >> np.uint64(9)).astype(np.float64) + 0.5) * 2.0 ** -23
+
+
 def uniforms(seed: int, pos: int, rnd: int, stream: int, n: int) -> np.ndarray:
     """u_v for v = 0..n-1 (fp64 holding values exact in fp32)."""
-    blocks = np.arange((n + 3) // 4, dtype=np.uint64)
-    words = philox4x32_10((blocks, pos, rnd, stream), _key(seed))
-    r = np.stack(words, axis=1).reshape(-1)[:n]
-    return ((r >> np.uint64(9)).astype(np.float64) + 0.5) * 2.0 ** -23
+    return uniforms_table(seed, pos, rnd, stream, n)
 
 
 def uniform(seed: int, pos: int, rnd: int, stream: int) -> float:
     return float(uniforms(seed, pos, rnd, stream, 1)[0])
 
 
+def gumbel_argmax_u(logw: np.ndarray, u: np.ndarray) -> int:
+    """Gumbel-max with given uniforms: argmax_v (logw_v - log(-log u_v)),
+    lowest index on ties."""
+    return int(np.argmax(logw - np.log(-np.log(u))))
+
+
 def gumbel_argmax(logw: np.ndarray, seed: int, pos: int, rnd: int, stream: int) -> int:
     """Sample v with probability proportional to exp(logw_v) by Gumbel-max."""
-    u = uniforms(seed, pos, rnd, stream, logw.shape[0])
-    g = -np.log(-np.log(u))
-    return int(np.argmax(logw + g))
+    return gumbel_argmax_u(logw, uniforms(seed, pos, rnd, stream, logw.shape[0]))

@@ -294,14 +294,6 @@ class SSDContext:
         self._check(_lib().ssd_set_device_loop(self._h, 1 if enable else 0, C.byref(active)))
         return bool(active.value)
 
-    def set_pass_kernel(self, enable: bool) -> bool:
-        """One persistent launch per decode pass (True) or one kernel per
-        step (False, the default); returns whether the persistent kernel is
-        in use.  Both compute the same bits."""
-        active = C.c_int32(0)
-        self._check(_lib().ssd_set_pass_kernel(self._h, 1 if enable else 0, C.byref(active)))
-        return bool(active.value)
-
 
 class _Ops:
     """Kernel-level entry points on torch CUDA tensors (ssd_ops.h)."""

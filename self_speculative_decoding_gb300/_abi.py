@@ -106,7 +106,6 @@ _SIGS = {
     "ssd_rewind": [_P, _I],
     "ssd_get_tokens": [_P, C.POINTER(_I), _I, C.POINTER(_I)],
     "ssd_set_timeout_ms": [_P, _I],
-    "ssd_set_pass_kernel": [_P, _I, C.POINTER(C.c_int32)],
     "ssd_set_device_loop": [_P, _I, C.POINTER(C.c_int32)],
     "ssd_debug_fail_alloc": [_I],
     "ssd_swift_generate": [_P, C.POINTER(SsdSwiftParams), _I, _P, _P, _P, _P, _I,

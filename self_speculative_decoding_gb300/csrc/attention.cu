@@ -60,16 +60,14 @@ size_t attn_part_floats(int Hkv, int H, int dh, int max_seq) {
 }
 
 static int sm_count() {
-  static int cached[64] = {0};
-  int dev = 0;
+  static int cached[kDeviceSlots] = {0};
+  const int dv = device_slot();
+  if (dv >= 0 && cached[dv]) return cached[dv];
+  int dev = 0, sms = 148;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  if (!cached[dev]) {
-    int sms = 148;
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev] = sms;
-  }
-  return cached[dev];
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (dv >= 0) cached[dv] = sms;
+  return sms;
 }
 
 int attn_grid(const AttnArgs& a) {
@@ -82,12 +80,13 @@ int attn_grid(const AttnArgs& a) {
 
 cudaError_t attn_prepare(const AttnArgs& a) {
   // raise the kernel's dynamic shared-memory limit to what this geometry needs
-  static size_t set_to = 0;
+  static size_t set_to[kDeviceSlots] = {};
   const size_t smem = attn_smem(a);
-  if (smem <= set_to) return cudaSuccess;
+  const int dv = device_slot();
+  if (dv >= 0 && smem <= set_to[dv]) return cudaSuccess;
   const cudaError_t e =
       cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e == cudaSuccess) set_to = smem;
+  if (e == cudaSuccess && dv >= 0) set_to[dv] = smem;
   return e;
 }
 

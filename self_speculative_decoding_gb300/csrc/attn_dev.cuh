@@ -1,5 +1,4 @@
 // Decode / verify attention: one work item = (KV head, 64-position chunk).
-// Shared by the standalone attention kernel and the persistent pass kernel.
 //
 // A pass carries M <= 16 query rows at consecutive positions pos0..pos0+M-1.
 // The item

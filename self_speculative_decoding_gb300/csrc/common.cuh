@@ -12,6 +12,17 @@ namespace ssd {
 
 typedef __nv_bfloat16 bf16;
 
+// Per-device one-time host set-up (a kernel's dynamic shared-memory limit
+// applies to the device that is current when it is set): the index of the
+// current device into tables of kDeviceSlots entries, or -1 for a device
+// beyond them (whose set-up then runs on every call).
+constexpr int kDeviceSlots = 64;
+inline int device_slot() {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kDeviceSlots) return -1;
+  return d;
+}
+
 // Largest number of rows (token positions) one pass processes together.
 constexpr int kMaxRows = 16;
 // Attention key chunk: keys are split into fixed absolute chunks of this many

@@ -1,6 +1,5 @@
-// Device bodies of the pass set-up and draft-control steps, shared by their
-// single-CTA kernels (control.cu) and by the persistent pass kernel
-// (pass.cu).  Data written by other CTAs earlier in the same kernel (row
+// Device bodies of the pass set-up and draft-control steps, run by their
+// single-CTA kernels (control.cu).  Data written by the preceding kernels (row
 // summaries, the residual stream) is read through L2 (ld.global.cg).
 #pragma once
 

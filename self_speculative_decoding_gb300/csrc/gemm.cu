@@ -478,12 +478,15 @@ cudaError_t launch_gemm_rows(const GemmArgs& a, cudaStream_t s) {
   const bool swiglu = a.epi == GEMM_SWIGLU;
   if (((uintptr_t)a.W0 | (uintptr_t)a.act | (swiglu ? (uintptr_t)a.W1 : 0)) & 15)
     return cudaErrorInvalidValue;
-  static int sms = 0;
+  static int sms_of[kDeviceSlots] = {};
+  const int dv0 = device_slot();
+  int sms = dv0 >= 0 ? sms_of[dv0] : 0;
   if (sms == 0) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
       sms = 1;
+    if (dv0 >= 0) sms_of[dv0] = sms;
   }
   const int m_tiles = (a.R / 16 + kTcGroups - 1) / kTcGroups;
   const TcShape sh = tc_shape(a.T, swiglu, m_tiles, sms);
@@ -497,12 +500,13 @@ cudaError_t launch_gemm_rows(const GemmArgs& a, cudaStream_t s) {
       !packed_map(&mx, a.act, a.K, tgroups, xbox))
     return cudaErrorInvalidValue;
   const int tx = ((swiglu ? 2 : 1) * wbox + xbox) * 1024;
-  static size_t smem_set = 0;
-  if (sh.smem > smem_set) {
+  static size_t smem_set[kDeviceSlots] = {};
+  const int dv = device_slot();
+  if (dv < 0 || sh.smem > smem_set[dv]) {
     const cudaError_t e = cudaFuncSetAttribute(
         gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sh.smem);
     if (e != cudaSuccess) return e;
-    smem_set = sh.smem;
+    if (dv >= 0) smem_set[dv] = sh.smem;
   }
   dim3 grid(sh.tiles, (groups + kTcGroups - 1) / kTcGroups);
   gemm_tc_kernel<<<grid, kTcThreads, sh.smem, s>>>(m0, m1, mx, a, sh.NT, sh.ncols, sh.stages,

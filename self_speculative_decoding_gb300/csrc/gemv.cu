@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(LinearArgs a
   pdl_trigger();
   const int M = rows_of(a.M_static, a.M_dev);
   if (warp == kEpilogue) {
-    epilogue_phase<EPI>(a, p, sm, b, M, lane, rp, nullptr);
+    epilogue_phase<EPI>(a, p, sm, b, M, lane, rp);
     return;
   }
   consumer_phase<IN, EPI>(a, p, sm, b, M, warp, lane, rp);
@@ -72,13 +72,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(LinearArgs a
 
 template <int IN, int EPI>
 cudaError_t launch_one(const LinearArgs& a, const Part& p, cudaStream_t st, bool pdl) {
-  static bool attr_set = false;
+  static bool attr_set[kDeviceSlots] = {};
   const int smem = (int)sizeof(GemvSmem) + 128;
-  if (!attr_set) {
+  const int dv = device_slot();
+  if (dv < 0 || !attr_set[dv]) {
     const cudaError_t e = cudaFuncSetAttribute(
         gemv_kernel<IN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    if (dv >= 0) attr_set[dv] = true;
   }
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(p.C);

@@ -1,12 +1,10 @@
 // Device side of the small-M weight-streaming GEMV: the packed-unit
 // partition, the producer / consumer / epilogue warp roles, and the
-// epilogues.  Used by the single-GEMV kernel (gemv.cu) and by the persistent
-// pass kernel (pass.cu), so both compute bit-identical results.
+// epilogues of the GEMV kernel (gemv.cu).
 //
-// Loads of data written earlier in the same kernel by other CTAs (the
-// residual stream, its sum-of-squares partials, activations) go through L2
-// (ld.global.cg): the persistent kernel runs several dependent phases
-// without a kernel boundary to invalidate L1.
+// Loads of data written by the preceding kernel or by other CTAs of this one
+// (the residual stream, its sum-of-squares partials, activations, split-group
+// partials) go through L2 (ld.global.cg).
 #pragma once
 
 #include "kernels.cuh"
@@ -289,10 +287,9 @@ SSD_DI void xres_prefetch(const LinearArgs& a, int vr, int M, int lane, XPre& xp
 
 // Runs in one warp once row group vr (or the gate/up pair containing it) is
 // complete; ep[h][row][tok] holds the finished sums.  Projections only (the
-// LM head goes through lm_group / lm_finish).  Returns true: the call
-// completes one signalled unit of the phase (a row group or a gate/up pair).
+// LM head goes through lm_group / lm_finish).
 template <int EPI>
-SSD_DI bool epilogue(const LinearArgs& a, const Part& p, int vr, float (*ep)[16][17], int M,
+SSD_DI void epilogue(const LinearArgs& a, const Part& p, int vr, float (*ep)[16][17], int M,
                      int lane, const XPre& xp) {
   if (EPI == EPI_STORE) {
     const int row0 = vr * 16;
@@ -328,7 +325,6 @@ SSD_DI bool epilogue(const LinearArgs& a, const Part& p, int vr, float (*ep)[16]
       a.u[(size_t)tok * a.R + row0 + row] = __float2bfloat16_rn(sl * up);
     }
   }
-  return true;
 }
 
 // Folds record q into r: top-2 and the Gumbel argmax under the total order,
@@ -751,16 +747,13 @@ SSD_DI void producer_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int
 // the consumer warps' sums added in warp order, so the result depends on the
 // matrix shape only.  The LM head (whole-group partition) folds its groups
 // into one running record per token and publishes it at the end.
-// `done` (nullable) counts finished row groups (gate/up pairs; 1 for the LM
-// head) for the persistent pass kernel.
 template <int EPI>
 SSD_DI void epilogue_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int b, int M,
-                           int lane, RingPos& rp, unsigned* done) {
+                           int lane, RingPos& rp) {
   if (b >= p.C || !rp.ok) return;
   const int U0 = unit_begin(p, b), U1 = unit_begin(p, b + 1);
   int vr = U0 / p.KB, kb = U0 % p.KB, left = U1 - U0;
   LmRec run = lm_empty();
-  unsigned nfin = 0;  // signalled units finished by this CTA
   int slot = 0, round = 0, pos0 = 0;
   if (EPI == EPI_LMHEAD) {
     slot = a.slot_dev ? __ldcg(a.slot_dev) : 0;
@@ -794,15 +787,11 @@ SSD_DI void epilogue_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.rempty[buf]);
       if (EPI == EPI_SWIGLU && h == 0) continue;  // the up group follows
-      bool fin;
-      if (EPI == EPI_LMHEAD) {
+      if (EPI == EPI_LMHEAD)
         lm_group(a, gvr, sm.ep, M, lane, slot, round, pos0, run);
-        fin = false;
-      } else {
-        fin = epilogue<EPI>(a, p, gvr, sm.ep, M, lane, xp);
-      }
+      else
+        epilogue<EPI>(a, p, gvr, sm.ep, M, lane, xp);
       __syncwarp();
-      nfin += fin ? 1u : 0u;
       continue;
     }
     // ---- split group (pair): every CTA stores its partial; the CTA that
@@ -871,18 +860,10 @@ SSD_DI void epilogue_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int
     }
     __syncwarp();
     if (lane == 0) a.counter[cidx] = 0u;
-    const bool fin = epilogue<EPI>(a, p, gvr, sm.ep, M, lane, xp);
+    epilogue<EPI>(a, p, gvr, sm.ep, M, lane, xp);
     __syncwarp();
-    nfin += fin ? 1u : 0u;
   }
-  if (EPI == EPI_LMHEAD)
-    nfin = lm_finish(a, p, b, M, lane, slot, run, reinterpret_cast<float*>(sm.stage)) ? 1u : 0u;
-  // one completion signal per CTA and phase: all of this CTA's finished
-  // units at once
-  if (done && nfin) {
-    __threadfence();
-    if (lane == 0) atomicAdd(done, nfin);
-  }
+  if (EPI == EPI_LMHEAD) lm_finish(a, p, b, M, lane, slot, run, reinterpret_cast<float*>(sm.stage));
 }
 
 // Consumer warps: RMSNorm statistics, activation staging and the MMAs for

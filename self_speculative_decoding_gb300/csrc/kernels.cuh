@@ -202,54 +202,6 @@ struct AcceptArgs {
 };
 cudaError_t launch_accept_stochastic(const AcceptArgs& a, cudaStream_t s, bool pdl);
 
-// ---------------------------------------------------------------------------
-// Persistent pass kernel: one launch runs a whole pass (embedding, layers, LM
-// head, draft control) as a program of phases; phase k starts once phase k-1
-// has signalled `target` completions on its counter.
-
-enum PassKind { PK_GEMV = 0, PK_ATTN = 1, PK_BEGIN = 2, PK_SAVE = 3, PK_DRAFT_END = 4, PK_AR_END = 5 };
-
-struct PassPhase {
-  int kind = PK_GEMV;
-  int in = IN_BF16, epi = EPI_STORE;  // PK_GEMV
-  int idx = 0;                        // index into the argument array of the kind
-  unsigned target = 1;                // completions that finish the phase
-  int use_d = 0;                      // PK_SAVE: boundary slot d (extra pass) or j
-  float tau = 0.f, temperature = 0.f; // PK_DRAFT_END / PK_AR_END
-  float tree_tau = 0.f;               // PK_DRAFT_END: sibling rule
-  int tree_max = 0;
-  int row_from_M = 0, reset = 0;      // PK_AR_END
-};
-
-struct PassProg {
-  int n = 0;
-  const PassPhase* ph = nullptr;
-  const LinearArgs* lin = nullptr;
-  const AttnArgs* att = nullptr;
-  const BeginArgs* beg = nullptr;
-  DevState* st = nullptr;
-  int32_t* tokens = nullptr;
-  const RowStats* dstats = nullptr;   // PK_DRAFT_END
-  const RowStats* vstats = nullptr;   // PK_AR_END
-  const float* x = nullptr;           // PK_SAVE
-  const float* ss = nullptr;
-  float* bx = nullptr;
-  float* bss = nullptr;
-  float* bxs = nullptr;
-  float* bsss = nullptr;
-  int D = 0;
-  unsigned* done = nullptr;           // [n], zero between launches
-  unsigned* exit_count = nullptr;     // zero between launches
-  int* abort = nullptr;               // set when any wait gave up
-  int* err = nullptr;                 // error code word (DevState::err)
-};
-
-// The pass kernel needs every CTA of its fixed grid resident at once and the
-// attention work item's shared memory to fit its staging area.
-bool pass_supported(int dh, int max_seq);
-cudaError_t pass_prepare();
-cudaError_t launch_pass(const PassProg& p, cudaStream_t s);
-
 cudaError_t launch_philox(const uint32_t* ctr, int count, uint64_t key, uint32_t* out,
                           cudaStream_t s);
 

@@ -35,7 +35,8 @@ static __device__ __align__(256) unsigned char g_linear_scratch[kNoAllocBytes];
 
 // Device address of g_linear_scratch, per device.  In host code the symbol
 // names a host-side stand-in, so the address is looked up once per device
-// with that device current.
+// with that device current.  cudaDeviceReset destroys the context that holds
+// the array, so the cached address is not valid after it.
 std::mutex g_mu;
 void* g_scratch_addr[64] = {};
 
@@ -76,8 +77,10 @@ ssd_status ssd_op_linear_noalloc(const void* W, int32_t R, int32_t K, const void
     if (!g_scratch_addr[dev]) {
       void* p = nullptr;
       e = cudaGetSymbolAddress(&p, g_linear_scratch);
-      if (e != cudaSuccess)
+      if (e != cudaSuccess) {
+        cudaGetLastError();
         return fail(SSD_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
+      }
       g_scratch_addr[dev] = p;
     }
     base = static_cast<unsigned char*>(g_scratch_addr[dev]);
@@ -86,7 +89,10 @@ ssd_status ssd_op_linear_noalloc(const void* W, int32_t R, int32_t K, const void
   // The counters (and the error word) must start at zero; the array keeps
   // whatever the previous call left there.
   e = cudaMemsetAsync(base + kCounterOffset, 0, kCounterCapacity + 256, s);
-  if (e != cudaSuccess) return fail(SSD_ERR_CUDA, std::string("cudaMemsetAsync: ") + cudaGetErrorString(e));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(SSD_ERR_CUDA, std::string("cudaMemsetAsync: ") + cudaGetErrorString(e));
+  }
 
   LinearArgs a;
   a.W0 = (const bf16*)W;
@@ -99,7 +105,10 @@ ssd_status ssd_op_linear_noalloc(const void* W, int32_t R, int32_t K, const void
   a.counter = reinterpret_cast<unsigned*>(base + kCounterOffset);
   a.err = reinterpret_cast<int*>(base + kErrOffset);
   e = launch_gemv(IN_BF16, EPI_STORE, a, s, false);
-  if (e != cudaSuccess) return fail(SSD_ERR_CUDA, std::string("launch: ") + cudaGetErrorString(e));
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // the error is reported here, not to the caller's next check
+    return fail(SSD_ERR_CUDA, std::string("launch: ") + cudaGetErrorString(e));
+  }
   return SSD_OK;
 }
 

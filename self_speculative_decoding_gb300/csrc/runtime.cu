@@ -33,18 +33,6 @@ namespace {
 
 enum Phase { PH_NONE = 0, PH_IDLE = 1, PH_DRAFTED = 2, PH_VERIFIED = 3 };
 
-// A pass program in device memory: phases, their arguments, the completion
-// counters and the abort flag (one allocation).
-struct PassDev {
-  void* buf = nullptr;
-  PassProg prog;
-  void reset() {
-    if (buf) cudaFree(buf);
-    buf = nullptr;
-    prog = PassProg();
-  }
-};
-
 struct Graph {
   cudaGraphExec_t exec = nullptr;
   int nodes = 0;
@@ -149,13 +137,8 @@ struct ssd_ctx {
   // verify pass for rounds whose d + 1 rows do not fit the GEMV activation
   // stage (norm pre-pass + bf16 projections); g_verify covers the others
   Graph g_verify_wide;
-  // persistent pass kernel programs (one launch per draft step / extra pass /
-  // verify pass / AR step) and whether they are used
   // static row bound of the passes being enqueued (0: up to 16 rows)
   int mmax = 0;
-  bool use_pass = false;
-  bool pass_ok = false;
-  PassDev p_draft, p_extra, p_verify, p_ar;
 
   Phase phase = PH_NONE;
   // profiling: events recorded around every eager launch
@@ -501,163 +484,6 @@ ssd_status enq_begin(ssd_ctx* c, int mode, cudaStream_t s, int M = 1, int pos0 =
   return note(c, launch_begin(begin_args(c, mode, M, pos0, toks_in, reset), s, c->pdl), "begin");
 }
 
-// ---------------------------------------------------------------------------
-// pass programs
-
-struct PassBuilder {
-  std::vector<PassPhase> ph;
-  std::vector<LinearArgs> lin;
-  std::vector<AttnArgs> att;
-  std::vector<BeginArgs> beg;
-
-  void gemv(int in, int epi, const LinearArgs& a, unsigned target) {
-    PassPhase p;
-    p.kind = PK_GEMV;
-    p.in = in;
-    p.epi = epi;
-    p.idx = (int)lin.size();
-    p.target = target;
-    lin.push_back(a);
-    ph.push_back(p);
-  }
-  void attention(const AttnArgs& a) {
-    PassPhase p;
-    p.kind = PK_ATTN;
-    p.idx = (int)att.size();
-    p.target = (unsigned)a.Hkv;  // one completion per combined KV head
-    att.push_back(a);
-    ph.push_back(p);
-  }
-  void begin(const BeginArgs& b) {
-    PassPhase p;
-    p.kind = PK_BEGIN;
-    p.idx = (int)beg.size();
-    beg.push_back(b);
-    ph.push_back(p);
-  }
-  void control(const PassPhase& p) { ph.push_back(p); }
-};
-
-void pb_layers(ssd_ctx* c, PassBuilder& B, const std::vector<int>& ls,
-               const std::vector<int>* parts = nullptr) {
-  const ssd_config& g = c->cfg;
-  for (size_t i = 0; i < ls.size(); ++i) {
-    const int l = ls[i], pt = parts ? (*parts)[i] : 3;
-    if (pt & 1) {
-      B.gemv(IN_NORM, EPI_STORE, qkv_args(c, l), (unsigned)(qkv_rows(g) / 16));
-      B.attention(attn_args(c, l));
-      B.gemv(IN_BF16, EPI_RESID, oproj_args(c, l), (unsigned)(g.d_model / 16));
-    }
-    if (pt & 2) {
-      B.gemv(IN_NORM, EPI_SWIGLU, gateup_args(c, l), (unsigned)(g.ffn_dim / 16));
-      B.gemv(IN_BF16, EPI_RESID, down_args(c, l), (unsigned)(g.d_model / 16));
-    }
-  }
-}
-
-size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
-
-// Uploads a built program (one device allocation).
-ssd_status pass_upload(ssd_ctx* c, const PassBuilder& B, PassDev& d) {
-  d.reset();
-  const size_t n = B.ph.size();
-  const size_t o_ph = 0;
-  const size_t o_lin = align256(o_ph + n * sizeof(PassPhase));
-  const size_t o_att = align256(o_lin + B.lin.size() * sizeof(LinearArgs));
-  const size_t o_beg = align256(o_att + B.att.size() * sizeof(AttnArgs));
-  const size_t o_done = align256(o_beg + B.beg.size() * sizeof(BeginArgs));
-  const size_t o_flags = align256(o_done + n * sizeof(unsigned));
-  const size_t total = o_flags + 256;
-  CK(cudaMalloc(&d.buf, total));
-  std::vector<unsigned char> h(total, 0);
-  memcpy(h.data() + o_ph, B.ph.data(), n * sizeof(PassPhase));
-  if (!B.lin.empty()) memcpy(h.data() + o_lin, B.lin.data(), B.lin.size() * sizeof(LinearArgs));
-  if (!B.att.empty()) memcpy(h.data() + o_att, B.att.data(), B.att.size() * sizeof(AttnArgs));
-  if (!B.beg.empty()) memcpy(h.data() + o_beg, B.beg.data(), B.beg.size() * sizeof(BeginArgs));
-  CK(cudaMemcpy(d.buf, h.data(), total, cudaMemcpyHostToDevice));
-  unsigned char* base = static_cast<unsigned char*>(d.buf);
-  PassProg& P = d.prog;
-  P.n = (int)n;
-  P.ph = reinterpret_cast<const PassPhase*>(base + o_ph);
-  P.lin = reinterpret_cast<const LinearArgs*>(base + o_lin);
-  P.att = reinterpret_cast<const AttnArgs*>(base + o_att);
-  P.beg = reinterpret_cast<const BeginArgs*>(base + o_beg);
-  P.done = reinterpret_cast<unsigned*>(base + o_done);
-  P.exit_count = reinterpret_cast<unsigned*>(base + o_flags);
-  P.abort = reinterpret_cast<int*>(base + o_flags + 64);
-  P.st = c->st;
-  P.tokens = c->tokens;
-  P.dstats = c->dstats;
-  P.vstats = c->vstats;
-  P.x = c->x;
-  P.ss = c->ss;
-  P.bx = c->bx;
-  P.bss = c->bss;
-  P.bxs = c->bxs;
-  P.bsss = c->bsss;
-  P.D = c->cfg.d_model;
-  P.err = &c->st->err;
-  return SSD_OK;
-}
-
-ssd_status build_pass_programs(ssd_ctx* c) {
-  ssd_status r;
-  {  // draft step
-    PassBuilder B;
-    B.begin(begin_args(c, BEGIN_DRAFT, 1, 0, nullptr, 0));
-    pb_layers(c, B, c->pre);
-    PassPhase sv;
-    sv.kind = PK_SAVE;
-    sv.use_d = 0;
-    B.control(sv);
-    pb_layers(c, B, c->post, &c->post_parts);
-    B.gemv(IN_NORM, EPI_LMHEAD, lm_args(c, c->dstats, c->dlogits, &c->st->slot, 0), 1u);
-    PassPhase de;
-    de.kind = PK_DRAFT_END;
-    const DraftEndArgs da = draft_end_args(c);
-    de.tau = da.tau;
-    de.temperature = da.temperature;
-    de.tree_tau = da.tree_tau;
-    de.tree_max = da.tree_max;
-    B.control(de);
-    if ((r = pass_upload(c, B, c->p_draft)) != SSD_OK) return r;
-  }
-  {  // extra pass (layers below the first skipped one for the last draft)
-    PassBuilder B;
-    B.begin(begin_args(c, BEGIN_EXTRA, 1, 0, nullptr, 0));
-    pb_layers(c, B, c->pre);
-    PassPhase sv;
-    sv.kind = PK_SAVE;
-    sv.use_d = 1;
-    B.control(sv);
-    if ((r = pass_upload(c, B, c->p_extra)) != SSD_OK) return r;
-  }
-  {  // verify pass
-    PassBuilder B;
-    B.begin(begin_args(c, BEGIN_VERIFY, 1, 0, nullptr, 0));
-    pb_layers(c, B, c->verify_layers);
-    B.gemv(IN_NORM, EPI_LMHEAD, lm_args(c, c->vstats, c->vlogits, nullptr, -1), 1u);
-    if ((r = pass_upload(c, B, c->p_verify)) != SSD_OK) return r;
-  }
-  {  // autoregressive step
-    PassBuilder B;
-    B.begin(begin_args(c, BEGIN_AR, 1, 0, nullptr, 0));
-    std::vector<int> all(c->cfg.n_layers);
-    for (int l = 0; l < c->cfg.n_layers; ++l) all[l] = l;
-    pb_layers(c, B, all);
-    B.gemv(IN_NORM, EPI_LMHEAD, lm_args(c, c->vstats, nullptr, nullptr, 2), 1u);
-    PassPhase ae;
-    ae.kind = PK_AR_END;
-    ae.temperature = c->pol.temperature;
-    ae.row_from_M = 0;
-    ae.reset = 0;
-    B.control(ae);
-    if ((r = pass_upload(c, B, c->p_ar)) != SSD_OK) return r;
-  }
-  return SSD_OK;
-}
-
-bool pass_active(const ssd_ctx* c) { return c->use_pass && c->pass_ok && !c->profiling; }
 
 // ---------------------------------------------------------------------------
 // graphs
@@ -694,7 +520,6 @@ ssd_status b_draft(ssd_ctx* c, cudaStream_t s) {
   return r;
 }
 ssd_status b_draft_body(ssd_ctx* c, cudaStream_t s) {
-  if (pass_active(c)) return note(c, launch_pass(c->p_draft.prog, s), "draft pass");
   ssd_status r;
   if ((r = enq_begin(c, BEGIN_DRAFT, s)) != SSD_OK) return r;
   if ((r = enq_layers(c, c->pre, s)) != SSD_OK) return r;
@@ -713,7 +538,6 @@ ssd_status b_extra(ssd_ctx* c, cudaStream_t s) {
   return r;
 }
 ssd_status b_extra_body(ssd_ctx* c, cudaStream_t s) {
-  if (pass_active(c)) return note(c, launch_pass(c->p_extra.prog, s), "extra pass");
   ssd_status r;
   if ((r = enq_begin(c, BEGIN_EXTRA, s)) != SSD_OK) return r;
   if ((r = enq_layers(c, c->pre, s)) != SSD_OK) return r;
@@ -743,7 +567,6 @@ ssd_status b_verify_wide(ssd_ctx* c, cudaStream_t s) {
   return r;
 }
 ssd_status b_verify_body(ssd_ctx* c, cudaStream_t s) {
-  if (pass_active(c)) return note(c, launch_pass(c->p_verify.prog, s), "verify pass");
   ssd_status r;
   if ((r = enq_begin(c, BEGIN_VERIFY, s)) != SSD_OK) return r;
   if ((r = enq_layers(c, c->verify_layers, s)) != SSD_OK) return r;
@@ -780,7 +603,6 @@ ssd_status b_ar(ssd_ctx* c, cudaStream_t s) {
   return r;
 }
 ssd_status b_ar_body(ssd_ctx* c, cudaStream_t s) {
-  if (pass_active(c)) return note(c, launch_pass(c->p_ar.prog, s), "ar pass");
   ssd_status r;
   if ((r = enq_begin(c, BEGIN_AR, s)) != SSD_OK) return r;
   std::vector<int> all(c->cfg.n_layers);
@@ -969,11 +791,9 @@ ssd_status build_loop_graph(ssd_ctx* c) {
   return r;
 }
 
-// Builds the per-pass graphs (build_pass_graphs), then the device-side
-// generation loop over them.
-ssd_status build_pass_graphs(ssd_ctx* c);
+// Builds the per-pass graphs, then the device-side generation loop over them.
 ssd_status build_graphs(ssd_ctx* c) {
-  const ssd_status r = build_pass_graphs(c);
+  const ssd_status r = build_graphs_once(c);
   if (r != SSD_OK) return r;
   // the loop graph is an optimisation: without it generation runs the same
   // graphs from the host
@@ -986,20 +806,6 @@ ssd_status build_graphs(ssd_ctx* c) {
     c->err = keep;
   }
   return SSD_OK;
-}
-
-// The per-pass graphs, with the persistent pass kernel when it is enabled and
-// usable on this device, else (or if that fails) with one kernel per step.
-ssd_status build_pass_graphs(ssd_ctx* c) {
-  c->pass_ok = false;
-  if (c->use_pass && pass_supported(c->cfg.head_dim, c->cfg.max_seq) &&
-      pass_prepare() == cudaSuccess && build_pass_programs(c) == SSD_OK) {
-    c->pass_ok = true;
-    if (build_graphs_once(c) == SSD_OK) return SSD_OK;
-    c->pass_ok = false;
-  }
-  cudaGetLastError();
-  return build_graphs_once(c);
 }
 
 ssd_status replay(ssd_ctx* c, Graph& g) {
@@ -1444,10 +1250,6 @@ ssd_status ssd_destroy(ssd_ctx* c) {
   c->g_ar.reset();
   c->g_lossy.reset();
   c->g_loop.reset();
-  c->p_draft.reset();
-  c->p_extra.reset();
-  c->p_verify.reset();
-  c->p_ar.reset();
   void* bufs[] = {c->kc, c->vc, c->x, c->ss, c->bx, c->bss, c->qkv, c->attn, c->u, c->xn, c->rope,
                   c->attn_part, c->attn_cnt, c->g_part, c->g_cnt, c->g_rec, c->dstats, c->vstats,
                   c->dlogits, c->vlogits, c->tokens, c->toks_in, c->st, c->fstats, c->ffeat,
@@ -2087,19 +1889,6 @@ ssd_status ssd_swift_generate(ssd_ctx* c, const ssd_swift_params* pp, int32_t n_
     rep->total_seconds =
         std::chrono::duration<double>(std::chrono::steady_clock::now() - t_begin).count();
   }
-  return SSD_OK;
-}
-
-ssd_status ssd_set_pass_kernel(ssd_ctx* c, int32_t enable, int32_t* active_out) {
-  if (!c) return SSD_ERR_INVALID_ARG;
-  if (c->phase == PH_DRAFTED || c->phase == PH_VERIFIED)
-    return fail(c, SSD_ERR_STATE, "a round is in flight");
-  c->use_pass = enable != 0;
-  if (c->has_policy) {
-    const ssd_status r = build_graphs(c);
-    if (r != SSD_OK) return r;
-  }
-  if (active_out) *active_out = c->use_pass && c->pass_ok ? 1 : 0;
   return SSD_OK;
 }
 

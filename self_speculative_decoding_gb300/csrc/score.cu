@@ -352,21 +352,22 @@ cudaError_t launch_score_attn(const ScoreAttnArgs& a, int n_active, cudaStream_t
   const int nw = a.N >= 64 ? 4 : (a.N + 15) / 16;
   dim3 grid((a.N + nw * 16 - 1) / (nw * 16), a.H, n_active);
   const size_t smem = score_attn_smem(a.dh);
-  static bool ready128 = false, ready64 = false;
+  static bool ready128[kDeviceSlots] = {}, ready64[kDeviceSlots] = {};
+  const int dv = device_slot();
   cudaError_t e = cudaSuccess;
   if (a.dh == 128) {
-    if (!ready128)
+    if (dv < 0 || !ready128[dv])
       e = cudaFuncSetAttribute(score_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem);
     if (e != cudaSuccess) return e;
-    ready128 = true;
+    if (dv >= 0) ready128[dv] = true;
     score_attn_kernel<128><<<grid, nw * 32, smem, s>>>(a);
   } else if (a.dh == 64) {
-    if (!ready64)
+    if (dv < 0 || !ready64[dv])
       e = cudaFuncSetAttribute(score_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem);
     if (e != cudaSuccess) return e;
-    ready64 = true;
+    if (dv >= 0) ready64[dv] = true;
     score_attn_kernel<64><<<grid, nw * 32, smem, s>>>(a);
   } else {
     return cudaErrorInvalidValue;

@@ -5,8 +5,7 @@ device) against the host-driven loop through the context C-ABI.
 * Same tokens, same committed context and the same counts (rounds, drafted,
   accepted, emitted, draft steps, siblings verified and taken) for greedy and
   sampled decoding, skip / sub-layer / exit policies, dynamic verification and
-  verify passes wider than the activation stage, with one kernel per step and
-  with the persistent pass kernel.
+  verify passes wider than the activation stage.
 * Generation continues across calls exactly as in one call.
 """
 
@@ -45,19 +44,17 @@ def ssd():
     return m
 
 
-@pytest.mark.parametrize("pass_kernel", [False, True])
 @pytest.mark.parametrize("ci", range(len(CASES)))
-def test_device_loop_equals_host_loop(ssd, ci, pass_kernel):
+def test_device_loop_equals_host_loop(ssd, ci):
     w, pol = CASES[ci]
     wts = make_weights(w, dtype="bf16", lm_head_scale=10.0, random_gains=True)
     ctx = ssd.SSDContext(w.shape, to_device_weights(wts), max_seq=256)
-    ctx.set_pass_kernel(pass_kernel)
     ctx.set_policy(pol)
     prompt = make_prompt(w, 20)
     res = {}
     for loop in (False, True):
         active = ctx.set_device_loop(loop)
-        if loop and not pass_kernel:
+        if loop:
             assert active, ctx.last_error()
         ctx.prefill(prompt)
         toks, st = ctx.generate(60)

@@ -2,8 +2,8 @@
 second choice verified with the chain) through the context C-ABI.
 
 * Greedy output with siblings is bit-identical to the library's own
-  autoregressive greedy output, with the persistent pass kernel and with one
-  kernel per step, up to 16 verify rows (the wide verify graph included).
+  autoregressive greedy output, up to 16 verify rows (the wide verify graph
+  included).
 * Round by round the emitted tokens (a taken sibling's extra token included)
   equal the oracle's until the oracle reports a near decision: a top-1/top-2
   logit gap <= 0.1 (draft, verify or sibling row), a second/third draft
@@ -60,12 +60,10 @@ def _ctx(ssd, w, head=10.0, max_seq=256):
     return ssd.SSDContext(w.shape, to_device_weights(wts), max_seq=max_seq), wts
 
 
-@pytest.mark.parametrize("pass_kernel", [False, True])
 @pytest.mark.parametrize("ci", range(len(CASES)))
-def test_tree_greedy_is_bit_identical_to_ar(ssd, ci, pass_kernel):
+def test_tree_greedy_is_bit_identical_to_ar(ssd, ci):
     w, pol = CASES[ci]
     ctx, _ = _ctx(ssd, w)
-    ctx.set_pass_kernel(pass_kernel)
     ctx.set_policy(pol)
     prompt = make_prompt(w, 20)
     ctx.prefill(prompt)

@@ -82,3 +82,16 @@ def test_gumbel_argmax_frequencies():
     keep = w > 0
     stat = chisquare(counts[keep], 20000 * w[keep])
     assert stat.pvalue > 1e-3
+
+
+def test_uniform_table_matches_single_draws():
+    # the table form (arrays of positions and rounds) gives every draw the
+    # single-position form gives, in the same vocabulary order
+    from oracle.philox import uniforms_table
+    pos = np.array([0, 5, 1023])
+    rnd = np.array([[0], [7]])
+    tab = uniforms_table(99, pos[None, :], rnd, 2, 11)
+    assert tab.shape == (2, 3, 11)
+    for i in range(2):
+        for j in range(3):
+            np.testing.assert_array_equal(tab[i, j], uniforms(99, int(pos[j]), int(rnd[i, 0]), 2, 11))
