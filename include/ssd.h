@@ -68,7 +68,18 @@ typedef struct {
   int32_t max_seq;     /* KV capacity in positions (multiple of 64)      */
   int32_t max_draft;   /* largest d_max any policy may use, 1..15        */
   int32_t max_score_rows; /* K*N capacity of ssd_score_masks (0: none)   */
+  int32_t dtype;       /* SSD_DTYPE_BF16 (0) or SSD_DTYPE_FP32 (1), below */
 } ssd_config;
+
+/* Weight and arithmetic precision of a model.  SSD_DTYPE_BF16: projection
+ * matrices bf16 in the packed layout, bf16 K/V cache, bf16 rounding at every
+ * projection input.  SSD_DTYPE_FP32: every weight fp32 and row-major (tok_embed
+ * [V, D], wqkv [(H + 2 Hkv) dh, D], wo [D, H dh], w_gate / w_up [F, D], w_down
+ * [D, F], lm_head [V, D]: not packed), fp32 K/V cache, activations and logits
+ * with no rounding anywhere; ssd_score_masks, ssd_swift_generate, dynamic
+ * verification (tree_tau > 0) and ssd_profile_kernels are for bf16 models
+ * only (SSD_ERR_INVALID_ARG). */
+enum { SSD_DTYPE_BF16 = 0, SSD_DTYPE_FP32 = 1 };
 
 /* Device pointers of one decoder layer (borrowed).  Projection matrices
  * are given in the packed layout written by ssd_pack_weight; the shapes
@@ -153,6 +164,16 @@ typedef struct {
  * device were out of memory; n < 0 disables it.  ssd_create must then return
  * SSD_ERR_OOM having released everything it allocated. */
 ssd_status ssd_debug_fail_alloc(int32_t n);
+
+/* Workspace canaries.  A library built with -DSSD_DEBUG_CHECKS follows every
+ * workspace of a context with 256 bytes of 0xA5 and bounds-checks token ids,
+ * K/V positions and pass row counts on the device (a failed check records
+ * its code, >= 100, and the offending value in the context's state, the
+ * access is skipped, and the next call reports SSD_ERR_STATE).  This call
+ * counts the canaries (*checked_out; 0 in release builds, which have none)
+ * and the canary bytes that no longer hold 0xA5 (*bad_out).  Synchronises
+ * the context's stream.  Errors: INVALID_ARG, CUDA, TIMEOUT. */
+ssd_status ssd_debug_canaries(ssd_ctx* ctx, int32_t* checked_out, int32_t* bad_out);
 
 /* Converts a row-major bf16 matrix W [R][K] (device memory) into the
  * library's packed layout at dst (device, R*K bf16, must not overlap src).
@@ -292,6 +313,20 @@ typedef struct {
   int64_t launches[8];
 } ssd_kernel_times;
 ssd_status ssd_profile_decode(ssd_ctx* ctx, int32_t n_steps, ssd_kernel_times* out);
+
+/* Per-kernel-class timing as the captured autoregressive step runs the
+ * kernels: for each class, one CUDA graph holding that class's launches for
+ * every layer (the LM head: n_layers launches of it) at the step's pass shape
+ * (one row at the pending position), chained with programmatic dependent
+ * launch as in the step's graph, replayed `reps` times after one warm-up
+ * replay between CUDA events on the context's stream.  ms[k] = device time
+ * per launch, bytes[k] = algorithmic HBM bytes per launch (weights; K/V of
+ * the current context for attention), launches[k] = launches of the class in
+ * one autoregressive step (n_layers, 1 for the LM head, 0 for class 6).  Only
+ * scratch buffers and the cache row of the pending position are written; the
+ * committed state is restored.  Errors: INVALID_ARG, STATE (no prefill, a
+ * round in flight), CAPACITY, CUDA, TIMEOUT. */
+ssd_status ssd_profile_kernels(ssd_ctx* ctx, int32_t reps, ssd_kernel_times* out);
 
 /* Host wait limit in milliseconds for calls that return host data
  * (default 120000). */

@@ -106,17 +106,24 @@ class SSDContext:
     def __init__(self, shape, weights: Dict, max_seq: int, max_draft: int = 15,
                  max_score_rows: int = 0, stream: Optional[torch.cuda.Stream] = None):
         self.shape = shape
-        if not weights.get("packed"):
-            raise ValueError("weights must be packed with pack_weights() first")
+        # fp32 models: every matrix fp32 and row-major (not packed); bf16
+        # models: projection matrices bf16 in the packed layout
+        self.fp32 = all(lw[k].dtype == torch.float32 for lw in weights["layers"] for k in MATRICES)
+        if self.fp32:
+            if weights["tok_embed"].dtype != torch.float32 or weights["lm_head"].dtype != torch.float32:
+                raise ValueError("an fp32 model needs fp32 tok_embed and lm_head")
+        elif not weights.get("packed"):
+            raise ValueError("bf16 weights must be packed with pack_weights() first")
         self._weights = weights  # keep the tensors alive
         cfg = SsdConfig(shape.n_layers, shape.d_model, shape.n_heads, shape.n_kv_heads,
                         shape.head_dim, shape.ffn_dim, shape.vocab, shape.rope_theta,
-                        shape.norm_eps, max_seq, max_draft, max_score_rows)
+                        shape.norm_eps, max_seq, max_draft, max_score_rows,
+                        _abi.SSD_DTYPE_FP32 if self.fp32 else _abi.SSD_DTYPE_BF16)
         self._layers = (SsdLayerWeights * shape.n_layers)()
         for i, lw in enumerate(weights["layers"]):
-            for k in ("wqkv", "wo", "w_gate", "w_up", "w_down"):
-                if lw[k].dtype != torch.bfloat16:
-                    raise ValueError(f"layer {i} {k}: the library computes with bf16 weights")
+            for k in MATRICES:
+                if lw[k].dtype != (torch.float32 if self.fp32 else torch.bfloat16):
+                    raise ValueError(f"layer {i} {k}: every matrix must have the model's dtype")
             self._layers[i] = SsdLayerWeights(_ptr(lw["attn_norm"]), _ptr(lw["wqkv"]),
                                               _ptr(lw["wo"]), _ptr(lw["mlp_norm"]),
                                               _ptr(lw["w_gate"]), _ptr(lw["w_up"]),
@@ -245,6 +252,21 @@ class SSDContext:
         """Per-kernel-class device time (CUDA events on the context stream)."""
         out = _abi.SsdKernelTimes()
         self._check(_lib().ssd_profile_decode(self._h, n_steps, C.byref(out)))
+        return out.as_dict()
+
+    def debug_canaries(self) -> Tuple[int, int]:
+        """(canaries checked, canary bytes overwritten); (0, 0) in release
+        builds (ssd_debug_canaries)."""
+        n, bad = C.c_int32(0), C.c_int32(0)
+        self._check(_lib().ssd_debug_canaries(self._h, C.byref(n), C.byref(bad)))
+        return n.value, bad.value
+
+    def profile_kernels(self, reps: int = 5) -> dict:
+        """Per-kernel-class device time with each class's launches of one
+        autoregressive step captured as a graph and replayed (ssd.h:
+        ssd_profile_kernels); launches = per step."""
+        out = _abi.SsdKernelTimes()
+        self._check(_lib().ssd_profile_kernels(self._h, reps, C.byref(out)))
         return out.as_dict()
 
     def set_timeout_ms(self, ms: int):

@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import ctypes as C
 import os
+from typing import Optional
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libssd.so")
@@ -18,13 +19,16 @@ STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "STATE", 3: "CAPACITY", 4: "OOM", 
                 6: "TIMEOUT"}
 SSD_MODE_SKIP = 0
 SSD_MODE_EXIT = 1
+SSD_DTYPE_BF16 = 0
+SSD_DTYPE_FP32 = 1
 
 
 class SsdConfig(C.Structure):
     _fields_ = [("n_layers", C.c_int32), ("d_model", C.c_int32), ("n_heads", C.c_int32),
                 ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("ffn_dim", C.c_int32),
                 ("vocab", C.c_int32), ("rope_theta", C.c_float), ("norm_eps", C.c_float),
-                ("max_seq", C.c_int32), ("max_draft", C.c_int32), ("max_score_rows", C.c_int32)]
+                ("max_seq", C.c_int32), ("max_draft", C.c_int32), ("max_score_rows", C.c_int32),
+                ("dtype", C.c_int32)]
 
 
 class SsdLayerWeights(C.Structure):
@@ -111,6 +115,8 @@ _SIGS = {
     "ssd_swift_generate": [_P, C.POINTER(SsdSwiftParams), _I, _P, _P, _P, _P, _I,
                            C.POINTER(SsdSwiftReport)],
     "ssd_profile_decode": [_P, _I, C.POINTER(SsdKernelTimes)],
+    "ssd_profile_kernels": [_P, _I, C.POINTER(SsdKernelTimes)],
+    "ssd_debug_canaries": [_P, C.POINTER(C.c_int32), C.POINTER(C.c_int32)],
     "ssd_last_error": [_P],
     "ssd_op_linear": [_P, _I, _I, _P, _I, _P, _P],
     "ssd_op_rmsnorm_linear": [_P, _I, _I, _P, _P, C.c_float, _I, _P, _P],
@@ -132,7 +138,10 @@ _SIGS = {
 EXPORTED = tuple(_SIGS)
 
 
-def load(path: str = LIB_PATH) -> C.CDLL:
+def load(path: Optional[str] = None) -> C.CDLL:
+    """The library at ``path``; default: $SSD_LIBSSD if set (another build of
+    the library, e.g. the debug build), else the in-tree libssd.so."""
+    path = path or os.environ.get("SSD_LIBSSD") or LIB_PATH
     if not os.path.exists(path):
         raise ImportError(
             f"libssd.so not found at {path}: build it with "

@@ -39,6 +39,19 @@ __global__ void __launch_bounds__(attn::kGroupThreads, 4) attn_kernel(AttnArgs a
   const int M = a.M_dev ? __ldcg(a.M_dev) : a.M_static;
   const int pos0 = a.pos0_dev ? __ldcg(a.pos0_dev) : a.pos0_static;
   const int ns = a.ns_dev ? __ldcg(a.ns_dev) : 0;  // side rows (after the chain rows)
+  {
+    // debug builds: the pass's rows and positions lie inside the cache
+    int* e = blockIdx.x == 0 && tid == 0 ? a.err : nullptr;
+    bool ok = SSD_CHECK_W(e, a.err_val, M >= 1 && M <= kMaxRows && ns >= 0 && ns <= kMaxSide &&
+                                            ns < M, DBG_ROWS, M);
+    ok = ok && SSD_CHECK_W(e, a.err_val, pos0 >= 0 && pos0 + M - ns <= a.max_seq, DBG_POS,
+                           pos0 + M - ns);
+    for (int i = 0; ok && i < ns; ++i) {
+      const int sp = __ldcg(a.side_pos + i);
+      ok = SSD_CHECK_W(e, a.err_val, sp >= 0 && sp < pos0 + M - ns, DBG_POS, sp);
+    }
+    if (!ok) return;
+  }
   const attn::Smem sm = attn::carve(smem_raw, a.dh, a.max_seq / kAttnChunk);
   const int n_items = ((pos0 + M - ns - 1) / kAttnChunk + 1) * a.Hkv;
   uint32_t phase = 0;

@@ -77,9 +77,46 @@ struct DevState {
   int32_t last_d;
   int32_t acc_rounds, acc_drafted, acc_accepted, acc_emitted;
   int32_t acc_steps, acc_extra, acc_side_rows, acc_side_acc;
-  int32_t pad2[1];
+  // debug builds (SSD_DEBUG_CHECKS): the value that failed the bounds check
+  // recorded in err (codes >= kDbgCodeBase), and the bounds the checks use
+  int32_t err_val;
+  int32_t vocab, max_seq;
+  int32_t pad2[2];
 };
 static_assert(sizeof(DevState) % 16 == 0, "DevState layout");
+
+// Debug builds (compiled with -DSSD_DEBUG_CHECKS): device-side bounds checks
+// on token ids, KV positions and pass row counts.  A failed check records
+// its code and the offending value in the state's error words (the first
+// failure wins) and the caller skips or clamps the access; nothing traps.
+// Release builds compile every check to `true`.
+constexpr int kDbgCodeBase = 100;
+enum DbgCode {
+  DBG_TOKEN = 101,     // a token id outside [0, vocab)
+  DBG_POS = 102,       // a K/V position outside [0, max_seq)
+  DBG_ROWS = 103,      // a pass row count outside [1, 16]
+  DBG_COMMIT = 104,    // committed tokens beyond max_seq
+};
+#ifdef SSD_DEBUG_CHECKS
+SSD_DI bool dbg_check(DevState* st, bool ok, int code, int value) {
+  if (ok) return true;
+  if (st && atomicCAS(&st->err, 0, code) == 0) st->err_val = value;
+  return false;
+}
+// The same for kernels given the error words (err, err_val) instead of the
+// state.
+SSD_DI bool dbg_check_words(int* err, int* err_val, bool ok, int code, int value) {
+  if (ok) return true;
+  if (err && atomicCAS(err, 0, code) == 0 && err_val) *err_val = value;
+  return false;
+}
+#define SSD_CHECK(st, cond, code, value) ::ssd::dbg_check((st), (cond), (code), (int)(value))
+#define SSD_CHECK_W(err, err_val, cond, code, value) \
+  ::ssd::dbg_check_words((err), (err_val), (cond), (code), (int)(value))
+#else
+#define SSD_CHECK(st, cond, code, value) true
+#define SSD_CHECK_W(err, err_val, cond, code, value) true
+#endif
 
 
 // ---------------------------------------------------------------------------
@@ -173,6 +210,11 @@ SSD_DI void cp_async16(void* dst, const void* src) {
                : "memory");
 }
 SSD_DI void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Closes this thread's group of cp.async copies issued since the last commit.
+SSD_DI void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's committed groups are still in flight.
+template <int N>
+SSD_DI void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // Bulk prefetch of global memory into L2 (address and size multiples of 16).
 SSD_DI void bulk_prefetch_l2(const void* src, uint32_t bytes) {

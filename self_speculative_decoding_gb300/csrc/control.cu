@@ -63,6 +63,10 @@ __global__ void accept_greedy_kernel(DevState* st, int32_t* tokens, const RowSta
       if (st->sib_depth[i] == a && st->sib_tok[i] == t) sib = i;
   int ne = a + 1;
   if (sib >= 0) st->emitted[ne++] = vstats[d + 1 + sib].top1;
+  for (int i = 0; i < ne; ++i)
+    if (!SSD_CHECK(st, st->emitted[i] >= 0 && st->emitted[i] < st->vocab, DBG_TOKEN, st->emitted[i]))
+      st->emitted[i] = 0;
+  if (!SSD_CHECK(st, n + ne <= st->max_seq, DBG_COMMIT, n + ne)) return;
   for (int i = 0; i < ne; ++i) tokens[n + i] = st->emitted[i];
   st->n = n + ne;
   st->n_emitted = ne;
@@ -257,6 +261,10 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_stoch_kernel(AcceptArgs
     if (st) {
       for (int i = 0; i < acc; ++i) st->emitted[i] = drafts[i];
       st->emitted[acc] = bi;
+      for (int i = 0; i <= acc; ++i)
+        if (!SSD_CHECK(st, st->emitted[i] >= 0 && st->emitted[i] < a.V, DBG_TOKEN, st->emitted[i]))
+          st->emitted[i] = 0;
+      if (!SSD_CHECK(st, n + acc + 1 <= st->max_seq, DBG_COMMIT, n + acc + 1)) return;
       for (int i = 0; i <= acc; ++i) a.tokens[n + i] = st->emitted[i];
       st->n = n + acc + 1;
       st->n_emitted = acc + 1;

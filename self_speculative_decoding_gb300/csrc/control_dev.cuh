@@ -69,6 +69,10 @@ SSD_DI void begin(const BeginArgs& a, int tid, int nthr, int* s_M, int* s_tok, S
         for (int i = 0; i < ns; ++i) st->side_pos[i] = st->n + st->sib_depth[i];
         break;
     }
+    if (!SSD_CHECK(st, M >= 1 && M <= kMaxRows, DBG_ROWS, M)) M = 1;
+    if (!SSD_CHECK(st, pos0 >= 0 && pos0 + M <= st->max_seq, DBG_POS, pos0 + M)) pos0 = 0;
+    for (int m = 0; m < M && a.mode != BEGIN_VERIFY; ++m)
+      if (!SSD_CHECK(st, s_tok[m] >= 0 && s_tok[m] < st->vocab, DBG_TOKEN, s_tok[m])) s_tok[m] = 0;
     st->M = M;
     st->pos0 = pos0;
     st->slot = slot;
@@ -91,11 +95,11 @@ SSD_DI void begin(const BeginArgs& a, int tid, int nthr, int* s_M, int* s_tok, S
   }
   for (int e = tid; e < M * NP; e += nthr) {
     const int m = e / NP, grp = e % NP;
-    const bf16* src = a.embed + (size_t)s_tok[m] * D + grp * kSsGroup;
+    const size_t off = (size_t)s_tok[m] * D + grp * kSsGroup;
     float* dst = a.x + (size_t)m * D + grp * kSsGroup;
     float s = 0.f;
     for (int i = 0; i < kSsGroup; ++i) {
-      const float v = __bfloat162float(src[i]);
+      const float v = a.embed32 ? a.embed32[off + i] : __bfloat162float(a.embed[off + i]);
       dst[i] = v;
       s += v * v;
     }
@@ -167,8 +171,10 @@ SSD_DI void ar_end(DevState* st, int32_t* tokens, const RowStats* vstats, int ro
                    int reset) {
   const int row = row_from_M ? st->M - 1 : 0;
   const RowStats rs = load_stats(vstats + row);
-  const int tok = T > 0.f ? rs.sample : rs.top1;
+  int tok = T > 0.f ? rs.sample : rs.top1;
   const int n = reset ? st->pos0 + st->M : st->n;
+  if (!SSD_CHECK(st, tok >= 0 && tok < st->vocab, DBG_TOKEN, tok)) tok = 0;
+  if (!SSD_CHECK(st, n >= 0 && n < st->max_seq, DBG_COMMIT, n)) return;
   tokens[n] = tok;
   st->n = n + 1;
   st->emitted[0] = tok;

@@ -51,23 +51,30 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(LinearArgs a
       mbar_init(&sm.rfull[s], kConsumers);
       mbar_init(&sm.rempty[s], 1);
     }
+    mbar_init(&sm.foldbar, 1);
     fence_mbar_init();
   }
   __syncthreads();
   RingPos rp;
   if (warp == kProducer) {
     // weights do not depend on the preceding kernel: no wait before streaming
-    producer_phase<EPI>(a, p, sm, b, lane, rp);
+    producer_phase<IN, EPI>(a, p, sm, b, lane, rp);
     return;
   }
   pdl_wait();
   pdl_trigger();
-  const int M = rows_of(a.M_static, a.M_dev);
+  int M = rows_of(a.M_static, a.M_dev);
+  if (!SSD_CHECK_W(b == 0 && warp == 0 && lane == 0 ? a.err : nullptr, a.err_val,
+                   M >= 1 && M <= kMaxRows, DBG_ROWS, M))
+    M = M < 1 ? 1 : kMaxRows;
   if (warp == kEpilogue) {
-    epilogue_phase<EPI>(a, p, sm, b, M, lane, rp);
+    LmRec run = lm_empty();
+    epilogue_phase<EPI>(a, p, sm, b, M, lane, rp, run);
+    if (EPI == EPI_LMHEAD) lm_end(a, p, sm, b, M, warp, lane, rp, run, true);
     return;
   }
   consumer_phase<IN, EPI>(a, p, sm, b, M, warp, lane, rp);
+  if (EPI == EPI_LMHEAD) lm_end(a, p, sm, b, M, warp, lane, rp, lm_empty(), false);
 }
 
 template <int IN, int EPI>
@@ -176,8 +183,10 @@ GemvScratch gemv_scratch(int R, int K, int epi) {
   return s;
 }
 
-cudaError_t launch_gemv(int in_mode, int epi, const LinearArgs& a, cudaStream_t st, bool pdl) {
-  if (!part_fits(a.R, a.K)) return cudaErrorInvalidValue;
+cudaError_t launch_gemv(int in_mode, int epi, const LinearArgs& a0, cudaStream_t st, bool pdl) {
+  if (!part_fits(a0.R, a0.K)) return cudaErrorInvalidValue;
+  LinearArgs a = a0;
+  if (!a.M_dev && a.M_static > gemv_stage_rows(a.K)) a.wide = 1;
   const Part p = make_part(a.R, a.K, epi);
 #define SSD_GEMV_CASE(I, E) \
   if (in_mode == I && epi == E) return launch_one<I, E>(a, p, st, pdl);

@@ -378,55 +378,55 @@ SSD_DI void lm_group(const LinearArgs& a, int vr, float (*ep)[16][17], int M, in
 }
 
 // LM head, end of CTA b's range: publish the CTA's records (one per token,
-// stored [tok][b]); the CTA that publishes last folds all CTAs' records in
-// CTA order and writes the row summaries.  `stage` holds C records.
-// Returns true in the CTA that wrote the summaries.
-SSD_DI bool lm_finish(const LinearArgs& a, const Part& p, int b, int M, int lane, int slot,
-                      const LmRec& run, float* stage) {
-  const float T = a.temperature;
+// stored [tok][b]).  Returns (in every lane) whether this CTA published
+// last, i.e. every CTA's records are in.
+SSD_DI bool lm_publish(const LinearArgs& a, const Part& p, int b, int M, int lane,
+                       const LmRec& run) {
   if (lane < M) lm_store(a.rec + ((size_t)lane * p.C + b) * 8, run);
   __threadfence();
   __syncwarp();
   int last = 0;
   if (lane == 0) last = atomicAdd(a.counter, 1u) == (unsigned)(p.C - 1);
-  last = __shfl_sync(0xffffffffu, last, 0);
-  if (!last) return false;
-  __threadfence();
-  for (int tok = 0; tok < M; ++tok) {
-    // all C records of this token into shared memory (independent loads)
-    const float4* src = reinterpret_cast<const float4*>(a.rec + (size_t)tok * p.C * 8);
-    float4* dst = reinterpret_cast<float4*>(stage);
-#pragma unroll 4
-    for (int i = lane; i < 2 * p.C; i += 32) dst[i] = __ldcg(src + i);
-    __syncwarp();
-    // lane l folds CTAs l, l+32, ... in order, then a butterfly
-    LmRec r = lm_empty();
-    for (int c = lane; c < p.C; c += 32) {
-      const float4 x0 = dst[2 * c], x1 = dst[2 * c + 1];
-      LmRec q;
-      q.v1 = x0.x; q.i1 = __float_as_int(x0.y); q.v2 = x0.z; q.i2 = __float_as_int(x0.w);
-      q.se = x1.x; q.set = x1.y; q.gv = x1.z; q.gi = __float_as_int(x1.w);
-      lm_combine(r, q, T);
-    }
-    r = lm_merge_warp(r, T);
-    if (lane == 0) {
-      RowStats rs;
-      rs.top1 = r.i1;
-      rs.top2 = r.i2;
-      rs.sample = T > 0.f && a.sample ? r.gi : r.i1;
-      rs.pad = 0;
-      rs.z1 = r.v1;
-      rs.z2 = r.v2;
-      rs.lse = r.v1 + logf(r.se);
-      rs.conf = expf(r.v1 - rs.lse);
-      rs.lse_t = T > 0.f ? r.v1 / T + logf(r.set) : rs.lse;
-      rs.pad2[0] = rs.pad2[1] = rs.pad2[2] = 0.f;
-      a.stats[slot + tok] = rs;
-    }
-    __syncwarp();
+  return __shfl_sync(0xffffffffu, last, 0) != 0;
+}
+
+// LM head, token tok's row summary from all C records (one warp): the
+// records go to `stage` (C x 32 bytes of shared memory, this warp's own)
+// with 16-byte asynchronous copies, all in flight at once; lane l folds
+// CTAs l, l+32, ... in order, then a butterfly.  The order depends on C
+// alone, so a token's summary does not depend on how many tokens the pass
+// carries or on which warp folds it.
+SSD_DI void lm_fold(const LinearArgs& a, const Part& p, int tok, int lane, int slot, float* stage) {
+  const float T = a.temperature;
+  const float4* src = reinterpret_cast<const float4*>(a.rec + (size_t)tok * p.C * 8);
+  float4* dst = reinterpret_cast<float4*>(stage);
+  for (int i = lane; i < 2 * p.C; i += 32) cp_async16(dst + i, src + i);
+  cp_async_wait_all();
+  __syncwarp();
+  LmRec r = lm_empty();
+  for (int c = lane; c < p.C; c += 32) {
+    const float4 x0 = dst[2 * c], x1 = dst[2 * c + 1];
+    LmRec q;
+    q.v1 = x0.x; q.i1 = __float_as_int(x0.y); q.v2 = x0.z; q.i2 = __float_as_int(x0.w);
+    q.se = x1.x; q.set = x1.y; q.gv = x1.z; q.gi = __float_as_int(x1.w);
+    lm_combine(r, q, T);
   }
-  if (lane == 0) a.counter[0] = 0u;
-  return true;
+  r = lm_merge_warp(r, T);
+  if (lane == 0) {
+    RowStats rs;
+    rs.top1 = r.i1;
+    rs.top2 = r.i2;
+    rs.sample = T > 0.f && a.sample ? r.gi : r.i1;
+    rs.pad = 0;
+    rs.z1 = r.v1;
+    rs.z2 = r.v2;
+    rs.lse = r.v1 + logf(r.se);
+    rs.conf = expf(r.v1 - rs.lse);
+    rs.lse_t = T > 0.f ? r.v1 / T + logf(r.set) : rs.lse;
+    rs.pad2[0] = rs.pad2[1] = rs.pad2[2] = 0.f;
+    a.stats[slot + tok] = rs;
+  }
+  __syncwarp();
 }
 
 // ---------------------------------------------------------------- kernel
@@ -440,8 +440,16 @@ struct __align__(16) GemvSmem {
   uint64_t empty[kSlots];            // slot consumed by all consumer warps
   uint64_t rfull[2];                 // partial buffer written by all consumer warps
   uint64_t rempty[2];                // partial buffer read by the epilogue warp
+  uint64_t foldbar;                  // LM head: the epilogue warp knows whether this CTA folds
+  int fold_last;
   __align__(16) bf16 stage[kStageBytes / 2];
 };
+// LM head fold: each of the kConsumers + 1 folding warps stages C records
+// (at most kGridCtas x 32 bytes) in its own part of the ring and the stage.
+constexpr int kFoldBytes = 10240;
+static_assert(kGridCtas * 32 <= kFoldBytes, "a warp's fold staging holds every CTA's record");
+static_assert(4 * kFoldBytes <= kRingBytes && (kConsumers - 3) * kFoldBytes <= kStageBytes,
+              "the folding warps' staging fits the ring and the stage");
 
 // Position of a warp role in the slot ring and in the partial hand-off
 // sequence; persists across the GEMV phases of one kernel.
@@ -570,19 +578,47 @@ SSD_DI void consume(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0, in
   rp.fl = fl;
 }
 
-// Windowed activations (bf16 input, whole-group partition, rows that do not
-// fit the stage at once): the consumer warps stage the activations of 16
-// units (512 K-columns) at a time in two shared buffers.  The loads of
-// window w + 2 are issued while window w is consumed; at the end of window w
-// they are stored into the buffer window w - 1 used, and one consumer
-// barrier publishes them.  B values and the MMA order are those of the
-// other layouts, so a row's result does not depend on the layout.
+// Batched K-outer order (bf16 input, whole-group partition, passes whose rows
+// may not fit the stage: LinearArgs::wide).  A CTA takes its row groups in
+// batches of up to kBatch (whole gate/up pairs for SwiGLU); within a batch it
+// goes through K in windows of kWinUnits units (512 columns), and within a
+// window through the batch's groups, each in chunks of up to kChunk units.
+// The activations of a window (the pass's rows x 512 columns) are copied to
+// shared memory once per batch with cp.async into a ring of kWinBufs buffers,
+// two windows ahead of the one being consumed.  The chunks, the unit each
+// warp takes and the order in which a warp accumulates a group's units are
+// those of the staged layout, so every row's bits are the same in both.
 constexpr int kWinUnits = 16;
 constexpr int kWinRow = kWinUnits * 32 * 2 + 64;   // bytes per row; rows 16 banks apart
 constexpr int kWinBytes = kMaxRows * kWinRow;
-constexpr int kWinPieces = kMaxRows * kWinUnits * 4 / (kConsumers * 32);  // 16-byte pieces per thread
-static_assert(2 * kWinBytes <= kStageBytes, "two activation windows fit the stage");
+constexpr int kWinBufs = 3;
+#ifndef SSD_GEMV_BATCH
+#define SSD_GEMV_BATCH 4
+#endif
+constexpr int kBatch = SSD_GEMV_BATCH;             // row groups per batch (even: whole pairs)
+static_assert(kWinBufs * kWinBytes <= kStageBytes, "the window ring fits the stage");
 static_assert(kWinUnits % kChunk == 0, "windows hold whole chunks");
+static_assert(kBatch % 2 == 0, "a batch holds whole gate/up pairs");
+
+template <int IN, int EPI>
+SSD_HD bool kouter_order(const LinearArgs& a, const Part& p) {
+  return IN == IN_BF16 && a.wide && p.G == p.KB * (EPI == EPI_SWIGLU ? 2 : 1);
+}
+
+// Calls f(vr, kb, n) for every chunk of CTA range [U0, U1) (whole groups) in
+// the batched K-outer order.
+template <class F>
+SSD_DI void kouter_chunks(const Part& p, int U0, int U1, F&& f) {
+  const int KB = p.KB, g_end = U1 / KB;
+  for (int g0 = U0 / KB; g0 < g_end; g0 += kBatch) {
+    const int nb = min(kBatch, g_end - g0);
+    for (int kw = 0; kw < KB; kw += kWinUnits) {
+      const int ke = min(kw + kWinUnits, KB);
+      for (int gi = 0; gi < nb; ++gi)
+        for (int kb = kw; kb < ke; kb += kChunk) f(g0 + gi, kb, min(kChunk, ke - kb));
+    }
+  }
+}
 
 template <int EPI>
 SSD_DI void consume_win(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0, int U1, int M,
@@ -591,98 +627,90 @@ SSD_DI void consume_win(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0
   const int g = lane >> 2, c = lane & 3;
   const bool two = M > 8;
   const bool v0 = g < M, v1 = two && (g + 8) < M;
-  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
   unsigned char* wb = reinterpret_cast<unsigned char*>(sm.stage);
   const int KB = p.KB;
-  const int nwin = (KB + kWinUnits - 1) / kWinUnits;  // windows per row group
-  const int vr_end = U1 / KB;
-  uint4 pre[kWinPieces];
-  // window (vr, kw) -> registers: row m, K columns kw*512 + 8q .. + 7
-  auto load = [&](int kw) {
-    const int wu = min(kWinUnits, KB - kw * kWinUnits);
-#pragma unroll
-    for (int i = 0; i < kWinPieces; ++i) {
-      const int e = tid + i * kConsumers * 32;
-      const int m = e / (kWinUnits * 4), q = e % (kWinUnits * 4);
-      pre[i] = m < M && q < wu * 4
-                   ? __ldcg(reinterpret_cast<const uint4*>(a.act + (size_t)m * a.K +
-                                                           (size_t)kw * kWinUnits * 32 + q * 8))
-                   : make_uint4(0u, 0u, 0u, 0u);
+  const int nwin = (KB + kWinUnits - 1) / kWinUnits;  // windows per batch
+  const int g_begin = U0 / KB, g_end = U1 / KB;
+  const int nbatch = (g_end - g_begin + kBatch - 1) / kBatch;
+  const int total = nbatch * nwin;                    // windows this CTA consumes
+  // window q (K window q % nwin of batch q / nwin) into buffer q % kWinBufs;
+  // one commit per window, empty past the end, so the group count is uniform
+  auto issue = [&](int q) {
+    if (q < total) {
+      const int kw = q % nwin;
+      const int wu = min(kWinUnits, KB - kw * kWinUnits);
+      unsigned char* dst = wb + (q % kWinBufs) * kWinBytes;
+      const bf16* src = a.act + (size_t)kw * kWinUnits * 32;
+      for (int e = tid; e < M * kWinUnits * 4; e += kConsumers * 32) {
+        const int m = e / (kWinUnits * 4), qq = e % (kWinUnits * 4);
+        if (qq < wu * 4) cp_async16(dst + m * kWinRow + qq * 16, src + (size_t)m * a.K + qq * 8);
+      }
     }
+    cp_async_commit();
   };
-  auto store = [&](int buf) {
+  issue(0);
+  issue(1);
+  float acc[kBatch][2][4];
 #pragma unroll
-    for (int i = 0; i < kWinPieces; ++i) {
-      const int e = tid + i * kConsumers * 32;
-      const int m = e / (kWinUnits * 4), q = e % (kWinUnits * 4);
-      if (m < M) *reinterpret_cast<uint4*>(wb + buf * kWinBytes + m * kWinRow + q * 16) = pre[i];
-    }
-  };
-  // the window after (vr, kw) in this CTA's sequence, as (vr, kw); vr == vr_end: none
-  auto advance = [&](int& vr, int& kw) {
-    if (++kw == nwin) { kw = 0; ++vr; }
-  };
-  int vr = U0 / KB, kw = 0, wseq = 0;
-  load(0);
-  store(0);
-  consumer_sync();
-  int nvr = vr, nkw = kw;  // the window whose loads are in flight in `pre`
-  advance(nvr, nkw);
-  if (nvr < vr_end) load(nkw);
-
-  int kb = 0, left = U1 - U0;
+  for (int gi = 0; gi < kBatch; ++gi)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) acc[gi][h][0] = acc[gi][h][1] = acc[gi][h][2] = acc[gi][h][3] = 0.f;
   int slot = rp.slot;
   uint32_t ph = rp.ph;
   int fl = rp.fl;
   // A failed wait does not leave the loop: every consumer warp must take part
   // in every window barrier, so a warp that gave up runs on without waiting.
   bool okw = rp.ok;
-  while (left > 0) {
-    const int n = chunk_len(p, kb, left);
-    if (okw && !mbar_wait(&sm.full[slot], ph)) {
-      if (lane == 0) atomicExch(a.err, 3);
-      okw = false;
-    }
-    const unsigned char* wbase = wb + (wseq & 1) * kWinBytes;
+  int q = 0;
+  for (int g0 = g_begin; g0 < g_end; g0 += kBatch) {
+    const int nb = min(kBatch, g_end - g0);
+    for (int kw = 0; kw < nwin; ++kw, ++q) {
+      // window q has landed (for every thread's copies) and every warp is
+      // done with window q - 1, whose buffer window q + 2 now takes
+      cp_async_wait_group<1>();
+      consumer_sync();
+      issue(q + 2);
+      const unsigned char* wbase = wb + (q % kWinBufs) * kWinBytes;
+      const int kb0 = kw * kWinUnits, ke = min(kb0 + kWinUnits, KB);
 #pragma unroll
-    for (int i = 0; i < kUPW; ++i) {
-      const int un = warp + i * kConsumers;
-      if (un < n) {
-        const unsigned char* base = sm.ring + slot * kSlotBytes + un * kUnitBytes;
-        const uint4 wa = *reinterpret_cast<const uint4*>(base + unit_slot(lane));
-        const uint4 wbv = *reinterpret_cast<const uint4*>(base + 512 + unit_slot(lane));
-        const int col = ((kb - kw * kWinUnits) + un) * 64 + c * 16;  // bytes into the row
-        const uint4 xa = v0 ? *reinterpret_cast<const uint4*>(wbase + g * kWinRow + col)
-                            : make_uint4(0u, 0u, 0u, 0u);
-        mma_bf16(acc[0], wa.x, wbv.x, wa.y, wbv.y, xa.x, xa.y);
-        mma_bf16(acc[0], wa.z, wbv.z, wa.w, wbv.w, xa.z, xa.w);
-        if (two) {
-          const uint4 xb = v1 ? *reinterpret_cast<const uint4*>(wbase + (g + 8) * kWinRow + col)
-                              : make_uint4(0u, 0u, 0u, 0u);
-          mma_bf16(acc[1], wa.x, wbv.x, wa.y, wbv.y, xb.x, xb.y);
-          mma_bf16(acc[1], wa.z, wbv.z, wa.w, wbv.w, xb.z, xb.w);
+      for (int gi = 0; gi < kBatch; ++gi) {
+        if (gi >= nb) break;
+        for (int kb = kb0; kb < ke; kb += kChunk) {
+          const int n = min(kChunk, ke - kb);
+          if (okw && !mbar_wait(&sm.full[slot], ph)) {
+            if (lane == 0) atomicExch(a.err, 3);
+            okw = false;
+          }
+#pragma unroll
+          for (int i = 0; i < kUPW; ++i) {
+            const int un = warp + i * kConsumers;
+            if (un < n) {
+              const unsigned char* base = sm.ring + slot * kSlotBytes + un * kUnitBytes;
+              const uint4 wa = *reinterpret_cast<const uint4*>(base + unit_slot(lane));
+              const uint4 wbv = *reinterpret_cast<const uint4*>(base + 512 + unit_slot(lane));
+              const int col = ((kb - kb0) + un) * 64 + c * 16;  // bytes into the row
+              const uint4 xa = v0 ? *reinterpret_cast<const uint4*>(wbase + g * kWinRow + col)
+                                  : make_uint4(0u, 0u, 0u, 0u);
+              mma_bf16(acc[gi][0], wa.x, wbv.x, wa.y, wbv.y, xa.x, xa.y);
+              mma_bf16(acc[gi][0], wa.z, wbv.z, wa.w, wbv.w, xa.z, xa.w);
+              if (two) {
+                const uint4 xb = v1 ? *reinterpret_cast<const uint4*>(wbase + (g + 8) * kWinRow + col)
+                                    : make_uint4(0u, 0u, 0u, 0u);
+                mma_bf16(acc[gi][1], wa.x, wbv.x, wa.y, wbv.y, xb.x, xb.y);
+                mma_bf16(acc[gi][1], wa.z, wbv.z, wa.w, wbv.w, xb.z, xb.w);
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.empty[slot]);
+          if (++slot == kSlots) { slot = 0; ph ^= 1u; }
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.empty[slot]);
-    if (++slot == kSlots) { slot = 0; ph ^= 1u; }
-    kb += n;
-    left -= n;
-    const bool group_done = kb == KB;
-    const bool win_done = group_done || kb % kWinUnits == 0;
-    if (win_done && left > 0) {
-      // the next window (loaded one window ago) goes into the other buffer
-      store((wseq + 1) & 1);
-      consumer_sync();
-      ++wseq;
-      advance(vr, kw);
-      advance(nvr, nkw);
-      if (nvr < vr_end) load(nkw);
-    }
-    if (group_done) kb = 0;
-    if (!group_done) continue;
-    {
+    // the batch's groups are done: hand them to the epilogue warp in order
+#pragma unroll
+    for (int gi = 0; gi < kBatch; ++gi) {
+      if (gi >= nb) break;
       const int buf = fl & 1;
       if (okw && fl >= 2 && !mbar_wait(&sm.rempty[buf], ((fl >> 1) - 1) & 1)) {
         if (lane == 0) atomicExch(a.err, 5);
@@ -691,17 +719,18 @@ SSD_DI void consume_win(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int tok = h * 8 + 2 * c;
-        sm.red[buf][warp][g][tok] = acc[h][0];
-        sm.red[buf][warp][g][tok + 1] = acc[h][1];
-        sm.red[buf][warp][g + 8][tok] = acc[h][2];
-        sm.red[buf][warp][g + 8][tok + 1] = acc[h][3];
-        acc[h][0] = acc[h][1] = acc[h][2] = acc[h][3] = 0.f;
+        sm.red[buf][warp][g][tok] = acc[gi][h][0];
+        sm.red[buf][warp][g][tok + 1] = acc[gi][h][1];
+        sm.red[buf][warp][g + 8][tok] = acc[gi][h][2];
+        sm.red[buf][warp][g + 8][tok + 1] = acc[gi][h][3];
+        acc[gi][h][0] = acc[gi][h][1] = acc[gi][h][2] = acc[gi][h][3] = 0.f;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.rfull[buf]);
       ++fl;
     }
   }
+  cp_async_wait_all();
   rp.slot = slot;
   rp.ph = ph;
   rp.fl = fl;
@@ -709,9 +738,10 @@ SSD_DI void consume_win(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0
 }
 
 // Producer warp (lane 0 issues): streams CTA b's units of one GEMV into the
-// ring.  Weights never depend on earlier phases, so the producer runs ahead
-// of the consumers, bounded only by free ring slots.
-template <int EPI>
+// ring, in the order the consumers take them (row groups in turn, or the
+// batched K-outer order).  Weights never depend on earlier phases, so the
+// producer runs ahead of the consumers, bounded only by free ring slots.
+template <int IN, int EPI>
 SSD_DI void producer_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int b, int lane,
                            RingPos& rp) {
   if (b >= p.C || lane != 0 || !rp.ok) return;
@@ -719,9 +749,8 @@ SSD_DI void producer_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int
   // it into L2 ahead of this CTA's weight stream
   if (a.gain && b == 0) bulk_prefetch_l2(a.gain, (uint32_t)(a.K * sizeof(float)));
   const int U0 = unit_begin(p, b), U1 = unit_begin(p, b + 1);
-  int vr = U0 / p.KB, kb = U0 % p.KB, left = U1 - U0;
-  while (left > 0) {
-    const int n = chunk_len(p, kb, left);
+  auto put = [&](int vr, int kb, int n) {
+    if (!rp.ok) return;
     if (rp.t >= kSlots && !mbar_wait(&sm.empty[rp.slot], rp.ph ^ 1u)) {
       atomicExch(a.err, 2);
       rp.ok = false;
@@ -730,11 +759,20 @@ SSD_DI void producer_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int
     mbar_arrive_expect_tx(&sm.full[rp.slot], (uint32_t)(n * kUnitBytes));
     bulk_g2s(sm.ring + rp.slot * kSlotBytes, unit_src<EPI>(a, p, vr, kb),
              (uint32_t)(n * kUnitBytes), &sm.full[rp.slot]);
+    if (++rp.slot == kSlots) { rp.slot = 0; rp.ph ^= 1u; }
+    ++rp.t;
+  };
+  if (kouter_order<IN, EPI>(a, p)) {
+    kouter_chunks(p, U0, U1, put);
+    return;
+  }
+  int vr = U0 / p.KB, kb = U0 % p.KB, left = U1 - U0;
+  while (left > 0 && rp.ok) {
+    const int n = chunk_len(p, kb, left);
+    put(vr, kb, n);
     kb += n;
     left -= n;
     if (kb == p.KB) { kb = 0; ++vr; }
-    if (++rp.slot == kSlots) { rp.slot = 0; rp.ph ^= 1u; }
-    ++rp.t;
   }
 }
 
@@ -749,11 +787,10 @@ SSD_DI void producer_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int
 // into one running record per token and publishes it at the end.
 template <int EPI>
 SSD_DI void epilogue_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int b, int M,
-                           int lane, RingPos& rp) {
+                           int lane, RingPos& rp, LmRec& run) {
   if (b >= p.C || !rp.ok) return;
   const int U0 = unit_begin(p, b), U1 = unit_begin(p, b + 1);
   int vr = U0 / p.KB, kb = U0 % p.KB, left = U1 - U0;
-  LmRec run = lm_empty();
   int slot = 0, round = 0, pos0 = 0;
   if (EPI == EPI_LMHEAD) {
     slot = a.slot_dev ? __ldcg(a.slot_dev) : 0;
@@ -863,7 +900,38 @@ SSD_DI void epilogue_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int
     epilogue<EPI>(a, p, gvr, sm.ep, M, lane, xp);
     __syncwarp();
   }
-  if (EPI == EPI_LMHEAD) lm_finish(a, p, b, M, lane, slot, run, reinterpret_cast<float*>(sm.stage));
+}
+
+// LM head, end of the kernel for the epilogue warp (is_epi, holding the
+// CTA's running records) and the consumer warps: the epilogue warp publishes
+// and tells the others through foldbar whether this CTA published last; if
+// so the kConsumers + 1 warps fold the pass's tokens, token t by warp
+// t mod (kConsumers + 1).  Every wait is bounded.
+SSD_DI void lm_end(const LinearArgs& a, const Part& p, GemvSmem& sm, int b, int M, int warp,
+                   int lane, const RingPos& rp, const LmRec& run, bool is_epi) {
+  int last = 0;
+  if (is_epi) {
+    if (rp.ok && b < p.C) last = lm_publish(a, p, b, M, lane, run);
+    if (lane == 0) {
+      sm.fold_last = last;
+      mbar_arrive(&sm.foldbar);
+    }
+    if (last && lane == 0) a.counter[0] = 0u;  // every CTA has counted
+  } else {
+    if (!mbar_wait(&sm.foldbar, 0u)) {
+      if (lane == 0) atomicExch(a.err, 7);
+      return;
+    }
+    last = *reinterpret_cast<volatile int*>(&sm.fold_last);
+  }
+  if (!last) return;
+  __threadfence();
+  const int slot = a.slot_dev ? __ldcg(a.slot_dev) : 0;
+  const int wi = is_epi ? kConsumers : warp;
+  float* stage = wi < 4 ? reinterpret_cast<float*>(sm.ring + wi * kFoldBytes)
+                        : reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(sm.stage) +
+                                                   (wi - 4) * kFoldBytes);
+  for (int tok = wi; tok < M; tok += kConsumers + 1) lm_fold(a, p, tok, lane, slot, stage);
 }
 
 // Consumer warps: RMSNorm statistics, activation staging and the MMAs for
@@ -874,7 +942,8 @@ SSD_DI void consumer_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int
   if (b >= p.C) return;
   const int U0 = unit_begin(p, b), U1 = unit_begin(p, b + 1);
   if (!rp.ok) return;
-  const bool staged = (size_t)M * (a.K + kPad) * sizeof(bf16) <= (size_t)kStageBytes;
+  const bool kouter = kouter_order<IN, EPI>(a, p);
+  const bool staged = !kouter && (size_t)M * (a.K + kPad) * sizeof(bf16) <= (size_t)kStageBytes;
   const int vpr = a.K / 8;  // 16-byte pieces per row
   const int nst = staged ? M * vpr : 0;
   constexpr int kPre = IN == IN_NORM ? 2 : 4;
@@ -922,7 +991,7 @@ SSD_DI void consumer_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int
     }
     consumer_sync();
     consume<IN, EPI, true>(a, p, sm, U0, U1, M, warp, lane, rp);
-  } else if (IN == IN_BF16 && p.G == p.KB * (EPI == EPI_SWIGLU ? 2 : 1)) {
+  } else if (kouter) {
     consume_win<EPI>(a, p, sm, U0, U1, M, warp, lane, rp);
   } else {
     consume<IN, EPI, false>(a, p, sm, U0, U1, M, warp, lane, rp);

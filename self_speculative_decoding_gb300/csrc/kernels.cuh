@@ -21,6 +21,13 @@ struct LinearArgs {
   float eps = 1e-5f;
   int M_static = 1;
   const int32_t* M_dev = nullptr;
+  // 1: the pass's rows may not fit the per-CTA activation stage.  A bf16-input
+  // projection whose CTAs own whole row groups then streams each CTA's groups
+  // in batches, K window by K window, and loads each activation window once
+  // per batch (the same sums in the same order as the staged layout).  Set by
+  // the caller from the pass's static row bound; launch_gemv sets it for a
+  // static M that does not fit.
+  int wide = 0;
   // outputs
   float* y = nullptr;         // EPI_STORE [M][R]
   float* xres = nullptr;      // EPI_RESID [M][R], read and written
@@ -32,6 +39,7 @@ struct LinearArgs {
   unsigned* counter = nullptr;
   float* rec = nullptr;       // EPI_LMHEAD summary records
   int* err = nullptr;         // set non-zero if a bulk copy never completed
+  int* err_val = nullptr;     // debug builds: the value a failed bounds check saw
   // EPI_LMHEAD
   float* logits = nullptr;    // [slot + M][R] (nullable)
   RowStats* stats = nullptr;  // [slot + M]
@@ -87,6 +95,7 @@ struct AttnArgs {
   float* part = nullptr;       // [Hkv][max_seq/kAttnChunk][G*16][dh+2]
   unsigned* counters = nullptr;  // [Hkv]
   int* err = nullptr;          // set to 1 if a bulk copy never completed
+  int* err_val = nullptr;      // debug builds: the value a failed bounds check saw
   float scale = 1.f;
   // Side rows (dynamic verification): the pass's last *ns_dev rows are
   // sibling candidates at positions side_pos[i] (not pos0 + m).  A side row
@@ -112,6 +121,65 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st, bool pdl);
 // in double precision and rounded to fp32.
 cudaError_t launch_rope_table(float2* tab, int n_pos, int half, double theta, cudaStream_t s);
 
+// ---------------------------------------------------------------------------
+// fp32 models (SSD_DTYPE_FP32): the same steps with fp32 weights (row-major,
+// not packed), fp32 activations, K/V and logits, and no rounding (fp32.cu).
+
+struct LinearArgs32 {
+  const float* W0 = nullptr;  // [R][K] row-major
+  const float* W1 = nullptr;  // EPI_SWIGLU: the up matrix
+  int R = 0, K = 0;
+  const float* act = nullptr; // IN_BF16 (plain input) [M][K]
+  const float* x = nullptr;   // IN_NORM [M][K]
+  const float* gain = nullptr;
+  float eps = 1e-5f;
+  int M_static = 1;
+  const int32_t* M_dev = nullptr;
+  float* y = nullptr;         // EPI_STORE [row0 + M][R]
+  const int32_t* row0_dev = nullptr;
+  float* xres = nullptr;      // EPI_RESID [M][R]
+  float* u = nullptr;         // EPI_SWIGLU [M][R]
+};
+cudaError_t launch_gemv32(int in_mode, int epi, const LinearArgs32& a, cudaStream_t st, bool pdl);
+
+// Row summaries (RowStats) of logits rows [slot + m], m < M.
+struct LmSummaryArgs32 {
+  const float* logits = nullptr;
+  int V = 0;
+  int M_static = 1;
+  const int32_t* M_dev = nullptr;
+  const int32_t* slot_dev = nullptr;
+  RowStats* stats = nullptr;
+  float temperature = 0.f;
+  int sample = 0;
+  uint64_t seed = 0;
+  int round_static = 0;
+  const int32_t* round_dev = nullptr;
+  int stream = 0;
+  int pos0_static = 0;
+  const int32_t* pos0_dev = nullptr;
+};
+cudaError_t launch_lm_summary32(const LmSummaryArgs32& a, cudaStream_t st, bool pdl);
+
+struct AttnArgs32 {
+  const float* qkv = nullptr;  // [M][ld_qkv]
+  int ld_qkv = 0;
+  int M_static = 1;
+  const int32_t* M_dev = nullptr;
+  int pos0_static = 0;
+  const int32_t* pos0_dev = nullptr;
+  float* kc = nullptr;         // [Hkv][max_seq][dh]
+  float* vc = nullptr;
+  int max_seq = 0;
+  int H = 0, Hkv = 0, dh = 0;
+  const float2* rope = nullptr;
+  float* out = nullptr;        // [M][H dh]
+  float scale = 1.f;
+};
+size_t attn32_smem(int dh, int max_seq);
+cudaError_t attn32_prepare(int dh, int max_seq);
+cudaError_t launch_attention32(const AttnArgs32& a, cudaStream_t st, bool pdl);
+
 // Embedding / pass set-up ("begin") kernel modes.
 enum BeginMode { BEGIN_TOKENS = 0, BEGIN_AR = 1, BEGIN_DRAFT = 2, BEGIN_EXTRA = 3, BEGIN_VERIFY = 4 };
 
@@ -123,6 +191,7 @@ struct BeginArgs {
   int M = 1, pos0 = 0;               // BEGIN_TOKENS
   int reset_round = 0;               // BEGIN_TOKENS: set round = 0 (prefill)
   const bf16* embed = nullptr;       // [V][D]
+  const float* embed32 = nullptr;    // fp32 models: [V][D] fp32 (embed unused)
   int D = 0;
   float* x = nullptr;                // [16][D]
   float* ss = nullptr;               // [16][D/16]

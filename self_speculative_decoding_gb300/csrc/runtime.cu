@@ -33,6 +33,10 @@ namespace {
 
 enum Phase { PH_NONE = 0, PH_IDLE = 1, PH_DRAFTED = 2, PH_VERIFIED = 3 };
 
+// Debug builds: the canary after every context workspace.
+constexpr size_t kCanaryBytes = 256;
+constexpr int kCanaryByte = 0xA5;
+
 struct Graph {
   cudaGraphExec_t exec = nullptr;
   int nodes = 0;
@@ -139,11 +143,20 @@ struct ssd_ctx {
   Graph g_verify_wide;
   // static row bound of the passes being enqueued (0: up to 16 rows)
   int mmax = 0;
+  // fp32 model (SSD_DTYPE_FP32): the K/V cache, attention output, SwiGLU
+  // product and logits scratch hold fp32 (kc, vc, attn, u allocated at 4
+  // bytes an element), weights are row-major fp32, fp32.cu runs the steps
+  bool fp32 = false;
+  std::vector<unsigned char*> canaries;  // debug builds: the workspaces' canaries
+  const float* embed32 = nullptr;
+  const float* lm_head32 = nullptr;
+  float* lg32 = nullptr;          // logits rows of passes that keep none [16][V]
 
   Phase phase = PH_NONE;
   // profiling: events recorded around every eager launch
   bool profiling = false;
   int prof_class = 6;
+  int prof_graph_cls = 0;   // kernel class captured by b_prof_class
   std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> prof_events;
   int64_t launches = 0;
   int capturing_nodes = 0;
@@ -218,6 +231,10 @@ ssd_status read_state(ssd_ctx* c) {
   CK(cudaMemcpyAsync(c->h_st, c->st, sizeof(DevState), cudaMemcpyDeviceToHost, c->stream));
   const ssd_status r = wait_stream(c);
   if (r != SSD_OK) return r;
+  if (c->h_st->err >= kDbgCodeBase)
+    return fail(c, SSD_ERR_STATE,
+                "a device bounds check failed (code " + std::to_string(c->h_st->err) + ", value " +
+                    std::to_string(c->h_st->err_val) + "); the context must be destroyed");
   if (c->h_st->err != 0)
     return fail(c, SSD_ERR_TIMEOUT,
                 "a device-side wait gave up (code " + std::to_string(c->h_st->err) +
@@ -254,10 +271,12 @@ void gemv_scratch_args(ssd_ctx* c, LinearArgs& a) {
   a.counter = c->g_cnt;
   a.rec = c->g_rec;
   a.err = &c->st->err;
+  a.err_val = &c->st->err_val;
+  a.wide = (c->mmax ? c->mmax : kMaxRows) > gemv_stage_rows(a.K) ? 1 : 0;
 }
 
-// Arguments of layer l's five steps (shared by the eager / captured launches
-// and by the pass programs).
+// Arguments of layer l's five steps (shared by the eager and the captured
+// launches).
 LinearArgs qkv_args(ssd_ctx* c, int l) {
   const ssd_config& g = c->cfg;
   const ssd_layer_weights& w = c->layers[l];
@@ -293,6 +312,7 @@ AttnArgs attn_args(ssd_ctx* c, int l) {
   a.part = c->attn_part;
   a.counters = c->attn_cnt;
   a.err = &c->st->err;
+  a.err_val = &c->st->err_val;
   a.scale = (float)(1.0 / std::sqrt((double)g.head_dim));
   a.ns_dev = &c->st->ns;
   a.side_pos = c->st->side_pos;
@@ -385,6 +405,7 @@ BeginArgs begin_args(ssd_ctx* c, int mode, int M, int pos0, const int32_t* toks_
   b.pos0 = pos0;
   b.reset_round = reset;
   b.embed = c->embed;
+  b.embed32 = c->embed32;
   b.D = c->cfg.d_model;
   b.x = c->x;
   b.ss = c->ss;
@@ -443,7 +464,100 @@ ssd_status enq_norm_gemv(ssd_ctx* c, int epi, const LinearArgs& a, cudaStream_t 
   return note(c, launch_gemv(IN_BF16, epi, b, s, c->pdl), what);
 }
 
+// fp32 models: layer l's steps and the LM head (fp32.cu).
+LinearArgs32 lin32(ssd_ctx* c, const void* W, int R, int K) {
+  LinearArgs32 a;
+  a.W0 = (const float*)W;
+  a.R = R;
+  a.K = K;
+  a.M_dev = &c->st->M;
+  a.eps = c->cfg.norm_eps;
+  return a;
+}
+
+ssd_status enq_layer32(ssd_ctx* c, int l, cudaStream_t s, int parts) {
+  const ssd_config& g = c->cfg;
+  const ssd_layer_weights& w = c->layers[l];
+  const int D = g.d_model, HD = g.n_heads * g.head_dim;
+  float* attn = reinterpret_cast<float*>(c->attn);
+  float* u = reinterpret_cast<float*>(c->u);
+  ssd_status r;
+  if (parts & 1) {
+    prof_begin(c, 0);
+    LinearArgs32 q = lin32(c, w.wqkv, qkv_rows(g), D);
+    q.x = c->x;
+    q.gain = (const float*)w.attn_norm;
+    q.y = c->qkv;
+    if ((r = note(c, launch_gemv32(IN_NORM, EPI_STORE, q, s, c->pdl), "qkv")) != SSD_OK) return r;
+    prof_begin(c, 1);
+    AttnArgs32 at;
+    at.qkv = c->qkv;
+    at.ld_qkv = qkv_rows(g);
+    at.M_dev = &c->st->M;
+    at.pos0_dev = &c->st->pos0;
+    at.kc = reinterpret_cast<float*>(c->kc) + (size_t)l * kv_layer_elems(g);
+    at.vc = reinterpret_cast<float*>(c->vc) + (size_t)l * kv_layer_elems(g);
+    at.max_seq = g.max_seq;
+    at.H = g.n_heads;
+    at.Hkv = g.n_kv_heads;
+    at.dh = g.head_dim;
+    at.rope = c->rope;
+    at.out = attn;
+    at.scale = (float)(1.0 / std::sqrt((double)g.head_dim));
+    if ((r = note(c, launch_attention32(at, s, c->pdl), "attention")) != SSD_OK) return r;
+    prof_begin(c, 2);
+    LinearArgs32 o = lin32(c, w.wo, D, HD);
+    o.act = attn;
+    o.xres = c->x;
+    if ((r = note(c, launch_gemv32(IN_BF16, EPI_RESID, o, s, c->pdl), "o_proj")) != SSD_OK) return r;
+  }
+  if (!(parts & 2)) return SSD_OK;
+  prof_begin(c, 3);
+  LinearArgs32 gu = lin32(c, w.w_gate, g.ffn_dim, D);
+  gu.W1 = (const float*)w.w_up;
+  gu.x = c->x;
+  gu.gain = (const float*)w.mlp_norm;
+  gu.u = u;
+  if ((r = note(c, launch_gemv32(IN_NORM, EPI_SWIGLU, gu, s, c->pdl), "gate_up")) != SSD_OK) return r;
+  prof_begin(c, 4);
+  LinearArgs32 dn = lin32(c, w.w_down, D, g.ffn_dim);
+  dn.act = u;
+  dn.xres = c->x;
+  return note(c, launch_gemv32(IN_BF16, EPI_RESID, dn, s, c->pdl), "down");
+}
+
+// fp32 LM head: logits rows [slot + m] (the logits buffer, or the scratch
+// rows when the pass keeps none), then their row summaries.
+ssd_status enq_lmhead32(ssd_ctx* c, RowStats* stats, float* logits, const int32_t* slot_dev,
+                        int sample_stream, cudaStream_t s) {
+  const ssd_config& g = c->cfg;
+  LinearArgs32 a = lin32(c, c->lm_head32, g.vocab, g.d_model);
+  a.x = c->x;
+  a.gain = c->final_norm;
+  a.y = logits ? logits : c->lg32;
+  a.row0_dev = logits ? slot_dev : nullptr;
+  ssd_status r = note(c, launch_gemv32(IN_NORM, EPI_STORE, a, s, c->pdl), "lm_head");
+  if (r != SSD_OK) return r;
+  LmSummaryArgs32 m;
+  m.logits = a.y;
+  m.V = g.vocab;
+  m.M_dev = &c->st->M;
+  m.slot_dev = slot_dev;
+  m.stats = stats;
+  m.temperature = c->pol.temperature;
+  m.sample = sample_stream >= 0 ? 1 : 0;
+  m.seed = c->pol.seed;
+  m.round_dev = &c->st->round;
+  m.stream = sample_stream < 0 ? 0 : sample_stream;
+  m.pos0_dev = &c->st->pos0;
+  // scratch rows are written from row 0 on; a pass that keeps its logits
+  // reads them at its slot
+  if (!logits) m.slot_dev = nullptr;
+  return note(c, launch_lm_summary32(m, s, c->pdl), "lm_summary");
+}
+
 ssd_status enq_layer(ssd_ctx* c, int l, cudaStream_t s, int parts = 3) {
+  if (c->fp32) return enq_layer32(c, l, s, parts);
   ssd_status r;
   if (!(parts & 1)) goto mlp;
   prof_begin(c, 0);
@@ -474,6 +588,7 @@ ssd_status enq_layers(ssd_ctx* c, const std::vector<int>& ls, cudaStream_t s,
 ssd_status enq_lmhead(ssd_ctx* c, RowStats* stats, float* logits, const int32_t* slot_dev,
                       int sample_stream, cudaStream_t s) {
   prof_begin(c, 5);
+  if (c->fp32) return enq_lmhead32(c, stats, logits, slot_dev, sample_stream, s);
   return enq_norm_gemv(c, EPI_LMHEAD, lm_args(c, stats, logits, slot_dev, sample_stream), s,
                        "lm_head");
 }
@@ -818,12 +933,13 @@ ssd_status replay(ssd_ctx* c, Graph& g) {
 // read for positions [0, pos0 + M) and written for M positions per layer.
 double pass_bytes(const ssd_ctx* c, int n_layers_run, bool lm, int pos0, int M) {
   const ssd_config& g = c->cfg;
-  const double layer_w = 2.0 * ((double)qkv_rows(g) * g.d_model +
-                                (double)g.d_model * g.n_heads * g.head_dim +
-                                3.0 * g.d_model * g.ffn_dim);
-  const double kv_pos = 2.0 * 2.0 * g.n_kv_heads * g.head_dim;
+  const double el = c->fp32 ? 4.0 : 2.0;
+  const double layer_w = el * ((double)qkv_rows(g) * g.d_model +
+                               (double)g.d_model * g.n_heads * g.head_dim +
+                               3.0 * g.d_model * g.ffn_dim);
+  const double kv_pos = 2.0 * el * g.n_kv_heads * g.head_dim;
   double b = n_layers_run * (layer_w + kv_pos * (pos0 + M) + kv_pos * M);
-  if (lm) b += 2.0 * (double)g.vocab * g.d_model;
+  if (lm) b += el * (double)g.vocab * g.d_model;
   return b;
 }
 
@@ -831,12 +947,13 @@ double pass_bytes(const ssd_ctx* c, int n_layers_run, bool lm, int pos0, int M) 
 // the sublayers the draft runs above it, and the LM head
 double draft_bytes(const ssd_ctx* c, int pos) {
   const ssd_config& g = c->cfg;
-  const double attn_w = 2.0 * ((double)qkv_rows(g) * g.d_model + (double)g.d_model * g.n_heads * g.head_dim);
-  const double mlp_w = 2.0 * 3.0 * g.d_model * g.ffn_dim;
-  const double kv = 2.0 * 2.0 * g.n_kv_heads * g.head_dim * (double)(pos + 2);
+  const double el = c->fp32 ? 4.0 : 2.0;
+  const double attn_w = el * ((double)qkv_rows(g) * g.d_model + (double)g.d_model * g.n_heads * g.head_dim);
+  const double mlp_w = el * 3.0 * g.d_model * g.ffn_dim;
+  const double kv = 2.0 * el * g.n_kv_heads * g.head_dim * (double)(pos + 2);
   double b = c->pre.size() * (attn_w + kv + mlp_w);
   for (int pt : c->post_parts) b += ((pt & 1) ? attn_w + kv : 0.0) + ((pt & 2) ? mlp_w : 0.0);
-  return b + 2.0 * (double)g.vocab * g.d_model;
+  return b + el * (double)g.vocab * g.d_model;
 }
 
 ssd_status check_capacity(ssd_ctx* c, int extra) {
@@ -1103,7 +1220,8 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
       g.vocab <= 0 || g.vocab % 16 || g.max_seq <= 0 || g.max_seq % kAttnChunk ||
       g.max_draft < 1 || g.max_draft > kMaxRows - 1 || g.max_score_rows < 0 ||
       (g.n_heads * g.head_dim) % 32 || g.n_heads / g.n_kv_heads > 8 || !(g.norm_eps > 0.f) ||
-      !(g.rope_theta > 0.f))
+      !(g.rope_theta > 0.f) || (g.dtype != SSD_DTYPE_BF16 && g.dtype != SSD_DTYPE_FP32) ||
+      (g.dtype == SSD_DTYPE_FP32 && g.max_score_rows > 0))
     return SSD_ERR_INVALID_ARG;
   for (int l = 0; l < g.n_layers; ++l) {
     const ssd_layer_weights& L = w->layers[l];
@@ -1113,9 +1231,14 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
   c = new ssd_ctx();
   c->cfg = g;
   c->layers.assign(w->layers, w->layers + g.n_layers);
+  c->fp32 = g.dtype == SSD_DTYPE_FP32;
   c->embed = (const bf16*)w->tok_embed;
   c->final_norm = (const float*)w->final_norm;
   c->lm_head = (const bf16*)w->lm_head;
+  if (c->fp32) {
+    c->embed32 = (const float*)w->tok_embed;
+    c->lm_head32 = (const float*)w->lm_head;
+  }
   c->stream = (cudaStream_t)stream;
 
   auto alloc = [&](void** p, size_t bytes) -> bool {
@@ -1123,14 +1246,28 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
       g_fail_alloc = -1;
       return false;
     }
+#ifdef SSD_DEBUG_CHECKS
+    // debug builds: every workspace is followed by a canary of kCanaryBytes
+    // bytes of kCanaryByte, checked by ssd_debug_canaries
+    const size_t body = (bytes + 255) & ~(size_t)255;
+    if (cudaMalloc(p, body + kCanaryBytes) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    unsigned char* guard = static_cast<unsigned char*>(*p) + body;
+    cudaMemsetAsync(guard, kCanaryByte, kCanaryBytes, c->stream);
+    c->canaries.push_back(guard);
+#else
     if (cudaMalloc(p, bytes) != cudaSuccess) {
       cudaGetLastError();
       return false;
     }
+#endif
     return true;
   };
   const int D = g.d_model, F = g.ffn_dim, V = g.vocab;
   const int nr = kMaxRows;
+  const size_t act_el = c->fp32 ? 4 : 2;  // K/V, attention output, SwiGLU product
   // one scratch area serves every GEMV of the context (they run in stream order)
   GemvScratch gs{0, 0, 0};
   {
@@ -1144,8 +1281,8 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
       gs.rec_floats = std::max(gs.rec_floats, x.rec_floats);
     }
   }
-  bool ok = alloc((void**)&c->kc, kv_elems(g) * sizeof(bf16)) &&
-            alloc((void**)&c->vc, kv_elems(g) * sizeof(bf16)) &&
+  bool ok = alloc((void**)&c->kc, kv_elems(g) * act_el) &&
+            alloc((void**)&c->vc, kv_elems(g) * act_el) &&
             alloc((void**)&c->x, (size_t)nr * D * 4) &&
             alloc((void**)&c->ss, (size_t)nr * (D / kSsGroup) * 4) &&
             alloc((void**)&c->bx, (size_t)nr * D * 4) &&
@@ -1155,8 +1292,9 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
             alloc((void**)&c->ks, (size_t)g.n_layers * g.n_kv_heads * kMaxSide * g.head_dim * 2) &&
             alloc((void**)&c->vs, (size_t)g.n_layers * g.n_kv_heads * kMaxSide * g.head_dim * 2) &&
             alloc((void**)&c->qkv, (size_t)nr * qkv_rows(g) * 4) &&
-            alloc((void**)&c->attn, (size_t)nr * g.n_heads * g.head_dim * 2) &&
-            alloc((void**)&c->u, (size_t)nr * F * 2) &&
+            alloc((void**)&c->attn, (size_t)nr * g.n_heads * g.head_dim * act_el) &&
+            alloc((void**)&c->u, (size_t)nr * F * act_el) &&
+            (!c->fp32 || alloc((void**)&c->lg32, (size_t)nr * V * 4)) &&
             alloc((void**)&c->xn, (size_t)nr * D * 2) &&
             alloc((void**)&c->rope, (size_t)g.max_seq * (g.head_dim / 2) * sizeof(float2)) &&
             alloc((void**)&c->attn_part,
@@ -1212,7 +1350,9 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
     return SSD_ERR_OOM;
   }
   memset(c->h_st, 0, sizeof(DevState));
-  cudaMemsetAsync(c->st, 0, sizeof(DevState), c->stream);
+  c->h_st->vocab = g.vocab;      // bounds of the debug builds' device checks
+  c->h_st->max_seq = g.max_seq;
+  cudaMemcpyAsync(c->st, c->h_st, sizeof(DevState), cudaMemcpyHostToDevice, c->stream);
   cudaMemsetAsync(c->attn_cnt, 0, (size_t)g.n_kv_heads * 4, c->stream);
   cudaMemsetAsync(c->g_cnt, 0, gs.counters * 4, c->stream);
   cudaMemsetAsync(c->tokens, 0, (size_t)g.max_seq * 4, c->stream);
@@ -1224,7 +1364,7 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
     probe.Hkv = g.n_kv_heads;
     probe.dh = g.head_dim;
     probe.max_seq = g.max_seq;
-    if (attn_prepare(probe) != cudaSuccess) {
+    if ((c->fp32 ? attn32_prepare(g.head_dim, g.max_seq) : attn_prepare(probe)) != cudaSuccess) {
       cudaGetLastError();
       ssd_destroy(c);
       return SSD_ERR_INVALID_ARG;
@@ -1251,7 +1391,7 @@ ssd_status ssd_destroy(ssd_ctx* c) {
   c->g_lossy.reset();
   c->g_loop.reset();
   void* bufs[] = {c->kc, c->vc, c->x, c->ss, c->bx, c->bss, c->qkv, c->attn, c->u, c->xn, c->rope,
-                  c->attn_part, c->attn_cnt, c->g_part, c->g_cnt, c->g_rec, c->dstats, c->vstats,
+                  c->attn_part, c->attn_cnt, c->lg32, c->g_part, c->g_cnt, c->g_rec, c->dstats, c->vstats,
                   c->dlogits, c->vlogits, c->tokens, c->toks_in, c->st, c->fstats, c->ffeat,
                   c->bxs, c->bsss, c->ks, c->vs};
   for (void* p : bufs)
@@ -1297,6 +1437,8 @@ ssd_status ssd_set_policy(ssd_ctx* c, const ssd_policy* p) {
       if (p->skip_attn_mask[w] || p->skip_mlp_mask[w])
         return fail(c, SSD_ERR_INVALID_ARG, "sublayer masks need skip mode");
   if (!std::isfinite(p->tree_tau)) return fail(c, SSD_ERR_INVALID_ARG, "tree_tau");
+  if (p->tree_tau > 0.f && c->fp32)
+    return fail(c, SSD_ERR_INVALID_ARG, "dynamic verification needs a bf16 model");
   if (p->tree_tau > 0.f) {
     if (p->temperature != 0.f)
       return fail(c, SSD_ERR_INVALID_ARG, "dynamic verification (tree_tau > 0) needs temperature 0");
@@ -1350,6 +1492,32 @@ ssd_status ssd_prefill(ssd_ctx* c, const int32_t* tokens, int32_t n, int32_t* fi
   const int D = c->cfg.d_model;
   cudaStream_t s = c->stream;
   ssd_status r;
+  if (c->fp32) {
+    // fp32 models: the prompt in passes of up to 16 rows through the decode
+    // kernels, then the last position's state through the LM head
+    int last = 0;
+    for (int c0 = 0; c0 < n; c0 += kMaxRows) {
+      const int m = std::min(kMaxRows, n - c0);
+      if ((r = enq_begin(c, BEGIN_TOKENS, s, m, c0, c->toks_in + c0, 1)) != SSD_OK) return r;
+      std::vector<int> all(c->cfg.n_layers);
+      for (int l = 0; l < c->cfg.n_layers; ++l) all[l] = l;
+      if ((r = enq_layers(c, all, s)) != SSD_OK) return r;
+      last = m;
+    }
+    CK(cudaMemcpyAsync(c->bx, c->x + (size_t)(last - 1) * D, (size_t)D * sizeof(float),
+                       cudaMemcpyDeviceToDevice, s));
+    if ((r = enq_begin(c, BEGIN_TOKENS, s, 1, n - 1, c->toks_in + n - 1, 1)) != SSD_OK) return r;
+    CK(cudaMemcpyAsync(c->x, c->bx, (size_t)D * sizeof(float), cudaMemcpyDeviceToDevice, s));
+    if ((r = enq_lmhead(c, c->vstats, nullptr, nullptr, 2, s)) != SSD_OK) return r;
+    if ((r = note(c, launch_ar_end(c->st, c->tokens, c->vstats, 1, c->pol.temperature, 1, s,
+                                   c->pdl), "prefill_end")) != SSD_OK)
+      return r;
+    if ((r = read_state(c)) != SSD_OK) return r;
+    if (first) *first = c->h_st->emitted[0];
+    c->phase = PH_IDLE;
+    c->lossy_from = -1;
+    return SSD_OK;
+  }
   CK(cudaMemsetAsync(c->sc_cand, 0, sizeof(int32_t), s));  // the one "candidate"
   int last = 0;
   for (int c0 = 0; c0 < n; c0 += c->pf_chunk) {
@@ -1751,10 +1919,90 @@ ssd_status ssd_profile_decode(ssd_ctx* c, int32_t n_steps, ssd_kernel_times* out
   return wait_stream(c);
 }
 
+namespace {
+
+// ssd_profile_kernels: the launches of one kernel class over every layer of
+// an autoregressive step (the LM head: n_layers launches of it), enqueued as
+// the step's graph enqueues them, so that consecutive launches overlap
+// through programmatic dependent launch as they do in the step.
+ssd_status b_prof_class(ssd_ctx* c, cudaStream_t s) {
+  c->mmax = 1;
+  ssd_status r = SSD_OK;
+  const int cls = c->prof_graph_cls;
+  for (int l = 0; l < c->cfg.n_layers && r == SSD_OK; ++l) {
+    switch (cls) {
+      case 0: r = enq_norm_gemv(c, EPI_STORE, qkv_args(c, l), s, "qkv"); break;
+      case 1: r = note(c, launch_attention(attn_args(c, l), s, c->pdl), "attention"); break;
+      case 2: r = note(c, launch_gemv(IN_BF16, EPI_RESID, oproj_args(c, l), s, c->pdl), "o_proj"); break;
+      case 3: r = enq_norm_gemv(c, EPI_SWIGLU, gateup_args(c, l), s, "gate_up"); break;
+      case 4: r = note(c, launch_gemv(IN_BF16, EPI_RESID, down_args(c, l), s, c->pdl), "down"); break;
+      default: r = enq_lmhead(c, c->vstats, nullptr, nullptr, 2, s); break;
+    }
+  }
+  c->mmax = 0;
+  return r;
+}
+
+}  // namespace
+
+ssd_status ssd_profile_kernels(ssd_ctx* c, int32_t reps, ssd_kernel_times* out) {
+  if (!c || !out || reps <= 0) return SSD_ERR_INVALID_ARG;
+  if (c->fp32) return fail(c, SSD_ERR_INVALID_ARG, "kernel profile of bf16 models only");
+  ssd_status r = ensure_policy(c);
+  if (r != SSD_OK) return r;
+  if (c->phase != PH_IDLE) return fail(c, SSD_ERR_STATE, "a round is in flight");
+  if ((r = read_state(c)) != SSD_OK) return r;
+  const int n0 = c->h_st->n;
+  if (n0 + 1 > c->cfg.max_seq) return fail(c, SSD_ERR_CAPACITY, "max_seq exceeded");
+  memset(out, 0, sizeof(*out));
+  const DevState saved = *c->h_st;
+  const ssd_config& g = c->cfg;
+  const int L = g.n_layers;
+  const double bytes[6] = {2.0 * qkv_rows(g) * g.d_model,
+                           2.0 * 2.0 * g.n_kv_heads * g.head_dim * (double)n0,
+                           2.0 * g.d_model * g.n_heads * g.head_dim,
+                           2.0 * 2.0 * g.ffn_dim * g.d_model,
+                           2.0 * g.d_model * g.ffn_dim,
+                           2.0 * g.vocab * g.d_model};
+  // the pass shape of an autoregressive step: one row at position n - 1
+  if ((r = enq_begin(c, BEGIN_AR, c->stream)) != SSD_OK) return r;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  CK(cudaEventCreate(&e0));
+  CK(cudaEventCreate(&e1));
+  for (int cls = 0; cls < 6 && r == SSD_OK; ++cls) {
+    Graph G;
+    c->prof_graph_cls = cls;
+    if ((r = build_graph(c, G, b_prof_class)) != SSD_OK) break;
+    cudaError_t e = cudaGraphLaunch(G.exec, c->stream);   // warm-up
+    if (e == cudaSuccess) e = cudaEventRecord(e0, c->stream);
+    for (int i = 0; i < reps && e == cudaSuccess; ++i) e = cudaGraphLaunch(G.exec, c->stream);
+    if (e == cudaSuccess) e = cudaEventRecord(e1, c->stream);
+    if (e != cudaSuccess) {
+      r = fail(c, SSD_ERR_CUDA, std::string("profile: ") + cudaGetErrorString(e));
+      break;
+    }
+    if ((r = wait_stream(c)) != SSD_OK) break;
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, e0, e1);
+    out->ms[cls] = ms / ((double)reps * L);
+    out->bytes[cls] = bytes[cls];
+    out->launches[cls] = cls == 5 ? 1 : L;
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (r != SSD_OK) return r;
+  // restore the committed state (the profile wrote only scratch buffers and
+  // the cache row of the pending position, which the next pass rewrites)
+  *c->h_st = saved;
+  CK(cudaMemcpyAsync(c->st, c->h_st, sizeof(DevState), cudaMemcpyHostToDevice, c->stream));
+  return wait_stream(c);
+}
+
 ssd_status ssd_swift_generate(ssd_ctx* c, const ssd_swift_params* pp, int32_t n_tokens,
                               int32_t* out, uint64_t* trace_masks, float* trace_scores,
                               int32_t* trace_best, int32_t trace_cap, ssd_swift_report* rep) {
   if (!c) return SSD_ERR_INVALID_ARG;
+  if (c->fp32) return fail(c, SSD_ERR_INVALID_ARG, "SWIFT optimisation needs a bf16 model");
   if (!pp || n_tokens < 0 || trace_cap < 0) return fail(c, SSD_ERR_INVALID_ARG, "swift arguments");
   const ssd_swift_params P = *pp;
   const int L = c->cfg.n_layers;
@@ -1892,6 +2140,20 @@ ssd_status ssd_swift_generate(ssd_ctx* c, const ssd_swift_params* pp, int32_t n_
   return SSD_OK;
 }
 
+ssd_status ssd_debug_canaries(ssd_ctx* c, int32_t* checked_out, int32_t* bad_out) {
+  if (!c || !checked_out || !bad_out) return SSD_ERR_INVALID_ARG;
+  *checked_out = (int32_t)c->canaries.size();
+  *bad_out = 0;
+  std::vector<unsigned char> h(kCanaryBytes);
+  for (unsigned char* g : c->canaries) {
+    CK(cudaMemcpyAsync(h.data(), g, kCanaryBytes, cudaMemcpyDeviceToHost, c->stream));
+    const ssd_status r = wait_stream(c);
+    if (r != SSD_OK) return r;
+    for (unsigned char b : h) *bad_out += b != kCanaryByte;
+  }
+  return SSD_OK;
+}
+
 ssd_status ssd_debug_fail_alloc(int32_t n) {
   g_fail_alloc = n < 0 ? -1 : n;
   return SSD_OK;
@@ -1923,6 +2185,7 @@ const char* ssd_last_error(const ssd_ctx* c) {
 ssd_status ssd_score_masks(ssd_ctx* c, const uint64_t* masks, int32_t K, int32_t N,
                            float* matchness_out, int32_t* best_out) {
   if (!c) return SSD_ERR_INVALID_ARG;
+  if (c->fp32) return fail(c, SSD_ERR_INVALID_ARG, "mask scoring needs a bf16 model");
   if (!masks || K < 1 || K > 256 || N < 1 || !matchness_out)
     return fail(c, SSD_ERR_INVALID_ARG, "score_masks arguments");
   ssd_status r = ensure_policy(c);

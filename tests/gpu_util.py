@@ -43,3 +43,25 @@ def pack_reference(bits: np.ndarray) -> np.ndarray:
         for c in range(4):
             out[:, :, :, g, c ^ ((g >> 1) & 3), :] = u[:, :, :, g, c, :]
     return out.reshape(R, K)
+
+
+def top_gap(z) -> float:
+    """Top-1 minus top-2 of a logit vector."""
+    s = np.sort(np.asarray(z, dtype=np.float64))
+    return float(s[-1] - s[-2])
+
+
+def oracle_prompt(m, w, pol, accept, length=None, max_seq=256, tries=400):
+    """A seeded prompt chosen on the oracle's values alone: the workload's own
+    prompt seed first, then seeds 1000, 1001, ...; the first prompt for which
+    accept(prompt, oracle state after the prefill) holds.  Parity tests use it
+    to start from a prompt whose first decisions are not near ties, so that a
+    comparison never has to be skipped."""
+    from oracle import prefill
+    from synthetic import make_prompt
+    for i in range(tries):
+        seed = w.prompt_seed if i == 0 else 1000 + i
+        prompt = make_prompt(w, length, seed=seed)
+        if accept(prompt, prefill(m, prompt, pol, max_seq)):
+            return prompt
+    raise AssertionError("no seeded prompt passes the oracle-side selection")

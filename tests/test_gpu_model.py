@@ -18,7 +18,7 @@ import torch
 
 from synthetic import TINY, make_weights, weights_to_numpy, make_prompt, shrink
 from synthetic.configs import Policy, ModelShape, Workload
-from tests.gpu_util import to_device_weights
+from tests.gpu_util import to_device_weights, top_gap, oracle_prompt
 
 pytestmark = pytest.mark.gpu
 
@@ -157,17 +157,78 @@ def test_rounds_match_oracle_in_lockstep(ssd, w, pol, head):
     from oracle import OracleModel, prefill, ssd_round
     ctx, wts = _ctx(ssd, w, lm_head_scale=head)
     ctx.set_policy(pol)
-    prompt = make_prompt(w)
-    first = ctx.prefill(prompt)
     m = OracleModel(w.shape, weights_to_numpy(wts))
+    prompt = oracle_prompt(m, w, pol, lambda p, st: not _near_tie(st.last_logits))
+    first = ctx.prefill(prompt)
     st = prefill(m, prompt, pol, 256)
-    if _near_tie(st.last_logits):
-        pytest.skip("near-tie at the first token")
     assert first == st.tokens[-1]
+    _lockstep(ctx, m, st, pol, head, min_rounds=1 if head == 1.0 else 3)
+    ctx.close()
+
+
+# Model with the workloads' own LM head (no sharpening) whose small vocabulary
+# and d_model 1024 give top-1/top-2 logit gaps well above the GPU-oracle
+# deviation (0.003-0.006 at this head), so that rounds can be compared at the
+# stated tolerances themselves.
+MID_V64 = Workload(name="mid-v64", shape=ModelShape(
+    n_layers=4, d_model=1024, n_heads=8, n_kv_heads=4, head_dim=128, ffn_dim=2816, vocab=64),
+    scaled_layers=(1, 2), scale=0.1)
+
+
+@pytest.mark.parametrize("pol", [
+    Policy(mode="skip", skip=(1, 2), d_max=3, tau=None),
+    Policy(mode="exit", exit_layer=0, d_max=4, tau=None),
+    Policy(mode="skip", skip=(2,), d_max=3, tau=0.05),
+], ids=["skip", "exit", "skip-tau"])
+def test_rounds_match_oracle_at_stated_tolerances(ssd, pol):
+    # logits within 5e-2 and confidences within 1e-3 (no sharpening factor)
+    # over at least three rounds.  The prompt is the first seeded prompt whose
+    # oracle rounds 1-3 decide every token with a top-1/top-2 gap above 0.02
+    # and every confidence stop more than 2e-3 from tau: chosen on the
+    # oracle's values alone.
+    from oracle import OracleModel, prefill, ssd_round
+    w = MID_V64
+    ctx, wts = _ctx(ssd, w, lm_head_scale=1.0)
+    ctx.set_policy(pol)
+    m = OracleModel(w.shape, weights_to_numpy(wts))
+
+    def clean(prompt, st):
+        if top_gap(st.last_logits) <= 0.02:
+            return False
+        for _ in range(3):
+            rec = ssd_round(m, st, pol)
+            confs = rec.conf + ([rec.stop_conf] if rec.stop_conf is not None else [])
+            if any(top_gap(z) <= 0.02 for z in rec.draft_logits):
+                return False
+            if any(top_gap(z) <= 0.02 for z in rec.verify_logits[: rec.accepted + 1]):
+                return False
+            if pol.tau is not None and any(abs(c - pol.tau) <= 2e-3 for c in confs):
+                return False
+        return True
+
+    prompt = oracle_prompt(m, w, pol, clean)
+    first = ctx.prefill(prompt)
+    st = prefill(m, prompt, pol, 256)
+    assert first == st.tokens[-1]
+    _lockstep(ctx, m, st, pol, 1.0, min_rounds=3)
+    ctx.close()
+
+
+def _lockstep(ctx, m, st, pol, head, min_rounds, max_rounds=12, logit_tol=5e-2, tie=0.1,
+              dev=None):
+    """Greedy rounds in lockstep with the oracle until the first divergence
+    at a near tie (top-1/top-2 gap <= tie, or a tau crossing); returns the
+    rounds compared.  dev (list, optional) collects each compared round's
+    largest verify-logit deviation."""
+    from oracle import ssd_round
     conf_tol = 1e-3 * head
+
+    def _near(z):
+        return _near_tie(z, tie)
+
     rounds = 0
     checked = 0
-    for _ in range(12):
+    for _ in range(max_rounds):
         drafts, confs = ctx.draft()
         vlog = ctx.verify(d=len(drafts))
         emitted = ctx.accept()
@@ -183,21 +244,24 @@ def test_rounds_match_oracle_in_lockstep(ssd, w, pol, head):
             checked += 1
         if drafts != rec.draft:
             # a divergence is only allowed at a near-tie or a tau crossing
-            tie = (j < len(rec.draft_logits) and _near_tie(rec.draft_logits[j])) or (
+            justified = (j < len(rec.draft_logits) and _near(rec.draft_logits[j])) or (
                 pol.tau is not None and j < len(ref_conf) and abs(ref_conf[j] - pol.tau) <= conf_tol)
-            assert tie, f"drafts diverge at step {j} without a near-tie"
+            assert justified, f"drafts diverge at step {j} without a near-tie"
             break
-        assert np.max(np.abs(vlog - rec.verify_logits)) <= 5e-2 * head
+        dz = float(np.max(np.abs(vlog - rec.verify_logits)))
+        if dev is not None:
+            dev.append(dz)
+        assert dz <= logit_tol * head
         if emitted != rec.emitted:
             j = next(i for i in range(len(emitted) + 1)
                      if i >= len(emitted) or i >= len(rec.emitted) or emitted[i] != rec.emitted[i])
-            assert _near_tie(rec.verify_logits[min(j, len(rec.verify_logits) - 1)]), \
+            assert _near(rec.verify_logits[min(j, len(rec.verify_logits) - 1)]), \
                 f"emitted tokens diverge at {j} without a near-tie"
             break
         rounds += 1
     assert checked >= 1
-    assert rounds >= (1 if head == 1.0 else 3), rounds
-    ctx.close()
+    assert rounds >= min_rounds, rounds
+    return rounds
 
 
 @pytest.mark.parametrize("w,pol,head", [
@@ -209,26 +273,40 @@ def test_sampled_rounds_match_oracle_in_lockstep(ssd, w, pol, head):
     # decisions and emitted tokens agree wherever the decision is not within
     # the tolerance of its boundary (Gumbel score gap > 0.1, |log u - log(p/q)|
     # > 0.05); the first legitimate divergence ends the comparison.
-    from oracle import OracleModel, prefill, ssd_round
-    from oracle.philox import uniforms
-    from oracle import ops as O
+    from oracle import OracleModel, prefill
     ctx, wts = _ctx(ssd, w, lm_head_scale=head)
     ctx.set_policy(pol)
-    prompt = make_prompt(w)
-    first = ctx.prefill(prompt)
     m = OracleModel(w.shape, weights_to_numpy(wts))
-    st = prefill(m, prompt, pol, 256)
-    if first != st.tokens[-1]:
-        pytest.skip("first sampled token sits on a Gumbel near-tie")
     T, seed = pol.temperature, pol.seed
-    V = w.shape.vocab
 
-    def gumbel_gap(z, pos, rnd, stream):
-        sc = np.sort(z / T - np.log(-np.log(uniforms(seed, pos, rnd, stream, V))))
-        return sc[-1] - sc[-2]
+    # the prefill's token is drawn like an AR step: round 0, stream 2, position P
+    prompt = oracle_prompt(
+        m, w, pol, lambda p, st: _gumbel_gap(st.last_logits, T, seed, len(p), 0, 2) > 0.1)
+    first = ctx.prefill(prompt)
+    st = prefill(m, prompt, pol, 256)
+    assert first == st.tokens[-1]
 
-    rounds = accepted_total = rejected_total = 0
-    for _ in range(16):
+    assert _sampled_lockstep(ctx, m, st, pol, head, max_rounds=16) >= 2
+    ctx.close()
+
+
+def _gumbel_gap(z, T, seed, pos, rnd, stream):
+    from oracle.philox import uniforms
+    sc = np.sort(z / T - np.log(-np.log(uniforms(seed, pos, rnd, stream, z.shape[0]))))
+    return sc[-1] - sc[-2]
+
+
+def _sampled_lockstep(ctx, m, st, pol, head, max_rounds, logit_tol=5e-2, tie=0.1,
+                      margin=0.05, dev=None):
+    """Rounds at T > 0 in lockstep with the oracle until the first decision
+    within the tolerance of its boundary (Gumbel-score gap <= tie,
+    |log u - log(p/q)| <= margin); returns the rounds compared."""
+    from oracle import ssd_round
+    from oracle import ops as O
+    T, seed = pol.temperature, pol.seed
+    V = m.s.vocab
+    rounds = 0
+    for _ in range(max_rounds):
         n, rnd = st.n, st.round + 1
         drafts, _ = ctx.draft()
         vlog = ctx.verify(d=len(drafts))
@@ -236,24 +314,25 @@ def test_sampled_rounds_match_oracle_in_lockstep(ssd, w, pol, head):
         rec = ssd_round(m, st, pol)
         if drafts != rec.draft:
             j = next(i for i in range(len(rec.draft)) if drafts[i] != rec.draft[i])
-            assert gumbel_gap(rec.draft_logits[j], n + j, rnd, 0) <= 0.1, "draft sample differs"
+            assert _gumbel_gap(rec.draft_logits[j], T, seed, n + j, rnd, 0) <= tie, \
+                "draft sample differs"
             break
-        assert np.max(np.abs(vlog - rec.verify_logits)) <= 5e-2 * head
+        dz = float(np.max(np.abs(vlog - rec.verify_logits)))
+        if dev is not None:
+            dev.append(dz)
+        assert dz <= logit_tol * head
         Q = np.stack(rec.draft_logits) if rec.draft else np.zeros((0, V))
         margins = O.accept_margins(rec.verify_logits, Q, rec.draft, T, seed, rnd, n)
         k = 0
-        while k < min(len(margins), rec.accepted + 1) and margins[k] > 0.05:
+        while k < min(len(margins), rec.accepted + 1) and margins[k] > margin:
             k += 1
         if k <= rec.accepted and k < len(margins):
             break        # a decision within tolerance of its boundary
-        if O.resample_gap(rec.verify_logits, Q, rec.accepted, T, seed, rnd, n) <= 0.1:
+        if O.resample_gap(rec.verify_logits, Q, rec.accepted, T, seed, rnd, n) <= tie:
             break
         assert emitted == rec.emitted
         rounds += 1
-        accepted_total += rec.accepted
-        rejected_total += int(rec.accepted < rec.d)
-    assert rounds >= 2, rounds
-    ctx.close()
+    return rounds
 
 
 def test_sublayer_masks_are_validated(ssd):

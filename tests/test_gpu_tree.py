@@ -20,7 +20,7 @@ import pytest
 
 from synthetic import TINY, make_weights, weights_to_numpy, make_prompt
 from synthetic.configs import Policy, ModelShape, Workload
-from tests.gpu_util import to_device_weights
+from tests.gpu_util import to_device_weights, oracle_prompt
 
 pytestmark = pytest.mark.gpu
 
@@ -112,12 +112,10 @@ def test_tree_rounds_match_oracle_in_lockstep(ssd, ci, head):
     w, pol = CASES[ci]
     ctx, wts = _ctx(ssd, w, head)
     ctx.set_policy(pol)
-    prompt = make_prompt(w)
-    first = ctx.prefill(prompt)
     m = OracleModel(w.shape, weights_to_numpy(wts))
+    prompt = oracle_prompt(m, w, pol, lambda p, st: not _near_tie(st.last_logits))
+    first = ctx.prefill(prompt)
     st = prefill(m, prompt, pol, 256)
-    if _near_tie(st.last_logits):
-        pytest.skip("near-tie at the first token")
     assert first == st.tokens[-1]
     conf_tol = 1e-3 * head
     rounds = taken = 0
