@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(LinearArgs a
     M = M < 1 ? 1 : kMaxRows;
   if (warp == kEpilogue) {
     LmRec run = lm_empty();
-    epilogue_phase<EPI>(a, p, sm, b, M, lane, rp, run);
+    epilogue_phase<IN, EPI>(a, p, sm, b, M, lane, rp, run);
     if (EPI == EPI_LMHEAD) lm_end(a, p, sm, b, M, warp, lane, rp, run, true);
     return;
   }

@@ -620,6 +620,65 @@ SSD_DI void kouter_chunks(const Part& p, int U0, int U1, F&& f) {
   }
 }
 
+// First row group of the batch that holds the last group of [g_begin,
+// g_end) in the batched K-outer order.
+SSD_HD int kouter_last_batch(int g_begin, int g_end) {
+  return g_begin + ((g_end - g_begin - 1) / kBatch) * kBatch;
+}
+
+// The last batch of a K-outer CTA range, finished by the consumer warps
+// (threads 0 .. kConsumers * 32 - 1) once their MMAs are done, so that the
+// kernel's tail is not one warp working through several 13-row groups.
+// part[gi][w][row][tok] holds warp w's sums of group g0 + gi; every output
+// is finished with the arithmetic of `epilogue` (the warps' sums added in
+// warp order, then the epilogue's own operations), so the bits are those
+// of the epilogue warp's path.  Projections only (not the LM head).
+template <int EPI>
+SSD_DI void final_batch_epilogue(const LinearArgs& a, const float* part, float* epv, int g0,
+                                 int nb, int M, int tid) {
+  constexpr int kT = kConsumers * 32;
+  for (int e = tid; e < nb * 16 * M; e += kT) {
+    const int gi = e / (16 * M), rem = e % (16 * M), row = rem / M, tok = rem % M;
+    float s2 = 0.f;
+    for (int w2 = 0; w2 < kConsumers; ++w2) s2 += part[((gi * kConsumers + w2) * 16 + row) * 16 + tok];
+    epv[(gi * 16 + row) * 16 + tok] = 0.f + s2;
+  }
+  consumer_sync();
+  if (EPI == EPI_STORE) {
+    for (int e = tid; e < nb * 16 * M; e += kT) {
+      const int gi = e / (16 * M), rem = e % (16 * M), row = rem / M, tok = rem % M;
+      a.y[(size_t)tok * a.R + (g0 + gi) * 16 + row] = epv[(gi * 16 + row) * 16 + tok];
+    }
+  } else if (EPI == EPI_RESID) {
+    for (int e = tid; e < nb * 16 * M; e += kT) {
+      const int gi = e / (16 * M), rem = e % (16 * M), row = rem / M, tok = rem % M;
+      float* xp = a.xres + (size_t)tok * a.R + (g0 + gi) * 16 + row;
+      const float xn = __ldcg(xp) + epv[(gi * 16 + row) * 16 + tok];
+      *xp = xn;
+      epv[(gi * 16 + row) * 16 + tok] = xn;
+    }
+    consumer_sync();
+    for (int e = tid; e < nb * M; e += kT) {
+      const int gi = e / M, tok = e % M;
+      float s = 0.f;
+      for (int row = 0; row < 16; ++row) {
+        const float v = epv[(gi * 16 + row) * 16 + tok];
+        s += v * v;
+      }
+      a.ss_out[(size_t)tok * (a.R / kSsGroup) + g0 + gi] = s;
+    }
+  } else if (EPI == EPI_SWIGLU) {
+    // groups g0 + gi (gate, gi even) and g0 + gi + 1 (up) are one feature block
+    for (int e = tid; e < (nb / 2) * 16 * M; e += kT) {
+      const int pi = e / (16 * M), rem = e % (16 * M), row = rem / M, tok = rem % M;
+      const float gt = epv[(2 * pi * 16 + row) * 16 + tok];
+      const float up = epv[((2 * pi + 1) * 16 + row) * 16 + tok];
+      const float sl = gt / (1.0f + expf(-gt));
+      a.u[(size_t)tok * a.R + ((g0 + 2 * pi) >> 1) * 16 + row] = __float2bfloat16_rn(sl * up);
+    }
+  }
+}
+
 template <int EPI>
 SSD_DI void consume_win(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0, int U1, int M,
                         int warp, int lane, RingPos& rp) {
@@ -707,6 +766,30 @@ SSD_DI void consume_win(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0
         }
       }
     }
+    if (EPI != EPI_LMHEAD && g0 == kouter_last_batch(g_begin, g_end)) {
+      // the last batch: every consumer warp is done with the windows and the
+      // ring, so the stage takes the warps' sums and the consumer warps
+      // finish the batch themselves (the epilogue warp stops before it)
+      consumer_sync();
+      float* part = reinterpret_cast<float*>(sm.stage);
+#pragma unroll
+      for (int gi = 0; gi < kBatch; ++gi) {
+        if (gi >= nb) break;
+        float* pw = part + (size_t)(gi * kConsumers + warp) * 256;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int tok = h * 8 + 2 * c;
+          pw[g * 16 + tok] = acc[gi][h][0];
+          pw[g * 16 + tok + 1] = acc[gi][h][1];
+          pw[(g + 8) * 16 + tok] = acc[gi][h][2];
+          pw[(g + 8) * 16 + tok + 1] = acc[gi][h][3];
+        }
+      }
+      consumer_sync();
+      final_batch_epilogue<EPI>(a, part, part + (size_t)nb * kConsumers * 256, g0, nb, M,
+                                threadIdx.x);
+      break;
+    }
     // the batch's groups are done: hand them to the epilogue warp in order
 #pragma unroll
     for (int gi = 0; gi < kBatch; ++gi) {
@@ -785,12 +868,15 @@ SSD_DI void producer_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int
 // the consumer warps' sums added in warp order, so the result depends on the
 // matrix shape only.  The LM head (whole-group partition) folds its groups
 // into one running record per token and publishes it at the end.
-template <int EPI>
+template <int IN, int EPI>
 SSD_DI void epilogue_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int b, int M,
                            int lane, RingPos& rp, LmRec& run) {
   if (b >= p.C || !rp.ok) return;
   const int U0 = unit_begin(p, b), U1 = unit_begin(p, b + 1);
   int vr = U0 / p.KB, kb = U0 % p.KB, left = U1 - U0;
+  // K-outer projections: the consumer warps finish the last batch
+  if (EPI != EPI_LMHEAD && kouter_order<IN, EPI>(a, p))
+    left = kouter_last_batch(U0 / p.KB, U1 / p.KB) * p.KB - U0;
   int slot = 0, round = 0, pos0 = 0;
   if (EPI == EPI_LMHEAD) {
     slot = a.slot_dev ? __ldcg(a.slot_dev) : 0;
