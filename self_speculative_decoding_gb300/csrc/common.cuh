@@ -288,6 +288,18 @@ SSD_DI float gumbel_at(uint64_t seed, int v, int pos, int round, int stream) {
   return -logf(-logf(u01(word_of(r, v & 3))));
 }
 
+// The Gumbel noise of entries 4 b .. 4 b + 3 from one Philox call (the four
+// words of counter block b): g[w] == gumbel_at(seed, 4 b + w, ...).
+SSD_DI void gumbel4(uint64_t seed, int b, int pos, int round, int stream, float (&g)[4]) {
+  const uint4 r = philox4x32_10(make_uint4((uint32_t)b, (uint32_t)pos, (uint32_t)round,
+                                           (uint32_t)stream),
+                                (uint32_t)seed, (uint32_t)(seed >> 32));
+  g[0] = -logf(-logf(u01(r.x)));
+  g[1] = -logf(-logf(u01(r.y)));
+  g[2] = -logf(-logf(u01(r.z)));
+  g[3] = -logf(-logf(u01(r.w)));
+}
+
 // Packed weight unit (16 rows x 32 columns bf16, 1 KB): each 8-row half is
 // row-major with 64-byte rows whose four 16-byte chunks are stored in the
 // 64-byte swizzle order (chunk c of row r at position c ^ ((r >> 1) & 3)),

@@ -236,24 +236,39 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_stoch_kernel(AcceptArgs
   if (row < d) {
     // residual norm(max(0, p - q)); p itself if the residual is empty
     const float* Q = a.Q + (size_t)row * V;
-    for (int v = threadIdx.x; v < V; v += blockDim.x) {
-      const float lp = P[v] / T - lseP;
-      const float w = expf(lp) - expf(Q[v] / T - lseQ);
-      const float g = gumbel_at(a.seed, v, pos, round, 2);
-      if (w > 0.f) {
-        const float sc = logf(w) + g;
-        if (better(sc, v, bv, bi)) { bv = sc; bi = v; }
+    // four consecutive entries per thread and Philox call (the argmax does
+    // not depend on which thread visits an entry)
+    for (int v4 = threadIdx.x * 4; v4 < V; v4 += blockDim.x * 4) {
+      float gg[4];
+      gumbel4(a.seed, v4 >> 2, pos, round, 2, gg);
+#pragma unroll
+      for (int w4 = 0; w4 < 4; ++w4) {
+        const int v = v4 + w4;
+        if (v >= V) break;
+        const float lp = P[v] / T - lseP;
+        const float w = expf(lp) - expf(Q[v] / T - lseQ);
+        const float g = gg[w4];
+        if (w > 0.f) {
+          const float sc = logf(w) + g;
+          if (better(sc, v, bv, bi)) { bv = sc; bi = v; }
+        }
+        const float sp = lp + g;
+        if (better(sp, v, pv, pi)) { pv = sp; pi = v; }
       }
-      const float sp = lp + g;
-      if (better(sp, v, pv, pi)) { pv = sp; pi = v; }
     }
     block_argmax(bv, bi, redv, redi);
     block_argmax(pv, pi, redv, redi);
     if (bv == -INFINITY) bi = pi;
   } else {
-    for (int v = threadIdx.x; v < V; v += blockDim.x) {
-      const float sc = P[v] / T + gumbel_at(a.seed, v, pos, round, 2);
-      if (better(sc, v, bv, bi)) { bv = sc; bi = v; }
+    for (int v4 = threadIdx.x * 4; v4 < V; v4 += blockDim.x * 4) {
+      float gg[4];
+      gumbel4(a.seed, v4 >> 2, pos, round, 2, gg);
+#pragma unroll
+      for (int w4 = 0; w4 < 4; ++w4) {
+        if (v4 + w4 >= V) break;
+        const float sc = P[v4 + w4] / T + gg[w4];
+        if (better(sc, v4 + w4, bv, bi)) { bv = sc; bi = v4 + w4; }
+      }
     }
     block_argmax(bv, bi, redv, redi);
   }

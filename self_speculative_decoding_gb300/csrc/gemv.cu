@@ -52,6 +52,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(LinearArgs a
       mbar_init(&sm.rempty[s], 1);
     }
     mbar_init(&sm.foldbar, 1);
+    mbar_init(&sm.lastbar, 1);
     fence_mbar_init();
   }
   __syncthreads();

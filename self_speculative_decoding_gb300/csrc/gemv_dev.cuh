@@ -347,34 +347,45 @@ SSD_DI void lm_combine(LmRec& r, const LmRec& q, float T) {
 // LM head, one finished row group (16 vocabulary rows in ep[0]): optional
 // logits, then lane tok < M folds the group's rows, in row order, into its
 // running record `run` (the CTA's vocabulary range so far).
+// LM head, token tok's record of one finished row group (vocabulary rows
+// row0 .. row0 + 15, logit of row r at z[r * zstride]), rows in order.
+SSD_DI LmRec lm_group_rec(const LinearArgs& a, int row0, const float* z, int zstride, int tok,
+                          int round, int pos0) {
+  const float T = a.temperature;
+  LmRec r = lm_empty();
+  const bool draw = T > 0.f && a.sample;
+  for (int rb = 0; rb < 16; rb += 4) {
+    float g[4] = {0.f, 0.f, 0.f, 0.f};
+    if (draw) gumbel4(a.seed, (row0 + rb) >> 2, pos0 + tok + 1, round, a.sample_stream, g);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const int row = rb + w;
+      const float zz = z[row * zstride];
+      top2_insert(zz, row0 + row, r.v1, r.i1, r.v2, r.i2);
+      if (draw) {
+        const float sc = zz / T + g[w];
+        if (better(sc, row0 + row, r.gv, r.gi)) { r.gv = sc; r.gi = row0 + row; }
+      }
+    }
+  }
+  for (int row = 0; row < 16; ++row) {
+    const float zz = z[row * zstride];
+    r.se += expf(zz - r.v1);
+    if (T > 0.f) r.set += expf(zz / T - r.v1 / T);
+  }
+  return r;
+}
+
 SSD_DI void lm_group(const LinearArgs& a, int vr, float (*ep)[16][17], int M, int lane, int slot,
                      int round, int pos0, LmRec& run) {
   const int row0 = vr * 16;
-  const float T = a.temperature;
   if (a.logits) {
     for (int e = lane; e < 16 * M; e += 32) {
       const int row = e / M, tok = e % M;
       a.logits[(size_t)(slot + tok) * a.R + row0 + row] = ep[0][row][tok];
     }
   }
-  if (lane < M) {
-    LmRec r = lm_empty();
-    for (int row = 0; row < 16; ++row) {
-      const float z = ep[0][row][lane];
-      top2_insert(z, row0 + row, r.v1, r.i1, r.v2, r.i2);
-      if (T > 0.f && a.sample) {
-        const float sc =
-            z / T + gumbel_at(a.seed, row0 + row, pos0 + lane + 1, round, a.sample_stream);
-        if (better(sc, row0 + row, r.gv, r.gi)) { r.gv = sc; r.gi = row0 + row; }
-      }
-    }
-    for (int row = 0; row < 16; ++row) {
-      const float z = ep[0][row][lane];
-      r.se += expf(z - r.v1);
-      if (T > 0.f) r.set += expf(z / T - r.v1 / T);
-    }
-    lm_combine(run, r, T);
-  }
+  if (lane < M) lm_combine(run, lm_group_rec(a, row0, &ep[0][0][lane], 17, lane, round, pos0), a.temperature);
 }
 
 // LM head, end of CTA b's range: publish the CTA's records (one per token,
@@ -441,6 +452,7 @@ struct __align__(16) GemvSmem {
   uint64_t rfull[2];                 // partial buffer written by all consumer warps
   uint64_t rempty[2];                // partial buffer read by the epilogue warp
   uint64_t foldbar;                  // LM head: the epilogue warp knows whether this CTA folds
+  uint64_t lastbar;                  // LM head: the consumers' records of the last batch are in
   int fold_last;
   __align__(16) bf16 stage[kStageBytes / 2];
 };
@@ -644,6 +656,25 @@ SSD_DI void final_batch_epilogue(const LinearArgs& a, const float* part, float* 
     epv[(gi * 16 + row) * 16 + tok] = 0.f + s2;
   }
   consumer_sync();
+  if (EPI == EPI_LMHEAD) {
+    // logits, then every (group, token) record of lm_group; the epilogue
+    // warp folds the records into its running records in group order
+    const int slot = a.slot_dev ? __ldcg(a.slot_dev) : 0;
+    const int round = a.round_dev ? __ldcg(a.round_dev) : a.round_static;
+    const int pos0 = a.pos0_dev ? __ldcg(a.pos0_dev) : a.pos0_static;
+    if (a.logits)
+      for (int e = tid; e < nb * 16 * M; e += kT) {
+        const int gi = e / (16 * M), rem = e % (16 * M), row = rem / M, tok = rem % M;
+        a.logits[(size_t)(slot + tok) * a.R + (g0 + gi) * 16 + row] = epv[(gi * 16 + row) * 16 + tok];
+      }
+    LmRec* recs = reinterpret_cast<LmRec*>(epv + nb * 256);  // [gi][tok]
+    for (int e = tid; e < nb * M; e += kT) {
+      const int gi = e / M, tok = e % M;
+      recs[gi * kMaxRows + tok] = lm_group_rec(a, (g0 + gi) * 16, epv + gi * 256 + tok, 16, tok,
+                                               round, pos0);
+    }
+    return;
+  }
   if (EPI == EPI_STORE) {
     for (int e = tid; e < nb * 16 * M; e += kT) {
       const int gi = e / (16 * M), rem = e % (16 * M), row = rem / M, tok = rem % M;
@@ -766,7 +797,7 @@ SSD_DI void consume_win(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0
         }
       }
     }
-    if (EPI != EPI_LMHEAD && g0 == kouter_last_batch(g_begin, g_end)) {
+    if (g0 == kouter_last_batch(g_begin, g_end)) {
       // the last batch: every consumer warp is done with the windows and the
       // ring, so the stage takes the warps' sums and the consumer warps
       // finish the batch themselves (the epilogue warp stops before it)
@@ -788,6 +819,10 @@ SSD_DI void consume_win(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0
       consumer_sync();
       final_batch_epilogue<EPI>(a, part, part + (size_t)nb * kConsumers * 256, g0, nb, M,
                                 threadIdx.x);
+      if (EPI == EPI_LMHEAD) {
+        consumer_sync();
+        if (threadIdx.x == 0) mbar_arrive(&sm.lastbar);
+      }
       break;
     }
     // the batch's groups are done: hand them to the epilogue warp in order
@@ -874,9 +909,10 @@ SSD_DI void epilogue_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int
   if (b >= p.C || !rp.ok) return;
   const int U0 = unit_begin(p, b), U1 = unit_begin(p, b + 1);
   int vr = U0 / p.KB, kb = U0 % p.KB, left = U1 - U0;
-  // K-outer projections: the consumer warps finish the last batch
-  if (EPI != EPI_LMHEAD && kouter_order<IN, EPI>(a, p))
-    left = kouter_last_batch(U0 / p.KB, U1 / p.KB) * p.KB - U0;
+  // K-outer ranges: the consumer warps finish the last batch
+  const bool kouter = kouter_order<IN, EPI>(a, p);
+  const int g_last = kouter ? kouter_last_batch(U0 / p.KB, U1 / p.KB) : 0;
+  if (kouter) left = g_last * p.KB - U0;
   int slot = 0, round = 0, pos0 = 0;
   if (EPI == EPI_LMHEAD) {
     slot = a.slot_dev ? __ldcg(a.slot_dev) : 0;
@@ -985,6 +1021,19 @@ SSD_DI void epilogue_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int
     if (lane == 0) a.counter[cidx] = 0u;
     epilogue<EPI>(a, p, gvr, sm.ep, M, lane, xp);
     __syncwarp();
+  }
+  if (EPI == EPI_LMHEAD && kouter) {
+    // the last batch's records, computed by the consumer warps, in group order
+    if (!mbar_wait(&sm.lastbar, 0u)) {
+      if (lane == 0) atomicExch(a.err, 8);
+      rp.ok = false;
+      return;
+    }
+    const LmRec* recs = reinterpret_cast<const LmRec*>(
+        reinterpret_cast<const float*>(sm.stage) + (size_t)(U1 / p.KB - g_last) * (kConsumers + 1) * 256);
+    if (lane < M)
+      for (int gi = 0; gi < U1 / p.KB - g_last; ++gi)
+        lm_combine(run, recs[gi * kMaxRows + lane], a.temperature);
   }
 }
 

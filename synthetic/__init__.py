@@ -14,6 +14,7 @@ from .configs import (  # noqa: F401
     TINY,
     LLAMA7B_SWIFT,
     LLAMA7B_LAYERSKIP,
+    LLAMA7B_EXIT_AGREE,
     LLAMA13B_SCORE,
     LLAMA70B_SWIFT,
     shrink,

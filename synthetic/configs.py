@@ -212,8 +212,19 @@ LLAMA70B_SWIFT = Workload(
 TINY_SHARP = replace(TINY, name="tiny-L4-d256-sharp", lm_head_scale=10.0, random_gains=True,
                      policy=Policy(mode="skip", skip=(2,), d_max=4, tau=None))
 
+# A draft-friendly 7B model (not a configured workload): the LayerSkip exit
+# workload with layers 9..31's residual outputs scaled x0.01, so that the exit
+# at layer 8 predicts nearly what the full model predicts.  On plain random
+# weights a draft is rarely accepted; this model shows what the library's
+# draft / verify / accept machinery delivers when drafts are accepted (the
+# situation trained early-exit models are built for), greedy.
+LLAMA7B_EXIT_AGREE = replace(LLAMA7B_LAYERSKIP, name="llama2-7b-exit8-agreeing", scale=0.01,
+                             gen_len=256,
+                             policy=Policy(mode="exit", exit_layer=8, d_max=12, tau=None))
+
 WORKLOADS = {w.name: w for w in (TINY, LLAMA7B_SWIFT, LLAMA7B_LAYERSKIP, LLAMA13B_SCORE,
-                                 LLAMA70B_SWIFT, LLAMA7B_SUBLAYER, TINY_SHARP)}
+                                 LLAMA70B_SWIFT, LLAMA7B_SUBLAYER, TINY_SHARP,
+                                 LLAMA7B_EXIT_AGREE)}
 
 
 def shrink(w: Workload, **shape_changes) -> Workload:
