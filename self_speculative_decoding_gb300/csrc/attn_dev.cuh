@@ -422,18 +422,26 @@ SSD_DI bool body(const AttnArgs& a, int M, int ns, int pos0, int item, const Sme
         }
       }
       sync();
+      // each row's maximum, then every (row, chunk) weight in parallel, then
+      // each row's sum in chunk order
       for (int rr = tid; rr < R; rr += kGroupThreads) {
         const int m = rr % M;
         const int nc = sm.rpos[m] / kAttnChunk + 1;
         const float* cm = CM + rr * n_active;
         float mx = -INFINITY;
         for (int cc = 0; cc < nc; ++cc) mx = fmaxf(mx, cm[cc]);
+        LR[rr] = mx;
+      }
+      sync();
+      for (int e = tid; e < R * n_active; e += kGroupThreads) {
+        const int rr = e / n_active, cc = e % n_active;
+        if (cc <= sm.rpos[rr % M] / kAttnChunk) CW[e] = expf(CM[e] - LR[rr]);
+      }
+      sync();
+      for (int rr = tid; rr < R; rr += kGroupThreads) {
+        const int nc = sm.rpos[rr % M] / kAttnChunk + 1;
         float L = 0.f;
-        for (int cc = 0; cc < nc; ++cc) {
-          const float w = expf(cm[cc] - mx);
-          CW[rr * n_active + cc] = w;
-          L = fmaf(CL[rr * n_active + cc], w, L);
-        }
+        for (int cc = 0; cc < nc; ++cc) L = fmaf(CL[rr * n_active + cc], CW[rr * n_active + cc], L);
         LR[rr] = L;
       }
       sync();

@@ -460,7 +460,10 @@ struct __align__(16) GemvSmem {
 // (at most kGridCtas x 32 bytes) in its own part of the ring and the stage.
 constexpr int kFoldBytes = 10240;
 static_assert(kGridCtas * 32 <= kFoldBytes, "a warp's fold staging holds every CTA's record");
-static_assert(4 * kFoldBytes <= kRingBytes && (kConsumers - 3) * kFoldBytes <= kStageBytes,
+constexpr int kFoldInRing = kRingBytes / kFoldBytes;    // folding warps staged in the ring
+constexpr int kFoldInStage = kStageBytes / kFoldBytes;  // then in the stage, then in red
+static_assert(kFoldInRing + kFoldInStage + (int)(sizeof(float) * 2 * kConsumers * 256 >= kFoldBytes) >=
+                  kConsumers + 1,
               "the folding warps' staging fits the ring and the stage");
 
 // Position of a warp role in the slot ring and in the partial hand-off
@@ -603,7 +606,10 @@ SSD_DI void consume(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0, in
 constexpr int kWinUnits = 16;
 constexpr int kWinRow = kWinUnits * 32 * 2 + 64;   // bytes per row; rows 16 banks apart
 constexpr int kWinBytes = kMaxRows * kWinRow;
-constexpr int kWinBufs = 3;
+#ifndef SSD_GEMV_WINBUFS
+#define SSD_GEMV_WINBUFS 3
+#endif
+constexpr int kWinBufs = SSD_GEMV_WINBUFS;         // window ring depth: kWinBufs - 1 ahead
 #ifndef SSD_GEMV_BATCH
 #define SSD_GEMV_BATCH 4
 #endif
@@ -738,8 +744,7 @@ SSD_DI void consume_win(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0
     }
     cp_async_commit();
   };
-  issue(0);
-  issue(1);
+  for (int q0 = 0; q0 < kWinBufs - 1; ++q0) issue(q0);
   float acc[kBatch][2][4];
 #pragma unroll
   for (int gi = 0; gi < kBatch; ++gi)
@@ -757,9 +762,9 @@ SSD_DI void consume_win(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0
     for (int kw = 0; kw < nwin; ++kw, ++q) {
       // window q has landed (for every thread's copies) and every warp is
       // done with window q - 1, whose buffer window q + 2 now takes
-      cp_async_wait_group<1>();
+      cp_async_wait_group<kWinBufs - 2>();
       consumer_sync();
-      issue(q + 2);
+      issue(q + kWinBufs - 1);
       const unsigned char* wbase = wb + (q % kWinBufs) * kWinBytes;
       const int kb0 = kw * kWinUnits, ke = min(kb0 + kWinUnits, KB);
 #pragma unroll
@@ -1063,9 +1068,12 @@ SSD_DI void lm_end(const LinearArgs& a, const Part& p, GemvSmem& sm, int b, int 
   __threadfence();
   const int slot = a.slot_dev ? __ldcg(a.slot_dev) : 0;
   const int wi = is_epi ? kConsumers : warp;
-  float* stage = wi < 4 ? reinterpret_cast<float*>(sm.ring + wi * kFoldBytes)
-                        : reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(sm.stage) +
-                                                   (wi - 4) * kFoldBytes);
+  float* stage =
+      wi < kFoldInRing ? reinterpret_cast<float*>(sm.ring + wi * kFoldBytes)
+      : wi < kFoldInRing + kFoldInStage
+          ? reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(sm.stage) +
+                                     (wi - kFoldInRing) * kFoldBytes)
+          : &sm.red[0][0][0][0];
   for (int tok = wi; tok < M; tok += kConsumers + 1) lm_fold(a, p, tok, lane, slot, stage);
 }
 
