@@ -186,6 +186,9 @@ GemvScratch gemv_scratch(int R, int K, int epi) {
 
 cudaError_t launch_gemv(int in_mode, int epi, const LinearArgs& a0, cudaStream_t st, bool pdl) {
   if (!part_fits(a0.R, a0.K)) return cudaErrorInvalidValue;
+  // norm-fused rows must fit the activation stage (callers with more rows
+  // run the RMSNorm pre-pass and a bf16-input projection)
+  if (in_mode == IN_NORM && a0.M_static > gemv_stage_rows(a0.K)) return cudaErrorInvalidValue;
   LinearArgs a = a0;
   if (!a.M_dev && a.M_static > gemv_stage_rows(a.K)) a.wide = 1;
   const Part p = make_part(a.R, a.K, epi);

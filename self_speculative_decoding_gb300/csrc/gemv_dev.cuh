@@ -22,7 +22,7 @@ namespace gemv {
 #define SSD_GEMV_CTAS (152 * SSD_GEMV_CPS)
 #endif
 #ifndef SSD_GEMV_STAGE_KB
-#define SSD_GEMV_STAGE_KB 52
+#define SSD_GEMV_STAGE_KB 44
 #endif
 constexpr int kConsumers = SSD_GEMV_CONSUMERS;   // consumer warps
 constexpr int kProducer = kConsumers;            // warp that issues the bulk copies
@@ -30,10 +30,10 @@ constexpr int kEpilogue = kConsumers + 1;        // warp that finishes row group
 constexpr int kThreads = (kConsumers + 2) * 32;
 constexpr int kCtasPerSm = SSD_GEMV_CPS;         // resident CTAs per SM
 #ifndef SSD_GEMV_CHUNK
-#define SSD_GEMV_CHUNK 8
+#define SSD_GEMV_CHUNK 16
 #endif
 #ifndef SSD_GEMV_SLOTS
-#define SSD_GEMV_SLOTS 5
+#define SSD_GEMV_SLOTS 3
 #endif
 constexpr int kGridCtas = SSD_GEMV_CTAS;         // kCtasPerSm resident CTAs x 152 SMs
 constexpr int kChunk = SSD_GEMV_CHUNK;           // units per ring slot (<= kConsumers * k)
@@ -481,7 +481,7 @@ SSD_DI int chunk_len(const Part& p, int kb, int left) {
   return min(kChunk, min(p.KB - kb, left));
 }
 
-// Consumer warps: take the ring's slots in order, one unit per warp per
+// Consumer warps: take the ring's slots in order, kUPW units per warp per
 // slot, and hand each finished row-group segment to the epilogue warp.
 template <int IN, int EPI, bool STAGED>
 SSD_DI void consume(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0, int U1,
@@ -599,24 +599,34 @@ SSD_DI void consume(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0, in
 // goes through K in windows of kWinUnits units (512 columns), and within a
 // window through the batch's groups, each in chunks of up to kChunk units.
 // The activations of a window (the pass's rows x 512 columns) are copied to
-// shared memory once per batch with cp.async into a ring of kWinBufs buffers,
-// two windows ahead of the one being consumed.  The chunks, the unit each
+// shared memory once per batch with cp.async into a ring of as many buffers
+// of M rows as the stage holds (at most kWinBufs), all but one of them ahead
+// of the window being consumed.  The chunks, the unit each
 // warp takes and the order in which a warp accumulates a group's units are
 // those of the staged layout, so every row's bits are the same in both.
 constexpr int kWinUnits = 16;
 constexpr int kWinRow = kWinUnits * 32 * 2 + 64;   // bytes per row; rows 16 banks apart
 constexpr int kWinBytes = kMaxRows * kWinRow;
 #ifndef SSD_GEMV_WINBUFS
-#define SSD_GEMV_WINBUFS 3
+#define SSD_GEMV_WINBUFS 4
 #endif
-constexpr int kWinBufs = SSD_GEMV_WINBUFS;         // window ring depth: kWinBufs - 1 ahead
+constexpr int kWinBufs = SSD_GEMV_WINBUFS;         // most window buffers (2 .. 4)
 #ifndef SSD_GEMV_BATCH
 #define SSD_GEMV_BATCH 4
 #endif
 constexpr int kBatch = SSD_GEMV_BATCH;             // row groups per batch (even: whole pairs)
-static_assert(kWinBufs * kWinBytes <= kStageBytes, "the window ring fits the stage");
+static_assert(2 * kWinBytes <= kStageBytes, "two windows of kMaxRows rows fit the stage");
+static_assert(kWinBufs >= 2 && kWinBufs <= 4, "window ring depth");
+// window buffers of M rows in the stage
+SSD_HD int win_bufs(int M) {
+  const int n = kStageBytes / (M * kWinRow);
+  return n < kWinBufs ? n : kWinBufs;
+}
 static_assert(kWinUnits % kChunk == 0, "windows hold whole chunks");
 static_assert(kBatch % 2 == 0, "a batch holds whole gate/up pairs");
+static_assert(sizeof(float) * kBatch * (kConsumers + 1) * 256 + sizeof(LmRec) * kBatch * kMaxRows <=
+                  (size_t)kStageBytes,
+              "the last batch's warp sums, outputs and records fit the stage");
 
 template <int IN, int EPI>
 SSD_HD bool kouter_order(const LinearArgs& a, const Part& p) {
@@ -729,13 +739,14 @@ SSD_DI void consume_win(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0
   const int g_begin = U0 / KB, g_end = U1 / KB;
   const int nbatch = (g_end - g_begin + kBatch - 1) / kBatch;
   const int total = nbatch * nwin;                    // windows this CTA consumes
-  // window q (K window q % nwin of batch q / nwin) into buffer q % kWinBufs;
+  // window q (K window q % nwin of batch q / nwin) into buffer q % nbuf;
   // one commit per window, empty past the end, so the group count is uniform
+  const int nbuf = win_bufs(M), wstride = M * kWinRow;
   auto issue = [&](int q) {
     if (q < total) {
       const int kw = q % nwin;
       const int wu = min(kWinUnits, KB - kw * kWinUnits);
-      unsigned char* dst = wb + (q % kWinBufs) * kWinBytes;
+      unsigned char* dst = wb + (q % nbuf) * wstride;
       const bf16* src = a.act + (size_t)kw * kWinUnits * 32;
       for (int e = tid; e < M * kWinUnits * 4; e += kConsumers * 32) {
         const int m = e / (kWinUnits * 4), qq = e % (kWinUnits * 4);
@@ -744,7 +755,7 @@ SSD_DI void consume_win(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0
     }
     cp_async_commit();
   };
-  for (int q0 = 0; q0 < kWinBufs - 1; ++q0) issue(q0);
+  for (int q0 = 0; q0 < nbuf - 1; ++q0) issue(q0);
   float acc[kBatch][2][4];
 #pragma unroll
   for (int gi = 0; gi < kBatch; ++gi)
@@ -761,11 +772,13 @@ SSD_DI void consume_win(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0
     const int nb = min(kBatch, g_end - g0);
     for (int kw = 0; kw < nwin; ++kw, ++q) {
       // window q has landed (for every thread's copies) and every warp is
-      // done with window q - 1, whose buffer window q + 2 now takes
-      cp_async_wait_group<kWinBufs - 2>();
+      // done with window q - 1, whose buffer window q + nbuf - 1 now takes
+      if (nbuf == 2) cp_async_wait_group<0>();
+      else if (nbuf == 3) cp_async_wait_group<1>();
+      else cp_async_wait_group<2>();
       consumer_sync();
-      issue(q + kWinBufs - 1);
-      const unsigned char* wbase = wb + (q % kWinBufs) * kWinBytes;
+      issue(q + nbuf - 1);
+      const unsigned char* wbase = wb + (q % nbuf) * wstride;
       const int kb0 = kw * kWinUnits, ke = min(kb0 + kWinUnits, KB);
 #pragma unroll
       for (int gi = 0; gi < kBatch; ++gi) {
@@ -1136,6 +1149,11 @@ SSD_DI void consumer_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int
     consume<IN, EPI, true>(a, p, sm, U0, U1, M, warp, lane, rp);
   } else if (kouter) {
     consume_win<EPI>(a, p, sm, U0, U1, M, warp, lane, rp);
+  } else if constexpr (IN == IN_NORM) {
+    // norm-fused rows always fit the stage (the host refuses more and runs
+    // the RMSNorm pre-pass with a bf16-input pass instead)
+    if (lane == 0) atomicExch(a.err, 9);
+    rp.ok = false;
   } else {
     consume<IN, EPI, false>(a, p, sm, U0, U1, M, warp, lane, rp);
   }

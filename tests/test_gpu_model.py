@@ -38,8 +38,8 @@ MID = Workload(name="mid-dh128", shape=ModelShape(
     n_layers=4, d_model=1024, n_heads=8, n_kv_heads=8, head_dim=128, ffn_dim=2816, vocab=4096),
     scaled_layers=(1, 2), scale=0.1)
 
-# wide enough that a verify pass of more than 6 rows does not fit the GEMV's
-# activation stage: the norm pre-pass and the windowed activation layout run
+# wide enough that a verify pass of more than 5 rows does not fit the GEMV's
+# 44 KB activation stage: the norm pre-pass and the windowed activation layout run
 WIDE = Workload(name="wide-d4096", shape=ModelShape(
     n_layers=3, d_model=4096, n_heads=32, n_kv_heads=8, head_dim=128, ffn_dim=2048, vocab=4096),
     scaled_layers=(1,), scale=0.1)
