@@ -113,7 +113,8 @@ ssd_status ssd_op_philox(const uint32_t* ctr, int32_t count, uint64_t key, uint3
  * give hundreds of rows): for T >= 1 rows of act (bf16 [T][K]),
  *   epi 0 (store):  out fp32 [T][R] = W act
  *   epi 1 (resid):  out fp32 [*][R]: out[map[t]] += W act[t] (map: device
- *                   int32 [T], NULL = identity; rows not named stay as they are)
+ *                   int32 [T] of distinct rows, NULL = identity; rows not
+ *                   named stay as they are)
  *   epi 2 (swiglu): out bf16 [T][R] = bf16(silu(W act) * (W1 act)), W1 the
  *                   up matrix (same shape as W)
  *   epi 3 (argmax): out int32 [T] = argmax_r (W act)[r], lowest r on ties

@@ -20,19 +20,22 @@
 // Operands are staged in shared memory in the K-major 64-byte-swizzle layout
 // the MMA descriptors read.  Weights and activations are both stored in the
 // packed unit layout (16 rows x 32 columns; each 8-row half is one 512-byte
-// swizzle atom), which a tensor map views as a 3-D tensor (256 elements of a
-// half unit, half units along K, 16-row groups): one tiled TMA copy brings 8
-// row groups of one K block (8 KB), another the token tile's K block
-// (NT x 64 bytes), rows beyond the matrix zero-filled.  A stage holds two
-// 32-wide K blocks; thread 0 issues the copies (stage barrier `full`,
-// transaction bytes).  One thread per accumulator, each in its own warp,
-// issues the MMAs: a single thread's issue rate (about 150 cycles per MMA,
-// measured) cannot keep the tensor core busy at N < 256.  Each commits its
-// MMAs of a stage to the stage's `empty` barrier (one arrival per issuer
-// frees it for the copies `stages` steps ahead), and last to `done`.  All loops advance
-// their slot and phase parity incrementally (no division in the issue
-// path).  Every accumulator sums its K steps in ascending order, so the
-// result depends on the shapes only.
+// swizzle atom), which a tensor map views as a 3-D tensor of 8-byte
+// elements (the 1 KB of a unit, 16-row groups, K blocks): one tiled TMA copy
+// brings 8 row groups of all the K blocks of a stage ([K block][group][unit],
+// 8 KB per K block), another the token tile's K blocks (NT x 64 bytes per K
+// block), rows beyond the matrix and K blocks beyond K zero-filled.  Thread 0
+// issues the copies (stage barrier `full`, transaction bytes): the copy
+// engine accepts one tiled copy every 75-110 ns per SM, so a copy per
+// operand per stage rather than per K block keeps the loads ahead of the
+// MMAs.  One thread per accumulator, each in its own warp, issues the MMAs
+// (a single thread issues M = 128 MMAs at the tensor core's own rate, about
+// N / 2 cycles each).  Each commits its MMAs of a stage to the stage's
+// `empty` barrier (one arrival per issuer frees it for the copies `stages`
+// steps ahead), and last to `done`.  All loops advance their slot and phase
+// parity incrementally (no division in the issue path).  Every accumulator
+// sums its K steps in ascending order, so the result depends on the shapes
+// only.
 //
 // Epilogue: each warp reads its 32 TMEM lanes (tcgen05.ld, 16 columns at a
 // time): store fp32; residual add into the rows named by a row map; SwiGLU to
@@ -57,7 +60,13 @@ constexpr int kTcMaxStages = 16;
 constexpr int kTcThreads = 160;    // warp 0: copies; warps 1-4: MMA issuers; warps 0-3: epilogue
 constexpr int kTcMaxN = 256;
 constexpr int kTcManyTiles = 100;  // 128-row tiles from which a matrix uses one accumulator
-constexpr int kTcSmemBudget = 216 * 1024;  // per SM, split among resident CTAs
+#ifndef SSD_TC_SMEM_KB
+#define SSD_TC_SMEM_KB 216
+#endif
+#ifndef SSD_TC_KBS
+#define SSD_TC_KBS 0  // K blocks per stage; 0: chosen per shape
+#endif
+constexpr int kTcSmemBudget = SSD_TC_SMEM_KB * 1024;  // per SM, split among resident CTAs
 constexpr int kWaitPolls = 1 << 24;
 
 // Tiled TMA load of a 3-D box at (c0, c1, c2), completing on `bar`.
@@ -130,6 +139,9 @@ SSD_DI void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// Barrier of the four epilogue warps (threads 0 .. 127).
+SSD_DI void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
 // float -> uint32 with the same order (argmax keys)
 SSD_DI uint32_t order_key(float v) {
   const uint32_t u = __float_as_uint(v);
@@ -186,6 +198,8 @@ TcShape tc_shape(int T, bool swiglu, int m_tiles, int sms) {
   // deeper stages (4 K blocks) amortise each issuer's per-stage barrier
   // wait, fence and commit when at least 3 of them still fit
   s.kbs = (kTcSmemBudget / per_sm) / (4 * kb_bytes) >= 3 ? 4 : 2;
+  // a stage's 2 kbs K16 steps are dealt to the issuers of a matrix by j mod per
+  if (SSD_TC_KBS > 0 && 2 * SSD_TC_KBS >= (swiglu ? s.nacc / 2 : s.nacc)) s.kbs = SSD_TC_KBS;
   s.stage_bytes = s.kbs * kb_bytes;
   s.stages = (kTcSmemBudget / per_sm) / s.stage_bytes;
   if (s.stages > kTcMaxStages) s.stages = kTcMaxStages;
@@ -197,7 +211,8 @@ TcShape tc_shape(int T, bool swiglu, int m_tiles, int sms) {
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ CUtensorMap mW1,
                    const __grid_constant__ CUtensorMap mAct, GemmArgs a, int NT, int ncols,
-                   int stages, int stage_bytes, int tx_kb, int nacc, int kbs) {
+                   int stages, int stage_bytes, int tx_stage, int nacc, int kbs, int kbox,
+                   int wsplit) {
   extern __shared__ unsigned char sm_raw[];
   // 1024-byte aligned stage area (the swizzle pattern repeats every 512 bytes
   // of the absolute shared-memory address)
@@ -212,7 +227,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int KB = a.K / 32;
   const bool swiglu = a.epi == GEMM_SWIGLU;
-  const int a_kb = (swiglu ? 2 : 1) * kTcGroups * 1024;   // weight bytes per K block
+  constexpr int wkb = kTcGroups * 1024;                    // one matrix's bytes per K block
+  const int a_kb = (swiglu ? 2 : 1) * wkb;                 // weight bytes per K block
   const int rg0 = blockIdx.y * kTcGroups;
   const int t0 = blockIdx.x * NT;
 
@@ -232,12 +248,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tslot;
 
-  // A stage holds kbs K blocks: weights [kbl][a_kb] then activations
+  // A stage holds kbs K blocks: the weights [kbl][8 KB] (SwiGLU: all the
+  // gate blocks, then all the up blocks), then the activations
   // [kbl][NT x 64 B].  Slots and phase parities advance incrementally.
   const int nst = (KB + kbs - 1) / kbs;
   if (warp == 0 && lane == 0) {
-    // producer: per K block one box of 8 weight row groups (two for SwiGLU)
-    // and one box of the tile's tokens
+    // producer: per stage one box of kbox K blocks of 8 weight row groups
+    // (one per K block for matrices of fewer row groups; two matrices for
+    // SwiGLU) and one box of the tile's tokens
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&mW0) : "memory");
+    if (swiglu) asm volatile("prefetch.tensormap [%0];" ::"l"(&mW1) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&mAct) : "memory");
     int s = 0, st = 0;
     uint32_t par = 0;
     unsigned char* S = sm;
@@ -246,15 +267,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         atomicExch(fail, 1);
         break;
       }
-      const int kb0 = s * kbs, nk = min(kbs, KB - kb0);
-      mbar_arrive_expect_tx(&full[st], (uint32_t)(nk * tx_kb));
-      for (int kbl = 0; kbl < nk; ++kbl) {
-        unsigned char* A = S + kbl * a_kb;
-        const int c1 = 2 * (kb0 + kbl);
-        tma_load_3d(A, &mW0, 0, c1, rg0, &full[st]);
-        if (swiglu) tma_load_3d(A + kTcGroups * 1024, &mW1, 0, c1, rg0, &full[st]);
-        tma_load_3d(S + kbs * a_kb + kbl * (NT * 64), &mAct, 0, c1, t0 / 16, &full[st]);
+      const int kb0 = s * kbs;
+      mbar_arrive_expect_tx(&full[st], (uint32_t)tx_stage);
+      if (!wsplit) {
+        tma_load_3d(S, &mW0, 0, rg0, kb0, &full[st]);
+        if (swiglu) tma_load_3d(S + kbs * wkb, &mW1, 0, rg0, kb0, &full[st]);
+      } else {
+        for (int kbl = 0; kbl < kbox; ++kbl) {
+          tma_load_3d(S + kbl * wkb, &mW0, 0, rg0, kb0 + kbl, &full[st]);
+          if (swiglu) tma_load_3d(S + (kbs + kbl) * wkb, &mW1, 0, rg0, kb0 + kbl, &full[st]);
+        }
       }
+      tma_load_3d(S + kbs * a_kb, &mAct, 0, t0 / 16, kb0, &full[st]);
       if (++st == stages) {
         st = 0;
         par ^= 1u;
@@ -277,7 +301,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t idesc = idesc_bf16(kTcM, NT);
     const uint64_t d0 = sw64_desc(smem_addr(sm));
     const uint32_t dcol = tmem + (uint32_t)(who * NT);
-    const uint32_t wofs = swiglu && who >= per ? (uint32_t)(kTcGroups * 1024 >> 4) : 0u;
+    const uint32_t wofs = swiglu && who >= per ? (uint32_t)(kbs * wkb >> 4) : 0u;
     int st = 0;
     uint32_t par = 0, off = 0;
     for (int s = 0; s < nst; ++s) {
@@ -289,7 +313,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int nj = 2 * min(kbs, KB - s * kbs);
       for (int j = r; j < nj; j += per) {
         const int kbl = j >> 1, ks = j & 1;
-        const uint64_t da = d0 + ((off + kbl * a_kb) >> 4) + wofs + 2 * ks;
+        const uint64_t da = d0 + ((off + kbl * wkb) >> 4) + wofs + 2 * ks;
         const uint64_t db = d0 + ((off + kbs * a_kb + kbl * (NT * 64)) >> 4) + 2 * ks;
         mma_bf16_tc(dcol, da, db, idesc, (s != 0 || j != r) ? 1u : 0u);
       }
@@ -337,61 +361,94 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
   const int row = rg0 * 16 + warp * 32 + lane;   // output row (feature for SwiGLU)
   const bool rv = row < a.R;
-  for (int c0 = 0; c0 < NT; c0 += 16) {
-    float v[16];
-    tmem_ld16(trow + (uint32_t)c0, v);
-    for (int q = 1; q < nsum; ++q) {
-      float v1[16];
-      tmem_ld16(trow + (uint32_t)(q * NT + c0), v1);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] += v1[j];
-    }
-    if (a.epi == GEMM_ARGMAX) {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int tok = t0 + c0 + j;
-        float bv = rv ? v[j] : -INFINITY;
-        int bi = rv ? row : 0x7fffffff;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-          if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-        }
-        if (lane == 0 && tok < a.T && bi != 0x7fffffff)
-          atomicMax(a.best + tok, ((unsigned long long)order_key(bv) << 32) |
-                                      (unsigned long long)(0xffffffffu - (uint32_t)bi));
+  // Residual add: the tile's residual rows are staged in the stage memory
+  // (idle once every MMA has completed) with 16-byte asynchronous copies, all
+  // in flight at once, in passes of as many tokens as it holds: xs[t][128]
+  // floats, then the pass's map rows.
+  const bool resid = a.epi == GEMM_RESID;
+  const int ns_max = min(NT, ((stages * stage_bytes - 1024) / 512) & ~15);
+  float* xs = reinterpret_cast<float*>(sm);
+  int* orow_s = reinterpret_cast<int*>(sm + (size_t)ns_max * 512);
+  const int rows_here = min(kTcM, a.R - rg0 * 16);  // tile rows inside the matrix (multiple of 16)
+  const int pass = resid ? ns_max : NT;
+  for (int p0 = 0; p0 < NT; p0 += pass) {
+    const int np = min(pass, NT - p0);
+    if (resid) {
+      epi_sync();  // the previous pass's reads of xs are done
+      for (int t = tid; t < np; t += kTcM) {
+        const int tok = t0 + p0 + t;
+        orow_s[t] = tok < a.T ? (a.rowmap ? __ldg(a.rowmap + tok) : tok) : -1;
       }
-    } else if (swiglu) {
-      float up[16];
-      tmem_ld16(trow + (uint32_t)(per * NT + c0), up);
+      epi_sync();
+      for (int e = tid; e < np * 32; e += kTcM) {
+        const int t = e >> 5, q = e & 31;
+        const int om = orow_s[t];
+        if (om >= 0 && q * 4 < rows_here)
+          cp_async16(xs + t * kTcM + q * 4, a.x + (size_t)om * a.R + rg0 * 16 + q * 4);
+      }
+      cp_async_wait_all();
+      epi_sync();
+    }
+    for (int c0 = p0; c0 < p0 + np; c0 += 16) {
+      float v[16];
+      tmem_ld16(trow + (uint32_t)c0, v);
       for (int q = 1; q < nsum; ++q) {
         float v1[16];
-        tmem_ld16(trow + (uint32_t)((per + q) * NT + c0), v1);
+        tmem_ld16(trow + (uint32_t)(q * NT + c0), v1);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) up[j] += v1[j];
+        for (int j = 0; j < 16; ++j) v[j] += v1[j];
       }
+      if (a.epi == GEMM_ARGMAX) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int tok = t0 + c0 + j;
-        if (rv && tok < a.T) {
-          const float gt = v[j];
-          const float sl = gt / (1.0f + expf(-gt));
-          a.u[a.u_packed ? packed_off(tok, row, a.R) : (size_t)tok * a.R + row] =
-              __float2bfloat16_rn(sl * up[j]);
-        }
-      }
-    } else if (rv) {
+        for (int j = 0; j < 16; ++j) {
+          const int tok = t0 + c0 + j;
+          float bv = rv ? v[j] : -INFINITY;
+          int bi = rv ? row : 0x7fffffff;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int tok = t0 + c0 + j;
-        if (tok < a.T) {
-          if (a.epi == GEMM_STORE) {
-            a.y[(size_t)tok * a.R + row] = v[j];
-          } else {
-            const size_t orow = a.rowmap ? (size_t)a.rowmap[tok] : (size_t)tok;
-            a.x[orow * a.R + row] += v[j];
+          for (int o = 1; o < 32; o <<= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
           }
+          if (lane == 0 && tok < a.T && bi != 0x7fffffff)
+            atomicMax(a.best + tok, ((unsigned long long)order_key(bv) << 32) |
+                                        (unsigned long long)(0xffffffffu - (uint32_t)bi));
+        }
+      } else if (swiglu) {
+        float up[16];
+        tmem_ld16(trow + (uint32_t)(per * NT + c0), up);
+        for (int q = 1; q < nsum; ++q) {
+          float v1[16];
+          tmem_ld16(trow + (uint32_t)((per + q) * NT + c0), v1);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) up[j] += v1[j];
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int tok = t0 + c0 + j;
+          if (rv && tok < a.T) {
+            // silu with the fast exponential and division: the full-precision
+            // pair costs most of the epilogue, and the product is rounded to bf16
+            const float gt = v[j];
+            const float sl = __fdividef(gt, 1.0f + __expf(-gt));
+            a.u[a.u_packed ? packed_off(tok, row, a.R) : (size_t)tok * a.R + row] =
+                __float2bfloat16_rn(sl * up[j]);
+          }
+        }
+      } else if (resid) {
+        if (rv) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int t = c0 - p0 + j;
+            const int om = orow_s[t];
+            if (om >= 0) a.x[(size_t)om * a.R + row] = xs[t * kTcM + warp * 32 + lane] + v[j];
+          }
+        }
+      } else if (rv) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int tok = t0 + c0 + j;
+          if (tok < a.T) a.y[(size_t)tok * a.R + row] = v[j];
         }
       }
     }
@@ -444,17 +501,18 @@ EncodeTiled encoder() {
   return fn;
 }
 
-// A packed [groups * 16][K] bf16 matrix seen as (256 elements, 2 K / 32 half
-// units, groups); boxes of (256, 2, box_groups): one K block of box_groups
-// row groups, landing as consecutive 1 KB units.
-bool packed_map(CUtensorMap* m, const void* base, int K, int groups, int box_groups) {
+// A packed [groups * 16][K] bf16 matrix seen as (128 8-byte elements of a
+// 1 KB unit, groups, K / 32 K blocks); boxes of (128, box_groups, box_kb):
+// box_kb K blocks of box_groups row groups, landing K block by K block as
+// consecutive 1 KB units.
+bool packed_map(CUtensorMap* m, const void* base, int K, int groups, int box_groups, int box_kb) {
   EncodeTiled enc = encoder();
   if (!enc) return false;
-  const cuuint64_t dims[3] = {256, (cuuint64_t)(2 * (K / 32)), (cuuint64_t)groups};
-  const cuuint64_t strides[2] = {512, (cuuint64_t)(K / 32) * 1024};
-  const cuuint32_t box[3] = {256, 2, (cuuint32_t)box_groups};
+  const cuuint64_t dims[3] = {128, (cuuint64_t)groups, (cuuint64_t)(K / 32)};
+  const cuuint64_t strides[2] = {(cuuint64_t)(K / 32) * 1024, 1024};
+  const cuuint32_t box[3] = {128, (cuuint32_t)box_groups, (cuuint32_t)box_kb};
   const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -476,7 +534,8 @@ cudaError_t launch_argmax_index(const unsigned long long* best, int T, int32_t* 
 cudaError_t launch_gemm_rows(const GemmArgs& a, cudaStream_t s) {
   if (a.R % 16 || a.K % 32 || a.T <= 0) return cudaErrorInvalidValue;
   const bool swiglu = a.epi == GEMM_SWIGLU;
-  if (((uintptr_t)a.W0 | (uintptr_t)a.act | (swiglu ? (uintptr_t)a.W1 : 0)) & 15)
+  if (((uintptr_t)a.W0 | (uintptr_t)a.act | (swiglu ? (uintptr_t)a.W1 : 0) |
+       (a.epi == GEMM_RESID ? (uintptr_t)a.x : 0)) & 15)
     return cudaErrorInvalidValue;
   static int sms_of[kDeviceSlots] = {};
   const int dv0 = device_slot();
@@ -495,11 +554,16 @@ cudaError_t launch_gemm_rows(const GemmArgs& a, cudaStream_t s) {
   const int groups = a.R / 16, tgroups = (a.T + 15) / 16;
   const int wbox = groups < kTcGroups ? groups : kTcGroups;
   const int xbox = tgroups < sh.NT / 16 ? tgroups : sh.NT / 16;
-  if (!packed_map(&m0, a.W0, a.K, groups, wbox) ||
-      !packed_map(&m1, swiglu ? a.W1 : a.W0, a.K, groups, wbox) ||
-      !packed_map(&mx, a.act, a.K, tgroups, xbox))
+  // K blocks per box: a stage's worth (fewer when K is shorter); a matrix of
+  // fewer than 8 row groups takes one box per K block, so that each K block
+  // still starts 8 KB after the previous one
+  const int kbox = sh.kbs < a.K / 32 ? sh.kbs : a.K / 32;
+  const int wsplit = wbox < kTcGroups ? 1 : 0;
+  if (!packed_map(&m0, a.W0, a.K, groups, wbox, wsplit ? 1 : kbox) ||
+      !packed_map(&m1, swiglu ? a.W1 : a.W0, a.K, groups, wbox, wsplit ? 1 : kbox) ||
+      !packed_map(&mx, a.act, a.K, tgroups, xbox, kbox))
     return cudaErrorInvalidValue;
-  const int tx = ((swiglu ? 2 : 1) * wbox + xbox) * 1024;
+  const int tx = kbox * ((swiglu ? 2 : 1) * wbox + xbox) * 1024;
   static size_t smem_set[kDeviceSlots] = {};
   const int dv = device_slot();
   if (dv < 0 || sh.smem > smem_set[dv]) {
@@ -510,7 +574,8 @@ cudaError_t launch_gemm_rows(const GemmArgs& a, cudaStream_t s) {
   }
   dim3 grid(sh.tiles, (groups + kTcGroups - 1) / kTcGroups);
   gemm_tc_kernel<<<grid, kTcThreads, sh.smem, s>>>(m0, m1, mx, a, sh.NT, sh.ncols, sh.stages,
-                                                   sh.stage_bytes, tx, sh.nacc, sh.kbs);
+                                                   sh.stage_bytes, tx, sh.nacc, sh.kbs, kbox,
+                                                   wsplit);
   return cudaGetLastError();
 }
 

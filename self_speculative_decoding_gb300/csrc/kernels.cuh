@@ -289,8 +289,8 @@ struct GemmArgs {
   const bf16* act = nullptr;           // [T][K] in the packed unit layout (packed_off), T padded to 16
   int epi = GEMM_STORE;
   float* y = nullptr;                  // GEMM_STORE [T][R]
-  float* x = nullptr;                  // GEMM_RESID: x[rowmap[t]][r] += out[t][r]
-  const int32_t* rowmap = nullptr;     // nullable: identity
+  float* x = nullptr;                  // GEMM_RESID: x[rowmap[t]][r] += out[t][r] (16-byte aligned)
+  const int32_t* rowmap = nullptr;     // nullable: identity; distinct rows
   bf16* u = nullptr;                   // GEMM_SWIGLU [T][R]: silu(gate) * up
   int u_packed = 0;                    // 1: u in the packed unit layout
   unsigned long long* best = nullptr;  // GEMM_ARGMAX [T]: atomic max of (value, -index) keys, zero before
