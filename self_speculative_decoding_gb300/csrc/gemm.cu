@@ -61,12 +61,15 @@ constexpr int kTcThreads = 160;    // warp 0: copies; warps 1-4: MMA issuers; wa
 constexpr int kTcMaxN = 256;
 constexpr int kTcManyTiles = 100;  // 128-row tiles from which a matrix uses one accumulator
 #ifndef SSD_TC_SMEM_KB
-#define SSD_TC_SMEM_KB 216
+#define SSD_TC_SMEM_KB 224
 #endif
 #ifndef SSD_TC_KBS
 #define SSD_TC_KBS 0  // K blocks per stage; 0: chosen per shape
 #endif
-constexpr int kTcSmemBudget = SSD_TC_SMEM_KB * 1024;  // per SM, split among resident CTAs
+// stage memory of a CTA alone on its SM, and of each of two CTAs on an SM
+// (227 KB per CTA at most; two CTAs share 228 KB less 1 KB each)
+constexpr int kTcSmemBudget1 = SSD_TC_SMEM_KB * 1024;
+constexpr int kTcSmemBudget2 = 108 * 1024;
 constexpr int kWaitPolls = 1 << 24;
 
 // Tiled TMA load of a 3-D box at (c0, c1, c2), completing on `bar`.
@@ -197,11 +200,15 @@ TcShape tc_shape(int T, bool swiglu, int m_tiles, int sms) {
   if (per_sm < 1) per_sm = 1;
   // deeper stages (4 K blocks) amortise each issuer's per-stage barrier
   // wait, fence and commit when at least 3 of them still fit
-  s.kbs = (kTcSmemBudget / per_sm) / (4 * kb_bytes) >= 3 ? 4 : 2;
-  // a stage's 2 kbs K16 steps are dealt to the issuers of a matrix by j mod per
-  if (SSD_TC_KBS > 0 && 2 * SSD_TC_KBS >= (swiglu ? s.nacc / 2 : s.nacc)) s.kbs = SSD_TC_KBS;
+  const int budget = per_sm == 1 ? kTcSmemBudget1 : kTcSmemBudget2;
+  s.kbs = budget / (4 * kb_bytes) >= 3 ? 4 : 2;
+  // a stage's 2 kbs K16 steps are dealt to the issuers of a matrix by j mod
+  // per, so kbs is 2 or 4 (the deal is then the step's index mod per)
+  if (SSD_TC_KBS == 2 || SSD_TC_KBS == 4) s.kbs = SSD_TC_KBS;
+  // no copy box above 32 KB (a 64 KB box of activations failed to encode)
+  if (s.kbs == 4 && 4 * s.NT * 64 > 32768) s.kbs = 2;
   s.stage_bytes = s.kbs * kb_bytes;
-  s.stages = (kTcSmemBudget / per_sm) / s.stage_bytes;
+  s.stages = budget / s.stage_bytes;
   if (s.stages > kTcMaxStages) s.stages = kTcMaxStages;
   if (s.stages < 2) s.stages = 2;
   s.smem = 1024 + (size_t)s.stages * s.stage_bytes + 512;
