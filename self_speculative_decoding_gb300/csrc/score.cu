@@ -129,27 +129,31 @@ SSD_DI void ldsm_x4_trans(uint32_t (&r)[4], const void* p) {
 constexpr int kSaKeys = 64;  // keys per block
 
 // Window-query attention.  CTA (row block, head h, active candidate ja):
-// warps own 16 query rows each.  Keys: the shared cache's positions
-// [0, split) then the candidate's own window rows w <= i.  S = Q K^T and
-// O += P V run on the tensor cores (bf16 operands, fp32 accumulation); the
-// softmax is the online form in base 2 with the running max per row.  Every
-// row sums its key blocks in ascending key order.
+// the row block's 16-row tiles each get two warps, which take the first and
+// the second 32 keys of every 64-key block (more warps per SM for the same
+// K/V buffers, half the dependent chain per warp).  Keys: the shared cache's
+// positions [0, split) then the candidate's own window rows w <= i.  S = Q K^T
+// and O += P V run on the tensor cores (bf16 operands, fp32 accumulation); the
+// softmax is the online form in base 2 with the running max per row.  Each
+// warp sums its key blocks in ascending key order; the two halves' states are
+// merged at the end (first half + second half, in that order).
 template <int DH>
-__global__ void __launch_bounds__(128) score_attn_kernel(ScoreAttnArgs a) {
+__global__ void __launch_bounds__(256) score_attn_kernel(ScoreAttnArgs a) {
   extern __shared__ __align__(16) unsigned char sm_raw[];
   constexpr int KT = DH / 16;      // k16 steps of Q K^T
   constexpr int NT = DH / 8;       // n8 tiles of the output
   constexpr int RS = DH + 8;       // padded smem row (bf16)
   bf16* smK = reinterpret_cast<bf16*>(sm_raw);          // [2][64][RS]
   bf16* smV = smK + 2 * kSaKeys * RS;                   // [2][64][RS]
-  const int nw = blockDim.x >> 5;
+  const int nwr = blockDim.x >> 6;                     // row tiles of the CTA
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rt = warp % nwr, kh = warp / nwr;          // row tile, key half
   const int g = lane >> 2, c = lane & 3;
   const int h = blockIdx.y, ja = blockIdx.z;
   const int kvh = h / (a.H / a.Hkv);
   const int cand = a.cand[ja];
-  const int r0 = blockIdx.x * nw * 16;                 // first window row of the CTA
-  const int i0 = r0 + warp * 16;                       // first row of the warp
+  const int r0 = blockIdx.x * nwr * 16;                // first window row of the CTA
+  const int i0 = r0 + rt * 16;                         // first row of the warp
   const int N = a.N;
 
   // Q fragments (rows beyond N are zero)
@@ -173,7 +177,7 @@ __global__ void __launch_bounds__(128) score_attn_kernel(ScoreAttnArgs a) {
   float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
 
   const int nb_pre = (a.split + kSaKeys - 1) / kSaKeys;
-  const int wmax = min(N, r0 + nw * 16);               // window keys the CTA needs
+  const int wmax = min(N, r0 + nwr * 16);              // window keys the CTA needs
   const int nb = nb_pre + (wmax + kSaKeys - 1) / kSaKeys;
   const bf16* kc = a.kc + (size_t)kvh * a.max_seq * DH;
   const bf16* vc = a.vc + (size_t)kvh * a.max_seq * DH;
@@ -211,12 +215,12 @@ __global__ void __launch_bounds__(128) score_attn_kernel(ScoreAttnArgs a) {
     __syncthreads();
     const bf16* Kb = smK + (size_t)buf * kSaKeys * RS;
     const bf16* Vb = smV + (size_t)buf * kSaKeys * RS;
-    // S = Q K^T for 64 keys
-    float s[8][4];
+    // S = Q K^T for this warp's 32 keys of the block
+    float s[4][4];
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+    for (int nt = 0; nt < 4; ++nt) {
       s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-      const bf16* kr = Kb + (size_t)(nt * 8 + g) * RS + 2 * c;
+      const bf16* kr = Kb + (size_t)(kh * 32 + nt * 8 + g) * RS + 2 * c;
 #pragma unroll
       for (int kt = 0; kt < KT; ++kt) {
         const uint32_t b0 = *reinterpret_cast<const uint32_t*>(kr + kt * 16);
@@ -226,10 +230,10 @@ __global__ void __launch_bounds__(128) score_attn_kernel(ScoreAttnArgs a) {
     }
     // mask, scale, online softmax
     const bool pre = b < nb_pre;
-    const int kbase = pre ? b * kSaKeys : (b - nb_pre) * kSaKeys;
+    const int kbase = (pre ? b * kSaKeys : (b - nb_pre) * kSaKeys) + kh * 32;
     float bm[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int key = kbase + nt * 8 + 2 * c + (e & 1);
@@ -249,9 +253,9 @@ __global__ void __launch_bounds__(128) score_attn_kernel(ScoreAttnArgs a) {
       mrow[r] = mn;
     }
     float ls[2] = {0.f, 0.f};
-    uint32_t pf[4][4];
+    uint32_t pf[2][4];
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+    for (int nt = 0; nt < 4; ++nt) {
       float pv[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -271,9 +275,9 @@ __global__ void __launch_bounds__(128) score_attn_kernel(ScoreAttnArgs a) {
       o[j][2] *= corr[1];
       o[j][3] *= corr[1];
     }
-    // O += P V: k16 step kk covers keys 16kk .. 16kk + 15
+    // O += P V: k16 step kk covers this warp's keys 16kk .. 16kk + 15
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
+    for (int kk = 0; kk < 2; ++kk) {
       // A fragment order: (row g, keys 2c..), (row g+8, keys 2c..),
       // (row g, keys 2c+8..), (row g+8, keys 2c+8..)
       const uint32_t a0 = pf[kk][0], a1 = pf[kk][1], a2 = pf[kk][2], a3 = pf[kk][3];
@@ -281,19 +285,53 @@ __global__ void __launch_bounds__(128) score_attn_kernel(ScoreAttnArgs a) {
 #pragma unroll
       for (int j = 0; j < NT; j += 2) {
         uint32_t vb[4];
-        ldsm_x4_trans(vb, Vb + (size_t)(kk * 16 + (mi & 1) * 8 + rr) * RS + j * 8 + (mi >> 1) * 8);
+        ldsm_x4_trans(vb, Vb + (size_t)(kh * 32 + kk * 16 + (mi & 1) * 8 + rr) * RS + j * 8 +
+                              (mi >> 1) * 8);
         mma_bf16(o[j], a0, a1, a2, a3, vb[0], vb[1]);
         mma_bf16(o[j + 1], a0, a1, a2, a3, vb[2], vb[3]);
       }
     }
     __syncthreads();
   }
-  // row sums over the 4 lanes of a row, normalise, store
+  // row sums over the 4 lanes of a row
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
     lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
   }
+  // the second key half hands its state to the first (the K/V buffers are
+  // free: every warp passed the loop's last barrier)
+  constexpr int XS = NT * 4 + 4;                       // floats per lane
+  float* xch = reinterpret_cast<float*>(sm_raw) + (size_t)(rt * 32 + lane) * XS;
+  if (kh == 1) {
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) xch[j * 4 + e] = o[j][e];
+    xch[NT * 4 + 0] = mrow[0];
+    xch[NT * 4 + 1] = mrow[1];
+    xch[NT * 4 + 2] = lrow[0];
+    xch[NT * 4 + 3] = lrow[1];
+  }
+  __syncthreads();
+  if (kh == 1) return;
+  float w0[2], w1[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const float m1 = xch[NT * 4 + r];
+    const float mn = fmaxf(mrow[r], m1);
+    w0[r] = mrow[r] == -INFINITY ? 0.f : exp2f(mrow[r] - mn);
+    w1[r] = m1 == -INFINITY ? 0.f : exp2f(m1 - mn);
+    lrow[r] = lrow[r] * w0[r] + xch[NT * 4 + 2 + r] * w1[r];
+  }
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    o[j][0] = o[j][0] * w0[0] + xch[j * 4 + 0] * w1[0];
+    o[j][1] = o[j][1] * w0[0] + xch[j * 4 + 1] * w1[0];
+    o[j][2] = o[j][2] * w0[1] + xch[j * 4 + 2] * w1[1];
+    o[j][3] = o[j][3] * w0[1] + xch[j * 4 + 3] * w1[1];
+  }
+  // normalise, store
   const int ia = i0 + g, ib = i0 + g + 8;
   const float inva = 1.0f / lrow[0], invb = 1.0f / lrow[1];
   const int HD = a.H * DH;
@@ -349,7 +387,7 @@ size_t score_attn_smem(int dh) { return (size_t)4 * kSaKeys * (dh + 8) * sizeof(
 
 cudaError_t launch_score_attn(const ScoreAttnArgs& a, int n_active, cudaStream_t s) {
   if (n_active <= 0) return cudaSuccess;
-  const int nw = a.N >= 64 ? 4 : (a.N + 15) / 16;
+  const int nw = a.N >= 64 ? 4 : (a.N + 15) / 16;     // row tiles per CTA
   dim3 grid((a.N + nw * 16 - 1) / (nw * 16), a.H, n_active);
   const size_t smem = score_attn_smem(a.dh);
   static bool ready128[kDeviceSlots] = {}, ready64[kDeviceSlots] = {};
@@ -361,14 +399,14 @@ cudaError_t launch_score_attn(const ScoreAttnArgs& a, int n_active, cudaStream_t
                                (int)smem);
     if (e != cudaSuccess) return e;
     if (dv >= 0) ready128[dv] = true;
-    score_attn_kernel<128><<<grid, nw * 32, smem, s>>>(a);
+    score_attn_kernel<128><<<grid, nw * 64, smem, s>>>(a);
   } else if (a.dh == 64) {
     if (dv < 0 || !ready64[dv])
       e = cudaFuncSetAttribute(score_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem);
     if (e != cudaSuccess) return e;
     if (dv >= 0) ready64[dv] = true;
-    score_attn_kernel<64><<<grid, nw * 32, smem, s>>>(a);
+    score_attn_kernel<64><<<grid, nw * 64, smem, s>>>(a);
   } else {
     return cudaErrorInvalidValue;
   }

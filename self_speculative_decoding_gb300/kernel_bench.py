@@ -8,9 +8,13 @@ kernel: rows processed, algorithmic bytes per launch (the weights, plus the
 K/V read for attention), mean microseconds per launch and GB/s.
 
     python -m self_speculative_decoding_gb300.kernel_bench \
-        [--kernel qkv,o_proj,gate_up,down,lm_head,attention,gate_up_rows,...]
+        [--kernel qkv,o_proj,gate_up,down,lm_head,attention,gate_up_rows,...,score_attn]
         [--model 7b|13b|70b] \
         [--rows M] [--iters N] [--context L] [--lib path/to/libssd.so]
+
+``score_attn`` times the window attention of candidate-mask scoring for
+--rows / 32 candidates of 32 window positions over a shared prefix of
+--context positions.
 
 ``--lib`` times another build of the library (e.g. one compiled with a
 different ring geometry by build.build_variant).
@@ -137,6 +141,27 @@ def bench_kernel(lib, name: str, model: str, M: int, iters: int, context: int) -
                      W.data_ptr(), U.data_ptr() if U is not None else None, R, K, act.data_ptr(),
                      M, epi | 16, out.data_ptr(), None, st)
                  for W, U in zip(Ws, W1)]
+    elif name == "score_attn":
+        N = 32
+        nc = max(1, M // N)
+        split = context
+        max_seq = ((split + N + 63) // 64) * 64
+        n = _copies(2 * Hkv * max_seq * dh * 2)
+        kc = [(torch.randn(Hkv, max_seq, dh, device="cuda") * 0.5).to(torch.bfloat16)
+              for _ in range(n)]
+        vc = [(torch.randn(Hkv, max_seq, dh, device="cuda") * 0.5).to(torch.bfloat16)
+              for _ in range(n)]
+        q = (torch.randn(nc * N, H, dh, device="cuda") * 0.5).to(torch.bfloat16)
+        wk = (torch.randn(nc * N, Hkv, dh, device="cuda") * 0.5).to(torch.bfloat16)
+        wv = (torch.randn(nc * N, Hkv, dh, device="cuda") * 0.5).to(torch.bfloat16)
+        cand = torch.arange(nc, dtype=torch.int32, device="cuda")
+        out = torch.empty(nc * N, H * dh, dtype=torch.bfloat16, device="cuda")
+        nbytes = 2 * Hkv * split * dh * 2
+        flop = 4.0 * nc * N * H * (split + (N + 1) / 2) * dh
+        calls = [lambda k=k, v=v: lib.ssd_op_score_attention(
+                     q.data_ptr(), cand.data_ptr(), nc, N, split, k.data_ptr(), v.data_ptr(),
+                     max_seq, wk.data_ptr(), wv.data_ptr(), H, Hkv, dh, out.data_ptr(), st)
+                 for k, v in zip(kc, vc)]
     else:
         raise ValueError(f"unknown kernel {name}")
     for i in range(3):
@@ -152,7 +177,7 @@ def bench_kernel(lib, name: str, model: str, M: int, iters: int, context: int) -
     us = e0.elapsed_time(e1) * 1000.0 / iters
     r = {"kernel": name, "model": model, "rows": M, "bytes": nbytes, "us": round(us, 2),
          "GBps": round(nbytes / us / 1e3, 1)}
-    if name in ROW_KERNELS:
+    if name in ROW_KERNELS or name == "score_attn":
         r["TFLOPs"] = round(flop / us / 1e6, 1)
     return r
 
