@@ -81,9 +81,11 @@ typedef struct {
  * only (SSD_ERR_INVALID_ARG). */
 enum { SSD_DTYPE_BF16 = 0, SSD_DTYPE_FP32 = 1 };
 
-/* Device pointers of one decoder layer (borrowed).  Projection matrices
- * are given in the packed layout written by ssd_pack_weight; the shapes
- * below are those of the row-major matrices they were packed from. */
+/* Device pointers of one decoder layer (borrowed), each 16-byte aligned
+ * (ssd_create returns SSD_ERR_INVALID_ARG otherwise; the same holds for the
+ * pointers of ssd_weights).  Projection matrices are given in the packed
+ * layout written by ssd_pack_weight; the shapes below are those of the
+ * row-major matrices they were packed from. */
 typedef struct {
   const void* attn_norm; /* [D] fp32 RMSNorm gain                          */
   const void* wqkv;      /* packed [(H + 2 Hkv) dh, D] bf16: q, k, v rows  */

@@ -128,8 +128,13 @@ SSD_DI void mma_commit(uint64_t* bar) {
           smem_addr(bar))
       : "memory");
 }
-SSD_DI void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
+
+// Barrier of the four epilogue warps (threads 0 .. 127).
+SSD_DI void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// TMEM loads whose wait is issued separately, so that one wait covers
+// several loads; tmem_pin16 keeps the uses of a loaded array after the wait.
+SSD_DI void tmem_ld16_nw(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
       "%15}, [%16];"
@@ -137,13 +142,16 @@ SSD_DI void tmem_ld16(uint32_t taddr, float (&v)[16]) {
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
         "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
-
-// Barrier of the four epilogue warps (threads 0 .. 127).
-SSD_DI void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+SSD_DI void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+SSD_DI void tmem_pin16(uint32_t (&r)[16]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+}
 
 // float -> uint32 with the same order (argmax keys)
 SSD_DI uint32_t order_key(float v) {
@@ -396,15 +404,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       cp_async_wait_all();
       epi_sync();
     }
-    for (int c0 = p0; c0 < p0 + np; c0 += 16) {
-      float v[16];
-      tmem_ld16(trow + (uint32_t)c0, v);
-      for (int q = 1; q < nsum; ++q) {
-        float v1[16];
-        tmem_ld16(trow + (uint32_t)(q * NT + c0), v1);
+    // 16 columns at a time (32 for a single accumulator without SwiGLU): every
+    // TMEM load of the step is issued before one wait; a matrix's value is
+    // its issuers' accumulators added in issuer order
+    for (int cs = p0; cs < p0 + np;) {
+      const bool two = nsum == 1 && !swiglu && cs + 32 <= p0 + np;
+      float vv[2][16], upv[16];
+      {
+        uint32_t r0[16], r1[16], r2[16], r3[16];
+        tmem_ld16_nw(trow + (uint32_t)cs, r0);
+        if (two || nsum > 1) tmem_ld16_nw(trow + (uint32_t)((two ? 0 : NT) + cs + (two ? 16 : 0)), r1);
+        if (nsum > 2) tmem_ld16_nw(trow + (uint32_t)(2 * NT + cs), r2);
+        if (nsum > 3) tmem_ld16_nw(trow + (uint32_t)(3 * NT + cs), r3);
+        if (swiglu) tmem_ld16_nw(trow + (uint32_t)(per * NT + cs), r3);  // per == nsum == 1
+        tmem_wait_ld();
+        tmem_pin16(r0);
+        if (two || nsum > 1) tmem_pin16(r1);
+        if (nsum > 2) tmem_pin16(r2);
+        if (nsum > 3 || swiglu) tmem_pin16(r3);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] += v1[j];
+        for (int j = 0; j < 16; ++j) {
+          float x = __uint_as_float(r0[j]);
+          if (!two && nsum > 1) x += __uint_as_float(r1[j]);
+          if (nsum > 2) x += __uint_as_float(r2[j]);
+          if (nsum > 3) x += __uint_as_float(r3[j]);
+          vv[0][j] = x;
+          vv[1][j] = __uint_as_float(r1[j]);
+          upv[j] = __uint_as_float(r3[j]);
+        }
       }
+      for (int hh = 0; hh < (two ? 2 : 1); ++hh) {
+      const int c0 = cs + 16 * hh;
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = vv[hh][j];
       if (a.epi == GEMM_ARGMAX) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -422,22 +455,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                         (unsigned long long)(0xffffffffu - (uint32_t)bi));
         }
       } else if (swiglu) {
-        float up[16];
-        tmem_ld16(trow + (uint32_t)(per * NT + c0), up);
-        for (int q = 1; q < nsum; ++q) {
-          float v1[16];
-          tmem_ld16(trow + (uint32_t)((per + q) * NT + c0), v1);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) up[j] += v1[j];
-        }
+        const float* up = upv;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int tok = t0 + c0 + j;
           if (rv && tok < a.T) {
-            // silu with the fast exponential and division: the full-precision
-            // pair costs most of the epilogue, and the product is rounded to bf16
+            // silu; the scoring forward takes the fast exponential and division
+            // (the full-precision pair costs most of its epilogue, and the product
+            // is rounded to bf16), the prefill the full-precision pair
             const float gt = v[j];
-            const float sl = __fdividef(gt, 1.0f + __expf(-gt));
+            const float sl = a.fast_silu ? __fdividef(gt, 1.0f + __expf(-gt))
+                                         : gt / (1.0f + expf(-gt));
             a.u[a.u_packed ? packed_off(tok, row, a.R) : (size_t)tok * a.R + row] =
                 __float2bfloat16_rn(sl * up[j]);
           }
@@ -458,6 +486,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (tok < a.T) a.y[(size_t)tok * a.R + row] = v[j];
         }
       }
+      }
+      cs += two ? 32 : 16;
     }
   }
   tc_fence_before();

@@ -293,6 +293,7 @@ struct GemmArgs {
   const int32_t* rowmap = nullptr;     // nullable: identity; distinct rows
   bf16* u = nullptr;                   // GEMM_SWIGLU [T][R]: silu(gate) * up
   int u_packed = 0;                    // 1: u in the packed unit layout
+  int fast_silu = 0;                   // 1: SiLU with the fast exponential and division
   unsigned long long* best = nullptr;  // GEMM_ARGMAX [T]: atomic max of (value, -index) keys, zero before
   int* err = nullptr;                  // set non-zero if a bounded wait gave up (nullable)
 };

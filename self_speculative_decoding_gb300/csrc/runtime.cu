@@ -1092,6 +1092,7 @@ ssd_status enq_rows_layer(ssd_ctx* c, int l, int T, const int32_t* map, const in
   gu.err = &c->st->err;
   gu.u = c->sc_u;
   gu.u_packed = 1;
+  gu.fast_silu = kv_write ? 0 : 1;  // the prefill's cache keeps the full-precision SiLU
   if ((r = note(c, launch_gemm_rows(gu, s), "score_gate_up")) != SSD_OK) return r;
   GemmArgs dn;
   dn.W0 = (const bf16*)w.w_down;
@@ -1223,9 +1224,15 @@ ssd_status ssd_create(const ssd_config* cfg, const ssd_weights* w, void* stream,
       !(g.rope_theta > 0.f) || (g.dtype != SSD_DTYPE_BF16 && g.dtype != SSD_DTYPE_FP32) ||
       (g.dtype == SSD_DTYPE_FP32 && g.max_score_rows > 0))
     return SSD_ERR_INVALID_ARG;
+  // every weight is read with 16-byte vector loads and bulk copies
+  auto al16 = [](const void* p) { return ((uintptr_t)p & 15) == 0; };
+  if (!al16(w->tok_embed) || !al16(w->final_norm) || !al16(w->lm_head)) return SSD_ERR_INVALID_ARG;
   for (int l = 0; l < g.n_layers; ++l) {
     const ssd_layer_weights& L = w->layers[l];
     if (!L.attn_norm || !L.wqkv || !L.wo || !L.mlp_norm || !L.w_gate || !L.w_up || !L.w_down)
+      return SSD_ERR_INVALID_ARG;
+    if (!al16(L.attn_norm) || !al16(L.wqkv) || !al16(L.wo) || !al16(L.mlp_norm) ||
+        !al16(L.w_gate) || !al16(L.w_up) || !al16(L.w_down))
       return SSD_ERR_INVALID_ARG;
   }
   c = new ssd_ctx();

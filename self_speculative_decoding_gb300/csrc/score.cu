@@ -28,21 +28,36 @@ __global__ void score_embed_kernel(const bf16* embed, const int32_t* tokens, int
 }
 
 // out[t] = bf16(rmsnorm(x[map[t]]) * gain), written in the packed unit
-// layout the projections read.  One 256-thread block per row: thread i sums
-// the squares of the pairs (2i, 2i + 1), (2i + 512, 2i + 513), ... in that
-// order; the block reduces the 256 partial sums in a fixed tree (butterfly
-// within each warp, then warp 0 over the 8 warp sums).
+// layout the projections read.  One 256-thread block per row.  The row is
+// read once, in 8-element chunks held in registers (thread i takes chunks i,
+// i + 256, ...); each thread sums the squares of its chunks in that order,
+// the block reduces the 256 partial sums in a fixed tree (butterfly within
+// each warp, then warp 0 over the 8 warp sums), and every chunk is written
+// as one 16-byte piece of the packed layout.
+constexpr int kNormChunks = 4;  // chunks per thread: rows of up to 8192
 __global__ void __launch_bounds__(256) score_norm_kernel(const float* x, const int32_t* map,
                                                          const float* gain, float eps, int T,
                                                          int D, bf16* out) {
   __shared__ float wsum[8];
   const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float* xr = x + (size_t)(map ? map[t] : t) * D;
+  const int nc = D / 8;
+  float4 va[kNormChunks][2];
   float s = 0.f;
-  for (int k = 2 * tid; k < D; k += 512) {
-    const float2 v = *reinterpret_cast<const float2*>(xr + k);
-    s += v.x * v.x;
-    s += v.y * v.y;
+#pragma unroll
+  for (int i = 0; i < kNormChunks; ++i) {
+    const int ch = tid + i * 256;
+    if (ch < nc) {
+      va[i][0] = *reinterpret_cast<const float4*>(xr + 8 * ch);
+      va[i][1] = *reinterpret_cast<const float4*>(xr + 8 * ch + 4);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        s += va[i][h].x * va[i][h].x;
+        s += va[i][h].y * va[i][h].y;
+        s += va[i][h].z * va[i][h].z;
+        s += va[i][h].w * va[i][h].w;
+      }
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
@@ -56,22 +71,35 @@ __global__ void __launch_bounds__(256) score_norm_kernel(const float* x, const i
   }
   __syncthreads();
   const float rs = 1.0f / sqrtf(wsum[0] / (float)D + eps);
-  for (int k = 2 * tid; k < D; k += 512) {
-    const float2 v = *reinterpret_cast<const float2*>(xr + k);
-    *reinterpret_cast<uint32_t*>(out + packed_off(t, k, D)) =
-        pack_bf16x2(v.x * rs * gain[k], v.y * rs * gain[k + 1]);
+#pragma unroll
+  for (int i = 0; i < kNormChunks; ++i) {
+    const int ch = tid + i * 256;
+    if (ch < nc) {
+      const float4 g0 = *reinterpret_cast<const float4*>(gain + 8 * ch);
+      const float4 g1 = *reinterpret_cast<const float4*>(gain + 8 * ch + 4);
+      const float4 v0 = va[i][0], v1 = va[i][1];
+      uint4 o;
+      o.x = pack_bf16x2(v0.x * rs * g0.x, v0.y * rs * g0.y);
+      o.y = pack_bf16x2(v0.z * rs * g0.z, v0.w * rs * g0.w);
+      o.z = pack_bf16x2(v1.x * rs * g1.x, v1.y * rs * g1.y);
+      o.w = pack_bf16x2(v1.z * rs * g1.z, v1.w * rs * g1.w);
+      *reinterpret_cast<uint4*>(out + packed_off(t, 8 * ch, D)) = o;
+    }
   }
 }
 
 // RoPE (rotate-half pairs (j, j + dh/2)) of the compact rows' q and k at
 // position split + p % N (p = map[t], or t without a map); q -> q[t] bf16,
 // k and v -> the window cache row p and, when kc is given, also the layer's
-// cache [Hkv][max_seq][dh] at that position (the batched prefill).
+// cache [Hkv][max_seq][dh] at that position (the batched prefill).  A thread
+// takes four consecutive pairs of one head (16-byte loads, 8-byte stores) or
+// eight consecutive values of one v head.
 __global__ void score_rope_kernel(const float* qkv, int T, const int32_t* map, int N, int split,
                                   int H, int Hkv, int dh, const float2* rope, bf16* q, bf16* sk,
                                   bf16* sv, bf16* kc, bf16* vc, int max_seq) {
   const int half = dh / 2;
-  const int per_row = (H + Hkv) * half + Hkv * half;  // rotations + v pairs
+  const int nrot = (H + Hkv) * (half / 4);            // rotation items per row
+  const int per_row = nrot + Hkv * (dh / 8);           // + v items
   const int ld = (H + 2 * Hkv) * dh;
   const size_t n = (size_t)T * per_row;
   for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < n;
@@ -81,33 +109,42 @@ __global__ void score_rope_kernel(const float* qkv, int T, const int32_t* map, i
     const int p = map ? map[t] : t;
     const int pos = split + p % N;
     const float* row = qkv + (size_t)t * ld;
-    if (r < (H + Hkv) * half) {
-      const int hh = r / half, j = r % half;
+    if (r < nrot) {
+      const int hh = r / (half / 4), j = 4 * (r % (half / 4));
       const float* v = row + (size_t)hh * dh;
-      const float2 cs = rope[(size_t)pos * half + j];
-      const float a = v[j], b = v[j + half];
-      const float ra = a * cs.x - b * cs.y, rb = a * cs.y + b * cs.x;
-      if (hh < H) {
-        bf16* d = q + (size_t)t * H * dh + (size_t)hh * dh;
-        d[j] = __float2bfloat16_rn(ra);
-        d[j + half] = __float2bfloat16_rn(rb);
-      } else {
-        bf16* d = sk + ((size_t)p * Hkv + (hh - H)) * dh;
-        d[j] = __float2bfloat16_rn(ra);
-        d[j + half] = __float2bfloat16_rn(rb);
-        if (kc) {
-          bf16* e2 = kc + ((size_t)(hh - H) * max_seq + pos) * dh;
-          e2[j] = d[j];
-          e2[j + half] = d[j + half];
-        }
+      const float4 av = *reinterpret_cast<const float4*>(v + j);
+      const float4 bv = *reinterpret_cast<const float4*>(v + j + half);
+      const float4 c01 = *reinterpret_cast<const float4*>(rope + (size_t)pos * half + j);
+      const float4 c23 = *reinterpret_cast<const float4*>(rope + (size_t)pos * half + j + 2);
+      const float a[4] = {av.x, av.y, av.z, av.w}, b[4] = {bv.x, bv.y, bv.z, bv.w};
+      const float cx[4] = {c01.x, c01.z, c23.x, c23.z}, cy[4] = {c01.y, c01.w, c23.y, c23.w};
+      float ra[4], rb[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        ra[k] = a[k] * cx[k] - b[k] * cy[k];
+        rb[k] = a[k] * cy[k] + b[k] * cx[k];
+      }
+      const uint2 lo = make_uint2(pack_bf16x2(ra[0], ra[1]), pack_bf16x2(ra[2], ra[3]));
+      const uint2 hi = make_uint2(pack_bf16x2(rb[0], rb[1]), pack_bf16x2(rb[2], rb[3]));
+      bf16* d = hh < H ? q + (size_t)t * H * dh + (size_t)hh * dh
+                       : sk + ((size_t)p * Hkv + (hh - H)) * dh;
+      *reinterpret_cast<uint2*>(d + j) = lo;
+      *reinterpret_cast<uint2*>(d + j + half) = hi;
+      if (hh >= H && kc) {
+        bf16* e2 = kc + ((size_t)(hh - H) * max_seq + pos) * dh;
+        *reinterpret_cast<uint2*>(e2 + j) = lo;
+        *reinterpret_cast<uint2*>(e2 + j + half) = hi;
       }
     } else {
-      r -= (H + Hkv) * half;
-      const int kvh = r / half, j2 = 2 * (r % half);
-      const float* v = row + (size_t)(H + Hkv) * dh + (size_t)kvh * dh;
-      const uint32_t vv = pack_bf16x2(v[j2], v[j2 + 1]);
-      *reinterpret_cast<uint32_t*>(sv + ((size_t)p * Hkv + kvh) * dh + j2) = vv;
-      if (vc) *reinterpret_cast<uint32_t*>(vc + ((size_t)kvh * max_seq + pos) * dh + j2) = vv;
+      r -= nrot;
+      const int kvh = r / (dh / 8), j8 = 8 * (r % (dh / 8));
+      const float* v = row + (size_t)(H + Hkv) * dh + (size_t)kvh * dh + j8;
+      const float4 v0 = *reinterpret_cast<const float4*>(v);
+      const float4 v1 = *reinterpret_cast<const float4*>(v + 4);
+      const uint4 vv = make_uint4(pack_bf16x2(v0.x, v0.y), pack_bf16x2(v0.z, v0.w),
+                                  pack_bf16x2(v1.x, v1.y), pack_bf16x2(v1.z, v1.w));
+      *reinterpret_cast<uint4*>(sv + ((size_t)p * Hkv + kvh) * dh + j8) = vv;
+      if (vc) *reinterpret_cast<uint4*>(vc + ((size_t)kvh * max_seq + pos) * dh + j8) = vv;
     }
   }
 }
@@ -370,7 +407,7 @@ cudaError_t launch_score_embed(const bf16* embed, const int32_t* tokens, int spl
 
 cudaError_t launch_score_norm(const float* x, const int32_t* map, const float* gain, float eps,
                               int T, int D, bf16* out, cudaStream_t s) {
-  if (D % 64) return cudaErrorInvalidValue;
+  if (D % 64 || D > 8 * 256 * kNormChunks) return cudaErrorInvalidValue;
   score_norm_kernel<<<T, 256, 0, s>>>(x, map, gain, eps, T, D, out);
   return cudaGetLastError();
 }
@@ -378,6 +415,7 @@ cudaError_t launch_score_norm(const float* x, const int32_t* map, const float* g
 cudaError_t launch_score_rope(const float* qkv, int T, const int32_t* map, int N, int split, int H,
                               int Hkv, int dh, const float2* rope, bf16* q, bf16* sk, bf16* sv,
                               bf16* kc, bf16* vc, int max_seq, cudaStream_t s) {
+  if (dh % 8) return cudaErrorInvalidValue;
   score_rope_kernel<<<1216, 256, 0, s>>>(qkv, T, map, N, split, H, Hkv, dh, rope, q, sk, sv, kc, vc,
                                          max_seq);
   return cudaGetLastError();

@@ -59,6 +59,18 @@ def test_injected_allocation_failure(ssd, n):
     ctx.close()
 
 
+def test_misaligned_weight_refused(ssd):
+    # every weight pointer must be 16-byte aligned (vector loads, bulk copies)
+    from self_speculative_decoding_gb300 import SSDError
+    wts = to_device_weights(make_weights(TINY, dtype="bf16"))
+    g = wts["layers"][1]["mlp_norm"]
+    buf = torch.zeros(g.numel() + 4, dtype=torch.float32, device="cuda")
+    buf[1:1 + g.numel()] = g
+    wts["layers"][1]["mlp_norm"] = buf[1:1 + g.numel()]          # 4 bytes off
+    with pytest.raises(SSDError, match="INVALID_ARG"):
+        ssd.SSDContext(TINY.shape, wts, max_seq=128)
+
+
 def test_pass_timing_statistics(ssd):
     wts = to_device_weights(make_weights(TINY, dtype="bf16", lm_head_scale=10.0))
     ctx = ssd.SSDContext(TINY.shape, wts, max_seq=128)
