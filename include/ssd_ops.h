@@ -136,12 +136,12 @@ ssd_status ssd_op_linear_rows(const void* W, const void* W1, int32_t R, int32_t 
  *   out[ja N + i][h dh ..] = bf16(softmax(q K^T / sqrt(dh)) V)
  * over the keys of the shared cache k_cache / v_cache ([Hkv][max_seq][dh]
  * bf16) at positions 0..split-1, then candidate k's own window keys
- * wk / wv (bf16 [rows][Hkv][dh], row k N + w) for w <= i.  split >= 1,
- * split <= max_seq; dh 64 or 128. */
+ * wk / wv (bf16 [w_rows][Hkv][dh], row k N + w) for w <= i; every k in cand
+ * has k N + N <= w_rows.  split >= 1, split <= max_seq; dh 64 or 128. */
 ssd_status ssd_op_score_attention(const void* q, const int32_t* cand, int32_t n_cand, int32_t N,
                                   int32_t split, const void* k_cache, const void* v_cache,
-                                  int32_t max_seq, const void* wk, const void* wv, int32_t H,
-                                  int32_t Hkv, int32_t dh, void* out, void* stream);
+                                  int32_t max_seq, const void* wk, const void* wv, int32_t w_rows,
+                                  int32_t H, int32_t Hkv, int32_t dh, void* out, void* stream);
 
 /* Description of the most recent failed op call on this host thread. */
 const char* ssd_ops_last_error(void);

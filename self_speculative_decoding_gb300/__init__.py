@@ -415,7 +415,8 @@ class _Ops:
         out = torch.empty(nc * N, H * dh, dtype=torch.bfloat16, device=q.device)
         self._check(_lib().ssd_op_score_attention(_ptr(q), _ptr(cand), nc, N, split,
                                                   _ptr(k_cache), _ptr(v_cache), k_cache.shape[1],
-                                                  _ptr(wk), _ptr(wv), H, Hkv, dh, _ptr(out),
+                                                  _ptr(wk), _ptr(wv), wk.shape[0], H, Hkv, dh,
+                                                  _ptr(out),
                                                   stream_handle()))
         return out
 

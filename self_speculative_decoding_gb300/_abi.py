@@ -131,7 +131,7 @@ _SIGS = {
     "ssd_op_linear_noalloc": [_P, _I, _I, _P, _I, _P, _P],
     "ssd_op_wait_selftest": [_I, C.POINTER(C.c_int32), _P],
     "ssd_op_linear_rows": [_P, _P, _I, _I, _P, _I, _I, _P, _P, _P],
-    "ssd_op_score_attention": [_P, _P, _I, _I, _I, _P, _P, _I, _P, _P, _I, _I, _I, _P, _P],
+    "ssd_op_score_attention": [_P, _P, _I, _I, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P],
     "ssd_op_linear_noalloc_last_error": [],
 }
 

@@ -49,10 +49,32 @@
 #include <cuda.h>
 
 #include "kernels.cuh"
+#include "tc_dev.cuh"
 
 namespace ssd {
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no
+// link-time dependency on the driver library); null if unavailable.
+EncodeTiled tma_encoder() {
+  static EncodeTiled fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
 namespace {
+
+using namespace tc;
 
 constexpr int kTcM = 128;          // outputs per tile
 constexpr int kTcGroups = 8;       // 16-row groups per tile
@@ -72,86 +94,8 @@ constexpr int kTcSmemBudget1 = SSD_TC_SMEM_KB * 1024;
 constexpr int kTcSmemBudget2 = 108 * 1024;
 constexpr int kWaitPolls = 1 << 24;
 
-// Tiled TMA load of a 3-D box at (c0, c1, c2), completing on `bar`.
-SSD_DI void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
-      : "memory");
-}
-
-// ---- tcgen05 helpers
-SSD_DI void tmem_alloc(uint32_t* slot, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   smem_addr(slot)),
-               "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-SSD_DI void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-SSD_DI void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-SSD_DI void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Shared-memory matrix descriptor: K-major, 64-byte swizzle, 8-row atoms of
-// 512 bytes stacked densely along M/N (stride 512 bytes).
-SSD_DI uint64_t sw64_desc(uint32_t saddr) {
-  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
-  d |= (uint64_t)1 << 16;                             // leading offset (unused here)
-  d |= (uint64_t)(512 >> 4) << 32;                    // stride offset
-  d |= (uint64_t)1 << 46;                             // descriptor version
-  d |= (uint64_t)4 << 61;                             // 64-byte swizzle
-  return d;
-}
-
-// Instruction descriptor of kind::f16: bf16 A and B, fp32 D, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
-}
-
-SSD_DI void mma_bf16_tc(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                        uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-SSD_DI void mma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_addr(bar))
-      : "memory");
-}
-
 // Barrier of the four epilogue warps (threads 0 .. 127).
 SSD_DI void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-// TMEM loads whose wait is issued separately, so that one wait covers
-// several loads; tmem_pin16 keeps the uses of a loaded array after the wait.
-SSD_DI void tmem_ld16_nw(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-      "%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
-SSD_DI void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-SSD_DI void tmem_pin16(uint32_t (&r)[16]) {
-  asm volatile(""
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
-                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
-               :
-               : "memory");
-}
 
 // float -> uint32 with the same order (argmax keys)
 SSD_DI uint32_t order_key(float v) {
@@ -516,34 +460,12 @@ __global__ void pack_act_kernel(const bf16* src, int T, int K, bf16* dst) {
 
 // ---- host: tensor maps over the packed layout
 
-using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiled encoder() {
-  static EncodeTiled fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiled>(p);
-    else
-      cudaGetLastError();
-  }
-  return fn;
-}
-
 // A packed [groups * 16][K] bf16 matrix seen as (128 8-byte elements of a
 // 1 KB unit, groups, K / 32 K blocks); boxes of (128, box_groups, box_kb):
 // box_kb K blocks of box_groups row groups, landing K block by K block as
 // consecutive 1 KB units.
 bool packed_map(CUtensorMap* m, const void* base, int K, int groups, int box_groups, int box_kb) {
-  EncodeTiled enc = encoder();
+  EncodeTiled enc = tma_encoder();
   if (!enc) return false;
   const cuuint64_t dims[3] = {128, (cuuint64_t)groups, (cuuint64_t)(K / 32)};
   const cuuint64_t strides[2] = {(cuuint64_t)(K / 32) * 1024, 1024};

@@ -313,8 +313,13 @@ struct ScoreAttnArgs {
   float scale_log2 = 0.f;     // log2(e) / sqrt(dh)
   bf16* out = nullptr;        // [T][H dh]
   int out_packed = 0;         // 1: out in the packed unit layout (packed_off)
+  int w_rows = 0;             // rows of sk / sv
+  int* err = nullptr;         // set non-zero if a bounded wait gave up (nullable)
 };
 cudaError_t launch_score_attn(const ScoreAttnArgs& a, int n_active, cudaStream_t s);
+// the tensor-core form (dh 128, N a multiple of 8 up to 128)
+bool score_attn_tc_ok(const ScoreAttnArgs& a);
+cudaError_t launch_score_attn_tc(const ScoreAttnArgs& a, int n_active, cudaStream_t s);
 size_t score_attn_smem(int dh);
 cudaError_t launch_score_embed(const bf16* embed, const int32_t* tokens, int split, int N, int rows,
                                int D, float* x, cudaStream_t s);

@@ -372,9 +372,9 @@ ssd_status ssd_op_linear_rows(const void* W, const void* W1, int32_t R, int32_t 
 
 ssd_status ssd_op_score_attention(const void* q, const int32_t* cand, int32_t n_cand, int32_t N,
                                   int32_t split, const void* k_cache, const void* v_cache,
-                                  int32_t max_seq, const void* wk, const void* wv, int32_t H,
-                                  int32_t Hkv, int32_t dh, void* out, void* stream) {
-  if (!al16(q) || !cand || n_cand < 1 || N < 1 || split < 1 || split > max_seq ||
+                                  int32_t max_seq, const void* wk, const void* wv, int32_t w_rows,
+                                  int32_t H, int32_t Hkv, int32_t dh, void* out, void* stream) {
+  if (!al16(q) || !cand || n_cand < 1 || N < 1 || split < 1 || split > max_seq || w_rows < N ||
       !al16(k_cache) || !al16(v_cache) || !al16(wk) || !al16(wv) || !al16(out) || H < 1 ||
       Hkv < 1 || H % Hkv || (dh != 64 && dh != 128))
     return op_fail(SSD_ERR_INVALID_ARG, "score_attention arguments");
@@ -393,6 +393,7 @@ ssd_status ssd_op_score_attention(const void* q, const int32_t* cand, int32_t n_
   a.dh = dh;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)dh));
   a.out = (bf16*)out;
+  a.w_rows = w_rows;
   return cu(launch_score_attn(a, n_cand, (cudaStream_t)stream), "score_attention");
 }
 

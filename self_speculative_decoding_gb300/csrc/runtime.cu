@@ -1065,6 +1065,8 @@ ssd_status enq_rows_layer(ssd_ctx* c, int l, int T, const int32_t* map, const in
   at.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)g.head_dim));
   at.out = c->sc_attn;
   at.out_packed = 1;
+  at.w_rows = std::max(g.max_score_rows, c->pf_chunk);  // rows of sc_sk / sc_sv
+  at.err = &c->st->err;
   if ((r = note(c, launch_score_attn(at, n_active, s), "score_attn")) != SSD_OK) return r;
   GemmArgs o;
   o.W0 = (const bf16*)w.wo;

@@ -160,7 +160,7 @@ def bench_kernel(lib, name: str, model: str, M: int, iters: int, context: int) -
         flop = 4.0 * nc * N * H * (split + (N + 1) / 2) * dh
         calls = [lambda k=k, v=v: lib.ssd_op_score_attention(
                      q.data_ptr(), cand.data_ptr(), nc, N, split, k.data_ptr(), v.data_ptr(),
-                     max_seq, wk.data_ptr(), wv.data_ptr(), H, Hkv, dh, out.data_ptr(), st)
+                     max_seq, wk.data_ptr(), wv.data_ptr(), nc * N, H, Hkv, dh, out.data_ptr(), st)
                  for k, v in zip(kc, vc)]
     else:
         raise ValueError(f"unknown kernel {name}")

@@ -9,7 +9,9 @@ through the C-ABI (ssd_op_linear_rows, ssd_op_score_attention).
 * A row's result does not depend on how many rows are processed together
   (bit for bit), across token-tile widths from 16 to 256 columns.
 * The window attention equals oracle.ops.score_attention within bf16
-  rounding of its operands (P and the output are bf16).
+  rounding of its operands (P and the output are bf16), on both forms: the
+  tensor-core one (dh 128, windows of a multiple of 8 rows) and the
+  mma.sync one (the other shapes).
 """
 
 import numpy as np
@@ -114,6 +116,13 @@ def test_rows_count_invariance(ops, R, K):
     (2, 2, 128, 33, 70, [1]),
     (8, 1, 64, 70, 130, [3, 0, 2]),
     (4, 4, 128, 32, 2040, [0, 1, 2, 3]),
+    # tensor-core form (dh 128, N a multiple of 8): several candidate groups,
+    # candidates out of order, a partial last prefix block, a prefix shorter
+    # than one block, GQA
+    (8, 8, 128, 32, 300, [5, 1, 3, 0, 2, 7, 9, 8, 4]),
+    (4, 2, 128, 16, 100, [2, 0, 3, 1, 4, 5, 7, 6, 8, 9, 10, 11, 12, 13, 14, 15]),
+    (8, 2, 128, 64, 129, [1, 0, 2, 3]),
+    (4, 1, 128, 8, 1, list(range(31, -1, -1))),
 ])
 def test_score_attention(ops, H, Hkv, dh, N, split, cand):
     from oracle import ops as O
