@@ -426,12 +426,17 @@ size_t score_attn_smem(int dh) { return (size_t)4 * kSaKeys * (dh + 8) * sizeof(
 cudaError_t launch_score_attn(const ScoreAttnArgs& a, int n_active, cudaStream_t s) {
   if (n_active <= 0) return cudaSuccess;
   // The tensor-core form runs one CTA per 128 query rows and head through all
-  // key blocks in turn (about 70 us at 2048 cached positions whatever the
-  // rows, 13B heads); the mma.sync form one CTA per candidate and head, whose
-  // time grows with the candidates (48 us up to 3 of 32 rows, 84 us at 9,
-  // 120 us at 12).  The tensor-core form takes passes of 256 rows or more.
+  // key blocks in turn (47-52 us at 2048 cached positions up to 12
+  // candidates of 32 rows, 13B heads); the mma.sync form one CTA per
+  // candidate and head, whose time grows with the candidates (48 us up to 3,
+  // 60 us at 4-7, 84 us at 9, 120 us at 12).  The tensor-core form takes
+  // passes of 128 rows or more.
+#ifndef SSD_SCORE_ATTN_TC_MIN_ROWS
+#define SSD_SCORE_ATTN_TC_MIN_ROWS 128
+#endif
 #ifndef SSD_SCORE_ATTN_MMA_SYNC
-  if (score_attn_tc_ok(a) && n_active * a.N >= 256) return launch_score_attn_tc(a, n_active, s);
+  if (score_attn_tc_ok(a) && n_active * a.N >= SSD_SCORE_ATTN_TC_MIN_ROWS)
+    return launch_score_attn_tc(a, n_active, s);
 #endif
   const int nw = a.N >= 64 ? 4 : (a.N + 15) / 16;     // row tiles per CTA
   dim3 grid((a.N + nw * 16 - 1) / (nw * 16), a.H, n_active);

@@ -13,13 +13,14 @@
 //   online softmax       eight warps, two threads per query row (TMEM lane),
 //                        each over 64 of the block's keys: mask, row max
 //                        (the pair's maxima exchanged in shared memory),
-//                        exp2 and a partial sum in key order (base 2);
+//                        2^x on the special-function unit, partial sums
+//                        added in a fixed order (base 2);
 //   O *= exp2(m - m')    in tensor memory, each thread of the pair over half
 //                        of O's columns, and only in warps where some row's
 //                        maximum grew (the factor is otherwise exactly 1);
 //   P, V^T               bf16 into shared memory in the K-major 128-byte
-//                        swizzle layout the MMA reads (V transposed with
-//                        ldmatrix.trans);
+//                        swizzle layout the MMA reads (V transposed by
+//                        ldmatrix and stmatrix.trans);
 //   O += P V             tcgen05 (M = 128, N = dh, K = 128 keys).
 // Warp 8 issues the TMA copies (Q once; K and V blocks in a 2-stage ring,
 // 128-byte swizzle, cache rows at or beyond split zero-filled; a stage is
@@ -57,27 +58,29 @@ SSD_DI uint32_t sw128_off(int row, int col) {
                     (col & 7) * 2);
 }
 
-SSD_DI void ldsm_x4_t(uint32_t (&r)[4], uint32_t saddr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+// Four 8x8 b16 tiles: lanes 8t .. 8t + 7 give the row addresses of tile t.
+SSD_DI void ldsm_x4(uint32_t (&r)[4], uint32_t saddr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(saddr));
 }
+// The same four tiles stored transposed (row addresses of the destination).
+SSD_DI void stsm_x4_t(uint32_t saddr, const uint32_t (&r)[4]) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(saddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+               : "memory");
+}
 
 SSD_DI bool flagged(const int* f) { return *reinterpret_cast<const volatile int*>(f) != 0; }
-// Barrier of the eight softmax warps, and the same barrier returning whether
-// v holds in all 256 threads: every decision to give up is taken by all of
-// them at once, so that none is left waiting at a barrier the others skip.
-SSD_DI void soft_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-SSD_DI bool soft_all(bool v) {
-  uint32_t out;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(out)
-      : "r"((uint32_t)v)
-      : "memory");
-  return out != 0;
+// 2^x by the special-function unit (ex2.approx: relative error about 2^-22;
+// the probabilities are rounded to bf16 before the PV MMA).
+SSD_DI float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
+// Barrier of the eight softmax warps.
+SSD_DI void soft_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kAtThreads, 1)
     score_attn_tc_kernel(const __grid_constant__ CUtensorMap mQ,
@@ -218,7 +221,10 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       mbar_wait_n(mdone, 0u, kAtPolls);
     }
   } else {
-    // ---- softmax, rescale, P and V^T, epilogue: query row r, key half hh
+    // ---- softmax, rescale, P and V^T, epilogue: query row r, key half hh.
+    // Every block runs the same sequence of barriers in all 256 threads; a
+    // wait that gives up (or a CTA already flagged) only skips the work that
+    // needed it, so no thread is ever left at a barrier the others skip.
     const int r = tid & 127, hh = tid >> 7;
     const int c = r / N, i = r - c * N;
     const bool rvalid = c < ncand;
@@ -226,29 +232,41 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     float* xch = reinterpret_cast<float*>(sm + kOffX);  // [2][128]
     const float scale = a.scale_log2;
     float m = -INFINITY, l = 0.f;                      // l: this thread's half of the sum
-    bool ok = true;
-    for (int j = 0; j < nb && ok; ++j) {
+    // bounded wait, warp-uniform result, nothing waited for once flagged
+    auto wait_w = [&](uint64_t* bar, uint32_t parity) -> bool {
+      bool okw = !flagged(fail) && mbar_wait_n(bar, parity, kAtPolls);
+      okw = __all_sync(0xffffffffu, okw);
+      if (!okw && lane == 0) atomicExch(fail, 1);
+      return okw;
+    };
+    for (int j = 0; j < nb; ++j) {
       const int st = j & 1;
       const uint32_t par = (uint32_t)((j >> 1) & 1);
-      ok = soft_all(mbar_wait_n(&sfull[st], par, kAtPolls) && !flagged(fail));
-      if (!ok) break;
-      tc_fence_after();
       uint32_t sr[2][32];
+      if (wait_w(&sfull[st], par)) {
+        tc_fence_after();
 #pragma unroll
-      for (int q = 0; q < 2; ++q)
-        tmem_ld32_nw(trow + (uint32_t)(st * 128 + hh * 64 + q * 32), sr[q]);
-      tmem_wait_ld();
+        for (int q = 0; q < 2; ++q)
+          tmem_ld32_nw(trow + (uint32_t)(st * 128 + hh * 64 + q * 32), sr[q]);
+        tmem_wait_ld();
 #pragma unroll
-      for (int q = 0; q < 2; ++q) tmem_pin32(sr[q]);
-      // scale; mask (partial prefix block, window block); this half's max
+        for (int q = 0; q < 2; ++q) tmem_pin32(sr[q]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) sr[q][e] = 0u;
+      }
+      // mask (partial prefix block, window block: masked scores -inf); this
+      // half's maximum in four independent chains
       const int kb = j * kAtKeys + hh * 64;             // first key of this half
       const bool full_pre = j < nbp && kb + 64 <= a.split;
-      float bm = -INFINITY;
+      float bmx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int q = 0; q < 2; ++q)
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          float v = __uint_as_float(sr[q][e]) * scale;
+          float v = __uint_as_float(sr[q][e]);
           if (!full_pre) {
             const int k = hh * 64 + q * 32 + e;
             bool valid;
@@ -261,34 +279,36 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             if (!valid) v = -INFINITY;
           }
           sr[q][e] = __float_as_uint(v);
-          bm = fmaxf(bm, v);
+          bmx[e & 3] = fmaxf(bmx[e & 3], v);
         }
-      // the row's block maximum over both halves
+      float bm = fmaxf(fmaxf(bmx[0], bmx[1]), fmaxf(bmx[2], bmx[3])) * scale;
+      // the row's block maximum over both halves (scaled, base 2)
       xch[hh * 128 + r] = bm;
       soft_sync();
       bm = fmaxf(bm, xch[(hh ^ 1) * 128 + r]);
       soft_sync();  // the exchange slots are free for the next block
       const float mn = fmaxf(m, bm);
-      const float corr = (m == -INFINITY || mn == -INFINITY) ? 1.f : exp2f(m - mn);
-      float ls = 0.f;
+      const float corr = (m == -INFINITY || mn == -INFINITY) ? 1.f : ex2(m - mn);
+      // p = 2^(s scale - m'), masked keys 0; four partial sums, added in a
+      // fixed order
+      const float nmn = mn == -INFINITY ? 0.f : -mn;
+      float lsx[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[2][16];
 #pragma unroll
       for (int q = 0; q < 2; ++q)
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const float s0 = __uint_as_float(sr[q][e]), s1 = __uint_as_float(sr[q][e + 1]);
-          const float p0 = mn == -INFINITY ? 0.f : exp2f(s0 - mn);
-          const float p1 = mn == -INFINITY ? 0.f : exp2f(s1 - mn);
-          ls += p0;
-          ls += p1;
+          const float p0 = ex2(fmaf(s0, scale, nmn));
+          const float p1 = ex2(fmaf(s1, scale, nmn));
+          lsx[(e >> 1) & 3] += p0 + p1;
           pk[q][e >> 1] = pack_bf16x2(p0, p1);
         }
+      const float ls = (lsx[0] + lsx[1]) + (lsx[2] + lsx[3]);
       l = l * corr + ls;
       m = mn;
       // the previous block's PV has completed: O, P and V^T may be touched
-      if (j > 0) {
-        ok = soft_all(mbar_wait_n(pvdone, (uint32_t)((j - 1) & 1), kAtPolls) && !flagged(fail));
-        if (!ok) break;
+      if (j > 0 && wait_w(pvdone, (uint32_t)((j - 1) & 1))) {
         tc_fence_after();
         if (__any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll
@@ -312,36 +332,28 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                                    pk[q8 >> 2][(q8 & 3) * 4 + 2], pk[q8 >> 2][(q8 & 3) * 4 + 3]);
         *reinterpret_cast<uint4*>(sm + kOffP + hh * kAtRegion + sw128_off(r, q8 * 8)) = v;
       }
-      // V^T: warp w takes dh rows 16w .. 16w + 15 of the block's V, two key
-      // tiles per ldmatrix
-      ok = soft_all(mbar_wait_n(&full[st], par, kAtPolls) && !flagged(fail));
-      if (!ok) break;
-      {
+      // V^T: warp w takes dh rows 16w .. 16w + 15 of the block's V: 8x8 tiles
+      // read with ldmatrix (rows = keys) and written back transposed with
+      // stmatrix.trans (rows = dh)
+      if (wait_w(&full[st], par)) {
         const unsigned char* Vb = sm + kOffV + st * 2 * kAtRegion;
-        const int tq = lane >> 3;                     // tile of this lane's row address
-        const int d0 = warp * 16 + (tq & 1) * 8;
-        const int tr = lane >> 2, tc2 = 2 * (lane & 3);
+        const int tq = lane >> 3, tr8 = lane & 7;      // tile of this lane's row address
+        const int d0 = warp * 16 + (tq & 1) * 8;        // dh of the tile
 #pragma unroll 4
         for (int kt = 0; kt < 16; kt += 2) {
-          const int kk = (kt + (tq >> 1)) * 8 + (lane & 7);
+          const int k0 = (kt + (tq >> 1)) * 8;          // keys of the tile
           uint32_t t4[4];
-          ldsm_x4_t(t4, smem_addr(Vb + (d0 >> 6) * kAtRegion + sw128_off(kk, d0 & 63)));
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int d = warp * 16 + (q & 1) * 8 + tr, k = (kt + (q >> 1)) * 8 + tc2;
-            *reinterpret_cast<uint32_t*>(sm + kOffVt + (k >> 6) * kAtRegion +
-                                         sw128_off(d, k & 63)) = t4[q];
-          }
+          ldsm_x4(t4, smem_addr(Vb + (d0 >> 6) * kAtRegion + sw128_off(k0 + tr8, d0 & 63)));
+          stsm_x4_t(smem_addr(sm + kOffVt + (k0 >> 6) * kAtRegion + sw128_off(d0 + tr8, k0 & 63)), t4);
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive_cta(pready);
     }
-    if (!ok) atomicExch(fail, 1);
     // epilogue: O / l (the two halves' sums added), bf16; each thread of the
     // pair writes half of the row's columns
-    ok = soft_all(ok && mbar_wait_n(pvdone, (uint32_t)((nb - 1) & 1), kAtPolls) && !flagged(fail));
+    const bool ok = wait_w(pvdone, (uint32_t)((nb - 1) & 1));
     xch[hh * 128 + r] = l;
     soft_sync();
     const float lt = hh == 0 ? l + xch[128 + r] : xch[r] + l;
