@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(LinearArgs a
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kSlots; ++s) {
+    for (int s = 0; s < kSlots + kStageBytes / kSlotBytes; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], kConsumers);
     }
@@ -57,6 +57,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(LinearArgs a
   }
   __syncthreads();
   RingPos rp;
+  rp.nslots = ring_slots(a, kouter_order<IN, EPI>(a, p));
   if (warp == kProducer) {
     // weights do not depend on the preceding kernel: no wait before streaming
     producer_phase<IN, EPI>(a, p, sm, b, lane, rp);
@@ -68,6 +69,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(LinearArgs a
   if (!SSD_CHECK_W(b == 0 && warp == 0 && lane == 0 ? a.err : nullptr, a.err_val,
                    M >= 1 && M <= kMaxRows, DBG_ROWS, M))
     M = M < 1 ? 1 : kMaxRows;
+  // the staged rows must stay clear of the ring slots borrowed from the stage
+  if (rp.nslots > kSlots) {
+    const int room = (kStageBytes - (rp.nslots - kSlots) * kSlotBytes) / ((a.K + kPad) * (int)sizeof(bf16));
+    if (M > room) {
+      if (b == 0 && warp == 0 && lane == 0) atomicExch(a.err, 10);
+      M = room;
+    }
+  }
   if (warp == kEpilogue) {
     LmRec run = lm_empty();
     epilogue_phase<IN, EPI>(a, p, sm, b, M, lane, rp, run);

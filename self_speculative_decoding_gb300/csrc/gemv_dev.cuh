@@ -447,8 +447,8 @@ struct __align__(16) GemvSmem {
   float red[2][kConsumers][16][16];  // per-warp partials, double-buffered per row group
   float ep[2][16][17];               // epilogue operands
   float rstd[kMaxRows];
-  uint64_t full[kSlots];             // slot filled by the bulk copy
-  uint64_t empty[kSlots];            // slot consumed by all consumer warps
+  uint64_t full[kSlots + kStageBytes / kSlotBytes];   // slot filled by the bulk copy
+  uint64_t empty[kSlots + kStageBytes / kSlotBytes];  // slot consumed by all consumer warps
   uint64_t rfull[2];                 // partial buffer written by all consumer warps
   uint64_t rempty[2];                // partial buffer read by the epilogue warp
   uint64_t foldbar;                  // LM head: the epilogue warp knows whether this CTA folds
@@ -469,12 +469,30 @@ static_assert(kFoldInRing + kFoldInStage + (int)(sizeof(float) * 2 * kConsumers 
 // Position of a warp role in the slot ring and in the partial hand-off
 // sequence; persists across the GEMV phases of one kernel.
 struct RingPos {
+  int nslots = kSlots;  // ring depth of this launch (ring_slots)
   int slot = 0;
   uint32_t ph = 0;   // parity of the current ring pass
   int t = 0;         // chunks issued so far (producer)
   int fl = 0;        // row-group segments handed over so far
   bool ok = true;
 };
+
+// Slots of the ring: kSlots in the ring proper, then slots borrowed from the
+// end of the activation stage when the most rows of the launch leave it free
+// (one-row passes stage 8 KB of their 44 KB at K = 4096): more weight bytes
+// in flight per CTA.  Never while the stage holds the K-outer windows.
+SSD_HD int ring_slots(const LinearArgs& a, bool kouter) {
+  if (kouter) return kSlots;
+  const int mm = a.m_max > 0 ? a.m_max : (a.M_dev ? kMaxRows : a.M_static);
+  const long need = (long)mm * (a.K + kPad) * (long)sizeof(bf16);
+  if (need > kStageBytes) return kSlots;
+  return kSlots + (int)((kStageBytes - need) / kSlotBytes);
+}
+SSD_DI unsigned char* slot_ptr(GemvSmem& sm, int slot) {
+  return slot < kSlots ? sm.ring + slot * kSlotBytes
+                       : reinterpret_cast<unsigned char*>(sm.stage) + kStageBytes -
+                             (slot - kSlots + 1) * kSlotBytes;
+}
 
 // Length of the next chunk: at most kChunk units, never crossing a row group.
 SSD_DI int chunk_len(const Part& p, int kb, int left) {
@@ -531,7 +549,7 @@ SSD_DI void consume(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0, in
     for (int i = 0; i < kUPW; ++i) {
       const int un = warp + i * kConsumers;
       if (un < n) {
-        const unsigned char* base = sm.ring + slot * kSlotBytes + un * kUnitBytes;
+        const unsigned char* base = slot_ptr(sm, slot) + un * kUnitBytes;
         const uint4 wa = *reinterpret_cast<const uint4*>(base + unit_slot(lane));
         const uint4 wb = *reinterpret_cast<const uint4*>(base + 512 + unit_slot(lane));
         const int off = (kb + un) * 32 + 8 * c;
@@ -551,7 +569,7 @@ SSD_DI void consume(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0, in
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[slot]);
-    if (++slot == kSlots) { slot = 0; ph ^= 1u; }
+    if (++slot == rp.nslots) { slot = 0; ph ^= 1u; }
     const bool group_done = kb2 == 0 || left2 == 0;
     vr = vr2;
     kb = kb2;
@@ -793,7 +811,7 @@ SSD_DI void consume_win(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0
           for (int i = 0; i < kUPW; ++i) {
             const int un = warp + i * kConsumers;
             if (un < n) {
-              const unsigned char* base = sm.ring + slot * kSlotBytes + un * kUnitBytes;
+              const unsigned char* base = slot_ptr(sm, slot) + un * kUnitBytes;
               const uint4 wa = *reinterpret_cast<const uint4*>(base + unit_slot(lane));
               const uint4 wbv = *reinterpret_cast<const uint4*>(base + 512 + unit_slot(lane));
               const int col = ((kb - kb0) + un) * 64 + c * 16;  // bytes into the row
@@ -811,7 +829,7 @@ SSD_DI void consume_win(const LinearArgs& a, const Part& p, GemvSmem& sm, int U0
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.empty[slot]);
-          if (++slot == kSlots) { slot = 0; ph ^= 1u; }
+          if (++slot == rp.nslots) { slot = 0; ph ^= 1u; }
         }
       }
     }
@@ -887,15 +905,15 @@ SSD_DI void producer_phase(const LinearArgs& a, const Part& p, GemvSmem& sm, int
   const int U0 = unit_begin(p, b), U1 = unit_begin(p, b + 1);
   auto put = [&](int vr, int kb, int n) {
     if (!rp.ok) return;
-    if (rp.t >= kSlots && !mbar_wait(&sm.empty[rp.slot], rp.ph ^ 1u)) {
+    if (rp.t >= rp.nslots && !mbar_wait(&sm.empty[rp.slot], rp.ph ^ 1u)) {
       atomicExch(a.err, 2);
       rp.ok = false;
       return;
     }
     mbar_arrive_expect_tx(&sm.full[rp.slot], (uint32_t)(n * kUnitBytes));
-    bulk_g2s(sm.ring + rp.slot * kSlotBytes, unit_src<EPI>(a, p, vr, kb),
-             (uint32_t)(n * kUnitBytes), &sm.full[rp.slot]);
-    if (++rp.slot == kSlots) { rp.slot = 0; rp.ph ^= 1u; }
+    bulk_g2s(slot_ptr(sm, rp.slot), unit_src<EPI>(a, p, vr, kb), (uint32_t)(n * kUnitBytes),
+             &sm.full[rp.slot]);
+    if (++rp.slot == rp.nslots) { rp.slot = 0; rp.ph ^= 1u; }
     ++rp.t;
   };
   if (kouter_order<IN, EPI>(a, p)) {

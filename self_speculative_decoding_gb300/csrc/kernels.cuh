@@ -19,6 +19,7 @@ struct LinearArgs {
   const float* ss = nullptr;  // IN_NORM: sum-of-squares partials [M][K/16]
   const float* gain = nullptr;
   float eps = 1e-5f;
+  int m_max = 0;           // most rows any launch of this GEMV carries (0: M_static, or 16 with M_dev)
   int M_static = 1;
   const int32_t* M_dev = nullptr;
   // 1: the pass's rows may not fit the per-CTA activation stage.  A bf16-input

@@ -273,6 +273,7 @@ void gemv_scratch_args(ssd_ctx* c, LinearArgs& a) {
   a.err = &c->st->err;
   a.err_val = &c->st->err_val;
   a.wide = (c->mmax ? c->mmax : kMaxRows) > gemv_stage_rows(a.K) ? 1 : 0;
+  a.m_max = c->mmax ? c->mmax : kMaxRows;
 }
 
 // Arguments of layer l's five steps (shared by the eager and the captured
