@@ -324,7 +324,10 @@ ssd_status ssd_profile_decode(ssd_ctx* ctx, int32_t n_steps, ssd_kernel_times* o
  * replay between CUDA events on the context's stream.  ms[k] = device time
  * per launch, bytes[k] = algorithmic HBM bytes per launch (weights; K/V of
  * the current context for attention), launches[k] = launches of the class in
- * one autoregressive step (n_layers, 1 for the LM head, 0 for class 6).  Only
+ * one autoregressive step (n_layers, 1 for the LM head, 0 for class 6).
+ * Entry 7 times attention and o_proj together, one pair per layer launched
+ * back to back as the step launches them (ms and bytes per pair, launches 0
+ * because the pair repeats classes 1 and 2).  Only
  * scratch buffers and the cache row of the pending position are written; the
  * committed state is restored.  Errors: INVALID_ARG, STATE (no prefill, a
  * round in flight), CAPACITY, CUDA, TIMEOUT. */

@@ -76,7 +76,8 @@ class SsdStats(C.Structure):
 class SsdKernelTimes(C.Structure):
     _fields_ = [("ms", C.c_double * 8), ("bytes", C.c_double * 8), ("launches", C.c_int64 * 8)]
 
-    CLASSES = ("qkv", "attention", "o_proj", "gate_up", "down", "lm_head", "control")
+    CLASSES = ("qkv", "attention", "o_proj", "gate_up", "down", "lm_head", "control",
+               "attention+o_proj")
 
     def as_dict(self) -> dict:
         return {name: {"ms": self.ms[i], "bytes": self.bytes[i], "launches": self.launches[i]}

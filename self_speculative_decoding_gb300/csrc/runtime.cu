@@ -1946,7 +1946,12 @@ ssd_status b_prof_class(ssd_ctx* c, cudaStream_t s) {
       case 2: r = note(c, launch_gemv(IN_BF16, EPI_RESID, oproj_args(c, l), s, c->pdl), "o_proj"); break;
       case 3: r = enq_norm_gemv(c, EPI_SWIGLU, gateup_args(c, l), s, "gate_up"); break;
       case 4: r = note(c, launch_gemv(IN_BF16, EPI_RESID, down_args(c, l), s, c->pdl), "down"); break;
-      default: r = enq_lmhead(c, c->vstats, nullptr, nullptr, 2, s); break;
+      case 5: r = enq_lmhead(c, c->vstats, nullptr, nullptr, 2, s); break;
+      default:   // attention and the o_proj that consumes its output, as the step pairs them
+        r = note(c, launch_attention(attn_args(c, l), s, c->pdl), "attention");
+        if (r == SSD_OK)
+          r = note(c, launch_gemv(IN_BF16, EPI_RESID, oproj_args(c, l), s, c->pdl), "o_proj");
+        break;
     }
   }
   c->mmax = 0;
@@ -1968,18 +1973,22 @@ ssd_status ssd_profile_kernels(ssd_ctx* c, int32_t reps, ssd_kernel_times* out) 
   const DevState saved = *c->h_st;
   const ssd_config& g = c->cfg;
   const int L = g.n_layers;
-  const double bytes[6] = {2.0 * qkv_rows(g) * g.d_model,
+  const double bytes[8] = {2.0 * qkv_rows(g) * g.d_model,
                            2.0 * 2.0 * g.n_kv_heads * g.head_dim * (double)n0,
                            2.0 * g.d_model * g.n_heads * g.head_dim,
                            2.0 * 2.0 * g.ffn_dim * g.d_model,
                            2.0 * g.d_model * g.ffn_dim,
-                           2.0 * g.vocab * g.d_model};
+                           2.0 * g.vocab * g.d_model,
+                           0.0,
+                           2.0 * 2.0 * g.n_kv_heads * g.head_dim * (double)n0 +
+                               2.0 * g.d_model * g.n_heads * g.head_dim};
   // the pass shape of an autoregressive step: one row at position n - 1
   if ((r = enq_begin(c, BEGIN_AR, c->stream)) != SSD_OK) return r;
   cudaEvent_t e0 = nullptr, e1 = nullptr;
   CK(cudaEventCreate(&e0));
   CK(cudaEventCreate(&e1));
-  for (int cls = 0; cls < 6 && r == SSD_OK; ++cls) {
+  for (int cls = 0; cls < 8 && r == SSD_OK; ++cls) {
+    if (cls == 6) continue;   // the control kernels are timed by ssd_profile_decode only
     Graph G;
     c->prof_graph_cls = cls;
     if ((r = build_graph(c, G, b_prof_class)) != SSD_OK) break;
@@ -1996,7 +2005,7 @@ ssd_status ssd_profile_kernels(ssd_ctx* c, int32_t reps, ssd_kernel_times* out) 
     cudaEventElapsedTime(&ms, e0, e1);
     out->ms[cls] = ms / ((double)reps * L);
     out->bytes[cls] = bytes[cls];
-    out->launches[cls] = cls == 5 ? 1 : L;
+    out->launches[cls] = cls == 5 ? 1 : cls == 7 ? 0 : L;
   }
   cudaEventDestroy(e0);
   cudaEventDestroy(e1);
