@@ -14,12 +14,16 @@
 // groups (whole gate/up pairs) in equal numbers where the matrix has enough
 // of them, else an equal share of single units (at most kGridCtas CTAs, two
 // per SM, one wave).  A producer warp streams the range into a ring of
-// shared-memory slots with bulk (TMA) copies of up to 8 units, completing on
-// mbarriers; eight consumer warps take one unit each per slot, read their
-// fragments with conflict-free 16-byte shared loads and run the MMAs.
-// Activations (the B operand: 8 or 16 token columns) are staged once per CTA
-// in shared memory (normalised with the RMSNorm statistics for the norm-fused
-// input) or, for wide passes, read from global memory a chunk ahead.
+// shared-memory slots with bulk (TMA) copies of up to 16 units, completing on
+// mbarriers; eight consumer warps take two units each per slot (warp w units
+// w and w + 8), read their fragments with conflict-free 16-byte shared loads
+// and run the MMAs.  The ring has 3 slots of 16 KB, plus, when a launch's
+// rows leave part of the activation stage unused (one-row passes), the whole
+// 16 KB slots that fit there.  Activations (the B operand: 8 or 16 token
+// columns) are staged once per CTA in shared memory (normalised with the
+// RMSNorm statistics for the norm-fused input); wide passes whose CTAs own
+// whole row groups copy them window by window (K-outer batches), other wide
+// passes read them from global memory a chunk ahead.
 //
 // Reduction order.  A row group's sum is the sum, in CTA order, of its CTAs'
 // partials; a partial is the sum, in warp order, of the consumer warps'
