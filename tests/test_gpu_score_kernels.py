@@ -96,6 +96,41 @@ def test_rows_argmax(ops, V, K, T):
             assert z[t][idx[t]] >= s[-1] - 1e-3
 
 
+# The 13B scoring projections at the launch shape of a layer that 9 of the 16
+# candidates keep (288 window rows): qkv 15360 x 5120 (store), o_proj
+# 5120 x 5120 and down 5120 x 13824 (residual through a row map).  The oracle
+# computes a seeded sample of 96 output features against every window row.
+T13 = 288
+
+
+def _sample(n, k, seed):
+    return np.sort(np.random.default_rng(seed).choice(n, size=k, replace=False))
+
+
+@pytest.mark.parametrize("epi,R,K", [("store", 15360, 5120), ("resid", 5120, 5120),
+                                     ("resid", 5120, 13824)])
+def test_rows_13b_shapes_sampled(ops, epi, R, K):
+    from oracle import ops as O
+    W, Wb = rand_bf16((R, K), seed=R + 3 * K)
+    act, _ = rand_bf16((T13, K), seed=31, std=1.0)
+    feats = _sample(R, 96, R + K)
+    ref = O.linear(Wb[feats], bf16_values(act))           # [T13, 96]
+    if epi == "store":
+        y = ops.linear_rows(P(W), act).cpu().numpy()
+        np.testing.assert_allclose(y[:, feats], ref, rtol=1e-4, atol=2e-6 * np.sqrt(K))
+        return
+    rows = 2 * T13 + 3
+    x0, x0n = rand_f32((rows, R), seed=32)
+    rmap = _sample(rows, T13, 33).astype(np.int32)
+    x = x0.clone()
+    ops.linear_rows(P(W), act, epi="resid", out=x, rowmap=torch.from_numpy(rmap).cuda())
+    got = x.cpu().numpy()
+    want = x0n[rmap][:, feats] + ref
+    np.testing.assert_allclose(got[rmap][:, feats], want, rtol=1e-4, atol=1e-5 * np.sqrt(K))
+    others = np.setdiff1d(np.arange(rows), rmap)
+    np.testing.assert_array_equal(got[others], x0.cpu().numpy()[others])
+
+
 @pytest.mark.parametrize("R,K", [(528, 704), (1600, 512), (16384, 256)])
 def test_rows_count_invariance(ops, R, K):
     # token tiles of different widths (16 .. 256 columns) for different T; the
